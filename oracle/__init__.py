@@ -1,0 +1,209 @@
+"""CPU oracle for the speculative-sampling verify step (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline / reference leg may import this module.  The CUDA
+library and its Python binding never do.
+
+The oracle itself is plain C (``specverify_oracle.c``), single-threaded and in
+double precision; this module compiles it with gcc on first use and wraps it
+with ctypes on numpy arrays.  bf16 logits are passed as their raw uint16 bit
+patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "specverify_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libspecverify_oracle.so")
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+
+BAD_TOKEN = 1
+BAD_K = 2
+BAD_TEMP = 4
+NONFINITE = 8
+BAD_TOTAL = 16
+NO_DRAFT = 64
+
+RACE_NONE = 0
+RACE_GREEDY = 1
+RACE_BONUS = 2
+RACE_RESIDUAL = 3
+RACE_FALLBACK = 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/_build (IEEE double, no FMA contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        lib.orc_philox4x32_10.argtypes = [P, P, P]
+        lib.orc_philox4x32_10.restype = None
+        lib.orc_random_word.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint64,
+                                        ctypes.c_uint32, ctypes.c_uint32]
+        lib.orc_random_word.restype = ctypes.c_uint32
+        lib.orc_uniform_accept.argtypes = [ctypes.c_uint32]
+        lib.orc_uniform_accept.restype = ctypes.c_double
+        lib.orc_exponential.argtypes = [ctypes.c_uint32]
+        lib.orc_exponential.restype = ctypes.c_double
+        lib.orc_softmax.argtypes = [P, ctypes.c_int, ctypes.c_size_t, ctypes.c_int,
+                                    ctypes.c_double, P]
+        lib.orc_softmax.restype = None
+        lib.orc_argmax.argtypes = [P, ctypes.c_int, ctypes.c_size_t, ctypes.c_int]
+        lib.orc_argmax.restype = ctypes.c_int
+        lib.orc_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, P, P, P, P, P, P, ctypes.c_uint64,
+                                   P, P, P, P, P, P, P, P, P, P, P, P]
+        lib.orc_verify.restype = ctypes.c_uint32
+        lib.orc_race_keys.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_float,
+                                      ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int,
+                                      ctypes.c_int, P]
+        lib.orc_race_keys.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(a):
+    """Return (contiguous array, dtype code) for fp32 or bf16-as-uint16 logits."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float32:
+        return a, DTYPE_F32
+    if a.dtype == np.uint16:
+        return a, DTYPE_BF16
+    raise TypeError(f"logits must be float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def philox4x32_10(ctr, key):
+    """Raw Philox4x32-10 block: ctr is 4 words, key is 2 words; returns 4 words."""
+    lib = _load()
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib.orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def random_word(seed, stream, request, position, v):
+    return int(_load().orc_random_word(seed, stream, request, position, v))
+
+
+def uniform_accept(word):
+    return float(_load().orc_uniform_accept(word))
+
+
+def exponential(word):
+    return float(_load().orc_exponential(word))
+
+
+def softmax(row, temperature):
+    """softmax(row / T) of one logit row (fp32 or bf16 bits), in float64."""
+    row, dt = _logits(np.asarray(row).reshape(1, -1))
+    vocab = row.shape[1]
+    out = np.zeros(vocab, dtype=np.float64)
+    _load().orc_softmax(_ptr(row), dt, 0, vocab, float(temperature), _ptr(out))
+    return out
+
+
+def argmax(row):
+    row, dt = _logits(np.asarray(row).reshape(1, -1))
+    return int(_load().orc_argmax(_ptr(row), dt, 0, row.shape[1]))
+
+
+def verify(target, draft, tokens, num_draft, temperature, seed, max_k,
+           request_ids=None, total_draft=None):
+    """Run the oracle over a ragged batch.
+
+    target: [sum(k_r+1), V] float32 or uint16 (bf16 bits); draft: [sum(k_r), V] or
+    None; tokens: [sum(k_r)] int32; num_draft: [B] int32; temperature: [B] float32.
+    Returns a dict of numpy arrays (see orc_verify in specverify_oracle.c).
+    """
+    lib = _load()
+    target, dt = _logits(target)
+    vocab = int(target.shape[1]) if target.ndim == 2 else 0
+    if draft is not None:
+        draft, dt2 = _logits(draft)
+        if draft.size and dt2 != dt:
+            raise TypeError("target and draft logits must share a dtype")
+        if draft.size == 0:
+            draft = np.zeros((0, vocab), dtype=target.dtype)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    num_draft = np.ascontiguousarray(num_draft, dtype=np.int32)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    batch = int(num_draft.shape[0])
+    if total_draft is None:
+        total_draft = int(tokens.shape[0])
+    rid = None if request_ids is None else np.ascontiguousarray(request_ids, dtype=np.int64)
+    width = max_k + 1
+    out = {
+        "accepted_len": np.zeros(batch, np.int32),
+        "committed": np.zeros((batch, width), np.int32),
+        "flags": np.zeros(total_draft, np.uint8),
+        "p_y": np.zeros(total_draft, np.float64),
+        "q_y": np.zeros(total_draft, np.float64),
+        "u": np.zeros(total_draft, np.float64),
+        "accept_margin": np.zeros(total_draft, np.float64),
+        "race_kind": np.zeros(batch, np.int32),
+        "race_pos": np.zeros(batch, np.int32),
+        "race_best": np.zeros(batch, np.float64),
+        "race_second": np.zeros(batch, np.float64),
+        "req_status": np.zeros(batch, np.int32),
+    }
+    status = lib.orc_verify(
+        dt, vocab, batch, max_k, int(total_draft), _ptr(target),
+        None if draft is None else _ptr(draft), _ptr(tokens), _ptr(num_draft),
+        _ptr(temperature), _ptr(rid), int(seed) & (2**64 - 1),
+        _ptr(out["accepted_len"]), _ptr(out["committed"]), _ptr(out["flags"]),
+        _ptr(out["p_y"]), _ptr(out["q_y"]), _ptr(out["u"]), _ptr(out["accept_margin"]),
+        _ptr(out["race_kind"]), _ptr(out["race_pos"]), _ptr(out["race_best"]),
+        _ptr(out["race_second"]), _ptr(out["req_status"]))
+    out["status"] = int(status)
+    return out
+
+
+def race_keys(target_row, draft_row, temperature, seed, request, position, kind):
+    """Keys E_v / w_v of one request's correction/bonus race for every v.
+
+    Returns (winner, keys[V]); keys are +inf where the weight is not positive.
+    """
+    lib = _load()
+    t, dt = _logits(np.asarray(target_row).reshape(1, -1))
+    d = None
+    if draft_row is not None:
+        d, _ = _logits(np.asarray(draft_row).reshape(1, -1))
+    vocab = t.shape[1]
+    keys = np.zeros(vocab, dtype=np.float64)
+    winner = lib.orc_race_keys(dt, vocab, _ptr(t), _ptr(d), float(temperature),
+                               int(seed) & (2**64 - 1), int(request) & (2**64 - 1),
+                               int(position), int(kind), _ptr(keys))
+    return int(winner), keys

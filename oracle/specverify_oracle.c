@@ -1,0 +1,435 @@
+/*
+ * specverify_oracle.c -- plain, slow, single-threaded CPU oracle for the
+ * target-side verify step of speculative sampling.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline / reference leg load this file.  The CUDA
+ * library never links, includes or calls it, and it shares no code with the
+ * CUDA library (its own Philox, its own softmax, its own scan and race).
+ *
+ * Everything is computed in double precision from logits that are read
+ * exactly (fp32 -> double and bf16 -> fp32 -> double are lossless).  Each step
+ * follows the passage of the pages it cites:
+ *
+ *   [SD]  "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and
+ *         DSpark", section 1 "What Speculative Decoding Actually Guarantees":
+ *         the worked example (draft A B C D, C rejected, commit A B R), the
+ *         acceptance probability alpha_i(y_i) = min(1, p_i(y_i)/q_i(y_i)),
+ *         the correction drawn from the normalised positive residual
+ *         [p_i - q_i]_+, the bonus token drawn from the target when every
+ *         draft survives, greedy equivalence (accepted tokens follow the
+ *         target argmax) and the rule that temperature enters p and q
+ *         consistently.
+ *   [SD2] same page, section 2 "The Cost Model Behind the Comparison": A is
+ *         the accepted draft-prefix length, excluding the correction/bonus.
+ *   [AMD] "Speculative Decoding on AMD GPUs" (vLLM blog), "Core idea of
+ *         speculative decoding": verification runs left to right and every
+ *         candidate after the first rejection is discarded.
+ *
+ * Randomness (not fixed by the pages; the reading this library takes):
+ *   Philox4x32-10 from Salmon, Moraes, Dror and Shaw, "Parallel Random
+ *   Numbers: As Easy as 1, 2, 3" (SC'11), keyed by the 64-bit seed
+ *   (key = seed low word, seed high word) with the counter
+ *       (floor(v/4), position, request low word, stream | request high << 8)
+ *   and output word v mod 4.  Stream 0 gives the acceptance uniform of a
+ *   position (v = 0), stream 1 the race exponentials of the correction or
+ *   bonus draw.
+ *     u      = (w >> 8) * 2^-24                 in [0, 1)       (exact in fp32)
+ *     E      = -ln((w + 1/2) * 2^-32)           in (1.2e-10, 22.9)
+ *   A categorical draw from weights w_v >= 0 is the exponential race
+ *   argmin_{v: w_v > 0} E_v / w_v with the lowest index winning ties.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <float.h>
+
+#define ORC_DTYPE_F32 0
+#define ORC_DTYPE_BF16 1
+
+/* Status bits (same meaning as the library's; defined here independently). */
+#define ORC_BAD_TOKEN 1u      /* a draft token outside [0, V) */
+#define ORC_BAD_K 2u          /* a num_draft outside [0, max_k] */
+#define ORC_BAD_TEMP 4u       /* temperature NaN, negative, infinite or subnormal */
+#define ORC_NONFINITE 8u      /* a read row holds NaN/+inf or no finite logit */
+#define ORC_BAD_TOTAL 16u     /* sum of num_draft differs from total_draft */
+#define ORC_NO_DRAFT 64u      /* T > 0 but no draft logits were given */
+
+/* Race kinds reported per request. */
+#define ORC_RACE_NONE 0
+#define ORC_RACE_GREEDY 1     /* token = target argmax (T = 0) */
+#define ORC_RACE_BONUS 2      /* every draft accepted: race on p_k */
+#define ORC_RACE_RESIDUAL 3   /* race on [p_j - q_j]_+ */
+#define ORC_RACE_FALLBACK 4   /* residual has no mass: race on p_j */
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10 (SC'11): ten rounds of two 32x32->64 multiplies; the key is  */
+/* bumped by the Weyl constants between rounds.                               */
+/* ------------------------------------------------------------------------ */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    const uint32_t mul0 = 0xD2511F53u, mul1 = 0xCD9E8D57u;
+    const uint32_t weyl0 = 0x9E3779B9u, weyl1 = 0xBB67AE85u;
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += weyl0;
+            k1 += weyl1;
+        }
+        uint64_t prod0 = (uint64_t)mul0 * (uint64_t)x0;
+        uint64_t prod1 = (uint64_t)mul1 * (uint64_t)x2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t y0 = hi1 ^ x1 ^ k0;
+        uint32_t y1 = lo1;
+        uint32_t y2 = hi0 ^ x3 ^ k1;
+        uint32_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* One 32-bit random word for (seed, stream, request, position, v). */
+uint32_t orc_random_word(uint64_t seed, uint32_t stream, uint64_t request,
+                         uint32_t position, uint32_t v)
+{
+    uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+    uint32_t ctr[4] = {v / 4u, position, (uint32_t)(request & 0xFFFFFFFFu),
+                       (stream & 0xFFu) | ((uint32_t)(request >> 32) << 8)};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    return out[v % 4u];
+}
+
+/* Acceptance uniform: the top 24 bits of the word, scaled into [0, 1). */
+double orc_uniform_accept(uint32_t w)
+{
+    return (double)(w >> 8) * 0x1p-24;
+}
+
+/* Race exponential: E = -ln(U) with U = (w + 1/2) * 2^-32 strictly in (0, 1). */
+double orc_exponential(uint32_t w)
+{
+    double u = ((double)w + 0.5) * 0x1p-32;
+    return -log(u);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Logit access: row-major [rows, V]; fp32 or bf16 (raw 16-bit patterns).     */
+/* ------------------------------------------------------------------------ */
+static double logit_at(const void *base, int dtype, size_t row, int vocab, int v)
+{
+    size_t idx = row * (size_t)vocab + (size_t)v;
+    if (dtype == ORC_DTYPE_F32)
+        return (double)((const float *)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* A row is usable when it has no NaN, no +inf and at least one finite logit. */
+static int row_is_valid(const void *base, int dtype, size_t row, int vocab)
+{
+    int any_finite = 0;
+    for (int v = 0; v < vocab; ++v) {
+        double x = logit_at(base, dtype, row, vocab, v);
+        if (isnan(x) || x == INFINITY)
+            return 0;
+        if (isfinite(x))
+            any_finite = 1;
+    }
+    return any_finite;
+}
+
+/* p = softmax(x / T) over the row, in double ([SD] section 1: temperature  */
+/* enters p and q alike).  A logit of -inf gets probability 0.              */
+void orc_softmax(const void *base, int dtype, size_t row, int vocab, double temperature,
+                 double *p)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < vocab; ++v) {
+        double z = logit_at(base, dtype, row, vocab, v) / temperature;
+        if (z > m)
+            m = z;
+    }
+    double total = 0.0;
+    for (int v = 0; v < vocab; ++v) {
+        double z = logit_at(base, dtype, row, vocab, v) / temperature;
+        p[v] = exp(z - m);
+        total += p[v];
+    }
+    for (int v = 0; v < vocab; ++v)
+        p[v] /= total;
+}
+
+/* Greedy choice: the first index holding the row maximum ([SD] section 1, */
+/* greedy equivalence).                                                     */
+int orc_argmax(const void *base, int dtype, size_t row, int vocab)
+{
+    int best = 0;
+    double best_x = logit_at(base, dtype, row, vocab, 0);
+    for (int v = 1; v < vocab; ++v) {
+        double x = logit_at(base, dtype, row, vocab, v);
+        if (x > best_x) {
+            best_x = x;
+            best = v;
+        }
+    }
+    return best;
+}
+
+/* Exponential race over weights w (length V): argmin_{w_v > 0} E_v / w_v,  */
+/* lowest index on ties.  keys_out (nullable) receives every key (+inf where */
+/* w_v <= 0).  Returns the winner, or -1 when no weight is positive.         */
+static int race(const double *w, int vocab, uint64_t seed, uint64_t request, uint32_t position,
+                double *keys_out, double *best_key, double *second_key)
+{
+    int winner = -1;
+    double best = INFINITY, second = INFINITY;
+    for (int v = 0; v < vocab; ++v) {
+        double key = INFINITY;
+        if (w[v] > 0.0) {
+            double e = orc_exponential(orc_random_word(seed, 1u, request, position, (uint32_t)v));
+            key = e / w[v];
+        }
+        if (keys_out)
+            keys_out[v] = key;
+        if (key < best) {
+            second = best;
+            best = key;
+            winner = v;
+        } else if (key < second) {
+            second = key;
+        }
+    }
+    if (best_key)
+        *best_key = best;
+    if (second_key)
+        *second_key = second;
+    return winner;
+}
+
+/* Temperature is usable when it is 0 (greedy) or a normal, finite positive. */
+static int temperature_ok(float t)
+{
+    if (isnan(t) || isinf(t) || t < 0.0f)
+        return 0;
+    return t == 0.0f || t >= FLT_MIN;
+}
+
+/*
+ * The verify step over a ragged batch.
+ *
+ * Layout: request r owns k_r = num_draft[r] draft positions.  Its target rows
+ * are rows tgt_off(r) .. tgt_off(r)+k_r of target_logits with
+ * tgt_off(r) = sum_{s<r} (k_s + 1); its draft rows are drf_off(r) ..
+ * drf_off(r)+k_r-1 of draft_logits, and its draft tokens are
+ * draft_tokens[drf_off(r) + i], with drf_off(r) = sum_{s<r} k_s.
+ *
+ * Outputs: accepted_len[r] = A_r ([SD2]); committed[r*(max_k+1) + i] holds the
+ * accepted draft tokens for i < A_r, the correction or bonus token at i = A_r,
+ * and -1 after it; accept_flags[drf_off(r) + i] = (i < A_r).  A request whose
+ * inputs are invalid gets accepted_len -1, a committed row of -1 and flags 0.
+ *
+ * Debug outputs (all nullable): p_y/q_y/u per draft position of stochastic
+ * requests (NaN for greedy ones); accept_margin = (p - u q) / max(p, u q);
+ * race_kind/race_pos/race_best/race_second per request; req_status per request.
+ * Returns the OR of all status bits.
+ */
+uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
+                    const void *target_logits, const void *draft_logits,
+                    const int32_t *draft_tokens, const int32_t *num_draft,
+                    const float *temperature, const int64_t *request_ids, uint64_t seed,
+                    int32_t *accepted_len, int32_t *committed, uint8_t *accept_flags,
+                    double *p_y, double *q_y, double *u_out, double *accept_margin,
+                    int32_t *race_kind, int32_t *race_pos, double *race_best,
+                    double *race_second, int32_t *req_status)
+{
+    const int width = max_k + 1;
+    uint32_t status = 0;
+
+    for (int r = 0; r < batch; ++r) {
+        accepted_len[r] = -1;
+        for (int i = 0; i < width; ++i)
+            committed[(size_t)r * width + i] = -1;
+        if (race_kind) race_kind[r] = ORC_RACE_NONE;
+        if (race_pos) race_pos[r] = -1;
+        if (race_best) race_best[r] = NAN;
+        if (race_second) race_second[r] = NAN;
+        if (req_status) req_status[r] = 0;
+    }
+    for (int d = 0; d < total_draft; ++d) {
+        accept_flags[d] = 0;
+        if (p_y) p_y[d] = NAN;
+        if (q_y) q_y[d] = NAN;
+        if (u_out) u_out[d] = NAN;
+        if (accept_margin) accept_margin[d] = NAN;
+    }
+
+    /* The layout is only trustworthy when every k_r is in range and they  */
+    /* add up to total_draft; otherwise nothing is verified.               */
+    long long sum_k = 0;
+    for (int r = 0; r < batch; ++r) {
+        if (num_draft[r] < 0 || num_draft[r] > max_k)
+            status |= ORC_BAD_K;
+        sum_k += num_draft[r];
+    }
+    if (status & ORC_BAD_K)
+        return status;
+    if (sum_k != total_draft)
+        return status | ORC_BAD_TOTAL;
+
+    double *p = (double *)malloc(sizeof(double) * (size_t)(vocab > 0 ? vocab : 1));
+    double *q = (double *)malloc(sizeof(double) * (size_t)(vocab > 0 ? vocab : 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)(vocab > 0 ? vocab : 1));
+
+    size_t tgt_off = 0, drf_off = 0;
+    for (int r = 0; r < batch; ++r) {
+        const int k = num_draft[r];
+        const float t = temperature[r];
+        const uint64_t req = request_ids ? (uint64_t)request_ids[r] : (uint64_t)r;
+        uint32_t rs = 0;
+
+        if (!temperature_ok(t))
+            rs |= ORC_BAD_TEMP;
+        for (int i = 0; i < k; ++i) {
+            int32_t y = draft_tokens[drf_off + i];
+            if (y < 0 || y >= vocab)
+                rs |= ORC_BAD_TOKEN;
+        }
+        const int greedy = (t == 0.0f);
+        if (!rs && !greedy && k > 0 && draft_logits == NULL)
+            rs |= ORC_NO_DRAFT;
+        if (!rs) {
+            /* Rows the method reads: every target row; draft rows only when */
+            /* the request samples.                                           */
+            for (int i = 0; i <= k; ++i)
+                if (!row_is_valid(target_logits, dtype, tgt_off + i, vocab))
+                    rs |= ORC_NONFINITE;
+            if (!greedy)
+                for (int i = 0; i < k; ++i)
+                    if (!row_is_valid(draft_logits, dtype, drf_off + i, vocab))
+                        rs |= ORC_NONFINITE;
+        }
+        if (rs) {
+            status |= rs;
+            if (req_status) req_status[r] = (int32_t)rs;
+            tgt_off += (size_t)k + 1;
+            drf_off += (size_t)k;
+            continue;
+        }
+
+        int accepted = 0;
+        int token = -1;
+        if (greedy) {
+            /* Greedy equivalence: keep y_i while it equals the target argmax; */
+            /* the committed extra token is the target argmax at position A.   */
+            while (accepted < k &&
+                   draft_tokens[drf_off + accepted] ==
+                       orc_argmax(target_logits, dtype, tgt_off + accepted, vocab))
+                ++accepted;
+            token = orc_argmax(target_logits, dtype, tgt_off + accepted, vocab);
+            if (race_kind) race_kind[r] = ORC_RACE_GREEDY;
+            if (race_pos) race_pos[r] = accepted;
+        } else {
+            const double temp = (double)t;
+            /* Accept y_i with probability min(1, p_i(y_i)/q_i(y_i)), tested as */
+            /* u_i q_i(y_i) < p_i(y_i); stop at the first rejection.             */
+            int rejected = 0;
+            for (int i = 0; i < k; ++i) {
+                const int32_t y = draft_tokens[drf_off + i];
+                orc_softmax(target_logits, dtype, tgt_off + i, vocab, temp, p);
+                orc_softmax(draft_logits, dtype, drf_off + i, vocab, temp, q);
+                const double u = orc_uniform_accept(orc_random_word(seed, 0u, req, (uint32_t)i, 0u));
+                const double lhs = u * q[y], rhs = p[y];
+                if (p_y) p_y[drf_off + i] = rhs;
+                if (q_y) q_y[drf_off + i] = q[y];
+                if (u_out) u_out[drf_off + i] = u;
+                if (accept_margin) {
+                    double scale = lhs > rhs ? lhs : rhs;
+                    accept_margin[drf_off + i] = scale > 0.0 ? (rhs - lhs) / scale : 0.0;
+                }
+                if (!rejected) {
+                    if (lhs < rhs)
+                        ++accepted;
+                    else
+                        rejected = 1;
+                }
+            }
+            double best = NAN, second = NAN;
+            if (accepted == k) {
+                /* Every draft survived: one more token from the target p_k. */
+                orc_softmax(target_logits, dtype, tgt_off + k, vocab, temp, p);
+                token = race(p, vocab, seed, req, (uint32_t)k, NULL, &best, &second);
+                if (race_kind) race_kind[r] = ORC_RACE_BONUS;
+            } else {
+                /* First rejection at j = A: draw from [p_j - q_j]_+, normalised */
+                /* (normalisation does not change the race winner).             */
+                const int j = accepted;
+                orc_softmax(target_logits, dtype, tgt_off + j, vocab, temp, p);
+                orc_softmax(draft_logits, dtype, drf_off + j, vocab, temp, q);
+                for (int v = 0; v < vocab; ++v)
+                    w[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
+                token = race(w, vocab, seed, req, (uint32_t)j, NULL, &best, &second);
+                if (token >= 0) {
+                    if (race_kind) race_kind[r] = ORC_RACE_RESIDUAL;
+                } else {
+                    /* p <= q everywhere means p == q: draw from p instead. */
+                    token = race(p, vocab, seed, req, (uint32_t)j, NULL, &best, &second);
+                    if (race_kind) race_kind[r] = ORC_RACE_FALLBACK;
+                }
+            }
+            if (race_pos) race_pos[r] = accepted;
+            if (race_best) race_best[r] = best;
+            if (race_second) race_second[r] = second;
+        }
+
+        accepted_len[r] = accepted;
+        for (int i = 0; i < accepted; ++i)
+            committed[(size_t)r * width + i] = draft_tokens[drf_off + i];
+        committed[(size_t)r * width + accepted] = token;
+        for (int i = 0; i < k; ++i)
+            accept_flags[drf_off + i] = (uint8_t)(i < accepted);
+
+        tgt_off += (size_t)k + 1;
+        drf_off += (size_t)k;
+    }
+    free(p);
+    free(q);
+    free(w);
+    return status;
+}
+
+/*
+ * Race keys of one request's correction/bonus draw, for every vocab id, so a
+ * test can look up the key of any token.  kind: ORC_RACE_BONUS or
+ * ORC_RACE_FALLBACK (weights p from target_row), ORC_RACE_RESIDUAL (weights
+ * [p - q]_+ from target_row and draft_row).  Rows are single rows [V].
+ * Returns the winner.
+ */
+int orc_race_keys(int dtype, int vocab, const void *target_row, const void *draft_row,
+                  float temperature, uint64_t seed, uint64_t request, int position, int kind,
+                  double *keys_out)
+{
+    double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
+    double *q = (double *)malloc(sizeof(double) * (size_t)vocab);
+    double *w = (double *)malloc(sizeof(double) * (size_t)vocab);
+    orc_softmax(target_row, dtype, 0, vocab, (double)temperature, p);
+    int winner;
+    if (kind == ORC_RACE_RESIDUAL) {
+        orc_softmax(draft_row, dtype, 0, vocab, (double)temperature, q);
+        for (int v = 0; v < vocab; ++v)
+            w[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
+        winner = race(w, vocab, seed, request, (uint32_t)position, keys_out, NULL, NULL);
+    } else {
+        winner = race(p, vocab, seed, request, (uint32_t)position, keys_out, NULL, NULL);
+    }
+    free(p);
+    free(q);
+    free(w);
+    return winner;
+}
