@@ -1,0 +1,389 @@
+"""Benchmark of the verify step (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one verify round (plan + row pass + residual) over one synthetic
+batch already resident in HBM.  value = verified logit rows (sum_r (k_r+1))
+per second over all ranks; ranks run independent batches (weak scaling, no
+collective on the data path).  The default workload, w4_v262144_bf16, is the
+largest synthetic batch: 512 requests, k = 4, V = 262144, bf16 logits (2.4 GB
+per step, far larger than the 129 MB L2, so no flush between steps).
+
+The line also carries:
+  roofline     achieved GB/s of the row-pass kernel = its algorithmic bytes (every
+               needed logit row once) / its CUDA-event time, against the measured
+               HBM copy bandwidth;
+  e2e          the same metric through specverify_run_host: pinned host inputs
+               copied in, outputs copied out, every step;
+  cpu_baseline the CPU oracle on a bounded sample of the same batch (1 core);
+  clocks       nvidia-smi samples taken during the timed region.
+--impl reference times the CPU oracle instead (the only other arm there is).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified logit rows/sec"
+UNIT = "rows/s"
+DEFAULT_WORKLOAD = "w4_v262144_bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-sample", type=int, default=0,
+                    help="requests in the oracle sample (0 = about 10 s of work)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_10_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per row-pass launch from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms; keeps those inside [start, stop]."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, "t_" + which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        inside = [s for t, s in self.samples if self.t_start <= t <= self.t_stop + 0.2]
+        window = "timed region"
+        if not inside:
+            inside = [s for _, s in self.samples][-3:]
+            window = "nearest samples (timed region shorter than the sampling period)"
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            parts = [p.strip() for p in s.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
+
+
+def oracle_rows_per_sec(batch, requests):
+    """Time the CPU oracle on the given requests of `batch` (single thread)."""
+    import oracle
+    from speculative_decoding_verification_10_gb300 import workloads as W
+    sub = W.subset(batch, requests)
+    inp = sub.numpy_inputs()
+    t0 = time.perf_counter()
+    oracle.verify(inp["target"], inp["draft"], inp["tokens"], inp["num_draft"],
+                  inp["temperature"], 1, inp["max_k"], request_ids=inp["request_ids"])
+    dt = time.perf_counter() - t0
+    rows = int(inp["num_draft"].astype(np.int64).sum()) + len(requests)
+    return rows / dt, dt, rows
+
+
+def estimate_sample(batch, target_seconds=10.0):
+    """Requests whose oracle run takes about target_seconds (from a 1-request probe)."""
+    _, dt, _ = oracle_rows_per_sec(batch, [0])
+    n = int(max(1, min(batch.batch, target_seconds / max(dt, 1e-4))))
+    return n
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from speculative_decoding_verification_10_gb300 import workloads as W
+    dev = f"cuda:{local}" if torch.cuda.is_available() else "cpu"
+    b = W.make_batch(args.workload, device=dev)
+    per_step = args.cpu_sample or max(1, min(b.batch, int(120.0 / max(1, args.steps + args.warmup)
+                                                        / max(_probe_seconds(b), 1e-4))))
+    times, rows_total = [], 0
+    order = np.arange(b.batch)
+    for s in range(args.warmup + args.steps):
+        start = (s * per_step) % b.batch
+        req = np.sort(order[(start + np.arange(per_step)) % b.batch])
+        rps, dt, rows = oracle_rows_per_sec(b, req)
+        if s >= args.warmup:
+            times.append(dt)
+            rows_total += rows
+    value = rows_total / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": b.batch, "vocab": b.vocab,
+                       "logits": b.dtype, "requests_per_step": per_step},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{per_step} requests of {args.workload} per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _probe_seconds(b):
+    _, dt, _ = oracle_rows_per_sec(b, [0])
+    return dt
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from speculative_decoding_verification_10_gb300 import Verifier, build, launches_per_run
+    from speculative_decoding_verification_10_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+
+    spec = W.SPECS[args.workload]
+    b = W.make_batch(args.workload, device=dev, gen_seed=spec.gen_seed + 7919 * rank)
+    rows_per_step = b.verified_rows()
+    alg_bytes = b.algorithmic_bytes()
+    es = 2 if b.dtype == "bf16" else 4
+    k = b.num_draft.cpu().numpy().astype(np.int64)
+    t = b.temperature.cpu().numpy()
+    rowpass_bytes = int(np.where(t > 0, 2 * k + 1, k + 1).sum()) * b.vocab * es
+
+    v = Verifier(b.batch, b.max_k, b.vocab, b.dtype, device=local, host_staging=True)
+    out = v.outputs(b.batch, b.total_draft)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 1, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if v.status() != 0:
+        raise RuntimeError(f"verify status {v.status()} on the benchmark batch")
+
+    n_ev = min(64, args.steps)
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+
+    # timed region: K steps, CUDA events on the launching stream
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    t_start.record(stream)
+    kernel_ms = []
+    done = 0
+    while done < args.steps:
+        chunk = min(n_ev, args.steps - done)
+        v.set_timing_events(ev_s[:chunk], ev_e[:chunk])
+        for _ in range(chunk):
+            step()
+        done += chunk
+        if done < args.steps:
+            stream.synchronize()   # read this chunk's kernel times before reusing events
+            kernel_ms += [ev_s[i].elapsed_time(ev_e[i]) for i in range(chunk)]
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("stop")
+    kernel_ms += [ev_s[i].elapsed_time(ev_e[i]) for i in range(chunk)]
+    v.set_timing_events([], [])
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_stop) / args.steps
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    clock_info = clocks.stop()
+
+    # end to end through the host-buffer entry point (pinned host inputs)
+    hb = b.to("cpu")
+    h_target = hb.target.pin_memory()
+    h_draft = hb.draft.pin_memory()
+    h_tokens, h_nd, h_temp = hb.tokens.pin_memory(), hb.num_draft.pin_memory(), hb.temperature.pin_memory()
+    h_acc = torch.empty(b.batch, dtype=torch.int32).pin_memory()
+    h_com = torch.empty(b.batch, b.max_k + 1, dtype=torch.int32).pin_memory()
+    h_flg = torch.empty(b.total_draft, dtype=torch.uint8).pin_memory()
+    for _ in range(2):
+        v.run_host(h_target, h_draft, h_tokens, h_nd, h_temp, 1, h_acc, h_com, h_flg)
+    if world > 1:
+        dist.barrier()
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        v.run_host(h_target, h_draft, h_tokens, h_nd, h_temp, 1, h_acc, h_com, h_flg)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_t = torch.tensor([e2e_s], device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_s = float(e2e_t.item())
+    h2d = (h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()
+           + 4 * (h_tokens.numel() + h_nd.numel() + h_temp.numel()))
+    d2h = 4 * h_acc.numel() + 4 * h_com.numel() + h_flg.numel()
+
+    # CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample or estimate_sample(b)
+        req = np.sort(np.random.default_rng(0).choice(b.batch, size=n, replace=False))
+        rps, dt, rows = oracle_rows_per_sec(b, req)
+        cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} of {b.batch} requests ({rows} verified rows), {dt:.1f} s"}
+
+    if rank != 0:
+        v.close()
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    kernel_avg_ms = float(np.mean(kernel_ms))
+    peak, peak_kind = measured_peak()
+    achieved = rowpass_bytes / (kernel_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": world * rows_per_step / (ms_max * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": b.batch, "k": spec.k,
+                   "vocab": b.vocab, "logits": b.dtype, "rows_per_step": rows_per_step,
+                   "alg_bytes_per_step": alg_bytes,
+                   "step_gbs": alg_bytes / (ms_max * 1e-3) / 1e9,
+                   "l2": "no flush: each step reads %.2f GB of logits, larger than the 129 MB L2"
+                         % (rowpass_bytes / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "sv_rowpass", "kernel_ms": kernel_avg_ms,
+                     "alg_bytes_per_launch": rowpass_bytes,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * rows_per_step / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "clocks": clock_info,
+        "gpu_launches": launches_per_run() * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    v.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

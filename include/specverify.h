@@ -1,0 +1,198 @@
+/*
+ * specverify.h -- C ABI of the GB300 verify step for speculative sampling.
+ *
+ * What the library computes (one call = one verify round for a ragged batch):
+ *
+ *   "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and DSpark",
+ *   section 1 "What Speculative Decoding Actually Guarantees": with p_i the
+ *   target distribution and q_i the proposal distribution at draft position
+ *   i, draft token y_i is accepted with probability
+ *       alpha_i(y_i) = min(1, p_i(y_i) / q_i(y_i)),
+ *   positions are tested left to right and everything after the first
+ *   rejection is discarded (draft A B C D with C rejected commits A B R); at
+ *   the first rejection one token is drawn from the normalised positive
+ *   residual [p_i - q_i]_+, and when every draft survives one extra token is
+ *   drawn from the target.  Greedy rounds keep y_i while it equals the target
+ *   argmax.  Temperature enters p and q alike: p_i = softmax(target_i / T),
+ *   q_i = softmax(draft_i / T).  Section 2 of the same page defines A, the
+ *   accepted draft-prefix length, excluding the correction or bonus token.
+ *
+ * Readings this library takes where the pages leave a step open:
+ *   - T == 0 means greedy (target argmax, lowest index on ties; draft logits
+ *     are not read); T > 0 means sampling.
+ *   - The test "u < p(y)/q(y)" is evaluated as u*q(y) < p(y) (strict).
+ *   - Randomness is counter-based Philox4x32-10 (Salmon et al., SC'11) with
+ *     key = (seed low 32 bits, seed high 32 bits) and counter
+ *       (floor(v/4), position, request low 32 bits, stream | request high << 8),
+ *     taking output word v mod 4.  Stream 0, v = 0: acceptance uniform
+ *     u = (word >> 8) * 2^-24.  Stream 1: race exponentials
+ *     E_v = -ln((word + 1/2) * 2^-32).
+ *   - Every categorical draw is the exponential race argmin_{w_v>0} E_v / w_v
+ *     (lowest index on ties), so the result does not depend on how the
+ *     vocabulary is split across threads.  Correction: w = [p_j - q_j]_+ at
+ *     position j = A and Philox position j; if that residual has no mass the
+ *     draw is made from p_j with the same exponentials.  Bonus: w = p_k at
+ *     position k.
+ *   - "request" is the batch index r unless request ids are given.
+ *
+ * Data layout (row-major, one row = V logits of one position):
+ *   request r has k_r = num_draft[r] draft positions;
+ *   its target rows are  target_logits[tgt_off(r) + i],  i = 0..k_r,
+ *       tgt_off(r) = sum_{s<r} (k_s + 1);
+ *   its draft rows are   draft_logits[drf_off(r) + i],   i = 0..k_r-1,
+ *   its draft tokens are draft_tokens[drf_off(r) + i],
+ *       drf_off(r) = sum_{s<r} k_s.
+ *
+ * Outputs (caller-owned device memory):
+ *   accepted_len[r]                   A_r, or -1 when request r was skipped;
+ *   committed_tokens[r*(max_k+1)+i]   y_i for i < A_r, the correction or bonus
+ *                                     token at i = A_r, -1 after it;
+ *   accept_flags[drf_off(r)+i]        1 if i < A_r else 0 (per-position flags).
+ *
+ * Errors.  Entry points return SPECVERIFY_OK or a negative error code and
+ * launch nothing on an error.  Problems that only the device can see (token
+ * out of range, bad temperature, NaN/+inf logits, inconsistent num_draft) set
+ * bits in a device status word and skip the affected request (or, for an
+ * inconsistent layout, the whole batch); read it with specverify_status().
+ * No kernel traps or asserts.
+ *
+ * Threading.  A handle may be used from one host thread and one stream at a
+ * time; concurrent runs on one handle race on its scratch memory.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct specverify_ctx *specverify_t;
+
+typedef enum {
+    SPECVERIFY_F32 = 0,   /* float32 logits */
+    SPECVERIFY_BF16 = 1   /* bfloat16 logits (raw 16-bit patterns) */
+} specverify_dtype;
+
+/* Return codes. */
+#define SPECVERIFY_OK 0
+#define SPECVERIFY_ERR_INVALID_ARG (-1)   /* null pointer, size out of range, misalignment */
+#define SPECVERIFY_ERR_DTYPE (-2)         /* unknown dtype */
+#define SPECVERIFY_ERR_CUDA (-3)          /* a CUDA runtime call or launch failed */
+#define SPECVERIFY_ERR_DESTROYED (-4)     /* handle already destroyed */
+#define SPECVERIFY_ERR_NO_STAGING (-5)    /* host entry point on a handle made without staging */
+
+/* Device status bits (specverify_status). */
+#define SPECVERIFY_STATUS_BAD_TOKEN 1     /* a draft token outside [0, V): request skipped */
+#define SPECVERIFY_STATUS_BAD_K 2         /* a num_draft outside [0, max_k]: batch skipped */
+#define SPECVERIFY_STATUS_BAD_TEMP 4      /* T NaN, negative, infinite or subnormal: request skipped */
+#define SPECVERIFY_STATUS_NONFINITE 8     /* NaN/+inf logit, or no finite logit, in a read row: request skipped */
+#define SPECVERIFY_STATUS_BAD_TOTAL 16    /* sum of num_draft != total_draft: batch skipped */
+#define SPECVERIFY_STATUS_NO_DRAFT 64     /* T > 0 and k > 0 but draft_logits is NULL: request skipped */
+
+/* Flags for specverify_create_ex. */
+#define SPECVERIFY_CREATE_HOST_STAGING 1  /* allocate device staging for specverify_run_host */
+
+/*
+ * specverify_create -- make a handle bound to CUDA device `device`.
+ *   max_batch  >= 1: largest batch a run may pass;
+ *   max_k      in [0, 31]: largest num_draft (committed rows are max_k+1 wide);
+ *   vocab      in [1, 2^30]: V, the logits row length;
+ *   dtype      SPECVERIFY_F32 or SPECVERIFY_BF16.
+ * Allocates all scratch memory now (a few MB: per-row partial results,
+ * counters, the residual work list); runs never allocate.
+ * Returns SPECVERIFY_ERR_INVALID_ARG / _DTYPE on bad sizes, _CUDA if the
+ * device cannot be used.  *out is NULL on failure.
+ */
+int specverify_create(specverify_t *out, int device, int max_batch, int max_k, int vocab,
+                      int dtype);
+
+/* As specverify_create; flags may add SPECVERIFY_CREATE_HOST_STAGING, which also
+ * allocates device buffers for the largest inputs and outputs so that
+ * specverify_run_host can copy host data in and out. */
+int specverify_create_ex(specverify_t *out, int device, int max_batch, int max_k, int vocab,
+                         int dtype, unsigned flags);
+
+/*
+ * specverify_run -- verify one ragged batch; asynchronous on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream).  All pointers are device
+ * pointers owned by the caller:
+ *   target_logits   [batch + total_draft, vocab] of dtype, element-aligned;
+ *   draft_logits    [total_draft, vocab] of dtype, or NULL when every request
+ *                   with k_r > 0 is greedy;
+ *   draft_tokens    [total_draft] int32;
+ *   num_draft       [batch] int32, each in [0, max_k];
+ *   temperature     [batch] float32; 0 = greedy, > 0 = sampling;
+ *   seed            Philox key;
+ *   batch           in [0, max_batch];
+ *   total_draft     host copy of sum_r num_draft[r], in [0, batch*max_k];
+ *   accepted_len    [batch] int32 out;
+ *   committed_tokens[batch, max_k+1] int32 out;
+ *   accept_flags    [total_draft] uint8 out.
+ * Launches three kernels and returns without waiting; nothing is allocated.
+ */
+int specverify_run(specverify_t h, const void *target_logits, const void *draft_logits,
+                   const int32_t *draft_tokens, const int32_t *num_draft,
+                   const float *temperature, uint64_t seed, int batch, int total_draft,
+                   int32_t *accepted_len, int32_t *committed_tokens, uint8_t *accept_flags,
+                   void *stream);
+
+/*
+ * specverify_run_ex -- specverify_run plus optional inputs/outputs (each may be NULL):
+ *   request_ids  [batch] int64: the "request" word of the Philox counter (so a
+ *                request draws the same numbers in any batch position);
+ *   p_y, q_y, u  [total_draft] float32: p_i(y_i), q_i(y_i) and u_i of every draft
+ *                position of sampling requests (NaN for greedy/skipped ones);
+ *   req_status   [batch] int32: the status bits that concern each request.
+ */
+int specverify_run_ex(specverify_t h, const void *target_logits, const void *draft_logits,
+                      const int32_t *draft_tokens, const int32_t *num_draft,
+                      const float *temperature, uint64_t seed, int batch, int total_draft,
+                      int32_t *accepted_len, int32_t *committed_tokens, uint8_t *accept_flags,
+                      const int64_t *request_ids, float *p_y, float *q_y, float *u,
+                      int32_t *req_status, void *stream);
+
+/*
+ * specverify_run_host -- the same verify round on HOST buffers (same shapes as
+ * specverify_run; draft_logits may be NULL as there).  Copies the inputs into
+ * the handle's device staging (pinned host memory makes the copies
+ * asynchronous DMA), runs, copies the three outputs back and waits for
+ * `stream`.  Needs a handle made with SPECVERIFY_CREATE_HOST_STAGING.
+ */
+int specverify_run_host(specverify_t h, const void *target_logits, const void *draft_logits,
+                        const int32_t *draft_tokens, const int32_t *num_draft,
+                        const float *temperature, uint64_t seed, int batch, int total_draft,
+                        int32_t *accepted_len, int32_t *committed_tokens,
+                        uint8_t *accept_flags, void *stream);
+
+/* Wait for the handle's last stream and return the status bits of its last run
+ * in *status_out (host pointer). */
+int specverify_status(specverify_t h, int32_t *status_out);
+
+/*
+ * specverify_set_timing_events -- measurement aid.  After this call, run number
+ * i (counting from 0) records start_events[i % n] on its stream just before the
+ * row-pass kernel (the kernel that streams every logit row) and
+ * stop_events[i % n] just after it.  The arrays hold cudaEvent_t values created
+ * by the caller, n in [1, 64]; they are copied.  n = 0 turns recording off.
+ */
+int specverify_set_timing_events(specverify_t h, int n, void *const *start_events,
+                                 void *const *stop_events);
+
+/* Kernel launches one run makes (for launch accounting). */
+int specverify_launches_per_run(void);
+
+/* Free the handle and its device memory.  Further use returns _ERR_DESTROYED
+ * only while the memory of the freed handle is not reused; do not use it. */
+int specverify_destroy(specverify_t h);
+
+/* Static English text for a return code. */
+const char *specverify_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

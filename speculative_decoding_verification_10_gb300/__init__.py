@@ -1,0 +1,200 @@
+"""GB300 verify step for speculative sampling -- Python binding of libspecverify.
+
+Thin argument marshalling over the C ABI in include/specverify.h: every step
+of the verify round runs in the library's CUDA kernels.  PyTorch supplies
+device memory and streams only.
+
+    v = Verifier(max_batch=512, max_k=4, vocab=262144, dtype="bf16")
+    out = v.run(target, draft, tokens, num_draft, temperature, seed=1)
+    out.accepted_len, out.committed, out.flags
+
+Layout: request r has k_r = num_draft[r] draft positions; its k_r+1 target
+rows start at row sum_{s<r}(k_s+1) of `target`, its k_r draft rows and draft
+tokens at sum_{s<r} k_s.  T = 0 requests are greedy.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import (CREATE_HOST_STAGING, STATUS_BAD_K, STATUS_BAD_TEMP, STATUS_BAD_TOKEN,
+                   STATUS_BAD_TOTAL, STATUS_NO_DRAFT, STATUS_NONFINITE)
+
+__all__ = ["Verifier", "VerifyResult", "SpecVerifyError", "verify", "launches_per_run",
+           "STATUS_BAD_TOKEN", "STATUS_BAD_K", "STATUS_BAD_TEMP", "STATUS_NONFINITE",
+           "STATUS_BAD_TOTAL", "STATUS_NO_DRAFT"]
+
+_DTYPES = {"f32": (_lib.DTYPE_F32, torch.float32), "bf16": (_lib.DTYPE_BF16, torch.bfloat16)}
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {_lib.error_string(code)} ({code})")
+        self.code = code
+
+
+def _check(code: int, what: str):
+    if code != _lib.OK:
+        raise SpecVerifyError(code, what)
+
+
+@dataclass
+class VerifyResult:
+    accepted_len: torch.Tensor          # [B] int32, -1 = skipped
+    committed: torch.Tensor             # [B, max_k+1] int32, -1 padded
+    flags: torch.Tensor                 # [sum k] uint8
+    p_y: torch.Tensor | None = None     # [sum k] float32 (debug)
+    q_y: torch.Tensor | None = None
+    u: torch.Tensor | None = None
+    req_status: torch.Tensor | None = None
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def launches_per_run() -> int:
+    return int(_lib.load().specverify_launches_per_run())
+
+
+class Verifier:
+    """Owns one library handle (scratch memory sized at construction)."""
+
+    def __init__(self, max_batch: int, max_k: int, vocab: int, dtype: str = "bf16",
+                 device: int | torch.device | None = None, host_staging: bool = False):
+        if dtype not in _DTYPES:
+            raise ValueError(f"dtype must be one of {list(_DTYPES)}")
+        self.lib = _lib.load()
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = torch.device("cuda", device if isinstance(device, int) else device.index)
+        self.max_batch, self.max_k, self.vocab, self.dtype = max_batch, max_k, vocab, dtype
+        self.code, self.torch_dtype = _DTYPES[dtype]
+        h = ctypes.c_void_p()
+        flags = CREATE_HOST_STAGING if host_staging else 0
+        _check(self.lib.specverify_create_ex(ctypes.byref(h), self.device.index, max_batch,
+                                             max_k, vocab, self.code, flags),
+               "specverify_create")
+        self._h = h
+
+    # -- helpers --------------------------------------------------------------
+    def _stream(self, stream):
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        return ctypes.c_void_p(s.cuda_stream)
+
+    def _check_inputs(self, target, draft, tokens, num_draft, temperature):
+        if target.dtype != self.torch_dtype:
+            raise TypeError(f"target logits must be {self.torch_dtype}")
+        if draft is not None and draft.numel() and draft.dtype != self.torch_dtype:
+            raise TypeError(f"draft logits must be {self.torch_dtype}")
+        for name, t, dt in (("draft_tokens", tokens, torch.int32),
+                            ("num_draft", num_draft, torch.int32),
+                            ("temperature", temperature, torch.float32)):
+            if t.dtype != dt:
+                raise TypeError(f"{name} must be {dt}")
+        for t in (target, draft, tokens, num_draft, temperature):
+            if t is not None and t.numel() and (t.device != self.device or not t.is_contiguous()):
+                raise ValueError("inputs must be contiguous tensors on the handle's device")
+        if target.dim() != 2 or target.shape[1] != self.vocab:
+            raise ValueError(f"target logits must be [rows, {self.vocab}]")
+
+    def outputs(self, batch: int, total_draft: int, debug: bool = False) -> VerifyResult:
+        """Allocate output tensors for a batch (run() does this when none are given)."""
+        dev = self.device
+        res = VerifyResult(torch.empty(batch, dtype=torch.int32, device=dev),
+                           torch.empty(batch, self.max_k + 1, dtype=torch.int32, device=dev),
+                           torch.empty(total_draft, dtype=torch.uint8, device=dev))
+        if debug:
+            res.p_y = torch.empty(total_draft, dtype=torch.float32, device=dev)
+            res.q_y = torch.empty(total_draft, dtype=torch.float32, device=dev)
+            res.u = torch.empty(total_draft, dtype=torch.float32, device=dev)
+            res.req_status = torch.empty(batch, dtype=torch.int32, device=dev)
+        return res
+
+    # -- entry points ------------------------------------------------------------
+    def run(self, target, draft, tokens, num_draft, temperature, seed: int, *,
+            total_draft: int | None = None, out: VerifyResult | None = None,
+            request_ids=None, debug: bool = False, stream=None) -> VerifyResult:
+        """One verify round on device tensors (asynchronous on the current stream)."""
+        self._check_inputs(target, draft, tokens, num_draft, temperature)
+        batch = int(num_draft.shape[0])
+        if total_draft is None:
+            total_draft = int(tokens.shape[0])
+        if out is None:
+            out = self.outputs(batch, total_draft, debug=debug)
+        if request_ids is not None and (request_ids.dtype != torch.int64
+                                        or request_ids.device != self.device):
+            raise TypeError("request_ids must be int64 on the handle's device")
+        d = draft if (draft is not None and draft.numel()) else None
+        code = self.lib.specverify_run_ex(
+            self._h, _ptr(target), _ptr(d), _ptr(tokens), _ptr(num_draft), _ptr(temperature),
+            int(seed) & (2**64 - 1), batch, int(total_draft), _ptr(out.accepted_len),
+            _ptr(out.committed), _ptr(out.flags), _ptr(request_ids), _ptr(out.p_y),
+            _ptr(out.q_y), _ptr(out.u), _ptr(out.req_status), self._stream(stream))
+        _check(code, "specverify_run")
+        return out
+
+    def run_host(self, target, draft, tokens, num_draft, temperature, seed: int,
+                 accepted_len, committed, flags, *, stream=None) -> None:
+        """One verify round on host (ideally pinned) CPU tensors; blocks until done."""
+        batch = int(num_draft.shape[0])
+        total_draft = int(tokens.shape[0])
+        for t in (target, tokens, num_draft, temperature, accepted_len, committed, flags):
+            if t.device.type != "cpu" or not t.is_contiguous():
+                raise ValueError("run_host takes contiguous CPU tensors")
+        d = draft if (draft is not None and draft.numel()) else None
+        code = self.lib.specverify_run_host(
+            self._h, _ptr(target), _ptr(d), _ptr(tokens), _ptr(num_draft), _ptr(temperature),
+            int(seed) & (2**64 - 1), batch, total_draft, _ptr(accepted_len), _ptr(committed),
+            _ptr(flags), self._stream(stream))
+        _check(code, "specverify_run_host")
+
+    def set_timing_events(self, starts, stops) -> None:
+        """Record the given torch.cuda.Event pairs around the row-pass kernel of the
+        following runs (run i uses pair i % n); pass empty lists to stop."""
+        n = len(starts)
+        arr_s = (ctypes.c_void_p * max(n, 1))(*[ctypes.c_void_p(e.cuda_event) for e in starts])
+        arr_e = (ctypes.c_void_p * max(n, 1))(*[ctypes.c_void_p(e.cuda_event) for e in stops])
+        _check(self.lib.specverify_set_timing_events(self._h, n, arr_s, arr_e),
+               "specverify_set_timing_events")
+
+    def status(self) -> int:
+        """Status bits of the last run (waits for its stream)."""
+        st = ctypes.c_int32()
+        _check(self.lib.specverify_status(self._h, ctypes.byref(st)), "specverify_status")
+        return int(st.value)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            _check(self.lib.specverify_destroy(self._h), "specverify_destroy")
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def verify(target, draft, tokens, num_draft, temperature, seed: int, max_k: int | None = None,
+           request_ids=None, debug: bool = False) -> VerifyResult:
+    """One-shot verify round (makes a handle sized for this batch)."""
+    batch = int(num_draft.shape[0])
+    if max_k is None:
+        max_k = int(num_draft.max().item()) if batch else 0
+    dtype = "bf16" if target.dtype == torch.bfloat16 else "f32"
+    with Verifier(max(batch, 1), max_k, int(target.shape[1]), dtype,
+                  device=target.device.index) as v:
+        out = v.run(target, draft, tokens, num_draft, temperature, seed,
+                    request_ids=request_ids, debug=debug)
+        torch.cuda.current_stream(v.device).synchronize()
+        return out

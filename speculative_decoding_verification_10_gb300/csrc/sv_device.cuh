@@ -1,0 +1,273 @@
+// sv_device.cuh -- device building blocks of the verify kernels (sm_103a).
+//
+// Counter-based randomness, vector loads, and the per-thread accumulators of
+// the three row reductions the verify step needs:
+//   * online max / sum-exp of x/T (the softmax normaliser of p_i and q_i),
+//   * argmax with lowest index (greedy rows),
+//   * the exponential race argmax_v (c*x_v - log2 E_v)  ==  argmin_v E_v / p_v
+//     (bonus draw; "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree,
+//     and DSpark", section 1: one more token from the target when every
+//     draft survives).
+// Every quantity is kept in the base-2 log domain: c = log2(e)/T, so
+// exp(x/T - m) = 2^(c*x - m2) and the MUFU ex2/lg2 units do the work.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).  Counter
+// (floor(v/4), position, request lo, stream | request hi << 8), key = seed.
+// ---------------------------------------------------------------------------
+struct PhiloxKey {
+  uint32_t k0, k1;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
+  uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t lo0 = c.x * 0xD2511F53u;
+    const uint32_t hi0 = __umulhi(c.x, 0xD2511F53u);
+    const uint32_t lo1 = c.z * 0xCD9E8D57u;
+    const uint32_t hi1 = __umulhi(c.z, 0xCD9E8D57u);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t word_of(uint4 r, int i) {
+  return i == 0 ? r.x : (i == 1 ? r.y : (i == 2 ? r.z : r.w));
+}
+
+// Acceptance uniform of one draft position: word 0 of stream 0, as
+// (w >> 8) * 2^-24 -- exactly representable in fp32.
+__device__ __forceinline__ float accept_uniform(PhiloxKey key, uint32_t pos, uint32_t req_lo,
+                                                uint32_t req_hi) {
+  const uint4 r = philox4x32_10(make_uint4(0u, pos, req_lo, 0u | (req_hi << 8)), key);
+  return (float)(r.x >> 8) * 0x1p-24f;
+}
+
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Race exponential E = -ln((w + 1/2) 2^-32), relative error ~1e-7 over its
+// whole range (1.2e-10 .. 22.9).  Below one half, U itself is accurate and
+// |log2 U| >= 1, so the hardware lg2 is relatively accurate; above one half,
+// d = 1 - U is formed exactly from ~w and E = -log1p(-d) keeps full relative
+// accuracy as E -> 0 (where the race winners live).
+__device__ __forceinline__ float race_exponential(uint32_t w) {
+  if (w < 0x80000000u) {
+    const float u = fmaf((float)w, 0x1p-32f, 0x1p-33f);
+    return -fast_lg2(u) * kLn2;
+  }
+  const float d = fmaf((float)(~w), 0x1p-32f, 0x1p-33f);
+  return -log1pf(-d);
+}
+
+// ---------------------------------------------------------------------------
+// Loads.  Logit rows are streamed once: 16-byte non-coherent loads that skip L1.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// Element types: fp32 (4 per 16 B) and bf16 (8 per 16 B).
+struct F32 {
+  static constexpr int kVec = 4;
+  static constexpr int kBytes = 4;
+  __device__ static __forceinline__ void unpack(uint4 v, float (&x)[kVec]) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ uint4 pad() {
+    const uint32_t n = 0xff800000u;  // -inf
+    return make_uint4(n, n, n, n);
+  }
+  __device__ static __forceinline__ float load1(const void* row, int i) {
+    return __ldg(reinterpret_cast<const float*>(row) + i);
+  }
+};
+
+struct BF16 {
+  static constexpr int kVec = 8;
+  static constexpr int kBytes = 2;
+  __device__ static __forceinline__ void unpack(uint4 v, float (&x)[kVec]) {
+    // little-endian: the lower-addressed element is the low half
+    x[0] = __uint_as_float(v.x << 16);
+    x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16);
+    x[3] = __uint_as_float(v.y & 0xffff0000u);
+    x[4] = __uint_as_float(v.z << 16);
+    x[5] = __uint_as_float(v.z & 0xffff0000u);
+    x[6] = __uint_as_float(v.w << 16);
+    x[7] = __uint_as_float(v.w & 0xffff0000u);
+  }
+  __device__ static __forceinline__ uint4 pad() {
+    const uint32_t n = 0xff80ff80u;  // -inf, -inf
+    return make_uint4(n, n, n, n);
+  }
+  __device__ static __forceinline__ float load1(const void* row, int i) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+    return __uint_as_float((uint32_t)h << 16);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Accumulators.  Each is a per-thread state with an element update and a
+// commutative, associative merge; results do not depend on how a row is split.
+// ---------------------------------------------------------------------------
+
+// Online softmax normaliser in base 2: m = max_v c*x_v, s = sum_v 2^(c*x_v - m).
+struct SoftmaxAcc {
+  float m, s;
+  __device__ __forceinline__ void init() {
+    m = kNegInf;
+    s = 0.f;
+  }
+  template <int N>
+  __device__ __forceinline__ void add(const float (&x)[N], float c) {
+    float mx = x[0];
+#pragma unroll
+    for (int e = 1; e < N; ++e) mx = fmaxf(mx, x[e]);
+    const float vm = mx * c;
+    if (vm > m) {
+      s *= fast_ex2(m - vm);
+      m = vm;
+    }
+    if (m != kNegInf) {
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < N; e += 2) {
+        s0 += fast_ex2(fmaf(x[e], c, -m));
+        if (e + 1 < N) s1 += fast_ex2(fmaf(x[e + 1], c, -m));
+      }
+      s += s0 + s1;
+    }
+  }
+  __device__ __forceinline__ void add1(float x, float c) {
+    float a[1] = {x};
+    add<1>(a, c);
+  }
+  __device__ static __forceinline__ SoftmaxAcc merge(SoftmaxAcc a, SoftmaxAcc b) {
+    SoftmaxAcc r;
+    r.m = fmaxf(a.m, b.m);
+    if (r.m == kNegInf) {
+      r.s = a.s + b.s;  // both empty (or NaN carried)
+    } else {
+      r.s = a.s * fast_ex2(a.m - r.m) + b.s * fast_ex2(b.m - r.m);
+    }
+    return r;
+  }
+  __device__ __forceinline__ SoftmaxAcc shfl_xor(int lane_mask) const {
+    SoftmaxAcc o;
+    o.m = __shfl_xor_sync(0xffffffffu, m, lane_mask);
+    o.s = __shfl_xor_sync(0xffffffffu, s, lane_mask);
+    return o;
+  }
+};
+
+// Best (value, index): larger value wins, lower index on ties; idx -1 = none.
+struct BestAcc {
+  float v;
+  int idx;
+  uint32_t nan;
+  __device__ __forceinline__ void init() {
+    v = kNegInf;
+    idx = -1;
+    nan = 0u;
+  }
+  __device__ __forceinline__ void take(float val, int i) {
+    // callers feed indices in increasing order, so strict '>' keeps the lowest
+    if (val > v) {
+      v = val;
+      idx = i;
+    }
+  }
+  __device__ static __forceinline__ bool better(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && (uint32_t)ia < (uint32_t)ib);
+  }
+  __device__ static __forceinline__ BestAcc merge(BestAcc a, BestAcc b) {
+    BestAcc r = better(b.v, b.idx, a.v, a.idx) ? b : a;
+    r.nan = a.nan | b.nan;
+    return r;
+  }
+  __device__ __forceinline__ BestAcc shfl_xor(int lane_mask) const {
+    BestAcc o;
+    o.v = __shfl_xor_sync(0xffffffffu, v, lane_mask);
+    o.idx = __shfl_xor_sync(0xffffffffu, idx, lane_mask);
+    o.nan = __shfl_xor_sync(0xffffffffu, nan, lane_mask);
+    return o;
+  }
+};
+
+// Two races at once (residual draw and its fallback on p).
+struct Best2Acc {
+  BestAcc a, b;
+  __device__ __forceinline__ void init() {
+    a.init();
+    b.init();
+  }
+  __device__ static __forceinline__ Best2Acc merge(Best2Acc x, Best2Acc y) {
+    Best2Acc r;
+    r.a = BestAcc::merge(x.a, y.a);
+    r.b = BestAcc::merge(x.b, y.b);
+    return r;
+  }
+  __device__ __forceinline__ Best2Acc shfl_xor(int lane_mask) const {
+    Best2Acc o;
+    o.a = a.shfl_xor(lane_mask);
+    o.b = b.shfl_xor(lane_mask);
+    return o;
+  }
+};
+
+template <typename Acc>
+__device__ __forceinline__ Acc warp_reduce(Acc a) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) a = Acc::merge(a, a.shfl_xor(off));
+  return a;
+}
+
+// Block-wide reduction; the result is valid in thread 0.  `scratch` holds one
+// Acc per warp.
+template <typename Acc, int kThreads>
+__device__ __forceinline__ Acc block_reduce(Acc a, Acc* scratch) {
+  constexpr int kWarps = kThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_reduce(a);
+  if (lane == 0) scratch[warp] = a;
+  __syncthreads();
+  if (warp == 0) {
+    Acc b = scratch[lane < kWarps ? lane : 0];
+    if (lane >= kWarps) b.init();
+    a = warp_reduce(b);
+  }
+  __syncthreads();
+  return a;
+}
+
+}  // namespace sv

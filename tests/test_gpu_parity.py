@@ -1,0 +1,310 @@
+"""GPU path (through the C ABI) against the CPU oracle, element by element.
+
+Run on a CUDA device (``-m gpu``).  Tolerances are those stated in
+tests/parity.py: exact tokens / lengths / flags, except decisions within a
+relative 1e-5 of their threshold, which are counted.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_10_gb300 import Verifier, build
+from speculative_decoding_verification_10_gb300 import workloads as W
+from tests import cases, parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _verifier(inp, dtype, max_batch=None, max_k=None):
+    B = len(inp["num_draft"])
+    V = inp["target"].shape[1]
+    return Verifier(max(1, max_batch or B), inp["max_k"] if max_k is None else max_k, V, dtype)
+
+
+def _dtype_of(inp):
+    return "bf16" if inp["target"].dtype == np.uint16 else "f32"
+
+
+def _check(inp, seeds=(1,), max_batch=None, max_k=None):
+    dtype = _dtype_of(inp)
+    reps = []
+    with _verifier(inp, dtype, max_batch, max_k) as v:
+        for seed in seeds:
+            g = parity.run_gpu(v, inp, seed)
+            o = parity.run_oracle(inp, seed)
+            reps.append(parity.compare(g, o, inp, seed))
+    return reps
+
+
+# --- the five synthetic workloads ------------------------------------------------
+
+@pytest.mark.parametrize("name", ["w0_v1024_f32", "w1_v32000_bf16"])
+def test_small_workloads_full_parity(name):
+    b = W.make_batch(name, device="cpu")
+    inp = b.numpy_inputs()
+    reps = _check(inp, seeds=(1, 2, 3, 4))
+    total = sum(r["sampling"] + r["greedy"] for r in reps)
+    exempt = sum(r["exempt_accept"] + r["exempt_race"] + r["exempt_residual_mass"] for r in reps)
+    print(name, reps)
+    assert exempt <= max(1, total // 100)
+
+
+@pytest.mark.parametrize("name", ["w2_v128256_bf16", "w3_v151936_bf16", "w4_v262144_bf16"])
+def test_large_vocab_reduced_batch_parity(name):
+    # full vocabulary, fewer requests: several vocab chunks per row and a ragged tail
+    b = W.make_batch(name, device="cuda", batch=20)
+    inp = b.numpy_inputs()
+    reps = _check(inp, seeds=(1, 7))
+    print(name, reps)
+
+
+def _slice_outputs(gpu, num_draft, idx):
+    d_off = np.concatenate([[0], np.cumsum(num_draft)])
+    sel = np.concatenate([np.arange(d_off[r], d_off[r + 1]) for r in idx]) if len(idx) else []
+    out = {"accepted_len": gpu["accepted_len"][idx], "committed": gpu["committed"][idx],
+           "flags": gpu["flags"][sel], "status": gpu["status"]}
+    for key in ("p_y", "q_y", "u"):
+        out[key] = gpu[key][sel]
+    out["req_status"] = gpu["req_status"][idx]
+    return out
+
+
+@pytest.mark.parametrize("name", ["w2_v128256_bf16", "w3_v151936_bf16", "w4_v262144_bf16"])
+def test_full_size_workload_sampled_parity(name):
+    """Full batch in the benchmark's launch configuration; the oracle re-verifies
+    a sample of requests one by one (keyed by their batch index)."""
+    b = W.make_batch(name, device="cuda")
+    seed = 1
+    nd = b.num_draft.cpu().numpy()
+    with Verifier(b.batch, b.max_k, b.vocab, b.dtype) as v:
+        res = v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, seed, debug=True)
+        torch.cuda.synchronize()
+        gpu = {"accepted_len": res.accepted_len.cpu().numpy(),
+               "committed": res.committed.cpu().numpy(), "flags": res.flags.cpu().numpy(),
+               "p_y": res.p_y.cpu().numpy(), "q_y": res.q_y.cpu().numpy(),
+               "u": res.u.cpu().numpy(), "req_status": res.req_status.cpu().numpy(),
+               "status": v.status()}
+    assert gpu["status"] == 0
+    rng = np.random.default_rng(0)
+    idx = np.sort(rng.choice(b.batch, size=min(16, b.batch), replace=False))
+    idx = np.unique(np.concatenate([idx, [0, b.batch - 1]]))
+    sub = W.subset(b, idx)
+    inp = sub.numpy_inputs()
+    o = parity.run_oracle(inp, seed)
+    rep = parity.compare(_slice_outputs(gpu, nd, idx), o, inp, seed)
+    print(name, rep)
+    # invariants over the whole batch
+    A = gpu["accepted_len"]
+    assert (A >= 0).all() and (A <= nd).all()
+    d_off = np.concatenate([[0], np.cumsum(nd)])
+    for r in range(b.batch):
+        f = gpu["flags"][d_off[r]:d_off[r + 1]]
+        assert f.sum() == A[r] and (f[:A[r]] == 1).all()
+        c = gpu["committed"][r]
+        assert (c[:A[r] + 1] >= 0).all() and (c[:A[r] + 1] < b.vocab).all()
+        assert (c[A[r] + 1:] == -1).all()
+
+
+# --- the worked examples on the GPU path ------------------------------------------
+
+@pytest.mark.parametrize("case", cases.read_worked_examples(), ids=lambda c: c["case"])
+@pytest.mark.parametrize("temperature", [1.0, 0.7, 0.0])
+@pytest.mark.parametrize("dtype,vocab", [("f32", 16), ("bf16", 16), ("bf16", 1001), ("f32", 70000)])
+def test_worked_examples_gpu(case, temperature, dtype, vocab):
+    inp, expect = cases.worked_case_batch(case, vocab=vocab, copies=48, temperature=temperature,
+                                          dtype=dtype)
+    A = case["expect_accepted"]
+    with _verifier(inp, dtype) as v:
+        for seed in (0, 1, 12345, 2**63 + 5):
+            g = parity.run_gpu(v, inp, seed)
+            assert g["status"] == 0
+            assert (g["accepted_len"] == A).all()
+            assert (g["committed"][:, :A + 1] == np.array(expect)).all()
+            assert (g["committed"][:, A + 1:] == -1).all()
+
+
+# --- ragged batches, odd vocabularies, mixed modes ---------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("vocab", [1, 5, 8, 1000, 1001, 4099, 33000])
+def test_random_ragged_batches(dtype, vocab):
+    rng = np.random.default_rng(vocab)
+    B = 37
+    k = rng.integers(0, 7, size=B)
+    temp = rng.choice([0.0, 0.5, 0.7, 1.0, 1.6], size=B)
+    inp = cases.random_batch(k, temp, vocab=vocab, sigma_t=2.5, sigma_d=1.0, dtype=dtype,
+                             seed=vocab + 1)
+    inp["max_k"] = 6
+    _check(inp, seeds=(3, 99))
+
+
+@pytest.mark.parametrize("max_k", [15, 31])
+def test_long_windows(max_k):
+    B = 9
+    k = np.array([max_k] * 4 + [0, 1, max_k // 2, max_k, 3])
+    temp = np.array([1.0, 0.8, 0.0, 1.0, 1.0, 0.0, 0.9, 1.0, 0.7])
+    inp = cases.random_batch(k, temp, vocab=2048, sigma_t=2.0, sigma_d=0.3, dtype="bf16", seed=5)
+    inp["max_k"] = max_k
+    _check(inp, seeds=(1, 2))
+
+
+def test_identical_and_disjoint_rows():
+    inp = cases.random_batch([4] * 16, [0.9] * 16, vocab=3000, dtype="bf16", seed=8)
+    t_off = np.concatenate([[0], np.cumsum(inp["num_draft"] + 1)])
+    src = np.concatenate([np.arange(t_off[r], t_off[r] + 4) for r in range(16)])
+    inp["draft"] = inp["target"][src].copy()
+    with _verifier(inp, "bf16") as v:
+        g = parity.run_gpu(v, inp, 4)
+    assert (g["accepted_len"] == 4).all()
+    V, B = 64, 100
+    tgt = np.full((2 * B, V), -np.inf, np.float32)
+    tgt[:, :32] = 0.0
+    drf = np.full((B, V), -np.inf, np.float32)
+    drf[:, 32:] = 0.0
+    inp = dict(target=tgt, draft=drf, tokens=(32 + np.arange(B) % 32).astype(np.int32),
+               num_draft=np.ones(B, np.int32), temperature=np.ones(B, np.float32), max_k=1)
+    reps = _check(inp, seeds=(1,))
+    with _verifier(inp, "f32") as v:
+        g = parity.run_gpu(v, inp, 1)
+    assert (g["accepted_len"] == 0).all() and (g["committed"][:, 0] < 32).all()
+
+
+def test_greedy_only_without_draft_logits():
+    inp = cases.random_batch([3, 0, 5, 2], [0.0] * 4, vocab=5000, dtype="bf16", seed=2)
+    inp["max_k"] = 5
+    o = parity.run_oracle(inp, 1)
+    inp2 = dict(inp)
+    inp2["draft"] = None
+    with _verifier(inp2, "bf16") as v:
+        g = parity.run_gpu(v, inp2, 1)
+    assert g["status"] == 0
+    assert (g["committed"] == o["committed"]).all() and (g["accepted_len"] == o["accepted_len"]).all()
+
+
+def test_all_zero_drafts_and_empty_batch():
+    inp = cases.random_batch([0] * 10, [1.0] * 5 + [0.0] * 5, vocab=777, dtype="bf16", seed=3)
+    inp["max_k"] = 2
+    _check(inp, seeds=(1, 2))
+    with Verifier(4, 2, 777, "bf16") as v:
+        e = torch.empty(0, dtype=torch.int32, device="cuda")
+        res = v.run(torch.empty(0, 777, dtype=torch.bfloat16, device="cuda"), None, e, e,
+                    torch.empty(0, dtype=torch.float32, device="cuda"), 1)
+        assert res.accepted_len.numel() == 0
+
+
+# --- invalid inputs: reported, skipped, never a fault --------------------------------
+
+def test_invalid_inputs_status_and_skip():
+    inp = cases.random_batch([2, 2, 2, 2, 2, 2, 2], [1.0, 1.0, 0.0, 1.0, 1.0, 1.0, 1.0],
+                             vocab=300, dtype="f32", seed=6)
+    bad = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in inp.items()}
+    bad["tokens"][2] = 300              # request 1: token == V
+    bad["tokens"][4] = -1               # request 2 (greedy): negative token
+    bad["temperature"][3] = np.nan      # request 3
+    bad["target"][4 * 3 + 1, 7] = np.nan   # request 4: NaN in a target row
+    bad["draft"][5 * 2 + 1, 9] = np.inf    # request 5: +inf in a draft row
+    bad["target"][6 * 3 + 2, :] = -np.inf  # request 6: bonus row without a finite logit
+    _check(bad, seeds=(1,))
+    with _verifier(bad, "f32") as v:
+        g = parity.run_gpu(v, bad, 1)
+    assert g["status"] == (oracle.BAD_TOKEN | oracle.BAD_TEMP | oracle.NONFINITE)
+    assert g["accepted_len"][0] >= 0 and (g["accepted_len"][1:] == -1).all()
+    # layout errors skip the whole batch
+    wrong = dict(inp)
+    wrong["num_draft"] = np.array([2, 2, 2, 2, 2, 2, 3], np.int32)   # k > max_k
+    with _verifier(inp, "f32") as v:
+        t = parity.to_torch(wrong, "cuda")
+        res = v.run(t["target"], t["draft"], t["tokens"], t["num_draft"], t["temperature"], 1,
+                    total_draft=14)
+        assert v.status() == oracle.BAD_K
+        assert (res.accepted_len.cpu().numpy() == -1).all()
+        t = parity.to_torch(inp, "cuda")
+        res = v.run(t["target"], t["draft"], t["tokens"][:13], t["num_draft"], t["temperature"], 1,
+                    total_draft=13)
+        assert v.status() == oracle.BAD_TOTAL
+        # a valid run right after clears the status
+        v.run(t["target"], t["draft"], t["tokens"], t["num_draft"], t["temperature"], 1)
+        assert v.status() == 0
+    nod = dict(inp)
+    nod["draft"] = None
+    with _verifier(inp, "f32") as v:
+        g = parity.run_gpu(v, nod, 1)
+    assert g["status"] == oracle.NO_DRAFT
+    assert (g["accepted_len"][[0, 1, 3, 4, 5, 6]] == -1).all() and g["accepted_len"][2] >= 0
+
+
+# --- properties of the randomness ------------------------------------------------------
+
+def test_request_ids_make_results_order_independent():
+    b = W.make_batch("w1_v32000_bf16", device="cuda", batch=24)
+    with Verifier(24, 3, b.vocab, "bf16") as v:
+        r1 = v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 5)
+        c1 = r1.committed.clone()
+        r2 = v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 5)
+        assert torch.equal(c1, r2.committed)            # deterministic
+        perm = np.random.default_rng(1).permutation(24)
+        sub = W.subset(b, perm)                           # request_ids = original index
+        r3 = v.run(sub.target, sub.draft, sub.tokens, sub.num_draft, sub.temperature, 5,
+                   request_ids=sub.request_ids)
+        assert torch.equal(r3.committed, c1[torch.as_tensor(perm, device="cuda")])
+
+
+def test_million_trials_distribution_and_bit_exactness():
+    rng = np.random.default_rng(2024)
+    V, k, T, n = 8, 2, 1.0, 1_000_000
+    tgt = (rng.normal(size=(k + 1, V)) * 1.5).astype(np.float32)
+    drf = (tgt[:k] + rng.normal(size=(k, V))).astype(np.float32)
+    toks = np.stack([rng.choice(V, size=n, p=_softmax(drf[i], T)) for i in range(k)], 1)
+    inp = dict(target=np.tile(tgt, (n, 1)), draft=np.tile(drf, (n, 1)),
+               tokens=toks.reshape(-1).astype(np.int32), num_draft=np.full(n, k, np.int32),
+               temperature=np.full(n, T, np.float32), max_k=k)
+    with _verifier(inp, "f32") as v:
+        g = parity.run_gpu(v, inp, 123, debug=False)
+    o = parity.run_oracle(inp, 123)
+    same = (g["committed"] == o["committed"]).all(1)
+    # exact agreement except near-threshold draws
+    assert same.mean() > 1 - 1e-4
+    p = [_softmax(tgt[i], T) for i in range(k + 1)]
+    scipy_stats = pytest.importorskip("scipy.stats")
+    for col, sel, probs in ((0, np.ones(n, bool), p[0]),
+                            (1, g["accepted_len"] >= 1, p[1]),
+                            (2, g["accepted_len"] == 2, p[2])):
+        cnt = np.bincount(g["committed"][sel, col], minlength=V).astype(np.float64)
+        e = probs * cnt.sum()
+        stat = ((cnt - e) ** 2 / e).sum()
+        assert scipy_stats.chi2.sf(stat, V - 1) > 1e-3
+    a0 = np.minimum(p[0], _softmax(drf[0], T)).sum()
+    z = ((g["accepted_len"] >= 1).mean() - a0) / math.sqrt(a0 * (1 - a0) / n)
+    assert abs(z) < 4.5
+
+
+def _softmax(x, t):
+    z = np.asarray(x, np.float64) / t
+    z = np.exp(z - z.max())
+    return z / z.sum()
+
+
+# --- host-buffer entry point ----------------------------------------------------------
+
+def test_run_host_matches_device_run():
+    b = W.make_batch("w3_v151936_bf16", device="cuda", batch=12)
+    with Verifier(12, b.max_k, b.vocab, "bf16", host_staging=True) as v:
+        dev = v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 9)
+        torch.cuda.synchronize()
+        h = b.to("cpu")
+        acc = torch.empty(12, dtype=torch.int32).pin_memory()
+        com = torch.empty(12, b.max_k + 1, dtype=torch.int32).pin_memory()
+        flg = torch.empty(b.total_draft, dtype=torch.uint8).pin_memory()
+        v.run_host(h.target.pin_memory(), h.draft.pin_memory(), h.tokens, h.num_draft,
+                   h.temperature, 9, acc, com, flg)
+        assert torch.equal(acc, dev.accepted_len.cpu())
+        assert torch.equal(com, dev.committed.cpu())
+        assert torch.equal(flg, dev.flags.cpu())
