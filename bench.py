@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=0,
                     help="requests in the oracle sample (0 = about 10 s of work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests per batch (0 = the workload's own); for profiling captures")
     return ap.parse_args()
 
 
@@ -224,85 +227,10 @@ def _probe_seconds(b):
     return dt
 
 
-def run_ours(args):
+def measure_e2e(args, b, v, world, dev):
+    """rows/s through specverify_run_host: pinned host inputs in, outputs out, per step."""
     import torch
     import torch.distributed as dist
-    from speculative_decoding_verification_10_gb300 import Verifier, build, launches_per_run
-    from speculative_decoding_verification_10_gb300 import workloads as W
-
-    rank, world, local = dist_env()
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if rank == 0:
-        build.build()
-    if world > 1:
-        dist.barrier()
-
-    spec = W.SPECS[args.workload]
-    b = W.make_batch(args.workload, device=dev, gen_seed=spec.gen_seed + 7919 * rank)
-    rows_per_step = b.verified_rows()
-    alg_bytes = b.algorithmic_bytes()
-    es = 2 if b.dtype == "bf16" else 4
-    k = b.num_draft.cpu().numpy().astype(np.int64)
-    t = b.temperature.cpu().numpy()
-    rowpass_bytes = int(np.where(t > 0, 2 * k + 1, k + 1).sum()) * b.vocab * es
-
-    v = Verifier(b.batch, b.max_k, b.vocab, b.dtype, device=local, host_staging=True)
-    out = v.outputs(b.batch, b.total_draft)
-    stream = torch.cuda.current_stream(dev)
-
-    def step():
-        v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 1, out=out)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    if v.status() != 0:
-        raise RuntimeError(f"verify status {v.status()} on the benchmark batch")
-
-    n_ev = min(64, args.steps)
-    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.5)
-
-    # timed region: K steps, CUDA events on the launching stream
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.mark("start")
-    t_start.record(stream)
-    kernel_ms = []
-    done = 0
-    while done < args.steps:
-        chunk = min(n_ev, args.steps - done)
-        v.set_timing_events(ev_s[:chunk], ev_e[:chunk])
-        for _ in range(chunk):
-            step()
-        done += chunk
-        if done < args.steps:
-            stream.synchronize()   # read this chunk's kernel times before reusing events
-            kernel_ms += [ev_s[i].elapsed_time(ev_e[i]) for i in range(chunk)]
-    t_stop.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark("stop")
-    kernel_ms += [ev_s[i].elapsed_time(ev_e[i]) for i in range(chunk)]
-    v.set_timing_events([], [])
-    if world > 1:
-        dist.barrier()
-    ms = t_start.elapsed_time(t_stop) / args.steps
-    ms_t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    clock_info = clocks.stop()
-
-    # end to end through the host-buffer entry point (pinned host inputs)
     hb = b.to("cpu")
     h_target = hb.target.pin_memory()
     h_draft = hb.draft.pin_memory()
@@ -326,6 +254,92 @@ def run_ours(args):
     h2d = (h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()
            + 4 * (h_tokens.numel() + h_nd.numel() + h_temp.numel()))
     d2h = 4 * h_acc.numel() + 4 * h_com.numel() + h_flg.numel()
+    return {"value": world * b.verified_rows() / e2e_s, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from speculative_decoding_verification_10_gb300 import Verifier, build, launches_per_run
+    from speculative_decoding_verification_10_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+
+    spec = W.SPECS[args.workload]
+    b = W.make_batch(args.workload, device=dev, gen_seed=spec.gen_seed + 7919 * rank,
+                     batch=args.batch or None)
+    torch.cuda.empty_cache()
+    rows_per_step = b.verified_rows()
+    alg_bytes = b.algorithmic_bytes()
+    es = 2 if b.dtype == "bf16" else 4
+    k = b.num_draft.cpu().numpy().astype(np.int64)
+    t = b.temperature.cpu().numpy()
+    rowpass_bytes = int(np.where(t > 0, 2 * k + 1, k + 1).sum()) * b.vocab * es
+
+    v = Verifier(b.batch, b.max_k, b.vocab, b.dtype, device=local, host_staging=not args.no_e2e)
+    out = v.outputs(b.batch, b.total_draft)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 1, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if v.status() != 0:
+        raise RuntimeError(f"verify status {v.status()} on the benchmark batch")
+
+    n_ev = min(64, args.steps)
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    for e in ev_s + ev_e:        # torch creates the CUDA event on first record
+        e.record(stream)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+
+    # timed region: K steps, CUDA events on the launching stream
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    t_start.record(stream)
+    # the row-pass kernel of the first n_ev timed steps is bracketed by events
+    v.set_timing_events(ev_s, ev_e)
+    for i in range(args.steps):
+        if i == n_ev:
+            v.set_timing_events([], [])
+        step()
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("stop")
+    kernel_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(n_ev)]
+    v.set_timing_events([], [])
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_stop) / args.steps
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    clock_info = clocks.stop()
+
+    # end to end through the host-buffer entry point (pinned host inputs)
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, b, v, world, dev)
 
     # CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
     cpu = None
@@ -360,14 +374,12 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "sv_rowpass", "kernel_ms": kernel_avg_ms,
+                     "kernel": "sv_verify", "kernel_ms": kernel_avg_ms,
                      "alg_bytes_per_launch": rowpass_bytes,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback"},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * rows_per_step / e2e_s, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_s * 1e3},
+        "e2e": e2e,
         "clocks": clock_info,
         "gpu_launches": launches_per_run() * args.steps,
     }

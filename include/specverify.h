@@ -97,7 +97,7 @@ typedef enum {
 
 /*
  * specverify_create -- make a handle bound to CUDA device `device`.
- *   max_batch  >= 1: largest batch a run may pass;
+ *   max_batch  in [1, 4096]: largest batch a run may pass;
  *   max_k      in [0, 31]: largest num_draft (committed rows are max_k+1 wide);
  *   vocab      in [1, 2^30]: V, the logits row length;
  *   dtype      SPECVERIFY_F32 or SPECVERIFY_BF16.
@@ -131,7 +131,7 @@ int specverify_create_ex(specverify_t *out, int device, int max_batch, int max_k
  *   accepted_len    [batch] int32 out;
  *   committed_tokens[batch, max_k+1] int32 out;
  *   accept_flags    [total_draft] uint8 out.
- * Launches three kernels and returns without waiting; nothing is allocated.
+ * Launches one kernel and returns without waiting; nothing is allocated.
  */
 int specverify_run(specverify_t h, const void *target_logits, const void *draft_logits,
                    const int32_t *draft_tokens, const int32_t *num_draft,
@@ -174,7 +174,7 @@ int specverify_status(specverify_t h, int32_t *status_out);
 /*
  * specverify_set_timing_events -- measurement aid.  After this call, run number
  * i (counting from 0) records start_events[i % n] on its stream just before the
- * row-pass kernel (the kernel that streams every logit row) and
+ * verify kernel (the single kernel of a run) and
  * stop_events[i % n] just after it.  The arrays hold cudaEvent_t values created
  * by the caller, n in [1, 64]; they are copied.  n = 0 turns recording off.
  */

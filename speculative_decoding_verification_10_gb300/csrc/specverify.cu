@@ -1,7 +1,7 @@
 // specverify.cu -- host side of the C ABI declared in include/specverify.h.
 //
-// Argument checking, scratch ownership and the three launches of a verify
-// round (plan, row pass, residual).  All device work lives in sv_kernels.cuh.
+// Argument checking, scratch ownership and the single launch of a verify
+// round.  All device work lives in sv_kernels.cuh.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -17,10 +17,9 @@ namespace {
 
 constexpr uint32_t kLiveMagic = 0x53564c56u;  // "SVLV"
 constexpr uint32_t kDeadMagic = 0x53564444u;  // "SVDD"
-constexpr size_t kChunkBytes = 64 * 1024;      // target bytes of logits per work item
-constexpr size_t kMinChunkBytes = 4 * 1024;
-constexpr int kMaxChunks = 64;
+constexpr int kMaxNper = 16;                   // 16-byte vectors per thread per chunk (64 KB of logits)
 constexpr size_t kPartialBudget = size_t(256) << 20;
+constexpr int kSpinLimit = 1 << 16;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -42,20 +41,18 @@ struct DeviceGuard {
 struct specverify_ctx {
   uint32_t magic;
   int device, max_batch, max_k, vocab, dtype, elem_bytes;
-  int num_sms, grid_rowpass, grid_resid, max_nch;
-  size_t max_rows;
+  int num_sms, grid, max_nch;
+  size_t max_rows, smem_bytes_max;
   void* scratch;
   size_t scratch_bytes;
-  sv::ReqInfo* req;
-  sv::RowInfo* rows;
   sv::Partial* part;
   sv::Partial* rowres;
   int* row_cnt;
   int* req_cnt;
-  int2* res_list;
-  sv::Partial2* part2;
+  unsigned long long* res_slots;
+  sv::Partial* part2;
   int* res_cnt;
-  int* counters;
+  int* ctr;
   // staging for specverify_run_host
   void* stage;
   char* st_target;
@@ -67,7 +64,8 @@ struct specverify_ctx {
   int32_t* st_committed;
   uint8_t* st_flags;
   cudaStream_t last_stream;
-  // optional timing events around the row-pass kernel
+  bool last_run_empty;
+  // optional timing events around the verify kernel
   int n_events;
   unsigned long long run_counter;
   cudaEvent_t ev_start[64];
@@ -81,28 +79,38 @@ static int check_handle(specverify_t h) {
   return SPECVERIFY_OK;
 }
 
-static int choose_nch(const specverify_ctx* h, int batch, int total_draft) {
-  const size_t row_bytes = (size_t)h->vocab * h->elem_bytes;
-  const long long rows_ub = (long long)batch + 2LL * total_draft;
-  long long nch = (long long)((row_bytes + kChunkBytes - 1) / kChunkBytes);
-  const long long want_items = 2LL * h->grid_rowpass;
-  if (rows_ub > 0 && rows_ub * nch < want_items) nch = (want_items + rows_ub - 1) / rows_ub;
-  const long long by_size = std::max<long long>(1, (long long)(row_bytes / kMinChunkBytes));
-  nch = std::min<long long>(nch, by_size);
-  nch = std::min<long long>(nch, h->max_nch);
-  return (int)std::max<long long>(nch, 1);
+static size_t ring_bytes() {
+  return sizeof(uint4) * sv::kStages * sv::kStageVecs * sv::kThreads;
+}
+
+// Vectors per thread per chunk (nper) and chunks per row (nch): 64 KB chunks,
+// smaller ones when the batch has too few rows to give every CTA two items.
+static void choose_chunks(const specverify_ctx* h, int batch, int total_draft, int* nper,
+                          int* nch) {
+  const long long nvec = std::max<long long>(1, (long long)h->vocab * h->elem_bytes / 16);
+  const long long rows = (long long)batch + 2LL * total_draft;
+  int np = kMaxNper;
+  while (np > sv::kStageVecs) {
+    const long long chunks = (nvec + (long long)np * sv::kThreads - 1) / ((long long)np * sv::kThreads);
+    if (rows * chunks >= 2LL * h->grid) break;
+    np /= 2;
+  }
+  // never more chunks than the scratch holds
+  while ((nvec + (long long)np * sv::kThreads - 1) / ((long long)np * sv::kThreads) > h->max_nch)
+    np *= 2;
+  *nper = np;
+  *nch = (int)((nvec + (long long)np * sv::kThreads - 1) / ((long long)np * sv::kThreads));
 }
 
 template <typename E>
 static int launch_round(specverify_ctx* h, const sv::Params& P, cudaStream_t s) {
-  sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
+  const size_t smem = ring_bytes() + sizeof(int) * ((size_t)P.batch + 1);
+  const int grid = (int)std::max<long long>(1, std::min<long long>(h->grid, P.n_items));
   const int slot = h->n_events > 0 ? (int)(h->run_counter % (unsigned long long)h->n_events) : -1;
   h->run_counter++;
   if (slot >= 0 && cudaEventRecord(h->ev_start[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-  sv::sv_rowpass<E><<<h->grid_rowpass, sv::kThreads, 0, s>>>(P);
+  sv::sv_verify<E><<<grid, sv::kThreads, smem, s>>>(P);
   if (slot >= 0 && cudaEventRecord(h->ev_stop[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-  const int grid2 = std::max(1, std::min(h->grid_resid, P.batch * P.nch));
-  sv::sv_residual<E><<<grid2, sv::kThreads, 0, s>>>(P);
   return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
 }
 
@@ -117,7 +125,10 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   if (batch < 0 || batch > h->max_batch) return SPECVERIFY_ERR_INVALID_ARG;
   if (total_draft < 0 || (long long)total_draft > (long long)batch * h->max_k)
     return SPECVERIFY_ERR_INVALID_ARG;
-  if (batch == 0) return SPECVERIFY_OK;
+  if (batch == 0) {
+    h->last_run_empty = true;
+    return SPECVERIFY_OK;
+  }
   if (!target_logits || !num_draft || !temperature || !accepted_len || !committed_tokens)
     return SPECVERIFY_ERR_INVALID_ARG;
   if (total_draft > 0 && (!draft_tokens || !accept_flags)) return SPECVERIFY_ERR_INVALID_ARG;
@@ -137,7 +148,9 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.total_draft = total_draft;
   P.max_k = h->max_k;
   P.vocab = h->vocab;
-  P.nch = choose_nch(h, batch, total_draft);
+  choose_chunks(h, batch, total_draft, &P.nper, &P.nch);
+  P.n_items = (batch + 2 * total_draft) * P.nch;
+  P.spin_limit = kSpinLimit;
   P.accepted_len = accepted_len;
   P.committed = committed_tokens;
   P.flags = accept_flags;
@@ -145,22 +158,21 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.q_y = q_y;
   P.u_dbg = u;
   P.req_status = req_status;
-  P.req = h->req;
-  P.rows = h->rows;
   P.part = h->part;
   P.rowres = h->rowres;
   P.row_cnt = h->row_cnt;
   P.req_cnt = h->req_cnt;
-  P.res_list = h->res_list;
+  P.res_slots = h->res_slots;
   P.part2 = h->part2;
   P.res_cnt = h->res_cnt;
-  P.counters = h->counters;
+  P.ctr = h->ctr;
 
   DeviceGuard guard(h->device);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   rc = h->dtype == SPECVERIFY_BF16 ? launch_round<sv::BF16>(h, P, s)
                                    : launch_round<sv::F32>(h, P, s);
   h->last_stream = s;
+  h->last_run_empty = false;
   return rc;
 }
 
@@ -171,7 +183,7 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   if (out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
   *out = nullptr;
   if (dtype != SPECVERIFY_F32 && dtype != SPECVERIFY_BF16) return SPECVERIFY_ERR_DTYPE;
-  if (max_batch < 1 || max_batch > (1 << 24) || max_k < 0 || max_k > 31 || vocab < 1 ||
+  if (max_batch < 1 || max_batch > sv::kMaxBatch || max_k < 0 || max_k > 31 || vocab < 1 ||
       vocab > (1 << 30))
     return SPECVERIFY_ERR_INVALID_ARG;
   if ((flags & ~(unsigned)SPECVERIFY_CREATE_HOST_STAGING) != 0u) return SPECVERIFY_ERR_INVALID_ARG;
@@ -195,34 +207,44 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   h->n_events = 0;
   h->run_counter = 0;
 
-  int occ1 = 0, occ2 = 0;
+  h->last_run_empty = true;
+  h->smem_bytes_max = ring_bytes() + sizeof(int) * ((size_t)max_batch + 1);
+  int occ = 0;
   bool ok = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) ==
             cudaSuccess;
   if (dtype == SPECVERIFY_BF16) {
-    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, sv::sv_rowpass<sv::BF16>,
-                                                             sv::kThreads, 0) == cudaSuccess;
-    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, sv::sv_residual<sv::BF16>,
-                                                             sv::kThreads, 0) == cudaSuccess;
+    ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::BF16>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)h->smem_bytes_max) == cudaSuccess;
+    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sv::sv_verify<sv::BF16>,
+                                                             sv::kThreads, h->smem_bytes_max) ==
+                   cudaSuccess;
   } else {
-    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, sv::sv_rowpass<sv::F32>,
-                                                             sv::kThreads, 0) == cudaSuccess;
-    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, sv::sv_residual<sv::F32>,
-                                                             sv::kThreads, 0) == cudaSuccess;
+    ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::F32>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)h->smem_bytes_max) == cudaSuccess;
+    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sv::sv_verify<sv::F32>,
+                                                             sv::kThreads, h->smem_bytes_max) ==
+                   cudaSuccess;
   }
-  if (!ok) {
+  if (!ok || occ < 1) {
     cudaGetLastError();
     delete h;
     return SPECVERIFY_ERR_CUDA;
   }
-  h->grid_rowpass = std::max(1, occ1) * h->num_sms;
-  h->grid_resid = std::max(1, occ2) * h->num_sms;
+  // persistent grid: every CTA resident at once
+  h->grid = occ * h->num_sms;
 
   h->max_rows = (size_t)max_batch * (2 * (size_t)max_k + 1);
   const size_t row_bytes = (size_t)vocab * h->elem_bytes;
-  size_t max_nch = std::min<size_t>(kMaxChunks, std::max<size_t>(1, row_bytes / kMinChunkBytes));
-  max_nch = std::min<size_t>(max_nch,
-                             std::max<size_t>(1, kPartialBudget / sizeof(sv::Partial) / h->max_rows));
-  h->max_nch = (int)max_nch;
+  const size_t nvec = std::max<size_t>(1, row_bytes / 16);
+  const size_t min_chv = (size_t)sv::kStageVecs * sv::kThreads;
+  size_t max_nch = (nvec + min_chv - 1) / min_chv;
+  max_nch = std::min<size_t>(max_nch, std::max<size_t>(
+                                          (nvec + (size_t)kMaxNper * sv::kThreads - 1) /
+                                              ((size_t)kMaxNper * sv::kThreads),
+                                          kPartialBudget / sizeof(sv::Partial) / h->max_rows));
+  h->max_nch = (int)std::max<size_t>(1, max_nch);
 
   // one scratch allocation, carved into aligned pieces
   size_t off = 0;
@@ -231,16 +253,14 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
     off = align_up(off + bytes, 256);
     return o;
   };
-  const size_t o_req = carve(sizeof(sv::ReqInfo) * max_batch);
-  const size_t o_rows = carve(sizeof(sv::RowInfo) * h->max_rows);
-  const size_t o_part = carve(sizeof(sv::Partial) * h->max_rows * max_nch);
+  const size_t o_part = carve(sizeof(sv::Partial) * h->max_rows * h->max_nch);
   const size_t o_rowres = carve(sizeof(sv::Partial) * h->max_rows);
   const size_t o_rowcnt = carve(sizeof(int) * h->max_rows);
   const size_t o_reqcnt = carve(sizeof(int) * max_batch);
-  const size_t o_reslist = carve(sizeof(int2) * max_batch);
-  const size_t o_part2 = carve(sizeof(sv::Partial2) * (size_t)max_batch * max_nch);
+  const size_t o_slots = carve(sizeof(unsigned long long) * max_batch);
+  const size_t o_part2 = carve(sizeof(sv::Partial) * (size_t)max_batch * h->max_nch);
   const size_t o_rescnt = carve(sizeof(int) * max_batch);
-  const size_t o_cnt = carve(sizeof(int) * sv::kCntCount);
+  const size_t o_ctr = carve(sizeof(int) * sv::kCntCount);
   h->scratch_bytes = off;
   if (cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -254,16 +274,14 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
     return SPECVERIFY_ERR_CUDA;
   }
   char* b = static_cast<char*>(h->scratch);
-  h->req = reinterpret_cast<sv::ReqInfo*>(b + o_req);
-  h->rows = reinterpret_cast<sv::RowInfo*>(b + o_rows);
   h->part = reinterpret_cast<sv::Partial*>(b + o_part);
   h->rowres = reinterpret_cast<sv::Partial*>(b + o_rowres);
   h->row_cnt = reinterpret_cast<int*>(b + o_rowcnt);
   h->req_cnt = reinterpret_cast<int*>(b + o_reqcnt);
-  h->res_list = reinterpret_cast<int2*>(b + o_reslist);
-  h->part2 = reinterpret_cast<sv::Partial2*>(b + o_part2);
+  h->res_slots = reinterpret_cast<unsigned long long*>(b + o_slots);
+  h->part2 = reinterpret_cast<sv::Partial*>(b + o_part2);
   h->res_cnt = reinterpret_cast<int*>(b + o_rescnt);
-  h->counters = reinterpret_cast<int*>(b + o_cnt);
+  h->ctr = reinterpret_cast<int*>(b + o_ctr);
 
   h->stage = nullptr;
   if (flags & SPECVERIFY_CREATE_HOST_STAGING) {
@@ -387,8 +405,12 @@ int specverify_status(specverify_t h, int32_t* status_out) {
   if (status_out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
   DeviceGuard guard(h->device);
   int32_t st = 0;
+  if (h->last_run_empty) {
+    *status_out = 0;
+    return SPECVERIFY_OK;
+  }
   if (cudaStreamSynchronize(h->last_stream) != cudaSuccess ||
-      cudaMemcpy(&st, h->counters + sv::kCntStatus, sizeof st, cudaMemcpyDeviceToHost) !=
+      cudaMemcpy(&st, h->ctr + sv::kCntLastStatus, sizeof st, cudaMemcpyDeviceToHost) !=
           cudaSuccess) {
     cudaGetLastError();
     return SPECVERIFY_ERR_CUDA;
@@ -413,7 +435,7 @@ int specverify_set_timing_events(specverify_t h, int n, void* const* start_event
   return SPECVERIFY_OK;
 }
 
-int specverify_launches_per_run(void) { return 3; }
+int specverify_launches_per_run(void) { return 1; }
 
 int specverify_destroy(specverify_t h) {
   int rc = check_handle(h);

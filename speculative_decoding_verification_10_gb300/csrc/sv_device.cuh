@@ -82,6 +82,43 @@ __device__ __forceinline__ float race_exponential(uint32_t w) {
   return -log1pf(-d);
 }
 
+// Upper bound of -log2(E) for the race exponential of word w, from integer
+// operations only, with a margin of 1e-3 over the computed -log2(E):
+//   w <  2^31:  U < 1/2, so E > ln 2 and -log2 E < 0.5288;
+//   w >= 2^31:  d = 1 - U = (~w + 1/2) 2^-32 > 2^-(1 + clz(~w)) and E > d,
+//               so -log2 E < 1 + clz(~w)   (clz(0) = 32 covers ~w = 0).
+// Because rounding is monotonic, fmaf(x, c, race_gain_bound(w)) is never
+// below the computed score fmaf(x, c, -log2 E): elements whose bound cannot
+// reach the best score so far can skip the exponential entirely.
+__device__ __forceinline__ float race_gain_bound(uint32_t w) {
+  return w < 0x80000000u ? 0.53f : (float)(1 + __clz(~w)) + 1.0e-3f;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Asynchronous global -> shared copies (cp.async, 16 bytes, L2 only).  Each
+// thread waits for its own copies with cp.async.wait_group, a hardware wait.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Loads.  Logit rows are streamed once: 16-byte non-coherent loads that skip L1.
 // ---------------------------------------------------------------------------

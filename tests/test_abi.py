@@ -35,6 +35,7 @@ def test_create_rejects_bad_arguments_before_touching_cuda(lib):
     assert lib.specverify_create(None, 0, 8, 3, 1024, 1) == _lib.ERR_INVALID_ARG
     assert lib.specverify_create(ctypes.byref(h), 0, 8, 3, 1024, 7) == _lib.ERR_DTYPE
     assert lib.specverify_create(ctypes.byref(h), 0, 0, 3, 1024, 1) == _lib.ERR_INVALID_ARG
+    assert lib.specverify_create(ctypes.byref(h), 0, 4097, 3, 1024, 1) == _lib.ERR_INVALID_ARG
     assert lib.specverify_create(ctypes.byref(h), 0, 8, 32, 1024, 1) == _lib.ERR_INVALID_ARG
     assert lib.specverify_create(ctypes.byref(h), 0, 8, 3, 0, 1) == _lib.ERR_INVALID_ARG
     assert lib.specverify_create_ex(ctypes.byref(h), 0, 8, 3, 1024, 1, 8) == _lib.ERR_INVALID_ARG
@@ -47,7 +48,7 @@ def test_calls_on_a_null_handle(lib):
     assert lib.specverify_destroy(None) == _lib.ERR_INVALID_ARG
     assert lib.specverify_run(None, None, None, None, None, None, 0, 1, 0,
                               None, None, None, None) == _lib.ERR_INVALID_ARG
-    assert lib.specverify_launches_per_run() == 3
+    assert lib.specverify_launches_per_run() == 1
 
 
 def test_no_device_reports_cuda_error(lib):
