@@ -109,7 +109,7 @@ static int launch_round(specverify_ctx* h, const sv::Params& P, cudaStream_t s) 
   const int slot = h->n_events > 0 ? (int)(h->run_counter % (unsigned long long)h->n_events) : -1;
   h->run_counter++;
   if (slot >= 0 && cudaEventRecord(h->ev_start[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-  sv::sv_verify<E><<<grid, sv::kThreads, smem, s>>>(P);
+  sv::sv_verify<E><<<grid, sv::kBlock, smem, s>>>(P);
   if (slot >= 0 && cudaEventRecord(h->ev_stop[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
 }
@@ -217,14 +217,14 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)h->smem_bytes_max) == cudaSuccess;
     ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sv::sv_verify<sv::BF16>,
-                                                             sv::kThreads, h->smem_bytes_max) ==
+                                                             sv::kBlock, h->smem_bytes_max) ==
                    cudaSuccess;
   } else {
     ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::F32>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)h->smem_bytes_max) == cudaSuccess;
     ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sv::sv_verify<sv::F32>,
-                                                             sv::kThreads, h->smem_bytes_max) ==
+                                                             sv::kBlock, h->smem_bytes_max) ==
                    cudaSuccess;
   }
   if (!ok || occ < 1) {
@@ -257,9 +257,10 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   const size_t o_rowres = carve(sizeof(sv::Partial) * h->max_rows);
   const size_t o_rowcnt = carve(sizeof(int) * h->max_rows);
   const size_t o_reqcnt = carve(sizeof(int) * max_batch);
-  const size_t o_slots = carve(sizeof(unsigned long long) * max_batch);
-  const size_t o_part2 = carve(sizeof(sv::Partial) * (size_t)max_batch * h->max_nch);
-  const size_t o_rescnt = carve(sizeof(int) * max_batch);
+  // job slots: one residual and at most one fallback job per request
+  const size_t o_slots = carve(sizeof(unsigned long long) * 2 * (size_t)max_batch);
+  const size_t o_part2 = carve(sizeof(sv::Partial) * 2 * (size_t)max_batch * h->max_nch);
+  const size_t o_rescnt = carve(sizeof(int) * 2 * (size_t)max_batch);
   const size_t o_ctr = carve(sizeof(int) * sv::kCntCount);
   h->scratch_bytes = off;
   if (cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess) {

@@ -90,8 +90,10 @@ __device__ __forceinline__ float race_exponential(uint32_t w) {
 // Because rounding is monotonic, fmaf(x, c, race_gain_bound(w)) is never
 // below the computed score fmaf(x, c, -log2 E): elements whose bound cannot
 // reach the best score so far can skip the exponential entirely.
+//   (For w < 2^31, ~w >= 2^31 gives clz = 0 and the bound 1.001, which is
+//   looser than 0.529 but still valid, so one branch-free formula serves.)
 __device__ __forceinline__ float race_gain_bound(uint32_t w) {
-  return w < 0x80000000u ? 0.53f : (float)(1 + __clz(~w)) + 1.0e-3f;
+  return (float)__clz(~w) + 1.001f;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -224,6 +226,67 @@ struct SoftmaxAcc {
     o.m = __shfl_xor_sync(0xffffffffu, m, lane_mask);
     o.s = __shfl_xor_sync(0xffffffffu, s, lane_mask);
     return o;
+  }
+};
+
+// Softmax normaliser with a lazy reference: m is fixed from the first finite
+// vector a thread sees, and only raised when a vector's terms overflow (a
+// term 2^(c*x - m) above 2^100).  Terms far below m underflow to 0, which is
+// harmless: the element that set m contributes 1 to s.  The sum is kept as a
+// float2 and updated with packed FMA/ADD (two lanes per instruction).
+struct LazySoftmax {
+  float m;
+  float2 s;
+  __device__ __forceinline__ void init() {
+    m = kNegInf;
+    s = make_float2(0.f, 0.f);
+  }
+  template <int N>
+  __device__ __forceinline__ float vmax(const float (&x)[N]) {
+    float mx = x[0];
+#pragma unroll
+    for (int e = 1; e < N; ++e) mx = fmaxf(mx, x[e]);
+    return mx;
+  }
+  // terms of one vector relative to the current m, summed in pairs
+  template <int N>
+  __device__ __forceinline__ float2 terms(const float (&x)[N], float c) const {
+    const float2 cc = make_float2(c, c), nm = make_float2(-m, -m);
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < N; e += 2) {
+      const float2 t = __ffma2_rn(make_float2(x[e], x[e + 1]), cc, nm);
+      acc = __fadd2_rn(acc, make_float2(fast_ex2(t.x), fast_ex2(t.y)));
+    }
+    return acc;
+  }
+  template <int N>
+  __device__ __forceinline__ void add(const float (&x)[N], float c) {
+    if (m == kNegInf) {
+      const float vm = vmax(x) * c;
+      if (vm == kNegInf) return;  // nothing finite yet (NaN falls through)
+      m = vm;
+    }
+    float2 t = terms(x, c);
+    if (!(t.x + t.y <= 0x1p100f)) {
+      // overflow (or NaN): raise m to this vector's maximum and redo it
+      const float vm = fmaxf(vmax(x) * c, m);
+      const float sc = fast_ex2(m - vm);
+      s = make_float2(s.x * sc, s.y * sc);
+      m = vm;
+      t = terms(x, c);
+    }
+    s = __fadd2_rn(s, t);
+  }
+  __device__ __forceinline__ void add1(float x, float c) {
+    float a[2] = {x, kNegInf};
+    add<2>(a, c);
+  }
+  __device__ __forceinline__ SoftmaxAcc result() const {
+    SoftmaxAcc r;
+    r.m = m;
+    r.s = s.x + s.y;
+    return r;
   }
 };
 

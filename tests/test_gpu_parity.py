@@ -266,8 +266,22 @@ def test_million_trials_distribution_and_bit_exactness():
     inp = dict(target=np.tile(tgt, (n, 1)), draft=np.tile(drf, (n, 1)),
                tokens=toks.reshape(-1).astype(np.int32), num_draft=np.full(n, k, np.int32),
                temperature=np.full(n, T, np.float32), max_k=k)
-    with _verifier(inp, "f32") as v:
-        g = parity.run_gpu(v, inp, 123, debug=False)
+    # one handle serves at most 4096 requests: verify in slices keyed by request
+    # id, which draws exactly what one large batch would
+    S = 4096
+    acc = np.empty(n, np.int32)
+    com = np.empty((n, k + 1), np.int32)
+    with Verifier(S, k, V, "f32") as v:
+        for a in range(0, n, S):
+            b = min(n, a + S)
+            part = dict(target=inp["target"][a * (k + 1):b * (k + 1)],
+                        draft=inp["draft"][a * k:b * k], tokens=inp["tokens"][a * k:b * k],
+                        num_draft=inp["num_draft"][a:b], temperature=inp["temperature"][a:b],
+                        request_ids=np.arange(a, b, dtype=np.int64), max_k=k)
+            gp = parity.run_gpu(v, part, 123, debug=False)
+            acc[a:b] = gp["accepted_len"]
+            com[a:b] = gp["committed"]
+    g = {"accepted_len": acc, "committed": com}
     o = parity.run_oracle(inp, 123)
     same = (g["committed"] == o["committed"]).all(1)
     # exact agreement except near-threshold draws
