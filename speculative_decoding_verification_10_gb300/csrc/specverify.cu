@@ -17,7 +17,7 @@ namespace {
 
 constexpr uint32_t kLiveMagic = 0x53564c56u;  // "SVLV"
 constexpr uint32_t kDeadMagic = 0x53564444u;  // "SVDD"
-constexpr int kMaxNper = 16;                   // 16-byte vectors per thread per chunk (64 KB of logits)
+constexpr int kMaxNper = 64;                   // 16-byte vectors per thread per chunk (224 KB of logits)
 constexpr size_t kPartialBudget = size_t(256) << 20;
 constexpr int kSpinLimit = 1 << 16;
 
@@ -83,23 +83,22 @@ static size_t ring_bytes() {
   return sizeof(uint4) * sv::kStages * sv::kStageVecs * sv::kThreads;
 }
 
-// Vectors per thread per chunk (nper) and chunks per row (nch): 64 KB chunks,
-// smaller ones when the batch has too few rows to give every CTA two items.
+// Vectors per thread per chunk (nper) and chunks per row (nch): the fewest
+// chunks of at most kMaxNper vectors per thread, balanced, and more (smaller)
+// chunks when the batch has too few rows to give every CTA two items.
 static void choose_chunks(const specverify_ctx* h, int batch, int total_draft, int* nper,
                           int* nch) {
   const long long nvec = std::max<long long>(1, (long long)h->vocab * h->elem_bytes / 16);
   const long long rows = (long long)batch + 2LL * total_draft;
-  int np = kMaxNper;
-  while (np > sv::kStageVecs) {
-    const long long chunks = (nvec + (long long)np * sv::kThreads - 1) / ((long long)np * sv::kThreads);
-    if (rows * chunks >= 2LL * h->grid) break;
-    np /= 2;
-  }
-  // never more chunks than the scratch holds
-  while ((nvec + (long long)np * sv::kThreads - 1) / ((long long)np * sv::kThreads) > h->max_nch)
-    np *= 2;
-  *nper = np;
-  *nch = (int)((nvec + (long long)np * sv::kThreads - 1) / ((long long)np * sv::kThreads));
+  const long long step = (long long)sv::kStageVecs * sv::kThreads;  // vectors per stage
+  long long n = (nvec + (long long)kMaxNper * sv::kThreads - 1) / ((long long)kMaxNper * sv::kThreads);
+  const long long n_max = std::max<long long>(1, std::min<long long>(h->max_nch, (nvec + step - 1) / step));
+  while (n < n_max && rows * n < 2LL * h->grid) ++n;
+  n = std::min(n, n_max);
+  // balanced chunk length, rounded up to whole stages
+  const long long chv = ((nvec + n - 1) / n + step - 1) / step * step;
+  *nper = (int)(chv / sv::kThreads);
+  *nch = (int)((nvec + chv - 1) / chv);
 }
 
 template <typename E>
@@ -150,6 +149,10 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.vocab = h->vocab;
   choose_chunks(h, batch, total_draft, &P.nper, &P.nch);
   P.n_items = (batch + 2 * total_draft) * P.nch;
+  {
+    const int spi = P.nper / sv::kStageVecs;
+    P.fill = std::min(sv::kQueue - 2, (sv::kStages - 1 + spi - 1) / spi + 1);
+  }
   P.spin_limit = kSpinLimit;
   P.accepted_len = accepted_len;
   P.committed = committed_tokens;
@@ -214,12 +217,18 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
             cudaSuccess;
   if (dtype == SPECVERIFY_BF16) {
     ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::BF16>,
+                                    cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+    ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::BF16>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)h->smem_bytes_max) == cudaSuccess;
     ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sv::sv_verify<sv::BF16>,
                                                              sv::kBlock, h->smem_bytes_max) ==
                    cudaSuccess;
   } else {
+    ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::F32>,
+                                    cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared) == cudaSuccess;
     ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::F32>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)h->smem_bytes_max) == cudaSuccess;

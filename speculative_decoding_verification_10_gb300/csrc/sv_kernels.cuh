@@ -18,7 +18,7 @@
 // [p_j - q_j]_+ over rows t_j and d_j, in nch chunks any CTA may claim.  Jobs
 // are claimed ahead of new items, while those two rows are still in L2.
 //
-// CTA layout: 8 compute warps and 1 control warp, one __syncthreads per work
+// CTA layout: 7 compute warps and 1 control warp, one __syncthreads per work
 // unit.  Compute warps stream the unit's bytes and leave one partial per warp
 // in shared memory.  During the next unit the control warp combines them and
 // does all latency-bound global work: partial stores, completion counters,
@@ -40,13 +40,12 @@
 
 namespace sv {
 
-constexpr int kComputeWarps = 8;
+constexpr int kComputeWarps = 7;
 constexpr int kThreads = kComputeWarps * 32;   // compute threads
 constexpr int kBlock = kThreads + 32;          // + the control warp
 constexpr int kStages = 8;
 constexpr int kStageVecs = 2;
 constexpr int kQueue = 16;                     // item queue entries (power of 2)
-constexpr int kFill = kStages + 1;             // items kept claimed ahead
 constexpr int kMaxBatch = 4096;                // requests per launch
 constexpr int kResUnroll = 2;
 
@@ -91,6 +90,7 @@ struct Params {
   int nch;      // chunks per row
   int nper;     // 16-byte vectors per thread per chunk (multiple of kStageVecs)
   int n_items;  // (batch + 2 total_draft) * nch
+  int fill;     // items kept claimed ahead: enough to cover kStages-1 stages, + 1
   int spin_limit;
   int32_t* accepted_len;
   int32_t* committed;
@@ -242,8 +242,9 @@ struct LoadCursor {
   bool active;
 
   // s_qend: items the control warp has queued, or -1 - n once the supply is
-  // exhausted at n items.  The control warp keeps it at least kStages items
-  // ahead of the unit being processed, so an entry below it is always written.
+  // exhausted at n items.  The control warp keeps P.fill items queued beyond
+  // the unit being processed, which covers the kStages-1 stages the cursor
+  // runs ahead, so every entry the cursor opens is already written.
   __device__ __forceinline__ void open(const QItem* queue, const int* s_qend) {
     const int qe = *reinterpret_cast<const volatile int*>(s_qend);
     __threadfence_block();
@@ -674,13 +675,13 @@ struct Ctrl {
   int spins;
 };
 
-// Keep kFill items queued ahead of q_used (lane 0 claims and decodes).
+// Keep P.fill items queued ahead of q_used (lane 0 claims and decodes).
 template <typename E>
 __device__ __forceinline__ void fill_queue(const Params& P, const int* s_doff, QItem* queue,
                                            int* s_qend, Ctrl& cs) {
   const int lane = threadIdx.x & 31;
-  while (!cs.exhausted && cs.q_head < cs.q_used + kFill) {
-    const int need = cs.q_used + kFill - cs.q_head;
+  while (!cs.exhausted && cs.q_head < cs.q_used + P.fill) {
+    const int need = cs.q_used + P.fill - cs.q_head;
     int base = 0;
     if (lane == 0) base = atomicAdd(P.ctr + kCntItems, need);
     base = __shfl_sync(0xffffffffu, base, 0);
@@ -877,7 +878,7 @@ __device__ void complete_job(const Params& P, const JobRef& jb, bool fallback, c
 // The kernel.
 // ---------------------------------------------------------------------------
 template <typename E>
-__global__ void __maxnreg__(112) sv_verify(Params P) {
+__global__ void __maxnreg__(128) sv_verify(Params P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* ring = reinterpret_cast<uint4*>(smem_raw);
   int* s_doff = reinterpret_cast<int*>(smem_raw + sizeof(uint4) * kStages * kStageVecs * kThreads);
