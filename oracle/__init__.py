@@ -80,12 +80,15 @@ def _load():
         lib.orc_argmax.restype = ctypes.c_int
         lib.orc_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, P, P, P, P, P, P, ctypes.c_uint64,
-                                   P, P, P, P, P, P, P, P, P, P, P, P]
+                                   P, P, P, P, P, P, P, P, P, P, P]
         lib.orc_verify.restype = ctypes.c_uint32
         lib.orc_race_keys.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_float,
                                       ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int,
-                                      ctypes.c_int, P]
+                                      ctypes.c_int, P, P]
         lib.orc_race_keys.restype = ctypes.c_int
+        lib.orc_race_weights.argtypes = [P, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
+                                         ctypes.c_int, P, P]
+        lib.orc_race_weights.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -175,8 +178,7 @@ def verify(target, draft, tokens, num_draft, temperature, seed, max_k,
         "accept_margin": np.zeros(total_draft, np.float64),
         "race_kind": np.zeros(batch, np.int32),
         "race_pos": np.zeros(batch, np.int32),
-        "race_best": np.zeros(batch, np.float64),
-        "race_second": np.zeros(batch, np.float64),
+        "race_margin": np.zeros(batch, np.float64),
         "req_status": np.zeros(batch, np.int32),
     }
     status = lib.orc_verify(
@@ -185,16 +187,20 @@ def verify(target, draft, tokens, num_draft, temperature, seed, max_k,
         _ptr(temperature), _ptr(rid), int(seed) & (2**64 - 1),
         _ptr(out["accepted_len"]), _ptr(out["committed"]), _ptr(out["flags"]),
         _ptr(out["p_y"]), _ptr(out["q_y"]), _ptr(out["u"]), _ptr(out["accept_margin"]),
-        _ptr(out["race_kind"]), _ptr(out["race_pos"]), _ptr(out["race_best"]),
-        _ptr(out["race_second"]), _ptr(out["req_status"]))
+        _ptr(out["race_kind"]), _ptr(out["race_pos"]), _ptr(out["race_margin"]),
+        _ptr(out["req_status"]))
     out["status"] = int(status)
     return out
 
 
-def race_keys(target_row, draft_row, temperature, seed, request, position, kind):
-    """Keys E_v / w_v of one request's correction/bonus race for every v.
+RACE_BLOCK = 128
 
-    Returns (winner, keys[V]); keys are +inf where the weight is not positive.
+
+def race_keys(target_row, draft_row, temperature, seed, request, position, kind):
+    """Keys of one request's correction/bonus draw.
+
+    Returns (winner, block_keys[ceil(V/128)], elem_keys[V]); keys are +inf where
+    the mass or weight is not positive.
     """
     lib = _load()
     t, dt = _logits(np.asarray(target_row).reshape(1, -1))
@@ -202,8 +208,22 @@ def race_keys(target_row, draft_row, temperature, seed, request, position, kind)
     if draft_row is not None:
         d, _ = _logits(np.asarray(draft_row).reshape(1, -1))
     vocab = t.shape[1]
-    keys = np.zeros(vocab, dtype=np.float64)
+    bkeys = np.zeros((vocab + RACE_BLOCK - 1) // RACE_BLOCK, dtype=np.float64)
+    ekeys = np.zeros(vocab, dtype=np.float64)
     winner = lib.orc_race_keys(dt, vocab, _ptr(t), _ptr(d), float(temperature),
                                int(seed) & (2**64 - 1), int(request) & (2**64 - 1),
-                               int(position), int(kind), _ptr(keys))
-    return int(winner), keys
+                               int(position), int(kind), _ptr(bkeys), _ptr(ekeys))
+    return int(winner), bkeys, ekeys
+
+
+def race_weights(weights, seed, request, position):
+    """The two-level race over explicit float64 weights: (winner, block_keys, elem_keys)."""
+    lib = _load()
+    w = np.ascontiguousarray(weights, dtype=np.float64)
+    vocab = len(w)
+    bkeys = np.zeros((vocab + RACE_BLOCK - 1) // RACE_BLOCK, dtype=np.float64)
+    ekeys = np.zeros(vocab, dtype=np.float64)
+    winner = lib.orc_race_weights(_ptr(w), vocab, int(seed) & (2**64 - 1),
+                                  int(request) & (2**64 - 1), int(position), _ptr(bkeys),
+                                  _ptr(ekeys))
+    return int(winner), bkeys, ekeys

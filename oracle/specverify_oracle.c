@@ -32,12 +32,15 @@
  *   (key = seed low word, seed high word) with the counter
  *       (floor(v/4), position, request low word, stream | request high << 8)
  *   and output word v mod 4.  Stream 0 gives the acceptance uniform of a
- *   position (v = 0), stream 1 the race exponentials of the correction or
- *   bonus draw.
+ *   position (v = 0); streams 1 and 2 the exponentials of the correction or
+ *   bonus draw (stream 2 indexed by vocab block, stream 1 by vocab id).
  *     u      = (w >> 8) * 2^-24                 in [0, 1)       (exact in fp32)
  *     E      = -ln((w + 1/2) * 2^-32)           in (1.2e-10, 22.9)
- *   A categorical draw from weights w_v >= 0 is the exponential race
- *   argmin_{v: w_v > 0} E_v / w_v with the lowest index winning ties.
+ *   A categorical draw from weights w_v >= 0 is a two-level exponential race
+ *   over fixed blocks of 128 consecutive vocab ids, lowest index on ties:
+ *     block  b* = argmin_{b: W_b > 0} E2_b / W_b,   W_b = sum_{v in block b} w_v,
+ *     token  v* = argmin_{v in b*, w_v > 0} E1_v / w_v.
+ *   P(v* = v) = (W_b / W) (w_v / W_b) = w_v / W, so it draws exactly from w.
  */
 #include <math.h>
 #include <stddef.h>
@@ -182,34 +185,67 @@ int orc_argmax(const void *base, int dtype, size_t row, int vocab)
     return best;
 }
 
-/* Exponential race over weights w (length V): argmin_{w_v > 0} E_v / w_v,  */
-/* lowest index on ties.  keys_out (nullable) receives every key (+inf where */
-/* w_v <= 0).  Returns the winner, or -1 when no weight is positive.         */
+#define ORC_RACE_BLOCK 128
+
+/* Two-level exponential race over weights w (length V), blocks of
+ * ORC_RACE_BLOCK ids: the block race picks b* = argmin E2_b / W_b over blocks
+ * with positive mass W_b, then the element race picks argmin E1_v / w_v over
+ * the positive weights of b* (lowest index on ties at both levels).
+ * block_keys_out [ceil(V/128)] and elem_keys_out [V] (nullable) receive every
+ * key (+inf where the mass or weight is not positive).  *margin (nullable)
+ * gets min(second/best - 1) over the two decisive comparisons.  Returns the
+ * winner, or -1 when no weight is positive. */
 static int race(const double *w, int vocab, uint64_t seed, uint64_t request, uint32_t position,
-                double *keys_out, double *best_key, double *second_key)
+                double *block_keys_out, double *elem_keys_out, double *margin)
 {
-    int winner = -1;
-    double best = INFINITY, second = INFINITY;
-    for (int v = 0; v < vocab; ++v) {
+    const int nblocks = (vocab + ORC_RACE_BLOCK - 1) / ORC_RACE_BLOCK;
+    int best_b = -1;
+    double b1 = INFINITY, b2 = INFINITY;
+    for (int b = 0; b < nblocks; ++b) {
+        double mass = 0.0;
+        for (int v = b * ORC_RACE_BLOCK; v < vocab && v < (b + 1) * ORC_RACE_BLOCK; ++v)
+            if (w[v] > 0.0)
+                mass += w[v];
         double key = INFINITY;
-        if (w[v] > 0.0) {
-            double e = orc_exponential(orc_random_word(seed, 1u, request, position, (uint32_t)v));
-            key = e / w[v];
-        }
-        if (keys_out)
-            keys_out[v] = key;
-        if (key < best) {
-            second = best;
-            best = key;
-            winner = v;
-        } else if (key < second) {
-            second = key;
+        if (mass > 0.0)
+            key = orc_exponential(orc_random_word(seed, 2u, request, position, (uint32_t)b)) / mass;
+        if (block_keys_out)
+            block_keys_out[b] = key;
+        if (key < b1) {
+            b2 = b1;
+            b1 = key;
+            best_b = b;
+        } else if (key < b2) {
+            b2 = key;
         }
     }
-    if (best_key)
-        *best_key = best;
-    if (second_key)
-        *second_key = second;
+    if (elem_keys_out)
+        for (int v = 0; v < vocab; ++v)
+            elem_keys_out[v] = w[v] > 0.0
+                ? orc_exponential(orc_random_word(seed, 1u, request, position, (uint32_t)v)) / w[v]
+                : INFINITY;
+    if (best_b < 0) {
+        if (margin) *margin = INFINITY;
+        return -1;
+    }
+    int winner = -1;
+    double e1 = INFINITY, e2 = INFINITY;
+    for (int v = best_b * ORC_RACE_BLOCK; v < vocab && v < (best_b + 1) * ORC_RACE_BLOCK; ++v) {
+        if (!(w[v] > 0.0))
+            continue;
+        double key = orc_exponential(orc_random_word(seed, 1u, request, position, (uint32_t)v)) / w[v];
+        if (key < e1) {
+            e2 = e1;
+            e1 = key;
+            winner = v;
+        } else if (key < e2) {
+            e2 = key;
+        }
+    }
+    if (margin) {
+        double m1 = b2 / b1 - 1.0, m2 = e2 / e1 - 1.0;
+        *margin = m1 < m2 ? m1 : m2;
+    }
     return winner;
 }
 
@@ -237,7 +273,8 @@ static int temperature_ok(float t)
  *
  * Debug outputs (all nullable): p_y/q_y/u per draft position of stochastic
  * requests (NaN for greedy ones); accept_margin = (p - u q) / max(p, u q);
- * race_kind/race_pos/race_best/race_second per request; req_status per request.
+ * race_kind/race_pos/race_margin per request (race_margin: the relative gap
+ * of the draw's decisive comparisons); req_status per request.
  * Returns the OR of all status bits.
  */
 uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
@@ -246,8 +283,8 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
                     const float *temperature, const int64_t *request_ids, uint64_t seed,
                     int32_t *accepted_len, int32_t *committed, uint8_t *accept_flags,
                     double *p_y, double *q_y, double *u_out, double *accept_margin,
-                    int32_t *race_kind, int32_t *race_pos, double *race_best,
-                    double *race_second, int32_t *req_status)
+                    int32_t *race_kind, int32_t *race_pos, double *race_margin,
+                    int32_t *req_status)
 {
     const int width = max_k + 1;
     uint32_t status = 0;
@@ -258,8 +295,7 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
             committed[(size_t)r * width + i] = -1;
         if (race_kind) race_kind[r] = ORC_RACE_NONE;
         if (race_pos) race_pos[r] = -1;
-        if (race_best) race_best[r] = NAN;
-        if (race_second) race_second[r] = NAN;
+        if (race_margin) race_margin[r] = NAN;
         if (req_status) req_status[r] = 0;
     }
     for (int d = 0; d < total_draft; ++d) {
@@ -360,11 +396,11 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
                         rejected = 1;
                 }
             }
-            double best = NAN, second = NAN;
+            double gap = NAN;
             if (accepted == k) {
                 /* Every draft survived: one more token from the target p_k. */
                 orc_softmax(target_logits, dtype, tgt_off + k, vocab, temp, p);
-                token = race(p, vocab, seed, req, (uint32_t)k, NULL, &best, &second);
+                token = race(p, vocab, seed, req, (uint32_t)k, NULL, NULL, &gap);
                 if (race_kind) race_kind[r] = ORC_RACE_BONUS;
             } else {
                 /* First rejection at j = A: draw from [p_j - q_j]_+, normalised */
@@ -374,18 +410,17 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
                 orc_softmax(draft_logits, dtype, drf_off + j, vocab, temp, q);
                 for (int v = 0; v < vocab; ++v)
                     w[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
-                token = race(w, vocab, seed, req, (uint32_t)j, NULL, &best, &second);
+                token = race(w, vocab, seed, req, (uint32_t)j, NULL, NULL, &gap);
                 if (token >= 0) {
                     if (race_kind) race_kind[r] = ORC_RACE_RESIDUAL;
                 } else {
                     /* p <= q everywhere means p == q: draw from p instead. */
-                    token = race(p, vocab, seed, req, (uint32_t)j, NULL, &best, &second);
+                    token = race(p, vocab, seed, req, (uint32_t)j, NULL, NULL, &gap);
                     if (race_kind) race_kind[r] = ORC_RACE_FALLBACK;
                 }
             }
             if (race_pos) race_pos[r] = accepted;
-            if (race_best) race_best[r] = best;
-            if (race_second) race_second[r] = second;
+            if (race_margin) race_margin[r] = gap;
         }
 
         accepted_len[r] = accepted;
@@ -405,15 +440,15 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
 }
 
 /*
- * Race keys of one request's correction/bonus draw, for every vocab id, so a
- * test can look up the key of any token.  kind: ORC_RACE_BONUS or
- * ORC_RACE_FALLBACK (weights p from target_row), ORC_RACE_RESIDUAL (weights
- * [p - q]_+ from target_row and draft_row).  Rows are single rows [V].
- * Returns the winner.
+ * Keys of one request's correction/bonus draw, so a test can check any token:
+ * block_keys [ceil(V/128)] and elem_keys [V] as in race().  kind:
+ * ORC_RACE_BONUS or ORC_RACE_FALLBACK (weights p from target_row),
+ * ORC_RACE_RESIDUAL (weights [p - q]_+ from target_row and draft_row).  Rows
+ * are single rows [V].  Returns the winner.
  */
 int orc_race_keys(int dtype, int vocab, const void *target_row, const void *draft_row,
                   float temperature, uint64_t seed, uint64_t request, int position, int kind,
-                  double *keys_out)
+                  double *block_keys, double *elem_keys)
 {
     double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
     double *q = (double *)malloc(sizeof(double) * (size_t)vocab);
@@ -424,12 +459,19 @@ int orc_race_keys(int dtype, int vocab, const void *target_row, const void *draf
         orc_softmax(draft_row, dtype, 0, vocab, (double)temperature, q);
         for (int v = 0; v < vocab; ++v)
             w[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
-        winner = race(w, vocab, seed, request, (uint32_t)position, keys_out, NULL, NULL);
+        winner = race(w, vocab, seed, request, (uint32_t)position, block_keys, elem_keys, NULL);
     } else {
-        winner = race(p, vocab, seed, request, (uint32_t)position, keys_out, NULL, NULL);
+        winner = race(p, vocab, seed, request, (uint32_t)position, block_keys, elem_keys, NULL);
     }
     free(p);
     free(q);
     free(w);
     return winner;
+}
+
+/* The race over explicit weights (for tests): returns the winner. */
+int orc_race_weights(const double *w, int vocab, uint64_t seed, uint64_t request, int position,
+                     double *block_keys, double *elem_keys)
+{
+    return race(w, vocab, seed, request, (uint32_t)position, block_keys, elem_keys, NULL);
 }

@@ -159,3 +159,36 @@ def test_planted_mistakes_fail_the_pins():
     dec = out["accepted_len"][:2000] == 1
     assert (dec == (u * q0[y[:2000]] < p0[y[:2000]])).all()
     assert not (dec == (u * p0[y[:2000]] < q0[y[:2000]])).all()
+
+
+def test_two_level_race_draws_from_the_weights():
+    """The block race then the element race draw token v with probability w_v / W:
+    checked over blocks with zero mass, a partial last block and zero weights."""
+    rng = np.random.default_rng(31)
+    V = 700                                       # blocks of 128: 5 full + one of 60 ids
+    w = rng.gamma(0.7, size=V)
+    w[128:256] = 0.0                              # a block without mass
+    w[rng.choice(V, 50, replace=False)] = 0.0     # scattered zero weights
+    n = 40_000
+    draws = np.array([oracle.race_weights(w, seed=3, request=r, position=2)[0] for r in range(n)])
+    assert not np.isin(draws, np.flatnonzero(w == 0)).any()
+    assert _chi2_pvalue(np.bincount(draws, minlength=V), w / w.sum()) > 1e-3
+    # the block of the draw follows the block masses
+    mass = np.add.reduceat(w, np.arange(0, V, 128))
+    assert _chi2_pvalue(np.bincount(draws // 128, minlength=len(mass)), mass / mass.sum()) > 1e-3
+
+
+def test_two_level_race_keys_are_consistent():
+    """The winner is the lowest key of the winning block, and that block has the
+    lowest block key; the keys use E / w."""
+    rng = np.random.default_rng(5)
+    w = rng.gamma(0.5, size=1000)
+    winner, bk, ek = oracle.race_weights(w, seed=9, request=77, position=0)
+    b = int(np.argmin(bk))
+    assert winner // 128 == b
+    assert winner == b * 128 + int(np.argmin(ek[b * 128:(b + 1) * 128]))
+    word = oracle.random_word(9, 2, 77, 0, b)
+    assert bk[b] == pytest.approx(oracle.exponential(word) / w[b * 128:(b + 1) * 128].sum(),
+                                  rel=1e-12)
+    word = oracle.random_word(9, 1, 77, 0, winner)
+    assert ek[winner] == pytest.approx(oracle.exponential(word) / w[winner], rel=1e-15)
