@@ -307,6 +307,13 @@ struct BestAcc {
       idx = i;
     }
   }
+  // the full order (value, then lower index): for callers without index order
+  __device__ __forceinline__ void take_cmp(float val, int i) {
+    if (better(val, i, v, idx)) {
+      v = val;
+      idx = i;
+    }
+  }
   __device__ static __forceinline__ bool better(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && (uint32_t)ia < (uint32_t)ib);
   }

@@ -51,8 +51,7 @@ constexpr int kResUnroll = 2;
 
 enum RowKind : int { kSkip = -1, kSoftmax = 0, kArgmax = 1, kRace = 2 };
 enum ReqMode : int { kBadTemp = 0, kGreedy = 1, kSampling = 2 };
-enum UnitType : int { kUnitEnd = 0, kUnitIdle = 1, kUnitItem = 2, kUnitResidual = 3,
-                      kUnitFallback = 4 };
+enum UnitType : int { kUnitEnd = 0, kUnitIdle = 1, kUnitItem = 2, kUnitResidual = 3 };
 
 // Status bits (equal to the SPECVERIFY_STATUS_* values of the header).
 constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite = 8u,
@@ -165,7 +164,7 @@ struct __align__(16) Job {
   const char* trow;
   const char* drow;
   int slot, r, j, ch;
-  float c, mp, inv_sp, mq, inv_sq, kbound;
+  float c, mp, inv_sp, mq, inv_sq;
   uint32_t req_lo, req_hi;
 };
 
@@ -173,7 +172,7 @@ struct __align__(16) Unit {
   int type;
   int qidx;   // kUnitItem: queue entry
   int pad[2];
-  Job job;    // kUnitResidual / kUnitFallback
+  Job job;    // kUnitResidual
 };
 
 template <typename E>
@@ -303,37 +302,188 @@ __device__ __forceinline__ void consume_item(const Params& P, const QItem* queue
   }
 }
 
-// Calls f(e, word) for the race words (stream 1) of elements e0 .. e0+N-1,
-// where e0 % 4 == OFF; each Philox block is made just before its first use so
-// that at most one block is live.
-template <int N, int OFF, typename F>
-__device__ __forceinline__ void for_each_race_word(int e0, uint32_t pos, uint32_t req_lo,
-                                                   uint32_t req_hi, PhiloxKey key, F&& f) {
-  const uint32_t b0 = (uint32_t)e0 >> 2;
-  uint4 blk = philox4x32_10(make_uint4(b0, pos, req_lo, 1u | (req_hi << 8)), key);
+// ---------------------------------------------------------------------------
+// Two-level exponential race: blocks of kRaceBlock vocab ids.  The block race
+// picks argmax_b log2 W_b - log2 E2_b over blocks with mass W_b > 0 (Philox
+// stream 2, indexed by block); the element race inside the winning block picks
+// argmax_v log2 w_v - log2 E1_v (stream 1, indexed by vocab id).  Lowest index
+// on ties at both levels.
+// ---------------------------------------------------------------------------
+constexpr int kRaceBlock = 128;
+
+__device__ __forceinline__ uint32_t race_word(uint32_t stream, int idx, uint32_t pos,
+                                              RequestKey rk, PhiloxKey key) {
+  const uint4 r = philox4x32_10(make_uint4((uint32_t)idx >> 2, pos, rk.lo, stream | (rk.hi << 8)), key);
+  return word_of(r, idx & 3);
+}
+
+// -log2 E for a race word (the additive "gain" of an element or block).
+__device__ __forceinline__ float race_gain(uint32_t w) { return -fast_lg2(race_exponential(w)); }
+
+template <int kLanes>
+__device__ __forceinline__ float group_max(float v) {
 #pragma unroll
-  for (int e = 0; e < N; ++e) {
-    if (e > 0 && ((OFF + e) & 3) == 0)
-      blk = philox4x32_10(make_uint4(b0 + ((OFF + e) >> 2), pos, req_lo, 1u | (req_hi << 8)), key);
-    f(e, word_of(blk, (OFF + e) & 3));
-  }
+  for (int off = kLanes / 2; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+template <int kLanes>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
 }
 
-__device__ __forceinline__ uint32_t race_word1(int e, uint32_t pos, uint32_t req_lo,
-                                               uint32_t req_hi, PhiloxKey key) {
-  const uint4 r = philox4x32_10(make_uint4((uint32_t)e >> 2, pos, req_lo, 1u | (req_hi << 8)), key);
-  return word_of(r, e & 3);
+// Block gains of a warp's vector groups, made 32 groups at a time: lane L
+// holds the gains of the kBlocksPerGroup blocks of group g0 + L.  A vector
+// group is the warp's 32 consecutive vectors (32 * kVec ids, block aligned).
+template <typename E>
+struct GroupGains {
+  static constexpr int kBlocksPerGroup = 32 * E::kVec / kRaceBlock;   // 2 (bf16) or 1 (fp32)
+  static constexpr int kLanesPerBlock = kRaceBlock / E::kVec;          // 16 or 32
+  float lo, hi;
+  // first element of group g of warp w, for a chunk starting at vector vbeg
+  __device__ static __forceinline__ int group_elem(int vbeg, int g, int w) {
+    return (vbeg + g * kThreads + w * 32) * E::kVec;
+  }
+  __device__ __forceinline__ void make(int vbeg, int g0, int w, uint32_t pos, RequestKey rk,
+                                       PhiloxKey key) {
+    const int lane = threadIdx.x & 31;
+    const int b = group_elem(vbeg, g0 + lane, w) / kRaceBlock;
+    const uint4 r = philox4x32_10(make_uint4((uint32_t)b >> 2, pos, rk.lo, 2u | (rk.hi << 8)), key);
+    lo = race_gain(word_of(r, b & 3));
+    hi = kBlocksPerGroup > 1 ? race_gain(word_of(r, (b & 3) + 1)) : lo;  // b is even here
+  }
+  // the gain of this lane's block in group g (all lanes call it)
+  __device__ __forceinline__ float get(int g) const {
+    const int src = g & 31;
+    const float a = __shfl_sync(0xffffffffu, lo, src);
+    const float c = __shfl_sync(0xffffffffu, hi, src);
+    return ((threadIdx.x & 31) / kLanesPerBlock) ? c : a;
+  }
+};
+
+// Bonus race over one vector group: block weight W_b = sum 2^(c x_v) (kept as
+// log2: block max + log2 of the rescaled sum), score log2 W_b + gain.
+template <typename E>
+__device__ __forceinline__ void group_bonus(BestAcc& acc, const float (&x)[E::kVec], int e_lane,
+                                            float c, float gain) {
+  constexpr int kL = GroupGains<E>::kLanesPerBlock;
+  float mx = x[0];
+#pragma unroll
+  for (int e = 1; e < E::kVec; ++e) mx = fmaxf(mx, x[e]);
+  const float m = group_max<kL>(mx) * c;
+  float s = 0.f;
+  if (m > kNegInf) {
+    const float2 cc = make_float2(c, c), nm = make_float2(-m, -m);
+    float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E::kVec; e += 2) {
+      const float2 t = __ffma2_rn(make_float2(x[e], x[e + 1]), cc, nm);
+      a2 = __fadd2_rn(a2, make_float2(fast_ex2(t.x), fast_ex2(t.y)));
+    }
+    s = a2.x + a2.y;
+  } else if (m != m) {
+    s = m;  // a block of NaNs
+  }
+  s = group_sum<kL>(s);
+  acc.nan |= (s != s);
+  if (s > 0.f) acc.take_cmp(m + fast_lg2(s) + gain, e_lane / kRaceBlock);
 }
 
-// Bonus/fallback race candidate: the integer bound decides whether the exact
-// exponential is needed; `thr` is the best exact score the warp has seen.
-__device__ __forceinline__ void race_take(BestAcc& acc, float thr, float x, float c, uint32_t w,
-                                          int e) {
-  acc.nan |= (x != x);
-  if (fmaf(x, c, race_gain_bound(w)) >= thr) {
-    const float s = fmaf(x, c, -fast_lg2(race_exponential(w)));
-    acc.take(s, e);
+// Residual race over one vector group: W_b = sum max(p_v - q_v, 0).
+struct ResidualRow {
+  float c, mp, inv_sp, mq, inv_sq;
+};
+
+template <typename E>
+__device__ __forceinline__ void group_residual(BestAcc& acc, const float (&x)[E::kVec],
+                                               const float (&z)[E::kVec], int e_lane,
+                                               const ResidualRow& rr, float gain) {
+  constexpr int kL = GroupGains<E>::kLanesPerBlock;
+  const float2 cc = make_float2(rr.c, rr.c), nm = make_float2(-rr.mp, -rr.mq);
+  const float2 inv = make_float2(rr.inv_sp, rr.inv_sq);
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < E::kVec; ++e) {
+    const float2 t = __ffma2_rn(make_float2(x[e], z[e]), cc, nm);
+    const float2 pq = __fmul2_rn(make_float2(fast_ex2(t.x), fast_ex2(t.y)), inv);
+    s += fmaxf(pq.x - pq.y, 0.f);
   }
+  s = group_sum<kL>(s);
+  if (s > 0.f) acc.take_cmp(fast_lg2(s) + gain, e_lane / kRaceBlock);
+}
+
+// Element race inside block b (one warp, lane l takes ids 128 b + 4 l .. +3):
+// bonus/fallback weights 2^(c x_v) (kResid false) or residual [p - q]_+.
+template <typename E, bool kResid>
+__device__ __forceinline__ int inner_race(const Params& P, const char* trow, const char* drow,
+                                          int b, const ResidualRow& rr, uint32_t pos,
+                                          RequestKey rk) {
+  const int lane = threadIdx.x & 31;
+  const int v0 = b * kRaceBlock + 4 * lane;
+  const uint4 r = philox4x32_10(make_uint4((uint32_t)v0 >> 2, pos, rk.lo, 1u | (rk.hi << 8)), P.key);
+  BestAcc acc;
+  acc.init();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int v = v0 + i;
+    if (v < P.vocab) {
+      const float x = E::load1(trow, v);
+      const float g = race_gain(word_of(r, i));
+      if (kResid) {
+        const float p = fast_ex2(fmaf(x, rr.c, -rr.mp)) * rr.inv_sp;
+        const float q = fast_ex2(fmaf(E::load1(drow, v), rr.c, -rr.mq)) * rr.inv_sq;
+        const float w = p - q;
+        if (w > 0.f) acc.take(fast_lg2(w) + g, v);
+      } else {
+        acc.take(fmaf(x, rr.c, g), v);
+      }
+    }
+  }
+  acc = warp_reduce(acc);
+  return acc.idx;
+}
+
+// The whole two-level race over one row by one warp, with plain loads (rows
+// that are not 16-byte aligned, and the rare fallback).  Weights as in
+// inner_race.  Reports NaN / +inf in the row through acc.nan.
+template <typename E, bool kResid>
+__device__ BestAcc slow_block_race(const Params& P, const char* trow, const char* drow,
+                                   const ResidualRow& rr, uint32_t pos, RequestKey rk) {
+  const int lane = threadIdx.x & 31;
+  const int nblocks = (P.vocab + kRaceBlock - 1) / kRaceBlock;
+  BestAcc acc;
+  acc.init();
+  for (int b = lane; b < nblocks; b += 32) {
+    const int v_end = min(P.vocab, (b + 1) * kRaceBlock);
+    float s = 0.f, m = kNegInf;
+    if (kResid) {
+      for (int v = b * kRaceBlock; v < v_end; ++v) {
+        const float p = fast_ex2(fmaf(E::load1(trow, v), rr.c, -rr.mp)) * rr.inv_sp;
+        const float q = fast_ex2(fmaf(E::load1(drow, v), rr.c, -rr.mq)) * rr.inv_sq;
+        s += fmaxf(p - q, 0.f);
+      }
+      m = 0.f;
+    } else {
+      for (int v = b * kRaceBlock; v < v_end; ++v) {
+        const float x = E::load1(trow, v);
+        acc.nan |= (x != x) || (x == -kNegInf);
+        m = fmaxf(m, x);
+      }
+      m *= rr.c;
+      if (m > kNegInf)
+        for (int v = b * kRaceBlock; v < v_end; ++v) s += fast_ex2(fmaf(E::load1(trow, v), rr.c, -m));
+    }
+    if (s > 0.f) acc.take(m + fast_lg2(s) + race_gain(race_word(2u, b, pos, rk, P.key)), b);
+  }
+  acc = warp_reduce(acc);
+  return acc;
+}
+
+// Rows whose vector groups line up with the race blocks.
+template <typename E>
+__device__ __forceinline__ bool row_fast(const char* row, int vocab) {
+  return ((reinterpret_cast<uintptr_t>(row) & 15u) == 0u) && (vocab % E::kVec == 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -391,117 +541,72 @@ __device__ __forceinline__ BestAcc item_argmax(const Params& P, const QItem* que
   return acc;
 }
 
-template <typename E, int OFF>
+// Bonus race item: block race over the chunk's vector groups.  Rows that are
+// not block aligned stream through the ring without work and are raced later
+// by the slow path (partial index -2).
+template <typename E>
 __device__ __forceinline__ BestAcc item_race(const Params& P, const QItem* queue,
                                              const int* s_qend, uint4* ring, LoadCursor<E>& lc,
                                              int& gs, const QItem& it) {
   BestAcc acc;
   acc.init();
-  const uint32_t pos = (uint32_t)it.pos;
-  float thr = kNegInf;
-  if (it.ch == 0 && (int)threadIdx.x < it.head) {
-    const int e = threadIdx.x;
-    race_take(acc, kNegInf, E::load1(it.row, e), it.c,
-              race_word1(e, pos, it.req_lo, it.req_hi, P.key), e);
+  if (!(it.head == 0 && it.tail == 0)) {
+    consume_item<E>(P, queue, s_qend, ring, lc, gs, it, [&](const float(&)[E::kVec], int) {});
+    acc.idx = -2;
+    return acc;
   }
+  const int w = threadIdx.x >> 5;
+  const RequestKey rk{it.req_lo, it.req_hi};
+  GroupGains<E> gg;
+  int g = 0;
   consume_item<E>(P, queue, s_qend, ring, lc, gs, it, [&](const float(&x)[E::kVec], int e0) {
-    for_each_race_word<E::kVec, OFF>(e0, pos, it.req_lo, it.req_hi, P.key,
-                                     [&](int e, uint32_t w) {
-                                       race_take(acc, thr, x[e], it.c, w, e0 + e);
-                                     });
-    thr = warp_max(acc.v);
+    if ((g & 31) == 0) gg.make(it.vbeg, g, w, (uint32_t)it.pos, rk, P.key);
+    group_bonus<E>(acc, x, e0, it.c, gg.get(g));
+    ++g;
   });
-  if (it.ch == P.nch - 1 && (int)threadIdx.x < it.tail) {
-    const int e = it.head + it.nvec * E::kVec + threadIdx.x;
-    race_take(acc, kNegInf, E::load1(it.row, e), it.c,
-              race_word1(e, pos, it.req_lo, it.req_hi, P.key), e);
-  }
   return acc;
 }
 
 // ---------------------------------------------------------------------------
-// Residual draw ("Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree,
-// and DSpark", section 1: at the first rejection, sample from the normalised
-// positive residual [p_j - q_j]_+).  Score log2 w_v - log2 E_v over w_v > 0.
-// Bound: w_v <= p_v = 2^(c x_v - M_p) / S_p, so an element whose
-// c x_v + kbound + (bound on -log2 E_v) cannot reach the warp's best is
-// skipped (kbound carries a margin for the fp32 rounding of the exact path).
-// A fallback job (residual without mass, i.e. p == q) races on p_j instead.
+// Residual job chunk ("Speculative Decoding: Medusa, MTP, EAGLE, DFlash,
+// DDTree, and DSpark", section 1: at the first rejection, sample from the
+// normalised positive residual [p_j - q_j]_+): the block race over the chunk,
+// rows t_j and d_j read through L2 (both are block aligned: jobs are only
+// published for such rows).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void residual_take(BestAcc& acc, float thr, float x, float z,
-                                              const Job& jb, uint32_t w, int e) {
-  if (fmaf(x, jb.c, race_gain_bound(w) + jb.kbound) >= thr) {
-    const float p = fast_ex2(fmaf(x, jb.c, -jb.mp)) * jb.inv_sp;
-    const float q = fast_ex2(fmaf(z, jb.c, -jb.mq)) * jb.inv_sq;
-    const float wv = p - q;
-    if (wv > 0.f) acc.take(fast_lg2(wv) - fast_lg2(race_exponential(w)), e);
-  }
-}
-
-template <typename E, bool kFallback, int OFF>
-__device__ __forceinline__ BestAcc job_chunk_vec(const Params& P, const Job& jb, const Geom<E>& g) {
+template <typename E>
+__device__ BestAcc job_chunk(const Params& P, const Job& jb) {
+  const int chv = P.nper * kThreads;
+  Geom<E> g;
+  g.init(jb.trow, P.vocab, jb.ch, chv);
+  const uint4* tp = g.vecs(jb.trow);
+  const uint4* dp = g.vecs(jb.drow);
+  const ResidualRow rr{jb.c, jb.mp, jb.inv_sp, jb.mq, jb.inv_sq};
+  const RequestKey rk{jb.req_lo, jb.req_hi};
+  const int w = threadIdx.x >> 5;
   BestAcc acc;
   acc.init();
-  float thr = kNegInf;
-  const uint4* tp = g.vecs(jb.trow);
-  const uint4* dp = kFallback ? tp : g.vecs(jb.drow);
-  const uint32_t pos = (uint32_t)jb.j;
-  // uniform trip count across the compute warps (warp_max needs every lane)
+  GroupGains<E> gg;
+  int gi = 0;
+  // uniform trip count across the compute warps (the shuffles need every lane)
   for (int v0 = g.vbeg; v0 < g.vend; v0 += kThreads * kResUnroll) {
     uint4 dt[kResUnroll], dd[kResUnroll];
 #pragma unroll
     for (int u = 0; u < kResUnroll; ++u) {
       const int vi = v0 + u * kThreads + (int)threadIdx.x;
       dt[u] = vi < g.vend ? __ldcg(tp + vi) : E::pad();
-      dd[u] = (!kFallback && vi < g.vend) ? __ldcg(dp + vi) : E::pad();
+      dd[u] = vi < g.vend ? __ldcg(dp + vi) : E::pad();
     }
 #pragma unroll
     for (int u = 0; u < kResUnroll; ++u) {
       float x[E::kVec], z[E::kVec];
       E::unpack(dt[u], x);
       E::unpack(dd[u], z);
-      const int e0 = g.head + (v0 + u * kThreads + (int)threadIdx.x) * E::kVec;
-      for_each_race_word<E::kVec, OFF>(e0, pos, jb.req_lo, jb.req_hi, P.key,
-                                       [&](int e, uint32_t w) {
-                                         if (kFallback) race_take(acc, thr, x[e], jb.c, w, e0 + e);
-                                         else residual_take(acc, thr, x[e], z[e], jb, w, e0 + e);
-                                       });
-      thr = warp_max(acc.v);
+      if ((gi & 31) == 0) gg.make(g.vbeg, gi, w, (uint32_t)jb.j, rk, P.key);
+      const int e0 = (v0 + u * kThreads + (int)threadIdx.x) * E::kVec;
+      group_residual<E>(acc, x, z, e0, rr, gg.get(gi));
+      ++gi;
     }
-  }
-  return acc;
-}
-
-template <typename E, bool kFallback>
-__device__ BestAcc job_chunk(const Params& P, const Job& jb) {
-  const int chv = P.nper * kThreads;
-  Geom<E> gt, gd;
-  gt.init(jb.trow, P.vocab, jb.ch, chv);
-  gd.init(kFallback ? jb.trow : jb.drow, P.vocab, jb.ch, chv);
-  const uint32_t pos = (uint32_t)jb.j;
-  auto one = [&](BestAcc& acc, int e) {
-    const uint32_t w = race_word1(e, pos, jb.req_lo, jb.req_hi, P.key);
-    const float x = E::load1(jb.trow, e);
-    if (kFallback) race_take(acc, kNegInf, x, jb.c, w, e);
-    else residual_take(acc, kNegInf, x, E::load1(jb.drow, e), jb, w, e);
-  };
-  BestAcc acc;
-  if (gt.head == gd.head) {
-    switch (gt.head & 3) {
-      case 0: acc = job_chunk_vec<E, kFallback, 0>(P, jb, gt); break;
-      case 1: acc = job_chunk_vec<E, kFallback, 1>(P, jb, gt); break;
-      case 2: acc = job_chunk_vec<E, kFallback, 2>(P, jb, gt); break;
-      default: acc = job_chunk_vec<E, kFallback, 3>(P, jb, gt); break;
-    }
-    if (jb.ch == 0 && (int)threadIdx.x < gt.head) one(acc, threadIdx.x);
-    if (jb.ch == P.nch - 1 && (int)threadIdx.x < gt.tail)
-      one(acc, gt.head + gt.nvec * E::kVec + threadIdx.x);
-  } else {
-    // rows with different 16-byte phases: plain element loads over the chunk
-    acc.init();
-    const int e_beg = jb.ch == 0 ? 0 : gt.head + gt.vbeg * E::kVec;
-    const int e_end = jb.ch == P.nch - 1 ? P.vocab : gt.head + gt.vend * E::kVec;
-    for (int e = e_beg + threadIdx.x; e < e_end; e += kThreads) one(acc, e);
   }
   return acc;
 }
@@ -527,12 +632,11 @@ __device__ __forceinline__ void write_skipped(const Params& P, int r, int d0, in
   }
 }
 
-// Publishes a job (residual or fallback) for request r at position j.
-__device__ __forceinline__ void publish_job(const Params& P, int r, int j, bool fallback) {
+// Publishes the residual job of request r at position j.
+__device__ __forceinline__ void publish_job(const Params& P, int r, int j) {
   const int slot = atomicAdd(P.ctr + kCntReserve, 1);
   const unsigned long long word = (unsigned long long)(uint32_t)r |
-                                  ((unsigned long long)(uint32_t)j << 24) |
-                                  (fallback ? (1ull << 30) : 0ull) | (1ull << 31) |
+                                  ((unsigned long long)(uint32_t)j << 24) | (1ull << 31) |
                                   ((unsigned long long)(uint32_t)P.nch << 32);
   __threadfence();
   atomicExch(P.res_slots + slot, word);
@@ -604,8 +708,8 @@ __device__ void scan_request(const Params& P, int r, const int* s_doff) {
         qy = fast_ex2(tq) / pd.b;
       } else if (lane == k) {
         const Partial pr = ld_cg(P.rowres + n0 + 2 * k);
-        bad = pr.bad;
-        tok = pr.idx;  // bonus race winner
+        bad = pr.bad || pr.idx == -1;  // -1: no block with mass (no finite logit)
+        tok = pr.idx;                   // winning block of the bonus race, or -2
       }
     }
     if (__any_sync(0xffffffffu, bad != 0u)) rs = kStNonfinite;
@@ -617,9 +721,48 @@ __device__ void scan_request(const Params& P, int r, const int* s_doff) {
   const uint32_t rej = __ballot_sync(0xffffffffu, lane < k && !accept);
   const int A = rej ? __ffs(rej) - 1 : k;
   const int tok_at_A = __shfl_sync(0xffffffffu, tok, A);
-  const bool residual = (mode == kSampling) && A < k;
+  // the committed extra token: greedy argmax, bonus draw, or (pending) residual
+  int token = -1;
+  bool pending = false;
+  if (mode == kGreedy) {
+    token = tok_at_A;
+  } else {
+    const RequestKey rk = request_key(P, r);
+    const float c = kLog2e / t;
+    const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(t0 + A) * row_bytes;
+    const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + A) * row_bytes;
+    ResidualRow rr{c, 0.f, 0.f, 0.f, 0.f};
+    if (A == k) {
+      // bonus: the block race ran in the row pass (index -2: not block aligned)
+      if (tok_at_A >= 0) {
+        token = inner_race<E, false>(P, trow, nullptr, tok_at_A, rr, (uint32_t)k, rk);
+      } else {
+        const BestAcc br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)k, rk);
+        if (br.nan || br.idx < 0) {
+          write_skipped(P, r, d0, k, kStNonfinite, lane);
+          return;
+        }
+        token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)k, rk);
+      }
+    } else if (row_fast<E>(trow, P.vocab) && row_fast<E>(drow, P.vocab)) {
+      pending = true;  // a residual job draws the token
+    } else {
+      const Partial pt = ld_cg(P.rowres + n0 + 2 * A);
+      const Partial pd = ld_cg(P.rowres + n0 + 2 * A + 1);
+      rr = ResidualRow{c, pt.a, 1.f / pt.b, pd.a, 1.f / pd.b};
+      BestAcc br = slow_block_race<E, true>(P, trow, drow, rr, (uint32_t)A, rk);
+      if (br.idx >= 0) {
+        token = inner_race<E, true>(P, trow, drow, br.idx, rr, (uint32_t)A, rk);
+      } else {
+        // the residual has no mass (p == q): draw from p_j instead
+        rr = ResidualRow{c, 0.f, 0.f, 0.f, 0.f};
+        br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)A, rk);
+        token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)A, rk);
+      }
+    }
+  }
   if (lane < width) {  // width = max_k + 1 <= 32; lane i holds y_i
-    const int v = lane < A ? y : ((lane == A && !residual) ? tok_at_A : -1);
+    const int v = lane < A ? y : (lane == A ? token : -1);
     P.committed[(size_t)r * width + lane] = v;
   }
   const float nan = __int_as_float(0x7fc00000);
@@ -632,17 +775,17 @@ __device__ void scan_request(const Params& P, int r, const int* s_doff) {
   if (lane == 0) {
     P.accepted_len[r] = A;
     if (P.req_status) P.req_status[r] = 0;
-    if (residual) publish_job(P, r, A, false);
+    if (pending) publish_job(P, r, A);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Job queue: claim one chunk (control lane 0), false if none is ready.
-// Slot word: r (bits 0-23) | j (24-29) | fallback (30) | published (31) |
-// chunks left (32-63).  *first_live skips slots already seen exhausted.
+// Slot word: r (bits 0-23) | j (24-29) | published (31) | chunks left (32-63).
+// *first_live skips slots already seen exhausted.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool claim_job(const Params& P, int* first_live, int* slot, int* r,
-                                          int* j, int* ch, bool* fallback) {
+                                          int* j, int* ch) {
   const int reserved = ld_volatile(P.ctr + kCntReserve);
   for (int s = *first_live; s < reserved; ++s) {
     unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(P.res_slots + s);
@@ -654,7 +797,6 @@ __device__ __forceinline__ bool claim_job(const Params& P, int* first_live, int*
         *slot = s;
         *r = (int)(w & 0xffffffull);
         *j = (int)((w >> 24) & 0x3full);
-        *fallback = (w >> 30) & 1ull;
         *ch = (int)(w >> 32) - 1;
         return true;
       }
@@ -711,10 +853,10 @@ __device__ __forceinline__ void fill_queue(const Params& P, const int* s_doff, Q
   __syncwarp();
 }
 
-// Fill in a residual / fallback job for (slot, r, j, ch) (lane 0).
+// Fill in the residual job chunk (slot, r, j, ch) (lane 0).
 template <typename E>
 __device__ __forceinline__ void make_job(const Params& P, const int* s_doff, int slot, int r,
-                                         int j, int ch, bool fallback, Job& jb) {
+                                         int j, int ch, Job& jb) {
   const size_t row_bytes = (size_t)P.vocab * E::kBytes;
   const int d0 = s_doff[r];
   const int n0 = r + 2 * d0;
@@ -728,19 +870,13 @@ __device__ __forceinline__ void make_job(const Params& P, const int* s_doff, int
   const RequestKey rk = request_key(P, r);
   jb.req_lo = rk.lo;
   jb.req_hi = rk.hi;
-  if (!fallback) {
-    __threadfence();
-    const Partial rt = ld_cg(P.rowres + n0 + 2 * j);
-    const Partial rd = ld_cg(P.rowres + n0 + 2 * j + 1);
-    jb.mp = rt.a;
-    jb.inv_sp = 1.f / rt.b;
-    jb.mq = rd.a;
-    jb.inv_sq = 1.f / rd.b;
-    // margin: 1/64 plus a few ulps of |M_p| (the exact path rounds at that scale)
-    jb.kbound = -rt.a - fast_lg2(rt.b) + 0.015625f + fabsf(rt.a) * 0x1p-20f;
-  } else {
-    jb.mp = jb.inv_sp = jb.mq = jb.inv_sq = jb.kbound = 0.f;
-  }
+  __threadfence();
+  const Partial rt = ld_cg(P.rowres + n0 + 2 * j);
+  const Partial rd = ld_cg(P.rowres + n0 + 2 * j + 1);
+  jb.mp = rt.a;
+  jb.inv_sp = 1.f / rt.b;
+  jb.mq = rd.a;
+  jb.inv_sq = 1.f / rd.b;
 }
 
 // Combine the compute warps' partials of a finished unit (control warp).
@@ -812,7 +948,10 @@ __device__ void complete_item(const Params& P, const int* s_doff, const QItem& i
       a = BestAcc::merge(a, b);
     }
     a = warp_reduce(a);
-    const bool bad = a.nan != 0u || a.idx < 0 || !(a.v < 3.0e38f);
+    // argmax rows need a finite maximum; race rows carry a block index (-1: no
+    // block with mass, -2: left to the slow path), judged by the scan
+    const bool bad = it.kind == kRace ? a.nan != 0u
+                                      : (a.nan != 0u || a.idx < 0 || !(a.v < 3.0e38f));
     res = Partial{a.v, 0.f, a.idx, bad ? 1u : 0u};
   }
   int last_row = 0;
@@ -836,12 +975,15 @@ __device__ void complete_item(const Params& P, const int* s_doff, const QItem& i
   }
 }
 
-// Completion of a job unit: the last chunk picks the token (or hands the
-// request to a fallback job when the residual had no mass).
+// Completion of a job unit: the last chunk merges the block race, runs the
+// element race in the winning block and commits the token (a residual without
+// mass, i.e. p == q, draws from p_j instead, by the slow path).
 struct JobRef {
   int slot, r, j, ch;
 };
-__device__ void complete_job(const Params& P, const JobRef& jb, bool fallback, const Partial* mb) {
+template <typename E>
+__device__ void complete_job(const Params& P, const int* s_doff, const JobRef& jb,
+                             const Partial* mb) {
   const int lane = threadIdx.x & 31;
   const Partial p = combine_best(mb);
   int last = 0;
@@ -864,13 +1006,27 @@ __device__ void complete_job(const Params& P, const JobRef& jb, bool fallback, c
     a = BestAcc::merge(a, b);
   }
   a = warp_reduce(a);
+  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
+  const int d0 = s_doff[jb.r];
+  const int n0 = jb.r + 2 * d0;
+  const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + jb.r + jb.j) * row_bytes;
+  const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + jb.j) * row_bytes;
+  const float c = kLog2e / __ldg(P.temperature + jb.r);
+  const RequestKey rk = request_key(P, jb.r);
+  int token;
+  if (a.idx >= 0) {
+    const Partial pt = ld_cg(P.rowres + n0 + 2 * jb.j);
+    const Partial pd = ld_cg(P.rowres + n0 + 2 * jb.j + 1);
+    const ResidualRow rr{c, pt.a, 1.f / pt.b, pd.a, 1.f / pd.b};
+    token = inner_race<E, true>(P, trow, drow, a.idx, rr, (uint32_t)jb.j, rk);
+  } else {
+    const ResidualRow rr{c, 0.f, 0.f, 0.f, 0.f};
+    const BestAcc br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)jb.j, rk);
+    token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)jb.j, rk);
+  }
   if (lane == 0) {
     P.res_cnt[jb.slot] = 0;
-    if (a.idx >= 0 || fallback) {
-      P.committed[(size_t)jb.r * (P.max_k + 1) + jb.j] = a.idx;
-    } else {
-      publish_job(P, jb.r, jb.j, true);
-    }
+    P.committed[(size_t)jb.r * (P.max_k + 1) + jb.j] = token;
   }
 }
 
@@ -992,21 +1148,15 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
             if (it.kind == kArgmax) {
               a = item_argmax<E>(P, queue, &s_qend, ring, lc, gs, it);
             } else {
-              switch (it.head & 3) {
-                case 0: a = item_race<E, 0>(P, queue, &s_qend, ring, lc, gs, it); break;
-                case 1: a = item_race<E, 1>(P, queue, &s_qend, ring, lc, gs, it); break;
-                case 2: a = item_race<E, 2>(P, queue, &s_qend, ring, lc, gs, it); break;
-                default: a = item_race<E, 3>(P, queue, &s_qend, ring, lc, gs, it); break;
-              }
+              a = item_race<E>(P, queue, &s_qend, ring, lc, gs, it);
             }
             a = warp_reduce(a);
             out = Partial{a.v, 0.f, a.idx, a.nan};
           }
           if (lane == 0) mailbox[u & 1][warp] = out;
-        } else if (type == kUnitResidual || type == kUnitFallback) {
+        } else if (type == kUnitResidual) {
           const Job jb = s_unit[u & 1].job;
-          BestAcc a = type == kUnitResidual ? job_chunk<E, false>(P, jb)
-                                            : job_chunk<E, true>(P, jb);
+          BestAcc a = job_chunk<E>(P, jb);
           a = warp_reduce(a);
           if (lane == 0) mailbox[u & 1][warp] = Partial{a.v, 0.f, a.idx, a.nan};
         }
@@ -1020,8 +1170,8 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
                          s_unit[u & 1].job.ch};
         if (prev_type == kUnitItem) {
           complete_item<E>(P, s_doff, queue[prev_qidx & (kQueue - 1)], mailbox[(u - 1) & 1]);
-        } else if (prev_type == kUnitResidual || prev_type == kUnitFallback) {
-          complete_job(P, prev_job, prev_type == kUnitFallback, mailbox[(u - 1) & 1]);
+        } else if (prev_type == kUnitResidual) {
+          complete_job<E>(P, s_doff, prev_job, mailbox[(u - 1) & 1]);
         }
         // keep the items the compute warps may stream during unit u+1 queued
         fill_queue<E>(P, s_doff, queue, &s_qend, cs);
@@ -1031,13 +1181,12 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
           Unit nx;
           nx.type = kUnitIdle;
           int slot, r, j, ch;
-          bool fb;
           bool got = false;
           if (ld_volatile(P.ctr + kCntPublished) != ld_volatile(P.ctr + kCntClaimed))
-            got = claim_job(P, &cs.first_live, &slot, &r, &j, &ch, &fb);
+            got = claim_job(P, &cs.first_live, &slot, &r, &j, &ch);
           if (got) {
-            nx.type = fb ? kUnitFallback : kUnitResidual;
-            make_job<E>(P, s_doff, slot, r, j, ch, fb, nx.job);
+            nx.type = kUnitResidual;
+            make_job<E>(P, s_doff, slot, r, j, ch, nx.job);
           } else if (cs.q_used < cs.q_head) {
             nx.type = kUnitItem;
             nx.qidx = cs.q_used;
