@@ -271,8 +271,8 @@ static int temperature_ok(float t)
  * and -1 after it; accept_flags[drf_off(r) + i] = (i < A_r).  A request whose
  * inputs are invalid gets accepted_len -1, a committed row of -1 and flags 0.
  *
- * Debug outputs (all nullable): p_y/q_y/u per draft position of stochastic
- * requests (NaN for greedy ones); accept_margin = (p - u q) / max(p, u q);
+ * Debug outputs (all nullable): p_y/q_y/u per decided draft position (0..A)
+ * of sampling requests, NaN elsewhere; accept_margin = (p - u q) / max(p, u q);
  * race_kind/race_pos/race_margin per request (race_margin: the relative gap
  * of the draw's decisive comparisons); req_status per request.
  * Returns the OR of all status bits.
@@ -340,17 +340,6 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
         const int greedy = (t == 0.0f);
         if (!rs && !greedy && k > 0 && draft_logits == NULL)
             rs |= ORC_NO_DRAFT;
-        if (!rs) {
-            /* Rows the method reads: every target row; draft rows only when */
-            /* the request samples.                                           */
-            for (int i = 0; i <= k; ++i)
-                if (!row_is_valid(target_logits, dtype, tgt_off + i, vocab))
-                    rs |= ORC_NONFINITE;
-            if (!greedy)
-                for (int i = 0; i < k; ++i)
-                    if (!row_is_valid(draft_logits, dtype, drf_off + i, vocab))
-                        rs |= ORC_NONFINITE;
-        }
         if (rs) {
             status |= rs;
             if (req_status) req_status[r] = (int32_t)rs;
@@ -359,16 +348,29 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
             continue;
         }
 
+        /* Positions are verified left to right and nothing after the first  */
+        /* rejection is kept ([SD] section 1, [AMD]), so a round reads the     */
+        /* rows of positions 0..A (and the bonus row when A = k) and no more. */
+        /* A row it reads with NaN, +inf or no finite logit skips the request. */
         int accepted = 0;
         int token = -1;
+        int bad_row = 0;
         if (greedy) {
             /* Greedy equivalence: keep y_i while it equals the target argmax; */
             /* the committed extra token is the target argmax at position A.   */
-            while (accepted < k &&
-                   draft_tokens[drf_off + accepted] ==
-                       orc_argmax(target_logits, dtype, tgt_off + accepted, vocab))
-                ++accepted;
-            token = orc_argmax(target_logits, dtype, tgt_off + accepted, vocab);
+            for (;;) {
+                if (!row_is_valid(target_logits, dtype, tgt_off + accepted, vocab)) {
+                    bad_row = 1;
+                    break;
+                }
+                const int a = orc_argmax(target_logits, dtype, tgt_off + accepted, vocab);
+                if (accepted < k && draft_tokens[drf_off + accepted] == a) {
+                    ++accepted;
+                    continue;
+                }
+                token = a;
+                break;
+            }
             if (race_kind) race_kind[r] = ORC_RACE_GREEDY;
             if (race_pos) race_pos[r] = accepted;
         } else {
@@ -376,7 +378,12 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
             /* Accept y_i with probability min(1, p_i(y_i)/q_i(y_i)), tested as */
             /* u_i q_i(y_i) < p_i(y_i); stop at the first rejection.             */
             int rejected = 0;
-            for (int i = 0; i < k; ++i) {
+            for (int i = 0; i < k && !rejected; ++i) {
+                if (!row_is_valid(target_logits, dtype, tgt_off + i, vocab) ||
+                    !row_is_valid(draft_logits, dtype, drf_off + i, vocab)) {
+                    bad_row = 1;
+                    break;
+                }
                 const int32_t y = draft_tokens[drf_off + i];
                 orc_softmax(target_logits, dtype, tgt_off + i, vocab, temp, p);
                 orc_softmax(draft_logits, dtype, drf_off + i, vocab, temp, q);
@@ -389,20 +396,22 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
                     double scale = lhs > rhs ? lhs : rhs;
                     accept_margin[drf_off + i] = scale > 0.0 ? (rhs - lhs) / scale : 0.0;
                 }
-                if (!rejected) {
-                    if (lhs < rhs)
-                        ++accepted;
-                    else
-                        rejected = 1;
-                }
+                if (lhs < rhs)
+                    ++accepted;
+                else
+                    rejected = 1;
             }
             double gap = NAN;
-            if (accepted == k) {
+            if (!bad_row && accepted == k) {
                 /* Every draft survived: one more token from the target p_k. */
-                orc_softmax(target_logits, dtype, tgt_off + k, vocab, temp, p);
-                token = race(p, vocab, seed, req, (uint32_t)k, NULL, NULL, &gap);
-                if (race_kind) race_kind[r] = ORC_RACE_BONUS;
-            } else {
+                if (!row_is_valid(target_logits, dtype, tgt_off + k, vocab)) {
+                    bad_row = 1;
+                } else {
+                    orc_softmax(target_logits, dtype, tgt_off + k, vocab, temp, p);
+                    token = race(p, vocab, seed, req, (uint32_t)k, NULL, NULL, &gap);
+                    if (race_kind) race_kind[r] = ORC_RACE_BONUS;
+                }
+            } else if (!bad_row) {
                 /* First rejection at j = A: draw from [p_j - q_j]_+, normalised */
                 /* (normalisation does not change the race winner).             */
                 const int j = accepted;
@@ -421,6 +430,22 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
             }
             if (race_pos) race_pos[r] = accepted;
             if (race_margin) race_margin[r] = gap;
+        }
+        if (bad_row) {
+            status |= ORC_NONFINITE;
+            if (req_status) req_status[r] = (int32_t)ORC_NONFINITE;
+            if (race_kind) race_kind[r] = ORC_RACE_NONE;
+            if (race_pos) race_pos[r] = -1;
+            if (race_margin) race_margin[r] = NAN;
+            for (int i = 0; i < k; ++i) {
+                if (p_y) p_y[drf_off + i] = NAN;
+                if (q_y) q_y[drf_off + i] = NAN;
+                if (u_out) u_out[drf_off + i] = NAN;
+                if (accept_margin) accept_margin[drf_off + i] = NAN;
+            }
+            tgt_off += (size_t)k + 1;
+            drf_off += (size_t)k;
+            continue;
         }
 
         accepted_len[r] = accepted;

@@ -232,8 +232,11 @@ def test_flags_are_the_accepted_prefix():
         A = out["accepted_len"][r]
         assert (flags[r, :A] == 1).all() and (flags[r, A:] == 0).all()
         assert out["committed"][r][A] >= 0 and (out["committed"][r][A + 1:] == -1).all()
-    # positions after the first rejection still report their test inputs
-    assert np.isfinite(out["p_y"]).all()
+    # the debug values cover exactly the decided positions 0..A
+    py = out["p_y"].reshape(64, 5)
+    for r in range(64):
+        A = out["accepted_len"][r]
+        assert np.isfinite(py[r, :min(A + 1, 5)]).all() and np.isnan(py[r, A + 1:]).all()
 
 
 # --- invalid inputs -----------------------------------------------------------------
@@ -246,7 +249,7 @@ def test_invalid_inputs_are_skipped_with_status():
     bad["temperature"] = inp["temperature"].copy()
     bad["temperature"][2] = -1.0                # request 2: negative temperature
     bad["target"] = inp["target"].copy()
-    bad["target"][3 * 3 + 1, 5] = np.nan        # request 3: NaN in a target row
+    bad["target"][3 * 3 + 0, 5] = np.nan        # request 3: NaN in its first target row
     out = oracle.verify(seed=1, **bad)
     assert out["status"] == oracle.BAD_TOKEN | oracle.BAD_TEMP | oracle.NONFINITE
     assert out["accepted_len"][0] >= 0
@@ -260,6 +263,32 @@ def test_invalid_inputs_are_skipped_with_status():
     assert out["status"] & oracle.BAD_K and (out["accepted_len"] == -1).all()
     out = oracle.verify(seed=1, total_draft=7, **inp)
     assert out["status"] == oracle.BAD_TOTAL and (out["accepted_len"] == -1).all()
+
+
+def test_rows_after_the_first_rejection_are_never_read():
+    """A round reads positions 0..A only: bad rows beyond A do not matter, bad rows
+    the left-to-right procedure reaches do."""
+    inp = cases.random_batch([4] * 40, [1.0] * 40, vocab=64, sigma_d=2.0, seed=12)
+    base = oracle.verify(seed=3, **inp)
+    A = base["accepted_len"]
+    t_off = np.concatenate([[0], np.cumsum(inp["num_draft"] + 1)])
+    d_off = np.concatenate([[0], np.cumsum(inp["num_draft"])])
+    early = [r for r in range(40) if A[r] < 3]
+    assert early
+    late = dict(inp)
+    late["target"], late["draft"] = inp["target"].copy(), inp["draft"].copy()
+    for r in early:
+        late["target"][t_off[r] + A[r] + 1:t_off[r + 1], 0] = np.nan   # beyond A
+        late["draft"][d_off[r] + A[r] + 1:d_off[r + 1], 0] = np.inf
+    out = oracle.verify(seed=3, **late)
+    assert out["status"] == 0
+    assert (out["committed"] == base["committed"]).all()
+    reached = dict(inp)
+    reached["target"] = inp["target"].copy()
+    r = early[0]
+    reached["target"][t_off[r] + A[r], 3] = np.nan                     # the rejected position
+    out = oracle.verify(seed=3, **reached)
+    assert out["status"] == oracle.NONFINITE and out["accepted_len"][r] == -1
 
 
 def test_greedy_request_ignores_draft_rows_and_accepts_null_draft():
