@@ -280,11 +280,10 @@ def run_ours(args):
                      batch=args.batch or None)
     torch.cuda.empty_cache()
     rows_per_step = b.verified_rows()
-    alg_bytes = b.algorithmic_bytes()
     es = 2 if b.dtype == "bf16" else 4
     k = b.num_draft.cpu().numpy().astype(np.int64)
     t = b.temperature.cpu().numpy()
-    rowpass_bytes = int(np.where(t > 0, 2 * k + 1, k + 1).sum()) * b.vocab * es
+    full_window_bytes = b.full_window_bytes()
 
     v = Verifier(b.batch, b.max_k, b.vocab, b.dtype, device=local, host_staging=not args.no_e2e)
     out = v.outputs(b.batch, b.total_draft)
@@ -298,6 +297,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     if v.status() != 0:
         raise RuntimeError(f"verify status {v.status()} on the benchmark batch")
+    # bytes the round must read: positions 0..A of each request (target and draft
+    # rows when sampling, target rows when greedy) and the bonus row when A = k
+    A = out.accepted_len.cpu().numpy().astype(np.int64)
+    rows_needed = np.where(t > 0, np.where(A < k, 2 * (A + 1), 2 * k + 1), A + 1)
+    rowpass_bytes = b.needed_bytes(A)
+    alg_bytes = rowpass_bytes + b.io_bytes()
 
     n_ev = min(64, args.steps)
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
@@ -369,6 +374,10 @@ def run_ours(args):
                    "vocab": b.vocab, "logits": b.dtype, "rows_per_step": rows_per_step,
                    "alg_bytes_per_step": alg_bytes,
                    "step_gbs": alg_bytes / (ms_max * 1e-3) / 1e9,
+                   "rows_read_per_step": int(rows_needed.sum()),
+                   "full_window_rows": int(np.where(t > 0, 2 * k + 1, k + 1).sum()),
+                   "full_window_gbs": full_window_bytes / (ms_max * 1e-3) / 1e9,
+                   "mean_accepted": float(A.mean()),
                    "l2": "no flush: each step reads %.2f GB of logits, larger than the 129 MB L2"
                          % (rowpass_bytes / 1e9),
                    "parallelism": f"replicas x{world}"},

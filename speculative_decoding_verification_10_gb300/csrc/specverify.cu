@@ -47,8 +47,10 @@ struct specverify_ctx {
   size_t scratch_bytes;
   sv::Partial* part;
   sv::Partial* rowres;
-  int* row_cnt;
-  int* req_cnt;
+  unsigned long long* row_cnt;
+  unsigned long long* pos_cnt;
+  uint32_t* done;
+  uint32_t epoch;
   unsigned long long* res_slots;
   sv::Partial* part2;
   int* res_cnt;
@@ -104,7 +106,8 @@ static void choose_chunks(const specverify_ctx* h, int batch, int total_draft, i
 template <typename E>
 static int launch_round(specverify_ctx* h, const sv::Params& P, cudaStream_t s) {
   const size_t smem = ring_bytes() + sizeof(int) * ((size_t)P.batch + 1);
-  const int grid = (int)std::max<long long>(1, std::min<long long>(h->grid, P.n_items));
+  const long long items = (long long)(h->max_k + 1) * 2 * P.batch * P.nch;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(h->grid, items));
   const int slot = h->n_events > 0 ? (int)(h->run_counter % (unsigned long long)h->n_events) : -1;
   h->run_counter++;
   if (slot >= 0 && cudaEventRecord(h->ev_start[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
@@ -148,7 +151,6 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.max_k = h->max_k;
   P.vocab = h->vocab;
   choose_chunks(h, batch, total_draft, &P.nper, &P.nch);
-  P.n_items = (batch + 2 * total_draft) * P.nch;
   {
     const int spi = P.nper / sv::kStageVecs;
     P.fill = std::min(sv::kQueue - 2, (sv::kStages - 1 + spi - 1) / spi + 1);
@@ -164,7 +166,9 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.part = h->part;
   P.rowres = h->rowres;
   P.row_cnt = h->row_cnt;
-  P.req_cnt = h->req_cnt;
+  P.pos_cnt = h->pos_cnt;
+  P.done = h->done;
+  P.epoch = ++h->epoch;  // never 0: 0 is the initial value of every tag
   P.res_slots = h->res_slots;
   P.part2 = h->part2;
   P.res_cnt = h->res_cnt;
@@ -244,7 +248,8 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   // persistent grid: every CTA resident at once
   h->grid = occ * h->num_sms;
 
-  h->max_rows = (size_t)max_batch * (2 * (size_t)max_k + 1);
+  // row slots: waves 0..max_k, a target and a draft slot per request each
+  h->max_rows = (size_t)max_batch * 2 * ((size_t)max_k + 1);
   const size_t row_bytes = (size_t)vocab * h->elem_bytes;
   const size_t nvec = std::max<size_t>(1, row_bytes / 16);
   const size_t min_chv = (size_t)sv::kStageVecs * sv::kThreads;
@@ -264,8 +269,9 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   };
   const size_t o_part = carve(sizeof(sv::Partial) * h->max_rows * h->max_nch);
   const size_t o_rowres = carve(sizeof(sv::Partial) * h->max_rows);
-  const size_t o_rowcnt = carve(sizeof(int) * h->max_rows);
-  const size_t o_reqcnt = carve(sizeof(int) * max_batch);
+  const size_t o_rowcnt = carve(sizeof(unsigned long long) * h->max_rows);
+  const size_t o_poscnt = carve(sizeof(unsigned long long) * (size_t)max_batch * (max_k + 1));
+  const size_t o_done = carve(sizeof(uint32_t) * max_batch);
   // job slots: one residual and at most one fallback job per request
   const size_t o_slots = carve(sizeof(unsigned long long) * 2 * (size_t)max_batch);
   const size_t o_part2 = carve(sizeof(sv::Partial) * 2 * (size_t)max_batch * h->max_nch);
@@ -286,8 +292,10 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   char* b = static_cast<char*>(h->scratch);
   h->part = reinterpret_cast<sv::Partial*>(b + o_part);
   h->rowres = reinterpret_cast<sv::Partial*>(b + o_rowres);
-  h->row_cnt = reinterpret_cast<int*>(b + o_rowcnt);
-  h->req_cnt = reinterpret_cast<int*>(b + o_reqcnt);
+  h->row_cnt = reinterpret_cast<unsigned long long*>(b + o_rowcnt);
+  h->pos_cnt = reinterpret_cast<unsigned long long*>(b + o_poscnt);
+  h->done = reinterpret_cast<uint32_t*>(b + o_done);
+  h->epoch = 0u;
   h->res_slots = reinterpret_cast<unsigned long long*>(b + o_slots);
   h->part2 = reinterpret_cast<sv::Partial*>(b + o_part2);
   h->res_cnt = reinterpret_cast<int*>(b + o_rescnt);

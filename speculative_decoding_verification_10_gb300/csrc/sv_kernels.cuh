@@ -1,28 +1,35 @@
 // sv_kernels.cuh -- the fused verify kernel: one persistent launch per round.
 //
-// Rows and items.  The logit rows of the batch are numbered request by request,
-//     request r:  t_0 d_0 t_1 d_1 ... t_{k-1} d_{k-1} t_k     (2 k_r + 1 entries)
-// so entry n of request r is n - (r + 2 drf_off(r)).  Each entry is split into
-// `nch` vocab chunks: item = n * nch + chunk.  Items are claimed in increasing
-// order from one global counter, so all chunks of a request are read at about
-// the same time.  Draft entries of greedy requests are skipped.
+// Left to right, and no further than needed.  A round verifies the positions
+// of each request left to right and discards everything after the first
+// rejection ("Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and
+// DSpark", section 1), so it only needs the rows of positions 0..A (and the
+// bonus row when all k are accepted).  Work is therefore ordered by position:
+// wave i holds, for every request, target row t_i and draft row d_i (slot
+// n = i * 2B + 2r + is_draft), each split into `nch` vocab chunks (item =
+// n * nch + chunk), claimed in increasing order from one global counter.  A
+// request that is already decided has its later items skipped at claim time.
 //
 // Per item the CTA reduces its chunk to a 16-byte partial:
 //   sampling target row i < k, draft row i : softmax normaliser (m, S) of c*x,
 //                                            c = log2(e)/T   (p_i, q_i)
-//   sampling target row k                  : bonus race argmax c*x_v - log2 E_v
+//   sampling target row k                  : block race of the bonus draw
 //   greedy (or bad-temperature) target row : argmax (lowest index)
-// The CTA that completes an entry merges its partials; the CTA that completes
-// a request runs the acceptance scan, writes all of its outputs and, on a
-// rejection at position j, publishes a residual job: the draw from
-// [p_j - q_j]_+ over rows t_j and d_j, in nch chunks any CTA may claim.  Jobs
-// are claimed ahead of new items, while those two rows are still in L2.
+// The CTA that completes a slot merges its partials and counts the slot
+// towards its position; position i of a request is decided by whichever CTA
+// brings that count to (rows of position i) + (1 if i > 0, the "position i-1
+// accepted" signal), so each position is decided exactly once, in order, as
+// soon as both its rows and its predecessor are done.  A rejection at j
+// publishes a residual job over rows t_j and d_j (still in L2), in nch chunks
+// any CTA may claim; jobs are claimed ahead of new items.  Completion
+// counters carry the round's epoch in their high word, so counters left
+// partial by skipped work need no reset.
 //
 // CTA layout: 7 compute warps and 1 control warp, one __syncthreads per work
 // unit.  Compute warps stream the unit's bytes and leave one partial per warp
 // in shared memory.  During the next unit the control warp combines them and
 // does all latency-bound global work: partial stores, completion counters,
-// merges, the acceptance scan, claiming items and residual jobs.
+// merges, decisions, claiming items and residual jobs.
 //
 // Memory pipeline.  Each compute thread streams its 16-byte vectors of
 // successive items through a private ring of shared memory with cp.async
@@ -70,7 +77,7 @@ enum Counter : int {
   kCntReserve = 1,    // job slots reserved
   kCntPublished = 2,  // job chunks published
   kCntClaimed = 3,    // job chunks claimed
-  kCntReqDone = 4,    // requests scanned
+  kCntReqDone = 4,    // requests decided
   kCntExit = 5,       // CTAs finished
   kCntStatus = 6,     // status bits of this round
   kCntLastStatus = 7, // status bits of the previous round
@@ -88,9 +95,9 @@ struct Params {
   int batch, total_draft, max_k, vocab;
   int nch;      // chunks per row
   int nper;     // 16-byte vectors per thread per chunk (multiple of kStageVecs)
-  int n_items;  // (batch + 2 total_draft) * nch
   int fill;     // items kept claimed ahead: enough to cover kStages-1 stages, + 1
   int spin_limit;
+  uint32_t epoch;  // this round's tag for completion counters and `done`
   int32_t* accepted_len;
   int32_t* committed;
   uint8_t* flags;
@@ -98,10 +105,11 @@ struct Params {
   float* q_y;
   float* u_dbg;
   int32_t* req_status;
-  Partial* part;       // [rows * nch]
-  Partial* rowres;     // [rows]
-  int* row_cnt;        // [rows]
-  int* req_cnt;        // [batch]
+  Partial* part;       // [slots * nch], slots = (max_k + 1) * 2 * batch
+  Partial* rowres;     // [slots]
+  unsigned long long* row_cnt;  // [slots] epoch | chunks merged
+  unsigned long long* pos_cnt;  // [batch * (max_k + 1)] epoch | rows merged (+1 signal)
+  uint32_t* done;      // [batch] epoch of the round that decided the request
   unsigned long long* res_slots;  // [2 * batch] job words
   Partial* part2;      // [2 * batch * nch]
   int* res_cnt;        // [2 * batch]
@@ -115,6 +123,14 @@ __device__ __forceinline__ Partial ld_cg(const Partial* p) {
 
 __device__ __forceinline__ int ld_volatile(const int* p) {
   return *reinterpret_cast<const volatile int*>(p);
+}
+
+// Adds one to an epoch-tagged counter and returns the count of this epoch: a
+// counter last touched in an earlier round is first raised to (epoch, 0).  The
+// two atomics of one thread on one address are performed in program order.
+__device__ __forceinline__ uint32_t epoch_add(unsigned long long* c, uint32_t epoch) {
+  atomicMax(c, (unsigned long long)epoch << 32);
+  return (uint32_t)atomicAdd(c, 1ull) + 1u;
 }
 
 __device__ __forceinline__ int req_mode(float t) {
@@ -175,6 +191,11 @@ struct __align__(16) Unit {
   Job job;    // kUnitResidual
 };
 
+// slot n = i * 2B + 2r + is_draft
+__device__ __forceinline__ int slot_of(const Params& P, int i, int r, int is_draft) {
+  return i * 2 * P.batch + 2 * r + is_draft;
+}
+
 template <typename E>
 __device__ __forceinline__ void decode_item(const Params& P, const int* s_doff, int item,
                                             QItem& it) {
@@ -182,31 +203,27 @@ __device__ __forceinline__ void decode_item(const Params& P, const int* s_doff, 
   it.item = item;
   it.n = n;
   it.ch = item - n * P.nch;
-  // largest r with r + 2 drf_off(r) <= n
-  int lo = 0, hi = P.batch - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (mid + 2 * s_doff[mid] <= n) lo = mid;
-    else hi = mid - 1;
-  }
-  const int r = lo;
+  const int i = n / (2 * P.batch);
+  const int rem = n - i * 2 * P.batch;
+  const int r = rem >> 1;
+  const bool is_draft = rem & 1;
   const int d0 = s_doff[r];
   const int k = s_doff[r + 1] - d0;
-  const int l = n - (r + 2 * d0);
   const float t = __ldg(P.temperature + r);
   const int mode = req_mode(t);
-  const bool is_draft = (l < 2 * k) && (l & 1);
-  const int pos = l < 2 * k ? (l >> 1) : k;
   it.r = r;
-  it.pos = pos;
+  it.pos = i;
   it.c = mode == kSampling ? kLog2e / t : 0.f;
   const size_t row_bytes = (size_t)P.vocab * E::kBytes;
-  if (is_draft) {
-    it.kind = (mode == kSampling && P.draft != nullptr) ? kSoftmax : kSkip;
-    it.row = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + pos) * row_bytes;
+  if (i > k) {
+    it.kind = kSkip;
+    it.row = nullptr;
+  } else if (is_draft) {
+    it.kind = (mode == kSampling && i < k && P.draft != nullptr) ? kSoftmax : kSkip;
+    it.row = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + i) * row_bytes;
   } else {
-    it.kind = mode == kSampling ? (pos < k ? kSoftmax : kRace) : kArgmax;
-    it.row = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + pos) * row_bytes;
+    it.kind = mode == kSampling ? (i < k ? kSoftmax : kRace) : kArgmax;
+    it.row = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + i) * row_bytes;
   }
   it.head = it.nvec = it.tail = it.vbeg = it.vend = 0;
   it.req_lo = it.req_hi = 0u;
@@ -224,9 +241,11 @@ __device__ __forceinline__ void decode_item(const Params& P, const int* s_doff, 
   }
 }
 
-// Entries a request contributes to its completion counter.
-__device__ __forceinline__ int rows_of_request(const Params& P, int k, int mode) {
-  return (mode == kSampling && P.draft != nullptr) ? 2 * k + 1 : k + 1;
+// The count that decides position i of a request: its rows, plus the signal
+// that position i-1 was accepted (i > 0).
+__device__ __forceinline__ uint32_t position_target(const Params& P, int i, int k, int mode) {
+  const uint32_t rows = (mode == kSampling && i < k && P.draft != nullptr) ? 2u : 1u;
+  return rows + (i > 0 ? 1u : 0u);
 }
 
 // ---------------------------------------------------------------------------
@@ -614,24 +633,6 @@ __device__ BestAcc job_chunk(const Params& P, const Job& jb) {
 // ---------------------------------------------------------------------------
 // Outputs of one request, and the acceptance scan (the control warp).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void write_skipped(const Params& P, int r, int d0, int k, uint32_t rs,
-                                              int lane) {
-  const int width = P.max_k + 1;
-  for (int i = lane; i < width; i += 32) P.committed[(size_t)r * width + i] = -1;
-  const float nan = __int_as_float(0x7fc00000);
-  for (int i = lane; i < k; i += 32) {
-    P.flags[d0 + i] = 0;
-    if (P.p_y) P.p_y[d0 + i] = nan;
-    if (P.q_y) P.q_y[d0 + i] = nan;
-    if (P.u_dbg) P.u_dbg[d0 + i] = nan;
-  }
-  if (lane == 0) {
-    P.accepted_len[r] = -1;
-    if (P.req_status) P.req_status[r] = (int32_t)rs;
-    if (rs) atomicOr(reinterpret_cast<unsigned int*>(P.ctr + kCntStatus), rs);
-  }
-}
-
 // Publishes the residual job of request r at position j.
 __device__ __forceinline__ void publish_job(const Params& P, int r, int j) {
   const int slot = atomicAdd(P.ctr + kCntReserve, 1);
@@ -643,139 +644,188 @@ __device__ __forceinline__ void publish_job(const Params& P, int r, int j) {
   atomicAdd(P.ctr + kCntPublished, P.nch);
 }
 
-// "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and DSpark",
-// section 1: accept y_i with probability min(1, p_i(y_i)/q_i(y_i)), left to
-// right, stopping at the first rejection (tested as u_i q_i(y_i) < p_i(y_i));
-// greedy rounds keep y_i while it equals the target argmax.  Lane i handles
-// draft position i (k <= 31).  A rejection publishes the residual job.
-template <typename E>
-__device__ void scan_request(const Params& P, int r, const int* s_doff) {
+// Outputs of a decided request (the control warp): accepted prefix, the extra
+// token (-1 while a residual job still has to draw it), flags, NaN debug values
+// after position A; then the request is marked done.
+__device__ void finish_request(const Params& P, int r, int d0, int k, int A, int token,
+                               bool pending) {
   const int lane = threadIdx.x & 31;
-  const int d0 = s_doff[r];
-  const int k = s_doff[r + 1] - d0;
-  const int t0 = d0 + r;                  // first target row
-  const int n0 = r + 2 * d0;              // first entry of the request
   const int width = P.max_k + 1;
-  const float t = __ldg(P.temperature + r);
-  const int mode = req_mode(t);
-  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
-
-  uint32_t rs = 0u;
-  if (mode == kBadTemp) rs |= kStBadTemp;
-  int y = -1;
-  if (lane < k) {
-    y = P.tokens[d0 + lane];
-    if (y < 0 || y >= P.vocab) rs |= kStBadToken;
-  }
-  if (!rs && mode == kSampling && k > 0 && P.draft == nullptr) rs |= kStNoDraft;
-  rs = __reduce_or_sync(0xffffffffu, rs);
-
-  bool accept = true;
-  uint32_t bad = 0u;
-  int tok = -1;
-  float py = 0.f, qy = 0.f, u = 0.f;
-  if (!rs) {
-    if (mode == kGreedy) {
-      if (lane <= k) {
-        // target row i sits at entry 2i of the request (draft entries unused)
-        const Partial pr = ld_cg(P.rowres + n0 + 2 * lane);
-        bad = pr.bad;
-        tok = pr.idx;
-        if (lane < k) accept = (y == tok);
-      }
-    } else {
-      if (lane < k) {
-        const Partial pt = ld_cg(P.rowres + n0 + 2 * lane);
-        const Partial pd = ld_cg(P.rowres + n0 + 2 * lane + 1);
-        bad = pt.bad | pd.bad;
-        const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(t0 + lane) * row_bytes;
-        const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + lane) * row_bytes;
-        const float c = kLog2e / t;
-        const float tp = fmaf(E::load1(trow, y), c, -pt.a);  // log2(p(y) S_p)
-        const float tq = fmaf(E::load1(drow, y), c, -pd.a);  // log2(q(y) S_q)
-        const RequestKey rk = request_key(P, r);
-        u = accept_uniform(P.key, (uint32_t)lane, rk.lo, rk.hi);
-        // u q(y) < p(y), both sides scaled by S_p S_q 2^-max(tp, tq) > 0
-        if (tp == kNegInf) {
-          accept = false;
-        } else if (tq == kNegInf) {
-          accept = true;
-        } else {
-          const float mx = fmaxf(tp, tq);
-          accept = u * (fast_ex2(tq - mx) * pt.b) < fast_ex2(tp - mx) * pd.b;
-        }
-        py = fast_ex2(tp) / pt.b;
-        qy = fast_ex2(tq) / pd.b;
-      } else if (lane == k) {
-        const Partial pr = ld_cg(P.rowres + n0 + 2 * k);
-        bad = pr.bad || pr.idx == -1;  // -1: no block with mass (no finite logit)
-        tok = pr.idx;                   // winning block of the bonus race, or -2
-      }
-    }
-    if (__any_sync(0xffffffffu, bad != 0u)) rs = kStNonfinite;
-  }
-  if (rs) {
-    write_skipped(P, r, d0, k, rs, lane);
-    return;
-  }
-  const uint32_t rej = __ballot_sync(0xffffffffu, lane < k && !accept);
-  const int A = rej ? __ffs(rej) - 1 : k;
-  const int tok_at_A = __shfl_sync(0xffffffffu, tok, A);
-  // the committed extra token: greedy argmax, bonus draw, or (pending) residual
-  int token = -1;
-  bool pending = false;
-  if (mode == kGreedy) {
-    token = tok_at_A;
-  } else {
-    const RequestKey rk = request_key(P, r);
-    const float c = kLog2e / t;
-    const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(t0 + A) * row_bytes;
-    const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + A) * row_bytes;
-    ResidualRow rr{c, 0.f, 0.f, 0.f, 0.f};
-    if (A == k) {
-      // bonus: the block race ran in the row pass (index -2: not block aligned)
-      if (tok_at_A >= 0) {
-        token = inner_race<E, false>(P, trow, nullptr, tok_at_A, rr, (uint32_t)k, rk);
-      } else {
-        const BestAcc br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)k, rk);
-        if (br.nan || br.idx < 0) {
-          write_skipped(P, r, d0, k, kStNonfinite, lane);
-          return;
-        }
-        token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)k, rk);
-      }
-    } else if (row_fast<E>(trow, P.vocab) && row_fast<E>(drow, P.vocab)) {
-      pending = true;  // a residual job draws the token
-    } else {
-      const Partial pt = ld_cg(P.rowres + n0 + 2 * A);
-      const Partial pd = ld_cg(P.rowres + n0 + 2 * A + 1);
-      rr = ResidualRow{c, pt.a, 1.f / pt.b, pd.a, 1.f / pd.b};
-      BestAcc br = slow_block_race<E, true>(P, trow, drow, rr, (uint32_t)A, rk);
-      if (br.idx >= 0) {
-        token = inner_race<E, true>(P, trow, drow, br.idx, rr, (uint32_t)A, rk);
-      } else {
-        // the residual has no mass (p == q): draw from p_j instead
-        rr = ResidualRow{c, 0.f, 0.f, 0.f, 0.f};
-        br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)A, rk);
-        token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)A, rk);
-      }
-    }
-  }
-  if (lane < width) {  // width = max_k + 1 <= 32; lane i holds y_i
-    const int v = lane < A ? y : (lane == A ? token : -1);
+  if (lane < width) {  // width <= 32
+    const int v = lane < A ? P.tokens[d0 + lane] : (lane == A && !pending ? token : -1);
     P.committed[(size_t)r * width + lane] = v;
   }
   const float nan = __int_as_float(0x7fc00000);
   if (lane < k) {
     P.flags[d0 + lane] = lane < A ? 1 : 0;
-    if (P.p_y) P.p_y[d0 + lane] = mode == kSampling ? py : nan;
-    if (P.q_y) P.q_y[d0 + lane] = mode == kSampling ? qy : nan;
-    if (P.u_dbg) P.u_dbg[d0 + lane] = mode == kSampling ? u : nan;
+    if (lane > A) {
+      if (P.p_y) P.p_y[d0 + lane] = nan;
+      if (P.q_y) P.q_y[d0 + lane] = nan;
+      if (P.u_dbg) P.u_dbg[d0 + lane] = nan;
+    }
   }
   if (lane == 0) {
     P.accepted_len[r] = A;
     if (P.req_status) P.req_status[r] = 0;
     if (pending) publish_job(P, r, A);
+    __threadfence();
+    *reinterpret_cast<volatile uint32_t*>(P.done + r) = P.epoch;
+    atomicAdd(P.ctr + kCntReqDone, 1);
+  }
+}
+
+// A request that cannot be verified: -1 outputs, flags 0, NaN debug values.
+__device__ void skip_request(const Params& P, int r, int d0, int k, uint32_t rs) {
+  const int lane = threadIdx.x & 31;
+  const int width = P.max_k + 1;
+  if (lane < width) P.committed[(size_t)r * width + lane] = -1;
+  const float nan = __int_as_float(0x7fc00000);
+  if (lane < k) {
+    P.flags[d0 + lane] = 0;
+    if (P.p_y) P.p_y[d0 + lane] = nan;
+    if (P.q_y) P.q_y[d0 + lane] = nan;
+    if (P.u_dbg) P.u_dbg[d0 + lane] = nan;
+  }
+  if (lane == 0) {
+    P.accepted_len[r] = -1;
+    if (P.req_status) P.req_status[r] = (int32_t)rs;
+    atomicOr(reinterpret_cast<unsigned int*>(P.ctr + kCntStatus), rs);
+    __threadfence();
+    *reinterpret_cast<volatile uint32_t*>(P.done + r) = P.epoch;
+    atomicAdd(P.ctr + kCntReqDone, 1);
+  }
+}
+
+// Decides position i of request r (the control warp; its rows are merged and
+// positions 0..i-1 were accepted).  "Speculative Decoding: Medusa, MTP, EAGLE,
+// DFlash, DDTree, and DSpark", section 1: accept y_i with probability
+// min(1, p_i(y_i)/q_i(y_i)), tested as u_i q_i(y_i) < p_i(y_i); at the first
+// rejection draw from [p_i - q_i]_+, after k acceptances draw the bonus from
+// p_k; greedy rounds keep y_i while it equals the target argmax.  Returns true
+// when position i was accepted and position i+1 comes next.
+template <typename E>
+__device__ bool decide_position(const Params& P, int r, int i, const int* s_doff) {
+  const int lane = threadIdx.x & 31;
+  const int d0 = s_doff[r];
+  const int k = s_doff[r + 1] - d0;
+  const float t = __ldg(P.temperature + r);
+  const int mode = req_mode(t);
+  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
+
+  if (i == 0) {
+    // inputs are checked once, before the first decision
+    uint32_t rs = 0u;
+    if (mode == kBadTemp) rs |= kStBadTemp;
+    if (lane < k) {
+      const int y = P.tokens[d0 + lane];
+      if (y < 0 || y >= P.vocab) rs |= kStBadToken;
+    }
+    if (!rs && mode == kSampling && k > 0 && P.draft == nullptr) rs |= kStNoDraft;
+    rs = __reduce_or_sync(0xffffffffu, rs);
+    if (rs) {
+      skip_request(P, r, d0, k, rs);
+      return false;
+    }
+  }
+  const Partial pt = ld_cg(P.rowres + slot_of(P, i, r, 0));
+  if (mode == kGreedy) {
+    if (pt.bad) {
+      skip_request(P, r, d0, k, kStNonfinite);
+      return false;
+    }
+    if (i < k && P.tokens[d0 + i] == pt.idx) return true;
+    finish_request(P, r, d0, k, i, pt.idx, false);
+    return false;
+  }
+  const RequestKey rk = request_key(P, r);
+  const float c = kLog2e / t;
+  const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + i) * row_bytes;
+  ResidualRow rr{c, 0.f, 0.f, 0.f, 0.f};
+  if (i == k) {
+    // every draft accepted: the bonus draw (block race done in the row pass,
+    // index -2 when the row is left to the slow path)
+    int token = -1;
+    if (pt.bad || pt.idx == -1) {
+      skip_request(P, r, d0, k, kStNonfinite);
+      return false;
+    }
+    if (pt.idx >= 0) {
+      token = inner_race<E, false>(P, trow, nullptr, pt.idx, rr, (uint32_t)k, rk);
+    } else {
+      const BestAcc br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)k, rk);
+      if (br.nan || br.idx < 0) {
+        skip_request(P, r, d0, k, kStNonfinite);
+        return false;
+      }
+      token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)k, rk);
+    }
+    finish_request(P, r, d0, k, k, token, false);
+    return false;
+  }
+  const Partial pd = ld_cg(P.rowres + slot_of(P, i, r, 1));
+  if (pt.bad || pd.bad) {
+    skip_request(P, r, d0, k, kStNonfinite);
+    return false;
+  }
+  const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + i) * row_bytes;
+  const int y = P.tokens[d0 + i];
+  const float tp = fmaf(E::load1(trow, y), c, -pt.a);  // log2(p(y) S_p)
+  const float tq = fmaf(E::load1(drow, y), c, -pd.a);  // log2(q(y) S_q)
+  const float u = accept_uniform(P.key, (uint32_t)i, rk.lo, rk.hi);
+  // u q(y) < p(y), both sides scaled by S_p S_q 2^-max(tp, tq) > 0
+  bool accept;
+  if (tp == kNegInf) {
+    accept = false;
+  } else if (tq == kNegInf) {
+    accept = true;
+  } else {
+    const float mx = fmaxf(tp, tq);
+    accept = u * (fast_ex2(tq - mx) * pt.b) < fast_ex2(tp - mx) * pd.b;
+  }
+  if (lane == 0) {
+    if (P.p_y) P.p_y[d0 + i] = fast_ex2(tp) / pt.b;
+    if (P.q_y) P.q_y[d0 + i] = fast_ex2(tq) / pd.b;
+    if (P.u_dbg) P.u_dbg[d0 + i] = u;
+  }
+  if (accept) return true;
+  // first rejection at i: the residual draw
+  if (row_fast<E>(trow, P.vocab) && row_fast<E>(drow, P.vocab)) {
+    finish_request(P, r, d0, k, i, -1, true);  // a residual job draws the token
+    return false;
+  }
+  rr = ResidualRow{c, pt.a, 1.f / pt.b, pd.a, 1.f / pd.b};
+  BestAcc br = slow_block_race<E, true>(P, trow, drow, rr, (uint32_t)i, rk);
+  int token;
+  if (br.idx >= 0) {
+    token = inner_race<E, true>(P, trow, drow, br.idx, rr, (uint32_t)i, rk);
+  } else {
+    // the residual has no mass (p == q): draw from p_i instead
+    rr = ResidualRow{c, 0.f, 0.f, 0.f, 0.f};
+    br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)i, rk);
+    token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)i, rk);
+  }
+  finish_request(P, r, d0, k, i, token, false);
+  return false;
+}
+
+// Counts one merged row (or the accept signal) towards position i of request
+// r; whoever completes the count decides, and an acceptance signals the next
+// position, which may already have all its rows.
+template <typename E>
+__device__ void count_position(const Params& P, int r, int i, const int* s_doff) {
+  const int lane = threadIdx.x & 31;
+  const int d0 = s_doff[r];
+  const int k = s_doff[r + 1] - d0;
+  const int mode = req_mode(__ldg(P.temperature + r));
+  const int width = P.max_k + 1;
+  for (;;) {
+    uint32_t cnt = 0;
+    if (lane == 0) cnt = epoch_add(P.pos_cnt + (size_t)r * width + i, P.epoch);
+    cnt = __shfl_sync(0xffffffffu, cnt, 0);
+    if (cnt != position_target(P, i, k, mode)) return;
+    __threadfence();
+    if (!decide_position<E>(P, r, i, s_doff)) return;
+    ++i;  // accepted: signal position i + 1
   }
 }
 
@@ -817,33 +867,30 @@ struct Ctrl {
   int spins;
 };
 
-// Keep P.fill items queued ahead of q_used (lane 0 claims and decodes).
+// Keep P.fill items queued ahead of q_used.  Items are claimed up to 8 at a
+// time and decoded by separate lanes; items of decided requests are dropped.
 template <typename E>
 __device__ __forceinline__ void fill_queue(const Params& P, const int* s_doff, QItem* queue,
-                                           int* s_qend, Ctrl& cs) {
+                                           int* s_qend, Ctrl& cs, int n_items) {
   const int lane = threadIdx.x & 31;
   while (!cs.exhausted && cs.q_head < cs.q_used + P.fill) {
-    const int need = cs.q_used + P.fill - cs.q_head;
+    const int room = kQueue - 1 - (cs.q_head - cs.q_used);
+    const int grab = min(8, room);
     int base = 0;
-    if (lane == 0) base = atomicAdd(P.ctr + kCntItems, need);
+    if (lane == 0) base = atomicAdd(P.ctr + kCntItems, grab);
     base = __shfl_sync(0xffffffffu, base, 0);
-    for (int i = 0; i < need; ++i) {
-      const int item = base + i;
-      if (item >= P.n_items) {
-        cs.exhausted = true;
-        break;
-      }
-      int kept = 0;
-      if (lane == 0) {
-        QItem it;
-        decode_item<E>(P, s_doff, item, it);
-        if (it.kind != kSkip) {
-          queue[cs.q_head & (kQueue - 1)] = it;
-          kept = 1;
-        }
-      }
-      cs.q_head += __shfl_sync(0xffffffffu, kept, 0);
+    const int item = base + lane;
+    bool keep = false;
+    QItem it;
+    if (lane < grab && item < n_items) {
+      decode_item<E>(P, s_doff, item, it);
+      keep = it.kind != kSkip &&
+             *reinterpret_cast<const volatile uint32_t*>(P.done + it.r) != P.epoch;
     }
+    const uint32_t mask = __ballot_sync(0xffffffffu, keep);
+    if (keep) queue[(cs.q_head + __popc(mask & ((1u << lane) - 1u))) & (kQueue - 1)] = it;
+    cs.q_head += __popc(mask);
+    if (base + grab >= n_items) cs.exhausted = true;
   }
   __syncwarp();
   if (lane == 0) {
@@ -859,7 +906,6 @@ __device__ __forceinline__ void make_job(const Params& P, const int* s_doff, int
                                          int j, int ch, Job& jb) {
   const size_t row_bytes = (size_t)P.vocab * E::kBytes;
   const int d0 = s_doff[r];
-  const int n0 = r + 2 * d0;
   jb.trow = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + j) * row_bytes;
   jb.drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + j) * row_bytes;
   jb.slot = slot;
@@ -871,8 +917,8 @@ __device__ __forceinline__ void make_job(const Params& P, const int* s_doff, int
   jb.req_lo = rk.lo;
   jb.req_hi = rk.hi;
   __threadfence();
-  const Partial rt = ld_cg(P.rowres + n0 + 2 * j);
-  const Partial rd = ld_cg(P.rowres + n0 + 2 * j + 1);
+  const Partial rt = ld_cg(P.rowres + slot_of(P, j, r, 0));
+  const Partial rd = ld_cg(P.rowres + slot_of(P, j, r, 1));
   jb.mp = rt.a;
   jb.inv_sp = 1.f / rt.b;
   jb.mq = rd.a;
@@ -917,7 +963,7 @@ __device__ void complete_item(const Params& P, const int* s_doff, const QItem& i
   if (lane == 0) {
     P.part[it.item] = p;
     __threadfence();
-    last = (atomicAdd(P.row_cnt + it.n, 1) == P.nch - 1) ? 1 : 0;
+    last = (epoch_add(P.row_cnt + it.n, P.epoch) == (uint32_t)P.nch) ? 1 : 0;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
@@ -954,25 +1000,12 @@ __device__ void complete_item(const Params& P, const int* s_doff, const QItem& i
                                       : (a.nan != 0u || a.idx < 0 || !(a.v < 3.0e38f));
     res = Partial{a.v, 0.f, a.idx, bad ? 1u : 0u};
   }
-  int last_row = 0;
   if (lane == 0) {
     P.rowres[it.n] = res;
-    P.row_cnt[it.n] = 0;
     __threadfence();
-    const int d0 = s_doff[it.r];
-    const int k = s_doff[it.r + 1] - d0;
-    const int need = rows_of_request(P, k, req_mode(__ldg(P.temperature + it.r)));
-    last_row = (atomicAdd(P.req_cnt + it.r, 1) == need - 1) ? 1 : 0;
   }
-  last_row = __shfl_sync(0xffffffffu, last_row, 0);
-  if (!last_row) return;
-  __threadfence();
-  scan_request<E>(P, it.r, s_doff);
-  if (lane == 0) {
-    P.req_cnt[it.r] = 0;
-    __threadfence();
-    atomicAdd(P.ctr + kCntReqDone, 1);
-  }
+  __syncwarp();
+  count_position<E>(P, it.r, it.pos, s_doff);
 }
 
 // Completion of a job unit: the last chunk merges the block race, runs the
@@ -1008,15 +1041,14 @@ __device__ void complete_job(const Params& P, const int* s_doff, const JobRef& j
   a = warp_reduce(a);
   const size_t row_bytes = (size_t)P.vocab * E::kBytes;
   const int d0 = s_doff[jb.r];
-  const int n0 = jb.r + 2 * d0;
   const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + jb.r + jb.j) * row_bytes;
   const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + jb.j) * row_bytes;
   const float c = kLog2e / __ldg(P.temperature + jb.r);
   const RequestKey rk = request_key(P, jb.r);
   int token;
   if (a.idx >= 0) {
-    const Partial pt = ld_cg(P.rowres + n0 + 2 * jb.j);
-    const Partial pd = ld_cg(P.rowres + n0 + 2 * jb.j + 1);
+    const Partial pt = ld_cg(P.rowres + slot_of(P, jb.j, jb.r, 0));
+    const Partial pd = ld_cg(P.rowres + slot_of(P, jb.j, jb.r, 1));
     const ResidualRow rr{c, pt.a, 1.f / pt.b, pd.a, 1.f / pd.b};
     token = inner_race<E, true>(P, trow, drow, a.idx, rr, (uint32_t)jb.j, rk);
   } else {
@@ -1043,6 +1075,7 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
   __shared__ Partial mailbox[2][kComputeWarps];
   __shared__ int s_w[kBlock / 32 + 1];
   __shared__ int s_qend;
+  __shared__ int s_kmax;
   __shared__ uint32_t s_layout;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -1050,7 +1083,10 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
   const bool control = warp == kComputeWarps;
 
   // --- prefix sums of num_draft, and the layout check (all threads) -----------
-  if (tid == 0) s_layout = 0u;
+  if (tid == 0) {
+    s_layout = 0u;
+    s_kmax = 0;
+  }
   __syncthreads();
   int carry = 0;
   for (int base = 0; base < P.batch; base += kBlock) {
@@ -1059,6 +1095,7 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
     const bool badk = k < 0 || k > P.max_k;
     if (badk) atomicOr(&s_layout, kStBadK);
     const int kk = badk ? 0 : k;
+    if (kk > 0) atomicMax(&s_kmax, kk);
     int v = kk;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -1089,6 +1126,8 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
   }
   __syncthreads();
   const uint32_t layout = s_layout;
+  // waves 0..max_k of this batch, two slots per request each
+  const int n_items = (s_kmax + 1) * 2 * P.batch * P.nch;
 
   if (layout) {
     // untrustworthy layout: nothing is verified; CTA 0 reports it
@@ -1118,7 +1157,7 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
     int cur_type = kUnitIdle, cur_qidx = 0;
     JobRef cur_job{0, 0, 0, 0};
     if (control) {
-      fill_queue<E>(P, s_doff, queue, &s_qend, cs);
+      fill_queue<E>(P, s_doff, queue, &s_qend, cs, n_items);
       if (lane == 0) s_unit[0].type = kUnitIdle;
     }
     __syncthreads();
@@ -1174,7 +1213,7 @@ __global__ void __maxnreg__(128) sv_verify(Params P) {
           complete_job<E>(P, s_doff, prev_job, mailbox[(u - 1) & 1]);
         }
         // keep the items the compute warps may stream during unit u+1 queued
-        fill_queue<E>(P, s_doff, queue, &s_qend, cs);
+        fill_queue<E>(P, s_doff, queue, &s_qend, cs, n_items);
         // next unit: a claimable job first, then the next queued item
         int next_type = kUnitIdle;
         if (lane == 0) {

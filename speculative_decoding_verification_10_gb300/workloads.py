@@ -118,18 +118,31 @@ class Batch:
         d = np.concatenate([[0], np.cumsum(k)])
         return t, d
 
-    def algorithmic_bytes(self) -> int:
-        """Logit bytes the verify step must read once, plus its inputs and outputs.
+    def io_bytes(self) -> int:
+        """Bytes of the small inputs and the outputs of one round."""
+        k = self.num_draft.cpu().numpy().astype(np.int64)
+        io_in = 4 * self.batch * 2 + 4 * int(k.sum())
+        io_out = 4 * self.batch + 4 * self.batch * (self.max_k + 1) + int(k.sum())
+        return io_in + io_out
 
-        A sampling request reads its 2k+1 rows, a greedy one its k+1 target rows.
-        """
+    def full_window_bytes(self) -> int:
+        """Logit bytes of every row of the batch a round could read: 2k+1 rows per
+        sampling request, k+1 per greedy one."""
         k = self.num_draft.cpu().numpy().astype(np.int64)
         t = self.temperature.cpu().numpy()
         es = 4 if self.dtype == "f32" else 2
-        rows = np.where(t > 0, 2 * k + 1, k + 1).sum()
-        io_in = 4 * self.batch * 2 + 4 * int(k.sum())
-        io_out = 4 * self.batch + 4 * self.batch * (self.max_k + 1) + int(k.sum())
-        return int(rows) * self.vocab * es + io_in + io_out
+        return int(np.where(t > 0, 2 * k + 1, k + 1).sum()) * self.vocab * es
+
+    def needed_bytes(self, accepted_len) -> int:
+        """Logit bytes a round must read given its outcome: positions 0..A of each
+        request (target and draft rows when sampling, target rows when greedy), plus
+        the bonus row when A = k.  Rows after the first rejection are never needed."""
+        k = self.num_draft.cpu().numpy().astype(np.int64)
+        t = self.temperature.cpu().numpy()
+        A = np.asarray(accepted_len, dtype=np.int64)
+        es = 4 if self.dtype == "f32" else 2
+        rows = np.where(t > 0, np.where(A < k, 2 * (A + 1), 2 * k + 1), A + 1)
+        return int(rows.sum()) * self.vocab * es
 
     def verified_rows(self) -> int:
         """Target positions verified per batch: sum_r (k_r + 1)."""

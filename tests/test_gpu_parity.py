@@ -200,6 +200,29 @@ def test_all_zero_drafts_and_empty_batch():
         assert res.accepted_len.numel() == 0
 
 
+def test_rows_after_the_first_rejection_do_not_matter():
+    """Garbage (NaN / +inf) in rows beyond the first rejection changes nothing:
+    those rows are never read."""
+    inp = cases.random_batch([5] * 48, [1.0] * 24 + [0.0] * 24, vocab=4096, sigma_d=2.5,
+                             dtype="bf16", seed=13)
+    with _verifier(inp, "bf16") as v:
+        base = parity.run_gpu(v, inp, 5)
+        A = base["accepted_len"]
+        k = inp["num_draft"]
+        t_off = np.concatenate([[0], np.cumsum(k + 1)])
+        d_off = np.concatenate([[0], np.cumsum(k)])
+        late = dict(inp)
+        late["target"], late["draft"] = inp["target"].copy(), inp["draft"].copy()
+        for r in range(48):
+            if A[r] + 1 <= k[r]:
+                late["target"][t_off[r] + A[r] + 1:t_off[r + 1]] = 0x7fc0   # bf16 NaN
+                late["draft"][d_off[r] + A[r] + 1:d_off[r + 1]] = 0x7f80    # bf16 +inf
+        g = parity.run_gpu(v, late, 5)
+    assert g["status"] == 0
+    assert (g["committed"] == base["committed"]).all()
+    assert (g["accepted_len"] == A).all()
+
+
 # --- invalid inputs: reported, skipped, never a fault --------------------------------
 
 def test_invalid_inputs_status_and_skip():
@@ -209,9 +232,12 @@ def test_invalid_inputs_status_and_skip():
     bad["tokens"][2] = 300              # request 1: token == V
     bad["tokens"][4] = -1               # request 2 (greedy): negative token
     bad["temperature"][3] = np.nan      # request 3
-    bad["target"][4 * 3 + 1, 7] = np.nan   # request 4: NaN in a target row
-    bad["draft"][5 * 2 + 1, 9] = np.inf    # request 5: +inf in a draft row
-    bad["target"][6 * 3 + 2, :] = -np.inf  # request 6: bonus row without a finite logit
+    bad["target"][4 * 3 + 0, 7] = np.nan   # request 4: NaN in its first target row
+    bad["draft"][5 * 2 + 0, 9] = np.inf    # request 5: +inf in its first draft row
+    # request 6: draft rows equal to the target rows (so both drafts are accepted
+    # and the bonus row is read), and a bonus row without a finite logit
+    bad["draft"][6 * 2:6 * 2 + 2] = bad["target"][6 * 3:6 * 3 + 2]
+    bad["target"][6 * 3 + 2, :] = -np.inf
     _check(bad, seeds=(1,))
     with _verifier(bad, "f32") as v:
         g = parity.run_gpu(v, bad, 1)
