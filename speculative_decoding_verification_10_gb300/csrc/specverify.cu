@@ -17,7 +17,8 @@ namespace {
 
 constexpr uint32_t kLiveMagic = 0x53564c56u;  // "SVLV"
 constexpr uint32_t kDeadMagic = 0x53564444u;  // "SVDD"
-constexpr int kMaxNper = 64;                   // 16-byte vectors per thread per chunk (224 KB of logits)
+constexpr int kMaxNper = 256;                  // 16-byte vectors per thread per chunk (896 KB of logits)
+constexpr size_t kJobChunkBytes = 128 * 1024;  // bytes of each row in one residual job chunk
 constexpr size_t kPartialBudget = size_t(256) << 20;
 constexpr int kSpinLimit = 1 << 16;
 
@@ -85,22 +86,36 @@ static size_t ring_bytes() {
   return sizeof(uint4) * sv::kStages * sv::kStageVecs * sv::kThreads;
 }
 
-// Vectors per thread per chunk (nper) and chunks per row (nch): the fewest
-// chunks of at most kMaxNper vectors per thread, balanced, and more (smaller)
-// chunks when the batch has too few rows to give every CTA two items.
-static void choose_chunks(const specverify_ctx* h, int batch, int total_draft, int* nper,
-                          int* nch) {
-  const long long nvec = std::max<long long>(1, (long long)h->vocab * h->elem_bytes / 16);
-  const long long rows = (long long)batch + 2LL * total_draft;
+// Balanced chunking of a row into n chunks: vectors per thread per chunk.
+static int chunk_nper(long long nvec, long long n) {
   const long long step = (long long)sv::kStageVecs * sv::kThreads;  // vectors per stage
-  long long n = (nvec + (long long)kMaxNper * sv::kThreads - 1) / ((long long)kMaxNper * sv::kThreads);
-  const long long n_max = std::max<long long>(1, std::min<long long>(h->max_nch, (nvec + step - 1) / step));
-  while (n < n_max && rows * n < 2LL * h->grid) ++n;
-  n = std::min(n, n_max);
-  // balanced chunk length, rounded up to whole stages
   const long long chv = ((nvec + n - 1) / n + step - 1) / step * step;
-  *nper = (int)(chv / sv::kThreads);
-  *nch = (int)((nvec + chv - 1) / chv);
+  return (int)(chv / sv::kThreads);
+}
+static int chunks_of(long long nvec, int nper) {
+  const long long chv = (long long)nper * sv::kThreads;
+  return (int)((nvec + chv - 1) / chv);
+}
+
+// Items: the fewest chunks per row (whole rows when possible) such that the
+// first wave -- a target and a draft row per request -- still gives every CTA
+// two items.  Residual jobs: chunks of about kJobChunkBytes of each row, and
+// at least as many as the items have.
+static void choose_chunks(const specverify_ctx* h, int batch, int* nper, int* nch, int* jnper,
+                          int* jnch) {
+  const long long nvec = std::max<long long>(1, (long long)h->vocab * h->elem_bytes / 16);
+  const long long step = (long long)sv::kStageVecs * sv::kThreads;
+  const long long n_max = std::max<long long>(1, std::min<long long>(h->max_nch, (nvec + step - 1) / step));
+  const long long rows0 = 2LL * batch;
+  long long n = (nvec + (long long)kMaxNper * sv::kThreads - 1) / ((long long)kMaxNper * sv::kThreads);
+  while (n < n_max && rows0 * n < 2LL * h->grid) ++n;
+  n = std::min(n, n_max);
+  *nper = chunk_nper(nvec, n);
+  *nch = chunks_of(nvec, *nper);
+  long long jn = std::max<long long>(1, ((long long)h->vocab * h->elem_bytes + kJobChunkBytes / 2) / kJobChunkBytes);
+  jn = std::min(std::max<long long>(jn, *nch), n_max);
+  *jnper = chunk_nper(nvec, jn);
+  *jnch = chunks_of(nvec, *jnper);
 }
 
 template <typename E>
@@ -150,7 +165,7 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.total_draft = total_draft;
   P.max_k = h->max_k;
   P.vocab = h->vocab;
-  choose_chunks(h, batch, total_draft, &P.nper, &P.nch);
+  choose_chunks(h, batch, &P.nper, &P.nch, &P.jnper, &P.jnch);
   {
     const int spi = P.nper / sv::kStageVecs;
     P.fill = std::min(sv::kQueue - 2, (sv::kStages - 1 + spi - 1) / spi + 1);
@@ -272,10 +287,10 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   const size_t o_rowcnt = carve(sizeof(unsigned long long) * h->max_rows);
   const size_t o_poscnt = carve(sizeof(unsigned long long) * (size_t)max_batch * (max_k + 1));
   const size_t o_done = carve(sizeof(uint32_t) * max_batch);
-  // job slots: one residual and at most one fallback job per request
-  const size_t o_slots = carve(sizeof(unsigned long long) * 2 * (size_t)max_batch);
-  const size_t o_part2 = carve(sizeof(sv::Partial) * 2 * (size_t)max_batch * h->max_nch);
-  const size_t o_rescnt = carve(sizeof(int) * 2 * (size_t)max_batch);
+  // job slots: at most one residual job per request
+  const size_t o_slots = carve(sizeof(unsigned long long) * (size_t)max_batch);
+  const size_t o_part2 = carve(sizeof(sv::Partial) * (size_t)max_batch * h->max_nch);
+  const size_t o_rescnt = carve(sizeof(int) * (size_t)max_batch);
   const size_t o_ctr = carve(sizeof(int) * sv::kCntCount);
   h->scratch_bytes = off;
   if (cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess) {

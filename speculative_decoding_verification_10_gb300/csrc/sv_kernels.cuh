@@ -54,7 +54,7 @@ constexpr int kStages = 8;
 constexpr int kStageVecs = 2;
 constexpr int kQueue = 16;                     // item queue entries (power of 2)
 constexpr int kMaxBatch = 4096;                // requests per launch
-constexpr int kResUnroll = 2;
+constexpr int kResUnroll = 4;
 
 enum RowKind : int { kSkip = -1, kSoftmax = 0, kArgmax = 1, kRace = 2 };
 enum ReqMode : int { kBadTemp = 0, kGreedy = 1, kSampling = 2 };
@@ -93,8 +93,10 @@ struct Params {
   const int64_t* request_ids;
   PhiloxKey key;
   int batch, total_draft, max_k, vocab;
-  int nch;      // chunks per row
+  int nch;      // chunks per row (items)
   int nper;     // 16-byte vectors per thread per chunk (multiple of kStageVecs)
+  int jnch;     // chunks per row of a residual job
+  int jnper;    // 16-byte vectors per thread per job chunk
   int fill;     // items kept claimed ahead: enough to cover kStages-1 stages, + 1
   int spin_limit;
   uint32_t epoch;  // this round's tag for completion counters and `done`
@@ -110,9 +112,9 @@ struct Params {
   unsigned long long* row_cnt;  // [slots] epoch | chunks merged
   unsigned long long* pos_cnt;  // [batch * (max_k + 1)] epoch | rows merged (+1 signal)
   uint32_t* done;      // [batch] epoch of the round that decided the request
-  unsigned long long* res_slots;  // [2 * batch] job words
-  Partial* part2;      // [2 * batch * nch]
-  int* res_cnt;        // [2 * batch]
+  unsigned long long* res_slots;  // [batch] job words
+  Partial* part2;      // [batch * jnch]
+  int* res_cnt;        // [batch]
   int* ctr;            // [kCntCount]
 };
 
@@ -595,7 +597,7 @@ __device__ __forceinline__ BestAcc item_race(const Params& P, const QItem* queue
 // ---------------------------------------------------------------------------
 template <typename E>
 __device__ BestAcc job_chunk(const Params& P, const Job& jb) {
-  const int chv = P.nper * kThreads;
+  const int chv = P.jnper * kThreads;
   Geom<E> g;
   g.init(jb.trow, P.vocab, jb.ch, chv);
   const uint4* tp = g.vecs(jb.trow);
@@ -638,10 +640,10 @@ __device__ __forceinline__ void publish_job(const Params& P, int r, int j) {
   const int slot = atomicAdd(P.ctr + kCntReserve, 1);
   const unsigned long long word = (unsigned long long)(uint32_t)r |
                                   ((unsigned long long)(uint32_t)j << 24) | (1ull << 31) |
-                                  ((unsigned long long)(uint32_t)P.nch << 32);
+                                  ((unsigned long long)(uint32_t)P.jnch << 32);
   __threadfence();
   atomicExch(P.res_slots + slot, word);
-  atomicAdd(P.ctr + kCntPublished, P.nch);
+  atomicAdd(P.ctr + kCntPublished, P.jnch);
 }
 
 // Outputs of a decided request (the control warp): accepted prefix, the extra
@@ -959,20 +961,27 @@ __device__ void complete_item(const Params& P, const int* s_doff, const QItem& i
                               const Partial* mb) {
   const int lane = threadIdx.x & 31;
   const Partial p = it.kind == kSoftmax ? combine_softmax(mb) : combine_best(mb);
-  int last = 0;
-  if (lane == 0) {
-    P.part[it.item] = p;
+  // a whole-row item is its own row result; chunks are merged by the last one
+  int last = 1;
+  if (P.nch > 1) {
+    if (lane == 0) {
+      P.part[it.item] = p;
+      __threadfence();
+      last = (epoch_add(P.row_cnt + it.n, P.epoch) == (uint32_t)P.nch) ? 1 : 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
     __threadfence();
-    last = (epoch_add(P.row_cnt + it.n, P.epoch) == (uint32_t)P.nch) ? 1 : 0;
   }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
   Partial res;
   if (it.kind == kSoftmax) {
     SoftmaxAcc a;
     a.init();
-    for (int q = lane; q < P.nch; q += 32) {
+    if (P.nch == 1 && lane == 0) {
+      a.m = p.a;
+      a.s = p.b;
+    }
+    for (int q = lane; P.nch > 1 && q < P.nch; q += 32) {
       const Partial pq = ld_cg(P.part + (size_t)it.n * P.nch + q);
       SoftmaxAcc b;
       b.m = pq.a;
@@ -985,7 +994,12 @@ __device__ void complete_item(const Params& P, const int* s_doff, const QItem& i
   } else {
     BestAcc a;
     a.init();
-    for (int q = lane; q < P.nch; q += 32) {
+    if (P.nch == 1 && lane == 0) {
+      a.v = p.a;
+      a.idx = p.idx;
+      a.nan = p.bad;
+    }
+    for (int q = lane; P.nch > 1 && q < P.nch; q += 32) {
       const Partial pq = ld_cg(P.part + (size_t)it.n * P.nch + q);
       BestAcc b;
       b.v = pq.a;
@@ -1021,17 +1035,17 @@ __device__ void complete_job(const Params& P, const int* s_doff, const JobRef& j
   const Partial p = combine_best(mb);
   int last = 0;
   if (lane == 0) {
-    P.part2[(size_t)jb.slot * P.nch + jb.ch] = p;
+    P.part2[(size_t)jb.slot * P.jnch + jb.ch] = p;
     __threadfence();
-    last = (atomicAdd(P.res_cnt + jb.slot, 1) == P.nch - 1) ? 1 : 0;
+    last = (atomicAdd(P.res_cnt + jb.slot, 1) == P.jnch - 1) ? 1 : 0;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   __threadfence();
   BestAcc a;
   a.init();
-  for (int q = lane; q < P.nch; q += 32) {
-    const Partial pq = ld_cg(P.part2 + (size_t)jb.slot * P.nch + q);
+  for (int q = lane; q < P.jnch; q += 32) {
+    const Partial pq = ld_cg(P.part2 + (size_t)jb.slot * P.jnch + q);
     BestAcc b;
     b.v = pq.a;
     b.idx = pq.idx;
