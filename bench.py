@@ -262,7 +262,7 @@ def measure_e2e(args, b, v, world, dev):
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    from speculative_decoding_verification_10_gb300 import Verifier, build, launches_per_run
+    from speculative_decoding_verification_10_gb300 import Verifier, build
     from speculative_decoding_verification_10_gb300 import workloads as W
 
     rank, world, local = dist_env()
@@ -321,7 +321,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks.mark("start")
     t_start.record(stream)
-    # the row-pass kernel of the first n_ev timed steps is bracketed by events
+    # the launches of each of the first n_ev timed rounds are bracketed by events
     v.set_timing_events(ev_s, ev_e)
     for i in range(args.steps):
         if i == n_ev:
@@ -383,14 +383,15 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "sv_verify", "kernel_ms": kernel_avg_ms,
+                     "kernel": "sv_wave", "kernel_ms": kernel_avg_ms,
+                     "window": "one round: sv_plan + sv_wave x (max_k + 1), back to back",
                      "alg_bytes_per_launch": rowpass_bytes,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clock_info,
-        "gpu_launches": launches_per_run() * args.steps,
+        "gpu_launches": v.launches_per_run() * args.steps,
     }
     print(json.dumps(line), flush=True)
     v.close()

@@ -181,8 +181,10 @@ int specverify_status(specverify_t h, int32_t *status_out);
 int specverify_set_timing_events(specverify_t h, int n, void *const *start_events,
                                  void *const *stop_events);
 
-/* Kernel launches one run makes (for launch accounting). */
-int specverify_launches_per_run(void);
+/* Kernel launches one run of handle h makes (for launch accounting): the plan
+ * launch and one wave launch per draft position 0..max_k, i.e. max_k + 2.
+ * Waves past the batch's own largest k return at once. */
+int specverify_launches_per_run(specverify_t h, int *launches_out);
 
 /* Free the handle and its device memory.  Further use returns _ERR_DESTROYED
  * only while the memory of the freed handle is not reused; do not use it. */

@@ -23,7 +23,7 @@ from . import _lib
 from ._lib import (CREATE_HOST_STAGING, STATUS_BAD_K, STATUS_BAD_TEMP, STATUS_BAD_TOKEN,
                    STATUS_BAD_TOTAL, STATUS_NO_DRAFT, STATUS_NONFINITE)
 
-__all__ = ["Verifier", "VerifyResult", "SpecVerifyError", "verify", "launches_per_run",
+__all__ = ["Verifier", "VerifyResult", "SpecVerifyError", "verify",
            "STATUS_BAD_TOKEN", "STATUS_BAD_K", "STATUS_BAD_TEMP", "STATUS_NONFINITE",
            "STATUS_BAD_TOTAL", "STATUS_NO_DRAFT"]
 
@@ -54,10 +54,6 @@ class VerifyResult:
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
-
-
-def launches_per_run() -> int:
-    return int(_lib.load().specverify_launches_per_run())
 
 
 class Verifier:
@@ -160,6 +156,13 @@ class Verifier:
         arr_e = (ctypes.c_void_p * max(n, 1))(*[ctypes.c_void_p(e.cuda_event) for e in stops])
         _check(self.lib.specverify_set_timing_events(self._h, n, arr_s, arr_e),
                "specverify_set_timing_events")
+
+    def launches_per_run(self) -> int:
+        """Kernel launches one run makes: the plan and one wave per position 0..max_k."""
+        n = ctypes.c_int()
+        _check(self.lib.specverify_launches_per_run(self._h, ctypes.byref(n)),
+               "specverify_launches_per_run")
+        return int(n.value)
 
     def status(self) -> int:
         """Status bits of the last run (waits for its stream)."""

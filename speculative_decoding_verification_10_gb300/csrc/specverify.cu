@@ -1,7 +1,8 @@
 // specverify.cu -- host side of the C ABI declared in include/specverify.h.
 //
-// Argument checking, scratch ownership and the single launch of a verify
-// round.  All device work lives in sv_kernels.cuh.
+// Argument checking, scratch ownership and the launches of a verify round
+// (a plan launch and one wave launch per draft position).  All device work
+// lives in sv_kernels.cuh.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -17,10 +18,6 @@ namespace {
 
 constexpr uint32_t kLiveMagic = 0x53564c56u;  // "SVLV"
 constexpr uint32_t kDeadMagic = 0x53564444u;  // "SVDD"
-constexpr int kMaxNper = 256;                  // 16-byte vectors per thread per chunk (896 KB of logits)
-constexpr size_t kJobChunkBytes = 128 * 1024;  // bytes of each row in one residual job chunk
-constexpr size_t kPartialBudget = size_t(256) << 20;
-constexpr int kSpinLimit = 1 << 16;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -42,20 +39,19 @@ struct DeviceGuard {
 struct specverify_ctx {
   uint32_t magic;
   int device, max_batch, max_k, vocab, dtype, elem_bytes;
-  int num_sms, grid, max_nch;
-  size_t max_rows, smem_bytes_max;
+  int num_sms, grid_aligned, grid_scalar;
   void* scratch;
   size_t scratch_bytes;
-  sv::Partial* part;
-  sv::Partial* rowres;
-  unsigned long long* row_cnt;
-  unsigned long long* pos_cnt;
-  uint32_t* done;
-  uint32_t epoch;
-  unsigned long long* res_slots;
-  sv::Partial* part2;
+  int* doff;
+  int* lists;
+  int* list_cnt;
+  sv::ResEntry* res;
   int* res_cnt;
+  unsigned long long* pos_cnt;
+  sv::Partial* part;
+  sv::Partial* rpart;
   int* ctr;
+  uint32_t epoch;
   // staging for specverify_run_host
   void* stage;
   char* st_target;
@@ -68,7 +64,7 @@ struct specverify_ctx {
   uint8_t* st_flags;
   cudaStream_t last_stream;
   bool last_run_empty;
-  // optional timing events around the verify kernel
+  // optional timing events around a round's launches
   int n_events;
   unsigned long long run_counter;
   cudaEvent_t ev_start[64];
@@ -86,47 +82,34 @@ static size_t ring_bytes() {
   return sizeof(uint4) * sv::kStages * sv::kStageVecs * sv::kThreads;
 }
 
-// Balanced chunking of a row into n chunks: vectors per thread per chunk.
-static int chunk_nper(long long nvec, long long n) {
-  const long long step = (long long)sv::kStageVecs * sv::kThreads;  // vectors per stage
-  const long long chv = ((nvec + n - 1) / n + step - 1) / step * step;
-  return (int)(chv / sv::kThreads);
-}
-static int chunks_of(long long nvec, int nper) {
-  const long long chv = (long long)nper * sv::kThreads;
-  return (int)((nvec + chv - 1) / chv);
-}
-
-// Items: the fewest chunks per row (whole rows when possible) such that the
-// first wave -- a target and a draft row per request -- still gives every CTA
-// two items.  Residual jobs: chunks of about kJobChunkBytes of each row, and
-// at least as many as the items have.
-static void choose_chunks(const specverify_ctx* h, int batch, int* nper, int* nch, int* jnper,
-                          int* jnch) {
-  const long long nvec = std::max<long long>(1, (long long)h->vocab * h->elem_bytes / 16);
-  const long long step = (long long)sv::kStageVecs * sv::kThreads;
-  const long long n_max = std::max<long long>(1, std::min<long long>(h->max_nch, (nvec + step - 1) / step));
-  const long long rows0 = 2LL * batch;
-  long long n = (nvec + (long long)kMaxNper * sv::kThreads - 1) / ((long long)kMaxNper * sv::kThreads);
-  while (n < n_max && rows0 * n < 2LL * h->grid) ++n;
-  n = std::min(n, n_max);
-  *nper = chunk_nper(nvec, n);
-  *nch = chunks_of(nvec, *nper);
-  long long jn = std::max<long long>(1, ((long long)h->vocab * h->elem_bytes + kJobChunkBytes / 2) / kJobChunkBytes);
-  jn = std::min(std::max<long long>(jn, *nch), n_max);
-  *jnper = chunk_nper(nvec, jn);
-  *jnch = chunks_of(nvec, *jnper);
-}
-
+// The kernels of one dtype: the wave kernel for 16-byte aligned rows and the
+// scalar one for any other row layout.
 template <typename E>
-static int launch_round(specverify_ctx* h, const sv::Params& P, cudaStream_t s) {
-  const size_t smem = ring_bytes() + sizeof(int) * ((size_t)P.batch + 1);
-  const long long items = (long long)(h->max_k + 1) * 2 * P.batch * P.nch;
-  const int grid = (int)std::max<long long>(1, std::min<long long>(h->grid, items));
+struct Kernels {
+  static void* wave(bool aligned) {
+    return aligned ? reinterpret_cast<void*>(sv::sv_wave<E, true>)
+                   : reinterpret_cast<void*>(sv::sv_wave<E, false>);
+  }
+};
+
+// One round: the plan launch, then waves 0..max_k (a wave with nothing to do
+// returns at once).
+template <typename E>
+static int launch_round(specverify_ctx* h, sv::Params P, bool aligned, cudaStream_t s) {
   const int slot = h->n_events > 0 ? (int)(h->run_counter % (unsigned long long)h->n_events) : -1;
   h->run_counter++;
   if (slot >= 0 && cudaEventRecord(h->ev_start[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-  sv::sv_verify<E><<<grid, sv::kBlock, smem, s>>>(P);
+  sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
+  const size_t smem = aligned ? ring_bytes() : 0;
+  const int grid = aligned ? h->grid_aligned : h->grid_scalar;
+  for (int i = 0; i <= h->max_k; ++i) {
+    P.wave = i;
+    if (aligned) {
+      sv::sv_wave<E, true><<<grid, sv::kBlock, smem, s>>>(P);
+    } else {
+      sv::sv_wave<E, false><<<grid, sv::kBlock, smem, s>>>(P);
+    }
+  }
   if (slot >= 0 && cudaEventRecord(h->ev_stop[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
 }
@@ -154,6 +137,7 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
     return SPECVERIFY_ERR_INVALID_ARG;
 
   sv::Params P;
+  std::memset(&P, 0, sizeof P);
   P.target = target_logits;
   P.draft = total_draft > 0 ? draft_logits : nullptr;
   P.tokens = draft_tokens;
@@ -165,12 +149,13 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.total_draft = total_draft;
   P.max_k = h->max_k;
   P.vocab = h->vocab;
-  choose_chunks(h, batch, &P.nper, &P.nch, &P.jnper, &P.jnch);
-  {
-    const int spi = P.nper / sv::kStageVecs;
-    P.fill = std::min(sv::kQueue - 2, (sv::kStages - 1 + spi - 1) / spi + 1);
-  }
-  P.spin_limit = kSpinLimit;
+  P.epoch = ++h->epoch;  // never 0: 0 is the initial value of every tag
+  P.nb = (h->vocab + sv::kRaceBlock - 1) / sv::kRaceBlock;
+  P.nvec = (int)((size_t)h->vocab * h->elem_bytes / 16);
+  const int block_bytes = sv::kRaceBlock * h->elem_bytes;
+  P.min_span = std::max(1, sv::kMinSpanBytes / block_bytes);
+  P.min_span_res = std::max(1, sv::kMinSpanBytes / (2 * block_bytes));
+  P.stride = h->max_batch;
   P.accepted_len = accepted_len;
   P.committed = committed_tokens;
   P.flags = accept_flags;
@@ -178,21 +163,24 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.q_y = q_y;
   P.u_dbg = u;
   P.req_status = req_status;
-  P.part = h->part;
-  P.rowres = h->rowres;
-  P.row_cnt = h->row_cnt;
-  P.pos_cnt = h->pos_cnt;
-  P.done = h->done;
-  P.epoch = ++h->epoch;  // never 0: 0 is the initial value of every tag
-  P.res_slots = h->res_slots;
-  P.part2 = h->part2;
+  P.doff = h->doff;
+  P.lists = h->lists;
+  P.list_cnt = h->list_cnt;
+  P.res = h->res;
   P.res_cnt = h->res_cnt;
+  P.pos_cnt = h->pos_cnt;
+  P.part = h->part;
+  P.rpart = h->rpart;
   P.ctr = h->ctr;
+  // the vector path needs every row on a 16-byte boundary
+  const bool aligned = ((size_t)h->vocab * h->elem_bytes) % 16 == 0 &&
+                       ((uintptr_t)target_logits & 15u) == 0 &&
+                       ((uintptr_t)P.draft & 15u) == 0;
 
   DeviceGuard guard(h->device);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  rc = h->dtype == SPECVERIFY_BF16 ? launch_round<sv::BF16>(h, P, s)
-                                   : launch_round<sv::F32>(h, P, s);
+  rc = h->dtype == SPECVERIFY_BF16 ? launch_round<sv::BF16>(h, P, aligned, s)
+                                   : launch_round<sv::F32>(h, P, aligned, s);
   h->last_stream = s;
   h->last_run_empty = false;
   return rc;
@@ -230,50 +218,31 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   h->run_counter = 0;
 
   h->last_run_empty = true;
-  h->smem_bytes_max = ring_bytes() + sizeof(int) * ((size_t)max_batch + 1);
-  int occ = 0;
   bool ok = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) ==
             cudaSuccess;
-  if (dtype == SPECVERIFY_BF16) {
-    ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::BF16>,
-                                    cudaFuncAttributePreferredSharedMemoryCarveout,
-                                    cudaSharedmemCarveoutMaxShared) == cudaSuccess;
-    ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::BF16>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)h->smem_bytes_max) == cudaSuccess;
-    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sv::sv_verify<sv::BF16>,
-                                                             sv::kBlock, h->smem_bytes_max) ==
+  int occ_a = 0, occ_s = 0;
+  const size_t smem = ring_bytes();
+  for (int a = 0; a < 2 && ok; ++a) {
+    const void* fn = dtype == SPECVERIFY_BF16 ? Kernels<sv::BF16>::wave(a == 1)
+                                              : Kernels<sv::F32>::wave(a == 1);
+    const size_t sm = a == 1 ? smem : 0;
+    ok = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+    ok = ok && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) ==
                    cudaSuccess;
-  } else {
-    ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::F32>,
-                                    cudaFuncAttributePreferredSharedMemoryCarveout,
-                                    cudaSharedmemCarveoutMaxShared) == cudaSuccess;
-    ok = ok && cudaFuncSetAttribute(sv::sv_verify<sv::F32>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)h->smem_bytes_max) == cudaSuccess;
-    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sv::sv_verify<sv::F32>,
-                                                             sv::kBlock, h->smem_bytes_max) ==
-                   cudaSuccess;
+    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(a == 1 ? &occ_a : &occ_s, fn,
+                                                             sv::kBlock, sm) == cudaSuccess;
   }
-  if (!ok || occ < 1) {
+  if (!ok || occ_a < 1 || occ_s < 1) {
     cudaGetLastError();
     delete h;
     return SPECVERIFY_ERR_CUDA;
   }
-  // persistent grid: every CTA resident at once
-  h->grid = occ * h->num_sms;
-
-  // row slots: waves 0..max_k, a target and a draft slot per request each
-  h->max_rows = (size_t)max_batch * 2 * ((size_t)max_k + 1);
+  // one wave of CTAs, all resident at once
+  h->grid_aligned = occ_a * h->num_sms;
+  h->grid_scalar = occ_s * h->num_sms;
+  const int grid = std::max(h->grid_aligned, h->grid_scalar);
   const size_t row_bytes = (size_t)vocab * h->elem_bytes;
-  const size_t nvec = std::max<size_t>(1, row_bytes / 16);
-  const size_t min_chv = (size_t)sv::kStageVecs * sv::kThreads;
-  size_t max_nch = (nvec + min_chv - 1) / min_chv;
-  max_nch = std::min<size_t>(max_nch, std::max<size_t>(
-                                          (nvec + (size_t)kMaxNper * sv::kThreads - 1) /
-                                              ((size_t)kMaxNper * sv::kThreads),
-                                          kPartialBudget / sizeof(sv::Partial) / h->max_rows));
-  h->max_nch = (int)std::max<size_t>(1, max_nch);
 
   // one scratch allocation, carved into aligned pieces
   size_t off = 0;
@@ -282,15 +251,15 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
     off = align_up(off + bytes, 256);
     return o;
   };
-  const size_t o_part = carve(sizeof(sv::Partial) * h->max_rows * h->max_nch);
-  const size_t o_rowres = carve(sizeof(sv::Partial) * h->max_rows);
-  const size_t o_rowcnt = carve(sizeof(unsigned long long) * h->max_rows);
-  const size_t o_poscnt = carve(sizeof(unsigned long long) * (size_t)max_batch * (max_k + 1));
-  const size_t o_done = carve(sizeof(uint32_t) * max_batch);
-  // job slots: at most one residual job per request
-  const size_t o_slots = carve(sizeof(unsigned long long) * (size_t)max_batch);
-  const size_t o_part2 = carve(sizeof(sv::Partial) * (size_t)max_batch * h->max_nch);
-  const size_t o_rescnt = carve(sizeof(int) * (size_t)max_batch);
+  const size_t mb = (size_t)max_batch, waves = (size_t)max_k + 1;
+  const size_t o_doff = carve(sizeof(int) * (mb + 1));
+  const size_t o_lists = carve(sizeof(int) * waves * 2 * mb);
+  const size_t o_lcnt = carve(sizeof(int) * waves);
+  const size_t o_res = carve(sizeof(sv::ResEntry) * std::max<size_t>(max_k, 1) * mb);
+  const size_t o_rcnt = carve(sizeof(int) * std::max<size_t>(max_k, 1));
+  const size_t o_poscnt = carve(sizeof(unsigned long long) * waves * mb);
+  const size_t o_part = carve(sizeof(sv::Partial) * ((size_t)grid + 2 * mb));
+  const size_t o_rpart = carve(sizeof(sv::Partial) * ((size_t)grid + mb));
   const size_t o_ctr = carve(sizeof(int) * sv::kCntCount);
   h->scratch_bytes = off;
   if (cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess) {
@@ -305,16 +274,16 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
     return SPECVERIFY_ERR_CUDA;
   }
   char* b = static_cast<char*>(h->scratch);
-  h->part = reinterpret_cast<sv::Partial*>(b + o_part);
-  h->rowres = reinterpret_cast<sv::Partial*>(b + o_rowres);
-  h->row_cnt = reinterpret_cast<unsigned long long*>(b + o_rowcnt);
+  h->doff = reinterpret_cast<int*>(b + o_doff);
+  h->lists = reinterpret_cast<int*>(b + o_lists);
+  h->list_cnt = reinterpret_cast<int*>(b + o_lcnt);
+  h->res = reinterpret_cast<sv::ResEntry*>(b + o_res);
+  h->res_cnt = reinterpret_cast<int*>(b + o_rcnt);
   h->pos_cnt = reinterpret_cast<unsigned long long*>(b + o_poscnt);
-  h->done = reinterpret_cast<uint32_t*>(b + o_done);
-  h->epoch = 0u;
-  h->res_slots = reinterpret_cast<unsigned long long*>(b + o_slots);
-  h->part2 = reinterpret_cast<sv::Partial*>(b + o_part2);
-  h->res_cnt = reinterpret_cast<int*>(b + o_rescnt);
+  h->part = reinterpret_cast<sv::Partial*>(b + o_part);
+  h->rpart = reinterpret_cast<sv::Partial*>(b + o_rpart);
   h->ctr = reinterpret_cast<int*>(b + o_ctr);
+  h->epoch = 0u;
 
   h->stage = nullptr;
   if (flags & SPECVERIFY_CREATE_HOST_STAGING) {
@@ -443,7 +412,7 @@ int specverify_status(specverify_t h, int32_t* status_out) {
     return SPECVERIFY_OK;
   }
   if (cudaStreamSynchronize(h->last_stream) != cudaSuccess ||
-      cudaMemcpy(&st, h->ctr + sv::kCntLastStatus, sizeof st, cudaMemcpyDeviceToHost) !=
+      cudaMemcpy(&st, h->ctr + sv::kCntStatus, sizeof st, cudaMemcpyDeviceToHost) !=
           cudaSuccess) {
     cudaGetLastError();
     return SPECVERIFY_ERR_CUDA;
@@ -468,7 +437,13 @@ int specverify_set_timing_events(specverify_t h, int n, void* const* start_event
   return SPECVERIFY_OK;
 }
 
-int specverify_launches_per_run(void) { return 1; }
+int specverify_launches_per_run(specverify_t h, int* launches_out) {
+  int rc = check_handle(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (launches_out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
+  *launches_out = h->max_k + 2;  // the plan and one wave per position 0..max_k
+  return SPECVERIFY_OK;
+}
 
 int specverify_destroy(specverify_t h) {
   int rc = check_handle(h);

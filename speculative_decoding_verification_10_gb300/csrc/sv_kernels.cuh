@@ -1,46 +1,38 @@
-// sv_kernels.cuh -- the fused verify kernel: one persistent launch per round.
+// sv_kernels.cuh -- the verify round as a plan launch and one wave launch per
+// draft position.
 //
-// Left to right, and no further than needed.  A round verifies the positions
-// of each request left to right and discards everything after the first
-// rejection ("Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and
-// DSpark", section 1), so it only needs the rows of positions 0..A (and the
-// bonus row when all k are accepted).  Work is therefore ordered by position:
-// wave i holds, for every request, target row t_i and draft row d_i (slot
-// n = i * 2B + 2r + is_draft), each split into `nch` vocab chunks (item =
-// n * nch + chunk), claimed in increasing order from one global counter.  A
-// request that is already decided has its later items skipped at claim time.
+// Left to right, and no further than needed.  A round tests the draft
+// positions of each request left to right and discards everything after the
+// first rejection ("Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree,
+// and DSpark", section 1), so only the rows of positions 0..A are needed, plus
+// the bonus row when all k drafts are accepted.  The round is therefore run as
+// waves: wave i streams, for every request still alive at position i, target
+// row t_i and draft row d_i (sampling, i < k), the bonus row t_k (sampling,
+// i = k) or target row t_i (greedy), and decides position i of each of them.
+// An accepted request is appended to the list of wave i+1; a rejected one to
+// the residual list, whose rows t_i and d_i the next wave reads again (first,
+// while they may still sit in L2) to draw the correction token.
 //
-// Per item the CTA reduces its chunk to a 16-byte partial:
-//   sampling target row i < k, draft row i : softmax normaliser (m, S) of c*x,
-//                                            c = log2(e)/T   (p_i, q_i)
-//   sampling target row k                  : block race of the bonus draw
-//   greedy (or bad-temperature) target row : argmax (lowest index)
-// The CTA that completes a slot merges its partials and counts the slot
-// towards its position; position i of a request is decided by whichever CTA
-// brings that count to (rows of position i) + (1 if i > 0, the "position i-1
-// accepted" signal), so each position is decided exactly once, in order, as
-// soon as both its rows and its predecessor are done.  A rejection at j
-// publishes a residual job over rows t_j and d_j (still in L2), in nch chunks
-// any CTA may claim; jobs are claimed ahead of new items.  Completion
-// counters carry the round's epoch in their high word, so counters left
-// partial by skipped work need no reset.
+// Inside a wave the work is split flat: the wave's rows form one sequence of
+// race blocks (128 vocab ids), and CTA c takes the contiguous range
+// [c*T/G, (c+1)*T/G) of it, so every CTA streams the same number of bytes
+// whatever the row lengths.  A CTA's range cuts into a few row segments; each
+// segment reduces to one 16-byte partial.  The CTA that brings the count of a
+// request's segments to its total merges them and decides the position: no
+// CTA ever waits for another, there is no work claiming, and the segment
+// count of any row follows from the split arithmetic alone.
 //
-// CTA layout: 7 compute warps and 1 control warp, one __syncthreads per work
-// unit.  Compute warps stream the unit's bytes and leave one partial per warp
-// in shared memory.  During the next unit the control warp combines them and
-// does all latency-bound global work: partial stores, completion counters,
-// merges, decisions, claiming items and residual jobs.
+// CTA layout: 7 compute warps and 1 control warp, one __syncthreads per
+// segment.  Compute warps stream the segment and leave one partial per warp in
+// shared memory; during the next segment the control warp combines them and
+// does every latency-bound step: partial stores, the completion count, the
+// merge, the decision, the list appends and the outputs.
 //
-// Memory pipeline.  Each compute thread streams its 16-byte vectors of
-// successive items through a private ring of shared memory with cp.async
-// (kStages stages of kStageVecs vectors), kStages-1 stages ahead and across
-// item boundaries; it only reads back what it copied itself, and
-// cp.async.wait_group is a hardware wait.
-//
-// No CTA waits for another, except that the control warp of a CTA with no
-// work left polls the job queue for at most P.spin_limit rounds in all;
-// exiting is always safe because the CTA that publishes a job drains it
-// itself.  The last CTA to exit resets the shared counters for the next round.
+// Memory pipeline (16-byte aligned rows): each compute thread streams its
+// vectors of successive segments through a private shared-memory ring with
+// cp.async, kStages-1 stages ahead and across segment boundaries, and only
+// reads back what it copied itself.  Rows that are not 16-byte aligned take a
+// scalar path with the same structure.
 #pragma once
 
 #include "sv_device.cuh"
@@ -52,17 +44,25 @@ constexpr int kThreads = kComputeWarps * 32;   // compute threads
 constexpr int kBlock = kThreads + 32;          // + the control warp
 constexpr int kStages = 8;
 constexpr int kStageVecs = 2;
-constexpr int kQueue = 16;                     // item queue entries (power of 2)
-constexpr int kMaxBatch = 4096;                // requests per launch
-constexpr int kResUnroll = 4;
+constexpr int kQueue = 16;                     // segment queue entries (power of 2)
+constexpr int kMaxBatch = 4096;                // requests per round
+constexpr int kPlanThreads = 1024;
+constexpr int kRaceBlock = 128;                // vocab ids per race block
+constexpr int kMinSpanBytes = 16384;           // smallest share of a wave per CTA
 
-enum RowKind : int { kSkip = -1, kSoftmax = 0, kArgmax = 1, kRace = 2 };
+enum RowKind : int { kSoftmax = 0, kArgmax = 1, kRace = 2, kResidual = 3 };
 enum ReqMode : int { kBadTemp = 0, kGreedy = 1, kSampling = 2 };
-enum UnitType : int { kUnitEnd = 0, kUnitIdle = 1, kUnitItem = 2, kUnitResidual = 3 };
+enum UnitType : int { kUnitEnd = 0, kUnitItem = 1 };
 
 // Status bits (equal to the SPECVERIFY_STATUS_* values of the header).
 constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite = 8u,
                    kStBadTotal = 16u, kStNoDraft = 64u;
+
+// A list entry of wave i: request r, which row, and whether the target and
+// draft rows of that position come as an adjacent pair (target first).
+__device__ __forceinline__ int entry_of(int r, int is_draft, int paired) {
+  return (r << 2) | (is_draft << 1) | paired;
+}
 
 struct __align__(16) Partial {
   float a;       // softmax: m  | best: value
@@ -71,18 +71,15 @@ struct __align__(16) Partial {
   uint32_t bad;  // NaN seen
 };
 
-// Shared counters of a round (reset by the last CTA to exit).
-enum Counter : int {
-  kCntItems = 0,      // items claimed
-  kCntReserve = 1,    // job slots reserved
-  kCntPublished = 2,  // job chunks published
-  kCntClaimed = 3,    // job chunks claimed
-  kCntReqDone = 4,    // requests decided
-  kCntExit = 5,       // CTAs finished
-  kCntStatus = 6,     // status bits of this round
-  kCntLastStatus = 7, // status bits of the previous round
-  kCntCount = 8
+// A rejected request waiting for its correction draw (written by the deciding
+// CTA of wave j, read by wave j+1).
+struct __align__(16) ResEntry {
+  int r, j, d0, pad;
+  float c, mp, inv_sp, mq;
+  float inv_sq, pad2, pad3, pad4;
 };
+
+enum Counter : int { kCntStatus = 0, kCntCount = 4 };
 
 struct Params {
   const void* target;
@@ -93,13 +90,13 @@ struct Params {
   const int64_t* request_ids;
   PhiloxKey key;
   int batch, total_draft, max_k, vocab;
-  int nch;      // chunks per row (items)
-  int nper;     // 16-byte vectors per thread per chunk (multiple of kStageVecs)
-  int jnch;     // chunks per row of a residual job
-  int jnper;    // 16-byte vectors per thread per job chunk
-  int fill;     // items kept claimed ahead: enough to cover kStages-1 stages, + 1
-  int spin_limit;
-  uint32_t epoch;  // this round's tag for completion counters and `done`
+  int wave;          // the draft position this launch decides
+  uint32_t epoch;    // this round's tag of the completion counters
+  int nb;            // race blocks per row
+  int nvec;          // 16-byte vectors per row (aligned rows)
+  int min_span;      // fewest race blocks per CTA share of the row phase
+  int min_span_res;  // ... and of the residual phase
+  int stride;        // capacity of a request-indexed array (max_batch)
   int32_t* accepted_len;
   int32_t* committed;
   uint8_t* flags;
@@ -107,24 +104,20 @@ struct Params {
   float* q_y;
   float* u_dbg;
   int32_t* req_status;
-  Partial* part;       // [slots * nch], slots = (max_k + 1) * 2 * batch
-  Partial* rowres;     // [slots]
-  unsigned long long* row_cnt;  // [slots] epoch | chunks merged
-  unsigned long long* pos_cnt;  // [batch * (max_k + 1)] epoch | rows merged (+1 signal)
-  uint32_t* done;      // [batch] epoch of the round that decided the request
-  unsigned long long* res_slots;  // [batch] job words
-  Partial* part2;      // [batch * jnch]
-  int* res_cnt;        // [batch]
-  int* ctr;            // [kCntCount]
+  int* doff;                    // [stride + 1] draft-row offsets of the requests
+  int* lists;                   // [(max_k + 1) * 2 * stride] row entries of each wave
+  int* list_cnt;                // [max_k + 1]
+  ResEntry* res;                // [max(max_k, 1) * stride] rejections of each position
+  int* res_cnt;                 // [max(max_k, 1)]
+  unsigned long long* pos_cnt;  // [(max_k + 1) * stride] epoch | segments merged
+  Partial* part;                // [grid + 2 * stride] row segment partials
+  Partial* rpart;               // [grid + stride] residual segment partials
+  int* ctr;                     // [kCntCount]
 };
 
 __device__ __forceinline__ Partial ld_cg(const Partial* p) {
   const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
   return Partial{__int_as_float(v.x), __int_as_float(v.y), v.z, (uint32_t)v.w};
-}
-
-__device__ __forceinline__ int ld_volatile(const int* p) {
-  return *reinterpret_cast<const volatile int*>(p);
 }
 
 // Adds one to an epoch-tagged counter and returns the count of this epoch: a
@@ -149,179 +142,49 @@ __device__ __forceinline__ RequestKey request_key(const Params& P, int r) {
   return RequestKey{(uint32_t)id, (uint32_t)(id >> 32)};
 }
 
-// Aligned-vector geometry of a row and the vector range of chunk ch.
-template <typename E>
-struct Geom {
-  int head, nvec, tail, vbeg, vend;
-  __device__ __forceinline__ void init(const char* row, int vocab, int ch, int chv) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
-    int h = (int)(((16u - (uint32_t)(a & 15u)) & 15u) / E::kBytes);
-    if (h > vocab) h = vocab;
-    head = h;
-    nvec = (vocab - h) / E::kVec;
-    tail = vocab - h - nvec * E::kVec;
-    vbeg = ch * chv;
-    vend = min(nvec, vbeg + chv);
+// ---------------------------------------------------------------------------
+// The flat split of one phase of a wave: n rows of nb race blocks, T = n * nb
+// blocks over G CTAs; CTA c takes blocks [c*T/G, (c+1)*T/G).
+// ---------------------------------------------------------------------------
+struct Split {
+  unsigned long long T;
+  int G;
+  __device__ __forceinline__ void init(int n, int nb, int min_span, int grid) {
+    T = (unsigned long long)n * (unsigned long long)nb;
+    const unsigned long long g = T / (unsigned long long)min_span;
+    G = (int)(g < 1ull ? 1ull : (g > (unsigned long long)grid ? (unsigned long long)grid : g));
+    if (n == 0) G = 0;
   }
-  __device__ __forceinline__ const uint4* vecs(const char* row) const {
-    return reinterpret_cast<const uint4*>(row + (size_t)head * E::kBytes);
+  __device__ __forceinline__ unsigned long long begin(int c) const {
+    return (unsigned long long)c * T / (unsigned long long)G;
+  }
+  // the CTA whose share holds block x
+  __device__ __forceinline__ int cta_of(unsigned long long x) const {
+    return (int)(((x + 1ull) * (unsigned long long)G - 1ull) / T);
+  }
+  __device__ __forceinline__ int first_cta(int e, int nb) const {
+    return cta_of((unsigned long long)e * nb);
+  }
+  __device__ __forceinline__ int last_cta(int e, int nb) const {
+    return cta_of((unsigned long long)(e + 1) * nb - 1ull);
   }
 };
 
-// A claimed item, decoded once by the control warp.
+// A segment of the CTA's share, decoded once by the control warp.
 struct __align__(16) QItem {
-  const char* row;   // element 0 of the logit row
-  int item, n, r, kind, ch, pos;
-  float c;
-  int head, nvec, tail, vbeg, vend;
+  const char* row;   // the row (target row of a residual segment)
+  const char* row2;  // draft row of a residual segment
+  int kind;          // RowKind of this segment
+  int e;             // list (or residual list) entry
+  int r, d0, k, y;   // request, its draft offset, k, the draft token y_i (or -1)
+  int paired, is_draft;
+  int vbeg, vend;    // vectors (aligned rows) or race blocks (scalar path)
+  int nst;           // ring stages (aligned rows)
+  int g;             // partial index: CTA + entry
+  float c;           // log2(e) / T
+  float mp, inv_sp, mq, inv_sq;  // residual segments: normalisers of p_j and q_j
   uint32_t req_lo, req_hi;
 };
-
-// A residual (or fallback) job chunk.
-struct __align__(16) Job {
-  const char* trow;
-  const char* drow;
-  int slot, r, j, ch;
-  float c, mp, inv_sp, mq, inv_sq;
-  uint32_t req_lo, req_hi;
-};
-
-struct __align__(16) Unit {
-  int type;
-  int qidx;   // kUnitItem: queue entry
-  int pad[2];
-  Job job;    // kUnitResidual
-};
-
-// slot n = i * 2B + 2r + is_draft
-__device__ __forceinline__ int slot_of(const Params& P, int i, int r, int is_draft) {
-  return i * 2 * P.batch + 2 * r + is_draft;
-}
-
-template <typename E>
-__device__ __forceinline__ void decode_item(const Params& P, const int* s_doff, int item,
-                                            QItem& it) {
-  const int n = item / P.nch;
-  it.item = item;
-  it.n = n;
-  it.ch = item - n * P.nch;
-  const int i = n / (2 * P.batch);
-  const int rem = n - i * 2 * P.batch;
-  const int r = rem >> 1;
-  const bool is_draft = rem & 1;
-  const int d0 = s_doff[r];
-  const int k = s_doff[r + 1] - d0;
-  const float t = __ldg(P.temperature + r);
-  const int mode = req_mode(t);
-  it.r = r;
-  it.pos = i;
-  it.c = mode == kSampling ? kLog2e / t : 0.f;
-  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
-  if (i > k) {
-    it.kind = kSkip;
-    it.row = nullptr;
-  } else if (is_draft) {
-    it.kind = (mode == kSampling && i < k && P.draft != nullptr) ? kSoftmax : kSkip;
-    it.row = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + i) * row_bytes;
-  } else {
-    it.kind = mode == kSampling ? (i < k ? kSoftmax : kRace) : kArgmax;
-    it.row = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + i) * row_bytes;
-  }
-  it.head = it.nvec = it.tail = it.vbeg = it.vend = 0;
-  it.req_lo = it.req_hi = 0u;
-  if (it.kind != kSkip) {
-    Geom<E> g;
-    g.init(it.row, P.vocab, it.ch, P.nper * kThreads);
-    it.head = g.head;
-    it.nvec = g.nvec;
-    it.tail = g.tail;
-    it.vbeg = g.vbeg;
-    it.vend = g.vend;
-    const RequestKey rk = request_key(P, r);
-    it.req_lo = rk.lo;
-    it.req_hi = rk.hi;
-  }
-}
-
-// The count that decides position i of a request: its rows, plus the signal
-// that position i-1 was accepted (i > 0).
-__device__ __forceinline__ uint32_t position_target(const Params& P, int i, int k, int mode) {
-  const uint32_t rows = (mode == kSampling && i < k && P.draft != nullptr) ? 2u : 1u;
-  return rows + (i > 0 ? 1u : 0u);
-}
-
-// ---------------------------------------------------------------------------
-// The per-thread copy ring (compute threads).
-// ---------------------------------------------------------------------------
-template <typename E>
-struct LoadCursor {
-  int q;             // queue index of the item being loaded
-  int st;            // stage within it
-  const uint4* base;
-  int vbeg, vend;
-  bool active;
-
-  // s_qend: items the control warp has queued, or -1 - n once the supply is
-  // exhausted at n items.  The control warp keeps P.fill items queued beyond
-  // the unit being processed, which covers the kStages-1 stages the cursor
-  // runs ahead, so every entry the cursor opens is already written.
-  __device__ __forceinline__ void open(const QItem* queue, const int* s_qend) {
-    const int qe = *reinterpret_cast<const volatile int*>(s_qend);
-    __threadfence_block();
-    const int avail = qe >= 0 ? qe : -1 - qe;
-    active = q < avail;
-    if (active) {
-      const QItem& it = queue[q & (kQueue - 1)];
-      base = reinterpret_cast<const uint4*>(it.row + (size_t)it.head * E::kBytes);
-      vbeg = it.vbeg;
-      vend = it.vend;
-      st = 0;
-    }
-  }
-
-  // copy the next stage into ring slot `slot` and commit one group
-  __device__ __forceinline__ void issue(const Params& P, const QItem* queue, const int* s_qend,
-                                        uint4* ring, int slot) {
-    if (!active) open(queue, s_qend);
-    if (active) {
-#pragma unroll
-      for (int u = 0; u < kStageVecs; ++u) {
-        const int vi = vbeg + (st * kStageVecs + u) * kThreads + (int)threadIdx.x;
-        if (vi < vend) cp_async16(ring + (slot * kStageVecs + u) * kThreads + threadIdx.x, base + vi);
-      }
-    }
-    cp_async_commit();
-    if (active && ++st == P.nper / kStageVecs) {
-      ++q;
-      open(queue, s_qend);
-    }
-  }
-};
-
-// Streams the item's vectors out of the ring: for each stage, wait for it,
-// refill the ring one stage ahead, then hand the thread's vectors to f(x, e0).
-template <typename E, typename F>
-__device__ __forceinline__ void consume_item(const Params& P, const QItem* queue,
-                                             const int* s_qend, uint4* ring, LoadCursor<E>& lc,
-                                             int& g_stage, const QItem& it, F&& f) {
-  const int spi = P.nper / kStageVecs;
-  for (int st = 0; st < spi; ++st) {
-    cp_async_wait<kStages - 2>();
-    const int slot = g_stage % kStages;
-    uint4 v[kStageVecs];
-#pragma unroll
-    for (int u = 0; u < kStageVecs; ++u) v[u] = ring[(slot * kStageVecs + u) * kThreads + threadIdx.x];
-    lc.issue(P, queue, s_qend, ring, (g_stage + kStages - 1) % kStages);
-    ++g_stage;
-#pragma unroll
-    for (int u = 0; u < kStageVecs; ++u) {
-      const int vi = it.vbeg + (st * kStageVecs + u) * kThreads + (int)threadIdx.x;
-      float x[E::kVec];
-      E::unpack(vi < it.vend ? v[u] : E::pad(), x);
-      f(x, it.head + vi * E::kVec);
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Two-level exponential race: blocks of kRaceBlock vocab ids.  The block race
@@ -330,8 +193,6 @@ __device__ __forceinline__ void consume_item(const Params& P, const QItem* queue
 // argmax_v log2 w_v - log2 E1_v (stream 1, indexed by vocab id).  Lowest index
 // on ties at both levels.
 // ---------------------------------------------------------------------------
-constexpr int kRaceBlock = 128;
-
 __device__ __forceinline__ uint32_t race_word(uint32_t stream, int idx, uint32_t pos,
                                               RequestKey rk, PhiloxKey key) {
   const uint4 r = philox4x32_10(make_uint4((uint32_t)idx >> 2, pos, rk.lo, stream | (rk.hi << 8)), key);
@@ -362,7 +223,7 @@ struct GroupGains {
   static constexpr int kBlocksPerGroup = 32 * E::kVec / kRaceBlock;   // 2 (bf16) or 1 (fp32)
   static constexpr int kLanesPerBlock = kRaceBlock / E::kVec;          // 16 or 32
   float lo, hi;
-  // first element of group g of warp w, for a chunk starting at vector vbeg
+  // first element of group g of warp w, for a segment starting at vector vbeg
   __device__ static __forceinline__ int group_elem(int vbeg, int g, int w) {
     return (vbeg + g * kThreads + w * 32) * E::kVec;
   }
@@ -372,7 +233,16 @@ struct GroupGains {
     const int b = group_elem(vbeg, g0 + lane, w) / kRaceBlock;
     const uint4 r = philox4x32_10(make_uint4((uint32_t)b >> 2, pos, rk.lo, 2u | (rk.hi << 8)), key);
     lo = race_gain(word_of(r, b & 3));
-    hi = kBlocksPerGroup > 1 ? race_gain(word_of(r, (b & 3) + 1)) : lo;  // b is even here
+    hi = lo;
+    if (kBlocksPerGroup > 1) {
+      // a segment may start on an odd block: block b + 1 can open the next
+      // Philox counter
+      const int b1 = b + 1;
+      const uint4 r1 = (b1 & 3) ? r
+                                : philox4x32_10(make_uint4((uint32_t)b1 >> 2, pos, rk.lo,
+                                                           2u | (rk.hi << 8)), key);
+      hi = race_gain(word_of(r1, b1 & 3));
+    }
   }
   // the gain of this lane's block in group g (all lanes call it)
   __device__ __forceinline__ float get(int g) const {
@@ -465,202 +335,267 @@ __device__ __forceinline__ int inner_race(const Params& P, const char* trow, con
   return acc.idx;
 }
 
-// The whole two-level race over one row by one warp, with plain loads (rows
-// that are not 16-byte aligned, and the rare fallback).  Weights as in
-// inner_race.  Reports NaN / +inf in the row through acc.nan.
-template <typename E, bool kResid>
-__device__ BestAcc slow_block_race(const Params& P, const char* trow, const char* drow,
-                                   const ResidualRow& rr, uint32_t pos, RequestKey rk) {
+// The block race over a whole row by one warp with plain loads: the draw from
+// p_j when a residual turns out to have no mass (p == q in fp32).
+template <typename E>
+__device__ BestAcc warp_block_race(const Params& P, const char* trow, float c, uint32_t pos,
+                                   RequestKey rk) {
   const int lane = threadIdx.x & 31;
   const int nblocks = (P.vocab + kRaceBlock - 1) / kRaceBlock;
   BestAcc acc;
   acc.init();
   for (int b = lane; b < nblocks; b += 32) {
     const int v_end = min(P.vocab, (b + 1) * kRaceBlock);
-    float s = 0.f, m = kNegInf;
-    if (kResid) {
-      for (int v = b * kRaceBlock; v < v_end; ++v) {
-        const float p = fast_ex2(fmaf(E::load1(trow, v), rr.c, -rr.mp)) * rr.inv_sp;
-        const float q = fast_ex2(fmaf(E::load1(drow, v), rr.c, -rr.mq)) * rr.inv_sq;
-        s += fmaxf(p - q, 0.f);
-      }
-      m = 0.f;
-    } else {
-      for (int v = b * kRaceBlock; v < v_end; ++v) {
-        const float x = E::load1(trow, v);
-        acc.nan |= (x != x) || (x == -kNegInf);
-        m = fmaxf(m, x);
-      }
-      m *= rr.c;
-      if (m > kNegInf)
-        for (int v = b * kRaceBlock; v < v_end; ++v) s += fast_ex2(fmaf(E::load1(trow, v), rr.c, -m));
-    }
+    float m = kNegInf, s = 0.f;
+    for (int v = b * kRaceBlock; v < v_end; ++v) m = fmaxf(m, E::load1(trow, v));
+    m *= c;
+    if (m > kNegInf)
+      for (int v = b * kRaceBlock; v < v_end; ++v) s += fast_ex2(fmaf(E::load1(trow, v), c, -m));
     if (s > 0.f) acc.take(m + fast_lg2(s) + race_gain(race_word(2u, b, pos, rk, P.key)), b);
   }
-  acc = warp_reduce(acc);
-  return acc;
-}
-
-// Rows whose vector groups line up with the race blocks.
-template <typename E>
-__device__ __forceinline__ bool row_fast(const char* row, int vocab) {
-  return ((reinterpret_cast<uintptr_t>(row) & 15u) == 0u) && (vocab % E::kVec == 0);
+  return warp_reduce(acc);
 }
 
 // ---------------------------------------------------------------------------
-// Per-kind item reductions (compute threads, ring-fed).
+// The per-thread copy ring (compute threads, aligned rows).
 // ---------------------------------------------------------------------------
-template <typename E>
-__device__ __forceinline__ SoftmaxAcc item_softmax(const Params& P, const QItem* queue,
-                                                   const int* s_qend, uint4* ring,
-                                                   LoadCursor<E>& lc, int& gs, const QItem& it) {
-  LazySoftmax acc;
-  acc.init();
-  if (it.ch == 0 && (int)threadIdx.x < it.head) acc.add1(E::load1(it.row, threadIdx.x), it.c);
-  consume_item<E>(P, queue, s_qend, ring, lc, gs, it,
-                  [&](const float(&x)[E::kVec], int) { acc.add(x, it.c); });
-  if (it.ch == P.nch - 1 && (int)threadIdx.x < it.tail)
-    acc.add1(E::load1(it.row, it.head + it.nvec * E::kVec + threadIdx.x), it.c);
-  return acc.result();
+struct LoadCursor {
+  int q;   // queue index of the segment being loaded
+  int st;  // stage within it
+  const uint4* base;
+  const uint4* base2;
+  int vbeg, vend, nst;
+  bool pair, active;
+
+  // s_qend: segments the control warp has queued, or -1 - n once all n are.
+  __device__ __forceinline__ void open(const QItem* queue, const int* s_qend) {
+    const int qe = *reinterpret_cast<const volatile int*>(s_qend);
+    __threadfence_block();
+    const int avail = qe >= 0 ? qe : -1 - qe;
+    active = q < avail;
+    if (active) {
+      const QItem& it = queue[q & (kQueue - 1)];
+      base = reinterpret_cast<const uint4*>(it.row);
+      base2 = reinterpret_cast<const uint4*>(it.row2);
+      vbeg = it.vbeg;
+      vend = it.vend;
+      nst = it.nst;
+      pair = it.kind == kResidual;
+      st = 0;
+    }
+  }
+
+  // copy the next stage into ring slot `slot` and commit one group
+  __device__ __forceinline__ void issue(const QItem* queue, const int* s_qend, uint4* ring,
+                                        int slot) {
+    if (!active) open(queue, s_qend);
+    if (active) {
+      if (pair) {
+        const int vi = vbeg + st * kThreads + (int)threadIdx.x;
+        if (vi < vend) {
+          cp_async16(ring + (slot * kStageVecs + 0) * kThreads + threadIdx.x, base + vi);
+          cp_async16(ring + (slot * kStageVecs + 1) * kThreads + threadIdx.x, base2 + vi);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kStageVecs; ++u) {
+          const int vi = vbeg + (st * kStageVecs + u) * kThreads + (int)threadIdx.x;
+          if (vi < vend) cp_async16(ring + (slot * kStageVecs + u) * kThreads + threadIdx.x, base + vi);
+        }
+      }
+    }
+    cp_async_commit();
+    if (active && ++st == nst) {
+      ++q;
+      open(queue, s_qend);
+    }
+  }
+};
+
+// Reads one stage of the ring (after its copies landed) and refills the ring
+// one stage ahead.
+__device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend, uint4* ring,
+                                          LoadCursor& lc, int& g_stage, uint4 (&v)[kStageVecs]) {
+  cp_async_wait<kStages - 2>();
+  const int slot = g_stage % kStages;
+#pragma unroll
+  for (int u = 0; u < kStageVecs; ++u) v[u] = ring[(slot * kStageVecs + u) * kThreads + threadIdx.x];
+  lc.issue(queue, s_qend, ring, (g_stage + kStages - 1) % kStages);
+  ++g_stage;
 }
 
+// Streams a single-row segment: f(x, first id, vector group).
+template <typename E, typename F>
+__device__ __forceinline__ void consume_row(const QItem* queue, const int* s_qend, uint4* ring,
+                                            LoadCursor& lc, int& g_stage, const QItem& it, F&& f) {
+  for (int st = 0; st < it.nst; ++st) {
+    uint4 v[kStageVecs];
+    ring_take(queue, s_qend, ring, lc, g_stage, v);
+#pragma unroll
+    for (int u = 0; u < kStageVecs; ++u) {
+      const int vi = it.vbeg + (st * kStageVecs + u) * kThreads + (int)threadIdx.x;
+      float x[E::kVec];
+      E::unpack(vi < it.vend ? v[u] : E::pad(), x);
+      f(x, vi * E::kVec, st * kStageVecs + u);
+    }
+  }
+}
+
+// Streams a residual segment (rows t_j and d_j side by side): f(x, z, first id, group).
+template <typename E, typename F>
+__device__ __forceinline__ void consume_pair(const QItem* queue, const int* s_qend, uint4* ring,
+                                             LoadCursor& lc, int& g_stage, const QItem& it, F&& f) {
+  for (int st = 0; st < it.nst; ++st) {
+    uint4 v[kStageVecs];
+    ring_take(queue, s_qend, ring, lc, g_stage, v);
+    const int vi = it.vbeg + st * kThreads + (int)threadIdx.x;
+    float x[E::kVec], z[E::kVec];
+    E::unpack(vi < it.vend ? v[0] : E::pad(), x);
+    E::unpack(vi < it.vend ? v[1] : E::pad(), z);
+    f(x, z, vi * E::kVec, st);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Segment reductions (compute threads).  Each returns this thread's partial.
+// ---------------------------------------------------------------------------
 template <typename E>
-__device__ __forceinline__ BestAcc item_argmax(const Params& P, const QItem* queue,
-                                               const int* s_qend, uint4* ring, LoadCursor<E>& lc,
+__device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
+                                               const int* s_qend, uint4* ring, LoadCursor& lc,
                                                int& gs, const QItem& it) {
-  BestAcc acc;
-  acc.init();
-  if (it.ch == 0 && (int)threadIdx.x < it.head) {
-    const float x = E::load1(it.row, threadIdx.x);
-    acc.nan |= (x != x);
-    acc.take(x, threadIdx.x);
-  }
-  consume_item<E>(P, queue, s_qend, ring, lc, gs, it, [&](const float(&x)[E::kVec], int e0) {
-    float mx = x[0];
-    uint32_t nan = (x[0] != x[0]);
-#pragma unroll
-    for (int e = 1; e < E::kVec; ++e) {
-      mx = fmaxf(mx, x[e]);
-      nan |= (x[e] != x[e]);
-    }
-    acc.nan |= nan;
-    if (mx > acc.v) {
-      int first = 0;
-#pragma unroll
-      for (int e = E::kVec - 1; e >= 0; --e)
-        if (x[e] == mx) first = e;
-      acc.v = mx;
-      acc.idx = e0 + first;
-    }
-  });
-  if (it.ch == P.nch - 1 && (int)threadIdx.x < it.tail) {
-    const int e = it.head + it.nvec * E::kVec + threadIdx.x;
-    const float x = E::load1(it.row, e);
-    acc.nan |= (x != x);
-    acc.take(x, e);
-  }
-  return acc;
-}
-
-// Bonus race item: block race over the chunk's vector groups.  Rows that are
-// not block aligned stream through the ring without work and are raced later
-// by the slow path (partial index -2).
-template <typename E>
-__device__ __forceinline__ BestAcc item_race(const Params& P, const QItem* queue,
-                                             const int* s_qend, uint4* ring, LoadCursor<E>& lc,
-                                             int& gs, const QItem& it) {
-  BestAcc acc;
-  acc.init();
-  if (!(it.head == 0 && it.tail == 0)) {
-    consume_item<E>(P, queue, s_qend, ring, lc, gs, it, [&](const float(&)[E::kVec], int) {});
-    acc.idx = -2;
-    return acc;
-  }
   const int w = threadIdx.x >> 5;
   const RequestKey rk{it.req_lo, it.req_hi};
-  GroupGains<E> gg;
-  int g = 0;
-  consume_item<E>(P, queue, s_qend, ring, lc, gs, it, [&](const float(&x)[E::kVec], int e0) {
-    if ((g & 31) == 0) gg.make(it.vbeg, g, w, (uint32_t)it.pos, rk, P.key);
-    group_bonus<E>(acc, x, e0, it.c, gg.get(g));
-    ++g;
-  });
-  return acc;
-}
-
-// ---------------------------------------------------------------------------
-// Residual job chunk ("Speculative Decoding: Medusa, MTP, EAGLE, DFlash,
-// DDTree, and DSpark", section 1: at the first rejection, sample from the
-// normalised positive residual [p_j - q_j]_+): the block race over the chunk,
-// rows t_j and d_j read through L2 (both are block aligned: jobs are only
-// published for such rows).
-// ---------------------------------------------------------------------------
-template <typename E>
-__device__ BestAcc job_chunk(const Params& P, const Job& jb) {
-  const int chv = P.jnper * kThreads;
-  Geom<E> g;
-  g.init(jb.trow, P.vocab, jb.ch, chv);
-  const uint4* tp = g.vecs(jb.trow);
-  const uint4* dp = g.vecs(jb.drow);
-  const ResidualRow rr{jb.c, jb.mp, jb.inv_sp, jb.mq, jb.inv_sq};
-  const RequestKey rk{jb.req_lo, jb.req_hi};
-  const int w = threadIdx.x >> 5;
+  if (it.kind == kSoftmax) {
+    LazySoftmax acc;
+    acc.init();
+    consume_row<E>(queue, s_qend, ring, lc, gs, it,
+                   [&](const float(&x)[E::kVec], int, int) { acc.add(x, it.c); });
+    SoftmaxAcc a = warp_reduce(acc.result());
+    return Partial{a.m, a.s, -1, 0u};
+  }
   BestAcc acc;
   acc.init();
-  GroupGains<E> gg;
-  int gi = 0;
-  // uniform trip count across the compute warps (the shuffles need every lane)
-  for (int v0 = g.vbeg; v0 < g.vend; v0 += kThreads * kResUnroll) {
-    uint4 dt[kResUnroll], dd[kResUnroll];
+  if (it.kind == kArgmax) {
+    consume_row<E>(queue, s_qend, ring, lc, gs, it, [&](const float(&x)[E::kVec], int e0, int) {
+      float mx = x[0];
+      uint32_t nan = (x[0] != x[0]);
 #pragma unroll
-    for (int u = 0; u < kResUnroll; ++u) {
-      const int vi = v0 + u * kThreads + (int)threadIdx.x;
-      dt[u] = vi < g.vend ? __ldcg(tp + vi) : E::pad();
-      dd[u] = vi < g.vend ? __ldcg(dp + vi) : E::pad();
-    }
+      for (int e = 1; e < E::kVec; ++e) {
+        mx = fmaxf(mx, x[e]);
+        nan |= (x[e] != x[e]);
+      }
+      acc.nan |= nan;
+      if (mx > acc.v) {
+        int first = 0;
 #pragma unroll
-    for (int u = 0; u < kResUnroll; ++u) {
-      float x[E::kVec], z[E::kVec];
-      E::unpack(dt[u], x);
-      E::unpack(dd[u], z);
-      if ((gi & 31) == 0) gg.make(g.vbeg, gi, w, (uint32_t)jb.j, rk, P.key);
-      const int e0 = (v0 + u * kThreads + (int)threadIdx.x) * E::kVec;
-      group_residual<E>(acc, x, z, e0, rr, gg.get(gi));
-      ++gi;
-    }
+        for (int e = E::kVec - 1; e >= 0; --e)
+          if (x[e] == mx) first = e;
+        acc.v = mx;
+        acc.idx = e0 + first;
+      }
+    });
+  } else if (it.kind == kRace) {
+    GroupGains<E> gg;
+    consume_row<E>(queue, s_qend, ring, lc, gs, it, [&](const float(&x)[E::kVec], int e0, int g) {
+      if ((g & 31) == 0) gg.make(it.vbeg, g, w, (uint32_t)P.wave, rk, P.key);
+      group_bonus<E>(acc, x, e0, it.c, gg.get(g));
+    });
+  } else {
+    const ResidualRow rr{it.c, it.mp, it.inv_sp, it.mq, it.inv_sq};
+    const uint32_t pos = (uint32_t)(P.wave - 1);
+    GroupGains<E> gg;
+    consume_pair<E>(queue, s_qend, ring, lc, gs, it,
+                    [&](const float(&x)[E::kVec], const float(&z)[E::kVec], int e0, int g) {
+                      if ((g & 31) == 0) gg.make(it.vbeg, g, w, pos, rk, P.key);
+                      group_residual<E>(acc, x, z, e0, rr, gg.get(g));
+                    });
   }
-  return acc;
+  acc = warp_reduce(acc);
+  return Partial{acc.v, 0.f, acc.idx, acc.nan};
+}
+
+// Scalar path (rows not 16-byte aligned): warp w takes race blocks
+// vbeg + w, vbeg + w + 7, ...; lane l the ids 128 b + l + 32 j.
+template <typename E>
+__device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const RequestKey rk{it.req_lo, it.req_hi};
+  if (it.kind == kSoftmax) {
+    LazySoftmax acc;
+    acc.init();
+    for (int b = it.vbeg + w; b < it.vend; b += kComputeWarps)
+      for (int j = 0; j < 4; ++j) {
+        const int v = b * kRaceBlock + lane + 32 * j;
+        if (v < P.vocab) acc.add1(E::load1(it.row, v), it.c);
+      }
+    SoftmaxAcc a = warp_reduce(acc.result());
+    return Partial{a.m, a.s, -1, 0u};
+  }
+  BestAcc acc;
+  acc.init();
+  const uint32_t pos = (uint32_t)(it.kind == kResidual ? P.wave - 1 : P.wave);
+  for (int b = it.vbeg + w; b < it.vend; b += kComputeWarps) {
+    if (it.kind == kArgmax) {
+      for (int j = 0; j < 4; ++j) {
+        const int v = b * kRaceBlock + lane + 32 * j;
+        if (v < P.vocab) {
+          const float x = E::load1(it.row, v);
+          acc.nan |= (x != x);
+          acc.take(x, v);
+        }
+      }
+      continue;
+    }
+    float s = 0.f;
+    float m = 0.f;
+    if (it.kind == kRace) {
+      float x[4];
+      float mx = kNegInf;
+      for (int j = 0; j < 4; ++j) {
+        const int v = b * kRaceBlock + lane + 32 * j;
+        x[j] = v < P.vocab ? E::load1(it.row, v) : kNegInf;
+        mx = fmaxf(mx, x[j]);
+        acc.nan |= (x[j] != x[j]) || (x[j] == -kNegInf);
+      }
+      m = warp_max(mx) * it.c;
+      if (m > kNegInf)
+        for (int j = 0; j < 4; ++j) s += fast_ex2(fmaf(x[j], it.c, -m));
+    } else {
+      for (int j = 0; j < 4; ++j) {
+        const int v = b * kRaceBlock + lane + 32 * j;
+        if (v < P.vocab) {
+          const float p = fast_ex2(fmaf(E::load1(it.row, v), it.c, -it.mp)) * it.inv_sp;
+          const float q = fast_ex2(fmaf(E::load1(it.row2, v), it.c, -it.mq)) * it.inv_sq;
+          s += fmaxf(p - q, 0.f);
+        }
+      }
+    }
+    s = group_sum<32>(s);
+    acc.nan = __reduce_or_sync(0xffffffffu, acc.nan);
+    if (s > 0.f) acc.take_cmp(m + fast_lg2(s) + race_gain(race_word(2u, b, pos, rk, P.key)), b);
+  }
+  acc = warp_reduce(acc);
+  return Partial{acc.v, 0.f, acc.idx, acc.nan};
 }
 
 // ---------------------------------------------------------------------------
-// Outputs of one request, and the acceptance scan (the control warp).
+// Outputs of one request (the control warp).
 // ---------------------------------------------------------------------------
-// Publishes the residual job of request r at position j.
-__device__ __forceinline__ void publish_job(const Params& P, int r, int j) {
-  const int slot = atomicAdd(P.ctr + kCntReserve, 1);
-  const unsigned long long word = (unsigned long long)(uint32_t)r |
-                                  ((unsigned long long)(uint32_t)j << 24) | (1ull << 31) |
-                                  ((unsigned long long)(uint32_t)P.jnch << 32);
-  __threadfence();
-  atomicExch(P.res_slots + slot, word);
-  atomicAdd(P.ctr + kCntPublished, P.jnch);
-}
-
-// Outputs of a decided request (the control warp): accepted prefix, the extra
-// token (-1 while a residual job still has to draw it), flags, NaN debug values
-// after position A; then the request is marked done.
+// Accepted prefix, the extra token (-1 while the residual wave still has to
+// draw it), flags, and NaN debug values where no acceptance test was made:
+// after position A, and everywhere for greedy requests.
 __device__ void finish_request(const Params& P, int r, int d0, int k, int A, int token,
-                               bool pending) {
+                               bool greedy) {
   const int lane = threadIdx.x & 31;
   const int width = P.max_k + 1;
   if (lane < width) {  // width <= 32
-    const int v = lane < A ? P.tokens[d0 + lane] : (lane == A && !pending ? token : -1);
+    const int v = lane < A ? P.tokens[d0 + lane] : (lane == A ? token : -1);
     P.committed[(size_t)r * width + lane] = v;
   }
   const float nan = __int_as_float(0x7fc00000);
   if (lane < k) {
     P.flags[d0 + lane] = lane < A ? 1 : 0;
-    if (lane > A) {
+    if (lane > A || greedy) {
       if (P.p_y) P.p_y[d0 + lane] = nan;
       if (P.q_y) P.q_y[d0 + lane] = nan;
       if (P.u_dbg) P.u_dbg[d0 + lane] = nan;
@@ -669,15 +604,28 @@ __device__ void finish_request(const Params& P, int r, int d0, int k, int A, int
   if (lane == 0) {
     P.accepted_len[r] = A;
     if (P.req_status) P.req_status[r] = 0;
-    if (pending) publish_job(P, r, A);
-    __threadfence();
-    *reinterpret_cast<volatile uint32_t*>(P.done + r) = P.epoch;
-    atomicAdd(P.ctr + kCntReqDone, 1);
   }
 }
 
-// A request that cannot be verified: -1 outputs, flags 0, NaN debug values.
-__device__ void skip_request(const Params& P, int r, int d0, int k, uint32_t rs) {
+// A request that cannot be verified (one thread): -1 outputs, flags 0, NaN
+// debug values, its status bits.
+__device__ void skip_request_thread(const Params& P, int r, int d0, int k, uint32_t rs) {
+  const int width = P.max_k + 1;
+  for (int i = 0; i < width; ++i) P.committed[(size_t)r * width + i] = -1;
+  const float nan = __int_as_float(0x7fc00000);
+  for (int i = 0; i < k; ++i) {
+    P.flags[d0 + i] = 0;
+    if (P.p_y) P.p_y[d0 + i] = nan;
+    if (P.q_y) P.q_y[d0 + i] = nan;
+    if (P.u_dbg) P.u_dbg[d0 + i] = nan;
+  }
+  P.accepted_len[r] = -1;
+  if (P.req_status) P.req_status[r] = (int32_t)rs;
+  atomicOr(reinterpret_cast<unsigned int*>(P.ctr + kCntStatus), rs);
+}
+
+// The same from the control warp (a row read in this wave held NaN/+inf).
+__device__ void skip_request_warp(const Params& P, int r, int d0, int k, uint32_t rs) {
   const int lane = threadIdx.x & 31;
   const int width = P.max_k + 1;
   if (lane < width) P.committed[(size_t)r * width + lane] = -1;
@@ -692,85 +640,65 @@ __device__ void skip_request(const Params& P, int r, int d0, int k, uint32_t rs)
     P.accepted_len[r] = -1;
     if (P.req_status) P.req_status[r] = (int32_t)rs;
     atomicOr(reinterpret_cast<unsigned int*>(P.ctr + kCntStatus), rs);
-    __threadfence();
-    *reinterpret_cast<volatile uint32_t*>(P.done + r) = P.epoch;
-    atomicAdd(P.ctr + kCntReqDone, 1);
   }
 }
 
-// Decides position i of request r (the control warp; its rows are merged and
-// positions 0..i-1 were accepted).  "Speculative Decoding: Medusa, MTP, EAGLE,
-// DFlash, DDTree, and DSpark", section 1: accept y_i with probability
-// min(1, p_i(y_i)/q_i(y_i)), tested as u_i q_i(y_i) < p_i(y_i); at the first
-// rejection draw from [p_i - q_i]_+, after k acceptances draw the bonus from
-// p_k; greedy rounds keep y_i while it equals the target argmax.  Returns true
-// when position i was accepted and position i+1 comes next.
-template <typename E>
-__device__ bool decide_position(const Params& P, int r, int i, const int* s_doff) {
-  const int lane = threadIdx.x & 31;
-  const int d0 = s_doff[r];
-  const int k = s_doff[r + 1] - d0;
-  const float t = __ldg(P.temperature + r);
-  const int mode = req_mode(t);
-  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
+// Appends request r's rows of position i+1 to the next wave (lane 0).
+__device__ __forceinline__ void append_next(const Params& P, int r, bool pair) {
+  const int i1 = P.wave + 1;
+  int* list = P.lists + (size_t)i1 * 2 * P.stride;
+  if (pair) {
+    const int at = atomicAdd(P.list_cnt + i1, 2);
+    list[at] = entry_of(r, 0, 1);
+    list[at + 1] = entry_of(r, 1, 1);
+  } else {
+    const int at = atomicAdd(P.list_cnt + i1, 1);
+    list[at] = entry_of(r, 0, 0);
+  }
+}
 
-  if (i == 0) {
-    // inputs are checked once, before the first decision
-    uint32_t rs = 0u;
-    if (mode == kBadTemp) rs |= kStBadTemp;
-    if (lane < k) {
-      const int y = P.tokens[d0 + lane];
-      if (y < 0 || y >= P.vocab) rs |= kStBadToken;
-    }
-    if (!rs && mode == kSampling && k > 0 && P.draft == nullptr) rs |= kStNoDraft;
-    rs = __reduce_or_sync(0xffffffffu, rs);
-    if (rs) {
-      skip_request(P, r, d0, k, rs);
-      return false;
-    }
-  }
-  const Partial pt = ld_cg(P.rowres + slot_of(P, i, r, 0));
-  if (mode == kGreedy) {
-    if (pt.bad) {
-      skip_request(P, r, d0, k, kStNonfinite);
-      return false;
-    }
-    if (i < k && P.tokens[d0 + i] == pt.idx) return true;
-    finish_request(P, r, d0, k, i, pt.idx, false);
-    return false;
-  }
-  const RequestKey rk = request_key(P, r);
-  const float c = kLog2e / t;
+// Decides position i = P.wave of request r from its merged rows (the control
+// warp).  "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and
+// DSpark", section 1: accept y_i with probability min(1, p_i(y_i)/q_i(y_i)),
+// tested as u_i q_i(y_i) < p_i(y_i); at the first rejection draw from
+// [p_i - q_i]_+ (queued for the next wave), after k acceptances draw the bonus
+// from p_k; greedy rounds keep y_i while it equals the target argmax.
+template <typename E>
+__device__ void decide(const Params& P, const QItem& it, int tkind, const Partial& pt,
+                       const Partial& pd) {
+  const int lane = threadIdx.x & 31;
+  const int r = it.r, d0 = it.d0, k = it.k, i = P.wave;
+  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
   const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + i) * row_bytes;
-  ResidualRow rr{c, 0.f, 0.f, 0.f, 0.f};
-  if (i == k) {
-    // every draft accepted: the bonus draw (block race done in the row pass,
-    // index -2 when the row is left to the slow path)
-    int token = -1;
-    if (pt.bad || pt.idx == -1) {
-      skip_request(P, r, d0, k, kStNonfinite);
-      return false;
-    }
-    if (pt.idx >= 0) {
-      token = inner_race<E, false>(P, trow, nullptr, pt.idx, rr, (uint32_t)k, rk);
+  const RequestKey rk{it.req_lo, it.req_hi};
+  if (tkind == kArgmax) {
+    if (pt.bad) {
+      skip_request_warp(P, r, d0, k, kStNonfinite);
+    } else if (i < k && it.y == pt.idx) {
+      if (lane == 0) append_next(P, r, false);
     } else {
-      const BestAcc br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)k, rk);
-      if (br.nan || br.idx < 0) {
-        skip_request(P, r, d0, k, kStNonfinite);
-        return false;
-      }
-      token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)k, rk);
+      finish_request(P, r, d0, k, i, pt.idx, true);
     }
-    finish_request(P, r, d0, k, k, token, false);
-    return false;
+    return;
   }
-  const Partial pd = ld_cg(P.rowres + slot_of(P, i, r, 1));
+  if (tkind == kRace) {
+    // every draft accepted: the element race inside the winning block
+    if (pt.bad || pt.idx < 0) {
+      skip_request_warp(P, r, d0, k, kStNonfinite);
+      return;
+    }
+    const ResidualRow rr{it.c, 0.f, 0.f, 0.f, 0.f};
+    const int token = inner_race<E, false>(P, trow, nullptr, pt.idx, rr, (uint32_t)k, rk);
+    finish_request(P, r, d0, k, k, token, false);
+    return;
+  }
   if (pt.bad || pd.bad) {
-    skip_request(P, r, d0, k, kStNonfinite);
-    return false;
+    skip_request_warp(P, r, d0, k, kStNonfinite);
+    return;
   }
   const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + i) * row_bytes;
-  const int y = P.tokens[d0 + i];
+  const int y = it.y;
+  const float c = it.c;
   const float tp = fmaf(E::load1(trow, y), c, -pt.a);  // log2(p(y) S_p)
   const float tq = fmaf(E::load1(drow, y), c, -pd.a);  // log2(q(y) S_q)
   const float u = accept_uniform(P.key, (uint32_t)i, rk.lo, rk.hi);
@@ -789,145 +717,32 @@ __device__ bool decide_position(const Params& P, int r, int i, const int* s_doff
     if (P.q_y) P.q_y[d0 + i] = fast_ex2(tq) / pd.b;
     if (P.u_dbg) P.u_dbg[d0 + i] = u;
   }
-  if (accept) return true;
-  // first rejection at i: the residual draw
-  if (row_fast<E>(trow, P.vocab) && row_fast<E>(drow, P.vocab)) {
-    finish_request(P, r, d0, k, i, -1, true);  // a residual job draws the token
-    return false;
+  if (accept) {
+    if (lane == 0) append_next(P, r, i + 1 < k);
+    return;
   }
-  rr = ResidualRow{c, pt.a, 1.f / pt.b, pd.a, 1.f / pd.b};
-  BestAcc br = slow_block_race<E, true>(P, trow, drow, rr, (uint32_t)i, rk);
-  int token;
-  if (br.idx >= 0) {
-    token = inner_race<E, true>(P, trow, drow, br.idx, rr, (uint32_t)i, rk);
-  } else {
-    // the residual has no mass (p == q): draw from p_i instead
-    rr = ResidualRow{c, 0.f, 0.f, 0.f, 0.f};
-    br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)i, rk);
-    token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)i, rk);
-  }
-  finish_request(P, r, d0, k, i, token, false);
-  return false;
-}
-
-// Counts one merged row (or the accept signal) towards position i of request
-// r; whoever completes the count decides, and an acceptance signals the next
-// position, which may already have all its rows.
-template <typename E>
-__device__ void count_position(const Params& P, int r, int i, const int* s_doff) {
-  const int lane = threadIdx.x & 31;
-  const int d0 = s_doff[r];
-  const int k = s_doff[r + 1] - d0;
-  const int mode = req_mode(__ldg(P.temperature + r));
-  const int width = P.max_k + 1;
-  for (;;) {
-    uint32_t cnt = 0;
-    if (lane == 0) cnt = epoch_add(P.pos_cnt + (size_t)r * width + i, P.epoch);
-    cnt = __shfl_sync(0xffffffffu, cnt, 0);
-    if (cnt != position_target(P, i, k, mode)) return;
-    __threadfence();
-    if (!decide_position<E>(P, r, i, s_doff)) return;
-    ++i;  // accepted: signal position i + 1
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Job queue: claim one chunk (control lane 0), false if none is ready.
-// Slot word: r (bits 0-23) | j (24-29) | published (31) | chunks left (32-63).
-// *first_live skips slots already seen exhausted.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool claim_job(const Params& P, int* first_live, int* slot, int* r,
-                                          int* j, int* ch) {
-  const int reserved = ld_volatile(P.ctr + kCntReserve);
-  for (int s = *first_live; s < reserved; ++s) {
-    unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(P.res_slots + s);
-    if ((w & (1ull << 31)) && (w >> 32) == 0ull && s == *first_live) ++*first_live;
-    while ((w >> 32) != 0ull) {
-      const unsigned long long old = atomicCAS(P.res_slots + s, w, w - (1ull << 32));
-      if (old == w) {
-        atomicAdd(P.ctr + kCntClaimed, 1);
-        *slot = s;
-        *r = (int)(w & 0xffffffull);
-        *j = (int)((w >> 24) & 0x3full);
-        *ch = (int)(w >> 32) - 1;
-        return true;
-      }
-      w = old;
-    }
-  }
-  return false;
-}
-
-// ---------------------------------------------------------------------------
-// Control-warp helpers.
-// ---------------------------------------------------------------------------
-struct Ctrl {
-  int q_head;      // items queued so far
-  int q_used;      // items handed out as units
-  bool exhausted;  // no more items to claim
-  int first_live;
-  int spins;
-};
-
-// Keep P.fill items queued ahead of q_used.  Items are claimed up to 8 at a
-// time and decoded by separate lanes; items of decided requests are dropped.
-template <typename E>
-__device__ __forceinline__ void fill_queue(const Params& P, const int* s_doff, QItem* queue,
-                                           int* s_qend, Ctrl& cs, int n_items) {
-  const int lane = threadIdx.x & 31;
-  while (!cs.exhausted && cs.q_head < cs.q_used + P.fill) {
-    const int room = kQueue - 1 - (cs.q_head - cs.q_used);
-    const int grab = min(8, room);
-    int base = 0;
-    if (lane == 0) base = atomicAdd(P.ctr + kCntItems, grab);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    const int item = base + lane;
-    bool keep = false;
-    QItem it;
-    if (lane < grab && item < n_items) {
-      decode_item<E>(P, s_doff, item, it);
-      keep = it.kind != kSkip &&
-             *reinterpret_cast<const volatile uint32_t*>(P.done + it.r) != P.epoch;
-    }
-    const uint32_t mask = __ballot_sync(0xffffffffu, keep);
-    if (keep) queue[(cs.q_head + __popc(mask & ((1u << lane) - 1u))) & (kQueue - 1)] = it;
-    cs.q_head += __popc(mask);
-    if (base + grab >= n_items) cs.exhausted = true;
-  }
-  __syncwarp();
+  // first rejection at i: the residual draw is made by the next wave
+  finish_request(P, r, d0, k, i, -1, false);
   if (lane == 0) {
-    __threadfence_block();  // queue entries before the count that publishes them
-    *reinterpret_cast<volatile int*>(s_qend) = cs.exhausted ? -1 - cs.q_head : cs.q_head;
+    const int at = atomicAdd(P.res_cnt + i, 1);
+    ResEntry re;
+    re.r = r;
+    re.j = i;
+    re.d0 = d0;
+    re.pad = 0;
+    re.c = c;
+    re.mp = pt.a;
+    re.inv_sp = 1.f / pt.b;
+    re.mq = pd.a;
+    re.inv_sq = 1.f / pd.b;
+    re.pad2 = re.pad3 = re.pad4 = 0.f;
+    P.res[(size_t)i * P.stride + at] = re;
   }
-  __syncwarp();
 }
 
-// Fill in the residual job chunk (slot, r, j, ch) (lane 0).
-template <typename E>
-__device__ __forceinline__ void make_job(const Params& P, const int* s_doff, int slot, int r,
-                                         int j, int ch, Job& jb) {
-  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
-  const int d0 = s_doff[r];
-  jb.trow = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + j) * row_bytes;
-  jb.drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + j) * row_bytes;
-  jb.slot = slot;
-  jb.r = r;
-  jb.j = j;
-  jb.ch = ch;
-  jb.c = kLog2e / __ldg(P.temperature + r);
-  const RequestKey rk = request_key(P, r);
-  jb.req_lo = rk.lo;
-  jb.req_hi = rk.hi;
-  __threadfence();
-  const Partial rt = ld_cg(P.rowres + slot_of(P, j, r, 0));
-  const Partial rd = ld_cg(P.rowres + slot_of(P, j, r, 1));
-  jb.mp = rt.a;
-  jb.inv_sp = 1.f / rt.b;
-  jb.mq = rd.a;
-  jb.inv_sq = 1.f / rd.b;
-}
-
-// Combine the compute warps' partials of a finished unit (control warp).
+// ---------------------------------------------------------------------------
+// Merging (control warp).
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ Partial combine_best(const Partial* mb) {
   const int lane = threadIdx.x & 31;
   BestAcc a;
@@ -954,341 +769,445 @@ __device__ __forceinline__ Partial combine_softmax(const Partial* mb) {
   return Partial{a.m, a.s, -1, 0u};
 }
 
-// Completion of an item unit: partial out, and the last arrivals merge the
-// entry and scan the request.
+// Whole-row result from the partials of one row's segments (lane-parallel
+// over the CTAs that cut it), or from `own` when the row is a single segment.
+__device__ Partial merge_row(const Params& P, const Partial* parts, const Split& sp, int e,
+                             int kind, bool single, const Partial& own) {
+  const int lane = threadIdx.x & 31;
+  const int c0 = single ? 0 : sp.first_cta(e, P.nb);
+  const int c1 = single ? 0 : sp.last_cta(e, P.nb);
+  if (kind == kSoftmax) {
+    SoftmaxAcc a;
+    a.init();
+    if (single) {
+      if (lane == 0) {
+        a.m = own.a;
+        a.s = own.b;
+      }
+    } else {
+      for (int c = c0 + lane; c <= c1; c += 32) {
+        const Partial q = ld_cg(parts + c + e);
+        SoftmaxAcc b;
+        b.m = q.a;
+        b.s = q.b;
+        a = SoftmaxAcc::merge(a, b);
+      }
+    }
+    a = warp_reduce(a);
+    const bool bad = !(a.s > 0.f) || !(a.s < 3.0e38f) || !(a.m > kNegInf) || !(a.m < 3.0e38f);
+    return Partial{a.m, a.s, -1, bad ? 1u : 0u};
+  }
+  BestAcc a;
+  a.init();
+  if (single) {
+    if (lane == 0) {
+      a.v = own.a;
+      a.idx = own.idx;
+      a.nan = own.bad;
+    }
+  } else {
+    for (int c = c0 + lane; c <= c1; c += 32) {
+      const Partial q = ld_cg(parts + c + e);
+      BestAcc b;
+      b.v = q.a;
+      b.idx = q.idx;
+      b.nan = q.bad;
+      a = BestAcc::merge(a, b);
+    }
+  }
+  a = warp_reduce(a);
+  // argmax rows need a finite maximum; race rows carry a block index (-1: no
+  // block with mass), judged by the decision
+  const bool bad = kind == kArgmax ? (a.nan != 0u || a.idx < 0 || !(a.v < 3.0e38f))
+                                   : a.nan != 0u;
+  return Partial{a.v, 0.f, a.idx, bad ? 1u : 0u};
+}
+
+// Completion of a row segment: partial out; the CTA completing the request's
+// segment count merges the position's rows and decides it.
 template <typename E>
-__device__ void complete_item(const Params& P, const int* s_doff, const QItem& it,
-                              const Partial* mb) {
+__device__ void complete_row(const Params& P, const Split& sp, const QItem& it,
+                             const Partial* mb) {
   const int lane = threadIdx.x & 31;
   const Partial p = it.kind == kSoftmax ? combine_softmax(mb) : combine_best(mb);
-  // a whole-row item is its own row result; chunks are merged by the last one
-  int last = 1;
-  if (P.nch > 1) {
+  const int et = (it.paired && it.is_draft) ? it.e - 1 : it.e;
+  const int nt = sp.last_cta(et, P.nb) - sp.first_cta(et, P.nb) + 1;
+  const int nd = it.paired ? sp.last_cta(et + 1, P.nb) - sp.first_cta(et + 1, P.nb) + 1 : 0;
+  const bool single = nt + nd == 1;
+  if (!single) {
+    int last = 0;
     if (lane == 0) {
-      P.part[it.item] = p;
+      P.part[it.g] = p;
       __threadfence();
-      last = (epoch_add(P.row_cnt + it.n, P.epoch) == (uint32_t)P.nch) ? 1 : 0;
+      last = epoch_add(P.pos_cnt + (size_t)P.wave * P.stride + it.r, P.epoch) ==
+             (uint32_t)(nt + nd);
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __threadfence();
   }
-  Partial res;
-  if (it.kind == kSoftmax) {
-    SoftmaxAcc a;
-    a.init();
-    if (P.nch == 1 && lane == 0) {
-      a.m = p.a;
-      a.s = p.b;
-    }
-    for (int q = lane; P.nch > 1 && q < P.nch; q += 32) {
-      const Partial pq = ld_cg(P.part + (size_t)it.n * P.nch + q);
-      SoftmaxAcc b;
-      b.m = pq.a;
-      b.s = pq.b;
-      a = SoftmaxAcc::merge(a, b);
-    }
-    a = warp_reduce(a);
-    const bool bad = !(a.s > 0.f) || !(a.s < 3.0e38f) || !(a.m > kNegInf) || !(a.m < 3.0e38f);
-    res = Partial{a.m, a.s, -1, bad ? 1u : 0u};
-  } else {
-    BestAcc a;
-    a.init();
-    if (P.nch == 1 && lane == 0) {
-      a.v = p.a;
-      a.idx = p.idx;
-      a.nan = p.bad;
-    }
-    for (int q = lane; P.nch > 1 && q < P.nch; q += 32) {
-      const Partial pq = ld_cg(P.part + (size_t)it.n * P.nch + q);
-      BestAcc b;
-      b.v = pq.a;
-      b.idx = pq.idx;
-      b.nan = pq.bad;
-      a = BestAcc::merge(a, b);
-    }
-    a = warp_reduce(a);
-    // argmax rows need a finite maximum; race rows carry a block index (-1: no
-    // block with mass, -2: left to the slow path), judged by the scan
-    const bool bad = it.kind == kRace ? a.nan != 0u
-                                      : (a.nan != 0u || a.idx < 0 || !(a.v < 3.0e38f));
-    res = Partial{a.v, 0.f, a.idx, bad ? 1u : 0u};
-  }
-  if (lane == 0) {
-    P.rowres[it.n] = res;
-    __threadfence();
-  }
-  __syncwarp();
-  count_position<E>(P, it.r, it.pos, s_doff);
+  const int tkind = it.paired ? kSoftmax : it.kind;
+  const Partial pt = merge_row(P, P.part, sp, et, tkind, single, p);
+  Partial pd{0.f, 0.f, -1, 0u};
+  if (it.paired) pd = merge_row(P, P.part, sp, et + 1, kSoftmax, false, p);
+  decide<E>(P, it, tkind, pt, pd);
 }
 
-// Completion of a job unit: the last chunk merges the block race, runs the
-// element race in the winning block and commits the token (a residual without
-// mass, i.e. p == q, draws from p_j instead, by the slow path).
-struct JobRef {
-  int slot, r, j, ch;
-};
+// Completion of a residual segment: the CTA completing the count merges the
+// block race, runs the element race in the winning block and commits the
+// correction token (a residual without mass in fp32, i.e. p == q, draws from
+// p_j instead).
 template <typename E>
-__device__ void complete_job(const Params& P, const int* s_doff, const JobRef& jb,
-                             const Partial* mb) {
+__device__ void complete_residual(const Params& P, const Split& sp, const QItem& it,
+                                  const Partial* mb) {
   const int lane = threadIdx.x & 31;
   const Partial p = combine_best(mb);
-  int last = 0;
-  if (lane == 0) {
-    P.part2[(size_t)jb.slot * P.jnch + jb.ch] = p;
+  const int n = sp.last_cta(it.e, P.nb) - sp.first_cta(it.e, P.nb) + 1;
+  if (n > 1) {
+    int last = 0;
+    if (lane == 0) {
+      P.rpart[it.g] = p;
+      __threadfence();
+      last = epoch_add(P.pos_cnt + (size_t)P.wave * P.stride + it.r, P.epoch) == (uint32_t)n;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
     __threadfence();
-    last = (atomicAdd(P.res_cnt + jb.slot, 1) == P.jnch - 1) ? 1 : 0;
   }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  BestAcc a;
-  a.init();
-  for (int q = lane; q < P.jnch; q += 32) {
-    const Partial pq = ld_cg(P.part2 + (size_t)jb.slot * P.jnch + q);
-    BestAcc b;
-    b.v = pq.a;
-    b.idx = pq.idx;
-    b.nan = 0u;
-    a = BestAcc::merge(a, b);
-  }
-  a = warp_reduce(a);
-  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
-  const int d0 = s_doff[jb.r];
-  const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + jb.r + jb.j) * row_bytes;
-  const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + jb.j) * row_bytes;
-  const float c = kLog2e / __ldg(P.temperature + jb.r);
-  const RequestKey rk = request_key(P, jb.r);
+  const Partial best = merge_row(P, P.rpart, sp, it.e, kResidual, n == 1, p);
+  const int j = P.wave - 1;
+  const RequestKey rk{it.req_lo, it.req_hi};
   int token;
-  if (a.idx >= 0) {
-    const Partial pt = ld_cg(P.rowres + slot_of(P, jb.j, jb.r, 0));
-    const Partial pd = ld_cg(P.rowres + slot_of(P, jb.j, jb.r, 1));
-    const ResidualRow rr{c, pt.a, 1.f / pt.b, pd.a, 1.f / pd.b};
-    token = inner_race<E, true>(P, trow, drow, a.idx, rr, (uint32_t)jb.j, rk);
+  if (best.idx >= 0) {
+    const ResidualRow rr{it.c, it.mp, it.inv_sp, it.mq, it.inv_sq};
+    token = inner_race<E, true>(P, it.row, it.row2, best.idx, rr, (uint32_t)j, rk);
   } else {
-    const ResidualRow rr{c, 0.f, 0.f, 0.f, 0.f};
-    const BestAcc br = slow_block_race<E, false>(P, trow, nullptr, rr, (uint32_t)jb.j, rk);
-    token = inner_race<E, false>(P, trow, nullptr, br.idx, rr, (uint32_t)jb.j, rk);
+    const ResidualRow rr{it.c, 0.f, 0.f, 0.f, 0.f};
+    const BestAcc br = warp_block_race<E>(P, it.row, it.c, (uint32_t)j, rk);
+    token = inner_race<E, false>(P, it.row, nullptr, br.idx, rr, (uint32_t)j, rk);
   }
-  if (lane == 0) {
-    P.res_cnt[jb.slot] = 0;
-    P.committed[(size_t)jb.r * (P.max_k + 1) + jb.j] = token;
-  }
+  if (lane == 0) P.committed[(size_t)it.r * (P.max_k + 1) + j] = token;
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.
+// Segment generation (control warp): the CTA's share of the residual phase,
+// then of the row phase, cut at row boundaries and decoded lane-parallel.
 // ---------------------------------------------------------------------------
-template <typename E>
-__global__ void __maxnreg__(128) sv_verify(Params P) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint4* ring = reinterpret_cast<uint4*>(smem_raw);
-  int* s_doff = reinterpret_cast<int*>(smem_raw + sizeof(uint4) * kStages * kStageVecs * kThreads);
-  __shared__ QItem queue[kQueue];
-  __shared__ Unit s_unit[2];
-  __shared__ Partial mailbox[2][kComputeWarps];
-  __shared__ int s_w[kBlock / 32 + 1];
-  __shared__ int s_qend;
-  __shared__ int s_kmax;
-  __shared__ uint32_t s_layout;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const bool control = warp == kComputeWarps;
+struct SegGen {
+  int phase;                  // 0 residual, 1 rows, 2 done
+  unsigned long long x, x1;   // next block, end of the share
+  int q_head, q_used;
+};
 
-  // --- prefix sums of num_draft, and the layout check (all threads) -----------
+template <typename E, bool kAligned>
+__device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1, QItem& it) {
+  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
+  const int i = P.wave;
+  it.e = e;
+  it.g = (int)blockIdx.x + e;
+  it.mp = it.inv_sp = it.mq = it.inv_sq = 0.f;
+  it.row2 = nullptr;
+  int r;
+  if (phase == 0) {
+    const ResEntry re = P.res[(size_t)(i - 1) * P.stride + e];
+    r = re.r;
+    it.kind = kResidual;
+    it.d0 = re.d0;
+    it.k = 0;
+    it.y = -1;
+    it.paired = 0;
+    it.is_draft = 0;
+    it.c = re.c;
+    it.mp = re.mp;
+    it.inv_sp = re.inv_sp;
+    it.mq = re.mq;
+    it.inv_sq = re.inv_sq;
+    it.row = reinterpret_cast<const char*>(P.target) + (size_t)(re.d0 + r + re.j) * row_bytes;
+    it.row2 = reinterpret_cast<const char*>(P.draft) + (size_t)(re.d0 + re.j) * row_bytes;
+  } else {
+    const int ent = P.lists[(size_t)i * 2 * P.stride + e];
+    r = ent >> 2;
+    it.is_draft = (ent >> 1) & 1;
+    it.paired = ent & 1;
+    const int d0 = P.doff[r];
+    const int k = P.doff[r + 1] - d0;
+    const float t = P.temperature[r];
+    const bool sampling = req_mode(t) == kSampling;
+    it.d0 = d0;
+    it.k = k;
+    it.y = i < k ? P.tokens[d0 + i] : -1;
+    it.c = sampling ? kLog2e / t : 0.f;
+    it.kind = it.is_draft ? kSoftmax : (sampling ? (i < k ? kSoftmax : kRace) : kArgmax);
+    it.row = it.is_draft
+                 ? reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + i) * row_bytes
+                 : reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + i) * row_bytes;
+  }
+  it.r = r;
+  const RequestKey rk = request_key(P, r);
+  it.req_lo = rk.lo;
+  it.req_hi = rk.hi;
+  if (kAligned) {
+    constexpr int kVPB = kRaceBlock / E::kVec;
+    it.vbeg = b0 * kVPB;
+    it.vend = min(b1 * kVPB, P.nvec);
+    const int per = it.kind == kResidual ? kThreads : kThreads * kStageVecs;
+    it.nst = (it.vend - it.vbeg + per - 1) / per;
+  } else {
+    it.vbeg = b0;
+    it.vend = b1;
+    it.nst = 0;
+  }
+}
+
+// Keeps the queue filled (up to kQueue - 2 segments ahead of the one in use),
+// decoding up to 8 segments at a time, one per lane.
+template <typename E, bool kAligned>
+__device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* s_qend,
+                           SegGen& sg) {
+  const int lane = threadIdx.x & 31;
+  while (sg.phase < 2 && sg.q_head < sg.q_used + kQueue - 2) {
+    const int room = min(8, kQueue - 2 - (sg.q_head - sg.q_used));
+    // cut the next `room` segments (all lanes alike); lane j keeps the j-th
+    int n = 0, my_phase = 0, my_e = 0, my_b0 = 0, my_b1 = 0;
+    while (n < room && sg.phase < 2) {
+      if (sg.x >= sg.x1) {
+        // next phase: the share of this CTA in it
+        ++sg.phase;
+        if (sg.phase == 1 && (int)blockIdx.x < sp[1].G) {
+          sg.x = sp[1].begin(blockIdx.x);
+          sg.x1 = sp[1].begin(blockIdx.x + 1);
+        }
+        continue;
+      }
+      const int e = (int)(sg.x / (unsigned long long)P.nb);
+      const unsigned long long row0 = (unsigned long long)e * P.nb;
+      const int b0 = (int)(sg.x - row0);
+      const unsigned long long end = sg.x1 < row0 + P.nb ? sg.x1 : row0 + P.nb;
+      const int b1 = (int)(end - row0);
+      if (lane == n) {
+        my_phase = sg.phase;
+        my_e = e;
+        my_b0 = b0;
+        my_b1 = b1;
+      }
+      sg.x = end;
+      ++n;
+    }
+    QItem it;
+    if (lane < n) decode_segment<E, kAligned>(P, my_phase, my_e, my_b0, my_b1, it);
+    if (lane < n) queue[(sg.q_head + lane) & (kQueue - 1)] = it;
+    sg.q_head += n;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();  // queue entries before the count that publishes them
+    *reinterpret_cast<volatile int*>(s_qend) = sg.phase >= 2 ? -1 - sg.q_head : sg.q_head;
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// The plan launch (one CTA): draft offsets, the layout and input checks, the
+// outputs of requests that cannot be verified, and the entries of wave 0.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
+  __shared__ int s_w[kPlanThreads / 32 + 1];
+  __shared__ uint32_t s_layout;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kW = kPlanThreads / 32;
+
   if (tid == 0) {
     s_layout = 0u;
-    s_kmax = 0;
+    P.ctr[kCntStatus] = 0;
   }
+  for (int i = tid; i <= P.max_k; i += kPlanThreads) P.list_cnt[i] = 0;
+  for (int i = tid; i < max(P.max_k, 1); i += kPlanThreads) P.res_cnt[i] = 0;
   __syncthreads();
-  int carry = 0;
-  for (int base = 0; base < P.batch; base += kBlock) {
-    const int r = base + tid;
-    const int k = r < P.batch ? P.num_draft[r] : 0;
-    const bool badk = k < 0 || k > P.max_k;
-    if (badk) atomicOr(&s_layout, kStBadK);
-    const int kk = badk ? 0 : k;
-    if (kk > 0) atomicMax(&s_kmax, kk);
-    int v = kk;
+
+  // block-wide exclusive scan of v (all threads call it); returns the prefix,
+  // *total gets the sum
+  auto scan = [&](int v, int* total) {
+    int incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, v, off);
-      if (lane >= off) v += o;
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
     }
-    if (lane == 31) s_w[warp] = v;
+    if (lane == 31) s_w[warp] = incl;
     __syncthreads();
-    if (tid < 32) {
-      const int w = tid < kBlock / 32 ? s_w[tid] : 0;
+    if (warp == 0) {
+      const int w = s_w[lane];
       int wi = w;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int o = __shfl_up_sync(0xffffffffu, wi, off);
         if (lane >= off) wi += o;
       }
-      if (tid < kBlock / 32) s_w[tid] = wi - w;
-      if (tid == kBlock / 32 - 1) s_w[kBlock / 32] = wi;
+      s_w[lane] = wi - w;
+      if (lane == 31) s_w[kW] = wi;
     }
     __syncthreads();
-    if (r < P.batch) s_doff[r] = carry + s_w[warp] + v - kk;
-    carry += s_w[kBlock / 32];
+    const int excl = s_w[warp] + incl - v;
+    *total = s_w[kW];
     __syncthreads();
+    return excl;
+  };
+
+  // draft-row offsets, and the checks that make the layout trustworthy
+  int carry = 0;
+  for (int base = 0; base < P.batch; base += kPlanThreads) {
+    const int r = base + tid;
+    const int k = r < P.batch ? P.num_draft[r] : 0;
+    const bool badk = k < 0 || k > P.max_k;
+    if (badk) atomicOr(&s_layout, kStBadK);
+    const int kk = badk ? 0 : k;
+    int tot;
+    const int ex = scan(kk, &tot);
+    if (r < P.batch) P.doff[r] = carry + ex;
+    carry += tot;
   }
   if (tid == 0) {
-    s_doff[P.batch] = carry;
+    P.doff[P.batch] = carry;
     if (!s_layout && carry != P.total_draft) s_layout = kStBadTotal;
   }
   __syncthreads();
   const uint32_t layout = s_layout;
-  // waves 0..max_k of this batch, two slots per request each
-  const int n_items = (s_kmax + 1) * 2 * P.batch * P.nch;
-
   if (layout) {
-    // untrustworthy layout: nothing is verified; CTA 0 reports it
-    if (blockIdx.x == 0) {
-      const int width = P.max_k + 1;
-      for (int i = tid; i < P.batch * width; i += kBlock) P.committed[i] = -1;
-      for (int r = tid; r < P.batch; r += kBlock) {
-        P.accepted_len[r] = -1;
-        if (P.req_status) P.req_status[r] = (int32_t)layout;
-      }
-      const float nan = __int_as_float(0x7fc00000);
-      for (int d = tid; d < P.total_draft; d += kBlock) {
-        P.flags[d] = 0;
-        if (P.p_y) P.p_y[d] = nan;
-        if (P.q_y) P.q_y[d] = nan;
-        if (P.u_dbg) P.u_dbg[d] = nan;
-      }
-      if (tid == 0) atomicOr(reinterpret_cast<unsigned int*>(P.ctr + kCntStatus), layout);
+    // nothing is verified
+    const int width = P.max_k + 1;
+    for (int i = tid; i < P.batch * width; i += kPlanThreads) P.committed[i] = -1;
+    for (int r = tid; r < P.batch; r += kPlanThreads) {
+      P.accepted_len[r] = -1;
+      if (P.req_status) P.req_status[r] = (int32_t)layout;
     }
+    const float nan = __int_as_float(0x7fc00000);
+    for (int d = tid; d < P.total_draft; d += kPlanThreads) {
+      P.flags[d] = 0;
+      if (P.p_y) P.p_y[d] = nan;
+      if (P.q_y) P.q_y[d] = nan;
+      if (P.u_dbg) P.u_dbg[d] = nan;
+    }
+    if (tid == 0) P.ctr[kCntStatus] = (int)layout;
+    return;
+  }
+
+  // per request: the input checks, then its entries of wave 0
+  int written = 0;
+  int* list0 = P.lists;
+  for (int base = 0; base < P.batch; base += kPlanThreads) {
+    const int r = base + tid;
+    int n = 0;
+    if (r < P.batch) {
+      const int d0 = P.doff[r];
+      const int k = P.doff[r + 1] - d0;
+      const int mode = req_mode(P.temperature[r]);
+      uint32_t rs = mode == kBadTemp ? kStBadTemp : 0u;
+      for (int i = 0; i < k; ++i) {
+        const int y = P.tokens[d0 + i];
+        if (y < 0 || y >= P.vocab) rs |= kStBadToken;
+      }
+      if (!rs && mode == kSampling && k > 0 && P.draft == nullptr) rs |= kStNoDraft;
+      if (rs) {
+        skip_request_thread(P, r, d0, k, rs);
+      } else {
+        n = (mode == kSampling && k > 0) ? 2 : 1;
+      }
+    }
+    int tot;
+    const int at = written + scan(n, &tot);
+    if (n == 2) {
+      list0[at] = entry_of(r, 0, 1);
+      list0[at + 1] = entry_of(r, 1, 1);
+    } else if (n == 1) {
+      list0[at] = entry_of(r, 0, 0);
+    }
+    written += tot;
+  }
+  if (tid == 0) P.list_cnt[0] = written;
+}
+
+// ---------------------------------------------------------------------------
+// The wave launch: position P.wave of every request still alive, and the
+// correction draws of the requests rejected at P.wave - 1.
+// ---------------------------------------------------------------------------
+template <typename E, bool kAligned>
+__global__ void __maxnreg__(128) sv_wave(Params P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint4* ring = reinterpret_cast<uint4*>(smem_raw);
+  __shared__ QItem queue[kQueue];
+  __shared__ int s_unit[2];
+  __shared__ Partial mailbox[2][kComputeWarps];
+  __shared__ int s_qend;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const bool control = warp == kComputeWarps;
+
+  const int n_rows = P.list_cnt[P.wave];
+  const int n_res = P.wave > 0 ? P.res_cnt[P.wave - 1] : 0;
+  Split sp[2];
+  sp[0].init(n_res, P.nb, P.min_span_res, gridDim.x);
+  sp[1].init(n_rows, P.nb, P.min_span, gridDim.x);
+  const int c = blockIdx.x;
+  if (c >= sp[0].G && c >= sp[1].G) return;  // no share in this wave
+
+  SegGen sg;
+  sg.phase = 0;
+  sg.q_head = sg.q_used = 0;
+  if (c < sp[0].G) {
+    sg.x = sp[0].begin(c);
+    sg.x1 = sp[0].begin(c + 1);
   } else {
-    Ctrl cs;
-    cs.q_head = cs.q_used = 0;
-    cs.exhausted = false;
-    cs.first_live = 0;
-    cs.spins = 0;
-    // control: the unit the compute warps are processing
-    int cur_type = kUnitIdle, cur_qidx = 0;
-    JobRef cur_job{0, 0, 0, 0};
-    if (control) {
-      fill_queue<E>(P, s_doff, queue, &s_qend, cs, n_items);
-      if (lane == 0) s_unit[0].type = kUnitIdle;
+    sg.x = sg.x1 = 0ull;
+  }
+  int cur = -1;  // control: queue index of the segment being processed
+  if (control) {
+    fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
+    if (lane == 0) s_unit[0] = sg.q_head > 0 ? kUnitItem : kUnitEnd;
+  }
+  __syncthreads();
+
+  LoadCursor lc;
+  int gs = 0;
+  if (kAligned && !control) {
+    lc.q = 0;
+    lc.active = false;
+    lc.open(queue, &s_qend);
+    for (int s = 0; s < kStages - 1; ++s) lc.issue(queue, &s_qend, ring, s);
+  }
+
+  for (int u = 0;; ++u) {
+    const int type = s_unit[u & 1];
+    if (!control) {
+      // ---- compute warps: stream segment u ------------------------------------
+      if (type == kUnitItem) {
+        const QItem& it = queue[u & (kQueue - 1)];
+        const Partial out = kAligned ? seg_aligned<E>(P, queue, &s_qend, ring, lc, gs, it)
+                                     : seg_scalar<E>(P, it);
+        if (lane == 0) mailbox[u & 1][warp] = out;
+      }
+    } else {
+      // ---- control warp: finish segment u-1, queue ahead, schedule u+1 ---------
+      if (cur >= 0) {
+        const QItem& pv = queue[cur & (kQueue - 1)];
+        if (pv.kind == kResidual) {
+          complete_residual<E>(P, sp[0], pv, mailbox[(u - 1) & 1]);
+        } else {
+          complete_row<E>(P, sp[1], pv, mailbox[(u - 1) & 1]);
+        }
+        sg.q_used = cur + 1;  // its queue entry may now be reused
+      }
+      cur = type == kUnitItem ? u : -1;
+      if (type == kUnitItem) {
+        fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
+        if (lane == 0) s_unit[(u + 1) & 1] = (u + 1 < sg.q_head) ? kUnitItem : kUnitEnd;
+      }
+      __syncwarp();
     }
     __syncthreads();
-
-    LoadCursor<E> lc;
-    int gs = 0;
-    if (!control) {
-      lc.q = 0;
-      lc.active = false;
-      lc.open(queue, &s_qend);
-      for (int s = 0; s < kStages - 1; ++s) lc.issue(P, queue, &s_qend, ring, s);
-    }
-
-    for (int u = 0;; ++u) {
-      if (!control) {
-        // ---- compute warps: process unit u ---------------------------------
-        const int type = s_unit[u & 1].type;
-        if (type == kUnitItem) {
-          const QItem it = queue[s_unit[u & 1].qidx & (kQueue - 1)];
-          Partial out;
-          if (it.kind == kSoftmax) {
-            SoftmaxAcc a = item_softmax<E>(P, queue, &s_qend, ring, lc, gs, it);
-            a = warp_reduce(a);
-            out = Partial{a.m, a.s, -1, 0u};
-          } else {
-            BestAcc a;
-            if (it.kind == kArgmax) {
-              a = item_argmax<E>(P, queue, &s_qend, ring, lc, gs, it);
-            } else {
-              a = item_race<E>(P, queue, &s_qend, ring, lc, gs, it);
-            }
-            a = warp_reduce(a);
-            out = Partial{a.v, 0.f, a.idx, a.nan};
-          }
-          if (lane == 0) mailbox[u & 1][warp] = out;
-        } else if (type == kUnitResidual) {
-          const Job jb = s_unit[u & 1].job;
-          BestAcc a = job_chunk<E>(P, jb);
-          a = warp_reduce(a);
-          if (lane == 0) mailbox[u & 1][warp] = Partial{a.v, 0.f, a.idx, a.nan};
-        }
-      } else {
-        // ---- control warp: finish unit u-1, schedule unit u+1 ----------------
-        const int prev_type = cur_type, prev_qidx = cur_qidx;
-        const JobRef prev_job = cur_job;
-        cur_type = s_unit[u & 1].type;
-        cur_qidx = s_unit[u & 1].qidx;
-        cur_job = JobRef{s_unit[u & 1].job.slot, s_unit[u & 1].job.r, s_unit[u & 1].job.j,
-                         s_unit[u & 1].job.ch};
-        if (prev_type == kUnitItem) {
-          complete_item<E>(P, s_doff, queue[prev_qidx & (kQueue - 1)], mailbox[(u - 1) & 1]);
-        } else if (prev_type == kUnitResidual) {
-          complete_job<E>(P, s_doff, prev_job, mailbox[(u - 1) & 1]);
-        }
-        // keep the items the compute warps may stream during unit u+1 queued
-        fill_queue<E>(P, s_doff, queue, &s_qend, cs, n_items);
-        // next unit: a claimable job first, then the next queued item
-        int next_type = kUnitIdle;
-        if (lane == 0) {
-          Unit nx;
-          nx.type = kUnitIdle;
-          int slot, r, j, ch;
-          bool got = false;
-          if (ld_volatile(P.ctr + kCntPublished) != ld_volatile(P.ctr + kCntClaimed))
-            got = claim_job(P, &cs.first_live, &slot, &r, &j, &ch);
-          if (got) {
-            nx.type = kUnitResidual;
-            make_job<E>(P, s_doff, slot, r, j, ch, nx.job);
-          } else if (cs.q_used < cs.q_head) {
-            nx.type = kUnitItem;
-            nx.qidx = cs.q_used;
-          } else if (cur_type == kUnitIdle) {
-            // nothing in flight here: finished once every request is scanned
-            // and every job claimed; otherwise wait a little for new jobs
-            const bool done = ld_volatile(P.ctr + kCntReqDone) == P.batch &&
-                              ld_volatile(P.ctr + kCntPublished) == ld_volatile(P.ctr + kCntClaimed);
-            if (done || cs.spins >= P.spin_limit) {
-              nx.type = kUnitEnd;
-            } else {
-              ++cs.spins;
-              __nanosleep(500);
-            }
-          }
-          s_unit[(u + 1) & 1] = nx;
-          next_type = nx.type;
-        }
-        next_type = __shfl_sync(0xffffffffu, next_type, 0);
-        cs.spins = __shfl_sync(0xffffffffu, cs.spins, 0);
-        cs.first_live = __shfl_sync(0xffffffffu, cs.first_live, 0);
-        if (next_type == kUnitItem) ++cs.q_used;
-        __syncwarp();
-      }
-      __syncthreads();
-      if (s_unit[(u + 1) & 1].type == kUnitEnd) break;
-    }
-    if (!control) cp_async_wait_all();
+    if (type == kUnitEnd) break;
   }
-
-  // --- the last CTA out resets the round's shared state ----------------------
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(P.ctr + kCntExit, 1) == (int)gridDim.x - 1) {
-      __threadfence();
-      const int reserved = ld_volatile(P.ctr + kCntReserve);
-      for (int s = 0; s < reserved; ++s) P.res_slots[s] = 0ull;
-      P.ctr[kCntLastStatus] = ld_volatile(P.ctr + kCntStatus);
-      P.ctr[kCntStatus] = 0;
-      P.ctr[kCntItems] = 0;
-      P.ctr[kCntReserve] = 0;
-      P.ctr[kCntPublished] = 0;
-      P.ctr[kCntClaimed] = 0;
-      P.ctr[kCntReqDone] = 0;
-      __threadfence();
-      P.ctr[kCntExit] = 0;
-    }
-  }
+  if (kAligned && !control) cp_async_wait_all();
 }
 
 }  // namespace sv

@@ -13,7 +13,7 @@ sits within a relative 1e-5 of its threshold, because fp32 (GPU) and fp64
     fp32 residual is then rounding noise).
 Exemptions are counted and returned.  Debug p(y)/q(y) must agree within 1e-5
 absolute and the acceptance uniforms exactly, on the decided positions
-0..A (both sides report NaN after the first rejection).
+0..A (both sides report NaN after the first rejection, and for greedy requests).
 """
 from __future__ import annotations
 
@@ -88,6 +88,9 @@ def compare(gpu: dict, orc: dict, inp: dict, seed: int) -> dict:
             rep["greedy"] += 1
             assert ga == oa and (gc == oc).all() and (gpu["flags"][fl] == orc["flags"][fl]).all(), \
                 (r, ga, oa, gc, oc)
+            if "p_y" in gpu:   # no acceptance test is made for greedy rows: NaN debug values
+                assert np.isnan(gpu["p_y"][fl]).all() and np.isnan(gpu["q_y"][fl]).all(), r
+                assert np.isnan(gpu["u"][fl]).all(), r
             continue
         rep["sampling"] += 1
         # debug values of the decided positions (NaN after the first rejection)

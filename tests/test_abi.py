@@ -48,7 +48,9 @@ def test_calls_on_a_null_handle(lib):
     assert lib.specverify_destroy(None) == _lib.ERR_INVALID_ARG
     assert lib.specverify_run(None, None, None, None, None, None, 0, 1, 0,
                               None, None, None, None) == _lib.ERR_INVALID_ARG
-    assert lib.specverify_launches_per_run() == 1
+    n = ctypes.c_int(-7)
+    assert lib.specverify_launches_per_run(None, ctypes.byref(n)) == _lib.ERR_INVALID_ARG
+    assert n.value == -7
 
 
 def test_no_device_reports_cuda_error(lib):
