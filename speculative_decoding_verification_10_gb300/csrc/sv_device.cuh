@@ -282,6 +282,22 @@ struct LazySoftmax {
     float a[2] = {x, kNegInf};
     add<2>(a, c);
   }
+  // Two vectors with one overflow check.  A failed check (the sum left
+  // (0, 2^100], including m = -inf, which makes the terms inf or NaN) raises m
+  // to the running maximum and redoes both vectors; NaN logits leave s NaN.
+  template <int N>
+  __device__ __forceinline__ void add2(const float (&x0)[N], const float (&x1)[N], float c) {
+    float2 t = __fadd2_rn(terms(x0, c), terms(x1, c));
+    if (!(t.x + t.y <= 0x1p100f)) {
+      const float vm = fmaxf(fmaxf(vmax(x0), vmax(x1)) * c, m);
+      if (vm == kNegInf) return;  // nothing finite yet
+      const float sc = fast_ex2(m - vm);
+      s = make_float2(s.x * sc, s.y * sc);
+      m = vm;
+      t = __fadd2_rn(terms(x0, c), terms(x1, c));
+    }
+    s = __fadd2_rn(s, t);
+  }
   __device__ __forceinline__ SoftmaxAcc result() const {
     SoftmaxAcc r;
     r.m = m;

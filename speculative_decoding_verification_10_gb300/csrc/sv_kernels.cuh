@@ -357,15 +357,18 @@ __device__ BestAcc warp_block_race(const Params& P, const char* trow, float c, u
 }
 
 // ---------------------------------------------------------------------------
-// The per-thread copy ring (compute threads, aligned rows).
+// The per-thread copy ring (compute threads, aligned rows).  Stage s of a
+// segment holds two vectors per thread: vectors vbeg + 2 s kThreads + tid and
+// + kThreads of a single row, or vector vbeg + s kThreads + tid of t_j and of
+// d_j for a residual segment.
 // ---------------------------------------------------------------------------
 struct LoadCursor {
-  int q;   // queue index of the segment being loaded
-  int st;  // stage within it
-  const uint4* base;
-  const uint4* base2;
-  int vbeg, vend, nst;
-  bool pair, active;
+  int q;      // queue index of the segment being loaded
+  int left;   // its stages still to copy
+  const uint4* b0;
+  const uint4* b1;
+  int i0, i1, step, vend;
+  bool active;
 
   // s_qend: segments the control warp has queued, or -1 - n once all n are.
   __device__ __forceinline__ void open(const QItem* queue, const int* s_qend) {
@@ -375,13 +378,14 @@ struct LoadCursor {
     active = q < avail;
     if (active) {
       const QItem& it = queue[q & (kQueue - 1)];
-      base = reinterpret_cast<const uint4*>(it.row);
-      base2 = reinterpret_cast<const uint4*>(it.row2);
-      vbeg = it.vbeg;
+      const bool pair = it.kind == kResidual;
+      b0 = reinterpret_cast<const uint4*>(it.row);
+      b1 = reinterpret_cast<const uint4*>(pair ? it.row2 : it.row);
+      i0 = it.vbeg + (int)threadIdx.x;
+      i1 = pair ? i0 : i0 + kThreads;
+      step = pair ? kThreads : kStageVecs * kThreads;
       vend = it.vend;
-      nst = it.nst;
-      pair = it.kind == kResidual;
-      st = 0;
+      left = it.nst;
     }
   }
 
@@ -390,93 +394,85 @@ struct LoadCursor {
                                         int slot) {
     if (!active) open(queue, s_qend);
     if (active) {
-      if (pair) {
-        const int vi = vbeg + st * kThreads + (int)threadIdx.x;
-        if (vi < vend) {
-          cp_async16(ring + (slot * kStageVecs + 0) * kThreads + threadIdx.x, base + vi);
-          cp_async16(ring + (slot * kStageVecs + 1) * kThreads + threadIdx.x, base2 + vi);
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < kStageVecs; ++u) {
-          const int vi = vbeg + (st * kStageVecs + u) * kThreads + (int)threadIdx.x;
-          if (vi < vend) cp_async16(ring + (slot * kStageVecs + u) * kThreads + threadIdx.x, base + vi);
-        }
+      uint4* dst = ring + slot * kStageVecs * kThreads + threadIdx.x;
+      if (i0 < vend) cp_async16(dst, b0 + i0);
+      if (i1 < vend) cp_async16(dst + kThreads, b1 + i1);
+      i0 += step;
+      i1 += step;
+      if (--left == 0) {
+        ++q;
+        open(queue, s_qend);
       }
     }
     cp_async_commit();
-    if (active && ++st == nst) {
-      ++q;
-      open(queue, s_qend);
-    }
   }
 };
 
 // Reads one stage of the ring (after its copies landed) and refills the ring
 // one stage ahead.
 __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend, uint4* ring,
-                                          LoadCursor& lc, int& g_stage, uint4 (&v)[kStageVecs]) {
+                                          LoadCursor& lc, int& g_stage, uint4& v0, uint4& v1) {
   cp_async_wait<kStages - 2>();
-  const int slot = g_stage % kStages;
-#pragma unroll
-  for (int u = 0; u < kStageVecs; ++u) v[u] = ring[(slot * kStageVecs + u) * kThreads + threadIdx.x];
-  lc.issue(queue, s_qend, ring, (g_stage + kStages - 1) % kStages);
+  const int slot = g_stage & (kStages - 1);
+  const uint4* src = ring + slot * kStageVecs * kThreads + threadIdx.x;
+  v0 = src[0];
+  v1 = src[kThreads];
+  lc.issue(queue, s_qend, ring, (g_stage + kStages - 1) & (kStages - 1));
   ++g_stage;
 }
 
-// Streams a single-row segment: f(x, first id, vector group).
-template <typename E, typename F>
-__device__ __forceinline__ void consume_row(const QItem* queue, const int* s_qend, uint4* ring,
-                                            LoadCursor& lc, int& g_stage, const QItem& it, F&& f) {
-  for (int st = 0; st < it.nst; ++st) {
-    uint4 v[kStageVecs];
-    ring_take(queue, s_qend, ring, lc, g_stage, v);
-#pragma unroll
-    for (int u = 0; u < kStageVecs; ++u) {
-      const int vi = it.vbeg + (st * kStageVecs + u) * kThreads + (int)threadIdx.x;
-      float x[E::kVec];
-      E::unpack(vi < it.vend ? v[u] : E::pad(), x);
-      f(x, vi * E::kVec, st * kStageVecs + u);
-    }
+// Streams a segment stage by stage: f(v0, v1, st, full).  Only the last stage
+// of a segment can reach past its end (full == false there); the caller pads
+// the vectors beyond vend.
+template <typename F>
+__device__ __forceinline__ void consume(const QItem* queue, const int* s_qend, uint4* ring,
+                                        LoadCursor& lc, int& g_stage, const QItem& it, F&& f) {
+  const int per = it.kind == kResidual ? kThreads : kStageVecs * kThreads;
+  const int nfull = (it.vend - it.vbeg) / per;
+  for (int st = 0; st < nfull; ++st) {
+    uint4 v0, v1;
+    ring_take(queue, s_qend, ring, lc, g_stage, v0, v1);
+    f(v0, v1, st, true);
   }
-}
-
-// Streams a residual segment (rows t_j and d_j side by side): f(x, z, first id, group).
-template <typename E, typename F>
-__device__ __forceinline__ void consume_pair(const QItem* queue, const int* s_qend, uint4* ring,
-                                             LoadCursor& lc, int& g_stage, const QItem& it, F&& f) {
-  for (int st = 0; st < it.nst; ++st) {
-    uint4 v[kStageVecs];
-    ring_take(queue, s_qend, ring, lc, g_stage, v);
-    const int vi = it.vbeg + st * kThreads + (int)threadIdx.x;
-    float x[E::kVec], z[E::kVec];
-    E::unpack(vi < it.vend ? v[0] : E::pad(), x);
-    E::unpack(vi < it.vend ? v[1] : E::pad(), z);
-    f(x, z, vi * E::kVec, st);
+  if (nfull < it.nst) {
+    uint4 v0, v1;
+    ring_take(queue, s_qend, ring, lc, g_stage, v0, v1);
+    f(v0, v1, nfull, false);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Segment reductions (compute threads).  Each returns this thread's partial.
+// Segment reductions (compute threads).  Each returns this warp's partial.
 // ---------------------------------------------------------------------------
 template <typename E>
 __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
                                                const int* s_qend, uint4* ring, LoadCursor& lc,
                                                int& gs, const QItem& it) {
   const int w = threadIdx.x >> 5;
+  const int tid = threadIdx.x;
   const RequestKey rk{it.req_lo, it.req_hi};
   if (it.kind == kSoftmax) {
     LazySoftmax acc;
     acc.init();
-    consume_row<E>(queue, s_qend, ring, lc, gs, it,
-                   [&](const float(&x)[E::kVec], int, int) { acc.add(x, it.c); });
+    const float c = it.c;
+    consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
+      if (!full) {
+        const int vi = it.vbeg + st * kStageVecs * kThreads + tid;
+        if (vi >= it.vend) v0 = E::pad();
+        if (vi + kThreads >= it.vend) v1 = E::pad();
+      }
+      float x0[E::kVec], x1[E::kVec];
+      E::unpack(v0, x0);
+      E::unpack(v1, x1);
+      acc.add2(x0, x1, c);
+    });
     SoftmaxAcc a = warp_reduce(acc.result());
     return Partial{a.m, a.s, -1, 0u};
   }
   BestAcc acc;
   acc.init();
   if (it.kind == kArgmax) {
-    consume_row<E>(queue, s_qend, ring, lc, gs, it, [&](const float(&x)[E::kVec], int e0, int) {
+    auto vec = [&](const float(&x)[E::kVec], int e0) {
       float mx = x[0];
       uint32_t nan = (x[0] != x[0]);
 #pragma unroll
@@ -493,22 +489,52 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
         acc.v = mx;
         acc.idx = e0 + first;
       }
+    };
+    consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
+      const int vi = it.vbeg + st * kStageVecs * kThreads + tid;
+      if (!full) {
+        if (vi >= it.vend) v0 = E::pad();
+        if (vi + kThreads >= it.vend) v1 = E::pad();
+      }
+      float x[E::kVec];
+      E::unpack(v0, x);
+      vec(x, vi * E::kVec);
+      E::unpack(v1, x);
+      vec(x, (vi + kThreads) * E::kVec);
     });
   } else if (it.kind == kRace) {
     GroupGains<E> gg;
-    consume_row<E>(queue, s_qend, ring, lc, gs, it, [&](const float(&x)[E::kVec], int e0, int g) {
+    const float c = it.c;
+    consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
+      const int vi = it.vbeg + st * kStageVecs * kThreads + tid;
+      if (!full) {
+        if (vi >= it.vend) v0 = E::pad();
+        if (vi + kThreads >= it.vend) v1 = E::pad();
+      }
+      const int g = st * kStageVecs;
       if ((g & 31) == 0) gg.make(it.vbeg, g, w, (uint32_t)P.wave, rk, P.key);
-      group_bonus<E>(acc, x, e0, it.c, gg.get(g));
+      float x[E::kVec];
+      E::unpack(v0, x);
+      group_bonus<E>(acc, x, vi * E::kVec, c, gg.get(g));
+      E::unpack(v1, x);
+      group_bonus<E>(acc, x, (vi + kThreads) * E::kVec, c, gg.get(g + 1));
     });
   } else {
     const ResidualRow rr{it.c, it.mp, it.inv_sp, it.mq, it.inv_sq};
     const uint32_t pos = (uint32_t)(P.wave - 1);
     GroupGains<E> gg;
-    consume_pair<E>(queue, s_qend, ring, lc, gs, it,
-                    [&](const float(&x)[E::kVec], const float(&z)[E::kVec], int e0, int g) {
-                      if ((g & 31) == 0) gg.make(it.vbeg, g, w, pos, rk, P.key);
-                      group_residual<E>(acc, x, z, e0, rr, gg.get(g));
-                    });
+    consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
+      const int vi = it.vbeg + st * kThreads + tid;
+      if (!full && vi >= it.vend) {
+        v0 = E::pad();
+        v1 = E::pad();
+      }
+      if ((st & 31) == 0) gg.make(it.vbeg, st, w, pos, rk, P.key);
+      float x[E::kVec], z[E::kVec];
+      E::unpack(v0, x);
+      E::unpack(v1, z);
+      group_residual<E>(acc, x, z, vi * E::kVec, rr, gg.get(st));
+    });
   }
   acc = warp_reduce(acc);
   return Partial{acc.v, 0.f, acc.idx, acc.nan};
