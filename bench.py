@@ -391,7 +391,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clock_info,
-        "gpu_launches": v.launches_per_run() * args.steps,
+        "gpu_launches": v.launches_per_run(b.batch) * args.steps,
     }
     print(json.dumps(line), flush=True)
     v.close()

@@ -131,7 +131,8 @@ int specverify_create_ex(specverify_t *out, int device, int max_batch, int max_k
  *   accepted_len    [batch] int32 out;
  *   committed_tokens[batch, max_k+1] int32 out;
  *   accept_flags    [total_draft] uint8 out.
- * Launches one kernel and returns without waiting; nothing is allocated.
+ * Enqueues the round's launches (specverify_launches_per_run) and returns
+ * without waiting; nothing is allocated.
  */
 int specverify_run(specverify_t h, const void *target_logits, const void *draft_logits,
                    const int32_t *draft_tokens, const int32_t *num_draft,
@@ -173,18 +174,29 @@ int specverify_status(specverify_t h, int32_t *status_out);
 
 /*
  * specverify_set_timing_events -- measurement aid.  After this call, run number
- * i (counting from 0) records start_events[i % n] on its stream just before the
- * verify kernel (the single kernel of a run) and
- * stop_events[i % n] just after it.  The arrays hold cudaEvent_t values created
+ * i (counting from 0) records start_events[i % n] on its stream just before its
+ * first launch and stop_events[i % n] just after its last.  The arrays hold cudaEvent_t values created
  * by the caller, n in [1, 64]; they are copied.  n = 0 turns recording off.
  */
 int specverify_set_timing_events(specverify_t h, int n, void *const *start_events,
                                  void *const *stop_events);
 
-/* Kernel launches one run of handle h makes (for launch accounting): the plan
- * launch and one wave launch per draft position 0..max_k, i.e. max_k + 2.
- * Waves past the batch's own largest k return at once. */
-int specverify_launches_per_run(specverify_t h, int *launches_out);
+/*
+ * specverify_set_depth -- positions verified per wave launch.  A round reads
+ * the rows of positions 0..A only when it decides one position per wave
+ * (depth 1, the least traffic); a larger depth reads up to depth - 1 rows past
+ * a rejection but needs fewer launches, which is faster for small batches.
+ * depth in [1, max_k + 1] fixes it; 0 (the default) chooses per run: max_k + 1
+ * when every row of the batch's verify window together takes at most 192 MiB,
+ * else 1.  Results do not depend on the depth.
+ */
+int specverify_set_depth(specverify_t h, int depth);
+
+/* Kernel launches a run of `batch` requests makes on handle h (for launch
+ * accounting): the plan launch and one launch per wave of `depth` positions
+ * (plus one for the last wave's correction draws when depth > 1).  Waves with
+ * nothing left to do return at once. */
+int specverify_launches_per_run(specverify_t h, int batch, int *launches_out);
 
 /* Free the handle and its device memory.  Further use returns _ERR_DESTROYED
  * only while the memory of the freed handle is not reused; do not use it. */

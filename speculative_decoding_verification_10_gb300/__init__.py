@@ -157,12 +157,16 @@ class Verifier:
         _check(self.lib.specverify_set_timing_events(self._h, n, arr_s, arr_e),
                "specverify_set_timing_events")
 
-    def launches_per_run(self) -> int:
-        """Kernel launches one run makes: the plan and one wave per position 0..max_k."""
+    def launches_per_run(self, batch: int) -> int:
+        """Kernel launches a run of `batch` requests makes (the plan and the waves)."""
         n = ctypes.c_int()
-        _check(self.lib.specverify_launches_per_run(self._h, ctypes.byref(n)),
+        _check(self.lib.specverify_launches_per_run(self._h, batch, ctypes.byref(n)),
                "specverify_launches_per_run")
         return int(n.value)
+
+    def set_depth(self, depth: int):
+        """Positions per wave launch: 1 .. max_k + 1, or 0 to choose per run."""
+        _check(self.lib.specverify_set_depth(self._h, depth), "specverify_set_depth")
 
     def status(self) -> int:
         """Status bits of the last run (waits for its stream)."""

@@ -71,8 +71,10 @@ def load(path: str | None = None):
     lib.specverify_status.restype = I
     lib.specverify_set_timing_events.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P)]
     lib.specverify_set_timing_events.restype = I
-    lib.specverify_launches_per_run.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+    lib.specverify_launches_per_run.argtypes = [P, I, ctypes.POINTER(ctypes.c_int)]
     lib.specverify_launches_per_run.restype = I
+    lib.specverify_set_depth.argtypes = [P, I]
+    lib.specverify_set_depth.restype = I
     lib.specverify_destroy.argtypes = [P]
     lib.specverify_destroy.restype = I
     lib.specverify_error_string.argtypes = [I]

@@ -40,14 +40,15 @@ struct specverify_ctx {
   uint32_t magic;
   int device, max_batch, max_k, vocab, dtype, elem_bytes;
   int num_sms, grid_aligned, grid_scalar;
+  int depth_setting;  // 0: chosen per run from the batch size
   void* scratch;
   size_t scratch_bytes;
-  int* doff;
-  int* lists;
+  sv::Entry* lists;
   int* list_cnt;
   sv::ResEntry* res;
   int* res_cnt;
   unsigned long long* pos_cnt;
+  unsigned long long* rcnt;
   sv::Partial* part;
   sv::Partial* rpart;
   int* ctr;
@@ -92,7 +93,37 @@ struct Kernels {
   }
 };
 
-// One round: the plan launch, then waves 0..max_k (a wave with nothing to do
+// Batches whose whole verify window (every row of every position) is at most
+// this many bytes are verified in one wave of all positions: reading rows past
+// a rejection costs less than a launch per position there.
+constexpr double kShallowBytes = 192.0 * (1 << 20);
+
+// Positions per wave for a run of `batch` requests.
+static int run_depth(const specverify_ctx* h, int batch) {
+  if (h->depth_setting > 0) return h->depth_setting;
+  const double window = (double)batch * (2.0 * h->max_k + 1.0) * h->vocab * h->elem_bytes;
+  return window <= kShallowBytes ? h->max_k + 1 : 1;
+}
+
+// A wave launch that may begin while the previous launch of the stream is
+// finishing (programmatic dependent launch; the kernel waits for it first).
+template <typename K>
+static cudaError_t launch_wave(K kernel, int grid, size_t smem, cudaStream_t s,
+                               const sv::Params& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(sv::kBlock);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
+// One round: the plan launch, then the waves (a wave with nothing to do
 // returns at once).
 template <typename E>
 static int launch_round(specverify_ctx* h, sv::Params P, bool aligned, cudaStream_t s) {
@@ -102,12 +133,15 @@ static int launch_round(specverify_ctx* h, sv::Params P, bool aligned, cudaStrea
   sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
   const size_t smem = aligned ? ring_bytes() : 0;
   const int grid = aligned ? h->grid_aligned : h->grid_scalar;
-  for (int i = 0; i <= h->max_k; ++i) {
-    P.wave = i;
-    if (aligned) {
-      sv::sv_wave<E, true><<<grid, sv::kBlock, smem, s>>>(P);
-    } else {
-      sv::sv_wave<E, false><<<grid, sv::kBlock, smem, s>>>(P);
+  for (int w = 0; w < P.n_waves; ++w) {
+    P.wave = w;
+    P.pos0 = std::min(w * P.depth, h->max_k + 1);
+    P.pos1 = std::min((w + 1) * P.depth, h->max_k + 1);
+    const cudaError_t e = aligned ? launch_wave(sv::sv_wave<E, true>, grid, smem, s, P)
+                                  : launch_wave(sv::sv_wave<E, false>, grid, smem, s, P);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return SPECVERIFY_ERR_CUDA;
     }
   }
   if (slot >= 0 && cudaEventRecord(h->ev_stop[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
@@ -150,6 +184,9 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.max_k = h->max_k;
   P.vocab = h->vocab;
   P.epoch = ++h->epoch;  // never 0: 0 is the initial value of every tag
+  P.depth = run_depth(h, batch);
+  P.n_waves = sv::wave_count(h->max_k, P.depth);
+  P.list_cap = 2 * P.depth * h->max_batch;
   P.nb = (h->vocab + sv::kRaceBlock - 1) / sv::kRaceBlock;
   P.nvec = (int)((size_t)h->vocab * h->elem_bytes / 16);
   const int block_bytes = sv::kRaceBlock * h->elem_bytes;
@@ -163,12 +200,12 @@ static int run_impl(specverify_t h, const void* target_logits, const void* draft
   P.q_y = q_y;
   P.u_dbg = u;
   P.req_status = req_status;
-  P.doff = h->doff;
   P.lists = h->lists;
   P.list_cnt = h->list_cnt;
   P.res = h->res;
   P.res_cnt = h->res_cnt;
   P.pos_cnt = h->pos_cnt;
+  P.rcnt = h->rcnt;
   P.part = h->part;
   P.rpart = h->rpart;
   P.ctr = h->ctr;
@@ -218,6 +255,7 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   h->run_counter = 0;
 
   h->last_run_empty = true;
+  h->depth_setting = 0;
   bool ok = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) ==
             cudaSuccess;
   int occ_a = 0, occ_s = 0;
@@ -251,14 +289,22 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
     off = align_up(off + bytes, 256);
     return o;
   };
-  const size_t mb = (size_t)max_batch, waves = (size_t)max_k + 1;
-  const size_t o_doff = carve(sizeof(int) * (mb + 1));
-  const size_t o_lists = carve(sizeof(int) * waves * 2 * mb);
-  const size_t o_lcnt = carve(sizeof(int) * waves);
-  const size_t o_res = carve(sizeof(sv::ResEntry) * std::max<size_t>(max_k, 1) * mb);
-  const size_t o_rcnt = carve(sizeof(int) * std::max<size_t>(max_k, 1));
-  const size_t o_poscnt = carve(sizeof(unsigned long long) * waves * mb);
-  const size_t o_part = carve(sizeof(sv::Partial) * ((size_t)grid + 2 * mb));
+  // sized for every wave depth D = 1 .. max_k + 1
+  const size_t mb = (size_t)max_batch;
+  size_t list_entries = 0, max_waves = 0, max_cap = 0;
+  for (int d = 1; d <= max_k + 1; ++d) {
+    const size_t w = (size_t)sv::wave_count(max_k, d), cap = 2 * (size_t)d * mb;
+    list_entries = std::max(list_entries, w * cap);
+    max_waves = std::max(max_waves, w);
+    max_cap = std::max(max_cap, cap);
+  }
+  const size_t o_lists = carve(sizeof(sv::Entry) * list_entries);
+  const size_t o_lcnt = carve(sizeof(int) * max_waves);
+  const size_t o_res = carve(sizeof(sv::ResEntry) * max_waves * mb);
+  const size_t o_rcnt = carve(sizeof(int) * max_waves);
+  const size_t o_poscnt = carve(sizeof(unsigned long long) * ((size_t)max_k + 1) * mb);
+  const size_t o_rescnt = carve(sizeof(unsigned long long) * mb);
+  const size_t o_part = carve(sizeof(sv::Partial) * ((size_t)grid + max_cap));
   const size_t o_rpart = carve(sizeof(sv::Partial) * ((size_t)grid + mb));
   const size_t o_ctr = carve(sizeof(int) * sv::kCntCount);
   h->scratch_bytes = off;
@@ -274,12 +320,12 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
     return SPECVERIFY_ERR_CUDA;
   }
   char* b = static_cast<char*>(h->scratch);
-  h->doff = reinterpret_cast<int*>(b + o_doff);
-  h->lists = reinterpret_cast<int*>(b + o_lists);
+  h->lists = reinterpret_cast<sv::Entry*>(b + o_lists);
   h->list_cnt = reinterpret_cast<int*>(b + o_lcnt);
   h->res = reinterpret_cast<sv::ResEntry*>(b + o_res);
   h->res_cnt = reinterpret_cast<int*>(b + o_rcnt);
   h->pos_cnt = reinterpret_cast<unsigned long long*>(b + o_poscnt);
+  h->rcnt = reinterpret_cast<unsigned long long*>(b + o_rescnt);
   h->part = reinterpret_cast<sv::Partial*>(b + o_part);
   h->rpart = reinterpret_cast<sv::Partial*>(b + o_rpart);
   h->ctr = reinterpret_cast<int*>(b + o_ctr);
@@ -437,11 +483,20 @@ int specverify_set_timing_events(specverify_t h, int n, void* const* start_event
   return SPECVERIFY_OK;
 }
 
-int specverify_launches_per_run(specverify_t h, int* launches_out) {
+int specverify_set_depth(specverify_t h, int depth) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
-  if (launches_out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
-  *launches_out = h->max_k + 2;  // the plan and one wave per position 0..max_k
+  if (depth < 0 || depth > h->max_k + 1) return SPECVERIFY_ERR_INVALID_ARG;
+  h->depth_setting = depth;
+  return SPECVERIFY_OK;
+}
+
+int specverify_launches_per_run(specverify_t h, int batch, int* launches_out) {
+  int rc = check_handle(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (launches_out == nullptr || batch < 0 || batch > h->max_batch)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  *launches_out = batch == 0 ? 0 : 1 + sv::wave_count(h->max_k, run_depth(h, batch));
   return SPECVERIFY_OK;
 }
 

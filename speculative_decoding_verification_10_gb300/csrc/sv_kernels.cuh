@@ -1,32 +1,37 @@
-// sv_kernels.cuh -- the verify round as a plan launch and one wave launch per
-// draft position.
+// sv_kernels.cuh -- the verify round as a plan launch and a short sequence of
+// wave launches.
 //
 // Left to right, and no further than needed.  A round tests the draft
 // positions of each request left to right and discards everything after the
 // first rejection ("Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree,
 // and DSpark", section 1), so only the rows of positions 0..A are needed, plus
 // the bonus row when all k drafts are accepted.  The round is therefore run as
-// waves: wave i streams, for every request still alive at position i, target
-// row t_i and draft row d_i (sampling, i < k), the bonus row t_k (sampling,
-// i = k) or target row t_i (greedy), and decides position i of each of them.
-// An accepted request is appended to the list of wave i+1; a rejected one to
-// the residual list, whose rows t_i and d_i the next wave reads again (first,
-// while they may still sit in L2) to draw the correction token.
+// waves of D positions: wave w streams, for every request still alive at
+// position w*D, its rows of positions w*D .. w*D+D-1 -- target row t_i and
+// draft row d_i (sampling, i < k), the bonus row t_k (sampling, i = k) or
+// target row t_i (greedy) -- and decides them in order.  A request that
+// survives the wave is appended to the list of wave w+1; a rejected one to the
+// residual list, whose rows t_j and d_j the next wave reads again (first,
+// while they may still sit in L2) to draw the correction token.  D = 1 reads
+// exactly the needed rows; a larger D trades rows read past a rejection for
+// fewer launches, which pays for small batches.
 //
 // Inside a wave the work is split flat: the wave's rows form one sequence of
 // race blocks (128 vocab ids), and CTA c takes the contiguous range
 // [c*T/G, (c+1)*T/G) of it, so every CTA streams the same number of bytes
 // whatever the row lengths.  A CTA's range cuts into a few row segments; each
-// segment reduces to one 16-byte partial.  The CTA that brings the count of a
-// request's segments to its total merges them and decides the position: no
-// CTA ever waits for another, there is no work claiming, and the segment
-// count of any row follows from the split arithmetic alone.
+// segment reduces to one 16-byte partial.  A position is decided by the CTA
+// that brings its count to the total: the segments of its rows, plus one for
+// "the previous position of this wave was accepted".  No CTA ever waits for
+// another, there is no work claiming, and the segment count of any row follows
+// from the split arithmetic alone.
 //
 // CTA layout: 7 compute warps and 1 control warp, one __syncthreads per
 // segment.  Compute warps stream the segment and leave one partial per warp in
 // shared memory; during the next segment the control warp combines them and
-// does every latency-bound step: partial stores, the completion count, the
-// merge, the decision, the list appends and the outputs.
+// does every latency-bound step: partial stores, the completion counts, the
+// merges, the decisions, the list appends and the outputs.  Consecutive waves
+// overlap their launch with programmatic dependent launch.
 //
 // Memory pipeline (16-byte aligned rows): each compute thread streams its
 // vectors of successive segments through a private shared-memory ring with
@@ -46,6 +51,7 @@ constexpr int kStages = 8;
 constexpr int kStageVecs = 2;
 constexpr int kQueue = 16;                     // segment queue entries (power of 2)
 constexpr int kMaxBatch = 4096;                // requests per round
+constexpr int kMaxK = 31;                      // draft positions per request
 constexpr int kPlanThreads = 1024;
 constexpr int kRaceBlock = 128;                // vocab ids per race block
 constexpr int kMinSpanBytes = 16384;           // smallest share of a wave per CTA
@@ -58,25 +64,44 @@ enum UnitType : int { kUnitEnd = 0, kUnitItem = 1 };
 constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite = 8u,
                    kStBadTotal = 16u, kStNoDraft = 64u;
 
-// A list entry of wave i: request r, which row, and whether the target and
-// draft rows of that position come as an adjacent pair (target first).
-__device__ __forceinline__ int entry_of(int r, int is_draft, int paired) {
-  return (r << 2) | (is_draft << 1) | paired;
+// Number of waves of a round with positions 0..max_k taken D at a time: one
+// per group of D positions, plus one for the residual draws of the last group
+// when it can reject (D > 1).
+__host__ __device__ __forceinline__ int wave_count(int max_k, int depth) {
+  return (max_k + depth) / depth + (depth > 1 ? 1 : 0);
+}
+
+// One row of a wave's list, written by the plan launch or by the CTA that
+// accepted the request's last position of the previous wave.
+struct __align__(16) Entry {
+  int meta;         // r | is_draft << 13 | paired << 14 | k << 15 | pos << 20
+  int d0;           // the request's first draft row
+  float c;          // log2(e) / T; 0 for greedy requests
+  int y;            // the draft token at pos; -1 at pos = k
+  uint32_t req_lo;  // Philox request word
+  uint32_t req_hi;
+  int base;         // list index of the request's first row in this wave
+  int pad;
+};
+
+__host__ __device__ __forceinline__ int entry_meta(int r, int is_draft, int paired, int k, int pos) {
+  return r | (is_draft << 13) | (paired << 14) | (k << 15) | (pos << 20);
 }
 
 struct __align__(16) Partial {
-  float a;       // softmax: m  | best: value
-  float b;       // softmax: S  | unused
-  int idx;       // best: index | unused
-  uint32_t bad;  // NaN seen
+  float a;       // softmax: m     | best: value
+  float b;       // softmax: S     | unused
+  int idx;       // softmax: x[y]  | best: index
+  uint32_t bad;  // softmax: 1 when the segment holds y | best: NaN seen
 };
 
 // A rejected request waiting for its correction draw (written by the deciding
-// CTA of wave j, read by wave j+1).
+// CTA of wave w, read by wave w+1).
 struct __align__(16) ResEntry {
   int r, j, d0, pad;
   float c, mp, inv_sp, mq;
-  float inv_sq, pad2, pad3, pad4;
+  float inv_sq;
+  uint32_t req_lo, req_hi, pad2;
 };
 
 enum Counter : int { kCntStatus = 0, kCntCount = 4 };
@@ -90,13 +115,17 @@ struct Params {
   const int64_t* request_ids;
   PhiloxKey key;
   int batch, total_draft, max_k, vocab;
-  int wave;          // the draft position this launch decides
+  int depth;         // D, positions per wave
+  int wave;          // this launch: wave w, positions [pos0, pos1)
+  int pos0, pos1;
+  int n_waves;
   uint32_t epoch;    // this round's tag of the completion counters
   int nb;            // race blocks per row
   int nvec;          // 16-byte vectors per row (aligned rows)
   int min_span;      // fewest race blocks per CTA share of the row phase
   int min_span_res;  // ... and of the residual phase
   int stride;        // capacity of a request-indexed array (max_batch)
+  int list_cap;      // entries per wave list: 2 * D * stride
   int32_t* accepted_len;
   int32_t* committed;
   uint8_t* flags;
@@ -104,13 +133,13 @@ struct Params {
   float* q_y;
   float* u_dbg;
   int32_t* req_status;
-  int* doff;                    // [stride + 1] draft-row offsets of the requests
-  int* lists;                   // [(max_k + 1) * 2 * stride] row entries of each wave
-  int* list_cnt;                // [max_k + 1]
-  ResEntry* res;                // [max(max_k, 1) * stride] rejections of each position
-  int* res_cnt;                 // [max(max_k, 1)]
-  unsigned long long* pos_cnt;  // [(max_k + 1) * stride] epoch | segments merged
-  Partial* part;                // [grid + 2 * stride] row segment partials
+  Entry* lists;                 // [n_waves * list_cap] rows of each wave
+  int* list_cnt;                // [n_waves]
+  ResEntry* res;                // [n_waves * stride] rejections of each wave
+  int* res_cnt;                 // [n_waves]
+  unsigned long long* pos_cnt;  // [(max_k + 1) * stride] epoch | count of a position
+  unsigned long long* rcnt;     // [stride] epoch | residual segments merged
+  Partial* part;                // [grid + list_cap] row segment partials
   Partial* rpart;               // [grid + stride] residual segment partials
   int* ctr;                     // [kCntCount]
 };
@@ -168,6 +197,9 @@ struct Split {
   __device__ __forceinline__ int last_cta(int e, int nb) const {
     return cta_of((unsigned long long)(e + 1) * nb - 1ull);
   }
+  __device__ __forceinline__ int segments(int e, int nb) const {
+    return last_cta(e, nb) - first_cta(e, nb) + 1;
+  }
 };
 
 // A segment of the CTA's share, decoded once by the control warp.
@@ -176,15 +208,28 @@ struct __align__(16) QItem {
   const char* row2;  // draft row of a residual segment
   int kind;          // RowKind of this segment
   int e;             // list (or residual list) entry
-  int r, d0, k, y;   // request, its draft offset, k, the draft token y_i (or -1)
+  int r, d0, k, y;   // request, its first draft row, k, the draft token at pos (or -1)
+  int pos;           // the position the row belongs to (Philox position)
+  int base;          // list index of the request's first row in this wave
   int paired, is_draft;
   int vbeg, vend;    // vectors (aligned rows) or race blocks (scalar path)
   int nst;           // ring stages (aligned rows)
   int g;             // partial index: CTA + entry
+  int yv;            // vector (aligned) or race block (scalar) holding y, -1 if none
   float c;           // log2(e) / T
   float mp, inv_sp, mq, inv_sq;  // residual segments: normalisers of p_j and q_j
   uint32_t req_lo, req_hi;
 };
+
+// The logit x[y] held by vector x at element e (a select chain, no local memory).
+template <int N>
+__device__ __forceinline__ float pick(const float (&x)[N], int e) {
+  float v = x[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i)
+    if (i == e) v = x[i];
+  return v;
+}
 
 // ---------------------------------------------------------------------------
 // Two-level exponential race: blocks of kRaceBlock vocab ids.  The block race
@@ -442,12 +487,13 @@ __device__ __forceinline__ void consume(const QItem* queue, const int* s_qend, u
 }
 
 // ---------------------------------------------------------------------------
-// Segment reductions (compute threads).  Each returns this warp's partial.
+// Segment reductions (compute threads).  Each returns this warp's partial; a
+// softmax segment that holds the draft token y also leaves x[y] in *s_xy.
 // ---------------------------------------------------------------------------
 template <typename E>
 __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
                                                const int* s_qend, uint4* ring, LoadCursor& lc,
-                                               int& gs, const QItem& it) {
+                                               int& gs, const QItem& it, float* s_xy) {
   const int w = threadIdx.x >> 5;
   const int tid = threadIdx.x;
   const RequestKey rk{it.req_lo, it.req_hi};
@@ -455,15 +501,18 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
     LazySoftmax acc;
     acc.init();
     const float c = it.c;
+    const int yv = it.yv, ye = it.y & (E::kVec - 1);
     consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
+      const int vi = it.vbeg + st * kStageVecs * kThreads + tid;
       if (!full) {
-        const int vi = it.vbeg + st * kStageVecs * kThreads + tid;
         if (vi >= it.vend) v0 = E::pad();
         if (vi + kThreads >= it.vend) v1 = E::pad();
       }
       float x0[E::kVec], x1[E::kVec];
       E::unpack(v0, x0);
       E::unpack(v1, x1);
+      if (vi == yv) *s_xy = pick(x0, ye);
+      if (vi + kThreads == yv) *s_xy = pick(x1, ye);
       acc.add2(x0, x1, c);
     });
     SoftmaxAcc a = warp_reduce(acc.result());
@@ -512,7 +561,7 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
         if (vi + kThreads >= it.vend) v1 = E::pad();
       }
       const int g = st * kStageVecs;
-      if ((g & 31) == 0) gg.make(it.vbeg, g, w, (uint32_t)P.wave, rk, P.key);
+      if ((g & 31) == 0) gg.make(it.vbeg, g, w, (uint32_t)it.pos, rk, P.key);
       float x[E::kVec];
       E::unpack(v0, x);
       group_bonus<E>(acc, x, vi * E::kVec, c, gg.get(g));
@@ -521,7 +570,6 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
     });
   } else {
     const ResidualRow rr{it.c, it.mp, it.inv_sp, it.mq, it.inv_sq};
-    const uint32_t pos = (uint32_t)(P.wave - 1);
     GroupGains<E> gg;
     consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
       const int vi = it.vbeg + st * kThreads + tid;
@@ -529,7 +577,7 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
         v0 = E::pad();
         v1 = E::pad();
       }
-      if ((st & 31) == 0) gg.make(it.vbeg, st, w, pos, rk, P.key);
+      if ((st & 31) == 0) gg.make(it.vbeg, st, w, (uint32_t)it.pos, rk, P.key);
       float x[E::kVec], z[E::kVec];
       E::unpack(v0, x);
       E::unpack(v1, z);
@@ -543,7 +591,7 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
 // Scalar path (rows not 16-byte aligned): warp w takes race blocks
 // vbeg + w, vbeg + w + 7, ...; lane l the ids 128 b + l + 32 j.
 template <typename E>
-__device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it) {
+__device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, float* s_xy) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const RequestKey rk{it.req_lo, it.req_hi};
   if (it.kind == kSoftmax) {
@@ -552,14 +600,18 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it) 
     for (int b = it.vbeg + w; b < it.vend; b += kComputeWarps)
       for (int j = 0; j < 4; ++j) {
         const int v = b * kRaceBlock + lane + 32 * j;
-        if (v < P.vocab) acc.add1(E::load1(it.row, v), it.c);
+        if (v < P.vocab) {
+          const float x = E::load1(it.row, v);
+          if (v == it.y) *s_xy = x;
+          acc.add1(x, it.c);
+        }
       }
     SoftmaxAcc a = warp_reduce(acc.result());
     return Partial{a.m, a.s, -1, 0u};
   }
   BestAcc acc;
   acc.init();
-  const uint32_t pos = (uint32_t)(it.kind == kResidual ? P.wave - 1 : P.wave);
+  const uint32_t pos = (uint32_t)it.pos;
   for (int b = it.vbeg + w; b < it.vend; b += kComputeWarps) {
     if (it.kind == kArgmax) {
       for (int j = 0; j < 4; ++j) {
@@ -605,11 +657,70 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it) 
 }
 
 // ---------------------------------------------------------------------------
+// Wave lists.
+// ---------------------------------------------------------------------------
+// Rows a request alive at position s has in the wave that starts there:
+// positions s .. min(s + D - 1, k), two rows each below k when sampling, one
+// (the bonus or greedy row) otherwise.
+__device__ __forceinline__ int wave_rows(const Params& P, bool sampling, int k, int s) {
+  const int last = min(s + P.depth - 1, k);
+  if (!sampling) return last - s + 1;
+  return 2 * (min(s + P.depth, k) - s) + (last == k ? 1 : 0);
+}
+
+// The j-th of those rows, as a list entry.
+__device__ __forceinline__ Entry wave_entry(const Params& P, bool sampling, int r, int d0, int k,
+                                            float c, RequestKey rk, int s, int j, int base) {
+  int pos, is_draft = 0, paired = 0;
+  if (!sampling) {
+    pos = s + j;
+  } else if (j < 2 * (min(s + P.depth, k) - s)) {
+    pos = s + j / 2;
+    is_draft = j & 1;
+    paired = 1;
+  } else {
+    pos = k;
+  }
+  Entry en;
+  en.meta = entry_meta(r, is_draft, paired, k, pos);
+  en.d0 = d0;
+  en.c = c;
+  en.y = pos < k ? P.tokens[d0 + pos] : -1;
+  en.req_lo = rk.lo;
+  en.req_hi = rk.hi;
+  en.base = base;
+  en.pad = 0;
+  return en;
+}
+
+// The request a decision is about.
+struct ReqInfo {
+  int r, d0, k, base;
+  float c;
+  RequestKey rk;
+};
+
+// A request accepted through the last position of this wave: its rows of the
+// next wave (control warp).
+__device__ void append_next_wave(const Params& P, const ReqInfo& q, int next) {
+  const int lane = threadIdx.x & 31;
+  const bool sampling = q.c > 0.f;
+  const int n = wave_rows(P, sampling, q.k, next);
+  const int w1 = P.wave + 1;
+  int at = 0;
+  if (lane == 0) at = atomicAdd(P.list_cnt + w1, n);
+  at = __shfl_sync(0xffffffffu, at, 0);
+  Entry* list = P.lists + (size_t)w1 * P.list_cap;
+  for (int j = lane; j < n; j += 32)
+    list[at + j] = wave_entry(P, sampling, q.r, q.d0, q.k, q.c, q.rk, next, j, at);
+}
+
+// ---------------------------------------------------------------------------
 // Outputs of one request (the control warp).
 // ---------------------------------------------------------------------------
-// Accepted prefix, the extra token (-1 while the residual wave still has to
-// draw it), flags, and NaN debug values where no acceptance test was made:
-// after position A, and everywhere for greedy requests.
+// Accepted prefix, the extra token (-1 while the next wave still has to draw
+// it), flags, and NaN debug values where no acceptance test was made: after
+// position A, and everywhere for greedy requests.
 __device__ void finish_request(const Params& P, int r, int d0, int k, int A, int token,
                                bool greedy) {
   const int lane = threadIdx.x & 31;
@@ -669,103 +780,6 @@ __device__ void skip_request_warp(const Params& P, int r, int d0, int k, uint32_
   }
 }
 
-// Appends request r's rows of position i+1 to the next wave (lane 0).
-__device__ __forceinline__ void append_next(const Params& P, int r, bool pair) {
-  const int i1 = P.wave + 1;
-  int* list = P.lists + (size_t)i1 * 2 * P.stride;
-  if (pair) {
-    const int at = atomicAdd(P.list_cnt + i1, 2);
-    list[at] = entry_of(r, 0, 1);
-    list[at + 1] = entry_of(r, 1, 1);
-  } else {
-    const int at = atomicAdd(P.list_cnt + i1, 1);
-    list[at] = entry_of(r, 0, 0);
-  }
-}
-
-// Decides position i = P.wave of request r from its merged rows (the control
-// warp).  "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and
-// DSpark", section 1: accept y_i with probability min(1, p_i(y_i)/q_i(y_i)),
-// tested as u_i q_i(y_i) < p_i(y_i); at the first rejection draw from
-// [p_i - q_i]_+ (queued for the next wave), after k acceptances draw the bonus
-// from p_k; greedy rounds keep y_i while it equals the target argmax.
-template <typename E>
-__device__ void decide(const Params& P, const QItem& it, int tkind, const Partial& pt,
-                       const Partial& pd) {
-  const int lane = threadIdx.x & 31;
-  const int r = it.r, d0 = it.d0, k = it.k, i = P.wave;
-  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
-  const char* trow = reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + i) * row_bytes;
-  const RequestKey rk{it.req_lo, it.req_hi};
-  if (tkind == kArgmax) {
-    if (pt.bad) {
-      skip_request_warp(P, r, d0, k, kStNonfinite);
-    } else if (i < k && it.y == pt.idx) {
-      if (lane == 0) append_next(P, r, false);
-    } else {
-      finish_request(P, r, d0, k, i, pt.idx, true);
-    }
-    return;
-  }
-  if (tkind == kRace) {
-    // every draft accepted: the element race inside the winning block
-    if (pt.bad || pt.idx < 0) {
-      skip_request_warp(P, r, d0, k, kStNonfinite);
-      return;
-    }
-    const ResidualRow rr{it.c, 0.f, 0.f, 0.f, 0.f};
-    const int token = inner_race<E, false>(P, trow, nullptr, pt.idx, rr, (uint32_t)k, rk);
-    finish_request(P, r, d0, k, k, token, false);
-    return;
-  }
-  if (pt.bad || pd.bad) {
-    skip_request_warp(P, r, d0, k, kStNonfinite);
-    return;
-  }
-  const char* drow = reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + i) * row_bytes;
-  const int y = it.y;
-  const float c = it.c;
-  const float tp = fmaf(E::load1(trow, y), c, -pt.a);  // log2(p(y) S_p)
-  const float tq = fmaf(E::load1(drow, y), c, -pd.a);  // log2(q(y) S_q)
-  const float u = accept_uniform(P.key, (uint32_t)i, rk.lo, rk.hi);
-  // u q(y) < p(y), both sides scaled by S_p S_q 2^-max(tp, tq) > 0
-  bool accept;
-  if (tp == kNegInf) {
-    accept = false;
-  } else if (tq == kNegInf) {
-    accept = true;
-  } else {
-    const float mx = fmaxf(tp, tq);
-    accept = u * (fast_ex2(tq - mx) * pt.b) < fast_ex2(tp - mx) * pd.b;
-  }
-  if (lane == 0) {
-    if (P.p_y) P.p_y[d0 + i] = fast_ex2(tp) / pt.b;
-    if (P.q_y) P.q_y[d0 + i] = fast_ex2(tq) / pd.b;
-    if (P.u_dbg) P.u_dbg[d0 + i] = u;
-  }
-  if (accept) {
-    if (lane == 0) append_next(P, r, i + 1 < k);
-    return;
-  }
-  // first rejection at i: the residual draw is made by the next wave
-  finish_request(P, r, d0, k, i, -1, false);
-  if (lane == 0) {
-    const int at = atomicAdd(P.res_cnt + i, 1);
-    ResEntry re;
-    re.r = r;
-    re.j = i;
-    re.d0 = d0;
-    re.pad = 0;
-    re.c = c;
-    re.mp = pt.a;
-    re.inv_sp = 1.f / pt.b;
-    re.mq = pd.a;
-    re.inv_sq = 1.f / pd.b;
-    re.pad2 = re.pad3 = re.pad4 = 0.f;
-    P.res[(size_t)i * P.stride + at] = re;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Merging (control warp).
 // ---------------------------------------------------------------------------
@@ -795,88 +809,247 @@ __device__ __forceinline__ Partial combine_softmax(const Partial* mb) {
   return Partial{a.m, a.s, -1, 0u};
 }
 
-// Whole-row result from the partials of one row's segments (lane-parallel
-// over the CTAs that cut it), or from `own` when the row is a single segment.
-__device__ Partial merge_row(const Params& P, const Partial* parts, const Split& sp, int e,
-                             int kind, bool single, const Partial& own) {
-  const int lane = threadIdx.x & 31;
-  const int c0 = single ? 0 : sp.first_cta(e, P.nb);
-  const int c1 = single ? 0 : sp.last_cta(e, P.nb);
-  if (kind == kSoftmax) {
-    SoftmaxAcc a;
-    a.init();
-    if (single) {
-      if (lane == 0) {
-        a.m = own.a;
-        a.s = own.b;
-      }
-    } else {
-      for (int c = c0 + lane; c <= c1; c += 32) {
-        const Partial q = ld_cg(parts + c + e);
-        SoftmaxAcc b;
-        b.m = q.a;
-        b.s = q.b;
-        a = SoftmaxAcc::merge(a, b);
-      }
-    }
-    a = warp_reduce(a);
-    const bool bad = !(a.s > 0.f) || !(a.s < 3.0e38f) || !(a.m > kNegInf) || !(a.m < 3.0e38f);
-    return Partial{a.m, a.s, -1, bad ? 1u : 0u};
-  }
-  BestAcc a;
-  a.init();
-  if (single) {
-    if (lane == 0) {
-      a.v = own.a;
-      a.idx = own.idx;
-      a.nan = own.bad;
-    }
-  } else {
-    for (int c = c0 + lane; c <= c1; c += 32) {
-      const Partial q = ld_cg(parts + c + e);
-      BestAcc b;
-      b.v = q.a;
-      b.idx = q.idx;
-      b.nan = q.bad;
-      a = BestAcc::merge(a, b);
-    }
-  }
-  a = warp_reduce(a);
-  // argmax rows need a finite maximum; race rows carry a block index (-1: no
-  // block with mass), judged by the decision
-  const bool bad = kind == kArgmax ? (a.nan != 0u || a.idx < 0 || !(a.v < 3.0e38f))
-                                   : a.nan != 0u;
-  return Partial{a.v, 0.f, a.idx, bad ? 1u : 0u};
+// A whole row: softmax (a = m, b = S, xy = x[y]) or best (a = value, idx).
+struct RowRes {
+  float a, b, xy;
+  int idx;
+  bool bad;
+};
+
+__device__ __forceinline__ RowRes softmax_res(SoftmaxAcc a, float xy) {
+  const bool bad = !(a.s > 0.f) || !(a.s < 3.0e38f) || !(a.m > kNegInf) || !(a.m < 3.0e38f);
+  return RowRes{a.m, a.s, xy, -1, bad};
 }
 
-// Completion of a row segment: partial out; the CTA completing the request's
-// segment count merges the position's rows and decides it.
-template <typename E>
-__device__ void complete_row(const Params& P, const Split& sp, const QItem& it,
-                             const Partial* mb) {
+// argmax rows need a finite maximum; race rows carry a block index (-1: no
+// block with mass), judged by the decision
+__device__ __forceinline__ RowRes best_res(BestAcc a, int kind) {
+  const bool bad = kind == kArgmax ? (a.nan != 0u || a.idx < 0 || !(a.v < 3.0e38f))
+                                   : a.nan != 0u;
+  return RowRes{a.v, 0.f, 0.f, a.idx, bad};
+}
+
+__device__ __forceinline__ RowRes single_res(const Partial& p, int kind) {
+  if (kind == kSoftmax) {
+    SoftmaxAcc a;
+    a.m = p.a;
+    a.s = p.b;
+    return softmax_res(a, __int_as_float(p.idx));
+  }
+  BestAcc a;
+  a.v = p.a;
+  a.idx = p.idx;
+  a.nan = p.bad;
+  return best_res(a, kind);
+}
+
+// The rows of one position from their segments' partials: the target row at
+// list entry et (kind tkind) and, when paired, the draft row at et + 1 -- all
+// partials loaded lane-parallel in one pass.
+__device__ void merge_position(const Params& P, const Partial* parts, const Split& sp, int et,
+                               bool paired, int tkind, RowRes& t, RowRes& d) {
   const int lane = threadIdx.x & 31;
-  const Partial p = it.kind == kSoftmax ? combine_softmax(mb) : combine_best(mb);
+  const int nt = sp.segments(et, P.nb);
+  const int nd = paired ? sp.segments(et + 1, P.nb) : 0;
+  const int ct = sp.first_cta(et, P.nb);
+  const int cd = paired ? sp.first_cta(et + 1, P.nb) : 0;
+  SoftmaxAcc st, sd;
+  st.init();
+  sd.init();
+  BestAcc bt;
+  bt.init();
+  float xyt = 0.f, xyd = 0.f;
+  bool ht = false, hd = false;
+  for (int q = lane; q < nt + nd; q += 32) {
+    const bool is_t = q < nt;
+    const Partial pp = ld_cg(parts + (is_t ? ct + q + et : cd + (q - nt) + et + 1));
+    if (is_t && tkind != kSoftmax) {
+      BestAcc x;
+      x.v = pp.a;
+      x.idx = pp.idx;
+      x.nan = pp.bad;
+      bt = BestAcc::merge(bt, x);
+    } else {
+      SoftmaxAcc x;
+      x.m = pp.a;
+      x.s = pp.b;
+      if (is_t) {
+        st = SoftmaxAcc::merge(st, x);
+        if (pp.bad) {
+          ht = true;
+          xyt = __int_as_float(pp.idx);
+        }
+      } else {
+        sd = SoftmaxAcc::merge(sd, x);
+        if (pp.bad) {
+          hd = true;
+          xyd = __int_as_float(pp.idx);
+        }
+      }
+    }
+  }
+  const float nan = __int_as_float(0x7fc00000);
+  if (tkind == kSoftmax) {
+    st = warp_reduce(st);
+    const unsigned hm = __ballot_sync(0xffffffffu, ht);
+    const float xy = __shfl_sync(0xffffffffu, xyt, hm ? __ffs(hm) - 1 : 0);
+    t = softmax_res(st, hm ? xy : nan);
+  } else {
+    t = best_res(warp_reduce(bt), tkind);
+  }
+  if (paired) {
+    sd = warp_reduce(sd);
+    const unsigned hm = __ballot_sync(0xffffffffu, hd);
+    const float xy = __shfl_sync(0xffffffffu, xyd, hm ? __ffs(hm) - 1 : 0);
+    d = softmax_res(sd, hm ? xy : nan);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Decisions (control warp).  "Speculative Decoding: Medusa, MTP, EAGLE,
+// DFlash, DDTree, and DSpark", section 1: accept y_i with probability
+// min(1, p_i(y_i)/q_i(y_i)), tested as u_i q_i(y_i) < p_i(y_i); at the first
+// rejection draw from [p_i - q_i]_+ (queued for the next wave), after k
+// acceptances draw the bonus from p_k; greedy rounds keep y_i while it equals
+// the target argmax.
+//
+// Decides position i of request q from its merged rows and, while positions
+// are accepted, hands on to the next one: inside the wave by counting the
+// "accepted" signal towards that position (whoever completes its count
+// decides it), past the wave by appending the request to the next wave.
+// ---------------------------------------------------------------------------
+template <typename E>
+__device__ void decide_chain(const Params& P, const Split& sp, const ReqInfo& q, int i, RowRes t,
+                             RowRes d, int y) {
+  const int lane = threadIdx.x & 31;
+  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
+  const bool sampling = q.c > 0.f;
+  for (;;) {
+    if (!sampling) {
+      if (t.bad) {
+        skip_request_warp(P, q.r, q.d0, q.k, kStNonfinite);
+        return;
+      }
+      if (!(i < q.k && y == t.idx)) {
+        finish_request(P, q.r, q.d0, q.k, i, t.idx, true);
+        return;
+      }
+    } else if (i == q.k) {
+      // every draft accepted: the element race inside the winning block
+      if (t.bad || t.idx < 0) {
+        skip_request_warp(P, q.r, q.d0, q.k, kStNonfinite);
+        return;
+      }
+      const char* trow =
+          reinterpret_cast<const char*>(P.target) + (size_t)(q.d0 + q.r + i) * row_bytes;
+      const ResidualRow rr{q.c, 0.f, 0.f, 0.f, 0.f};
+      const int token = inner_race<E, false>(P, trow, nullptr, t.idx, rr, (uint32_t)i, q.rk);
+      finish_request(P, q.r, q.d0, q.k, i, token, false);
+      return;
+    } else {
+      if (t.bad || d.bad) {
+        skip_request_warp(P, q.r, q.d0, q.k, kStNonfinite);
+        return;
+      }
+      const float tp = fmaf(t.xy, q.c, -t.a);  // log2(p(y) S_p)
+      const float tq = fmaf(d.xy, q.c, -d.a);  // log2(q(y) S_q)
+      const float u = accept_uniform(P.key, (uint32_t)i, q.rk.lo, q.rk.hi);
+      // u q(y) < p(y), both sides scaled by S_p S_q 2^-max(tp, tq) > 0
+      bool accept;
+      if (tp == kNegInf) {
+        accept = false;
+      } else if (tq == kNegInf) {
+        accept = true;
+      } else {
+        const float mx = fmaxf(tp, tq);
+        accept = u * (fast_ex2(tq - mx) * t.b) < fast_ex2(tp - mx) * d.b;
+      }
+      if (lane == 0) {
+        if (P.p_y) P.p_y[q.d0 + i] = fast_ex2(tp) / t.b;
+        if (P.q_y) P.q_y[q.d0 + i] = fast_ex2(tq) / d.b;
+        if (P.u_dbg) P.u_dbg[q.d0 + i] = u;
+      }
+      if (!accept) {
+        // first rejection at i: the next wave draws the correction
+        finish_request(P, q.r, q.d0, q.k, i, -1, false);
+        if (lane == 0) {
+          const int at = atomicAdd(P.res_cnt + P.wave, 1);
+          ResEntry re;
+          re.r = q.r;
+          re.j = i;
+          re.d0 = q.d0;
+          re.pad = 0;
+          re.c = q.c;
+          re.mp = t.a;
+          re.inv_sp = 1.f / t.b;
+          re.mq = d.a;
+          re.inv_sq = 1.f / d.b;
+          re.req_lo = q.rk.lo;
+          re.req_hi = q.rk.hi;
+          re.pad2 = 0u;
+          P.res[(size_t)P.wave * P.stride + at] = re;
+        }
+        return;
+      }
+    }
+    // position i accepted (i < k)
+    const int next = i + 1;
+    if (next >= P.pos1) {
+      append_next_wave(P, q, next);
+      return;
+    }
+    const int et = q.base + (sampling ? 2 * (next - P.pos0) : next - P.pos0);
+    const bool paired = sampling && next < q.k;
+    const int tkind = sampling ? (paired ? kSoftmax : kRace) : kArgmax;
+    const int target = sp.segments(et, P.nb) + (paired ? sp.segments(et + 1, P.nb) : 0) + 1;
+    int last = 0;
+    if (lane == 0)
+      last = epoch_add(P.pos_cnt + (size_t)next * P.stride + q.r, P.epoch) == (uint32_t)target;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;  // the last segment of position `next` decides it
+    __threadfence();
+    y = (!sampling && next < q.k) ? P.tokens[q.d0 + next] : -1;
+    merge_position(P, P.part, sp, et, paired, tkind, t, d);
+    i = next;
+  }
+}
+
+// Completion of a row segment: partial out; the CTA that completes the count
+// of the segment's position merges the position's rows and decides it.
+template <typename E>
+__device__ void complete_row(const Params& P, const Split& sp, const QItem& it, const Partial* mb,
+                             float xy) {
+  const int lane = threadIdx.x & 31;
+  Partial p;
+  if (it.kind == kSoftmax) {
+    p = combine_softmax(mb);
+    p.idx = __float_as_int(xy);
+    p.bad = it.yv >= 0 ? 1u : 0u;
+  } else {
+    p = combine_best(mb);
+  }
+  const int i = it.pos;
   const int et = (it.paired && it.is_draft) ? it.e - 1 : it.e;
-  const int nt = sp.last_cta(et, P.nb) - sp.first_cta(et, P.nb) + 1;
-  const int nd = it.paired ? sp.last_cta(et + 1, P.nb) - sp.first_cta(et + 1, P.nb) + 1 : 0;
-  const bool single = nt + nd == 1;
-  if (!single) {
+  const int tkind = it.paired ? kSoftmax : it.kind;
+  const int target = sp.segments(et, P.nb) + (it.paired ? sp.segments(et + 1, P.nb) : 0) +
+                     (i > P.pos0 ? 1 : 0);
+  RowRes t, d{0.f, 0.f, 0.f, -1, false};
+  if (target == 1) {
+    t = single_res(p, tkind);
+  } else {
     int last = 0;
     if (lane == 0) {
       P.part[it.g] = p;
       __threadfence();
-      last = epoch_add(P.pos_cnt + (size_t)P.wave * P.stride + it.r, P.epoch) ==
-             (uint32_t)(nt + nd);
+      last = epoch_add(P.pos_cnt + (size_t)i * P.stride + it.r, P.epoch) == (uint32_t)target;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __threadfence();
+    merge_position(P, P.part, sp, et, it.paired != 0, tkind, t, d);
   }
-  const int tkind = it.paired ? kSoftmax : it.kind;
-  const Partial pt = merge_row(P, P.part, sp, et, tkind, single, p);
-  Partial pd{0.f, 0.f, -1, 0u};
-  if (it.paired) pd = merge_row(P, P.part, sp, et + 1, kSoftmax, false, p);
-  decide<E>(P, it, tkind, pt, pd);
+  const ReqInfo q{it.r, it.d0, it.k, it.base, it.c, RequestKey{it.req_lo, it.req_hi}};
+  decide_chain<E>(P, sp, q, i, t, d, it.y);
 }
 
 // Completion of a residual segment: the CTA completing the count merges the
@@ -888,20 +1061,24 @@ __device__ void complete_residual(const Params& P, const Split& sp, const QItem&
                                   const Partial* mb) {
   const int lane = threadIdx.x & 31;
   const Partial p = combine_best(mb);
-  const int n = sp.last_cta(it.e, P.nb) - sp.first_cta(it.e, P.nb) + 1;
-  if (n > 1) {
+  const int n = sp.segments(it.e, P.nb);
+  RowRes best;
+  if (n == 1) {
+    best = single_res(p, kResidual);
+  } else {
     int last = 0;
     if (lane == 0) {
       P.rpart[it.g] = p;
       __threadfence();
-      last = epoch_add(P.pos_cnt + (size_t)P.wave * P.stride + it.r, P.epoch) == (uint32_t)n;
+      last = epoch_add(P.rcnt + it.r, P.epoch) == (uint32_t)n;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __threadfence();
+    RowRes unused;
+    merge_position(P, P.rpart, sp, it.e, false, kResidual, best, unused);
   }
-  const Partial best = merge_row(P, P.rpart, sp, it.e, kResidual, n == 1, p);
-  const int j = P.wave - 1;
+  const int j = it.pos;
   const RequestKey rk{it.req_lo, it.req_hi};
   int token;
   if (best.idx >= 0) {
@@ -928,19 +1105,19 @@ struct SegGen {
 template <typename E, bool kAligned>
 __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1, QItem& it) {
   const size_t row_bytes = (size_t)P.vocab * E::kBytes;
-  const int i = P.wave;
   it.e = e;
   it.g = (int)blockIdx.x + e;
   it.mp = it.inv_sp = it.mq = it.inv_sq = 0.f;
   it.row2 = nullptr;
-  int r;
   if (phase == 0) {
-    const ResEntry re = P.res[(size_t)(i - 1) * P.stride + e];
-    r = re.r;
+    const ResEntry re = P.res[(size_t)(P.wave - 1) * P.stride + e];
+    it.r = re.r;
     it.kind = kResidual;
     it.d0 = re.d0;
     it.k = 0;
     it.y = -1;
+    it.pos = re.j;
+    it.base = 0;
     it.paired = 0;
     it.is_draft = 0;
     it.c = re.c;
@@ -948,40 +1125,43 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
     it.inv_sp = re.inv_sp;
     it.mq = re.mq;
     it.inv_sq = re.inv_sq;
-    it.row = reinterpret_cast<const char*>(P.target) + (size_t)(re.d0 + r + re.j) * row_bytes;
+    it.req_lo = re.req_lo;
+    it.req_hi = re.req_hi;
+    it.row = reinterpret_cast<const char*>(P.target) + (size_t)(re.d0 + re.r + re.j) * row_bytes;
     it.row2 = reinterpret_cast<const char*>(P.draft) + (size_t)(re.d0 + re.j) * row_bytes;
   } else {
-    const int ent = P.lists[(size_t)i * 2 * P.stride + e];
-    r = ent >> 2;
-    it.is_draft = (ent >> 1) & 1;
-    it.paired = ent & 1;
-    const int d0 = P.doff[r];
-    const int k = P.doff[r + 1] - d0;
-    const float t = P.temperature[r];
-    const bool sampling = req_mode(t) == kSampling;
-    it.d0 = d0;
-    it.k = k;
-    it.y = i < k ? P.tokens[d0 + i] : -1;
-    it.c = sampling ? kLog2e / t : 0.f;
-    it.kind = it.is_draft ? kSoftmax : (sampling ? (i < k ? kSoftmax : kRace) : kArgmax);
+    const Entry en = P.lists[(size_t)P.wave * P.list_cap + e];
+    const int r = en.meta & 0x1fff;
+    it.r = r;
+    it.is_draft = (en.meta >> 13) & 1;
+    it.paired = (en.meta >> 14) & 1;
+    it.k = (en.meta >> 15) & 31;
+    it.pos = (en.meta >> 20) & 31;
+    it.d0 = en.d0;
+    it.c = en.c;
+    it.y = en.y;
+    it.base = en.base;
+    it.req_lo = en.req_lo;
+    it.req_hi = en.req_hi;
+    it.kind = en.c == 0.f ? kArgmax : (it.is_draft || it.pos < it.k ? kSoftmax : kRace);
     it.row = it.is_draft
-                 ? reinterpret_cast<const char*>(P.draft) + (size_t)(d0 + i) * row_bytes
-                 : reinterpret_cast<const char*>(P.target) + (size_t)(d0 + r + i) * row_bytes;
+                 ? reinterpret_cast<const char*>(P.draft) + (size_t)(en.d0 + it.pos) * row_bytes
+                 : reinterpret_cast<const char*>(P.target) + (size_t)(en.d0 + r + it.pos) * row_bytes;
   }
-  it.r = r;
-  const RequestKey rk = request_key(P, r);
-  it.req_lo = rk.lo;
-  it.req_hi = rk.hi;
   if (kAligned) {
     constexpr int kVPB = kRaceBlock / E::kVec;
     it.vbeg = b0 * kVPB;
     it.vend = min(b1 * kVPB, P.nvec);
     const int per = it.kind == kResidual ? kThreads : kThreads * kStageVecs;
     it.nst = (it.vend - it.vbeg + per - 1) / per;
+    const int vy = it.y >= 0 ? it.y / E::kVec : -1;
+    it.yv = (it.kind == kSoftmax && vy >= it.vbeg && vy < it.vend) ? vy : -1;
   } else {
     it.vbeg = b0;
     it.vend = b1;
     it.nst = 0;
+    const int by = it.y >= 0 ? it.y / kRaceBlock : -1;
+    it.yv = (it.kind == kSoftmax && by >= b0 && by < b1) ? by : -1;
   }
 }
 
@@ -1032,26 +1212,34 @@ __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* 
   __syncwarp();
 }
 
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // The plan launch (one CTA): draft offsets, the layout and input checks, the
-// outputs of requests that cannot be verified, and the entries of wave 0.
+// outputs of requests that cannot be verified, and the rows of wave 0.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
   __shared__ int s_w[kPlanThreads / 32 + 1];
   __shared__ uint32_t s_layout;
+  __shared__ int s_doff[kMaxBatch + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kW = kPlanThreads / 32;
 
+  pdl_launch_dependents();  // wave 0 may be scheduled; it waits for this grid
   if (tid == 0) {
     s_layout = 0u;
     P.ctr[kCntStatus] = 0;
   }
-  for (int i = tid; i <= P.max_k; i += kPlanThreads) P.list_cnt[i] = 0;
-  for (int i = tid; i < max(P.max_k, 1); i += kPlanThreads) P.res_cnt[i] = 0;
+  for (int i = tid; i < P.n_waves; i += kPlanThreads) {
+    P.list_cnt[i] = 0;
+    P.res_cnt[i] = 0;
+  }
   __syncthreads();
 
-  // block-wide exclusive scan of v (all threads call it); returns the prefix,
-  // *total gets the sum
+  // block-wide exclusive scan of v (all threads call it); *total gets the sum
   auto scan = [&](int v, int* total) {
     int incl = v;
 #pragma unroll
@@ -1089,11 +1277,11 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
     const int kk = badk ? 0 : k;
     int tot;
     const int ex = scan(kk, &tot);
-    if (r < P.batch) P.doff[r] = carry + ex;
+    if (r < P.batch) s_doff[r] = carry + ex;
     carry += tot;
   }
   if (tid == 0) {
-    P.doff[P.batch] = carry;
+    s_doff[P.batch] = carry;
     if (!s_layout && carry != P.total_draft) s_layout = kStBadTotal;
   }
   __syncthreads();
@@ -1117,16 +1305,18 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
     return;
   }
 
-  // per request: the input checks, then its entries of wave 0
+  // per request: the input checks, then its rows of wave 0
   int written = 0;
-  int* list0 = P.lists;
   for (int base = 0; base < P.batch; base += kPlanThreads) {
     const int r = base + tid;
-    int n = 0;
+    int n = 0, d0 = 0, k = 0;
+    float c = 0.f;
+    bool sampling = false;
     if (r < P.batch) {
-      const int d0 = P.doff[r];
-      const int k = P.doff[r + 1] - d0;
-      const int mode = req_mode(P.temperature[r]);
+      d0 = s_doff[r];
+      k = s_doff[r + 1] - d0;
+      const float t = P.temperature[r];
+      const int mode = req_mode(t);
       uint32_t rs = mode == kBadTemp ? kStBadTemp : 0u;
       for (int i = 0; i < k; ++i) {
         const int y = P.tokens[d0 + i];
@@ -1136,16 +1326,16 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
       if (rs) {
         skip_request_thread(P, r, d0, k, rs);
       } else {
-        n = (mode == kSampling && k > 0) ? 2 : 1;
+        sampling = mode == kSampling;
+        c = sampling ? kLog2e / t : 0.f;
+        n = wave_rows(P, sampling, k, 0);
       }
     }
     int tot;
     const int at = written + scan(n, &tot);
-    if (n == 2) {
-      list0[at] = entry_of(r, 0, 1);
-      list0[at + 1] = entry_of(r, 1, 1);
-    } else if (n == 1) {
-      list0[at] = entry_of(r, 0, 0);
+    if (n > 0) {
+      const RequestKey rk = request_key(P, r);
+      for (int j = 0; j < n; ++j) P.lists[at + j] = wave_entry(P, sampling, r, d0, k, c, rk, 0, j, at);
     }
     written += tot;
   }
@@ -1153,8 +1343,8 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
 }
 
 // ---------------------------------------------------------------------------
-// The wave launch: position P.wave of every request still alive, and the
-// correction draws of the requests rejected at P.wave - 1.
+// The wave launch: positions [pos0, pos1) of every request alive at pos0, and
+// the correction draws of the requests the previous wave rejected.
 // ---------------------------------------------------------------------------
 template <typename E, bool kAligned>
 __global__ void __maxnreg__(128) sv_wave(Params P) {
@@ -1163,11 +1353,15 @@ __global__ void __maxnreg__(128) sv_wave(Params P) {
   __shared__ QItem queue[kQueue];
   __shared__ int s_unit[2];
   __shared__ Partial mailbox[2][kComputeWarps];
+  __shared__ float s_xy[2];
   __shared__ int s_qend;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const bool control = warp == kComputeWarps;
+
+  pdl_launch_dependents();  // the next wave may be scheduled as CTAs of this one exit
+  pdl_wait();               // the previous launch's lists are complete
 
   const int n_rows = P.list_cnt[P.wave];
   const int n_res = P.wave > 0 ? P.res_cnt[P.wave - 1] : 0;
@@ -1208,8 +1402,9 @@ __global__ void __maxnreg__(128) sv_wave(Params P) {
       // ---- compute warps: stream segment u ------------------------------------
       if (type == kUnitItem) {
         const QItem& it = queue[u & (kQueue - 1)];
-        const Partial out = kAligned ? seg_aligned<E>(P, queue, &s_qend, ring, lc, gs, it)
-                                     : seg_scalar<E>(P, it);
+        const Partial out = kAligned
+                                ? seg_aligned<E>(P, queue, &s_qend, ring, lc, gs, it, &s_xy[u & 1])
+                                : seg_scalar<E>(P, it, &s_xy[u & 1]);
         if (lane == 0) mailbox[u & 1][warp] = out;
       }
     } else {
@@ -1219,7 +1414,7 @@ __global__ void __maxnreg__(128) sv_wave(Params P) {
         if (pv.kind == kResidual) {
           complete_residual<E>(P, sp[0], pv, mailbox[(u - 1) & 1]);
         } else {
-          complete_row<E>(P, sp[1], pv, mailbox[(u - 1) & 1]);
+          complete_row<E>(P, sp[1], pv, mailbox[(u - 1) & 1], s_xy[(u - 1) & 1]);
         }
         sg.q_used = cur + 1;  // its queue entry may now be reused
       }

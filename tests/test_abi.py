@@ -49,7 +49,8 @@ def test_calls_on_a_null_handle(lib):
     assert lib.specverify_run(None, None, None, None, None, None, 0, 1, 0,
                               None, None, None, None) == _lib.ERR_INVALID_ARG
     n = ctypes.c_int(-7)
-    assert lib.specverify_launches_per_run(None, ctypes.byref(n)) == _lib.ERR_INVALID_ARG
+    assert lib.specverify_launches_per_run(None, 4, ctypes.byref(n)) == _lib.ERR_INVALID_ARG
+    assert lib.specverify_set_depth(None, 1) == _lib.ERR_INVALID_ARG
     assert n.value == -7
 
 

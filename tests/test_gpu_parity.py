@@ -23,20 +23,22 @@ def _built():
     build.build()
 
 
-def _verifier(inp, dtype, max_batch=None, max_k=None):
+def _verifier(inp, dtype, max_batch=None, max_k=None, depth=0):
     B = len(inp["num_draft"])
     V = inp["target"].shape[1]
-    return Verifier(max(1, max_batch or B), inp["max_k"] if max_k is None else max_k, V, dtype)
+    v = Verifier(max(1, max_batch or B), inp["max_k"] if max_k is None else max_k, V, dtype)
+    v.set_depth(depth)
+    return v
 
 
 def _dtype_of(inp):
     return "bf16" if inp["target"].dtype == np.uint16 else "f32"
 
 
-def _check(inp, seeds=(1,), max_batch=None, max_k=None):
+def _check(inp, seeds=(1,), max_batch=None, max_k=None, depth=0):
     dtype = _dtype_of(inp)
     reps = []
-    with _verifier(inp, dtype, max_batch, max_k) as v:
+    with _verifier(inp, dtype, max_batch, max_k, depth) as v:
         for seed in seeds:
             g = parity.run_gpu(v, inp, seed)
             o = parity.run_oracle(inp, seed)
@@ -146,6 +148,28 @@ def test_random_ragged_batches(dtype, vocab):
     _check(inp, seeds=(3, 99))
 
 
+@pytest.mark.parametrize("depth", [1, 2, 3, 5, 7])
+@pytest.mark.parametrize("dtype,vocab", [("bf16", 4096), ("bf16", 1001), ("f32", 3000)])
+def test_wave_depths(depth, dtype, vocab):
+    """Positions per wave launch change the launches, never the results: every
+    depth is compared with the oracle (aligned and scalar paths, ragged k with
+    k = 0, greedy and sampling requests mixed, groups cut mid-window)."""
+    rng = np.random.default_rng(depth * 7 + vocab)
+    B = 41
+    k = rng.integers(0, 7, size=B)
+    temp = rng.choice([0.0, 0.6, 1.0, 1.3], size=B)
+    inp = cases.random_batch(k, temp, vocab=vocab, sigma_t=2.0, sigma_d=0.6, dtype=dtype,
+                             seed=depth + vocab)
+    inp["max_k"] = 6
+    _check(inp, seeds=(2, 5), depth=depth)
+
+
+@pytest.mark.parametrize("depth", [1, 4])
+def test_small_workload_depths(depth):
+    b = W.make_batch("w1_v32000_bf16", device="cpu")
+    _check(b.numpy_inputs(), seeds=(1, 2), depth=depth)
+
+
 @pytest.mark.parametrize("max_k", [15, 31])
 def test_long_windows(max_k):
     B = 9
@@ -200,12 +224,14 @@ def test_all_zero_drafts_and_empty_batch():
         assert res.accepted_len.numel() == 0
 
 
-def test_rows_after_the_first_rejection_do_not_matter():
+@pytest.mark.parametrize("depth", [1, 2, 6])
+def test_rows_after_the_first_rejection_do_not_matter(depth):
     """Garbage (NaN / +inf) in rows beyond the first rejection changes nothing:
-    those rows are never read."""
+    at depth 1 those rows are never read; at larger depths they may be read but
+    their positions are never decided."""
     inp = cases.random_batch([5] * 48, [1.0] * 24 + [0.0] * 24, vocab=4096, sigma_d=2.5,
                              dtype="bf16", seed=13)
-    with _verifier(inp, "bf16") as v:
+    with _verifier(inp, "bf16", depth=depth) as v:
         base = parity.run_gpu(v, inp, 5)
         A = base["accepted_len"]
         k = inp["num_draft"]
