@@ -83,6 +83,7 @@ typedef enum {
 #define SPECVERIFY_ERR_CUDA (-3)          /* a CUDA runtime call or launch failed */
 #define SPECVERIFY_ERR_DESTROYED (-4)     /* handle already destroyed */
 #define SPECVERIFY_ERR_NO_STAGING (-5)    /* host entry point on a handle made without staging */
+#define SPECVERIFY_ERR_TOO_LARGE (-6)     /* above the static scratch limits (specverify_run_static) */
 
 /* Device status bits (specverify_status). */
 #define SPECVERIFY_STATUS_BAD_TOKEN 1     /* a draft token outside [0, V): request skipped */
@@ -167,6 +168,43 @@ int specverify_run_host(specverify_t h, const void *target_logits, const void *d
                         const float *temperature, uint64_t seed, int batch, int total_draft,
                         int32_t *accepted_len, int32_t *committed_tokens,
                         uint8_t *accept_flags, void *stream);
+
+/* Limits of specverify_run_static. */
+#define SPECVERIFY_STATIC_MAX_BATCH 256
+#define SPECVERIFY_STATIC_MAX_K 7
+
+/*
+ * specverify_run_static -- the verify round of specverify_run without a handle
+ * and without allocating anything: no cudaMalloc/cudaFree, no allocating
+ * library routine.  The pages have no counterpart of this entry point; it
+ * exists for callers that must not allocate device memory (graph capture of a
+ * fixed pool, allocator-free serving loops).
+ *
+ * Scratch is one file-scope static device array of about 0.55 MiB, sized for
+ * batch <= SPECVERIFY_STATIC_MAX_BATCH (256) and max_k <=
+ * SPECVERIFY_STATIC_MAX_K (7) on a grid of at most 1024 CTAs.  On its first use
+ * on a device the call takes the array's address (cudaGetSymbolAddress,
+ * checked), sizes the kernel grids, and clears the array on `stream` (its
+ * completion counters must start at zero); later calls on that device reuse
+ * them.  Every other piece of scratch is reset by the round itself.
+ *
+ * Arguments as specverify_run, plus device, max_k (width of committed_tokens
+ * is max_k + 1; every num_draft must lie in [0, max_k]), vocab and dtype.
+ * Returns SPECVERIFY_ERR_TOO_LARGE, launching nothing, when batch or max_k
+ * exceeds the limits; the other errors as specverify_run.  Status bits are
+ * not reported (there is no handle); inputs that set them still skip their
+ * requests (accepted_len = -1).
+ *
+ * There is one arena per device: calls that overlap in time -- on different
+ * streams, or from different host threads without ordering -- race on it and
+ * produce garbage.  Serialise them on one stream.
+ */
+int specverify_run_static(int device, int max_k, int vocab, int dtype,
+                          const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const int32_t *num_draft,
+                          const float *temperature, uint64_t seed, int batch, int total_draft,
+                          int32_t *accepted_len, int32_t *committed_tokens,
+                          uint8_t *accept_flags, void *stream);
 
 /* Wait for the handle's last stream and return the status bits of its last run
  * in *status_out (host pointer). */

@@ -23,7 +23,7 @@ from . import _lib
 from ._lib import (CREATE_HOST_STAGING, STATUS_BAD_K, STATUS_BAD_TEMP, STATUS_BAD_TOKEN,
                    STATUS_BAD_TOTAL, STATUS_NO_DRAFT, STATUS_NONFINITE)
 
-__all__ = ["Verifier", "VerifyResult", "SpecVerifyError", "verify",
+__all__ = ["Verifier", "VerifyResult", "SpecVerifyError", "verify", "verify_static",
            "STATUS_BAD_TOKEN", "STATUS_BAD_K", "STATUS_BAD_TEMP", "STATUS_NONFINITE",
            "STATUS_BAD_TOTAL", "STATUS_NO_DRAFT"]
 
@@ -190,6 +190,27 @@ class Verifier:
             self.close()
         except Exception:
             pass
+
+
+def verify_static(target, draft, tokens, num_draft, temperature, seed: int, max_k: int,
+                  accepted_len, committed, flags, stream=None) -> None:
+    """One verify round through specverify_run_static: no handle and no device
+    allocation (scratch is the library's static arena; batch <= 256, max_k <= 7).
+    Outputs go to the caller's tensors: accepted_len [B] int32, committed
+    [B, max_k + 1] int32, flags [sum k] uint8.  Calls that overlap in time race
+    on the arena: keep them on one stream."""
+    lib = _lib.load()
+    dtype = "bf16" if target.dtype == torch.bfloat16 else "f32"
+    code_dtype = _DTYPES[dtype][0]
+    dev = target.device
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    d = draft if (draft is not None and draft.numel()) else None
+    code = lib.specverify_run_static(
+        dev.index, int(max_k), int(target.shape[1]), code_dtype, _ptr(target), _ptr(d),
+        _ptr(tokens), _ptr(num_draft), _ptr(temperature), int(seed) & (2**64 - 1),
+        int(num_draft.shape[0]), int(tokens.shape[0]), _ptr(accepted_len), _ptr(committed),
+        _ptr(flags), ctypes.c_void_p(s.cuda_stream))
+    _check(code, "specverify_run_static")
 
 
 def verify(target, draft, tokens, num_draft, temperature, seed: int, max_k: int | None = None,

@@ -19,6 +19,10 @@ ERR_DTYPE = -2
 ERR_CUDA = -3
 ERR_DESTROYED = -4
 ERR_NO_STAGING = -5
+ERR_TOO_LARGE = -6
+
+STATIC_MAX_BATCH = 256
+STATIC_MAX_K = 7
 
 STATUS_BAD_TOKEN = 1
 STATUS_BAD_K = 2
@@ -73,6 +77,9 @@ def load(path: str | None = None):
     lib.specverify_set_timing_events.restype = I
     lib.specverify_launches_per_run.argtypes = [P, I, ctypes.POINTER(ctypes.c_int)]
     lib.specverify_launches_per_run.restype = I
+    lib.specverify_run_static.argtypes = [I, I, I, I, P, P, P, P, P, ctypes.c_uint64, I, I,
+                                          P, P, P, P]
+    lib.specverify_run_static.restype = I
     lib.specverify_set_depth.argtypes = [P, I]
     lib.specverify_set_depth.restype = I
     lib.specverify_destroy.argtypes = [P]

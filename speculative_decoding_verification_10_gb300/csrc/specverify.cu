@@ -1,14 +1,17 @@
 // specverify.cu -- host side of the C ABI declared in include/specverify.h.
 //
 // Argument checking, scratch ownership and the launches of a verify round
-// (a plan launch and one wave launch per draft position).  All device work
-// lives in sv_kernels.cuh.
+// (a plan launch and a few wave launches).  All device work lives in
+// sv_kernels.cuh.  Two owners of scratch memory share one launch path: a
+// handle (cudaMalloc at create) and a fixed-size static device arena
+// (specverify_run_static, no allocation at all).
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "specverify.h"
@@ -19,7 +22,7 @@ namespace {
 constexpr uint32_t kLiveMagic = 0x53564c56u;  // "SVLV"
 constexpr uint32_t kDeadMagic = 0x53564444u;  // "SVDD"
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct DeviceGuard {
   int prev = -1;
@@ -34,24 +37,280 @@ struct DeviceGuard {
   }
 };
 
-}  // namespace
+// ---------------------------------------------------------------------------
+// Scratch: byte offsets of every piece, sized for `mb` requests, positions
+// 0..max_k, every wave depth 1..max_k+1 and a grid of at most `grid` CTAs.
+// ---------------------------------------------------------------------------
+struct ScratchLayout {
+  size_t lists, lcnt, res, rcnt, pos, rescnt, part, rpart, ctr, bytes;
+};
 
-struct specverify_ctx {
-  uint32_t magic;
-  int device, max_batch, max_k, vocab, dtype, elem_bytes;
-  int num_sms, grid_aligned, grid_scalar;
-  int depth_setting;  // 0: chosen per run from the batch size
-  void* scratch;
-  size_t scratch_bytes;
+constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid) {
+  size_t list_entries = 0, max_waves = 0, max_cap = 0;
+  for (int d = 1; d <= max_k + 1; ++d) {
+    const size_t w = (size_t)sv::wave_count(max_k, d), cap = 2 * (size_t)d * mb;
+    list_entries = std::max(list_entries, w * cap);
+    max_waves = std::max(max_waves, w);
+    max_cap = std::max(max_cap, cap);
+  }
+  ScratchLayout L{};
+  size_t off = 0;
+  L.lists = off;
+  off = align_up(off + sizeof(sv::Entry) * list_entries, 256);
+  L.lcnt = off;
+  off = align_up(off + sizeof(int) * max_waves, 256);
+  L.res = off;
+  off = align_up(off + sizeof(sv::ResEntry) * max_waves * mb, 256);
+  L.rcnt = off;
+  off = align_up(off + sizeof(int) * max_waves, 256);
+  L.pos = off;
+  off = align_up(off + sizeof(unsigned long long) * ((size_t)max_k + 1) * mb, 256);
+  L.rescnt = off;
+  off = align_up(off + sizeof(unsigned long long) * mb, 256);
+  L.part = off;
+  off = align_up(off + sizeof(sv::Partial) * (grid + max_cap), 256);
+  L.rpart = off;
+  off = align_up(off + sizeof(sv::Partial) * (grid + mb), 256);
+  L.ctr = off;
+  off = align_up(off + sizeof(int) * sv::kCntCount, 256);
+  L.bytes = off;
+  return L;
+}
+
+struct Scratch {
   sv::Entry* lists;
   int* list_cnt;
   sv::ResEntry* res;
   int* res_cnt;
-  unsigned long long* pos_cnt;
-  unsigned long long* rcnt;
+  unsigned long long* pos_cnt;  // epoch-tagged: must start at zero
+  unsigned long long* rcnt;     // epoch-tagged: must start at zero
   sv::Partial* part;
   sv::Partial* rpart;
   int* ctr;
+};
+
+Scratch scratch_at(char* b, const ScratchLayout& L) {
+  Scratch s;
+  s.lists = reinterpret_cast<sv::Entry*>(b + L.lists);
+  s.list_cnt = reinterpret_cast<int*>(b + L.lcnt);
+  s.res = reinterpret_cast<sv::ResEntry*>(b + L.res);
+  s.res_cnt = reinterpret_cast<int*>(b + L.rcnt);
+  s.pos_cnt = reinterpret_cast<unsigned long long*>(b + L.pos);
+  s.rcnt = reinterpret_cast<unsigned long long*>(b + L.rescnt);
+  s.part = reinterpret_cast<sv::Partial*>(b + L.part);
+  s.rpart = reinterpret_cast<sv::Partial*>(b + L.rpart);
+  s.ctr = reinterpret_cast<int*>(b + L.ctr);
+  return s;
+}
+
+size_t ring_bytes() { return sizeof(uint4) * sv::kStages * sv::kStageVecs * sv::kThreads; }
+
+template <typename E>
+const void* wave_kernel(bool aligned) {
+  return aligned ? reinterpret_cast<const void*>(sv::sv_wave<E, true>)
+                 : reinterpret_cast<const void*>(sv::sv_wave<E, false>);
+}
+
+// Grids of the wave kernels on the current device: every CTA resident at once.
+struct KernelShape {
+  int grid_aligned, grid_scalar;
+};
+
+bool kernel_shape(int device, int dtype, KernelShape* out) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return false;
+  int occ[2] = {0, 0};
+  for (int a = 0; a < 2; ++a) {
+    const void* fn = dtype == SPECVERIFY_BF16 ? wave_kernel<sv::BF16>(a == 1)
+                                              : wave_kernel<sv::F32>(a == 1);
+    const size_t sm = a == 1 ? ring_bytes() : 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[a], fn, sv::kBlock, sm) !=
+            cudaSuccess)
+      return false;
+  }
+  if (occ[0] < 1 || occ[1] < 1) return false;
+  out->grid_scalar = occ[0] * sms;
+  out->grid_aligned = occ[1] * sms;
+  return true;
+}
+
+// What a round needs besides its arguments.
+struct RunConfig {
+  int device, max_batch, max_k, vocab, dtype, elem_bytes;
+  int depth_setting;  // 0: chosen per run from the batch size
+  KernelShape shape;
+  Scratch sc;
+};
+
+// Batches whose whole verify window (every row of every position) is at most
+// this many bytes are verified in one wave of all positions: reading rows past
+// a rejection costs less than a launch per position there.
+constexpr double kShallowBytes = 192.0 * (1 << 20);
+
+// Positions per wave for a run of `batch` requests.
+int run_depth(const RunConfig& c, int batch) {
+  if (c.depth_setting > 0) return c.depth_setting;
+  const double window = (double)batch * (2.0 * c.max_k + 1.0) * c.vocab * c.elem_bytes;
+  return window <= kShallowBytes ? c.max_k + 1 : 1;
+}
+
+// A wave launch that may begin while the previous launch of the stream is
+// finishing (programmatic dependent launch; the kernel waits for it first).
+template <typename K>
+cudaError_t launch_wave(K kernel, int grid, size_t smem, cudaStream_t s, const sv::Params& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(sv::kBlock);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
+// One round: the plan launch, then the waves (a wave with nothing to do
+// returns at once), optionally bracketed by two events.
+template <typename E>
+int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
+                 cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+  if (ev_start && cudaEventRecord(ev_start, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+  sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
+  const size_t smem = aligned ? ring_bytes() : 0;
+  const int grid = aligned ? c.shape.grid_aligned : c.shape.grid_scalar;
+  for (int w = 0; w < P.n_waves; ++w) {
+    P.wave = w;
+    P.pos0 = std::min(w * P.depth, c.max_k + 1);
+    P.pos1 = std::min((w + 1) * P.depth, c.max_k + 1);
+    const cudaError_t e = aligned ? launch_wave(sv::sv_wave<E, true>, grid, smem, s, P)
+                                  : launch_wave(sv::sv_wave<E, false>, grid, smem, s, P);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return SPECVERIFY_ERR_CUDA;
+    }
+  }
+  if (ev_stop && cudaEventRecord(ev_stop, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
+}
+
+struct RunArgs {
+  const void* target_logits;
+  const void* draft_logits;
+  const int32_t* draft_tokens;
+  const int32_t* num_draft;
+  const float* temperature;
+  uint64_t seed;
+  int batch, total_draft;
+  int32_t* accepted_len;
+  int32_t* committed_tokens;
+  uint8_t* accept_flags;
+  const int64_t* request_ids;
+  float* p_y;
+  float* q_y;
+  float* u;
+  int32_t* req_status;
+};
+
+// Checks that need no device (the batch must already be in range).
+int check_args(const RunConfig& c, const RunArgs& a) {
+  if (a.total_draft < 0 || (long long)a.total_draft > (long long)a.batch * c.max_k)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  if (a.batch == 0) return SPECVERIFY_OK;
+  if (!a.target_logits || !a.num_draft || !a.temperature || !a.accepted_len ||
+      !a.committed_tokens)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  if (a.total_draft > 0 && (!a.draft_tokens || !a.accept_flags)) return SPECVERIFY_ERR_INVALID_ARG;
+  const uintptr_t ea = (uintptr_t)(c.elem_bytes - 1);
+  if (((uintptr_t)a.target_logits & ea) || ((uintptr_t)a.draft_logits & ea))
+    return SPECVERIFY_ERR_INVALID_ARG;
+  return SPECVERIFY_OK;
+}
+
+// Enqueues one round (a.batch > 0, arguments checked) on the current device.
+int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStream_t s,
+                  cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+  sv::Params P;
+  std::memset(&P, 0, sizeof P);
+  P.target = a.target_logits;
+  P.draft = a.total_draft > 0 ? a.draft_logits : nullptr;
+  P.tokens = a.draft_tokens;
+  P.num_draft = a.num_draft;
+  P.temperature = a.temperature;
+  P.request_ids = a.request_ids;
+  P.key = sv::PhiloxKey{(uint32_t)(a.seed & 0xffffffffu), (uint32_t)(a.seed >> 32)};
+  P.batch = a.batch;
+  P.total_draft = a.total_draft;
+  P.max_k = c.max_k;
+  P.vocab = c.vocab;
+  P.epoch = epoch;
+  P.depth = run_depth(c, a.batch);
+  P.n_waves = sv::wave_count(c.max_k, P.depth);
+  P.list_cap = 2 * P.depth * c.max_batch;
+  P.nb = (c.vocab + sv::kRaceBlock - 1) / sv::kRaceBlock;
+  P.nvec = (int)((size_t)c.vocab * c.elem_bytes / 16);
+  const int block_bytes = sv::kRaceBlock * c.elem_bytes;
+  P.min_span = std::max(1, sv::kMinSpanBytes / block_bytes);
+  P.min_span_res = std::max(1, sv::kMinSpanBytes / (2 * block_bytes));
+  P.stride = c.max_batch;
+  P.accepted_len = a.accepted_len;
+  P.committed = a.committed_tokens;
+  P.flags = a.accept_flags;
+  P.p_y = a.p_y;
+  P.q_y = a.q_y;
+  P.u_dbg = a.u;
+  P.req_status = a.req_status;
+  P.lists = c.sc.lists;
+  P.list_cnt = c.sc.list_cnt;
+  P.res = c.sc.res;
+  P.res_cnt = c.sc.res_cnt;
+  P.pos_cnt = c.sc.pos_cnt;
+  P.rcnt = c.sc.rcnt;
+  P.part = c.sc.part;
+  P.rpart = c.sc.rpart;
+  P.ctr = c.sc.ctr;
+  // the vector path needs every row on a 16-byte boundary
+  const bool aligned = ((size_t)c.vocab * c.elem_bytes) % 16 == 0 &&
+                       ((uintptr_t)a.target_logits & 15u) == 0 &&
+                       ((uintptr_t)P.draft & 15u) == 0;
+  return c.dtype == SPECVERIFY_BF16 ? launch_round<sv::BF16>(c, P, aligned, s, ev_start, ev_stop)
+                                    : launch_round<sv::F32>(c, P, aligned, s, ev_start, ev_stop);
+}
+
+// ---------------------------------------------------------------------------
+// The static arena of specverify_run_static: a fixed-size device array, set up
+// once per device (its address, the kernel grids, zeroed counters).
+// ---------------------------------------------------------------------------
+constexpr int kStaticMaxDevices = 64;
+constexpr size_t kStaticGrid = 1024;  // CTAs a wave of the static path may use
+constexpr ScratchLayout kStaticLayout =
+    scratch_layout(SPECVERIFY_STATIC_MAX_BATCH, SPECVERIFY_STATIC_MAX_K, kStaticGrid);
+
+struct StaticDevice {
+  bool ready;
+  char* base;
+  KernelShape shape[2];  // per dtype
+  uint32_t epoch;
+};
+
+StaticDevice g_static_dev[kStaticMaxDevices];
+std::mutex g_static_mu;
+
+}  // namespace
+
+// The arena (file scope, static storage on the device).
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticLayout.bytes];
+
+struct specverify_ctx {
+  uint32_t magic;
+  RunConfig cfg;
+  void* scratch;
   uint32_t epoch;
   // staging for specverify_run_host
   void* stage;
@@ -79,145 +338,23 @@ static int check_handle(specverify_t h) {
   return SPECVERIFY_OK;
 }
 
-static size_t ring_bytes() {
-  return sizeof(uint4) * sv::kStages * sv::kStageVecs * sv::kThreads;
-}
-
-// The kernels of one dtype: the wave kernel for 16-byte aligned rows and the
-// scalar one for any other row layout.
-template <typename E>
-struct Kernels {
-  static void* wave(bool aligned) {
-    return aligned ? reinterpret_cast<void*>(sv::sv_wave<E, true>)
-                   : reinterpret_cast<void*>(sv::sv_wave<E, false>);
-  }
-};
-
-// Batches whose whole verify window (every row of every position) is at most
-// this many bytes are verified in one wave of all positions: reading rows past
-// a rejection costs less than a launch per position there.
-constexpr double kShallowBytes = 192.0 * (1 << 20);
-
-// Positions per wave for a run of `batch` requests.
-static int run_depth(const specverify_ctx* h, int batch) {
-  if (h->depth_setting > 0) return h->depth_setting;
-  const double window = (double)batch * (2.0 * h->max_k + 1.0) * h->vocab * h->elem_bytes;
-  return window <= kShallowBytes ? h->max_k + 1 : 1;
-}
-
-// A wave launch that may begin while the previous launch of the stream is
-// finishing (programmatic dependent launch; the kernel waits for it first).
-template <typename K>
-static cudaError_t launch_wave(K kernel, int grid, size_t smem, cudaStream_t s,
-                               const sv::Params& P) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(sv::kBlock);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, P);
-}
-
-// One round: the plan launch, then the waves (a wave with nothing to do
-// returns at once).
-template <typename E>
-static int launch_round(specverify_ctx* h, sv::Params P, bool aligned, cudaStream_t s) {
-  const int slot = h->n_events > 0 ? (int)(h->run_counter % (unsigned long long)h->n_events) : -1;
-  h->run_counter++;
-  if (slot >= 0 && cudaEventRecord(h->ev_start[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-  sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
-  const size_t smem = aligned ? ring_bytes() : 0;
-  const int grid = aligned ? h->grid_aligned : h->grid_scalar;
-  for (int w = 0; w < P.n_waves; ++w) {
-    P.wave = w;
-    P.pos0 = std::min(w * P.depth, h->max_k + 1);
-    P.pos1 = std::min((w + 1) * P.depth, h->max_k + 1);
-    const cudaError_t e = aligned ? launch_wave(sv::sv_wave<E, true>, grid, smem, s, P)
-                                  : launch_wave(sv::sv_wave<E, false>, grid, smem, s, P);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return SPECVERIFY_ERR_CUDA;
-    }
-  }
-  if (slot >= 0 && cudaEventRecord(h->ev_stop[slot], s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
-}
-
-static int run_impl(specverify_t h, const void* target_logits, const void* draft_logits,
-                    const int32_t* draft_tokens, const int32_t* num_draft,
-                    const float* temperature, uint64_t seed, int batch, int total_draft,
-                    int32_t* accepted_len, int32_t* committed_tokens, uint8_t* accept_flags,
-                    const int64_t* request_ids, float* p_y, float* q_y, float* u,
-                    int32_t* req_status, void* stream) {
+static int run_impl(specverify_t h, const RunArgs& a, void* stream) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
-  if (batch < 0 || batch > h->max_batch) return SPECVERIFY_ERR_INVALID_ARG;
-  if (total_draft < 0 || (long long)total_draft > (long long)batch * h->max_k)
-    return SPECVERIFY_ERR_INVALID_ARG;
-  if (batch == 0) {
+  if (a.batch < 0 || a.batch > h->cfg.max_batch) return SPECVERIFY_ERR_INVALID_ARG;
+  rc = check_args(h->cfg, a);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (a.batch == 0) {
     h->last_run_empty = true;
     return SPECVERIFY_OK;
   }
-  if (!target_logits || !num_draft || !temperature || !accepted_len || !committed_tokens)
-    return SPECVERIFY_ERR_INVALID_ARG;
-  if (total_draft > 0 && (!draft_tokens || !accept_flags)) return SPECVERIFY_ERR_INVALID_ARG;
-  const uintptr_t ea = (uintptr_t)(h->elem_bytes - 1);
-  if (((uintptr_t)target_logits & ea) || ((uintptr_t)draft_logits & ea))
-    return SPECVERIFY_ERR_INVALID_ARG;
-
-  sv::Params P;
-  std::memset(&P, 0, sizeof P);
-  P.target = target_logits;
-  P.draft = total_draft > 0 ? draft_logits : nullptr;
-  P.tokens = draft_tokens;
-  P.num_draft = num_draft;
-  P.temperature = temperature;
-  P.request_ids = request_ids;
-  P.key = sv::PhiloxKey{(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
-  P.batch = batch;
-  P.total_draft = total_draft;
-  P.max_k = h->max_k;
-  P.vocab = h->vocab;
-  P.epoch = ++h->epoch;  // never 0: 0 is the initial value of every tag
-  P.depth = run_depth(h, batch);
-  P.n_waves = sv::wave_count(h->max_k, P.depth);
-  P.list_cap = 2 * P.depth * h->max_batch;
-  P.nb = (h->vocab + sv::kRaceBlock - 1) / sv::kRaceBlock;
-  P.nvec = (int)((size_t)h->vocab * h->elem_bytes / 16);
-  const int block_bytes = sv::kRaceBlock * h->elem_bytes;
-  P.min_span = std::max(1, sv::kMinSpanBytes / block_bytes);
-  P.min_span_res = std::max(1, sv::kMinSpanBytes / (2 * block_bytes));
-  P.stride = h->max_batch;
-  P.accepted_len = accepted_len;
-  P.committed = committed_tokens;
-  P.flags = accept_flags;
-  P.p_y = p_y;
-  P.q_y = q_y;
-  P.u_dbg = u;
-  P.req_status = req_status;
-  P.lists = h->lists;
-  P.list_cnt = h->list_cnt;
-  P.res = h->res;
-  P.res_cnt = h->res_cnt;
-  P.pos_cnt = h->pos_cnt;
-  P.rcnt = h->rcnt;
-  P.part = h->part;
-  P.rpart = h->rpart;
-  P.ctr = h->ctr;
-  // the vector path needs every row on a 16-byte boundary
-  const bool aligned = ((size_t)h->vocab * h->elem_bytes) % 16 == 0 &&
-                       ((uintptr_t)target_logits & 15u) == 0 &&
-                       ((uintptr_t)P.draft & 15u) == 0;
-
-  DeviceGuard guard(h->device);
+  DeviceGuard guard(h->cfg.device);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  rc = h->dtype == SPECVERIFY_BF16 ? launch_round<sv::BF16>(h, P, aligned, s)
-                                   : launch_round<sv::F32>(h, P, aligned, s);
+  const int slot = h->n_events > 0 ? (int)(h->run_counter % (unsigned long long)h->n_events) : -1;
+  h->run_counter++;
+  rc = enqueue_round(h->cfg, a, ++h->epoch,  // never 0: 0 is the initial value of every tag
+                     s, slot >= 0 ? h->ev_start[slot] : nullptr,
+                     slot >= 0 ? h->ev_stop[slot] : nullptr);
   h->last_stream = s;
   h->last_run_empty = false;
   return rc;
@@ -230,8 +367,8 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   if (out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
   *out = nullptr;
   if (dtype != SPECVERIFY_F32 && dtype != SPECVERIFY_BF16) return SPECVERIFY_ERR_DTYPE;
-  if (max_batch < 1 || max_batch > sv::kMaxBatch || max_k < 0 || max_k > 31 || vocab < 1 ||
-      vocab > (1 << 30))
+  if (max_batch < 1 || max_batch > sv::kMaxBatch || max_k < 0 || max_k > sv::kMaxK ||
+      vocab < 1 || vocab > (1 << 30))
     return SPECVERIFY_ERR_INVALID_ARG;
   if ((flags & ~(unsigned)SPECVERIFY_CREATE_HOST_STAGING) != 0u) return SPECVERIFY_ERR_INVALID_ARG;
 
@@ -244,94 +381,40 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
 
   specverify_ctx* h = new (std::nothrow) specverify_ctx();
   if (!h) return SPECVERIFY_ERR_CUDA;
-  h->device = device;
-  h->max_batch = max_batch;
-  h->max_k = max_k;
-  h->vocab = vocab;
-  h->dtype = dtype;
-  h->elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
+  RunConfig& c = h->cfg;
+  c.device = device;
+  c.max_batch = max_batch;
+  c.max_k = max_k;
+  c.vocab = vocab;
+  c.dtype = dtype;
+  c.elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
+  c.depth_setting = 0;
   h->last_stream = nullptr;
+  h->last_run_empty = true;
   h->n_events = 0;
   h->run_counter = 0;
-
-  h->last_run_empty = true;
-  h->depth_setting = 0;
-  bool ok = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) ==
-            cudaSuccess;
-  int occ_a = 0, occ_s = 0;
-  const size_t smem = ring_bytes();
-  for (int a = 0; a < 2 && ok; ++a) {
-    const void* fn = dtype == SPECVERIFY_BF16 ? Kernels<sv::BF16>::wave(a == 1)
-                                              : Kernels<sv::F32>::wave(a == 1);
-    const size_t sm = a == 1 ? smem : 0;
-    ok = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared) == cudaSuccess;
-    ok = ok && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) ==
-                   cudaSuccess;
-    ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(a == 1 ? &occ_a : &occ_s, fn,
-                                                             sv::kBlock, sm) == cudaSuccess;
-  }
-  if (!ok || occ_a < 1 || occ_s < 1) {
+  h->epoch = 0u;
+  h->stage = nullptr;
+  if (!kernel_shape(device, dtype, &c.shape)) {
     cudaGetLastError();
     delete h;
     return SPECVERIFY_ERR_CUDA;
   }
-  // one wave of CTAs, all resident at once
-  h->grid_aligned = occ_a * h->num_sms;
-  h->grid_scalar = occ_s * h->num_sms;
-  const int grid = std::max(h->grid_aligned, h->grid_scalar);
-  const size_t row_bytes = (size_t)vocab * h->elem_bytes;
-
-  // one scratch allocation, carved into aligned pieces
-  size_t off = 0;
-  auto carve = [&](size_t bytes) {
-    const size_t o = off;
-    off = align_up(off + bytes, 256);
-    return o;
-  };
-  // sized for every wave depth D = 1 .. max_k + 1
-  const size_t mb = (size_t)max_batch;
-  size_t list_entries = 0, max_waves = 0, max_cap = 0;
-  for (int d = 1; d <= max_k + 1; ++d) {
-    const size_t w = (size_t)sv::wave_count(max_k, d), cap = 2 * (size_t)d * mb;
-    list_entries = std::max(list_entries, w * cap);
-    max_waves = std::max(max_waves, w);
-    max_cap = std::max(max_cap, cap);
-  }
-  const size_t o_lists = carve(sizeof(sv::Entry) * list_entries);
-  const size_t o_lcnt = carve(sizeof(int) * max_waves);
-  const size_t o_res = carve(sizeof(sv::ResEntry) * max_waves * mb);
-  const size_t o_rcnt = carve(sizeof(int) * max_waves);
-  const size_t o_poscnt = carve(sizeof(unsigned long long) * ((size_t)max_k + 1) * mb);
-  const size_t o_rescnt = carve(sizeof(unsigned long long) * mb);
-  const size_t o_part = carve(sizeof(sv::Partial) * ((size_t)grid + max_cap));
-  const size_t o_rpart = carve(sizeof(sv::Partial) * ((size_t)grid + mb));
-  const size_t o_ctr = carve(sizeof(int) * sv::kCntCount);
-  h->scratch_bytes = off;
-  if (cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess) {
+  const ScratchLayout L = scratch_layout(
+      (size_t)max_batch, max_k, (size_t)std::max(c.shape.grid_aligned, c.shape.grid_scalar));
+  if (cudaMalloc(&h->scratch, L.bytes) != cudaSuccess) {
     cudaGetLastError();
     delete h;
     return SPECVERIFY_ERR_CUDA;
   }
-  if (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess) {
+  if (cudaMemset(h->scratch, 0, L.bytes) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->scratch);
     delete h;
     return SPECVERIFY_ERR_CUDA;
   }
-  char* b = static_cast<char*>(h->scratch);
-  h->lists = reinterpret_cast<sv::Entry*>(b + o_lists);
-  h->list_cnt = reinterpret_cast<int*>(b + o_lcnt);
-  h->res = reinterpret_cast<sv::ResEntry*>(b + o_res);
-  h->res_cnt = reinterpret_cast<int*>(b + o_rcnt);
-  h->pos_cnt = reinterpret_cast<unsigned long long*>(b + o_poscnt);
-  h->rcnt = reinterpret_cast<unsigned long long*>(b + o_rescnt);
-  h->part = reinterpret_cast<sv::Partial*>(b + o_part);
-  h->rpart = reinterpret_cast<sv::Partial*>(b + o_rpart);
-  h->ctr = reinterpret_cast<int*>(b + o_ctr);
-  h->epoch = 0u;
+  c.sc = scratch_at(static_cast<char*>(h->scratch), L);
 
-  h->stage = nullptr;
   if (flags & SPECVERIFY_CREATE_HOST_STAGING) {
     size_t so = 0;
     auto scarve = [&](size_t bytes) {
@@ -339,6 +422,7 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
       so = align_up(so + bytes, 256);
       return o;
     };
+    const size_t row_bytes = (size_t)vocab * c.elem_bytes;
     const size_t rows_t = (size_t)max_batch * (max_k + 1), rows_d = (size_t)max_batch * max_k;
     const size_t s_t = scarve(rows_t * row_bytes);
     const size_t s_d = scarve(rows_d * row_bytes);
@@ -379,9 +463,10 @@ int specverify_run(specverify_t h, const void* target_logits, const void* draft_
                    const float* temperature, uint64_t seed, int batch, int total_draft,
                    int32_t* accepted_len, int32_t* committed_tokens, uint8_t* accept_flags,
                    void* stream) {
-  return run_impl(h, target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
-                  batch, total_draft, accepted_len, committed_tokens, accept_flags, nullptr,
-                  nullptr, nullptr, nullptr, nullptr, stream);
+  const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
+                  batch, total_draft, accepted_len, committed_tokens, accept_flags,
+                  nullptr, nullptr, nullptr, nullptr, nullptr};
+  return run_impl(h, a, stream);
 }
 
 int specverify_run_ex(specverify_t h, const void* target_logits, const void* draft_logits,
@@ -390,9 +475,10 @@ int specverify_run_ex(specverify_t h, const void* target_logits, const void* dra
                       int32_t* accepted_len, int32_t* committed_tokens, uint8_t* accept_flags,
                       const int64_t* request_ids, float* p_y, float* q_y, float* u,
                       int32_t* req_status, void* stream) {
-  return run_impl(h, target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
-                  batch, total_draft, accepted_len, committed_tokens, accept_flags, request_ids,
-                  p_y, q_y, u, req_status, stream);
+  const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
+                  batch, total_draft, accepted_len, committed_tokens, accept_flags,
+                  request_ids, p_y, q_y, u, req_status};
+  return run_impl(h, a, stream);
 }
 
 int specverify_run_host(specverify_t h, const void* target_logits, const void* draft_logits,
@@ -403,17 +489,18 @@ int specverify_run_host(specverify_t h, const void* target_logits, const void* d
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
   if (h->stage == nullptr) return SPECVERIFY_ERR_NO_STAGING;
-  if (batch < 0 || batch > h->max_batch) return SPECVERIFY_ERR_INVALID_ARG;
-  if (total_draft < 0 || (long long)total_draft > (long long)batch * h->max_k)
+  const RunConfig& c = h->cfg;
+  if (batch < 0 || batch > c.max_batch) return SPECVERIFY_ERR_INVALID_ARG;
+  if (total_draft < 0 || (long long)total_draft > (long long)batch * c.max_k)
     return SPECVERIFY_ERR_INVALID_ARG;
   if (batch == 0) return SPECVERIFY_OK;
   if (!target_logits || !num_draft || !temperature || !accepted_len || !committed_tokens)
     return SPECVERIFY_ERR_INVALID_ARG;
   if (total_draft > 0 && (!draft_tokens || !accept_flags)) return SPECVERIFY_ERR_INVALID_ARG;
 
-  DeviceGuard guard(h->device);
+  DeviceGuard guard(c.device);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t row_bytes = (size_t)h->vocab * h->elem_bytes;
+  const size_t row_bytes = (size_t)c.vocab * c.elem_bytes;
   bool ok = true;
   auto h2d = [&](void* dst, const void* src, size_t n) {
     if (n && ok) ok = cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
@@ -431,13 +518,14 @@ int specverify_run_host(specverify_t h, const void* target_logits, const void* d
     cudaGetLastError();
     return SPECVERIFY_ERR_CUDA;
   }
-  rc = run_impl(h, h->st_target, has_draft ? h->st_draft : nullptr, h->st_tokens,
-                h->st_num_draft, h->st_temperature, seed, batch, total_draft, h->st_accepted,
-                h->st_committed, h->st_flags, nullptr, nullptr, nullptr, nullptr, nullptr,
-                stream);
+  const RunArgs a{h->st_target, has_draft ? h->st_draft : nullptr, h->st_tokens,
+                  h->st_num_draft, h->st_temperature, seed, batch, total_draft,
+                  h->st_accepted, h->st_committed, h->st_flags,
+                  nullptr, nullptr, nullptr, nullptr, nullptr};
+  rc = run_impl(h, a, stream);
   if (rc != SPECVERIFY_OK) return rc;
   d2h(accepted_len, h->st_accepted, sizeof(int32_t) * (size_t)batch);
-  d2h(committed_tokens, h->st_committed, sizeof(int32_t) * (size_t)batch * (h->max_k + 1));
+  d2h(committed_tokens, h->st_committed, sizeof(int32_t) * (size_t)batch * (c.max_k + 1));
   d2h(accept_flags, h->st_flags, (size_t)total_draft);
   if (ok) ok = cudaStreamSynchronize(s) == cudaSuccess;
   if (!ok) {
@@ -447,18 +535,78 @@ int specverify_run_host(specverify_t h, const void* target_logits, const void* d
   return SPECVERIFY_OK;
 }
 
+int specverify_run_static(int device, int max_k, int vocab, int dtype,
+                          const void* target_logits, const void* draft_logits,
+                          const int32_t* draft_tokens, const int32_t* num_draft,
+                          const float* temperature, uint64_t seed, int batch, int total_draft,
+                          int32_t* accepted_len, int32_t* committed_tokens,
+                          uint8_t* accept_flags, void* stream) {
+  if (dtype != SPECVERIFY_F32 && dtype != SPECVERIFY_BF16) return SPECVERIFY_ERR_DTYPE;
+  if (device < 0 || device >= kStaticMaxDevices || vocab < 1 || vocab > (1 << 30) || batch < 0 ||
+      max_k < 0)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  if (batch > SPECVERIFY_STATIC_MAX_BATCH || max_k > SPECVERIFY_STATIC_MAX_K)
+    return SPECVERIFY_ERR_TOO_LARGE;
+  RunConfig c;
+  c.device = device;
+  c.max_batch = SPECVERIFY_STATIC_MAX_BATCH;
+  c.max_k = max_k;
+  c.vocab = vocab;
+  c.dtype = dtype;
+  c.elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
+  c.depth_setting = 0;
+  const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
+                  batch, total_draft, accepted_len, committed_tokens, accept_flags,
+                  nullptr, nullptr, nullptr, nullptr, nullptr};
+  int rc = check_args(c, a);
+  if (rc != SPECVERIFY_OK || batch == 0) return rc;
+
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) {
+    cudaGetLastError();
+    return SPECVERIFY_ERR_CUDA;
+  }
+  DeviceGuard guard(device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  StaticDevice& sd = g_static_dev[device];
+  if (!sd.ready) {
+    // set-up, once per device: the arena's address, the kernel grids, and
+    // zero counters (every epoch-tagged counter must start at zero)
+    void* base = nullptr;
+    if (cudaGetSymbolAddress(&base, g_static_scratch) != cudaSuccess || base == nullptr ||
+        !kernel_shape(device, SPECVERIFY_F32, &sd.shape[SPECVERIFY_F32]) ||
+        !kernel_shape(device, SPECVERIFY_BF16, &sd.shape[SPECVERIFY_BF16]) ||
+        cudaMemsetAsync(base, 0, kStaticLayout.bytes, s) != cudaSuccess) {
+      cudaGetLastError();
+      return SPECVERIFY_ERR_CUDA;
+    }
+    for (int t = 0; t < 2; ++t) {
+      sd.shape[t].grid_aligned = std::min<int>(sd.shape[t].grid_aligned, (int)kStaticGrid);
+      sd.shape[t].grid_scalar = std::min<int>(sd.shape[t].grid_scalar, (int)kStaticGrid);
+    }
+    sd.base = static_cast<char*>(base);
+    sd.epoch = 0u;
+    sd.ready = true;
+  }
+  c.shape = sd.shape[dtype];
+  c.sc = scratch_at(sd.base, kStaticLayout);
+  if (++sd.epoch == 0u) ++sd.epoch;  // 0 is the tag of a counter never used
+  return enqueue_round(c, a, sd.epoch, s, nullptr, nullptr);
+}
+
 int specverify_status(specverify_t h, int32_t* status_out) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
   if (status_out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
-  DeviceGuard guard(h->device);
+  DeviceGuard guard(h->cfg.device);
   int32_t st = 0;
   if (h->last_run_empty) {
     *status_out = 0;
     return SPECVERIFY_OK;
   }
   if (cudaStreamSynchronize(h->last_stream) != cudaSuccess ||
-      cudaMemcpy(&st, h->ctr + sv::kCntStatus, sizeof st, cudaMemcpyDeviceToHost) !=
+      cudaMemcpy(&st, h->cfg.sc.ctr + sv::kCntStatus, sizeof st, cudaMemcpyDeviceToHost) !=
           cudaSuccess) {
     cudaGetLastError();
     return SPECVERIFY_ERR_CUDA;
@@ -486,24 +634,24 @@ int specverify_set_timing_events(specverify_t h, int n, void* const* start_event
 int specverify_set_depth(specverify_t h, int depth) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
-  if (depth < 0 || depth > h->max_k + 1) return SPECVERIFY_ERR_INVALID_ARG;
-  h->depth_setting = depth;
+  if (depth < 0 || depth > h->cfg.max_k + 1) return SPECVERIFY_ERR_INVALID_ARG;
+  h->cfg.depth_setting = depth;
   return SPECVERIFY_OK;
 }
 
 int specverify_launches_per_run(specverify_t h, int batch, int* launches_out) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
-  if (launches_out == nullptr || batch < 0 || batch > h->max_batch)
+  if (launches_out == nullptr || batch < 0 || batch > h->cfg.max_batch)
     return SPECVERIFY_ERR_INVALID_ARG;
-  *launches_out = batch == 0 ? 0 : 1 + sv::wave_count(h->max_k, run_depth(h, batch));
+  *launches_out = batch == 0 ? 0 : 1 + sv::wave_count(h->cfg.max_k, run_depth(h->cfg, batch));
   return SPECVERIFY_OK;
 }
 
 int specverify_destroy(specverify_t h) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
-  DeviceGuard guard(h->device);
+  DeviceGuard guard(h->cfg.device);
   // the small host record is kept (marked dead) so later calls report
   // SPECVERIFY_ERR_DESTROYED instead of touching freed memory
   h->magic = kDeadMagic;
@@ -527,6 +675,9 @@ const char* specverify_error_string(int code) {
     case SPECVERIFY_ERR_CUDA: return "CUDA runtime error";
     case SPECVERIFY_ERR_DESTROYED: return "handle already destroyed";
     case SPECVERIFY_ERR_NO_STAGING: return "handle has no host staging buffers";
+    case SPECVERIFY_ERR_TOO_LARGE:
+      return "batch or max_k above the static scratch limits (SPECVERIFY_STATIC_MAX_BATCH, "
+             "SPECVERIFY_STATIC_MAX_K)";
     default: return "unknown error code";
   }
 }

@@ -67,7 +67,7 @@ constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite
 // Number of waves of a round with positions 0..max_k taken D at a time: one
 // per group of D positions, plus one for the residual draws of the last group
 // when it can reject (D > 1).
-__host__ __device__ __forceinline__ int wave_count(int max_k, int depth) {
+__host__ __device__ constexpr int wave_count(int max_k, int depth) {
   return (max_k + depth) / depth + (depth > 1 ? 1 : 0);
 }
 

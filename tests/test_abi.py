@@ -65,3 +65,17 @@ def test_no_device_reports_cuda_error(lib):
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         _lib.load(str(tmp_path / "missing.so"))
+
+
+def test_static_entry_rejects_inputs_above_its_limits(lib):
+    # checked before any device call: nothing is launched, nothing allocated
+    args = [None] * 5
+    big = lib.specverify_run_static(0, 3, 1024, 1, *args, 1, _lib.STATIC_MAX_BATCH + 1, 0,
+                                    None, None, None, None)
+    assert big == _lib.ERR_TOO_LARGE
+    deep = lib.specverify_run_static(0, _lib.STATIC_MAX_K + 1, 1024, 1, *args, 1, 4, 0,
+                                     None, None, None, None)
+    assert deep == _lib.ERR_TOO_LARGE
+    assert lib.specverify_run_static(0, 3, 1024, 9, *args, 1, 4, 0,
+                                     None, None, None, None) == _lib.ERR_DTYPE
+    assert b"static scratch limits" in lib.specverify_error_string(_lib.ERR_TOO_LARGE)
