@@ -55,6 +55,10 @@ def parse_args():
                     help="requests in the oracle sample (0 = about 10 s of work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "waves", "clusters"],
+                    help="launch layout of a round (results do not depend on it)")
+    ap.add_argument("--depth", type=int, default=0,
+                    help="positions per wave launch (0 = chosen per run)")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per batch (0 = the workload's own); for profiling captures")
     return ap.parse_args()
@@ -286,6 +290,8 @@ def run_ours(args):
     full_window_bytes = b.full_window_bytes()
 
     v = Verifier(b.batch, b.max_k, b.vocab, b.dtype, device=local, host_staging=not args.no_e2e)
+    v.set_schedule(args.schedule)
+    v.set_depth(args.depth)
     out = v.outputs(b.batch, b.total_draft)
     stream = torch.cuda.current_stream(dev)
 
@@ -380,7 +386,8 @@ def run_ours(args):
                    "mean_accepted": float(A.mean()),
                    "l2": "no flush: each step reads %.2f GB of logits, larger than the 129 MB L2"
                          % (rowpass_bytes / 1e9),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "schedule": args.schedule, "depth": args.depth},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "sv_wave", "kernel_ms": kernel_avg_ms,

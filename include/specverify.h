@@ -92,6 +92,7 @@ typedef enum {
 #define SPECVERIFY_STATUS_NONFINITE 8     /* NaN/+inf logit, or no finite logit, in a read row: request skipped */
 #define SPECVERIFY_STATUS_BAD_TOTAL 16    /* sum of num_draft != total_draft: batch skipped */
 #define SPECVERIFY_STATUS_NO_DRAFT 64     /* T > 0 and k > 0 but draft_logits is NULL: request skipped */
+#define SPECVERIFY_STATUS_OVERRUN 128     /* internal: a cluster launch hit its unit cap (a bug); outputs incomplete */
 
 /* Flags for specverify_create_ex. */
 #define SPECVERIFY_CREATE_HOST_STAGING 1  /* allocate device staging for specverify_run_host */
@@ -230,10 +231,27 @@ int specverify_set_timing_events(specverify_t h, int n, void *const *start_event
  */
 int specverify_set_depth(specverify_t h, int depth);
 
+/*
+ * specverify_set_schedule -- how a round is laid out on the GPU.  Results do
+ * not depend on it.
+ *   SPECVERIFY_SCHEDULE_WAVES: a wave launch per group of `depth` positions
+ *     (specverify_set_depth), every request in lockstep;
+ *   SPECVERIFY_SCHEDULE_CLUSTERS: one launch of thread-block clusters, each
+ *     taking requests one at a time and deciding each position as soon as its
+ *     rows are read (16-byte aligned rows only; others use waves);
+ *   SPECVERIFY_SCHEDULE_AUTO (default): waves (the faster layout on every
+ *     batch measured so far).
+ */
+#define SPECVERIFY_SCHEDULE_AUTO 0
+#define SPECVERIFY_SCHEDULE_WAVES 1
+#define SPECVERIFY_SCHEDULE_CLUSTERS 2
+int specverify_set_schedule(specverify_t h, int schedule);
+
 /* Kernel launches a run of `batch` requests makes on handle h (for launch
  * accounting): the plan launch and one launch per wave of `depth` positions
- * (plus one for the last wave's correction draws when depth > 1).  Waves with
- * nothing left to do return at once. */
+ * (plus one for the last wave's correction draws when depth > 1), or the plan
+ * and one cluster launch.  Waves with nothing left to do return at once.
+ * Counts assume 16-byte aligned rows. */
 int specverify_launches_per_run(specverify_t h, int batch, int *launches_out);
 
 /* Free the handle and its device memory.  Further use returns _ERR_DESTROYED

@@ -164,6 +164,12 @@ class Verifier:
                "specverify_launches_per_run")
         return int(n.value)
 
+    def set_schedule(self, schedule: str):
+        """'auto', 'waves' or 'clusters' (see specverify_set_schedule)."""
+        code = {"auto": _lib.SCHEDULE_AUTO, "waves": _lib.SCHEDULE_WAVES,
+                "clusters": _lib.SCHEDULE_CLUSTERS}[schedule]
+        _check(self.lib.specverify_set_schedule(self._h, code), "specverify_set_schedule")
+
     def set_depth(self, depth: int):
         """Positions per wave launch: 1 .. max_k + 1, or 0 to choose per run."""
         _check(self.lib.specverify_set_depth(self._h, depth), "specverify_set_depth")

@@ -21,6 +21,10 @@ ERR_DESTROYED = -4
 ERR_NO_STAGING = -5
 ERR_TOO_LARGE = -6
 
+SCHEDULE_AUTO = 0
+SCHEDULE_WAVES = 1
+SCHEDULE_CLUSTERS = 2
+
 STATIC_MAX_BATCH = 256
 STATIC_MAX_K = 7
 
@@ -80,6 +84,8 @@ def load(path: str | None = None):
     lib.specverify_run_static.argtypes = [I, I, I, I, P, P, P, P, P, ctypes.c_uint64, I, I,
                                           P, P, P, P]
     lib.specverify_run_static.restype = I
+    lib.specverify_set_schedule.argtypes = [P, I]
+    lib.specverify_set_schedule.restype = I
     lib.specverify_set_depth.argtypes = [P, I]
     lib.specverify_set_depth.restype = I
     lib.specverify_destroy.argtypes = [P]

@@ -15,7 +15,7 @@
 #include <new>
 
 #include "specverify.h"
-#include "sv_kernels.cuh"
+#include "sv_cluster.cuh"
 
 namespace {
 
@@ -111,10 +111,14 @@ const void* wave_kernel(bool aligned) {
                  : reinterpret_cast<const void*>(sv::sv_wave<E, false>);
 }
 
-// Grids of the wave kernels on the current device: every CTA resident at once.
+// Grids on the current device, every CTA resident at once: the wave kernels
+// (aligned and scalar rows) and the cluster kernel (clusters of cluster_n).
 struct KernelShape {
   int grid_aligned, grid_scalar;
+  int grid_cluster, cluster_n;
 };
+
+constexpr int kClusterN = 8;  // CTAs per cluster (portable size)
 
 bool kernel_shape(int device, int dtype, KernelShape* out) {
   int sms = 0;
@@ -136,13 +140,38 @@ bool kernel_shape(int device, int dtype, KernelShape* out) {
   if (occ[0] < 1 || occ[1] < 1) return false;
   out->grid_scalar = occ[0] * sms;
   out->grid_aligned = occ[1] * sms;
+  // the cluster kernel: as many clusters as fit at once
+  const void* fc = dtype == SPECVERIFY_BF16 ? reinterpret_cast<const void*>(sv::sv_cluster<sv::BF16>)
+                                            : reinterpret_cast<const void*>(sv::sv_cluster<sv::F32>);
+  if (cudaFuncSetAttribute(fc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+      cudaFuncSetAttribute(fc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_bytes()) !=
+          cudaSuccess)
+    return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(kClusterN * sms));
+  cfg.blockDim = dim3(sv::kBlock);
+  cfg.dynamicSmemBytes = ring_bytes();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterN;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, fc, &cfg) != cudaSuccess || clusters < 1)
+    return false;
+  out->cluster_n = kClusterN;
+  out->grid_cluster = clusters * kClusterN;
   return true;
 }
 
 // What a round needs besides its arguments.
 struct RunConfig {
   int device, max_batch, max_k, vocab, dtype, elem_bytes;
-  int depth_setting;  // 0: chosen per run from the batch size
+  int depth_setting;     // 0: chosen per run from the batch size
+  int schedule_setting;  // SPECVERIFY_SCHEDULE_*
   KernelShape shape;
   Scratch sc;
 };
@@ -157,6 +186,19 @@ int run_depth(const RunConfig& c, int batch) {
   if (c.depth_setting > 0) return c.depth_setting;
   const double window = (double)batch * (2.0 * c.max_k + 1.0) * c.vocab * c.elem_bytes;
   return window <= kShallowBytes ? c.max_k + 1 : 1;
+}
+
+// Cluster launch or waves: waves unless clusters are asked for (and the rows
+// are 16-byte aligned).  Measured on GB300 the wave launches are faster on
+// every workload so far, so they are the default.
+bool run_clusters(const RunConfig& c, int batch, bool aligned) {
+  (void)batch;
+  return aligned && c.schedule_setting == SPECVERIFY_SCHEDULE_CLUSTERS;
+}
+
+bool rows_aligned(const RunConfig& c, const void* target, const void* draft) {
+  return ((size_t)c.vocab * c.elem_bytes) % 16 == 0 && ((uintptr_t)target & 15u) == 0 &&
+         ((uintptr_t)draft & 15u) == 0;
 }
 
 // A wave launch that may begin while the previous launch of the stream is
@@ -176,13 +218,42 @@ cudaError_t launch_wave(K kernel, int grid, size_t smem, cudaStream_t s, const s
   return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 
-// One round: the plan launch, then the waves (a wave with nothing to do
-// returns at once), optionally bracketed by two events.
+// The cluster launch after the plan: clusters of kClusterN CTAs, programmatic
+// dependent launch on the plan.
+template <typename E>
+cudaError_t launch_cluster(const RunConfig& c, cudaStream_t s, const sv::Params& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)c.shape.grid_cluster);
+  cfg.blockDim = dim3(sv::kBlock);
+  cfg.dynamicSmemBytes = ring_bytes();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)c.shape.cluster_n;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, sv::sv_cluster<E>, P);
+}
+
+// One round: the plan launch, then the cluster launch or the waves (a wave
+// with nothing to do returns at once), optionally bracketed by two events.
 template <typename E>
 int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
                  cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (ev_start && cudaEventRecord(ev_start, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
   sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
+  if (P.cluster_mode) {
+    if (launch_cluster<E>(c, s, P) != cudaSuccess) {
+      cudaGetLastError();
+      return SPECVERIFY_ERR_CUDA;
+    }
+    if (ev_stop && cudaEventRecord(ev_stop, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
+  }
   const size_t smem = aligned ? ring_bytes() : 0;
   const int grid = aligned ? c.shape.grid_aligned : c.shape.grid_scalar;
   for (int w = 0; w < P.n_waves; ++w) {
@@ -276,9 +347,14 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
   P.rpart = c.sc.rpart;
   P.ctr = c.sc.ctr;
   // the vector path needs every row on a 16-byte boundary
-  const bool aligned = ((size_t)c.vocab * c.elem_bytes) % 16 == 0 &&
-                       ((uintptr_t)a.target_logits & 15u) == 0 &&
-                       ((uintptr_t)P.draft & 15u) == 0;
+  const bool aligned = rows_aligned(c, a.target_logits, P.draft);
+  if (run_clusters(c, a.batch, aligned)) {
+    P.cluster_mode = 1;
+    P.unit_cap = 2 * a.batch * (c.max_k + 2) + 16;
+    P.depth = 1;
+    P.n_waves = 1;
+    P.list_cap = c.max_batch;
+  }
   return c.dtype == SPECVERIFY_BF16 ? launch_round<sv::BF16>(c, P, aligned, s, ev_start, ev_stop)
                                     : launch_round<sv::F32>(c, P, aligned, s, ev_start, ev_stop);
 }
@@ -389,6 +465,7 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   c.dtype = dtype;
   c.elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
   c.depth_setting = 0;
+  c.schedule_setting = SPECVERIFY_SCHEDULE_AUTO;
   h->last_stream = nullptr;
   h->last_run_empty = true;
   h->n_events = 0;
@@ -555,6 +632,7 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
   c.dtype = dtype;
   c.elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
   c.depth_setting = 0;
+  c.schedule_setting = SPECVERIFY_SCHEDULE_AUTO;
   const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
                   batch, total_draft, accepted_len, committed_tokens, accept_flags,
                   nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -584,6 +662,8 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
     for (int t = 0; t < 2; ++t) {
       sd.shape[t].grid_aligned = std::min<int>(sd.shape[t].grid_aligned, (int)kStaticGrid);
       sd.shape[t].grid_scalar = std::min<int>(sd.shape[t].grid_scalar, (int)kStaticGrid);
+      sd.shape[t].grid_cluster = std::min<int>(sd.shape[t].grid_cluster,
+                                               (int)kStaticGrid / kClusterN * kClusterN);
     }
     sd.base = static_cast<char*>(base);
     sd.epoch = 0u;
@@ -639,12 +719,28 @@ int specverify_set_depth(specverify_t h, int depth) {
   return SPECVERIFY_OK;
 }
 
+int specverify_set_schedule(specverify_t h, int schedule) {
+  int rc = check_handle(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (schedule != SPECVERIFY_SCHEDULE_AUTO && schedule != SPECVERIFY_SCHEDULE_WAVES &&
+      schedule != SPECVERIFY_SCHEDULE_CLUSTERS)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  h->cfg.schedule_setting = schedule;
+  return SPECVERIFY_OK;
+}
+
 int specverify_launches_per_run(specverify_t h, int batch, int* launches_out) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
   if (launches_out == nullptr || batch < 0 || batch > h->cfg.max_batch)
     return SPECVERIFY_ERR_INVALID_ARG;
-  *launches_out = batch == 0 ? 0 : 1 + sv::wave_count(h->cfg.max_k, run_depth(h->cfg, batch));
+  // rows are taken as 16-byte aligned (the caller's tensors decide in the end)
+  if (batch == 0)
+    *launches_out = 0;
+  else if (run_clusters(h->cfg, batch, rows_aligned(h->cfg, nullptr, nullptr)))
+    *launches_out = 2;
+  else
+    *launches_out = 1 + sv::wave_count(h->cfg.max_k, run_depth(h->cfg, batch));
   return SPECVERIFY_OK;
 }
 

@@ -121,6 +121,20 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Publishing a count in shared memory: a release store by the writer, an
+// acquire load by the readers (orders only what these two accesses need, unlike
+// a fence, which would also wait for the reader's copies in flight).
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+  int v;
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_shared(int* p, int v) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Loads.  Logit rows are streamed once: 16-byte non-coherent loads that skip L1.
 // ---------------------------------------------------------------------------

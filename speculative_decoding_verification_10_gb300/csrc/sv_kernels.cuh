@@ -62,7 +62,7 @@ enum UnitType : int { kUnitEnd = 0, kUnitItem = 1 };
 
 // Status bits (equal to the SPECVERIFY_STATUS_* values of the header).
 constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite = 8u,
-                   kStBadTotal = 16u, kStNoDraft = 64u;
+                   kStBadTotal = 16u, kStNoDraft = 64u, kStOverrun = 128u;
 
 // Number of waves of a round with positions 0..max_k taken D at a time: one
 // per group of D positions, plus one for the residual draws of the last group
@@ -104,7 +104,7 @@ struct __align__(16) ResEntry {
   uint32_t req_lo, req_hi, pad2;
 };
 
-enum Counter : int { kCntStatus = 0, kCntCount = 4 };
+enum Counter : int { kCntStatus = 0, kCntClaim = 1, kCntCount = 4 };
 
 struct Params {
   const void* target;
@@ -126,6 +126,8 @@ struct Params {
   int min_span_res;  // ... and of the residual phase
   int stride;        // capacity of a request-indexed array (max_batch)
   int list_cap;      // entries per wave list: 2 * D * stride
+  int cluster_mode;  // the plan lists one entry per request (the cluster launch)
+  int unit_cap;      // cluster launch: more units than any round needs
   int32_t* accepted_len;
   int32_t* committed;
   uint8_t* flags;
@@ -417,8 +419,7 @@ struct LoadCursor {
 
   // s_qend: segments the control warp has queued, or -1 - n once all n are.
   __device__ __forceinline__ void open(const QItem* queue, const int* s_qend) {
-    const int qe = *reinterpret_cast<const volatile int*>(s_qend);
-    __threadfence_block();
+    const int qe = ld_acquire_shared(s_qend);
     const int avail = qe >= 0 ? qe : -1 - qe;
     active = q < avail;
     if (active) {
@@ -466,26 +467,6 @@ __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend,
   ++g_stage;
 }
 
-// Streams a segment stage by stage: f(v0, v1, st, full).  Only the last stage
-// of a segment can reach past its end (full == false there); the caller pads
-// the vectors beyond vend.
-template <typename F>
-__device__ __forceinline__ void consume(const QItem* queue, const int* s_qend, uint4* ring,
-                                        LoadCursor& lc, int& g_stage, const QItem& it, F&& f) {
-  const int per = it.kind == kResidual ? kThreads : kStageVecs * kThreads;
-  const int nfull = (it.vend - it.vbeg) / per;
-  for (int st = 0; st < nfull; ++st) {
-    uint4 v0, v1;
-    ring_take(queue, s_qend, ring, lc, g_stage, v0, v1);
-    f(v0, v1, st, true);
-  }
-  if (nfull < it.nst) {
-    uint4 v0, v1;
-    ring_take(queue, s_qend, ring, lc, g_stage, v0, v1);
-    f(v0, v1, nfull, false);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Segment reductions (compute threads).  Each returns this warp's partial; a
 // softmax segment that holds the draft token y also leaves x[y] in *s_xy.
@@ -493,20 +474,27 @@ __device__ __forceinline__ void consume(const QItem* queue, const int* s_qend, u
 template <typename E>
 __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
                                                const int* s_qend, uint4* ring, LoadCursor& lc,
-                                               int& gs, const QItem& it, float* s_xy) {
+                                               int& gs, const QItem& itm, float* s_xy) {
   const int w = threadIdx.x >> 5;
   const int tid = threadIdx.x;
-  const RequestKey rk{it.req_lo, it.req_hi};
-  if (it.kind == kSoftmax) {
+  // the segment's fields in registers (the queue is shared memory, which the
+  // copy ring's memory clobbers would otherwise make the loop reload)
+  const int kind = itm.kind, vbeg = itm.vbeg, vend = itm.vend, nst = itm.nst, pos = itm.pos;
+  const float c = itm.c;
+  const RequestKey rk{itm.req_lo, itm.req_hi};
+  const int per = kind == kResidual ? kThreads : kStageVecs * kThreads;
+  const int nfull = (vend - vbeg) / per;
+  if (kind == kSoftmax) {
     LazySoftmax acc;
     acc.init();
-    const float c = it.c;
-    const int yv = it.yv, ye = it.y & (E::kVec - 1);
-    consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
-      const int vi = it.vbeg + st * kStageVecs * kThreads + tid;
-      if (!full) {
-        if (vi >= it.vend) v0 = E::pad();
-        if (vi + kThreads >= it.vend) v1 = E::pad();
+    const int yv = itm.yv, ye = itm.y & (E::kVec - 1);
+    for (int st = 0; st < nst; ++st) {
+      uint4 v0, v1;
+      ring_take(queue, s_qend, ring, lc, gs, v0, v1);
+      const int vi = vbeg + st * kStageVecs * kThreads + tid;
+      if (st >= nfull) {
+        if (vi >= vend) v0 = E::pad();
+        if (vi + kThreads >= vend) v1 = E::pad();
       }
       float x0[E::kVec], x1[E::kVec];
       E::unpack(v0, x0);
@@ -514,13 +502,13 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
       if (vi == yv) *s_xy = pick(x0, ye);
       if (vi + kThreads == yv) *s_xy = pick(x1, ye);
       acc.add2(x0, x1, c);
-    });
+    }
     SoftmaxAcc a = warp_reduce(acc.result());
     return Partial{a.m, a.s, -1, 0u};
   }
   BestAcc acc;
   acc.init();
-  if (it.kind == kArgmax) {
+  if (kind == kArgmax) {
     auto vec = [&](const float(&x)[E::kVec], int e0) {
       float mx = x[0];
       uint32_t nan = (x[0] != x[0]);
@@ -539,50 +527,55 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
         acc.idx = e0 + first;
       }
     };
-    consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
-      const int vi = it.vbeg + st * kStageVecs * kThreads + tid;
-      if (!full) {
-        if (vi >= it.vend) v0 = E::pad();
-        if (vi + kThreads >= it.vend) v1 = E::pad();
+    for (int st = 0; st < nst; ++st) {
+      uint4 v[kStageVecs];
+      ring_take(queue, s_qend, ring, lc, gs, v[0], v[1]);
+      const int vi = vbeg + st * kStageVecs * kThreads + tid;
+      if (st >= nfull) {
+        if (vi >= vend) v[0] = E::pad();
+        if (vi + kThreads >= vend) v[1] = E::pad();
       }
       float x[E::kVec];
-      E::unpack(v0, x);
+      E::unpack(v[0], x);
       vec(x, vi * E::kVec);
-      E::unpack(v1, x);
+      E::unpack(v[1], x);
       vec(x, (vi + kThreads) * E::kVec);
-    });
-  } else if (it.kind == kRace) {
+    }
+  } else if (kind == kRace) {
     GroupGains<E> gg;
-    const float c = it.c;
-    consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
-      const int vi = it.vbeg + st * kStageVecs * kThreads + tid;
-      if (!full) {
-        if (vi >= it.vend) v0 = E::pad();
-        if (vi + kThreads >= it.vend) v1 = E::pad();
+    for (int st = 0; st < nst; ++st) {
+      uint4 v[kStageVecs];
+      ring_take(queue, s_qend, ring, lc, gs, v[0], v[1]);
+      const int vi = vbeg + st * kStageVecs * kThreads + tid;
+      if (st >= nfull) {
+        if (vi >= vend) v[0] = E::pad();
+        if (vi + kThreads >= vend) v[1] = E::pad();
       }
       const int g = st * kStageVecs;
-      if ((g & 31) == 0) gg.make(it.vbeg, g, w, (uint32_t)it.pos, rk, P.key);
+      if ((g & 31) == 0) gg.make(vbeg, g, w, (uint32_t)pos, rk, P.key);
       float x[E::kVec];
-      E::unpack(v0, x);
+      E::unpack(v[0], x);
       group_bonus<E>(acc, x, vi * E::kVec, c, gg.get(g));
-      E::unpack(v1, x);
+      E::unpack(v[1], x);
       group_bonus<E>(acc, x, (vi + kThreads) * E::kVec, c, gg.get(g + 1));
-    });
+    }
   } else {
-    const ResidualRow rr{it.c, it.mp, it.inv_sp, it.mq, it.inv_sq};
+    const ResidualRow rr{c, itm.mp, itm.inv_sp, itm.mq, itm.inv_sq};
     GroupGains<E> gg;
-    consume(queue, s_qend, ring, lc, gs, it, [&](uint4 v0, uint4 v1, int st, bool full) {
-      const int vi = it.vbeg + st * kThreads + tid;
-      if (!full && vi >= it.vend) {
-        v0 = E::pad();
-        v1 = E::pad();
+    for (int st = 0; st < nst; ++st) {
+      uint4 v[kStageVecs];
+      ring_take(queue, s_qend, ring, lc, gs, v[0], v[1]);
+      const int vi = vbeg + st * kThreads + tid;
+      if (st >= nfull && vi >= vend) {
+        v[0] = E::pad();
+        v[1] = E::pad();
       }
-      if ((st & 31) == 0) gg.make(it.vbeg, st, w, (uint32_t)it.pos, rk, P.key);
+      if ((st & 31) == 0) gg.make(vbeg, st, w, (uint32_t)pos, rk, P.key);
       float x[E::kVec], z[E::kVec];
-      E::unpack(v0, x);
-      E::unpack(v1, z);
+      E::unpack(v[0], x);
+      E::unpack(v[1], z);
       group_residual<E>(acc, x, z, vi * E::kVec, rr, gg.get(st));
-    });
+    }
   }
   acc = warp_reduce(acc);
   return Partial{acc.v, 0.f, acc.idx, acc.nan};
@@ -1206,8 +1199,8 @@ __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* 
   }
   __syncwarp();
   if (lane == 0) {
-    __threadfence_block();  // queue entries before the count that publishes them
-    *reinterpret_cast<volatile int*>(s_qend) = sg.phase >= 2 ? -1 - sg.q_head : sg.q_head;
+    // queue entries before the count that publishes them
+    st_release_shared(s_qend, sg.phase >= 2 ? -1 - sg.q_head : sg.q_head);
   }
   __syncwarp();
 }
@@ -1232,6 +1225,7 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
   if (tid == 0) {
     s_layout = 0u;
     P.ctr[kCntStatus] = 0;
+    P.ctr[kCntClaim] = 0;
   }
   for (int i = tid; i < P.n_waves; i += kPlanThreads) {
     P.list_cnt[i] = 0;
@@ -1328,7 +1322,7 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
       } else {
         sampling = mode == kSampling;
         c = sampling ? kLog2e / t : 0.f;
-        n = wave_rows(P, sampling, k, 0);
+        n = P.cluster_mode ? 1 : wave_rows(P, sampling, k, 0);
       }
     }
     int tot;

@@ -23,11 +23,12 @@ def _built():
     build.build()
 
 
-def _verifier(inp, dtype, max_batch=None, max_k=None, depth=0):
+def _verifier(inp, dtype, max_batch=None, max_k=None, depth=0, schedule="auto"):
     B = len(inp["num_draft"])
     V = inp["target"].shape[1]
     v = Verifier(max(1, max_batch or B), inp["max_k"] if max_k is None else max_k, V, dtype)
     v.set_depth(depth)
+    v.set_schedule(schedule)
     return v
 
 
@@ -35,10 +36,10 @@ def _dtype_of(inp):
     return "bf16" if inp["target"].dtype == np.uint16 else "f32"
 
 
-def _check(inp, seeds=(1,), max_batch=None, max_k=None, depth=0):
+def _check(inp, seeds=(1,), max_batch=None, max_k=None, depth=0, schedule="auto"):
     dtype = _dtype_of(inp)
     reps = []
-    with _verifier(inp, dtype, max_batch, max_k, depth) as v:
+    with _verifier(inp, dtype, max_batch, max_k, depth, schedule) as v:
         for seed in seeds:
             g = parity.run_gpu(v, inp, seed)
             o = parity.run_oracle(inp, seed)
@@ -66,6 +67,8 @@ def test_large_vocab_reduced_batch_parity(name):
     inp = b.numpy_inputs()
     reps = _check(inp, seeds=(1, 7))
     print(name, reps)
+    _check(inp, seeds=(3,), schedule="clusters")
+    _check(inp, seeds=(3,), schedule="waves")
 
 
 def _slice_outputs(gpu, num_draft, idx):
@@ -164,6 +167,29 @@ def test_wave_depths(depth, dtype, vocab):
     _check(inp, seeds=(2, 5), depth=depth)
 
 
+@pytest.mark.parametrize("B", [5, 41, 300])
+@pytest.mark.parametrize("dtype,vocab", [("bf16", 4096), ("bf16", 16), ("f32", 3000),
+                                         ("bf16", 32000)])
+def test_cluster_schedule(B, dtype, vocab):
+    """The cluster launch (requests claimed by clusters, positions decided as
+    soon as their rows are read, correction drawn right after) against the
+    oracle: fewer requests than slots, a few per cluster, and many; a row
+    narrower than the cluster (16 ids: empty slices)."""
+    rng = np.random.default_rng(B + vocab)
+    k = rng.integers(0, 7, size=B)
+    temp = rng.choice([0.0, 0.6, 1.0, 1.3], size=B)
+    inp = cases.random_batch(k, temp, vocab=vocab, sigma_t=2.0, sigma_d=0.8, dtype=dtype,
+                             seed=B * 3 + vocab)
+    inp["max_k"] = 6
+    _check(inp, seeds=(2, 9), schedule="clusters")
+
+
+@pytest.mark.parametrize("name", ["w0_v1024_f32", "w1_v32000_bf16"])
+def test_small_workloads_cluster_schedule(name):
+    b = W.make_batch(name, device="cpu")
+    _check(b.numpy_inputs(), seeds=(1, 2), schedule="clusters")
+
+
 @pytest.mark.parametrize("depth", [1, 4])
 def test_small_workload_depths(depth):
     b = W.make_batch("w1_v32000_bf16", device="cpu")
@@ -224,14 +250,15 @@ def test_all_zero_drafts_and_empty_batch():
         assert res.accepted_len.numel() == 0
 
 
-@pytest.mark.parametrize("depth", [1, 2, 6])
-def test_rows_after_the_first_rejection_do_not_matter(depth):
+@pytest.mark.parametrize("depth,schedule", [(1, "waves"), (2, "waves"), (6, "waves"),
+                                            (0, "clusters")])
+def test_rows_after_the_first_rejection_do_not_matter(depth, schedule):
     """Garbage (NaN / +inf) in rows beyond the first rejection changes nothing:
     at depth 1 those rows are never read; at larger depths they may be read but
     their positions are never decided."""
     inp = cases.random_batch([5] * 48, [1.0] * 24 + [0.0] * 24, vocab=4096, sigma_d=2.5,
                              dtype="bf16", seed=13)
-    with _verifier(inp, "bf16", depth=depth) as v:
+    with _verifier(inp, "bf16", depth=depth, schedule=schedule) as v:
         base = parity.run_gpu(v, inp, 5)
         A = base["accepted_len"]
         k = inp["num_draft"]
@@ -265,10 +292,12 @@ def test_invalid_inputs_status_and_skip():
     bad["draft"][6 * 2:6 * 2 + 2] = bad["target"][6 * 3:6 * 3 + 2]
     bad["target"][6 * 3 + 2, :] = -np.inf
     _check(bad, seeds=(1,))
-    with _verifier(bad, "f32") as v:
-        g = parity.run_gpu(v, bad, 1)
-    assert g["status"] == (oracle.BAD_TOKEN | oracle.BAD_TEMP | oracle.NONFINITE)
-    assert g["accepted_len"][0] >= 0 and (g["accepted_len"][1:] == -1).all()
+    for schedule in ("waves", "clusters"):
+        _check(bad, seeds=(1,), schedule=schedule)
+        with _verifier(bad, "f32", schedule=schedule) as v:
+            g = parity.run_gpu(v, bad, 1)
+        assert g["status"] == (oracle.BAD_TOKEN | oracle.BAD_TEMP | oracle.NONFINITE)
+        assert g["accepted_len"][0] >= 0 and (g["accepted_len"][1:] == -1).all()
     # layout errors skip the whole batch
     wrong = dict(inp)
     wrong["num_draft"] = np.array([2, 2, 2, 2, 2, 2, 3], np.int32)   # k > max_k
