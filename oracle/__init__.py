@@ -89,6 +89,8 @@ def _load():
         lib.orc_race_weights.argtypes = [P, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
                                          ctypes.c_int, P, P]
         lib.orc_race_weights.restype = ctypes.c_int
+        lib.orc_metrics.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
+        lib.orc_metrics.restype = None
         _lib = lib
         return lib
 
@@ -227,3 +229,33 @@ def race_weights(weights, seed, request, position):
                                   int(request) & (2**64 - 1), int(position), _ptr(bkeys),
                                   _ptr(ekeys))
     return int(winner), bkeys, ekeys
+
+
+def metrics(accepted_len, num_draft, max_k, hist=None, proposed=None, accepted=None):
+    """Add a batch of round outputs to acceptance counts (see orc_metrics).
+
+    Returns (hist [max_k + 2], proposed [max_k], accepted [max_k]) as uint64."""
+    lib = _load()
+    a = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    k = np.ascontiguousarray(num_draft, dtype=np.int32)
+    hist = np.zeros(max_k + 2, np.uint64) if hist is None else hist
+    proposed = np.zeros(max(max_k, 1), np.uint64) if proposed is None else proposed
+    accepted = np.zeros(max(max_k, 1), np.uint64) if accepted is None else accepted
+    lib.orc_metrics(len(a), max_k, _ptr(a), _ptr(k), _ptr(hist), _ptr(proposed), _ptr(accepted))
+    return hist, proposed, accepted
+
+
+def summarize(hist, proposed, accepted):
+    """The [AMD] signals from acceptance counts: mean accepted length MAL (the
+    round's committed tokens, the target's own token included), the overall
+    acceptance rate and the per-position rates."""
+    hist = np.asarray(hist, dtype=np.float64)
+    proposed = np.asarray(proposed, dtype=np.float64)
+    accepted = np.asarray(accepted, dtype=np.float64)
+    rounds = hist[:-1].sum()
+    mal = 1.0 + (np.arange(len(hist) - 1) * hist[:-1]).sum() / rounds if rounds else float("nan")
+    with np.errstate(invalid="ignore", divide="ignore"):
+        per_pos = accepted / proposed
+    overall = accepted.sum() / proposed.sum() if proposed.sum() else float("nan")
+    return {"mal": mal, "acceptance_rate": overall, "per_position": per_pos,
+            "rounds": int(rounds), "skipped": int(hist[-1])}

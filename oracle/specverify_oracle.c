@@ -500,3 +500,37 @@ int orc_race_weights(const double *w, int vocab, uint64_t seed, uint64_t request
 {
     return race(w, vocab, seed, request, (uint32_t)position, block_keys, elem_keys, NULL);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Acceptance statistics of verify rounds.                                   */
+/*                                                                          */
+/* [AMD] "Monitor acceptance behavior" names the signals: mean accepted      */
+/* length (draft tokens committed per round), overall acceptance rate (the   */
+/* share of proposed draft tokens accepted) and per-position acceptance      */
+/* rate; its appendix tables print MAL = 1 + the sum of the per-position     */
+/* rates, i.e. MAL counts the target's own token of the round as well.       */
+/* This adds one batch of round outputs to running counts:                   */
+/*   hist[a]        rounds that accepted a draft tokens (a = 0..max_k),      */
+/*   hist[max_k+1]  requests that were skipped (accepted_len = -1),          */
+/*   proposed[j]    rounds with a draft at position j  (num_draft > j),      */
+/*   accepted[j]    rounds that accepted position j    (accepted_len > j).   */
+/* A num_draft outside [0, max_k] counts only as far as max_k.               */
+/* ------------------------------------------------------------------------ */
+void orc_metrics(int batch, int max_k, const int32_t *accepted_len, const int32_t *num_draft,
+                 uint64_t *hist, uint64_t *proposed, uint64_t *accepted)
+{
+    for (int r = 0; r < batch; ++r) {
+        const int a = accepted_len[r];
+        if (a < 0) {
+            hist[max_k + 1] += 1;
+            continue;
+        }
+        hist[a <= max_k ? a : max_k] += 1;
+        int k = num_draft[r];
+        if (k > max_k) k = max_k;
+        for (int j = 0; j < k; ++j) {
+            proposed[j] += 1;
+            if (a > j) accepted[j] += 1;
+        }
+    }
+}
