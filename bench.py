@@ -55,7 +55,7 @@ def parse_args():
                     help="requests in the oracle sample (0 = about 10 s of work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--schedule", default="auto", choices=["auto", "waves", "clusters"],
+    ap.add_argument("--schedule", default="auto", choices=["auto", "waves", "clusters", "stream"],
                     help="launch layout of a round (results do not depend on it)")
     ap.add_argument("--depth", type=int, default=0,
                     help="positions per wave launch (0 = chosen per run)")

@@ -93,6 +93,8 @@ typedef enum {
 #define SPECVERIFY_STATUS_BAD_TOTAL 16    /* sum of num_draft != total_draft: batch skipped */
 #define SPECVERIFY_STATUS_NO_DRAFT 64     /* T > 0 and k > 0 but draft_logits is NULL: request skipped */
 #define SPECVERIFY_STATUS_OVERRUN 128     /* internal: a cluster launch hit its unit cap (a bug); outputs incomplete */
+#define SPECVERIFY_STATUS_TIMEOUT 256     /* stream schedule: a bounded wait ran out (a bug, or the GPU
+                                             was held by other work for seconds); outputs incomplete */
 
 /* Flags for specverify_create_ex. */
 #define SPECVERIFY_CREATE_HOST_STAGING 1  /* allocate device staging for specverify_run_host */
@@ -239,12 +241,17 @@ int specverify_set_depth(specverify_t h, int depth);
  *   SPECVERIFY_SCHEDULE_CLUSTERS: one launch of thread-block clusters, each
  *     taking requests one at a time and deciding each position as soon as its
  *     rows are read (16-byte aligned rows only; others use waves);
+ *   SPECVERIFY_SCHEDULE_STREAM: one persistent launch whose CTAs take the
+ *     rows from a queue that the decisions feed, in bands that every CTA
+ *     splits alike; the correction draw re-reads its rows two or three bands
+ *     later, from L2 (16-byte aligned rows only; others use waves);
  *   SPECVERIFY_SCHEDULE_AUTO (default): waves (the faster layout on every
  *     batch measured so far).
  */
 #define SPECVERIFY_SCHEDULE_AUTO 0
 #define SPECVERIFY_SCHEDULE_WAVES 1
 #define SPECVERIFY_SCHEDULE_CLUSTERS 2
+#define SPECVERIFY_SCHEDULE_STREAM 3
 int specverify_set_schedule(specverify_t h, int schedule);
 
 /* Kernel launches a run of `batch` requests makes on handle h (for launch

@@ -165,9 +165,9 @@ class Verifier:
         return int(n.value)
 
     def set_schedule(self, schedule: str):
-        """'auto', 'waves' or 'clusters' (see specverify_set_schedule)."""
+        """'auto', 'waves', 'clusters' or 'stream' (see specverify_set_schedule)."""
         code = {"auto": _lib.SCHEDULE_AUTO, "waves": _lib.SCHEDULE_WAVES,
-                "clusters": _lib.SCHEDULE_CLUSTERS}[schedule]
+                "clusters": _lib.SCHEDULE_CLUSTERS, "stream": _lib.SCHEDULE_STREAM}[schedule]
         _check(self.lib.specverify_set_schedule(self._h, code), "specverify_set_schedule")
 
     def set_depth(self, depth: int):

@@ -24,6 +24,7 @@ ERR_TOO_LARGE = -6
 SCHEDULE_AUTO = 0
 SCHEDULE_WAVES = 1
 SCHEDULE_CLUSTERS = 2
+SCHEDULE_STREAM = 3
 
 STATIC_MAX_BATCH = 256
 STATIC_MAX_K = 7

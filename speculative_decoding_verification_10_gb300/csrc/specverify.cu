@@ -16,6 +16,7 @@
 
 #include "specverify.h"
 #include "sv_cluster.cuh"
+#include "sv_stream.cuh"
 
 namespace {
 
@@ -39,13 +40,40 @@ struct DeviceGuard {
 
 // ---------------------------------------------------------------------------
 // Scratch: byte offsets of every piece, sized for `mb` requests, positions
-// 0..max_k, every wave depth 1..max_k+1 and a grid of at most `grid` CTAs.
+// 0..max_k, every wave depth 1..max_k+1 and a grid of at most `grid` CTAs;
+// with `stream`, also the bands and ready tags of the stream schedule.
 // ---------------------------------------------------------------------------
 struct ScratchLayout {
-  size_t lists, lcnt, res, rcnt, pos, rescnt, part, rpart, ctr, bytes;
+  size_t lists, lcnt, res, rcnt, pos, rescnt, part, rpart, ctr;
+  size_t bands, ready_n, ready_u, spart, srpart;
+  size_t list_entries, band_cap, bytes;
 };
 
-constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid) {
+// Fewest race blocks in one CTA's share of a wave or band: rows and residual
+// row pairs (each CTA streams at least 16 KB of a split).
+int min_span_blocks(int elem_bytes) {
+  return std::max(1, sv::kMinSpanBytes / (sv::kRaceBlock * elem_bytes));
+}
+int min_span_res_blocks(int elem_bytes) {
+  return std::max(1, sv::kMinSpanBytes / (2 * sv::kRaceBlock * elem_bytes));
+}
+
+// Most segments a flat split cuts one entry of nb race blocks into: shares
+// are at least `span` blocks long, so at most (nb - 1) / span share
+// boundaries fall inside the entry.
+constexpr size_t max_segments(size_t nb, size_t span) { return (nb - 1) / span + 2; }
+
+// Segment counts of the stream schedule's per-entry partial slots.
+struct StreamSegs {
+  size_t rows, res;
+};
+
+// Bands a stream round can form: each holds at least one queue entry, and a
+// round queues at most (2 max_k + 1) rows and one residual per request.
+constexpr size_t stream_band_cap(size_t mb, int max_k) { return (2 * (size_t)max_k + 2) * mb + 2; }
+
+constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid, bool stream,
+                                       StreamSegs segs = StreamSegs{0, 0}) {
   size_t list_entries = 0, max_waves = 0, max_cap = 0;
   for (int d = 1; d <= max_k + 1; ++d) {
     const size_t w = (size_t)sv::wave_count(max_k, d), cap = 2 * (size_t)d * mb;
@@ -73,6 +101,20 @@ constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid) {
   off = align_up(off + sizeof(sv::Partial) * (grid + mb), 256);
   L.ctr = off;
   off = align_up(off + sizeof(int) * sv::kCntCount, 256);
+  L.list_entries = list_entries;
+  L.band_cap = stream ? stream_band_cap(mb, max_k) : 0;
+  L.bands = off;
+  off = align_up(off + sizeof(sv::Band) * L.band_cap, 256);
+  // a stream round queues at most 2 max_k + 1 rows per request
+  const size_t stream_entries = (2 * (size_t)max_k + 1) * mb;
+  L.ready_n = off;
+  off = align_up(off + (stream ? sizeof(uint32_t) * stream_entries : 0), 256);
+  L.ready_u = off;
+  off = align_up(off + (stream ? sizeof(uint32_t) * mb : 0), 256);
+  L.spart = off;
+  off = align_up(off + (stream ? sizeof(sv::Partial) * stream_entries * segs.rows : 0), 256);
+  L.srpart = off;
+  off = align_up(off + (stream ? sizeof(sv::Partial) * mb * segs.res : 0), 256);
   L.bytes = off;
   return L;
 }
@@ -87,6 +129,12 @@ struct Scratch {
   sv::Partial* part;
   sv::Partial* rpart;
   int* ctr;
+  sv::Band* bands;     // epoch-tagged: must start at zero (stream schedule only)
+  uint32_t* ready_n;   // epoch tags: must start at zero (stream schedule only)
+  uint32_t* ready_u;
+  sv::Partial* spart;
+  sv::Partial* srpart;
+  int band_cap;
 };
 
 Scratch scratch_at(char* b, const ScratchLayout& L) {
@@ -100,6 +148,12 @@ Scratch scratch_at(char* b, const ScratchLayout& L) {
   s.part = reinterpret_cast<sv::Partial*>(b + L.part);
   s.rpart = reinterpret_cast<sv::Partial*>(b + L.rpart);
   s.ctr = reinterpret_cast<int*>(b + L.ctr);
+  s.band_cap = (int)L.band_cap;
+  s.bands = L.band_cap ? reinterpret_cast<sv::Band*>(b + L.bands) : nullptr;
+  s.ready_n = L.band_cap ? reinterpret_cast<uint32_t*>(b + L.ready_n) : nullptr;
+  s.ready_u = L.band_cap ? reinterpret_cast<uint32_t*>(b + L.ready_u) : nullptr;
+  s.spart = L.band_cap ? reinterpret_cast<sv::Partial*>(b + L.spart) : nullptr;
+  s.srpart = L.band_cap ? reinterpret_cast<sv::Partial*>(b + L.srpart) : nullptr;
   return s;
 }
 
@@ -116,6 +170,7 @@ const void* wave_kernel(bool aligned) {
 struct KernelShape {
   int grid_aligned, grid_scalar;
   int grid_cluster, cluster_n;
+  int grid_stream;
 };
 
 constexpr int kClusterN = 8;  // CTAs per cluster (portable size)
@@ -164,6 +219,19 @@ bool kernel_shape(int device, int dtype, KernelShape* out) {
     return false;
   out->cluster_n = kClusterN;
   out->grid_cluster = clusters * kClusterN;
+  // the stream kernel: every CTA resident at once (its CTAs wait on one another)
+  const void* fs = dtype == SPECVERIFY_BF16 ? reinterpret_cast<const void*>(sv::sv_stream<sv::BF16>)
+                                            : reinterpret_cast<const void*>(sv::sv_stream<sv::F32>);
+  int occ_s = 0;
+  if (cudaFuncSetAttribute(fs, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+      cudaFuncSetAttribute(fs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_bytes()) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_s, fs, sv::kBlock, ring_bytes()) !=
+          cudaSuccess ||
+      occ_s < 1)
+    return false;
+  out->grid_stream = occ_s * sms;
   return true;
 }
 
@@ -175,6 +243,9 @@ struct RunConfig {
   KernelShape shape;
   Scratch sc;
 };
+
+// Largest handle scratch that still carries the stream schedule's arrays.
+constexpr size_t kStreamScratchCap = (size_t)512 << 20;
 
 // Batches whose whole verify window (every row of every position) is at most
 // this many bytes are verified in one wave of all positions: reading rows past
@@ -194,6 +265,13 @@ int run_depth(const RunConfig& c, int batch) {
 bool run_clusters(const RunConfig& c, int batch, bool aligned) {
   (void)batch;
   return aligned && c.schedule_setting == SPECVERIFY_SCHEDULE_CLUSTERS;
+}
+
+// The stream launch: asked for, with 16-byte aligned rows and scratch that
+// has the bands.
+bool run_stream(const RunConfig& c, int batch, bool aligned) {
+  (void)batch;
+  return aligned && c.sc.bands != nullptr && c.schedule_setting == SPECVERIFY_SCHEDULE_STREAM;
 }
 
 bool rows_aligned(const RunConfig& c, const void* target, const void* draft) {
@@ -239,13 +317,28 @@ cudaError_t launch_cluster(const RunConfig& c, cudaStream_t s, const sv::Params&
   return cudaLaunchKernelEx(&cfg, sv::sv_cluster<E>, P);
 }
 
-// One round: the plan launch, then the cluster launch or the waves (a wave
-// with nothing to do returns at once), optionally bracketed by two events.
+// The stream launch after the plan (programmatic dependent launch on it).
+template <typename E>
+cudaError_t launch_stream(const RunConfig& c, cudaStream_t s, const sv::Params& P) {
+  return launch_wave(sv::sv_stream<E>, c.shape.grid_stream, ring_bytes(), s, P);
+}
+
+// One round: the plan launch, then the stream launch, the cluster launch or
+// the waves (a wave with nothing to do returns at once), optionally bracketed
+// by two events.
 template <typename E>
 int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
                  cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (ev_start && cudaEventRecord(ev_start, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
   sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
+  if (P.stream_mode) {
+    if (launch_stream<E>(c, s, P) != cudaSuccess) {
+      cudaGetLastError();
+      return SPECVERIFY_ERR_CUDA;
+    }
+    if (ev_stop && cudaEventRecord(ev_stop, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
+  }
   if (P.cluster_mode) {
     if (launch_cluster<E>(c, s, P) != cudaSuccess) {
       cudaGetLastError();
@@ -327,8 +420,9 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
   P.nb = (c.vocab + sv::kRaceBlock - 1) / sv::kRaceBlock;
   P.nvec = (int)((size_t)c.vocab * c.elem_bytes / 16);
   const int block_bytes = sv::kRaceBlock * c.elem_bytes;
-  P.min_span = std::max(1, sv::kMinSpanBytes / block_bytes);
-  P.min_span_res = std::max(1, sv::kMinSpanBytes / (2 * block_bytes));
+  (void)block_bytes;
+  P.min_span = min_span_blocks(c.elem_bytes);
+  P.min_span_res = min_span_res_blocks(c.elem_bytes);
   P.stride = c.max_batch;
   P.accepted_len = a.accepted_len;
   P.committed = a.committed_tokens;
@@ -346,9 +440,28 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
   P.part = c.sc.part;
   P.rpart = c.sc.rpart;
   P.ctr = c.sc.ctr;
+  P.bands = c.sc.bands;
+  P.ready_n = c.sc.ready_n;
+  P.ready_u = c.sc.ready_u;
+  P.band_cap = c.sc.band_cap;
+  P.spart = c.sc.spart;
+  P.srpart = c.sc.srpart;
+  P.seg_max = (int)max_segments((size_t)P.nb, (size_t)P.min_span);
+  // a residual entry streams two rows: 2 nb units of the stream split
+  P.seg_max_res = (int)max_segments(2 * (size_t)P.nb, (size_t)P.min_span);
   // the vector path needs every row on a 16-byte boundary
   const bool aligned = rows_aligned(c, a.target_logits, P.draft);
-  if (run_clusters(c, a.batch, aligned)) {
+  if (run_stream(c, a.batch, aligned)) {
+    P.stream_mode = 1;
+    P.depth = 1;
+    P.n_waves = 1;
+    P.list_cap = 0;
+    const size_t row_bytes = (size_t)c.vocab * c.elem_bytes;
+    // a full band: about kBandSpanBytes per CTA, at most kBandMaxRows entries
+    P.band_rows = (int)std::max<size_t>(
+        1, std::min<size_t>((size_t)c.shape.grid_stream * sv::kBandSpanBytes / row_bytes,
+                            (size_t)sv::kBandMaxRows));
+  } else if (run_clusters(c, a.batch, aligned)) {
     P.cluster_mode = 1;
     P.unit_cap = 2 * a.batch * (c.max_k + 2) + 16;
     P.depth = 1;
@@ -366,7 +479,7 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
 constexpr int kStaticMaxDevices = 64;
 constexpr size_t kStaticGrid = 1024;  // CTAs a wave of the static path may use
 constexpr ScratchLayout kStaticLayout =
-    scratch_layout(SPECVERIFY_STATIC_MAX_BATCH, SPECVERIFY_STATIC_MAX_K, kStaticGrid);
+    scratch_layout(SPECVERIFY_STATIC_MAX_BATCH, SPECVERIFY_STATIC_MAX_K, kStaticGrid, false);
 
 struct StaticDevice {
   bool ready;
@@ -477,8 +590,15 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
     delete h;
     return SPECVERIFY_ERR_CUDA;
   }
-  const ScratchLayout L = scratch_layout(
-      (size_t)max_batch, max_k, (size_t)std::max(c.shape.grid_aligned, c.shape.grid_scalar));
+  // the stream schedule's scratch grows with the number of segments a row can
+  // be cut into; above kStreamScratchCap it is left out (waves only)
+  const size_t nb = ((size_t)vocab + sv::kRaceBlock - 1) / sv::kRaceBlock;
+  const StreamSegs segs{max_segments(nb, (size_t)min_span_blocks(c.elem_bytes)),
+                        max_segments(2 * nb, (size_t)min_span_blocks(c.elem_bytes))};
+  const size_t grid_all =
+      (size_t)std::max({c.shape.grid_aligned, c.shape.grid_scalar, c.shape.grid_stream});
+  ScratchLayout L = scratch_layout((size_t)max_batch, max_k, grid_all, true, segs);
+  if (L.bytes > kStreamScratchCap) L = scratch_layout((size_t)max_batch, max_k, grid_all, false);
   if (cudaMalloc(&h->scratch, L.bytes) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -632,7 +752,7 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
   c.dtype = dtype;
   c.elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
   c.depth_setting = 0;
-  c.schedule_setting = SPECVERIFY_SCHEDULE_AUTO;
+  c.schedule_setting = SPECVERIFY_SCHEDULE_WAVES;  // the arena has no bands
   const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
                   batch, total_draft, accepted_len, committed_tokens, accept_flags,
                   nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -723,7 +843,7 @@ int specverify_set_schedule(specverify_t h, int schedule) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
   if (schedule != SPECVERIFY_SCHEDULE_AUTO && schedule != SPECVERIFY_SCHEDULE_WAVES &&
-      schedule != SPECVERIFY_SCHEDULE_CLUSTERS)
+      schedule != SPECVERIFY_SCHEDULE_CLUSTERS && schedule != SPECVERIFY_SCHEDULE_STREAM)
     return SPECVERIFY_ERR_INVALID_ARG;
   h->cfg.schedule_setting = schedule;
   return SPECVERIFY_OK;
@@ -735,9 +855,10 @@ int specverify_launches_per_run(specverify_t h, int batch, int* launches_out) {
   if (launches_out == nullptr || batch < 0 || batch > h->cfg.max_batch)
     return SPECVERIFY_ERR_INVALID_ARG;
   // rows are taken as 16-byte aligned (the caller's tensors decide in the end)
+  const bool aligned = rows_aligned(h->cfg, nullptr, nullptr);
   if (batch == 0)
     *launches_out = 0;
-  else if (run_clusters(h->cfg, batch, rows_aligned(h->cfg, nullptr, nullptr)))
+  else if (run_stream(h->cfg, batch, aligned) || run_clusters(h->cfg, batch, aligned))
     *launches_out = 2;
   else
     *launches_out = 1 + sv::wave_count(h->cfg.max_k, run_depth(h->cfg, batch));

@@ -40,6 +40,8 @@
 // scalar path with the same structure.
 #pragma once
 
+#include <cstddef>
+
 #include "sv_device.cuh"
 
 namespace sv {
@@ -62,7 +64,7 @@ enum UnitType : int { kUnitEnd = 0, kUnitItem = 1 };
 
 // Status bits (equal to the SPECVERIFY_STATUS_* values of the header).
 constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite = 8u,
-                   kStBadTotal = 16u, kStNoDraft = 64u, kStOverrun = 128u;
+                   kStBadTotal = 16u, kStNoDraft = 64u, kStOverrun = 128u, kStTimeout = 256u;
 
 // Number of waves of a round with positions 0..max_k taken D at a time: one
 // per group of D positions, plus one for the residual draws of the last group
@@ -104,7 +106,34 @@ struct __align__(16) ResEntry {
   uint32_t req_lo, req_hi, pad2;
 };
 
-enum Counter : int { kCntStatus = 0, kCntClaim = 1, kCntCount = 4 };
+// Global counters.  The stream schedule uses the reservation counts of its two
+// queues, the number of finished requests and the number it must finish.
+enum Counter : int {
+  kCntStatus = 0,
+  kCntClaim = 1,
+  kCntNRes = 2,   // row entries reserved in the normal queue
+  kCntURes = 3,   // residual entries reserved in the urgent queue
+  kCntDone = 4,   // requests whose outputs are final
+  kCntLive = 5,   // requests the plan left to verify
+  kCntCount = 8
+};
+
+// A band of the stream schedule: the urgent entries [u0, u1) and the row
+// entries [n0, n1) that every CTA splits the same way, where u0 and n0 are
+// where the band before it ended.  One 64-bit word, written once per round:
+// epoch << 32 | payload, payload = u1 << 18 | n1 for a formed band, or one of
+// the markers below; a word of an earlier round reads as open.
+struct Band {
+  unsigned long long word;
+};
+constexpr uint32_t kBandFormingMark = 0xffffffffu;  // being formed by one CTA
+constexpr uint32_t kBandEndMark = 0xfffffffeu;      // the round is over
+constexpr int kBandRowBits = 18;                    // n1 < 2^18, u1 < 2^13
+__host__ __device__ constexpr uint32_t band_payload(int u1, int n1) {
+  return ((uint32_t)u1 << kBandRowBits) | (uint32_t)n1;
+}
+__host__ __device__ constexpr int band_u1(uint32_t p) { return (int)((p >> kBandRowBits) & 0x1fffu); }
+__host__ __device__ constexpr int band_n1(uint32_t p) { return (int)(p & ((1u << kBandRowBits) - 1u)); }
 
 struct Params {
   const void* target;
@@ -128,6 +157,9 @@ struct Params {
   int list_cap;      // entries per wave list: 2 * D * stride
   int cluster_mode;  // the plan lists one entry per request (the cluster launch)
   int unit_cap;      // cluster launch: more units than any round needs
+  int stream_mode;   // the plan publishes its rows to the stream schedule's queue
+  int band_rows;     // stream schedule: rows a full band takes
+  int band_cap;      // stream schedule: bands a round may form
   int32_t* accepted_len;
   int32_t* committed;
   uint8_t* flags;
@@ -144,6 +176,12 @@ struct Params {
   Partial* part;                // [grid + list_cap] row segment partials
   Partial* rpart;               // [grid + stride] residual segment partials
   int* ctr;                     // [kCntCount]
+  Band* bands;                  // [band_cap] stream schedule
+  Partial* spart;               // stream: [list entries * seg_max] row segment partials
+  Partial* srpart;              // stream: [stride * seg_max_res] residual segment partials
+  int seg_max, seg_max_res;     // stream: most segments one row entry is cut into
+  uint32_t* ready_n;            // [list entries] epoch once a row entry is written
+  uint32_t* ready_u;            // [stride] epoch once a residual entry is written
 };
 
 __device__ __forceinline__ Partial ld_cg(const Partial* p) {
@@ -221,6 +259,12 @@ struct __align__(16) QItem {
   float c;           // log2(e) / T
   float mp, inv_sp, mq, inv_sq;  // residual segments: normalisers of p_j and q_j
   uint32_t req_lo, req_hi;
+  // stream schedule: the split of the segment's band phase and that phase's
+  // first queue index (entry e of the phase is queue entry e0 + e)
+  unsigned long long sT;
+  int sG, e0;
+  int band;
+  int snu;  // stream schedule: urgent entries of the segment's band
 };
 
 // The logit x[y] held by vector x at element e (a select chain, no local memory).
@@ -471,10 +515,10 @@ __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend,
 // Segment reductions (compute threads).  Each returns this warp's partial; a
 // softmax segment that holds the draft token y also leaves x[y] in *s_xy.
 // ---------------------------------------------------------------------------
-template <typename E>
-__device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
-                                               const int* s_qend, uint4* ring, LoadCursor& lc,
-                                               int& gs, const QItem& itm, float* s_xy) {
+// `take(v0, v1)` hands over the next stage of the segment from the copy ring.
+template <typename E, typename Take>
+__device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm, float* s_xy,
+                                              Take& take) {
   const int w = threadIdx.x >> 5;
   const int tid = threadIdx.x;
   // the segment's fields in registers (the queue is shared memory, which the
@@ -490,7 +534,7 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
     const int yv = itm.yv, ye = itm.y & (E::kVec - 1);
     for (int st = 0; st < nst; ++st) {
       uint4 v0, v1;
-      ring_take(queue, s_qend, ring, lc, gs, v0, v1);
+      take(v0, v1);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
       if (st >= nfull) {
         if (vi >= vend) v0 = E::pad();
@@ -529,7 +573,7 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
     };
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      ring_take(queue, s_qend, ring, lc, gs, v[0], v[1]);
+      take(v[0], v[1]);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
       if (st >= nfull) {
         if (vi >= vend) v[0] = E::pad();
@@ -545,7 +589,7 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
     GroupGains<E> gg;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      ring_take(queue, s_qend, ring, lc, gs, v[0], v[1]);
+      take(v[0], v[1]);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
       if (st >= nfull) {
         if (vi >= vend) v[0] = E::pad();
@@ -564,7 +608,7 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
     GroupGains<E> gg;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      ring_take(queue, s_qend, ring, lc, gs, v[0], v[1]);
+      take(v[0], v[1]);
       const int vi = vbeg + st * kThreads + tid;
       if (st >= nfull && vi >= vend) {
         v[0] = E::pad();
@@ -579,6 +623,14 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
   }
   acc = warp_reduce(acc);
   return Partial{acc.v, 0.f, acc.idx, acc.nan};
+}
+
+template <typename E>
+__device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
+                                               const int* s_qend, uint4* ring, LoadCursor& lc,
+                                               int& gs, const QItem& itm, float* s_xy) {
+  auto take = [&](uint4& v0, uint4& v1) { ring_take(queue, s_qend, ring, lc, gs, v0, v1); };
+  return seg_reduce<E>(P, itm, s_xy, take);
 }
 
 // Scalar path (rows not 16-byte aligned): warp w takes race blocks
@@ -839,13 +891,11 @@ __device__ __forceinline__ RowRes single_res(const Partial& p, int kind) {
 // The rows of one position from their segments' partials: the target row at
 // list entry et (kind tkind) and, when paired, the draft row at et + 1 -- all
 // partials loaded lane-parallel in one pass.
-__device__ void merge_position(const Params& P, const Partial* parts, const Split& sp, int et,
-                               bool paired, int tkind, RowRes& t, RowRes& d) {
+// The nt partials of the target row are pt[0..nt), the nd of the draft row
+// pd[0..nd).
+__device__ void merge_rows(const Partial* pt, int nt, const Partial* pd, int nd, bool paired,
+                           int tkind, RowRes& t, RowRes& d) {
   const int lane = threadIdx.x & 31;
-  const int nt = sp.segments(et, P.nb);
-  const int nd = paired ? sp.segments(et + 1, P.nb) : 0;
-  const int ct = sp.first_cta(et, P.nb);
-  const int cd = paired ? sp.first_cta(et + 1, P.nb) : 0;
   SoftmaxAcc st, sd;
   st.init();
   sd.init();
@@ -855,7 +905,7 @@ __device__ void merge_position(const Params& P, const Partial* parts, const Spli
   bool ht = false, hd = false;
   for (int q = lane; q < nt + nd; q += 32) {
     const bool is_t = q < nt;
-    const Partial pp = ld_cg(parts + (is_t ? ct + q + et : cd + (q - nt) + et + 1));
+    const Partial pp = ld_cg(is_t ? pt + q : pd + (q - nt));
     if (is_t && tkind != kSoftmax) {
       BestAcc x;
       x.v = pp.a;
@@ -896,6 +946,17 @@ __device__ void merge_position(const Params& P, const Partial* parts, const Spli
     const float xy = __shfl_sync(0xffffffffu, xyd, hm ? __ffs(hm) - 1 : 0);
     d = softmax_res(sd, hm ? xy : nan);
   }
+}
+
+// The same for the segments of a wave's flat split: segment s of entry e
+// (s counted from the entry's first CTA c) left its partial at parts[c + s + e].
+__device__ void merge_position(const Params& P, const Partial* parts, const Split& sp, int et,
+                               bool paired, int tkind, RowRes& t, RowRes& d) {
+  const int nt = sp.segments(et, P.nb);
+  const int nd = paired ? sp.segments(et + 1, P.nb) : 0;
+  const int ct = sp.first_cta(et, P.nb);
+  const int cd = paired ? sp.first_cta(et + 1, P.nb) : 0;
+  merge_rows(parts + ct + et, nt, parts + cd + et + 1, nd, paired, tkind, t, d);
 }
 
 // ---------------------------------------------------------------------------
@@ -1095,15 +1156,55 @@ struct SegGen {
   int q_head, q_used;
 };
 
+// Queue entries are read from L2 (another CTA may have written them during
+// this launch).
+__device__ __forceinline__ Entry ldcg_entry(const Entry* p) {
+  const int4 a = __ldcg(reinterpret_cast<const int4*>(p));
+  const int4 b = __ldcg(reinterpret_cast<const int4*>(p) + 1);
+  Entry e;
+  e.meta = a.x;
+  e.d0 = a.y;
+  e.c = __int_as_float(a.z);
+  e.y = a.w;
+  e.req_lo = (uint32_t)b.x;
+  e.req_hi = (uint32_t)b.y;
+  e.base = b.z;
+  e.pad = b.w;
+  return e;
+}
+__device__ __forceinline__ ResEntry ldcg_res(const ResEntry* p) {
+  const int4 a = __ldcg(reinterpret_cast<const int4*>(p));
+  const int4 b = __ldcg(reinterpret_cast<const int4*>(p) + 1);
+  const int4 c = __ldcg(reinterpret_cast<const int4*>(p) + 2);
+  ResEntry r;
+  r.r = a.x;
+  r.j = a.y;
+  r.d0 = a.z;
+  r.pad = a.w;
+  r.c = __int_as_float(b.x);
+  r.mp = __int_as_float(b.y);
+  r.inv_sp = __int_as_float(b.z);
+  r.mq = __int_as_float(b.w);
+  r.inv_sq = __int_as_float(c.x);
+  r.req_lo = (uint32_t)c.y;
+  r.req_hi = (uint32_t)c.z;
+  r.pad2 = (uint32_t)c.w;
+  return r;
+}
+
+// Entry e of a phase is res[e] (phase 0) or list[e] (phase 1); its segment
+// partials go to slot CTA + e0 + e.
 template <typename E, bool kAligned>
-__device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1, QItem& it) {
+__device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1, QItem& it,
+                               const ResEntry* res, const Entry* list, int e0) {
   const size_t row_bytes = (size_t)P.vocab * E::kBytes;
   it.e = e;
-  it.g = (int)blockIdx.x + e;
+  it.g = (int)blockIdx.x + e0 + e;
+  it.e0 = e0;
   it.mp = it.inv_sp = it.mq = it.inv_sq = 0.f;
   it.row2 = nullptr;
   if (phase == 0) {
-    const ResEntry re = P.res[(size_t)(P.wave - 1) * P.stride + e];
+    const ResEntry re = ldcg_res(res + e);
     it.r = re.r;
     it.kind = kResidual;
     it.d0 = re.d0;
@@ -1123,7 +1224,7 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
     it.row = reinterpret_cast<const char*>(P.target) + (size_t)(re.d0 + re.r + re.j) * row_bytes;
     it.row2 = reinterpret_cast<const char*>(P.draft) + (size_t)(re.d0 + re.j) * row_bytes;
   } else {
-    const Entry en = P.lists[(size_t)P.wave * P.list_cap + e];
+    const Entry en = ldcg_entry(list + e);
     const int r = en.meta & 0x1fff;
     it.r = r;
     it.is_draft = (en.meta >> 13) & 1;
@@ -1193,7 +1294,10 @@ __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* 
       ++n;
     }
     QItem it;
-    if (lane < n) decode_segment<E, kAligned>(P, my_phase, my_e, my_b0, my_b1, it);
+    if (lane < n)
+      decode_segment<E, kAligned>(P, my_phase, my_e, my_b0, my_b1, it,
+                                  P.res + (P.wave > 0 ? (size_t)(P.wave - 1) * P.stride : 0),
+                                  P.lists + (size_t)P.wave * P.list_cap, 0);
     if (lane < n) queue[(sg.q_head + lane) & (kQueue - 1)] = it;
     sg.q_head += n;
   }
@@ -1226,6 +1330,10 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
     s_layout = 0u;
     P.ctr[kCntStatus] = 0;
     P.ctr[kCntClaim] = 0;
+    P.ctr[kCntNRes] = 0;
+    P.ctr[kCntURes] = 0;
+    P.ctr[kCntDone] = 0;
+    P.ctr[kCntLive] = 0;
   }
   for (int i = tid; i < P.n_waves; i += kPlanThreads) {
     P.list_cnt[i] = 0;
@@ -1300,7 +1408,7 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
   }
 
   // per request: the input checks, then its rows of wave 0
-  int written = 0;
+  int written = 0, live = 0;
   for (int base = 0; base < P.batch; base += kPlanThreads) {
     const int r = base + tid;
     int n = 0, d0 = 0, k = 0;
@@ -1329,11 +1437,25 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
     const int at = written + scan(n, &tot);
     if (n > 0) {
       const RequestKey rk = request_key(P, r);
-      for (int j = 0; j < n; ++j) P.lists[at + j] = wave_entry(P, sampling, r, d0, k, c, rk, 0, j, at);
+      for (int j = 0; j < n; ++j) {
+        P.lists[at + j] = wave_entry(P, sampling, r, d0, k, c, rk, 0, j, at);
+        if (P.stream_mode) P.ready_n[at + j] = P.epoch;
+      }
     }
     written += tot;
+    live += __syncthreads_count(n > 0);
   }
-  if (tid == 0) P.list_cnt[0] = written;
+  if (P.stream_mode) {
+    // the stream schedule counts segments with plain atomics from zero
+    for (int i = tid; i < (P.max_k + 1) * P.batch; i += kPlanThreads)
+      P.pos_cnt[(size_t)(i / P.batch) * P.stride + i % P.batch] = 0ull;
+    for (int r = tid; r < P.batch; r += kPlanThreads) P.rcnt[r] = 0ull;
+  }
+  if (tid == 0) {
+    P.list_cnt[0] = written;
+    P.ctr[kCntNRes] = written;
+    P.ctr[kCntLive] = live;
+  }
 }
 
 // ---------------------------------------------------------------------------

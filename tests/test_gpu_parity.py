@@ -69,6 +69,7 @@ def test_large_vocab_reduced_batch_parity(name):
     print(name, reps)
     _check(inp, seeds=(3,), schedule="clusters")
     _check(inp, seeds=(3,), schedule="waves")
+    _check(inp, seeds=(3, 8), schedule="stream")
 
 
 def _slice_outputs(gpu, num_draft, idx):
@@ -82,14 +83,16 @@ def _slice_outputs(gpu, num_draft, idx):
     return out
 
 
+@pytest.mark.parametrize("schedule", ["auto", "stream"])
 @pytest.mark.parametrize("name", ["w2_v128256_bf16", "w3_v151936_bf16", "w4_v262144_bf16"])
-def test_full_size_workload_sampled_parity(name):
+def test_full_size_workload_sampled_parity(name, schedule):
     """Full batch in the benchmark's launch configuration; the oracle re-verifies
     a sample of requests one by one (keyed by their batch index)."""
     b = W.make_batch(name, device="cuda")
     seed = 1
     nd = b.num_draft.cpu().numpy()
     with Verifier(b.batch, b.max_k, b.vocab, b.dtype) as v:
+        v.set_schedule(schedule)
         res = v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, seed, debug=True)
         torch.cuda.synchronize()
         gpu = {"accepted_len": res.accepted_len.cpu().numpy(),
@@ -184,6 +187,29 @@ def test_cluster_schedule(B, dtype, vocab):
     _check(inp, seeds=(2, 9), schedule="clusters")
 
 
+@pytest.mark.parametrize("B", [1, 5, 41, 300, 1500])
+@pytest.mark.parametrize("dtype,vocab", [("bf16", 4096), ("bf16", 16), ("f32", 3000),
+                                         ("bf16", 32000), ("f32", 1024)])
+def test_stream_schedule(B, dtype, vocab):
+    """The stream launch (rows queued by the decisions, consumed in bands that
+    every CTA splits alike, corrections through the urgent queue) against the
+    oracle: one request, a few, many, more bands than requests; rows narrower
+    than a CTA's share; ragged k with k = 0, greedy and sampling mixed."""
+    rng = np.random.default_rng(B * 11 + vocab)
+    k = rng.integers(0, 7, size=B)
+    temp = rng.choice([0.0, 0.6, 1.0, 1.3], size=B)
+    inp = cases.random_batch(k, temp, vocab=vocab, sigma_t=2.0, sigma_d=0.8, dtype=dtype,
+                             seed=B * 5 + vocab)
+    inp["max_k"] = 6
+    _check(inp, seeds=(2, 9), schedule="stream")
+
+
+@pytest.mark.parametrize("name", ["w0_v1024_f32", "w1_v32000_bf16"])
+def test_small_workloads_stream_schedule(name):
+    b = W.make_batch(name, device="cpu")
+    _check(b.numpy_inputs(), seeds=(1, 2, 3), schedule="stream")
+
+
 @pytest.mark.parametrize("name", ["w0_v1024_f32", "w1_v32000_bf16"])
 def test_small_workloads_cluster_schedule(name):
     b = W.make_batch(name, device="cpu")
@@ -196,22 +222,24 @@ def test_small_workload_depths(depth):
     _check(b.numpy_inputs(), seeds=(1, 2), depth=depth)
 
 
+@pytest.mark.parametrize("schedule", ["auto", "stream"])
 @pytest.mark.parametrize("max_k", [15, 31])
-def test_long_windows(max_k):
+def test_long_windows(max_k, schedule):
     B = 9
     k = np.array([max_k] * 4 + [0, 1, max_k // 2, max_k, 3])
     temp = np.array([1.0, 0.8, 0.0, 1.0, 1.0, 0.0, 0.9, 1.0, 0.7])
     inp = cases.random_batch(k, temp, vocab=2048, sigma_t=2.0, sigma_d=0.3, dtype="bf16", seed=5)
     inp["max_k"] = max_k
-    _check(inp, seeds=(1, 2))
+    _check(inp, seeds=(1, 2), schedule=schedule)
 
 
-def test_identical_and_disjoint_rows():
+@pytest.mark.parametrize("schedule", ["auto", "stream"])
+def test_identical_and_disjoint_rows(schedule):
     inp = cases.random_batch([4] * 16, [0.9] * 16, vocab=3000, dtype="bf16", seed=8)
     t_off = np.concatenate([[0], np.cumsum(inp["num_draft"] + 1)])
     src = np.concatenate([np.arange(t_off[r], t_off[r] + 4) for r in range(16)])
     inp["draft"] = inp["target"][src].copy()
-    with _verifier(inp, "bf16") as v:
+    with _verifier(inp, "bf16", schedule=schedule) as v:
         g = parity.run_gpu(v, inp, 4)
     assert (g["accepted_len"] == 4).all()
     V, B = 64, 100
@@ -221,19 +249,20 @@ def test_identical_and_disjoint_rows():
     drf[:, 32:] = 0.0
     inp = dict(target=tgt, draft=drf, tokens=(32 + np.arange(B) % 32).astype(np.int32),
                num_draft=np.ones(B, np.int32), temperature=np.ones(B, np.float32), max_k=1)
-    reps = _check(inp, seeds=(1,))
-    with _verifier(inp, "f32") as v:
+    reps = _check(inp, seeds=(1,), schedule=schedule)
+    with _verifier(inp, "f32", schedule=schedule) as v:
         g = parity.run_gpu(v, inp, 1)
     assert (g["accepted_len"] == 0).all() and (g["committed"][:, 0] < 32).all()
 
 
-def test_greedy_only_without_draft_logits():
+@pytest.mark.parametrize("schedule", ["auto", "stream"])
+def test_greedy_only_without_draft_logits(schedule):
     inp = cases.random_batch([3, 0, 5, 2], [0.0] * 4, vocab=5000, dtype="bf16", seed=2)
     inp["max_k"] = 5
     o = parity.run_oracle(inp, 1)
     inp2 = dict(inp)
     inp2["draft"] = None
-    with _verifier(inp2, "bf16") as v:
+    with _verifier(inp2, "bf16", schedule=schedule) as v:
         g = parity.run_gpu(v, inp2, 1)
     assert g["status"] == 0
     assert (g["committed"] == o["committed"]).all() and (g["accepted_len"] == o["accepted_len"]).all()
@@ -243,6 +272,9 @@ def test_all_zero_drafts_and_empty_batch():
     inp = cases.random_batch([0] * 10, [1.0] * 5 + [0.0] * 5, vocab=777, dtype="bf16", seed=3)
     inp["max_k"] = 2
     _check(inp, seeds=(1, 2))
+    inp = cases.random_batch([0] * 10, [1.0] * 5 + [0.0] * 5, vocab=776, dtype="bf16", seed=3)
+    inp["max_k"] = 2
+    _check(inp, seeds=(1, 2), schedule="stream")
     with Verifier(4, 2, 777, "bf16") as v:
         e = torch.empty(0, dtype=torch.int32, device="cuda")
         res = v.run(torch.empty(0, 777, dtype=torch.bfloat16, device="cuda"), None, e, e,
@@ -251,7 +283,7 @@ def test_all_zero_drafts_and_empty_batch():
 
 
 @pytest.mark.parametrize("depth,schedule", [(1, "waves"), (2, "waves"), (6, "waves"),
-                                            (0, "clusters")])
+                                            (0, "clusters"), (0, "stream")])
 def test_rows_after_the_first_rejection_do_not_matter(depth, schedule):
     """Garbage (NaN / +inf) in rows beyond the first rejection changes nothing:
     at depth 1 those rows are never read; at larger depths they may be read but
@@ -292,7 +324,7 @@ def test_invalid_inputs_status_and_skip():
     bad["draft"][6 * 2:6 * 2 + 2] = bad["target"][6 * 3:6 * 3 + 2]
     bad["target"][6 * 3 + 2, :] = -np.inf
     _check(bad, seeds=(1,))
-    for schedule in ("waves", "clusters"):
+    for schedule in ("waves", "clusters", "stream"):
         _check(bad, seeds=(1,), schedule=schedule)
         with _verifier(bad, "f32", schedule=schedule) as v:
             g = parity.run_gpu(v, bad, 1)
@@ -301,7 +333,18 @@ def test_invalid_inputs_status_and_skip():
     # layout errors skip the whole batch
     wrong = dict(inp)
     wrong["num_draft"] = np.array([2, 2, 2, 2, 2, 2, 3], np.int32)   # k > max_k
+    for schedule in ("auto", "stream"):
+        _layout_errors(inp, wrong, schedule)
+    nod = dict(inp)
+    nod["draft"] = None
     with _verifier(inp, "f32") as v:
+        g = parity.run_gpu(v, nod, 1)
+    assert g["status"] == oracle.NO_DRAFT
+    assert (g["accepted_len"][[0, 1, 3, 4, 5, 6]] == -1).all() and g["accepted_len"][2] >= 0
+
+
+def _layout_errors(inp, wrong, schedule):
+    with _verifier(inp, "f32", schedule=schedule) as v:
         t = parity.to_torch(wrong, "cuda")
         res = v.run(t["target"], t["draft"], t["tokens"], t["num_draft"], t["temperature"], 1,
                     total_draft=14)
@@ -314,12 +357,6 @@ def test_invalid_inputs_status_and_skip():
         # a valid run right after clears the status
         v.run(t["target"], t["draft"], t["tokens"], t["num_draft"], t["temperature"], 1)
         assert v.status() == 0
-    nod = dict(inp)
-    nod["draft"] = None
-    with _verifier(inp, "f32") as v:
-        g = parity.run_gpu(v, nod, 1)
-    assert g["status"] == oracle.NO_DRAFT
-    assert (g["accepted_len"][[0, 1, 3, 4, 5, 6]] == -1).all() and g["accepted_len"][2] >= 0
 
 
 # --- properties of the randomness ------------------------------------------------------
