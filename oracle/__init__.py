@@ -91,6 +91,8 @@ def _load():
         lib.orc_race_weights.restype = ctypes.c_int
         lib.orc_metrics.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
         lib.orc_metrics.restype = None
+        lib.orc_tree_greedy.argtypes = [ctypes.c_int] * 5 + [P] * 8
+        lib.orc_tree_greedy.restype = ctypes.c_uint32
         _lib = lib
         return lib
 
@@ -259,3 +261,30 @@ def summarize(hist, proposed, accepted):
     overall = accepted.sum() / proposed.sum() if proposed.sum() else float("nan")
     return {"mal": mal, "acceptance_rate": overall, "per_position": per_pos,
             "rounds": int(rounds), "skipped": int(hist[-1])}
+
+
+BAD_PARENT = 32
+
+
+def tree_greedy(target, num_nodes, parent, tokens, max_nodes, total_nodes=None):
+    """Greedy tree verification (see orc_tree_greedy): returns a dict with
+    accepted_len [B], path [B, max_nodes], committed [B, max_nodes + 1],
+    req_status [B] and the status bits."""
+    lib = _load()
+    t, dt = _logits(target)
+    n = np.ascontiguousarray(num_nodes, dtype=np.int32)
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    B = len(n)
+    total = int(n.astype(np.int64).sum()) if total_nodes is None else int(total_nodes)
+    acc = np.empty(B, np.int32)
+    path = np.empty((B, max(max_nodes, 0)), np.int32)
+    com = np.empty((B, max_nodes + 1), np.int32)
+    rs = np.empty(B, np.int32)
+    st = lib.orc_tree_greedy(dt, t.shape[1], B, int(max_nodes), total, _ptr(t), _ptr(n),
+                             _ptr(par if par.size else np.zeros(1, np.int32)),
+                             _ptr(tok if tok.size else np.zeros(1, np.int32)),
+                             _ptr(acc), _ptr(path if path.size else np.zeros(1, np.int32)),
+                             _ptr(com), _ptr(rs))
+    return {"accepted_len": acc, "path": path, "committed": com, "req_status": rs,
+            "status": int(st)}

@@ -534,3 +534,102 @@ void orc_metrics(int batch, int max_k, const int32_t *accepted_len, const int32_
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Greedy tree verification.                                                */
+/*                                                                          */
+/* [SD] section 5, "DDTree: Build a Tree from Parallel Marginals": the      */
+/* drafted tree uses depth-based positions and ancestor-only attention;     */
+/* verification walks the target's selected tokens, and when no child       */
+/* matches, that target token becomes the next bonus token; only the        */
+/* accepted path survives.  [SD] section 1 gives no sampling rule for trees */
+/* (the single-chain formula is not a tree algorithm), so only greedy       */
+/* selection (the target argmax, lowest index on ties) is defined here.     */
+/*                                                                          */
+/* Request r has n_r draft nodes, 0 <= n_r <= max_nodes; node i has token   */
+/* tokens[i] and parent[i] in [-1, i) (-1: a child of the root, the last    */
+/* committed token).  Its n_r + 1 target rows are consecutive, starting at  */
+/* row sum_{s<r} (n_s + 1): row 0 is the target's output at the root, row   */
+/* 1 + i its output after node i.  Node arrays start at sum_{s<r} n_s.      */
+/*                                                                          */
+/* The walk: at the current node (the root first) tau = argmax of its row;  */
+/* the lowest-index child of the current node whose token is tau is         */
+/* accepted and becomes current; when none is, tau is the bonus token and   */
+/* the walk ends.  Outputs: accepted_len[r] = A (accepted nodes),           */
+/* path[r * max_nodes + d] the accepted node at depth d (d < A, else -1),   */
+/* committed[r * (max_nodes + 1) + d] the accepted tokens then the bonus    */
+/* (d <= A, else -1).  A request whose parents or tokens are out of range,  */
+/* or whose walk reads a row with NaN, +inf or no finite logit, is skipped  */
+/* (accepted_len -1, outputs -1) with its status bit; a num_nodes outside   */
+/* [0, max_nodes], or a total other than total_nodes, skips the batch.      */
+/* ------------------------------------------------------------------------ */
+#define ORC_BAD_PARENT 32u
+
+uint32_t orc_tree_greedy(int dtype, int vocab, int batch, int max_nodes, int total_nodes,
+                         const void *target, const int32_t *num_nodes, const int32_t *parent,
+                         const int32_t *tokens, int32_t *accepted_len, int32_t *path,
+                         int32_t *committed, int32_t *req_status)
+{
+    uint32_t status = 0;
+    const int pw = max_nodes, cw = max_nodes + 1;
+    for (int r = 0; r < batch; ++r) {
+        accepted_len[r] = -1;
+        for (int d = 0; d < pw; ++d) path[(size_t)r * pw + d] = -1;
+        for (int d = 0; d < cw; ++d) committed[(size_t)r * cw + d] = -1;
+        if (req_status) req_status[r] = 0;
+    }
+    long long total = 0;
+    for (int r = 0; r < batch; ++r) {
+        if (num_nodes[r] < 0 || num_nodes[r] > max_nodes) status |= ORC_BAD_K;
+        total += num_nodes[r];
+    }
+    if (!status && total != total_nodes) status |= ORC_BAD_TOTAL;
+    if (status) {
+        for (int r = 0; r < batch; ++r)
+            if (req_status) req_status[r] = (int32_t)status;
+        return status;
+    }
+    size_t t_off = 0, n_off = 0;
+    for (int r = 0; r < batch; ++r) {
+        const int n = num_nodes[r];
+        const int32_t *par = parent + n_off, *tok = tokens + n_off;
+        uint32_t rs = 0;
+        for (int i = 0; i < n; ++i) {
+            if (par[i] < -1 || par[i] >= i) rs |= ORC_BAD_PARENT;
+            if (tok[i] < 0 || tok[i] >= vocab) rs |= ORC_BAD_TOKEN;
+        }
+        int cur = -1, a = 0;
+        int32_t *pth = path + (size_t)r * pw, *com = committed + (size_t)r * cw;
+        while (!rs) {
+            const size_t row = t_off + (size_t)(cur + 1);
+            if (!row_is_valid(target, dtype, row, vocab)) {
+                rs |= ORC_NONFINITE;
+                break;
+            }
+            const int tau = orc_argmax(target, dtype, row, vocab);
+            int child = -1;
+            for (int i = 0; i < n; ++i)
+                if (par[i] == cur && tok[i] == tau) {
+                    child = i;
+                    break;
+                }
+            com[a] = tau;
+            if (child < 0)
+                break;
+            pth[a] = child;
+            ++a;
+            cur = child;
+        }
+        if (rs) {
+            for (int d = 0; d < pw; ++d) pth[d] = -1;
+            for (int d = 0; d < cw; ++d) com[d] = -1;
+            status |= rs;
+        } else {
+            accepted_len[r] = a;
+        }
+        if (req_status) req_status[r] = (int32_t)rs;
+        t_off += (size_t)n + 1;
+        n_off += (size_t)n;
+    }
+    return status;
+}
