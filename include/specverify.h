@@ -70,6 +70,7 @@ extern "C" {
 #endif
 
 typedef struct specverify_ctx *specverify_t;
+typedef struct specverify_tree_ctx *specverify_tree_t;
 
 typedef enum {
     SPECVERIFY_F32 = 0,   /* float32 logits */
@@ -91,6 +92,7 @@ typedef enum {
 #define SPECVERIFY_STATUS_BAD_TEMP 4      /* T NaN, negative, infinite or subnormal: request skipped */
 #define SPECVERIFY_STATUS_NONFINITE 8     /* NaN/+inf logit, or no finite logit, in a read row: request skipped */
 #define SPECVERIFY_STATUS_BAD_TOTAL 16    /* sum of num_draft != total_draft: batch skipped */
+#define SPECVERIFY_STATUS_BAD_PARENT 32   /* tree: a parent outside [-1, node index): request skipped */
 #define SPECVERIFY_STATUS_NO_DRAFT 64     /* T > 0 and k > 0 but draft_logits is NULL: request skipped */
 #define SPECVERIFY_STATUS_OVERRUN 128     /* internal: a cluster launch hit its unit cap (a bug); outputs incomplete */
 #define SPECVERIFY_STATUS_TIMEOUT 256     /* stream schedule: a bounded wait ran out (a bug, or the GPU
@@ -260,6 +262,83 @@ int specverify_set_schedule(specverify_t h, int schedule);
  * and one cluster launch.  Waves with nothing left to do return at once.
  * Counts assume 16-byte aligned rows. */
 int specverify_launches_per_run(specverify_t h, int batch, int *launches_out);
+
+/*
+ * specverify_metrics -- acceptance statistics of verify rounds, accumulated on
+ * the device ("Speculative Decoding on AMD GPUs", "Monitor acceptance
+ * behavior" and the appendix tables: mean accepted length MAL, overall
+ * acceptance rate, per-position acceptance rates; the printed rows satisfy
+ * MAL = 1 + the sum of the per-position rates, so MAL counts the round's
+ * correction or bonus token as well).  Needs no handle; runs on the current
+ * device, asynchronously on `stream`, one single-CTA launch.  Device pointers:
+ *   accepted_len [batch] int32  a round's output (-1: request skipped);
+ *   num_draft    [batch] int32  the round's k_r;
+ *   hist     [max_k + 2] uint64 in/out: hist[a] += rounds with A = a (a <= max_k;
+ *                               larger A counts in hist[max_k]), hist[max_k + 1]
+ *                               += skipped requests;
+ *   proposed [max_k] uint64     in/out: += rounds with k_r > j (k_r counts up to max_k);
+ *   accepted [max_k] uint64     in/out: += rounds with A_r > j;
+ *   summary  [max_k + 4] double out, may be NULL: from the counts after this
+ *                               batch: MAL = 1 + sum_a a hist[a] / rounds, the
+ *                               acceptance rate sum(accepted) / sum(proposed), the
+ *                               max_k per-position rates accepted[j] / proposed[j],
+ *                               the number of rounds and of skipped requests
+ *                               (NaN where a denominator is 0).
+ * The counts are running totals owned by the caller (zero them to start);
+ * they are added to with atomics.  proposed and accepted may be NULL when
+ * max_k = 0.  Returns SPECVERIFY_ERR_INVALID_ARG on a bad size or pointer
+ * (max_k in [0, 31]), _CUDA if the launch fails.
+ */
+int specverify_metrics(const int32_t *accepted_len, const int32_t *num_draft, int batch,
+                       int max_k, uint64_t *hist, uint64_t *proposed, uint64_t *accepted,
+                       double *summary, void *stream);
+
+/*
+ * Greedy verification of drafted token trees.
+ *
+ * "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and DSpark",
+ * section 5 (DDTree): the tree uses depth-based positions and ancestor-only
+ * attention; verification walks the target's selected tokens, and when no
+ * child matches, that target token becomes the next bonus token; only the
+ * accepted path survives.  Selection is the target argmax (lowest index on
+ * ties); section 1 of the same page gives no sampling rule for trees, so none
+ * is offered.
+ *
+ * Layout (row-major, one row = V logits; device pointers, caller-owned):
+ *   request r has n_r = num_nodes[r] nodes, 0 <= n_r <= max_nodes;
+ *   node_tokens[n_off(r) + i], parent[n_off(r) + i]  token and parent of node i,
+ *       parent in [-1, i) (-1: child of the root, the last committed token),
+ *       n_off(r) = sum_{s<r} n_s;
+ *   target_logits[t_off(r) + 0]      the target's output at the root,
+ *   target_logits[t_off(r) + 1 + i]  its output after node i,
+ *       t_off(r) = sum_{s<r} (n_s + 1): batch + total_nodes rows in all.
+ * The walk: from the root, tau = argmax of the current node's row; the
+ * lowest-index child of the current node whose token is tau is accepted and
+ * becomes current; when none is, tau is the bonus token.
+ * Outputs:
+ *   accepted_len [batch] int32       A_r, the accepted nodes (-1: skipped);
+ *   path         [batch, max_nodes]  accepted node indices by depth, -1 after;
+ *   committed    [batch, max_nodes+1] accepted tokens then the bonus, -1 after;
+ *   req_status   [batch] int32 (nullable) status bits of each request.
+ * Device-side problems set status bits (specverify_tree_status) and skip the
+ * request: a parent out of range (BAD_PARENT), a token outside [0, V)
+ * (BAD_TOKEN), NaN/+inf or no finite logit in a row the walk reads
+ * (NONFINITE); a num_nodes outside [0, max_nodes] (BAD_K) or a sum other
+ * than total_nodes (BAD_TOTAL) skips the batch.  Every row is read once, in
+ * one HBM pass, then the walk runs (three launches, asynchronous on stream).
+ */
+/* max_batch in [1, 4096], max_nodes in [0, 1024], vocab in [1, 2^30]; allocates
+ * the scratch (chunk maxima of max_batch * (max_nodes + 1) rows) now. */
+int specverify_tree_create(specverify_tree_t *out, int device, int max_batch, int max_nodes,
+                           int vocab, int dtype);
+/* batch in [0, max_batch], total_nodes = host copy of sum num_nodes. */
+int specverify_tree_run(specverify_tree_t h, const void *target_logits, const int32_t *num_nodes,
+                        const int32_t *parent, const int32_t *node_tokens, int batch,
+                        int total_nodes, int32_t *accepted_len, int32_t *path,
+                        int32_t *committed, int32_t *req_status, void *stream);
+/* Waits for the last run's stream and returns its status bits. */
+int specverify_tree_status(specverify_tree_t h, int32_t *status_out);
+int specverify_tree_destroy(specverify_tree_t h);
 
 /* Free the handle and its device memory.  Further use returns _ERR_DESTROYED
  * only while the memory of the freed handle is not reused; do not use it. */

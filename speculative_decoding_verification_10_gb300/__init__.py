@@ -24,6 +24,7 @@ from ._lib import (CREATE_HOST_STAGING, STATUS_BAD_K, STATUS_BAD_TEMP, STATUS_BA
                    STATUS_BAD_TOTAL, STATUS_NO_DRAFT, STATUS_NONFINITE)
 
 __all__ = ["Verifier", "VerifyResult", "SpecVerifyError", "verify", "verify_static",
+           "AcceptanceCounts", "acceptance_metrics", "TreeVerifier", "TreeResult",
            "STATUS_BAD_TOKEN", "STATUS_BAD_K", "STATUS_BAD_TEMP", "STATUS_NONFINITE",
            "STATUS_BAD_TOTAL", "STATUS_NO_DRAFT"]
 
@@ -232,3 +233,113 @@ def verify(target, draft, tokens, num_draft, temperature, seed: int, max_k: int 
                     request_ids=request_ids, debug=debug)
         torch.cuda.current_stream(v.device).synchronize()
         return out
+
+
+@dataclass
+class AcceptanceCounts:
+    """Running acceptance counts on the device (see specverify_metrics):
+    hist [max_k + 2], proposed [max_k], accepted [max_k] (uint64 as int64
+    tensors), and the summary written by the last call: [MAL, acceptance rate,
+    per-position rates (max_k), rounds, skipped] as float64."""
+    max_k: int
+    hist: torch.Tensor
+    proposed: torch.Tensor
+    accepted: torch.Tensor
+    summary: torch.Tensor
+
+    @classmethod
+    def zeros(cls, max_k: int, device) -> "AcceptanceCounts":
+        z = lambda n: torch.zeros(n, dtype=torch.int64, device=device)
+        return cls(max_k, z(max_k + 2), z(max(max_k, 1)), z(max(max_k, 1)),
+                   torch.full((max_k + 4,), float("nan"), dtype=torch.float64, device=device))
+
+    def as_dict(self) -> dict:
+        s = self.summary.cpu().tolist()
+        k = self.max_k
+        return {"mal": s[0], "acceptance_rate": s[1], "per_position": s[2:2 + k],
+                "rounds": int(s[2 + k]), "skipped": int(s[3 + k])}
+
+
+def acceptance_metrics(accepted_len, num_draft, max_k: int, counts: AcceptanceCounts | None = None,
+                       stream=None) -> AcceptanceCounts:
+    """Adds one batch of round outputs (device int32 tensors) to `counts` (new
+    zero counts if None) and writes their summary, asynchronously on `stream`."""
+    lib = _lib.load()
+    dev = accepted_len.device
+    if counts is None:
+        counts = AcceptanceCounts.zeros(max_k, dev)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    code = lib.specverify_metrics(_ptr(accepted_len), _ptr(num_draft), int(accepted_len.shape[0]),
+                                  int(max_k), _ptr(counts.hist), _ptr(counts.proposed),
+                                  _ptr(counts.accepted), _ptr(counts.summary),
+                                  ctypes.c_void_p(s.cuda_stream))
+    _check(code, "specverify_metrics")
+    return counts
+
+
+@dataclass
+class TreeResult:
+    accepted_len: torch.Tensor   # [B] int32, -1 = skipped
+    path: torch.Tensor           # [B, max_nodes] int32 accepted node indices, -1 after
+    committed: torch.Tensor      # [B, max_nodes + 1] int32 accepted tokens then the bonus
+    req_status: torch.Tensor     # [B] int32
+
+
+class TreeVerifier:
+    """Greedy verification of drafted token trees (one library tree handle)."""
+
+    def __init__(self, max_batch: int, max_nodes: int, vocab: int, dtype: str = "bf16",
+                 device: int | None = None):
+        self.lib = _lib.load()
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        self.max_batch, self.max_nodes, self.vocab, self.dtype = max_batch, max_nodes, vocab, dtype
+        h = ctypes.c_void_p()
+        _check(self.lib.specverify_tree_create(ctypes.byref(h), self.device, max_batch, max_nodes,
+                                               vocab, _DTYPES[dtype][0]), "specverify_tree_create")
+        self._h = h
+
+    def run(self, target, num_nodes, parent, tokens, total_nodes: int | None = None,
+            stream=None) -> TreeResult:
+        """One round on device tensors: target [B + sum n, V], num_nodes [B],
+        parent and tokens [sum n] (int32).  Asynchronous on the current stream."""
+        B = int(num_nodes.shape[0])
+        dev = torch.device("cuda", self.device)
+        if total_nodes is None:
+            total_nodes = int(tokens.shape[0])
+        out = TreeResult(torch.empty(B, dtype=torch.int32, device=dev),
+                         torch.empty(B, max(self.max_nodes, 1), dtype=torch.int32, device=dev),
+                         torch.empty(B, self.max_nodes + 1, dtype=torch.int32, device=dev),
+                         torch.empty(B, dtype=torch.int32, device=dev))
+        s = torch.cuda.current_stream(dev) if stream is None else stream
+        p = parent if parent.numel() else None
+        t = tokens if tokens.numel() else None
+        _check(self.lib.specverify_tree_run(self._h, _ptr(target), _ptr(num_nodes), _ptr(p),
+                                            _ptr(t), B, int(total_nodes), _ptr(out.accepted_len),
+                                            _ptr(out.path), _ptr(out.committed),
+                                            _ptr(out.req_status), ctypes.c_void_p(s.cuda_stream)),
+               "specverify_tree_run")
+        if self.max_nodes == 0:
+            out.path = out.path[:, :0]
+        return out
+
+    def status(self) -> int:
+        st = ctypes.c_int32()
+        _check(self.lib.specverify_tree_status(self._h, ctypes.byref(st)), "specverify_tree_status")
+        return int(st.value)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            _check(self.lib.specverify_tree_destroy(self._h), "specverify_tree_destroy")
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

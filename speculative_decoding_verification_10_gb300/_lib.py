@@ -34,6 +34,7 @@ STATUS_BAD_K = 2
 STATUS_BAD_TEMP = 4
 STATUS_NONFINITE = 8
 STATUS_BAD_TOTAL = 16
+STATUS_BAD_PARENT = 32
 STATUS_NO_DRAFT = 64
 
 CREATE_HOST_STAGING = 1
@@ -89,6 +90,16 @@ def load(path: str | None = None):
     lib.specverify_set_schedule.restype = I
     lib.specverify_set_depth.argtypes = [P, I]
     lib.specverify_set_depth.restype = I
+    lib.specverify_metrics.argtypes = [P, P, I, I, P, P, P, P, P]
+    lib.specverify_metrics.restype = I
+    lib.specverify_tree_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I]
+    lib.specverify_tree_create.restype = I
+    lib.specverify_tree_run.argtypes = [P, P, P, P, P, I, I, P, P, P, P, P]
+    lib.specverify_tree_run.restype = I
+    lib.specverify_tree_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
+    lib.specverify_tree_status.restype = I
+    lib.specverify_tree_destroy.argtypes = [P]
+    lib.specverify_tree_destroy.restype = I
     lib.specverify_destroy.argtypes = [P]
     lib.specverify_destroy.restype = I
     lib.specverify_error_string.argtypes = [I]

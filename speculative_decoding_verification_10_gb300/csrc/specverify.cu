@@ -16,7 +16,9 @@
 
 #include "specverify.h"
 #include "sv_cluster.cuh"
+#include "sv_metrics.cuh"
 #include "sv_stream.cuh"
+#include "sv_tree.cuh"
 
 namespace {
 
@@ -520,6 +522,29 @@ struct specverify_ctx {
   cudaEvent_t ev_stop[64];
 };
 
+// A greedy tree verifier: scratch for the chunk partials of every row of the
+// largest batch, the prefix offsets and the status words.
+struct specverify_tree_ctx {
+  uint32_t magic;
+  int device, max_batch, max_nodes, vocab, dtype, elem_bytes;
+  int grid_aligned, grid_scalar;
+  int nchunk;
+  void* scratch;
+  sv::Partial* part;
+  int* t_off;
+  int* n_off;
+  int* ctr;
+  cudaStream_t last_stream;
+  bool last_run_empty;
+};
+
+static int check_tree(specverify_tree_t h) {
+  if (h == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
+  if (h->magic == kDeadMagic) return SPECVERIFY_ERR_DESTROYED;
+  if (h->magic != kLiveMagic) return SPECVERIFY_ERR_INVALID_ARG;
+  return SPECVERIFY_OK;
+}
+
 static int check_handle(specverify_t h) {
   if (h == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
   if (h->magic == kDeadMagic) return SPECVERIFY_ERR_DESTROYED;
@@ -877,6 +902,195 @@ int specverify_destroy(specverify_t h) {
   if (h->stage) ok = (cudaFree(h->stage) == cudaSuccess) && ok;
   h->scratch = nullptr;
   h->stage = nullptr;
+  if (!ok) {
+    cudaGetLastError();
+    return SPECVERIFY_ERR_CUDA;
+  }
+  return SPECVERIFY_OK;
+}
+
+int specverify_metrics(const int32_t* accepted_len, const int32_t* num_draft, int batch,
+                       int max_k, uint64_t* hist, uint64_t* proposed, uint64_t* accepted,
+                       double* summary, void* stream) {
+  if (batch < 0 || max_k < 0 || max_k > sv::kMetricsMaxK || hist == nullptr ||
+      (max_k > 0 && (proposed == nullptr || accepted == nullptr)))
+    return SPECVERIFY_ERR_INVALID_ARG;
+  if (batch > 0 && (accepted_len == nullptr || num_draft == nullptr))
+    return SPECVERIFY_ERR_INVALID_ARG;
+  if (batch == 0 && summary == nullptr) return SPECVERIFY_OK;
+  sv::sv_metrics<<<1, sv::kMetricsThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      accepted_len, num_draft, batch, max_k, reinterpret_cast<unsigned long long*>(hist),
+      reinterpret_cast<unsigned long long*>(proposed),
+      reinterpret_cast<unsigned long long*>(accepted), summary);
+  if (cudaGetLastError() != cudaSuccess) return SPECVERIFY_ERR_CUDA;
+  return SPECVERIFY_OK;
+}
+
+int specverify_tree_create(specverify_tree_t* out, int device, int max_batch, int max_nodes,
+                           int vocab, int dtype) {
+  if (out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (dtype != SPECVERIFY_F32 && dtype != SPECVERIFY_BF16) return SPECVERIFY_ERR_DTYPE;
+  if (max_batch < 1 || max_batch > sv::kMaxBatch || max_nodes < 0 ||
+      max_nodes > sv::kTreeMaxNodes || vocab < 1 || vocab > (1 << 30))
+    return SPECVERIFY_ERR_INVALID_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return SPECVERIFY_ERR_CUDA;
+  }
+  DeviceGuard guard(device);
+  specverify_tree_ctx* h = new (std::nothrow) specverify_tree_ctx();
+  if (!h) return SPECVERIFY_ERR_CUDA;
+  h->device = device;
+  h->max_batch = max_batch;
+  h->max_nodes = max_nodes;
+  h->vocab = vocab;
+  h->dtype = dtype;
+  h->elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
+  h->last_stream = nullptr;
+  h->last_run_empty = true;
+  const int per_vec = 16 / h->elem_bytes;
+  const long long chunk = (long long)sv::kTreeChunkVecs * per_vec;
+  h->nchunk = (int)((vocab + chunk - 1) / chunk);
+  int sms = 0, occ[2] = {0, 0};
+  const void* fn[2];
+  if (dtype == SPECVERIFY_BF16) {
+    fn[0] = reinterpret_cast<const void*>(sv::sv_tree_rows<sv::BF16, false>);
+    fn[1] = reinterpret_cast<const void*>(sv::sv_tree_rows<sv::BF16, true>);
+  } else {
+    fn[0] = reinterpret_cast<const void*>(sv::sv_tree_rows<sv::F32, false>);
+    fn[1] = reinterpret_cast<const void*>(sv::sv_tree_rows<sv::F32, true>);
+  }
+  bool ok = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess;
+  for (int a = 0; a < 2 && ok; ++a)
+    ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[a], fn[a], sv::kTreeThreads, 0) ==
+             cudaSuccess && occ[a] > 0;
+  if (!ok) {
+    cudaGetLastError();
+    delete h;
+    return SPECVERIFY_ERR_CUDA;
+  }
+  h->grid_scalar = occ[0] * sms;
+  h->grid_aligned = occ[1] * sms;
+  const size_t rows = (size_t)max_batch * ((size_t)max_nodes + 1);
+  size_t off = 0;
+  const size_t o_part = off;
+  off = align_up(off + sizeof(sv::Partial) * rows * (size_t)h->nchunk, 256);
+  const size_t o_t = off;
+  off = align_up(off + sizeof(int) * ((size_t)max_batch + 1), 256);
+  const size_t o_n = off;
+  off = align_up(off + sizeof(int) * ((size_t)max_batch + 1), 256);
+  const size_t o_c = off;
+  off = align_up(off + sizeof(int) * 4, 256);
+  if (cudaMalloc(&h->scratch, off) != cudaSuccess ||
+      cudaMemset(h->scratch, 0, off) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->scratch) cudaFree(h->scratch);
+    delete h;
+    return SPECVERIFY_ERR_CUDA;
+  }
+  char* b = static_cast<char*>(h->scratch);
+  h->part = reinterpret_cast<sv::Partial*>(b + o_part);
+  h->t_off = reinterpret_cast<int*>(b + o_t);
+  h->n_off = reinterpret_cast<int*>(b + o_n);
+  h->ctr = reinterpret_cast<int*>(b + o_c);
+  h->magic = kLiveMagic;
+  *out = h;
+  return SPECVERIFY_OK;
+}
+
+int specverify_tree_run(specverify_tree_t h, const void* target_logits, const int32_t* num_nodes,
+                        const int32_t* parent, const int32_t* node_tokens, int batch,
+                        int total_nodes, int32_t* accepted_len, int32_t* path,
+                        int32_t* committed, int32_t* req_status, void* stream) {
+  int rc = check_tree(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (batch < 0 || batch > h->max_batch || total_nodes < 0 ||
+      (long long)total_nodes > (long long)batch * h->max_nodes)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  if (batch == 0) {
+    h->last_run_empty = true;
+    return SPECVERIFY_OK;
+  }
+  if (!target_logits || !num_nodes || !accepted_len || !committed ||
+      (h->max_nodes > 0 && !path) || (total_nodes > 0 && (!parent || !node_tokens)))
+    return SPECVERIFY_ERR_INVALID_ARG;
+  if ((uintptr_t)target_logits & (uintptr_t)(h->elem_bytes - 1)) return SPECVERIFY_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  sv::TreeParams P;
+  std::memset(&P, 0, sizeof P);
+  P.target = target_logits;
+  P.num_nodes = num_nodes;
+  P.parent = parent;
+  P.tokens = node_tokens;
+  P.batch = batch;
+  P.total_nodes = total_nodes;
+  P.max_nodes = h->max_nodes;
+  P.vocab = h->vocab;
+  P.nvec = (int)((size_t)h->vocab * h->elem_bytes / 16);
+  P.nchunk = h->nchunk;
+  P.chunk = sv::kTreeChunkVecs * (16 / h->elem_bytes);
+  P.rows = batch + total_nodes;
+  P.accepted_len = accepted_len;
+  P.path = path;
+  P.committed = committed;
+  P.req_status = req_status;
+  P.part = h->part;
+  P.t_off = h->t_off;
+  P.n_off = h->n_off;
+  P.ctr = h->ctr;
+  const bool aligned = ((size_t)h->vocab * h->elem_bytes) % 16 == 0 &&
+                       ((uintptr_t)target_logits & 15u) == 0;
+  const long long items = (long long)P.rows * P.nchunk;
+  const int grid = (int)std::min<long long>(items, aligned ? h->grid_aligned : h->grid_scalar);
+  sv::sv_tree_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
+  if (h->dtype == SPECVERIFY_BF16) {
+    if (aligned)
+      sv::sv_tree_rows<sv::BF16, true><<<grid, sv::kTreeThreads, 0, s>>>(P);
+    else
+      sv::sv_tree_rows<sv::BF16, false><<<grid, sv::kTreeThreads, 0, s>>>(P);
+  } else {
+    if (aligned)
+      sv::sv_tree_rows<sv::F32, true><<<grid, sv::kTreeThreads, 0, s>>>(P);
+    else
+      sv::sv_tree_rows<sv::F32, false><<<grid, sv::kTreeThreads, 0, s>>>(P);
+  }
+  const int walk_grid = (batch + sv::kTreeWalkWarps - 1) / sv::kTreeWalkWarps;
+  sv::sv_tree_walk<<<walk_grid, sv::kTreeWalkWarps * 32, 0, s>>>(P);
+  h->last_stream = s;
+  h->last_run_empty = false;
+  return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
+}
+
+int specverify_tree_status(specverify_tree_t h, int32_t* status_out) {
+  int rc = check_tree(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (status_out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
+  if (h->last_run_empty) {
+    *status_out = 0;
+    return SPECVERIFY_OK;
+  }
+  DeviceGuard guard(h->device);
+  int32_t st = 0;
+  if (cudaStreamSynchronize(h->last_stream) != cudaSuccess ||
+      cudaMemcpy(&st, h->ctr, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return SPECVERIFY_ERR_CUDA;
+  }
+  *status_out = st;
+  return SPECVERIFY_OK;
+}
+
+int specverify_tree_destroy(specverify_tree_t h) {
+  int rc = check_tree(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  DeviceGuard guard(h->device);
+  h->magic = kDeadMagic;
+  bool ok = cudaDeviceSynchronize() == cudaSuccess;
+  if (h->scratch) ok = (cudaFree(h->scratch) == cudaSuccess) && ok;
+  h->scratch = nullptr;
   if (!ok) {
     cudaGetLastError();
     return SPECVERIFY_ERR_CUDA;
