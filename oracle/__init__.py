@@ -93,6 +93,8 @@ def _load():
         lib.orc_metrics.restype = None
         lib.orc_tree_greedy.argtypes = [ctypes.c_int] * 5 + [P] * 8
         lib.orc_tree_greedy.restype = ctypes.c_uint32
+        lib.orc_trim.argtypes = [ctypes.c_int, P, P, P, P]
+        lib.orc_trim.restype = ctypes.c_uint32
         _lib = lib
         return lib
 
@@ -288,3 +290,60 @@ def tree_greedy(target, num_nodes, parent, tokens, max_nodes, total_nodes=None):
                              _ptr(com), _ptr(rs))
     return {"accepted_len": acc, "path": path, "committed": com, "req_status": rs,
             "status": int(st)}
+
+
+BAD_CONF = 512
+
+
+def trim(window, confidence, cost):
+    """Trimmed window per request (see orc_trim): returns (k [B] int32, status)."""
+    lib = _load()
+    w = np.ascontiguousarray(window, dtype=np.int32)
+    c = np.ascontiguousarray(confidence, dtype=np.float32)
+    lam = np.ascontiguousarray(cost, dtype=np.float32)
+    k = np.empty(len(w), np.int32)
+    st = lib.orc_trim(len(w), _ptr(w), _ptr(c if c.size else np.zeros(1, np.float32)),
+                      _ptr(lam if lam.size else np.zeros(1, np.float32)), _ptr(k))
+    return k, int(st)
+
+
+def verify_trimmed(target, draft, tokens, window, confidence, cost, temperature, seed, max_k,
+                   request_ids=None):
+    """Verify the trimmed windows of a full-window layout ([SD] section 5: compact,
+    variable-length verification of the selected per-request windows): trim, copy
+    each request's rows of positions 0..k* into a compact batch, verify it, and
+    put the per-position flags back in the full layout (0 past k*).  A request
+    with bad confidences is skipped (accepted_len -1)."""
+    w = np.ascontiguousarray(window, dtype=np.int32)
+    B = len(w)
+    k, st = trim(w, confidence, cost)
+    t_off = np.concatenate([[0], np.cumsum(w + 1)])
+    d_off = np.concatenate([[0], np.cumsum(w)])
+    keep = k >= 0
+    kk = np.where(keep, k, 0).astype(np.int32)
+    t_rows = np.concatenate([np.arange(t_off[r], t_off[r] + kk[r] + 1) for r in range(B)]) \
+        if B else np.zeros(0, np.int64)
+    d_rows = np.concatenate([np.arange(d_off[r], d_off[r] + kk[r]) for r in range(B)]) \
+        if B else np.zeros(0, np.int64)
+    t_rows = t_rows.astype(np.int64)
+    d_rows = d_rows.astype(np.int64)
+    sub_draft = None if draft is None else np.asarray(draft)[d_rows]
+    ids = np.arange(B, dtype=np.int64) if request_ids is None else np.asarray(request_ids, np.int64)
+    o = verify(np.asarray(target)[t_rows], sub_draft, np.asarray(tokens)[d_rows], kk,
+               temperature, seed, max_k, request_ids=ids)
+    # per-position values back in the full layout: flags 0, debug values NaN and
+    # no near-threshold margin (+inf) past the trimmed window
+    total = int(w.sum())
+    c_off = np.concatenate([[0], np.cumsum(kk)])
+    for key, fill, dt in (("flags", 0, np.uint8), ("p_y", np.nan, np.float64),
+                          ("q_y", np.nan, np.float64), ("u", np.nan, np.float64),
+                          ("accept_margin", np.inf, np.float64)):
+        full = np.full(total, fill, dt)
+        for r in range(B):
+            full[d_off[r]:d_off[r] + kk[r]] = o[key][c_off[r]:c_off[r + 1]]
+        o[key] = full
+    o["verified_k"] = k
+    o["accepted_len"] = np.where(keep, o["accepted_len"], -1).astype(np.int32)
+    o["committed"] = np.where(keep[:, None], o["committed"], -1).astype(np.int32)
+    o["status"] = int(o["status"]) | st
+    return o

@@ -633,3 +633,56 @@ uint32_t orc_tree_greedy(int dtype, int vocab, int batch, int max_nodes, int tot
     }
     return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Confidence-based window trimming.                                        */
+/*                                                                          */
+/* [SD] section 5, "DSpark: Dependencies Plus a Verification Budget": with  */
+/* conditional confidence estimates c_i, the estimated probability of       */
+/* accepting through position j is s_j = prod_{i<=j} c_i, and verifying a   */
+/* prefix of length k has estimated progress 1 + sum_{j<=k} s_j; the        */
+/* scheduler asks whether another verification position is worth its       */
+/* marginal cost.  Reading taken: with a cost of `cost` (units of progress) */
+/* per verified position, the window is the k in [0, K] that maximises      */
+/* 1 + sum_{j<=k} s_j - cost * k, the shortest on ties.  Request r's        */
+/* confidences are conf[d_off(r) + i], i < K_r (the window's layout).       */
+/* A confidence that is NaN or outside [0, 1], or a NaN cost, sets          */
+/* ORC_BAD_CONF and gives k = -1.                                           */
+/* ------------------------------------------------------------------------ */
+#define ORC_BAD_CONF 512u
+
+uint32_t orc_trim(int batch, const int32_t *window, const float *conf, const float *cost,
+                  int32_t *k_out)
+{
+    uint32_t status = 0;
+    size_t off = 0;
+    for (int r = 0; r < batch; ++r) {
+        const int K = window[r];
+        const double lam = (double)cost[r];
+        int bad = isnan(lam);
+        for (int i = 0; i < K; ++i) {
+            const double c = (double)conf[off + (size_t)i];
+            if (!(c >= 0.0 && c <= 1.0))
+                bad = 1;
+        }
+        if (bad) {
+            k_out[r] = -1;
+            status |= ORC_BAD_CONF;
+        } else {
+            /* the objective, evaluated for every k; the first maximum wins */
+            double best = 1.0, s = 1.0, value = 1.0;
+            int best_k = 0;
+            for (int j = 1; j <= K; ++j) {
+                s *= (double)conf[off + (size_t)(j - 1)];
+                value += s - lam;
+                if (value > best) {
+                    best = value;
+                    best_k = j;
+                }
+            }
+            k_out[r] = best_k;
+        }
+        off += (size_t)(K > 0 ? K : 0);
+    }
+    return status;
+}
