@@ -311,39 +311,45 @@ def verify_trimmed(target, draft, tokens, window, confidence, cost, temperature,
                    request_ids=None):
     """Verify the trimmed windows of a full-window layout ([SD] section 5: compact,
     variable-length verification of the selected per-request windows): trim, copy
-    each request's rows of positions 0..k* into a compact batch, verify it, and
-    put the per-position flags back in the full layout (0 past k*).  A request
-    with bad confidences is skipped (accepted_len -1)."""
+    the rows of positions 0..k* of every request with valid confidences into a
+    compact batch (keeping its request id, so it draws the same numbers), verify
+    it, and put the results back in the full layout (flags 0, debug values NaN
+    past k*).  A request with invalid confidences or cost is skipped with
+    BAD_CONF alone (accepted_len -1)."""
     w = np.ascontiguousarray(window, dtype=np.int32)
     B = len(w)
     k, st = trim(w, confidence, cost)
-    t_off = np.concatenate([[0], np.cumsum(w + 1)])
-    d_off = np.concatenate([[0], np.cumsum(w)])
-    keep = k >= 0
-    kk = np.where(keep, k, 0).astype(np.int32)
-    t_rows = np.concatenate([np.arange(t_off[r], t_off[r] + kk[r] + 1) for r in range(B)]) \
-        if B else np.zeros(0, np.int64)
-    d_rows = np.concatenate([np.arange(d_off[r], d_off[r] + kk[r]) for r in range(B)]) \
-        if B else np.zeros(0, np.int64)
-    t_rows = t_rows.astype(np.int64)
-    d_rows = d_rows.astype(np.int64)
+    t_off = np.concatenate([[0], np.cumsum(w + 1)]).astype(np.int64)
+    d_off = np.concatenate([[0], np.cumsum(w)]).astype(np.int64)
+    good = np.nonzero(k >= 0)[0]
+    kk = k[good].astype(np.int32)
+    t_rows = np.concatenate([np.arange(t_off[r], t_off[r] + k[r] + 1) for r in good] +
+                            [np.zeros(0, np.int64)]).astype(np.int64)
+    d_rows = np.concatenate([np.arange(d_off[r], d_off[r] + k[r]) for r in good] +
+                            [np.zeros(0, np.int64)]).astype(np.int64)
     sub_draft = None if draft is None else np.asarray(draft)[d_rows]
     ids = np.arange(B, dtype=np.int64) if request_ids is None else np.asarray(request_ids, np.int64)
-    o = verify(np.asarray(target)[t_rows], sub_draft, np.asarray(tokens)[d_rows], kk,
-               temperature, seed, max_k, request_ids=ids)
-    # per-position values back in the full layout: flags 0, debug values NaN and
-    # no near-threshold margin (+inf) past the trimmed window
+    temp = np.asarray(temperature, np.float32)
+    c = verify(np.asarray(target)[t_rows], sub_draft, np.asarray(tokens)[d_rows], kk,
+               temp[good], seed, max_k, request_ids=ids[good])
     total = int(w.sum())
-    c_off = np.concatenate([[0], np.cumsum(kk)])
+    out = {"accepted_len": np.full(B, -1, np.int32),
+           "committed": np.full((B, max_k + 1), -1, np.int32),
+           "race_kind": np.zeros(B, np.int32), "race_pos": np.zeros(B, np.int32),
+           "race_margin": np.zeros(B, np.float64),
+           "req_status": np.full(B, BAD_CONF, np.int32),
+           "verified_k": k, "status": int(c["status"]) | st}
+    for key in ("accepted_len", "committed", "race_kind", "race_pos", "race_margin",
+                "req_status"):
+        out[key][good] = c[key]
+    # per-position values in the full layout: flags 0, debug values NaN and no
+    # near-threshold margin (+inf) past the trimmed window
+    c_off = np.concatenate([[0], np.cumsum(kk)]).astype(np.int64)
     for key, fill, dt in (("flags", 0, np.uint8), ("p_y", np.nan, np.float64),
                           ("q_y", np.nan, np.float64), ("u", np.nan, np.float64),
                           ("accept_margin", np.inf, np.float64)):
         full = np.full(total, fill, dt)
-        for r in range(B):
-            full[d_off[r]:d_off[r] + kk[r]] = o[key][c_off[r]:c_off[r + 1]]
-        o[key] = full
-    o["verified_k"] = k
-    o["accepted_len"] = np.where(keep, o["accepted_len"], -1).astype(np.int32)
-    o["committed"] = np.where(keep[:, None], o["committed"], -1).astype(np.int32)
-    o["status"] = int(o["status"]) | st
-    return o
+        for i, r in enumerate(good):
+            full[d_off[r]:d_off[r] + k[r]] = c[key][c_off[i]:c_off[i + 1]]
+        out[key] = full
+    return out
