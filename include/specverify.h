@@ -95,6 +95,8 @@ typedef enum {
 #define SPECVERIFY_STATUS_BAD_PARENT 32   /* tree: a parent outside [-1, node index): request skipped */
 #define SPECVERIFY_STATUS_NO_DRAFT 64     /* T > 0 and k > 0 but draft_logits is NULL: request skipped */
 #define SPECVERIFY_STATUS_OVERRUN 128     /* internal: a cluster launch hit its unit cap (a bug); outputs incomplete */
+#define SPECVERIFY_STATUS_BAD_CONF 512    /* trimmed run: a confidence NaN or outside [0, 1], or a NaN cost:
+                                             request skipped */
 #define SPECVERIFY_STATUS_TIMEOUT 256     /* stream schedule: a bounded wait ran out (a bug, or the GPU
                                              was held by other work for seconds); outputs incomplete */
 
@@ -160,6 +162,41 @@ int specverify_run_ex(specverify_t h, const void *target_logits, const void *dra
                       int32_t *accepted_len, int32_t *committed_tokens, uint8_t *accept_flags,
                       const int64_t *request_ids, float *p_y, float *q_y, float *u,
                       int32_t *req_status, void *stream);
+
+/*
+ * specverify_run_trimmed -- verify per-request windows chosen from draft
+ * confidences, in place in a full-window layout.
+ *
+ * "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and DSpark",
+ * section 5 (DSpark): with conditional confidence estimates c_i the estimated
+ * probability of accepting through position j is s_j = prod_{i<=j} c_i, and
+ * verifying a prefix of length k has estimated progress 1 + sum_{j<=k} s_j;
+ * the scheduler asks whether another verification position is worth its
+ * marginal cost, and compact verification executes only the selected
+ * per-request windows.  Here request r verifies the k_r in [0, K_r] that
+ * maximises 1 + sum_{j<=k} s_j - cost[r] * k (the shortest on ties; fp64),
+ * i.e. a verify round with num_draft = k_r on the same rows: rows past
+ * position k_r are never read, the bonus after k_r acceptances comes from
+ * target row k_r.
+ *   window       [batch] int32: K_r, the layout of the inputs (as num_draft in
+ *                specverify_run: target rows K_r + 1, draft rows and tokens K_r);
+ *   confidence   [total_draft] float32: c_i of each draft position of the
+ *                layout, in [0, 1] (may be NULL when total_draft == 0);
+ *   cost         [batch] float32: cost of one verified position, in units of
+ *                expected progress (any value but NaN; <= 0 keeps every position);
+ *   verified_k   [batch] int32 out: k_r (-1 when the confidences are invalid);
+ *   p_y, q_y, u, req_status: as specverify_run_ex (nullable).
+ * The other arguments and outputs are those of specverify_run; flags are 0
+ * (and debug values NaN) past k_r.  A request with a confidence NaN or outside
+ * [0, 1], or a NaN cost, is skipped with SPECVERIFY_STATUS_BAD_CONF.
+ */
+int specverify_run_trimmed(specverify_t h, const void *target_logits, const void *draft_logits,
+                           const int32_t *draft_tokens, const int32_t *window,
+                           const float *confidence, const float *cost, const float *temperature,
+                           uint64_t seed, int batch, int total_draft, int32_t *verified_k,
+                           int32_t *accepted_len, int32_t *committed_tokens,
+                           uint8_t *accept_flags, float *p_y, float *q_y, float *u,
+                           int32_t *req_status, void *stream);
 
 /*
  * specverify_run_host -- the same verify round on HOST buffers (same shapes as

@@ -51,6 +51,7 @@ class VerifyResult:
     q_y: torch.Tensor | None = None
     u: torch.Tensor | None = None
     req_status: torch.Tensor | None = None
+    verified_k: torch.Tensor | None = None  # trimmed runs: [B] int32 window verified
 
 
 def _ptr(t):
@@ -132,6 +133,29 @@ class Verifier:
             _ptr(out.committed), _ptr(out.flags), _ptr(request_ids), _ptr(out.p_y),
             _ptr(out.q_y), _ptr(out.u), _ptr(out.req_status), self._stream(stream))
         _check(code, "specverify_run")
+        return out
+
+    def run_trimmed(self, target, draft, tokens, window, confidence, cost, temperature,
+                    seed: int, *, total_draft: int | None = None, debug: bool = False,
+                    stream=None) -> VerifyResult:
+        """Verify the windows trimmed from draft confidences (specverify_run_trimmed):
+        `window` [B] is the layout of the inputs, `confidence` [sum window] float32
+        the c_i, `cost` [B] float32 the cost of a verified position.  The result
+        also carries verified_k [B] (the window each request verified)."""
+        self._check_inputs(target, draft, tokens, window, temperature)
+        batch = int(window.shape[0])
+        if total_draft is None:
+            total_draft = int(tokens.shape[0])
+        out = self.outputs(batch, total_draft, debug=debug)
+        out.verified_k = torch.empty(batch, dtype=torch.int32, device=self.device)
+        d = draft if (draft is not None and draft.numel()) else None
+        c = confidence if confidence.numel() else None
+        code = self.lib.specverify_run_trimmed(
+            self._h, _ptr(target), _ptr(d), _ptr(tokens), _ptr(window), _ptr(c), _ptr(cost),
+            _ptr(temperature), int(seed) & (2**64 - 1), batch, int(total_draft),
+            _ptr(out.verified_k), _ptr(out.accepted_len), _ptr(out.committed), _ptr(out.flags),
+            _ptr(out.p_y), _ptr(out.q_y), _ptr(out.u), _ptr(out.req_status), self._stream(stream))
+        _check(code, "specverify_run_trimmed")
         return out
 
     def run_host(self, target, draft, tokens, num_draft, temperature, seed: int,

@@ -36,6 +36,7 @@ STATUS_NONFINITE = 8
 STATUS_BAD_TOTAL = 16
 STATUS_BAD_PARENT = 32
 STATUS_NO_DRAFT = 64
+STATUS_BAD_CONF = 512
 
 CREATE_HOST_STAGING = 1
 
@@ -92,6 +93,9 @@ def load(path: str | None = None):
     lib.specverify_set_depth.restype = I
     lib.specverify_metrics.argtypes = [P, P, I, I, P, P, P, P, P]
     lib.specverify_metrics.restype = I
+    lib.specverify_run_trimmed.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_uint64, I, I,
+                                           P, P, P, P, P, P, P, P, P]
+    lib.specverify_run_trimmed.restype = I
     lib.specverify_tree_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I]
     lib.specverify_tree_create.restype = I
     lib.specverify_tree_run.argtypes = [P, P, P, P, P, I, I, P, P, P, P, P]

@@ -382,6 +382,10 @@ struct RunArgs {
   float* q_y;
   float* u;
   int32_t* req_status;
+  const float* confidence;  // trimmed runs only (NULL when total_draft == 0)
+  const float* cost;
+  int32_t* verified_k;
+  bool trimmed = false;
 };
 
 // Checks that need no device (the batch must already be in range).
@@ -433,6 +437,10 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
   P.q_y = a.q_y;
   P.u_dbg = a.u;
   P.req_status = a.req_status;
+  P.trimmed = a.trimmed ? 1 : 0;
+  P.confidence = a.confidence;
+  P.cost = a.cost;
+  P.verified_k = a.verified_k;
   P.lists = c.sc.lists;
   P.list_cnt = c.sc.list_cnt;
   P.res = c.sc.res;
@@ -687,7 +695,7 @@ int specverify_run(specverify_t h, const void* target_logits, const void* draft_
                    void* stream) {
   const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
                   batch, total_draft, accepted_len, committed_tokens, accept_flags,
-                  nullptr, nullptr, nullptr, nullptr, nullptr};
+                  nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   return run_impl(h, a, stream);
 }
 
@@ -699,7 +707,24 @@ int specverify_run_ex(specverify_t h, const void* target_logits, const void* dra
                       int32_t* req_status, void* stream) {
   const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
                   batch, total_draft, accepted_len, committed_tokens, accept_flags,
-                  request_ids, p_y, q_y, u, req_status};
+                  request_ids, p_y, q_y, u, req_status, nullptr, nullptr, nullptr};
+  return run_impl(h, a, stream);
+}
+
+int specverify_run_trimmed(specverify_t h, const void* target_logits, const void* draft_logits,
+                           const int32_t* draft_tokens, const int32_t* window,
+                           const float* confidence, const float* cost, const float* temperature,
+                           uint64_t seed, int batch, int total_draft, int32_t* verified_k,
+                           int32_t* accepted_len, int32_t* committed_tokens,
+                           uint8_t* accept_flags, float* p_y, float* q_y, float* u,
+                           int32_t* req_status, void* stream) {
+  if (batch > 0 && (cost == nullptr || verified_k == nullptr ||
+                    (total_draft > 0 && confidence == nullptr)))
+    return SPECVERIFY_ERR_INVALID_ARG;
+  RunArgs a{target_logits, draft_logits, draft_tokens, window, temperature, seed,
+            batch, total_draft, accepted_len, committed_tokens, accept_flags,
+            nullptr, p_y, q_y, u, req_status, confidence, cost, verified_k};
+  a.trimmed = true;
   return run_impl(h, a, stream);
 }
 
@@ -743,7 +768,7 @@ int specverify_run_host(specverify_t h, const void* target_logits, const void* d
   const RunArgs a{h->st_target, has_draft ? h->st_draft : nullptr, h->st_tokens,
                   h->st_num_draft, h->st_temperature, seed, batch, total_draft,
                   h->st_accepted, h->st_committed, h->st_flags,
-                  nullptr, nullptr, nullptr, nullptr, nullptr};
+                  nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   rc = run_impl(h, a, stream);
   if (rc != SPECVERIFY_OK) return rc;
   d2h(accepted_len, h->st_accepted, sizeof(int32_t) * (size_t)batch);
@@ -780,7 +805,7 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
   c.schedule_setting = SPECVERIFY_SCHEDULE_WAVES;  // the arena has no bands
   const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
                   batch, total_draft, accepted_len, committed_tokens, accept_flags,
-                  nullptr, nullptr, nullptr, nullptr, nullptr};
+                  nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   int rc = check_args(c, a);
   if (rc != SPECVERIFY_OK || batch == 0) return rc;
 

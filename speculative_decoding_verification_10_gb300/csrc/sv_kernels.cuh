@@ -64,7 +64,8 @@ enum UnitType : int { kUnitEnd = 0, kUnitItem = 1 };
 
 // Status bits (equal to the SPECVERIFY_STATUS_* values of the header).
 constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite = 8u,
-                   kStBadTotal = 16u, kStNoDraft = 64u, kStOverrun = 128u, kStTimeout = 256u;
+                   kStBadTotal = 16u, kStNoDraft = 64u, kStOverrun = 128u, kStTimeout = 256u,
+                   kStBadConf = 512u;
 
 // Number of waves of a round with positions 0..max_k taken D at a time: one
 // per group of D positions, plus one for the residual draws of the last group
@@ -160,6 +161,10 @@ struct Params {
   int stream_mode;   // the plan publishes its rows to the stream schedule's queue
   int band_rows;     // stream schedule: rows a full band takes
   int band_cap;      // stream schedule: bands a round may form
+  int trimmed;              // num_draft is the window layout; verify trimmed windows
+  const float* confidence;  // trimmed runs: c_i per draft position of the window layout
+  const float* cost;        // trimmed runs: cost of one verified position, per request
+  int32_t* verified_k;      // trimmed runs: the window verified per request (out)
   int32_t* accepted_len;
   int32_t* committed;
   uint8_t* flags;
@@ -1315,8 +1320,41 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
+// Confidence-based window trimming ("Speculative Decoding: Medusa, MTP,
+// EAGLE, DFlash, DDTree, and DSpark", section 5, DSpark): with conditional
+// confidences c_i the estimated probability of accepting through position j
+// is s_j = prod_{i<=j} c_i and verifying a prefix of length k has estimated
+// progress 1 + sum_{j<=k} s_j.  The window kept is the k in [0, K] that
+// maximises 1 + sum_{j<=k} s_j - cost * k, the shortest on ties, evaluated in
+// fp64 without contraction.  -1 when a confidence is NaN or outside [0, 1],
+// or the cost is NaN.
+// ---------------------------------------------------------------------------
+__device__ int trim_window(const Params& P, int r, int d0, int K) {
+  const double lam = (double)P.cost[r];
+  bool bad = lam != lam;
+  for (int i = 0; i < K; ++i) {
+    const double c = (double)P.confidence[d0 + i];
+    if (!(c >= 0.0 && c <= 1.0)) bad = true;
+  }
+  if (bad) return -1;
+  double best = 1.0, s = 1.0, value = 1.0;
+  int best_k = 0;
+  for (int j = 1; j <= K; ++j) {
+    s = __dmul_rn(s, (double)P.confidence[d0 + j - 1]);
+    value = __dadd_rn(value, __dsub_rn(s, lam));
+    if (value > best) {
+      best = value;
+      best_k = j;
+    }
+  }
+  return best_k;
+}
+
+// ---------------------------------------------------------------------------
 // The plan launch (one CTA): draft offsets, the layout and input checks, the
-// outputs of requests that cannot be verified, and the rows of wave 0.
+// outputs of requests that cannot be verified, and the rows of wave 0.  In a
+// trimmed run num_draft is the window layout K_r and each request verifies
+// its trimmed window k_r <= K_r in place (rows past k_r are never read).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
   __shared__ int s_w[kPlanThreads / 32 + 1];
@@ -1416,17 +1454,37 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
     bool sampling = false;
     if (r < P.batch) {
       d0 = s_doff[r];
-      k = s_doff[r + 1] - d0;
+      const int K = s_doff[r + 1] - d0;  // the window's layout
+      k = K;
+      uint32_t rs = 0u;
+      if (P.trimmed) {
+        k = trim_window(P, r, d0, K);
+        if (P.verified_k) P.verified_k[r] = k;
+        if (k < 0) {
+          rs = kStBadConf;
+        } else {
+          // positions past the trimmed window: never verified
+          const float nan = __int_as_float(0x7fc00000);
+          for (int i = k; i < K; ++i) {
+            P.flags[d0 + i] = 0;
+            if (P.p_y) P.p_y[d0 + i] = nan;
+            if (P.q_y) P.q_y[d0 + i] = nan;
+            if (P.u_dbg) P.u_dbg[d0 + i] = nan;
+          }
+        }
+      }
       const float t = P.temperature[r];
       const int mode = req_mode(t);
-      uint32_t rs = mode == kBadTemp ? kStBadTemp : 0u;
-      for (int i = 0; i < k; ++i) {
-        const int y = P.tokens[d0 + i];
-        if (y < 0 || y >= P.vocab) rs |= kStBadToken;
+      if (!rs) {
+        if (mode == kBadTemp) rs |= kStBadTemp;
+        for (int i = 0; i < k; ++i) {
+          const int y = P.tokens[d0 + i];
+          if (y < 0 || y >= P.vocab) rs |= kStBadToken;
+        }
+        if (!rs && mode == kSampling && k > 0 && P.draft == nullptr) rs |= kStNoDraft;
       }
-      if (!rs && mode == kSampling && k > 0 && P.draft == nullptr) rs |= kStNoDraft;
       if (rs) {
-        skip_request_thread(P, r, d0, k, rs);
+        skip_request_thread(P, r, d0, K, rs);
       } else {
         sampling = mode == kSampling;
         c = sampling ? kLog2e / t : 0.f;
