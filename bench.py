@@ -61,6 +61,9 @@ def parse_args():
                     help="positions per wave launch (0 = chosen per run)")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per batch (0 = the workload's own); for profiling captures")
+    ap.add_argument("--trim", type=float, default=None,
+                    help="verify windows trimmed from draft confidences, at this cost per "
+                         "verified position (specverify_run_trimmed)")
     return ap.parse_args()
 
 
@@ -295,19 +298,34 @@ def run_ours(args):
     out = v.outputs(b.batch, b.total_draft)
     stream = torch.cuda.current_stream(dev)
 
+    conf = cost = None
+    if args.trim is not None:
+        # synthetic draft confidences: c_i uniform in [0.6, 1) from a seeded generator
+        gconf = torch.Generator("cpu").manual_seed(4242 + rank)
+        conf = (0.6 + 0.4 * torch.rand(b.total_draft, generator=gconf)).to(dev)
+        cost = torch.full((b.batch,), float(args.trim), dtype=torch.float32, device=dev)
+
     def step():
+        if conf is not None:
+            return v.run_trimmed(b.target, b.draft, b.tokens, b.num_draft, conf, cost,
+                                 b.temperature, 1)
         v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 1, out=out)
+        return out
 
     for _ in range(max(3, args.warmup)):
-        step()
+        res = step()
     torch.cuda.synchronize()
     if v.status() != 0:
         raise RuntimeError(f"verify status {v.status()} on the benchmark batch")
     # bytes the round must read: positions 0..A of each request (target and draft
     # rows when sampling, target rows when greedy) and the bonus row when A = k
-    A = out.accepted_len.cpu().numpy().astype(np.int64)
+    # (k = the verified window: the trimmed one in a trimmed round)
+    A = res.accepted_len.cpu().numpy().astype(np.int64)
+    if conf is not None:
+        k = res.verified_k.cpu().numpy().astype(np.int64)
+        rows_per_step = int((k + 1).sum())
     rows_needed = np.where(t > 0, np.where(A < k, 2 * (A + 1), 2 * k + 1), A + 1)
-    rowpass_bytes = b.needed_bytes(A)
+    rowpass_bytes = int(rows_needed.sum()) * b.vocab * es
     alg_bytes = rowpass_bytes + b.io_bytes()
 
     n_ev = min(64, args.steps)
@@ -387,7 +405,8 @@ def run_ours(args):
                    "l2": "no flush: each step reads %.2f GB of logits, larger than the 129 MB L2"
                          % (rowpass_bytes / 1e9),
                    "parallelism": f"replicas x{world}",
-                   "schedule": args.schedule, "depth": args.depth},
+                   "schedule": args.schedule, "depth": args.depth,
+                   "trim_cost": args.trim},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "sv_wave", "kernel_ms": kernel_avg_ms,
@@ -407,10 +426,118 @@ def run_ours(args):
     return 0
 
 
+def run_tree(args):
+    """Greedy tree verification rounds (specverify_tree_run) on a synthetic tree batch."""
+    import torch
+    import torch.distributed as dist
+    from speculative_decoding_verification_10_gb300 import TreeVerifier, build
+    from speculative_decoding_verification_10_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    tb = W.make_tree_batch(args.workload, device=dev, batch=args.batch or None)
+    tv = TreeVerifier(tb.batch, tb.max_nodes, tb.vocab, tb.dtype, device=local)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        res = tv.run(tb.target, tb.num_nodes, tb.parent, tb.tokens)
+    torch.cuda.synchronize()
+    if tv.status() != 0:
+        raise RuntimeError(f"tree status {tv.status()}")
+    A = res.accepted_len.cpu().numpy()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    t0.record(stream)
+    for _ in range(args.steps):
+        tv.run(tb.target, tb.num_nodes, tb.parent, tb.tokens)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("stop")
+    ms = t0.elapsed_time(t1) / args.steps
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    clock_info = clocks.stop()
+    # end to end through the public API: pinned host inputs copied in, outputs back
+    h = [x.cpu().pin_memory() for x in (tb.target, tb.num_nodes, tb.parent, tb.tokens)]
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    torch.cuda.synchronize()
+    te = time.perf_counter()
+    for _ in range(e2e_steps):
+        d = [x.to(dev, non_blocking=True) for x in h]
+        r2 = tv.run(*d)
+        out_host = (r2.accepted_len.cpu(), r2.path.cpu(), r2.committed.cpu())
+    e2e_s = (time.perf_counter() - te) / e2e_steps
+    rows = tb.rows()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = min(tb.batch, 8)
+        sub = slice(0, n * (tb.max_nodes + 1))
+        tgt = tb.target[sub].cpu()
+        tgt = tgt.view(torch.int16).numpy().view(np.uint16) if tb.dtype == "bf16" else tgt.numpy()
+        tc = time.perf_counter()
+        oracle.tree_greedy(tgt, tb.num_nodes[:n].cpu().numpy(),
+                           tb.parent[:n * tb.max_nodes].cpu().numpy(),
+                           tb.tokens[:n * tb.max_nodes].cpu().numpy(), tb.max_nodes)
+        dt = time.perf_counter() - tc
+        cpu = {"value": n * (tb.max_nodes + 1) / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} of {tb.batch} trees ({n * (tb.max_nodes + 1)} rows), {dt:.1f} s"}
+    tv.close()
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peak()
+    alg = rows * tb.row_bytes()
+    achieved = alg / (ms_max * 1e-3) / 1e9
+    h2d = sum(x.numel() * x.element_size() for x in h)
+    d2h = sum(x.numel() * x.element_size() for x in out_host)
+    line = {
+        "metric": METRIC, "value": world * rows / (ms_max * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": tb.batch, "nodes": tb.max_nodes,
+                   "vocab": tb.vocab, "logits": tb.dtype, "rows_per_step": rows,
+                   "mean_accepted": float(A.mean()),
+                   "l2": "no flush: each step reads %.2f GB of logits, larger than the 129 MB L2"
+                         % (alg / 1e9), "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "sv_tree_rows", "alg_bytes_per_launch": alg,
+                     "window": "one round: sv_tree_plan + sv_tree_rows + sv_tree_walk",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * rows / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "clocks": clock_info,
+        "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    from speculative_decoding_verification_10_gb300 import workloads as W
+    if args.workload in W.TREE_SPECS:
+        return run_tree(args)
     return run_ours(args)
 
 

@@ -232,3 +232,79 @@ def subset(b: Batch, requests) -> Batch:
                  b.tokens[di].contiguous(), b.num_draft[ri].contiguous(),
                  b.temperature[ri].contiguous(), b.max_k, b.vocab, b.dtype,
                  base_ids.to(torch.int64), dict(b.info))
+
+
+# ---------------------------------------------------------------------------
+# Drafted token trees (greedy tree verification).
+#
+#   t0_v151936_bf16 : 64 requests, trees of 32 nodes (a DDTree-sized node
+#                     budget), V=151936, bf16; node parents drawn so that depth
+#                     grows along the node order (each node hangs off one of the
+#                     8 nodes before it, or the root); target rows N(0, 3^2);
+#                     a node's token is its parent row's argmax with
+#                     probability 0.6 (a drafter that often agrees), else a
+#                     uniform token.
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class TreeSpec:
+    name: str
+    batch: int
+    nodes: int
+    vocab: int
+    dtype: str
+    sigma_t: float
+    p_agree: float
+    gen_seed: int
+
+
+TREE_SPECS = {
+    "t0_v151936_bf16": TreeSpec("t0_v151936_bf16", 64, 32, 151936, "bf16", 3.0, 0.6, 1100),
+}
+
+
+@dataclass
+class TreeBatch:
+    name: str
+    target: torch.Tensor      # [B + sum n, V]
+    num_nodes: torch.Tensor   # [B] int32
+    parent: torch.Tensor      # [sum n] int32
+    tokens: torch.Tensor      # [sum n] int32
+    max_nodes: int
+    vocab: int
+    dtype: str
+
+    @property
+    def batch(self) -> int:
+        return int(self.num_nodes.shape[0])
+
+    def rows(self) -> int:
+        return int(self.target.shape[0])
+
+    def row_bytes(self) -> int:
+        return self.vocab * (2 if self.dtype == "bf16" else 4)
+
+
+def make_tree_batch(name: str, device="cpu", batch: int | None = None) -> TreeBatch:
+    spec = TREE_SPECS[name]
+    B = spec.batch if batch is None else batch
+    g = torch.Generator("cpu").manual_seed(spec.gen_seed)
+    rng = np.random.default_rng(spec.gen_seed)
+    n = spec.nodes
+    num = np.full(B, n, np.int32)
+    parents = []
+    for _ in range(B):
+        parents.append([-1] + [int(rng.integers(max(-1, i - 8), i)) for i in range(1, n)])
+    target = torch.randn((B * (n + 1), spec.vocab), generator=g) * spec.sigma_t
+    target = _to_dtype(target, spec.dtype)
+    # the drafter's token at node i: the parent row's argmax (torch) or uniform noise
+    arg = target.float().argmax(dim=1).numpy()
+    toks = []
+    for r in range(B):
+        for i in range(n):
+            row = r * (n + 1) + parents[r][i] + 1
+            toks.append(int(arg[row]) if rng.random() < spec.p_agree
+                        else int(rng.integers(0, spec.vocab)))
+    return TreeBatch(name, target.to(device), torch.from_numpy(num).to(device),
+                     torch.tensor(sum(parents, []), dtype=torch.int32, device=device),
+                     torch.tensor(toks, dtype=torch.int32, device=device), n, spec.vocab,
+                     spec.dtype)
