@@ -35,6 +35,7 @@ constexpr int kTreeThreads = 256;
 constexpr int kTreeVecsPerThread = 8;                                  // loads in flight
 constexpr int kTreeChunkVecs = kTreeThreads * kTreeVecsPerThread * 2;  // 64 KB chunks
 constexpr int kTreeWalkWarps = 8;
+constexpr int kTreeRegNodes = 4;  // nodes per lane the walk keeps in registers (128 per tree)
 constexpr int kTreeMaxNodes = 1024;
 constexpr uint32_t kStBadParent = 32u;
 
@@ -190,9 +191,19 @@ __global__ void __launch_bounds__(kTreeWalkWarps * 32) sv_tree_walk(TreeParams P
     const int n0 = P.n_off[r], t0 = P.t_off[r];
     const int32_t* par = P.parent + n0;
     const int32_t* tok = P.tokens + n0;
+    // the first 32 * kTreeRegNodes nodes stay in registers for the whole walk
+    int rp[kTreeRegNodes], rt[kTreeRegNodes];
+#pragma unroll
+    for (int j = 0; j < kTreeRegNodes; ++j) {
+      const int i = j * 32 + lane;
+      rp[j] = i < n ? par[i] : -2;
+      rt[j] = i < n ? tok[i] : -1;
+    }
     for (int i = lane; i < n; i += 32) {
-      if (par[i] < -1 || par[i] >= i) rs |= kStBadParent;
-      if (tok[i] < 0 || tok[i] >= P.vocab) rs |= kStBadToken;
+      const int pi = i < 32 * kTreeRegNodes ? rp[i / 32] : par[i];
+      const int ti = i < 32 * kTreeRegNodes ? rt[i / 32] : tok[i];
+      if (pi < -1 || pi >= i) rs |= kStBadParent;
+      if (ti < 0 || ti >= P.vocab) rs |= kStBadToken;
     }
     rs = __reduce_or_sync(0xffffffffu, rs);
     int cur = -1;
@@ -218,7 +229,12 @@ __global__ void __launch_bounds__(kTreeWalkWarps * 32) sv_tree_walk(TreeParams P
       if (lane == 0) com[a] = tau;
       // the lowest-index child of `cur` whose token is tau
       int child = -1;
-      for (int i0 = 0; i0 < n && child < 0; i0 += 32) {
+#pragma unroll
+      for (int j = 0; j < kTreeRegNodes; ++j) {
+        const unsigned m = __ballot_sync(0xffffffffu, rp[j] == cur && rt[j] == tau);
+        if (child < 0 && m) child = j * 32 + __ffs(m) - 1;
+      }
+      for (int i0 = 32 * kTreeRegNodes; i0 < n && child < 0; i0 += 32) {
         const int i = i0 + lane;
         const unsigned m = __ballot_sync(0xffffffffu, i < n && par[i] == cur && tok[i] == tau);
         if (m) child = i0 + __ffs(m) - 1;
