@@ -95,6 +95,8 @@ def _load():
         lib.orc_tree_greedy.restype = ctypes.c_uint32
         lib.orc_trim.argtypes = [ctypes.c_int, P, P, P, P]
         lib.orc_trim.restype = ctypes.c_uint32
+        lib.orc_truncate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int] + [P] * 10
+        lib.orc_truncate.restype = ctypes.c_uint32
         _lib = lib
         return lib
 
@@ -353,3 +355,28 @@ def verify_trimmed(target, draft, tokens, window, confidence, cost, temperature,
             full[d_off[r]:d_off[r] + k[r]] = c[key][c_off[i]:c_off[i + 1]]
         out[key] = full
     return out
+
+
+BAD_TRUNC = 1024
+
+
+def truncate(target, draft, num_draft, temperature, top_k, top_p):
+    """Top-k / top-p truncation of every row (see orc_truncate).  Returns
+    (target_out, draft_out, margin_t, margin_d, status); logits keep their dtype
+    (float32, or bf16 bits as uint16) with -inf where truncated."""
+    lib = _load()
+    t, dt = _logits(target)
+    d = None if draft is None else _logits(draft)[0]
+    nd = np.ascontiguousarray(num_draft, dtype=np.int32)
+    temp = np.ascontiguousarray(temperature, dtype=np.float32)
+    k = np.ascontiguousarray(top_k, dtype=np.int32)
+    p = np.ascontiguousarray(top_p, dtype=np.float32)
+    t_out = np.empty_like(t)
+    d_out = None if d is None else np.empty_like(d)
+    m_t = np.empty(t.shape[0], np.float64)
+    m_d = np.empty(0 if d is None else d.shape[0], np.float64)
+    st = lib.orc_truncate(dt, t.shape[1], len(nd), _ptr(nd), _ptr(temp), _ptr(k), _ptr(p),
+                          _ptr(t), None if d is None or d.size == 0 else _ptr(d), _ptr(t_out),
+                          None if d is None or d.size == 0 else _ptr(d_out), _ptr(m_t),
+                          _ptr(m_d) if m_d.size else None)
+    return t_out, d_out, m_t, m_d, int(st)

@@ -686,3 +686,135 @@ uint32_t orc_trim(int batch, const int32_t *window, const float *conf, const flo
     }
     return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Top-k / top-p truncation, applied alike to the target and draft rows.    */
+/*                                                                          */
+/* [SD] section 1: temperature, truncation, penalties and grammar           */
+/* constraints must be incorporated consistently -- the acceptance test and */
+/* the residual must use the distributions the target and the drafter       */
+/* actually sample from.  Readings taken (the page names no rule):          */
+/*   temperature first: p = softmax(x / T);                                 */
+/*   top-k (0 < K < V): keep every logit >= the K-th largest logit (ties    */
+/*     with it are kept);                                                   */
+/*   top-p (0 < P < 1), on the top-k survivors renormalised: keep v when    */
+/*     the mass of the survivors with a strictly larger logit is below P    */
+/*     (the most probable token is always kept);                            */
+/*   the kept logits are copied, the others become -inf, so softmax of the  */
+/*   output row is the truncated, renormalised distribution.                */
+/* K <= 0 or K >= V turns top-k off, P >= 1 turns top-p off; P NaN or <= 0  */
+/* is invalid (ORC_BAD_TRUNC, row copied unchanged).  Rows of greedy        */
+/* requests (T = 0) and rows holding NaN are copied unchanged (the verify   */
+/* itself reads them).  margin_out[row] (nullable) gets the relative        */
+/* distance of the top-p decision from its threshold, min over the last     */
+/* kept and the first dropped logit of |mass_gt - P| / P (+inf without      */
+/* top-p): fp32 arithmetic may decide rows within 1e-5 differently.          */
+/* ------------------------------------------------------------------------ */
+#define ORC_BAD_TRUNC 1024u
+
+static int cmp_desc(const void *a, const void *b)
+{
+    const double x = *(const double *)a, y = *(const double *)b;
+    return x < y ? 1 : (x > y ? -1 : 0);
+}
+
+static uint32_t truncate_row(int dtype, int vocab, const void *in, size_t row, float t, int k,
+                             float p, void *out, double *margin)
+{
+    const size_t esz = dtype == ORC_DTYPE_F32 ? 4 : 2;
+    memcpy((char *)out + row * (size_t)vocab * esz, (const char *)in + row * (size_t)vocab * esz,
+           (size_t)vocab * esz);
+    *margin = INFINITY;
+    const int top_k = k > 0 && k < vocab;
+    const int top_p = p < 1.0f;
+    if (p != p || p <= 0.0f)
+        return ORC_BAD_TRUNC;
+    if (!(t > 0.0f) || (!top_k && !top_p))
+        return 0;
+    double *x = malloc(sizeof(double) * (size_t)vocab);
+    double *srt = malloc(sizeof(double) * (size_t)vocab);
+    for (int v = 0; v < vocab; ++v) {
+        x[v] = logit_at(in, dtype, row, vocab, v);
+        if (isnan(x[v])) {
+            free(x);
+            free(srt);
+            return 0;
+        }
+        srt[v] = x[v];
+    }
+    qsort(srt, (size_t)vocab, sizeof(double), cmp_desc);
+    double tau = -INFINITY;   /* keep x >= tau */
+    if (top_k)
+        tau = srt[k - 1];
+    if (top_p) {
+        /* masses of the survivors, renormalised, from the largest logit down;  */
+        /* every logit value of a run of equal values shares mass_gt            */
+        const double m = srt[0];
+        double total = 0.0;
+        int n_kept = 0;
+        while (n_kept < vocab && srt[n_kept] >= tau) {
+            total += exp((srt[n_kept] - m) / (double)t);
+            ++n_kept;
+        }
+        double gt = 0.0;      /* mass of strictly larger survivors */
+        int i = 0;
+        double tau_p = srt[0], last_kept_gt = 0.0, first_drop_gt = INFINITY;
+        while (i < n_kept) {
+            int j = i;
+            double run = 0.0;
+            while (j < n_kept && srt[j] == srt[i]) {
+                run += exp((srt[j] - m) / (double)t);
+                ++j;
+            }
+            if (gt / total < (double)p) {
+                tau_p = srt[i];
+                last_kept_gt = gt / total;
+            } else {
+                first_drop_gt = gt / total;
+                break;
+            }
+            gt += run;
+            i = j;
+        }
+        tau = tau_p > tau ? tau_p : tau;
+        const double mk = ((double)p - last_kept_gt) / (double)p;
+        const double md = (first_drop_gt - (double)p) / (double)p;
+        *margin = mk < md ? mk : md;
+    }
+    for (int v = 0; v < vocab; ++v) {
+        if (x[v] >= tau)
+            continue;
+        if (dtype == ORC_DTYPE_F32) {
+            ((float *)out)[row * (size_t)vocab + (size_t)v] = -INFINITY;
+        } else {
+            ((uint16_t *)out)[row * (size_t)vocab + (size_t)v] = 0xff80u;  /* bf16 -inf */
+        }
+    }
+    free(x);
+    free(srt);
+    return 0;
+}
+
+/* Truncates every target and draft row of a ragged batch (layout as        */
+/* orc_verify) with its request's temperature, top_k and top_p.  draft_in   */
+/* may be NULL.  Returns the status bits.                                   */
+uint32_t orc_truncate(int dtype, int vocab, int batch, const int32_t *num_draft,
+                      const float *temperature, const int32_t *top_k, const float *top_p,
+                      const void *target_in, const void *draft_in, void *target_out,
+                      void *draft_out, double *margin_t, double *margin_d)
+{
+    uint32_t status = 0;
+    size_t t_row = 0, d_row = 0;
+    double scratch;
+    for (int r = 0; r < batch; ++r) {
+        const int k = num_draft[r];
+        for (int i = 0; i <= k; ++i, ++t_row)
+            status |= truncate_row(dtype, vocab, target_in, t_row, temperature[r], top_k[r],
+                                   top_p[r], target_out, margin_t ? &margin_t[t_row] : &scratch);
+        if (draft_in)
+            for (int i = 0; i < k; ++i, ++d_row)
+                status |= truncate_row(dtype, vocab, draft_in, d_row, temperature[r], top_k[r],
+                                       top_p[r], draft_out, margin_d ? &margin_d[d_row] : &scratch);
+    }
+    return status;
+}
