@@ -97,6 +97,7 @@ typedef enum {
 #define SPECVERIFY_STATUS_OVERRUN 128     /* internal: a cluster launch hit its unit cap (a bug); outputs incomplete */
 #define SPECVERIFY_STATUS_BAD_CONF 512    /* trimmed run: a confidence NaN or outside [0, 1], or a NaN cost:
                                              request skipped */
+#define SPECVERIFY_STATUS_BAD_TRUNC 1024  /* truncation: a top_p NaN or <= 0 (its rows copied) */
 #define SPECVERIFY_STATUS_TIMEOUT 256     /* stream schedule: a bounded wait ran out (a bug, or the GPU
                                              was held by other work for seconds); outputs incomplete */
 
@@ -329,6 +330,40 @@ int specverify_launches_per_run(specverify_t h, int batch, int *launches_out);
 int specverify_metrics(const int32_t *accepted_len, const int32_t *num_draft, int batch,
                        int max_k, uint64_t *hist, uint64_t *proposed, uint64_t *accepted,
                        double *summary, void *stream);
+
+/*
+ * specverify_truncate -- top-k / top-p truncation applied alike to the target
+ * and draft rows of a ragged batch, before a verify round.
+ *
+ * "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and DSpark",
+ * section 1: temperature, truncation, penalties and grammar constraints must be
+ * incorporated consistently -- the acceptance test and the residual must use
+ * the distributions the target and the drafter actually sample from.  Per
+ * request r (T_r > 0):
+ *   top_k[r] = K (0 < K < V): keep every logit >= the K-th largest (ties kept);
+ *   top_p[r] = P (0 < P < 1): on the top-k survivors renormalised
+ *     (softmax(x / T)), keep a logit while the mass of the survivors with a
+ *     strictly larger logit is below P;
+ *   kept logits are copied to the output, the others become -inf, so softmax
+ *   of an output row is the truncated, renormalised distribution and
+ *   specverify_run on the outputs verifies the truncated distributions (draft
+ *   tokens must have been sampled from the truncated draft distribution).
+ * K <= 0 or K >= V turns top-k off, P >= 1 turns top-p off; rows of greedy
+ * requests (T = 0) and rows holding NaN are copied; a P NaN or <= 0 copies the
+ * rows and sets SPECVERIFY_STATUS_BAD_TRUNC in *status (nullable device int32,
+ * OR-ed).  The top-k threshold is exact; the top-p masses are fp32 2^(c x)
+ * summed as 2^-40 fixed-point integers (independent of summation order), so a
+ * top-p decision within about 1e-6 of its threshold can differ from an exact
+ * computation.
+ * Layout as specverify_run: target_in/_out [batch + total_draft, vocab],
+ * draft_in/_out [total_draft, vocab] (both NULL, or both given), dtype F32 or
+ * BF16, device pointers on the current device; asynchronous on stream, one
+ * launch (one CTA per SM, a few passes over each row through L2).
+ */
+int specverify_truncate(int dtype, int vocab, const void *target_in, const void *draft_in,
+                        const int32_t *num_draft, const float *temperature, const int32_t *top_k,
+                        const float *top_p, int batch, int total_draft, void *target_out,
+                        void *draft_out, int32_t *status, void *stream);
 
 /*
  * Greedy verification of drafted token trees.

@@ -24,7 +24,7 @@ from ._lib import (CREATE_HOST_STAGING, STATUS_BAD_K, STATUS_BAD_TEMP, STATUS_BA
                    STATUS_BAD_TOTAL, STATUS_NO_DRAFT, STATUS_NONFINITE)
 
 __all__ = ["Verifier", "VerifyResult", "SpecVerifyError", "verify", "verify_static",
-           "AcceptanceCounts", "acceptance_metrics", "TreeVerifier", "TreeResult",
+           "AcceptanceCounts", "acceptance_metrics", "TreeVerifier", "TreeResult", "truncate",
            "STATUS_BAD_TOKEN", "STATUS_BAD_K", "STATUS_BAD_TEMP", "STATUS_NONFINITE",
            "STATUS_BAD_TOTAL", "STATUS_NO_DRAFT"]
 
@@ -367,3 +367,27 @@ class TreeVerifier:
             self.close()
         except Exception:
             pass
+
+
+def truncate(target, draft, num_draft, temperature, top_k, top_p, *, out_target=None,
+             out_draft=None, status=None, stream=None):
+    """Top-k / top-p truncation of every target and draft row (specverify_truncate):
+    returns (target_out, draft_out) with -inf where truncated.  top_k [B] int32,
+    top_p [B] float32; status (optional [1] int32 device tensor) gets BAD_TRUNC OR-ed."""
+    lib = _lib.load()
+    dtype = "bf16" if target.dtype == torch.bfloat16 else "f32"
+    dev = target.device
+    B = int(num_draft.shape[0])
+    d = draft if (draft is not None and draft.numel()) else None
+    out_target = torch.empty_like(target) if out_target is None else out_target
+    if d is not None and out_draft is None:
+        out_draft = torch.empty_like(d)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    total = 0 if d is None else int(d.shape[0])
+    code = lib.specverify_truncate(_DTYPES[dtype][0], int(target.shape[1]), _ptr(target), _ptr(d),
+                                   _ptr(num_draft), _ptr(temperature), _ptr(top_k), _ptr(top_p),
+                                   B, total if d is not None else int(target.shape[0]) - B,
+                                   _ptr(out_target), _ptr(out_draft if d is not None else None),
+                                   _ptr(status), ctypes.c_void_p(s.cuda_stream))
+    _check(code, "specverify_truncate")
+    return out_target, (out_draft if d is not None else draft)

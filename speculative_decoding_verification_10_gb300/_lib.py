@@ -37,6 +37,7 @@ STATUS_BAD_TOTAL = 16
 STATUS_BAD_PARENT = 32
 STATUS_NO_DRAFT = 64
 STATUS_BAD_CONF = 512
+STATUS_BAD_TRUNC = 1024
 
 CREATE_HOST_STAGING = 1
 
@@ -96,6 +97,8 @@ def load(path: str | None = None):
     lib.specverify_run_trimmed.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_uint64, I, I,
                                            P, P, P, P, P, P, P, P, P]
     lib.specverify_run_trimmed.restype = I
+    lib.specverify_truncate.argtypes = [I, I, P, P, P, P, P, P, I, I, P, P, P, P]
+    lib.specverify_truncate.restype = I
     lib.specverify_tree_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I]
     lib.specverify_tree_create.restype = I
     lib.specverify_tree_run.argtypes = [P, P, P, P, P, I, I, P, P, P, P, P]

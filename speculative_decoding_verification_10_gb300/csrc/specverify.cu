@@ -19,6 +19,7 @@
 #include "sv_metrics.cuh"
 #include "sv_stream.cuh"
 #include "sv_tree.cuh"
+#include "sv_trunc.cuh"
 
 namespace {
 
@@ -1121,6 +1122,62 @@ int specverify_tree_destroy(specverify_tree_t h) {
     return SPECVERIFY_ERR_CUDA;
   }
   return SPECVERIFY_OK;
+}
+
+int specverify_truncate(int dtype, int vocab, const void* target_in, const void* draft_in,
+                        const int32_t* num_draft, const float* temperature, const int32_t* top_k,
+                        const float* top_p, int batch, int total_draft, void* target_out,
+                        void* draft_out, int32_t* status, void* stream) {
+  if (dtype != SPECVERIFY_F32 && dtype != SPECVERIFY_BF16) return SPECVERIFY_ERR_DTYPE;
+  if (vocab < 1 || vocab > (1 << 30) || batch < 0 || total_draft < 0)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  if (batch == 0) return SPECVERIFY_OK;
+  if (!target_in || !target_out || !num_draft || !temperature || !top_k || !top_p ||
+      (draft_in != nullptr) != (draft_out != nullptr))
+    return SPECVERIFY_ERR_INVALID_ARG;
+  const int es = dtype == SPECVERIFY_BF16 ? 2 : 4;
+  const uintptr_t mask = 15u;
+  const bool aligned = ((size_t)vocab * es) % 16 == 0 && ((uintptr_t)target_in & mask) == 0 &&
+                       ((uintptr_t)target_out & mask) == 0 &&
+                       ((uintptr_t)draft_in & mask) == 0 && ((uintptr_t)draft_out & mask) == 0;
+  if (((uintptr_t)target_in | (uintptr_t)target_out | (uintptr_t)draft_in |
+       (uintptr_t)draft_out) & (uintptr_t)(es - 1))
+    return SPECVERIFY_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SPECVERIFY_ERR_CUDA;
+  }
+  sv::TruncParams P;
+  P.target_in = target_in;
+  P.draft_in = total_draft > 0 ? draft_in : nullptr;
+  P.target_out = target_out;
+  P.draft_out = total_draft > 0 ? draft_out : nullptr;
+  P.num_draft = num_draft;
+  P.temperature = temperature;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.batch = batch;
+  P.total_draft = total_draft;
+  P.vocab = vocab;
+  P.status = status;
+  // one CTA per SM: the rows in flight (one per CTA) stay in L2 across the passes
+  const long long rows = (long long)batch + 2ll * total_draft;
+  const int grid = (int)std::min<long long>(rows, sms);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == SPECVERIFY_BF16) {
+    if (aligned)
+      sv::sv_truncate<sv::BF16, true><<<grid, sv::kTruncThreads, 0, s>>>(P);
+    else
+      sv::sv_truncate<sv::BF16, false><<<grid, sv::kTruncThreads, 0, s>>>(P);
+  } else {
+    if (aligned)
+      sv::sv_truncate<sv::F32, true><<<grid, sv::kTruncThreads, 0, s>>>(P);
+    else
+      sv::sv_truncate<sv::F32, false><<<grid, sv::kTruncThreads, 0, s>>>(P);
+  }
+  return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
 }
 
 const char* specverify_error_string(int code) {
