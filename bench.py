@@ -61,6 +61,10 @@ def parse_args():
                     help="positions per wave launch (0 = chosen per run)")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per batch (0 = the workload's own); for profiling captures")
+    ap.add_argument("--top-k", type=int, default=None,
+                    help="truncate every row to its top-k logits before the round (specverify_truncate)")
+    ap.add_argument("--top-p", type=float, default=None,
+                    help="truncate every row to its top-p nucleus before the round (specverify_truncate)")
     ap.add_argument("--trim", type=float, default=None,
                     help="verify windows trimmed from draft confidences, at this cost per "
                          "verified position (specverify_run_trimmed)")
@@ -305,7 +309,22 @@ def run_ours(args):
         conf = (0.6 + 0.4 * torch.rand(b.total_draft, generator=gconf)).to(dev)
         cost = torch.full((b.batch,), float(args.trim), dtype=torch.float32, device=dev)
 
+    trunc = None
+    if args.top_k is not None or args.top_p is not None:
+        from speculative_decoding_verification_10_gb300 import truncate
+        tk = torch.full((b.batch,), int(args.top_k or 0), dtype=torch.int32, device=dev)
+        tp = torch.full((b.batch,), float(args.top_p if args.top_p is not None else 1.0),
+                        dtype=torch.float32, device=dev)
+        tgt_out, drf_out = torch.empty_like(b.target), torch.empty_like(b.draft)
+        trunc = (truncate, tk, tp, tgt_out, drf_out)
+
     def step():
+        if trunc is not None:
+            fn, tk, tp, to, do = trunc
+            fn(b.target, b.draft, b.num_draft, b.temperature, tk, tp, out_target=to,
+               out_draft=do)
+            v.run(to, do, b.tokens, b.num_draft, b.temperature, 1, out=out)
+            return out
         if conf is not None:
             return v.run_trimmed(b.target, b.draft, b.tokens, b.num_draft, conf, cost,
                                  b.temperature, 1)
@@ -327,6 +346,19 @@ def run_ours(args):
     rows_needed = np.where(t > 0, np.where(A < k, 2 * (A + 1), 2 * k + 1), A + 1)
     rowpass_bytes = int(rows_needed.sum()) * b.vocab * es
     alg_bytes = rowpass_bytes + b.io_bytes()
+
+    trunc_ms = None
+    if trunc is not None:
+        # the truncation pass alone (it reads every window row and writes it once)
+        fn, tk, tp, to, do = trunc
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(20):
+            fn(b.target, b.draft, b.num_draft, b.temperature, tk, tp, out_target=to, out_draft=do)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        trunc_ms = e0.elapsed_time(e1) / 20
 
     n_ev = min(64, args.steps)
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
@@ -406,7 +438,12 @@ def run_ours(args):
                          % (rowpass_bytes / 1e9),
                    "parallelism": f"replicas x{world}",
                    "schedule": args.schedule, "depth": args.depth,
-                   "trim_cost": args.trim},
+                   "trim_cost": args.trim, "top_k": args.top_k, "top_p": args.top_p,
+                   "truncation_bytes_per_step": (2 * full_window_bytes
+                                                 if trunc is not None else 0),
+                   "truncation_ms": trunc_ms,
+                   "truncation_gbs": (2 * full_window_bytes / (trunc_ms * 1e-3) / 1e9
+                                      if trunc_ms else None)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "sv_wave", "kernel_ms": kernel_avg_ms,

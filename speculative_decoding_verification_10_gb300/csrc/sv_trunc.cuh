@@ -54,10 +54,12 @@ __device__ __forceinline__ uint32_t trunc_key(float x) {
 
 // The digit a warp-0 scan picks from 256 bins, lanes holding 8 bins each.
 // mode 0 (top-k): the highest digit d with sum_{digits >= d} cnt >= need;
-// mode 1 (top-p): the lowest digit d with cnt[d] > 0 and mass above d < target.
-// Returns the digit and, in *above, the count or mass of the digits above it.
+// mode 1 (top-p): the lowest digit d with cnt[d] > 0 and scale * (mass above
+// d) < target.  Returns the digit and, in *above, the count or mass of the
+// digits above it.
 __device__ int pick_digit(const unsigned int* cnt, const unsigned long long* mass, int mode,
-                          unsigned long long need, double target, unsigned long long* above) {
+                          unsigned long long need, double target, double scale,
+                          unsigned long long* above) {
   const int lane = threadIdx.x & 31;
   unsigned long long loc[8];
   unsigned long long sum = 0;
@@ -85,7 +87,7 @@ __device__ int pick_digit(const unsigned int* cnt, const unsigned long long* mas
         best = d;
         best_above = run;
       }
-    } else if (cnt[d] > 0u && (double)run < target) {
+    } else if (cnt[d] > 0u && (double)run * scale < target) {
       best = d;  // keeps the lowest such digit of this lane
       best_above = run;
     }
@@ -103,14 +105,27 @@ __device__ int pick_digit(const unsigned int* cnt, const unsigned long long* mas
   return min(max(pick, 0), 255);  // always found for a consistent histogram
 }
 
+// Counts one element per lane into this warp's own histogram (lanes with
+// !valid add nothing): no other warp shares the histogram, so atomics only
+// meet those of the same warp.
+__device__ __forceinline__ void count_add(unsigned int* whist, bool valid, int d) {
+  if (valid) atomicAdd(&whist[d], 1u);
+}
+
+constexpr int kWin = 8;  // octave bins the first top-p level resolves below the maximum
+
 template <typename E, bool kAligned>
-__global__ void __launch_bounds__(kTruncThreads) sv_truncate(TruncParams P) {
+__global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
+  constexpr int kWarps = kTruncThreads / 32;
+  __shared__ unsigned int s_whist[kWarps][256];  // per-warp counts
   __shared__ unsigned int s_cnt[256];
   __shared__ unsigned long long s_mass[256];
-  __shared__ float s_red[kTruncThreads / 32];
+  __shared__ float s_wsum[kWarps][2 * kWin + 2];
+  __shared__ float s_red[kWarps];
   __shared__ unsigned int s_nan;
   __shared__ int s_digit;
   __shared__ unsigned long long s_above;
+  __shared__ double s_dval[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kLevels = E::kBytes;  // 8-bit digits of the key
   const int V = P.vocab;
@@ -148,41 +163,66 @@ __global__ void __launch_bounds__(kTruncThreads) sv_truncate(TruncParams P) {
     bool copy = bad || !(T > 0.f) || (!use_k && !use_p);
     if (bad && tid == 0 && P.status) atomicOr(reinterpret_cast<unsigned int*>(P.status), kStBadTrunc);
 
-    // visit every element of the row: f(x) (vector loads on aligned rows)
+    // visit every element of the row: f(ok, x), warp-uniform (every lane of a
+    // warp runs the same iterations; ok is false past the row's end); vector
+    // loads on aligned rows
     auto each = [&](auto&& f) {
       if (kAligned) {
         const uint4* rv = reinterpret_cast<const uint4*>(in);
-        for (int i = tid; i < nvec; i += kTruncThreads) {
+        for (int i0 = warp * 32; i0 < nvec; i0 += kTruncThreads) {
+          const int i = i0 + lane;
+          const bool ok = i < nvec;
           float x[E::kVec];
-          E::unpack(ld_stream(rv + i), x);
+          E::unpack(ok ? ld_stream(rv + i) : E::pad(), x);
 #pragma unroll
-          for (int e = 0; e < E::kVec; ++e) f(x[e]);
+          for (int e = 0; e < E::kVec; ++e) f(ok, x[e]);
         }
       } else {
-        for (int v = tid; v < V; v += kTruncThreads) f(E::load1(in, v));
+        for (int v0 = warp * 32; v0 < V; v0 += kTruncThreads) {
+          const int v = v0 + lane;
+          const bool ok = v < V;
+          f(ok, ok ? E::load1(in, v) : kNegInf);
+        }
       }
+    };
+    // the per-warp counts, zeroed before / summed into s_cnt after a pass
+    auto clear_counts = [&]() {
+      for (int i = lane; i < 256; i += 32) s_whist[warp][i] = 0u;
+      if (tid < 256) {
+        s_cnt[tid] = 0u;
+        s_mass[tid] = 0ull;
+      }
+      __syncthreads();
+    };
+    auto sum_counts = [&]() {
+      __syncthreads();
+      if (tid < 256) {
+        unsigned int c = 0u;
+        for (int w = 0; w < kWarps; ++w) c += s_whist[w][tid];
+        s_cnt[tid] += c;
+      }
+      __syncthreads();
     };
 
     uint32_t tau = 0u;  // keep keys >= tau
     if (!copy) {
       // ---- pass 0: maximum, NaN, the first top-k level ---------------------------
-      if (tid < 256) s_cnt[tid] = 0u;
       if (tid == 0) s_nan = 0u;
-      __syncthreads();
+      clear_counts();
       float mx = kNegInf;
       bool nan = false;
       const int shift0 = 8 * (kLevels - 1);
-      each([&](float x) {
-        nan |= x != x;
+      each([&](bool ok, float x) {
+        nan |= ok && x != x;
         mx = fmaxf(mx, x);
-        if (use_k) atomicAdd(&s_cnt[trunc_key<E>(x) >> shift0], 1u);
+        if (use_k) count_add(s_whist[warp], ok, (int)(trunc_key<E>(x) >> shift0));
       });
       if (__any_sync(0xffffffffu, nan) && lane == 0) s_nan = 1u;
       mx = warp_max(mx);
       if (lane == 0) s_red[warp] = mx;
-      __syncthreads();
+      sum_counts();
       if (warp == 0) {
-        float m = lane < kTruncThreads / 32 ? s_red[lane] : kNegInf;
+        float m = lane < kWarps ? s_red[lane] : kNegInf;
         m = warp_max(m);
         if (lane == 0) s_red[0] = m;
       }
@@ -197,17 +237,17 @@ __global__ void __launch_bounds__(kTruncThreads) sv_truncate(TruncParams P) {
         for (int L = 0; L < kLevels; ++L) {
           const int shift = 8 * (kLevels - 1 - L);
           if (L > 0) {
-            if (tid < 256) s_cnt[tid] = 0u;
-            __syncthreads();
-            each([&](float x) {
+            clear_counts();
+            each([&](bool ok, float x) {
               const uint32_t k = trunc_key<E>(x);
-              if ((k >> (shift + 8)) == prefix) atomicAdd(&s_cnt[(k >> shift) & 0xffu], 1u);
+              count_add(s_whist[warp], ok && (k >> (shift + 8)) == prefix,
+                        (int)((k >> shift) & 0xffu));
             });
-            __syncthreads();
+            sum_counts();
           }
           if (warp == 0) {
             unsigned long long above;
-            const int d = pick_digit(s_cnt, nullptr, 0, need, 0.0, &above);
+            const int d = pick_digit(s_cnt, nullptr, 0, need, 0.0, 1.0, &above);
             if (lane == 0) {
               s_digit = d;
               s_above = above;
@@ -221,41 +261,118 @@ __global__ void __launch_bounds__(kTruncThreads) sv_truncate(TruncParams P) {
         tau = prefix;
       }
       if (!copy && use_p) {
-        // ---- top-p on the survivors: masses 2^(c (x - mx)) in 2^-40 fixed point --
+        // ---- top-p on the survivors, masses w = 2^(c (x - mx)) ---------------------
         const float c = kLog2e / T;
         const float cm = c * mx;
-        double target = 0.0;
-        unsigned long long above_all = 0ull;
-        uint32_t prefix = 0u;
         const uint32_t tau_k = tau;
-        for (int L = 0; L < kLevels; ++L) {
-          const int shift = 8 * (kLevels - 1 - L);
-          if (tid < 256) {
-            s_cnt[tid] = 0u;
-            s_mass[tid] = 0ull;
+        // first level: per-thread sums over kWin octave bins from the maximum's
+        // digit down, and one sum below them (fixed order: deterministic); the
+        // window slides down while the boundary lies below it
+        const int d_top = (int)(trunc_key<E>(mx) >> shift0);
+        double above_all = 0.0, target = 0.0;
+        int d0 = -1;
+        for (int base = d_top; base >= 0 && d0 < 0; base -= kWin) {
+          float acc[kWin], below = 0.f, nbelow = 0.f, cnt[kWin];
+#pragma unroll
+          for (int j = 0; j < kWin; ++j) acc[j] = cnt[j] = 0.f;
+          each([&](bool ok, float x) {
+            const uint32_t k = trunc_key<E>(x);
+            if (!(ok && k >= tau_k)) return;
+            const float w = fast_ex2(fmaf(x, c, -cm));
+            const int j = base - (int)(k >> shift0);
+            if (j >= kWin) {
+              below += w;
+              nbelow += 1.f;
+            }
+#pragma unroll
+            for (int i = 0; i < kWin; ++i)
+              if (j == i) {
+                acc[i] += w;
+                cnt[i] += 1.f;
+              }
+          });
+          // block sums in a fixed order
+#pragma unroll
+          for (int i = 0; i < kWin; ++i) {
+            acc[i] = group_sum<32>(acc[i]);
+            cnt[i] = group_sum<32>(cnt[i]);
+          }
+          below = group_sum<32>(below);
+          nbelow = group_sum<32>(nbelow);
+          if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < kWin; ++i) {
+              s_wsum[warp][i] = acc[i];
+              s_wsum[warp][kWin + i] = cnt[i];
+            }
+            s_wsum[warp][2 * kWin] = below;
+            s_wsum[warp][2 * kWin + 1] = nbelow;
           }
           __syncthreads();
-          each([&](float x) {
-            const uint32_t k = trunc_key<E>(x);
-            if (k >= tau_k && (L == 0 || (k >> (shift + 8)) == prefix)) {
-              const float w = fast_ex2(fmaf(x, c, -cm));
-              const unsigned long long q = __float2ull_rn(w * 0x1p40f);
-              const int d = (k >> shift) & 0xff;
-              atomicAdd(&s_cnt[d], 1u);
-              if (q) atomicAdd(&s_mass[d], q);
+          if (tid == 0) {
+            double a[kWin], n[kWin], bl = 0.0, bn = 0.0;
+            for (int i = 0; i < kWin; ++i) a[i] = n[i] = 0.0;
+            for (int w = 0; w < kWarps; ++w) {
+              for (int i = 0; i < kWin; ++i) {
+                a[i] += s_wsum[w][i];
+                n[i] += s_wsum[w][kWin + i];
+              }
+              bl += s_wsum[w][2 * kWin];
+              bn += s_wsum[w][2 * kWin + 1];
             }
-          });
+            if (base == d_top) {
+              double total = bl;
+              for (int i = 0; i < kWin; ++i) total += a[i];
+              target = (double)Pp * total;
+            }
+            // the lowest digit of the window with elements and mass above < target
+            int pick = -1;
+            double above = above_all, pick_above = 0.0;
+            for (int i = 0; i < kWin && base - i >= 0; ++i) {
+              if (n[i] > 0.0) {
+                if (above < target) {
+                  pick = base - i;
+                  pick_above = above;
+                } else {
+                  break;
+                }
+              }
+              above += a[i];
+            }
+            // the boundary is below the window only if the mass of the window and
+            // of everything above it is still below the target and elements
+            // remain below it
+            const bool lower = above < target && bn > 0.0 && base - kWin >= 0;
+            s_digit = lower ? -1 : pick;
+            s_dval[0] = lower ? above : pick_above;
+            s_dval[1] = target;
+          }
           __syncthreads();
-          if (warp == 0) {
-            if (L == 0) {
-              unsigned long long tot = 0ull;
-              for (int d = lane; d < 256; d += 32) tot += s_mass[d];
-#pragma unroll
-              for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-              target = (double)Pp * (double)tot;
+          d0 = s_digit;
+          above_all = s_dval[0];
+          target = s_dval[1];
+          __syncthreads();
+        }
+        // further levels inside the chosen bin: fixed-point masses (2^-40) with
+        // shared atomics, only for the elements of that bin
+        uint32_t prefix = (uint32_t)max(d0, 0);
+        for (int L = 1; L < kLevels; ++L) {
+          const int shift = 8 * (kLevels - 1 - L);
+          clear_counts();
+          each([&](bool ok, float x) {
+            const uint32_t k = trunc_key<E>(x);
+            const bool in = ok && k >= tau_k && (k >> (shift + 8)) == prefix;
+            if (in) {
+              const float w = fast_ex2(fmaf(x, c, -cm));
+              const int d = (int)((k >> shift) & 0xffu);
+              atomicAdd(&s_mass[d], __float2ull_rn(w * 0x1p40f));
             }
+            count_add(s_whist[warp], in, (int)((k >> shift) & 0xffu));
+          });
+          sum_counts();
+          if (warp == 0) {
             unsigned long long above;
-            const int d = pick_digit(s_cnt, s_mass, 1, 0ull, target - (double)above_all, &above);
+            const int d = pick_digit(s_cnt, s_mass, 1, 0ull, target - above_all, 0x1p-40, &above);
             if (lane == 0) {
               s_digit = d;
               s_above = above;
@@ -263,7 +380,7 @@ __global__ void __launch_bounds__(kTruncThreads) sv_truncate(TruncParams P) {
           }
           __syncthreads();
           prefix = (prefix << 8) | (uint32_t)s_digit;
-          above_all += s_above;
+          above_all += (double)s_above * 0x1p-40;
           __syncthreads();
         }
         tau = max(tau, prefix);
