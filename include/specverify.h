@@ -223,7 +223,7 @@ int specverify_run_host(specverify_t h, const void *target_logits, const void *d
  * exists for callers that must not allocate device memory (graph capture of a
  * fixed pool, allocator-free serving loops).
  *
- * Scratch is one file-scope static device array of about 0.55 MiB, sized for
+ * Scratch is one file-scope static device array of about 0.62 MiB, sized for
  * batch <= SPECVERIFY_STATIC_MAX_BATCH (256) and max_k <=
  * SPECVERIFY_STATIC_MAX_K (7) on a grid of at most 1024 CTAs.  On its first use
  * on a device the call takes the array's address (cudaGetSymbolAddress,

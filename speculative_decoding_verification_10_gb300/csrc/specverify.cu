@@ -47,7 +47,7 @@ struct DeviceGuard {
 // with `stream`, also the bands and ready tags of the stream schedule.
 // ---------------------------------------------------------------------------
 struct ScratchLayout {
-  size_t lists, lcnt, res, rcnt, pos, rescnt, part, rpart, ctr;
+  size_t lists, lcnt, res, rcnt, pos, rescnt, part, rpart, ctr, recs, rdy;
   size_t bands, ready_n, ready_u, spart, srpart;
   size_t list_entries, band_cap, bytes;
 };
@@ -104,6 +104,10 @@ constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid, bool s
   off = align_up(off + sizeof(sv::Partial) * (grid + mb), 256);
   L.ctr = off;
   off = align_up(off + sizeof(int) * sv::kCntCount, 256);
+  L.recs = off;
+  off = align_up(off + sizeof(sv::PosRec) * ((size_t)max_k + 1) * mb, 256);
+  L.rdy = off;
+  off = align_up(off + sizeof(unsigned long long) * max_waves * mb, 256);
   L.list_entries = list_entries;
   L.band_cap = stream ? stream_band_cap(mb, max_k) : 0;
   L.bands = off;
@@ -132,6 +136,8 @@ struct Scratch {
   sv::Partial* part;
   sv::Partial* rpart;
   int* ctr;
+  sv::PosRec* recs;
+  unsigned long long* rdy;  // epoch-tagged: must start at zero
   sv::Band* bands;     // epoch-tagged: must start at zero (stream schedule only)
   uint32_t* ready_n;   // epoch tags: must start at zero (stream schedule only)
   uint32_t* ready_u;
@@ -151,6 +157,8 @@ Scratch scratch_at(char* b, const ScratchLayout& L) {
   s.part = reinterpret_cast<sv::Partial*>(b + L.part);
   s.rpart = reinterpret_cast<sv::Partial*>(b + L.rpart);
   s.ctr = reinterpret_cast<int*>(b + L.ctr);
+  s.recs = reinterpret_cast<sv::PosRec*>(b + L.recs);
+  s.rdy = reinterpret_cast<unsigned long long*>(b + L.rdy);
   s.band_cap = (int)L.band_cap;
   s.bands = L.band_cap ? reinterpret_cast<sv::Band*>(b + L.bands) : nullptr;
   s.ready_n = L.band_cap ? reinterpret_cast<uint32_t*>(b + L.ready_n) : nullptr;
@@ -451,6 +459,8 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
   P.part = c.sc.part;
   P.rpart = c.sc.rpart;
   P.ctr = c.sc.ctr;
+  P.recs = c.sc.recs;
+  P.rdy = c.sc.rdy;
   P.bands = c.sc.bands;
   P.ready_n = c.sc.ready_n;
   P.ready_u = c.sc.ready_u;

@@ -98,6 +98,16 @@ struct __align__(16) Partial {
   uint32_t bad;  // softmax: 1 when the segment holds y | best: NaN seen
 };
 
+// The merged rows of one position (a wave of several positions per request):
+// target row (a = m or best value, b = S, xy = x[y], idx = best index) and
+// draft row, with their NaN / non-finite flags (bit 0 target, bit 1 draft).
+struct __align__(16) PosRec {
+  float ta, tb, txy;
+  int tidx;
+  float da, db, dxy;
+  uint32_t bad;
+};
+
 // A rejected request waiting for its correction draw (written by the deciding
 // CTA of wave w, read by wave w+1).
 struct __align__(16) ResEntry {
@@ -181,6 +191,8 @@ struct Params {
   Partial* part;                // [grid + list_cap] row segment partials
   Partial* rpart;               // [grid + stride] residual segment partials
   int* ctr;                     // [kCntCount]
+  PosRec* recs;                 // [(max_k + 1) * stride] merged rows of multi-position waves
+  unsigned long long* rdy;      // [n_waves * stride] epoch | positions of a request merged
   Band* bands;                  // [band_cap] stream schedule
   Partial* spart;               // stream: [list entries * seg_max] row segment partials
   Partial* srpart;              // stream: [stride * seg_max_res] residual segment partials
@@ -977,9 +989,49 @@ __device__ void merge_position(const Params& P, const Partial* parts, const Spli
 // "accepted" signal towards that position (whoever completes its count
 // decides it), past the wave by appending the request to the next wave.
 // ---------------------------------------------------------------------------
+// The records of a request's positions in this wave, lane j holding position
+// pos0 + j (one round trip for the whole chain), and the draft token there.
+struct WaveRecs {
+  int4 a, b;
+  int y;
+};
+__device__ __forceinline__ WaveRecs load_wave_recs(const Params& P, const ReqInfo& q) {
+  const int lane = threadIdx.x & 31;
+  const int i = P.pos0 + lane;
+  WaveRecs w;
+  w.a = w.b = make_int4(0, 0, 0, 0);
+  w.y = -1;
+  if (i < P.pos1 && i <= q.k) {
+    const int4* src = reinterpret_cast<const int4*>(P.recs + (size_t)i * P.stride + q.r);
+    w.a = __ldcg(src);
+    w.b = __ldcg(src + 1);
+    if (i < q.k) w.y = P.tokens[q.d0 + i];
+  }
+  return w;
+}
+// position pos0 + j of the loaded records (all lanes call it)
+__device__ __forceinline__ void rec_of(const WaveRecs& w, int j, RowRes& t, RowRes& d, int& y) {
+  int4 a, b;
+  a.x = __shfl_sync(0xffffffffu, w.a.x, j);
+  a.y = __shfl_sync(0xffffffffu, w.a.y, j);
+  a.z = __shfl_sync(0xffffffffu, w.a.z, j);
+  a.w = __shfl_sync(0xffffffffu, w.a.w, j);
+  b.x = __shfl_sync(0xffffffffu, w.b.x, j);
+  b.y = __shfl_sync(0xffffffffu, w.b.y, j);
+  b.z = __shfl_sync(0xffffffffu, w.b.z, j);
+  b.w = __shfl_sync(0xffffffffu, w.b.w, j);
+  y = __shfl_sync(0xffffffffu, w.y, j);
+  t = RowRes{__int_as_float(a.x), __int_as_float(a.y), __int_as_float(a.z), a.w, (b.w & 1) != 0};
+  d = RowRes{__int_as_float(b.x), __int_as_float(b.y), __int_as_float(b.z), -1, (b.w & 2) != 0};
+}
+
+// Decides position i of request q from its merged rows and, while positions
+// are accepted inside the wave, the ones after it from their records (every
+// position of the request in this wave has been merged when this runs).
 template <typename E>
 __device__ void decide_chain(const Params& P, const Split& sp, const ReqInfo& q, int i, RowRes t,
-                             RowRes d, int y) {
+                             RowRes d, int y, const WaveRecs* recs = nullptr) {
+  (void)sp;
   const int lane = threadIdx.x & 31;
   const size_t row_bytes = (size_t)P.vocab * E::kBytes;
   const bool sampling = q.c > 0.f;
@@ -1057,18 +1109,8 @@ __device__ void decide_chain(const Params& P, const Split& sp, const ReqInfo& q,
       append_next_wave(P, q, next);
       return;
     }
-    const int et = q.base + (sampling ? 2 * (next - P.pos0) : next - P.pos0);
-    const bool paired = sampling && next < q.k;
-    const int tkind = sampling ? (paired ? kSoftmax : kRace) : kArgmax;
-    const int target = sp.segments(et, P.nb) + (paired ? sp.segments(et + 1, P.nb) : 0) + 1;
-    int last = 0;
-    if (lane == 0)
-      last = epoch_add(P.pos_cnt + (size_t)next * P.stride + q.r, P.epoch) == (uint32_t)target;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;  // the last segment of position `next` decides it
-    __threadfence();
-    y = (!sampling && next < q.k) ? P.tokens[q.d0 + next] : -1;
-    merge_position(P, P.part, sp, et, paired, tkind, t, d);
+    rec_of(*recs, next - P.pos0, t, d, y);  // several positions: all merged and loaded
+    if (sampling) y = -1;
     i = next;
   }
 }
@@ -1090,8 +1132,7 @@ __device__ void complete_row(const Params& P, const Split& sp, const QItem& it, 
   const int i = it.pos;
   const int et = (it.paired && it.is_draft) ? it.e - 1 : it.e;
   const int tkind = it.paired ? kSoftmax : it.kind;
-  const int target = sp.segments(et, P.nb) + (it.paired ? sp.segments(et + 1, P.nb) : 0) +
-                     (i > P.pos0 ? 1 : 0);
+  const int target = sp.segments(et, P.nb) + (it.paired ? sp.segments(et + 1, P.nb) : 0);
   RowRes t, d{0.f, 0.f, 0.f, -1, false};
   if (target == 1) {
     t = single_res(p, tkind);
@@ -1108,7 +1149,33 @@ __device__ void complete_row(const Params& P, const Split& sp, const QItem& it, 
     merge_position(P, P.part, sp, et, it.paired != 0, tkind, t, d);
   }
   const ReqInfo q{it.r, it.d0, it.k, it.base, it.c, RequestKey{it.req_lo, it.req_hi}};
-  decide_chain<E>(P, sp, q, i, t, d, it.y);
+  // positions of this request in this wave: each is merged where its last
+  // segment lands, in parallel; the last one merged decides them left to right
+  const int n_pos = min(P.pos1, it.k + 1) - P.pos0;
+  if (n_pos <= 1) {
+    decide_chain<E>(P, sp, q, i, t, d, it.y);
+    return;
+  }
+  int last = 0;
+  if (lane == 0) {
+    const int4 a = make_int4(__float_as_int(t.a), __float_as_int(t.b), __float_as_int(t.xy), t.idx);
+    const int4 b = make_int4(__float_as_int(d.a), __float_as_int(d.b), __float_as_int(d.xy),
+                             (t.bad ? 1 : 0) | (d.bad ? 2 : 0));
+    int4* dst = reinterpret_cast<int4*>(P.recs + (size_t)i * P.stride + it.r);
+    dst[0] = a;
+    dst[1] = b;
+    __threadfence();
+    last = epoch_add(P.rdy + (size_t)P.wave * P.stride + it.r, P.epoch) == (uint32_t)n_pos;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  const WaveRecs recs = load_wave_recs(P, q);
+  RowRes t0, d0;
+  int y0;
+  rec_of(recs, 0, t0, d0, y0);
+  if (it.c != 0.f) y0 = -1;
+  decide_chain<E>(P, sp, q, P.pos0, t0, d0, y0, &recs);
 }
 
 // Completion of a residual segment: the CTA completing the count merges the
