@@ -267,9 +267,9 @@ int specverify_set_timing_events(specverify_t h, int n, void *const *start_event
  * the rows of positions 0..A only when it decides one position per wave
  * (depth 1, the least traffic); a larger depth reads up to depth - 1 rows past
  * a rejection but needs fewer launches, which is faster for small batches.
- * depth in [1, max_k + 1] fixes it; 0 (the default) chooses per run: max_k + 1
- * when every row of the batch's verify window together takes at most 192 MiB,
- * else 1.  Results do not depend on the depth.
+ * depth in [1, max_k + 1] fixes it; 0 (the default) chooses per run from the
+ * bytes of every row of the batch's verify window: max_k + 1 up to 192 MiB,
+ * 2 up to 1 GiB, else 1.  Results do not depend on the depth.
  */
 int specverify_set_depth(specverify_t h, int depth);
 

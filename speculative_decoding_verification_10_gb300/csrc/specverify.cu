@@ -259,15 +259,19 @@ struct RunConfig {
 constexpr size_t kStreamScratchCap = (size_t)512 << 20;
 
 // Batches whose whole verify window (every row of every position) is at most
-// this many bytes are verified in one wave of all positions: reading rows past
-// a rejection costs less than a launch per position there.
+// kShallowBytes are verified in one wave of all positions: reading rows past a
+// rejection costs less than a launch per position there.  Up to kPairBytes,
+// two positions per wave; above, one (measured on GB300: a 613 MB window
+// verifies fastest at depth 2, a 2.4 GB one at depth 1).
 constexpr double kShallowBytes = 192.0 * (1 << 20);
+constexpr double kPairBytes = 1024.0 * (1 << 20);
 
 // Positions per wave for a run of `batch` requests.
 int run_depth(const RunConfig& c, int batch) {
   if (c.depth_setting > 0) return c.depth_setting;
   const double window = (double)batch * (2.0 * c.max_k + 1.0) * c.vocab * c.elem_bytes;
-  return window <= kShallowBytes ? c.max_k + 1 : 1;
+  if (window <= kShallowBytes) return c.max_k + 1;
+  return window <= kPairBytes ? std::min(2, c.max_k + 1) : 1;
 }
 
 // Cluster launch or waves: waves unless clusters are asked for (and the rows
