@@ -10,9 +10,14 @@ largest synthetic batch: 512 requests, k = 4, V = 262144, bf16 logits (2.4 GB
 per step, far larger than the 129 MB L2, so no flush between steps).
 
 The line also carries:
-  roofline     achieved GB/s of the row-pass kernel = its algorithmic bytes (every
-               needed logit row once) / its CUDA-event time, against the measured
-               HBM copy bandwidth;
+  roofline     achieved GB/s of the round = its algorithmic bytes B_alg / its
+               CUDA-event time, against the measured HBM copy bandwidth.  B_alg is
+               every logit row of the verified windows read once (2k+1 rows per
+               sampling request, k+1 per greedy one) plus the small inputs and the
+               outputs; re-reads for the correction draw are not counted.  Rows past
+               a request's first rejection are never read, so the line also gives
+               the bytes the round needed (positions 0..A) and, from the committed
+               ncu capture, the DRAM bytes it actually moved;
   e2e          the same metric through specverify_run_host: pinned host inputs
                copied in, outputs copied out, every step;
   cpu_baseline the CPU oracle on a bounded sample of the same batch (1 core);
@@ -361,8 +366,11 @@ def run_ours(args):
         k = res.verified_k.cpu().numpy().astype(np.int64)
         rows_per_step = int((k + 1).sum())
     rows_needed = np.where(t > 0, np.where(A < k, 2 * (A + 1), 2 * k + 1), A + 1)
-    rowpass_bytes = int(rows_needed.sum()) * b.vocab * es
-    alg_bytes = rowpass_bytes + b.io_bytes()
+    needed_bytes = int(rows_needed.sum()) * b.vocab * es
+    # B_alg: every row of the verified windows once, plus inputs and outputs
+    window_rows = np.where(t > 0, 2 * k + 1, k + 1)
+    window_bytes = int(window_rows.sum()) * b.vocab * es
+    alg_bytes = window_bytes + b.io_bytes()
 
     trunc_ms = None
     if trunc is not None:
@@ -433,8 +441,9 @@ def run_ours(args):
 
     kernel_avg_ms = float(np.mean(kernel_ms))
     peak, peak_kind = measured_peak()
-    achieved = rowpass_bytes / (kernel_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    achieved = alg_bytes / (kernel_avg_ms * 1e-3) / 1e9
+    needed_gbs = needed_bytes / (kernel_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload) if conf is None and trunc is None else None
     line = {
         "metric": METRIC, "value": job_rows_per_sec(rows_per_step, world, ms_max), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
@@ -444,12 +453,11 @@ def run_ours(args):
                    "vocab": b.vocab, "logits": b.dtype, "rows_per_step": rows_per_step,
                    "alg_bytes_per_step": alg_bytes,
                    "step_gbs": alg_bytes / (ms_max * 1e-3) / 1e9,
-                   "rows_read_per_step": int(rows_needed.sum()),
-                   "full_window_rows": int(np.where(t > 0, 2 * k + 1, k + 1).sum()),
-                   "full_window_gbs": full_window_bytes / (ms_max * 1e-3) / 1e9,
+                   "rows_needed_per_step": int(rows_needed.sum()),
+                   "window_rows_per_step": int(window_rows.sum()),
                    "mean_accepted": float(A.mean()),
                    "l2": "no flush: each step reads %.2f GB of logits, larger than the 129 MB L2"
-                         % (rowpass_bytes / 1e9),
+                         % (needed_bytes / 1e9),
                    "parallelism": f"replicas x{world}",
                    "schedule": args.schedule, "depth": args.depth,
                    "trim_cost": args.trim, "top_k": args.top_k, "top_p": args.top_p,
@@ -461,8 +469,12 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "sv_wave", "kernel_ms": kernel_avg_ms,
-                     "window": "one round: sv_plan + sv_wave x (max_k + 1), back to back",
-                     "alg_bytes_per_launch": rowpass_bytes,
+                     "window": "one round: sv_plan + its sv_wave launches, back to back",
+                     "alg_bytes_per_launch": alg_bytes,
+                     "needed_bytes_per_launch": needed_bytes,
+                     "needed_gbs": needed_gbs, "needed_frac": needed_gbs / peak,
+                     "dram_gbs": (traffic / (kernel_avg_ms * 1e-3) / 1e9
+                                  if traffic is not None else None),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback"},
         "cpu_baseline": cpu,

@@ -389,6 +389,84 @@ __device__ __forceinline__ void group_bonus(BestAcc& acc, const float (&x)[E::kV
   if (s > 0.f) acc.take_cmp(m + fast_lg2(s) + gain, e_lane / kRaceBlock);
 }
 
+// Bonus-race gains of a warp's blocks for one window of kGroups vector groups
+// (8 stages in bf16, 16 in fp32): lane L holds the gain of block slot L, which
+// is block L % kBlocksPerGroup of group g0 + L / kBlocksPerGroup.
+template <typename E>
+struct WindowGains {
+  static constexpr int kBPG = GroupGains<E>::kBlocksPerGroup;
+  static constexpr int kGroups = 32 / kBPG;
+  float g;
+  __device__ __forceinline__ void make(int vbeg, int g0, int w, uint32_t pos, RequestKey rk,
+                                       PhiloxKey key) {
+    const int lane = threadIdx.x & 31;
+    const int b = GroupGains<E>::group_elem(vbeg, g0 + lane / kBPG, w) / kRaceBlock + lane % kBPG;
+    g = race_gain(race_word(2u, b, pos, rk, key));
+  }
+  __device__ __forceinline__ float get(int slot) const {
+    return __shfl_sync(0xffffffffu, g, slot);
+  }
+};
+
+// Bonus race over one stage: the warp's two vector groups x0 (group g) and x1
+// (group g + 1), kBPG blocks each.  Block weights are summed against a
+// warp-uniform reference R, the largest c*x the warp has seen (log2 domain):
+//   log2 W_b = R + log2 sum_v 2^(c x_v - R),
+// which needs no per-block maximum.  R is raised (and the sums redone) when it
+// is still -inf or a lane's sum passes 2^64, i.e. an element stands more than
+// about 60 above R.  Terms that underflow (c x_v < R - 126) are dropped; a
+// block made only of such terms scores below R - 95 even with the largest
+// gain, while the block holding R's element scores at least R - 4.1, so it
+// cannot win.  The reduction is transposed: one exchange leaves slot-0 sums in
+// the lanes whose bit kL/2 is clear and slot-1 sums in the others, so both
+// groups' blocks are reduced by the same log2(kL) shuffles.
+template <typename E>
+__device__ __forceinline__ void stage_bonus(BestAcc& acc, float& R, const float (&x0)[E::kVec],
+                                            const float (&x1)[E::kVec], int vbeg, int g, int w,
+                                            int g0, float c, const WindowGains<E>& wg) {
+  constexpr int kL = GroupGains<E>::kLanesPerBlock;
+  const int lane = threadIdx.x & 31;
+  float s0 = 0.f, s1 = 0.f;
+  auto sums = [&]() {
+    const float2 cc = make_float2(c, c), nr = make_float2(-R, -R);
+    float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E::kVec; e += 2) {
+      const float2 t = __ffma2_rn(make_float2(x0[e], x0[e + 1]), cc, nr);
+      a = __fadd2_rn(a, make_float2(fast_ex2(t.x), fast_ex2(t.y)));
+      const float2 u = __ffma2_rn(make_float2(x1[e], x1[e + 1]), cc, nr);
+      b = __fadd2_rn(b, make_float2(fast_ex2(u.x), fast_ex2(u.y)));
+    }
+    s0 = a.x + a.y;
+    s1 = b.x + b.y;
+  };
+  if (R > kNegInf) sums();
+  if (__any_sync(0xffffffffu, !(R > kNegInf) || s0 > 0x1p64f || s1 > 0x1p64f)) {
+    float mx = x0[0];
+#pragma unroll
+    for (int e = 1; e < E::kVec; ++e) mx = fmaxf(mx, x0[e]);
+#pragma unroll
+    for (int e = 0; e < E::kVec; ++e) mx = fmaxf(mx, x1[e]);
+    R = fmaxf(R, warp_max(mx) * c);
+    if (R > kNegInf) {
+      sums();
+    } else {
+      s0 = s1 = 0.f;
+    }
+  }
+  const bool hi = (lane & (kL / 2)) != 0;
+  float v = (hi ? s1 : s0) + __shfl_xor_sync(0xffffffffu, hi ? s0 : s1, kL / 2);
+#pragma unroll
+  for (int off = kL / 4; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  const int grp = g + (hi ? 1 : 0);
+  const int sub = lane / kL;
+  const float gain = wg.get((grp - g0) * WindowGains<E>::kBPG + sub);
+  acc.nan |= (v != v);
+  if (v > 0.f)
+    acc.take_cmp(R + fast_lg2(v) + gain,
+                 GroupGains<E>::group_elem(vbeg, grp, w) / kRaceBlock + sub);
+}
+
 // Residual race over one vector group: W_b = sum max(p_v - q_v, 0).
 struct ResidualRow {
   float c, mp, inv_sp, mq, inv_sq;
@@ -603,7 +681,10 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       vec(x, (vi + kThreads) * E::kVec);
     }
   } else if (kind == kRace) {
-    GroupGains<E> gg;
+    static_assert(kStageVecs == 2, "a stage holds two vector groups");
+    WindowGains<E> wg;
+    float R = kNegInf;
+    int g0 = 0;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
       take(v[0], v[1]);
@@ -613,12 +694,14 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
         if (vi + kThreads >= vend) v[1] = E::pad();
       }
       const int g = st * kStageVecs;
-      if ((g & 31) == 0) gg.make(vbeg, g, w, (uint32_t)pos, rk, P.key);
-      float x[E::kVec];
-      E::unpack(v[0], x);
-      group_bonus<E>(acc, x, vi * E::kVec, c, gg.get(g));
-      E::unpack(v[1], x);
-      group_bonus<E>(acc, x, (vi + kThreads) * E::kVec, c, gg.get(g + 1));
+      if (g % WindowGains<E>::kGroups == 0) {
+        g0 = g;
+        wg.make(vbeg, g0, w, (uint32_t)pos, rk, P.key);
+      }
+      float x0[E::kVec], x1[E::kVec];
+      E::unpack(v[0], x0);
+      E::unpack(v[1], x1);
+      stage_bonus<E>(acc, R, x0, x1, vbeg, g, w, g0, c, wg);
     }
   } else {
     const ResidualRow rr{c, itm.mp, itm.inv_sp, itm.mq, itm.inv_sq};
