@@ -171,15 +171,19 @@ Scratch scratch_at(char* b, const ScratchLayout& L) {
 size_t ring_bytes() { return sizeof(uint4) * sv::kStages * sv::kStageVecs * sv::kThreads; }
 
 template <typename E>
-const void* wave_kernel(bool aligned) {
-  return aligned ? reinterpret_cast<const void*>(sv::sv_wave<E, true>)
-                 : reinterpret_cast<const void*>(sv::sv_wave<E, false>);
+const void* wave_kernel(bool aligned, bool three) {
+  if (three)
+    return aligned ? reinterpret_cast<const void*>(sv::sv_wave<E, true, 3>)
+                   : reinterpret_cast<const void*>(sv::sv_wave<E, false, 3>);
+  return aligned ? reinterpret_cast<const void*>(sv::sv_wave<E, true, 2>)
+                 : reinterpret_cast<const void*>(sv::sv_wave<E, false, 2>);
 }
 
 // Grids on the current device, every CTA resident at once: the wave kernels
 // (aligned and scalar rows) and the cluster kernel (clusters of cluster_n).
 struct KernelShape {
-  int grid_aligned, grid_scalar;
+  int grid_aligned, grid_scalar;    // the wave kernel built for two CTAs per SM
+  int grid3_aligned, grid3_scalar;  // ... and for three
   int grid_cluster, cluster_n;
   int grid_stream;
 };
@@ -190,22 +194,24 @@ bool kernel_shape(int device, int dtype, KernelShape* out) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return false;
-  int occ[2] = {0, 0};
-  for (int a = 0; a < 2; ++a) {
-    const void* fn = dtype == SPECVERIFY_BF16 ? wave_kernel<sv::BF16>(a == 1)
-                                              : wave_kernel<sv::F32>(a == 1);
-    const size_t sm = a == 1 ? ring_bytes() : 0;
+  int occ[4] = {0, 0, 0, 0};  // [three][aligned]
+  for (int v = 0; v < 4; ++v) {
+    const bool aligned = (v & 1) != 0, three = (v & 2) != 0;
+    const void* fn = dtype == SPECVERIFY_BF16 ? wave_kernel<sv::BF16>(aligned, three)
+                                              : wave_kernel<sv::F32>(aligned, three);
+    const size_t sm = aligned ? ring_bytes() : 0;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[a], fn, sv::kBlock, sm) !=
-            cudaSuccess)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[v], fn, sv::kBlock, sm) !=
+            cudaSuccess || occ[v] < 1)
       return false;
   }
-  if (occ[0] < 1 || occ[1] < 1) return false;
   out->grid_scalar = occ[0] * sms;
   out->grid_aligned = occ[1] * sms;
+  out->grid3_scalar = occ[2] * sms;
+  out->grid3_aligned = occ[3] * sms;
   // the cluster kernel: as many clusters as fit at once
   const void* fc = dtype == SPECVERIFY_BF16 ? reinterpret_cast<const void*>(sv::sv_cluster<sv::BF16>)
                                             : reinterpret_cast<const void*>(sv::sv_cluster<sv::F32>);
@@ -272,6 +278,16 @@ int run_depth(const RunConfig& c, int batch) {
   const double window = (double)batch * (2.0 * c.max_k + 1.0) * c.vocab * c.elem_bytes;
   if (window <= kShallowBytes) return c.max_k + 1;
   return window <= kPairBytes ? std::min(2, c.max_k + 1) : 1;
+}
+
+// The wave kernel built for three CTAs per SM (up to 80 registers a thread)
+// or for two (up to 128).  Measured on GB300: windows up to kShallowBytes are
+// bound by latency (a few segments per CTA, decisions at the end) and run
+// fastest on the most CTAs; larger windows stream best on two per SM with the
+// larger register budget.
+bool wave_three(const RunConfig& c, int batch) {
+  const double window = (double)batch * (2.0 * c.max_k + 1.0) * c.vocab * c.elem_bytes;
+  return window <= kShallowBytes;
 }
 
 // Cluster launch or waves: waves unless clusters are asked for (and the rows
@@ -363,13 +379,20 @@ int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
     return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
   }
   const size_t smem = aligned ? ring_bytes() : 0;
-  const int grid = aligned ? c.shape.grid_aligned : c.shape.grid_scalar;
+  const bool three = wave_three(c, P.batch);
+  const int grid = three ? (aligned ? c.shape.grid3_aligned : c.shape.grid3_scalar)
+                         : (aligned ? c.shape.grid_aligned : c.shape.grid_scalar);
   for (int w = 0; w < P.n_waves; ++w) {
     P.wave = w;
     P.pos0 = std::min(w * P.depth, c.max_k + 1);
     P.pos1 = std::min((w + 1) * P.depth, c.max_k + 1);
-    const cudaError_t e = aligned ? launch_wave(sv::sv_wave<E, true>, grid, smem, s, P)
-                                  : launch_wave(sv::sv_wave<E, false>, grid, smem, s, P);
+    cudaError_t e;
+    if (three)
+      e = aligned ? launch_wave(sv::sv_wave<E, true, 3>, grid, smem, s, P)
+                  : launch_wave(sv::sv_wave<E, false, 3>, grid, smem, s, P);
+    else
+      e = aligned ? launch_wave(sv::sv_wave<E, true, 2>, grid, smem, s, P)
+                  : launch_wave(sv::sv_wave<E, false, 2>, grid, smem, s, P);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return SPECVERIFY_ERR_CUDA;
@@ -644,7 +667,8 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   const StreamSegs segs{max_segments(nb, (size_t)min_span_blocks(c.elem_bytes)),
                         max_segments(2 * nb, (size_t)min_span_blocks(c.elem_bytes))};
   const size_t grid_all =
-      (size_t)std::max({c.shape.grid_aligned, c.shape.grid_scalar, c.shape.grid_stream});
+      (size_t)std::max({c.shape.grid_aligned, c.shape.grid_scalar, c.shape.grid3_aligned,
+                        c.shape.grid3_scalar, c.shape.grid_stream});
   ScratchLayout L = scratch_layout((size_t)max_batch, max_k, grid_all, true, segs);
   if (L.bytes > kStreamScratchCap) L = scratch_layout((size_t)max_batch, max_k, grid_all, false);
   if (cudaMalloc(&h->scratch, L.bytes) != cudaSuccess) {
@@ -847,6 +871,8 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
     for (int t = 0; t < 2; ++t) {
       sd.shape[t].grid_aligned = std::min<int>(sd.shape[t].grid_aligned, (int)kStaticGrid);
       sd.shape[t].grid_scalar = std::min<int>(sd.shape[t].grid_scalar, (int)kStaticGrid);
+      sd.shape[t].grid3_aligned = std::min<int>(sd.shape[t].grid3_aligned, (int)kStaticGrid);
+      sd.shape[t].grid3_scalar = std::min<int>(sd.shape[t].grid3_scalar, (int)kStaticGrid);
       sd.shape[t].grid_cluster = std::min<int>(sd.shape[t].grid_cluster,
                                                (int)kStaticGrid / kClusterN * kClusterN);
     }

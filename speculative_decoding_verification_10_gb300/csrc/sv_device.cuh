@@ -121,6 +121,17 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Named CTA barriers (hardware, no polling): `arrive` counts the calling warp
+// in and goes on, `sync` counts it in and waits until `n` threads have come.
+// Both order the caller's earlier memory accesses before the barrier's
+// completion for every participating thread.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Publishing a count in shared memory: a release store by the writer, an
 // acquire load by the readers (orders only what these two accesses need, unlike
 // a fence, which would also wait for the reader's copies in flight).

@@ -60,7 +60,12 @@ constexpr int kMinSpanBytes = 16384;           // smallest share of a wave per C
 
 enum RowKind : int { kSoftmax = 0, kArgmax = 1, kRace = 2, kResidual = 3 };
 enum ReqMode : int { kBadTemp = 0, kGreedy = 1, kSampling = 2 };
-enum UnitType : int { kUnitEnd = 0, kUnitItem = 1 };
+// Mailbox slots between the compute warps and the control warp, and the named
+// barriers that hand them over (0 is __syncthreads).
+constexpr int kMailSlots = 4;
+constexpr int kBarReady = 1;          // kBarReady + slot: partials of the slot are in
+constexpr int kBarFree = 1 + kMailSlots;  // kBarFree + slot: the slot may be refilled
+constexpr int kCtaThreads = kThreads + 32;
 
 // Status bits (equal to the SPECVERIFY_STATUS_* values of the header).
 constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite = 8u,
@@ -1670,17 +1675,17 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
 // The wave launch: positions [pos0, pos1) of every request alive at pos0, and
 // the correction draws of the requests the previous wave rejected.
 // ---------------------------------------------------------------------------
-template <typename E, bool kAligned>
-__global__ void __maxnreg__(128) sv_wave(Params P) {
+// kMinBlocks CTAs per SM bound the registers: 2 (up to 128 a thread) for
+// windows that stream long shares, 3 (up to 80) for small, latency-bound ones.
+template <typename E, bool kAligned, int kMinBlocks>
+__global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* ring = reinterpret_cast<uint4*>(smem_raw);
   __shared__ QItem queue[kQueue];
-  __shared__ int s_unit[2];
-  __shared__ Partial mailbox[2][kComputeWarps];
-  __shared__ float s_xy[2];
+  __shared__ Partial mailbox[kMailSlots][kComputeWarps];
+  __shared__ float s_xy[kMailSlots];
   __shared__ int s_qend;
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
   const int warp = tid >> 5;
   const bool control = warp == kComputeWarps;
 
@@ -1704,55 +1709,62 @@ __global__ void __maxnreg__(128) sv_wave(Params P) {
   } else {
     sg.x = sg.x1 = 0ull;
   }
-  int cur = -1;  // control: queue index of the segment being processed
-  if (control) {
-    fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
-    if (lane == 0) s_unit[0] = sg.q_head > 0 ? kUnitItem : kUnitEnd;
-  }
+  if (control) fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
   __syncthreads();
 
-  LoadCursor lc;
-  int gs = 0;
-  if (kAligned && !control) {
-    lc.q = 0;
-    lc.active = false;
-    lc.open(queue, &s_qend);
-    for (int s = 0; s < kStages - 1; ++s) lc.issue(queue, &s_qend, ring, s);
-  }
-
-  for (int u = 0;; ++u) {
-    const int type = s_unit[u & 1];
-    if (!control) {
-      // ---- compute warps: stream segment u ------------------------------------
-      if (type == kUnitItem) {
-        const QItem& it = queue[u & (kQueue - 1)];
-        const Partial out = kAligned
-                                ? seg_aligned<E>(P, queue, &s_qend, ring, lc, gs, it, &s_xy[u & 1])
-                                : seg_scalar<E>(P, it, &s_xy[u & 1]);
-        if (lane == 0) mailbox[u & 1][warp] = out;
-      }
-    } else {
-      // ---- control warp: finish segment u-1, queue ahead, schedule u+1 ---------
-      if (cur >= 0) {
-        const QItem& pv = queue[cur & (kQueue - 1)];
-        if (pv.kind == kResidual) {
-          complete_residual<E>(P, sp[0], pv, mailbox[(u - 1) & 1]);
-        } else {
-          complete_row<E>(P, sp[1], pv, mailbox[(u - 1) & 1], s_xy[(u - 1) & 1]);
-        }
-        sg.q_used = cur + 1;  // its queue entry may now be reused
-      }
-      cur = type == kUnitItem ? u : -1;
-      if (type == kUnitItem) {
-        fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
-        if (lane == 0) s_unit[(u + 1) & 1] = (u + 1 < sg.q_head) ? kUnitItem : kUnitEnd;
-      }
-      __syncwarp();
+  // Segment u travels through mailbox slot u % kMailSlots.  The compute warps
+  // arrive on kBarReady + slot when its partials are in; the control warp
+  // syncs there, completes the segment, refills the queue and then arrives on
+  // kBarFree + slot.  A compute warp syncs on kBarFree + (u % kMailSlots)
+  // before every index u >= kMailSlots, including the index equal to the
+  // final count, where it then stops; so the control warp arrives after
+  // completing u exactly when u + kMailSlots <= the count.  It knows: its
+  // refill leaves the queue either final or at least kQueue - 2 > kMailSlots
+  // entries past u.  For the same reason a compute warp past that barrier
+  // (or, below kMailSlots, past the initial fill) reads a published count
+  // that is final or larger than its index.  The compute warps thus run up to
+  // kMailSlots segments ahead of the control warp's completions (merges,
+  // decisions) and do not wait for them while those are shorter than the
+  // streaming.
+  if (!control) {
+    // ---- compute warps: stream segment after segment ---------------------------
+    LoadCursor lc;
+    int gs = 0;
+    if (kAligned) {
+      lc.q = 0;
+      lc.active = false;
+      lc.open(queue, &s_qend);
+      for (int s = 0; s < kStages - 1; ++s) lc.issue(queue, &s_qend, ring, s);
     }
-    __syncthreads();
-    if (type == kUnitEnd) break;
+    for (int u = 0;; ++u) {
+      const int slot = u % kMailSlots;
+      if (u >= kMailSlots) named_bar_sync(kBarFree + slot, kCtaThreads);
+      const int qe = ld_acquire_shared(&s_qend);
+      if (u >= (qe >= 0 ? qe : -1 - qe)) break;  // only once the count is final
+      const QItem& it = queue[u & (kQueue - 1)];
+      const Partial out = kAligned
+                              ? seg_aligned<E>(P, queue, &s_qend, ring, lc, gs, it, &s_xy[slot])
+                              : seg_scalar<E>(P, it, &s_xy[slot]);
+      if ((tid & 31) == 0) mailbox[slot][warp] = out;
+      named_bar_arrive(kBarReady + slot, kCtaThreads);
+    }
+    if (kAligned) cp_async_wait_all();
+  } else {
+    // ---- control warp: complete segment after segment, keep the queue full ----
+    for (int u = 0; u < sg.q_head; ++u) {
+      const int slot = u % kMailSlots;
+      named_bar_sync(kBarReady + slot, kCtaThreads);
+      const QItem& pv = queue[u & (kQueue - 1)];
+      if (pv.kind == kResidual) {
+        complete_residual<E>(P, sp[0], pv, mailbox[slot]);
+      } else {
+        complete_row<E>(P, sp[1], pv, mailbox[slot], s_xy[slot]);
+      }
+      sg.q_used = u + 1;  // its queue entry may now be reused
+      fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
+      if (u + kMailSlots <= sg.q_head) named_bar_arrive(kBarFree + slot, kCtaThreads);
+    }
   }
-  if (kAligned && !control) cp_async_wait_all();
 }
 
 }  // namespace sv
