@@ -121,6 +121,15 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// GPU-scope release/acquire fence: a writer's fence before its counter RMW and
+// the reader's fence after the RMW that completes the count order the
+// writer's earlier stores before the reader's later loads (the counter's RMWs
+// carry the order from every writer to the last one).  Lighter than the
+// sequentially consistent fence, which these hand-offs do not need.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // Named CTA barriers (hardware, no polling): `arrive` counts the calling warp
 // in and goes on, `sync` counts it in and waits until `n` threads have come.
 // Both order the caller's earlier memory accesses before the barrier's

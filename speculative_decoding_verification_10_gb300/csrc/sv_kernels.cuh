@@ -1228,12 +1228,13 @@ __device__ void complete_row(const Params& P, const Split& sp, const QItem& it, 
     int last = 0;
     if (lane == 0) {
       P.part[it.g] = p;
-      __threadfence();
+      fence_acq_rel_gpu();
       last = epoch_add(P.pos_cnt + (size_t)i * P.stride + it.r, P.epoch) == (uint32_t)target;
+      if (last) fence_acq_rel_gpu();  // acquire: every writer's data is visible here
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
-    __threadfence();
+    __syncwarp();  // ... and, past the warp barrier, to every lane
     merge_position(P, P.part, sp, et, it.paired != 0, tkind, t, d);
   }
   const ReqInfo q{it.r, it.d0, it.k, it.base, it.c, RequestKey{it.req_lo, it.req_hi}};
@@ -1252,12 +1253,13 @@ __device__ void complete_row(const Params& P, const Split& sp, const QItem& it, 
     int4* dst = reinterpret_cast<int4*>(P.recs + (size_t)i * P.stride + it.r);
     dst[0] = a;
     dst[1] = b;
-    __threadfence();
+    fence_acq_rel_gpu();
     last = epoch_add(P.rdy + (size_t)P.wave * P.stride + it.r, P.epoch) == (uint32_t)n_pos;
+    if (last) fence_acq_rel_gpu();  // acquire: every position's record is visible here
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
-  __threadfence();
+  __syncwarp();  // ... and, past the warp barrier, to every lane
   const WaveRecs recs = load_wave_recs(P, q);
   RowRes t0, d0;
   int y0;
@@ -1283,12 +1285,13 @@ __device__ void complete_residual(const Params& P, const Split& sp, const QItem&
     int last = 0;
     if (lane == 0) {
       P.rpart[it.g] = p;
-      __threadfence();
+      fence_acq_rel_gpu();
       last = epoch_add(P.rcnt + it.r, P.epoch) == (uint32_t)n;
+      if (last) fence_acq_rel_gpu();  // acquire: every writer's data is visible here
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
-    __threadfence();
+    __syncwarp();  // ... and, past the warp barrier, to every lane
     RowRes unused;
     merge_position(P, P.rpart, sp, it.e, false, kResidual, best, unused);
   }
@@ -1419,12 +1422,21 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
   }
 }
 
-// Keeps the queue filled (up to kQueue - 2 segments ahead of the one in use),
-// decoding up to 8 segments at a time, one per lane.
+// Keeps the queue filled: once fewer than kRefillAt segments are queued past
+// the completed ones it refills up to kQueue - 2, decoding up to 8 segments at
+// a time, one per lane (one round trip for the list entries of several
+// completions).  kRefillAt covers what the compute warps may touch before the
+// next refill: they stream at most kMailSlots - 1 segments past the completed
+// ones, and their copy cursor reaches at most kStages - 1 segments (each is at
+// least one stage) past the one they stream.
+constexpr int kRefillAt = kMailSlots + kStages - 1;
+static_assert(kRefillAt <= kQueue - 2, "the refill level fits the queue");
+
 template <typename E, bool kAligned>
 __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* s_qend,
                            SegGen& sg) {
   const int lane = threadIdx.x & 31;
+  if (sg.phase < 2 && sg.q_head >= sg.q_used + kRefillAt) return;
   while (sg.phase < 2 && sg.q_head < sg.q_used + kQueue - 2) {
     const int room = min(8, kQueue - 2 - (sg.q_head - sg.q_used));
     // cut the next `room` segments (all lanes alike); lane j keeps the j-th
@@ -1719,7 +1731,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   // before every index u >= kMailSlots, including the index equal to the
   // final count, where it then stops; so the control warp arrives after
   // completing u exactly when u + kMailSlots <= the count.  It knows: its
-  // refill leaves the queue either final or at least kQueue - 2 > kMailSlots
+  // refill leaves the queue either final or at least kRefillAt > kMailSlots
   // entries past u.  For the same reason a compute warp past that barrier
   // (or, below kMailSlots, past the initial fill) reads a published count
   // that is final or larger than its index.  The compute warps thus run up to
