@@ -18,8 +18,9 @@ The line also carries:
                a request's first rejection are never read, so the line also gives
                the bytes the round needed (positions 0..A) and, from the committed
                ncu capture, the DRAM bytes it actually moved;
-  e2e          the same metric through specverify_run_host: pinned host inputs
-               copied in, outputs copied out, every step;
+  e2e          the same metric through specverify_run_host on pinned host inputs,
+               outputs copied back, every step; the kernels read the pinned
+               logits in place (only the rows a round reads cross the link);
   cpu_baseline the CPU oracle on a bounded sample of the same batch (1 core);
   clocks       nvidia-smi samples taken during the timed region.
 --impl reference times the CPU oracle instead (the only other arm there is).
@@ -60,6 +61,8 @@ def parse_args():
                     help="requests in the oracle sample (0 = about 10 s of work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--host-reads", default="auto", choices=["auto", "stage"],
+                    help="e2e: read pinned host logits in place (auto) or copy them in (stage)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "waves", "clusters", "stream"],
                     help="launch layout of a round (results do not depend on it)")
     ap.add_argument("--depth", type=int, default=0,
@@ -284,11 +287,29 @@ def measure_e2e(args, b, v, world, dev):
     if world > 1:
         dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
     e2e_s = float(e2e_t.item())
-    h2d = (h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()
-           + 4 * (h_tokens.numel() + h_nd.numel() + h_temp.numel()))
+    small = 4 * (h_tokens.numel() + h_nd.numel() + h_temp.numel())
+    in_place = v.last_host_reads() == 1
+    if in_place:
+        # the kernels read the rows of every wave a request takes part in, where
+        # they lie, plus the two rows a correction draw reads again
+        depth = v.wave_depth(b.batch)
+        A = h_acc.numpy().astype(np.int64)
+        k = h_nd.numpy().astype(np.int64)
+        sampling = h_temp.numpy() > 0
+        last = np.minimum(k, (A // depth + 1) * depth - 1)
+        rows = np.where(sampling, 2 * np.minimum(last + 1, k) + (last == k),
+                        last + 1)
+        rows = rows + np.where(sampling & (A < k), 2, 0)
+        logits = int(rows.sum()) * b.vocab * h_target.element_size()
+    else:
+        logits = h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()
+    h2d = logits + small
     d2h = 4 * h_acc.numel() + 4 * h_com.numel() + h_flg.numel()
     return {"value": world * b.verified_rows() / e2e_s, "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+            "logits": ("pinned host rows read in place by the kernels (only the rows a round "
+                       "reads cross the link)" if in_place else
+                       "whole window copied host to device each step")}
 
 
 
@@ -321,6 +342,7 @@ def run_ours(args):
     v = Verifier(b.batch, b.max_k, b.vocab, b.dtype, device=local, host_staging=not args.no_e2e)
     v.set_schedule(args.schedule)
     v.set_depth(args.depth)
+    v.set_host_reads(args.host_reads)
     out = v.outputs(b.batch, b.total_draft)
     stream = torch.cuda.current_stream(dev)
 

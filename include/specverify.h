@@ -201,10 +201,16 @@ int specverify_run_trimmed(specverify_t h, const void *target_logits, const void
 
 /*
  * specverify_run_host -- the same verify round on HOST buffers (same shapes as
- * specverify_run; draft_logits may be NULL as there).  Copies the inputs into
- * the handle's device staging (pinned host memory makes the copies
- * asynchronous DMA), runs, copies the three outputs back and waits for
- * `stream`.  Needs a handle made with SPECVERIFY_CREATE_HOST_STAGING.
+ * specverify_run; draft_logits may be NULL as there).  When both logits
+ * buffers lie in pinned host memory that the device maps (cudaHostAlloc, or
+ * cudaHostRegister with mapping, on a unified-address system) and the mode
+ * (specverify_set_host_reads) is AUTO, the kernels read the logits where they
+ * lie: only the rows the round needs cross to the GPU (over NVLink-C2C on
+ * Grace-Blackwell), and the host buffers must stay unchanged until the call
+ * returns.  Otherwise the logits are copied into the handle's device staging
+ * first (asynchronous DMA from pinned memory).  The small inputs are copied
+ * in, the three outputs copied back, and the call waits for `stream`.  Needs a
+ * handle made with SPECVERIFY_CREATE_HOST_STAGING.
  */
 int specverify_run_host(specverify_t h, const void *target_logits, const void *draft_logits,
                         const int32_t *draft_tokens, const int32_t *num_draft,
@@ -273,6 +279,10 @@ int specverify_set_timing_events(specverify_t h, int n, void *const *start_event
  */
 int specverify_set_depth(specverify_t h, int depth);
 
+/* The depth a wave-schedule run of `batch` requests on h uses (the setting, or
+ * the per-run choice above) in *depth_out. */
+int specverify_wave_depth(specverify_t h, int batch, int *depth_out);
+
 /*
  * specverify_set_schedule -- how a round is laid out on the GPU.  Results do
  * not depend on it.
@@ -293,6 +303,24 @@ int specverify_set_depth(specverify_t h, int depth);
 #define SPECVERIFY_SCHEDULE_CLUSTERS 2
 #define SPECVERIFY_SCHEDULE_STREAM 3
 int specverify_set_schedule(specverify_t h, int schedule);
+
+/*
+ * specverify_set_host_reads -- how specverify_run_host gets the logits to the
+ * GPU.  Results do not depend on it.
+ *   SPECVERIFY_HOST_READS_AUTO (default): read in place when both logits
+ *     buffers are pinned and mapped host memory, else staged copies;
+ *   SPECVERIFY_HOST_READS_STAGE: always copy the whole window into the
+ *     device staging first.
+ * Returns SPECVERIFY_ERR_INVALID_ARG for another mode.
+ */
+#define SPECVERIFY_HOST_READS_AUTO 0
+#define SPECVERIFY_HOST_READS_STAGE 1
+int specverify_set_host_reads(specverify_t h, int mode);
+
+/* How the last specverify_run_host on h got its logits: *in_place_out = 1 read
+ * in place, 0 copied into staging, -1 no host run yet (or it returned before
+ * choosing). */
+int specverify_last_host_reads(specverify_t h, int *in_place_out);
 
 /* Kernel launches a run of `batch` requests makes on handle h (for launch
  * accounting): the plan launch and one launch per wave of `depth` positions

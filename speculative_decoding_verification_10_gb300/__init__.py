@@ -195,6 +195,27 @@ class Verifier:
                 "clusters": _lib.SCHEDULE_CLUSTERS, "stream": _lib.SCHEDULE_STREAM}[schedule]
         _check(self.lib.specverify_set_schedule(self._h, code), "specverify_set_schedule")
 
+    def set_host_reads(self, mode: str):
+        """'auto' (read pinned, mapped host logits in place) or 'stage' (copy them
+        in first): how run_host gets the logits to the GPU."""
+        code = {"auto": _lib.HOST_READS_AUTO, "stage": _lib.HOST_READS_STAGE}[mode]
+        _check(self.lib.specverify_set_host_reads(self._h, code), "specverify_set_host_reads")
+
+    def wave_depth(self, batch: int) -> int:
+        """Positions per wave launch a run of `batch` requests uses."""
+        out = ctypes.c_int(0)
+        _check(self.lib.specverify_wave_depth(self._h, batch, ctypes.byref(out)),
+               "specverify_wave_depth")
+        return out.value
+
+    def last_host_reads(self) -> int:
+        """1 if the last run_host read the logits in place, 0 if it staged them,
+        -1 before the first."""
+        out = ctypes.c_int(0)
+        _check(self.lib.specverify_last_host_reads(self._h, ctypes.byref(out)),
+               "specverify_last_host_reads")
+        return out.value
+
     def set_depth(self, depth: int):
         """Positions per wave launch: 1 .. max_k + 1, or 0 to choose per run."""
         _check(self.lib.specverify_set_depth(self._h, depth), "specverify_set_depth")

@@ -26,6 +26,9 @@ SCHEDULE_WAVES = 1
 SCHEDULE_CLUSTERS = 2
 SCHEDULE_STREAM = 3
 
+HOST_READS_AUTO = 0
+HOST_READS_STAGE = 1
+
 STATIC_MAX_BATCH = 256
 STATIC_MAX_K = 7
 
@@ -92,6 +95,12 @@ def load(path: str | None = None):
     lib.specverify_set_schedule.restype = I
     lib.specverify_set_depth.argtypes = [P, I]
     lib.specverify_set_depth.restype = I
+    lib.specverify_set_host_reads.argtypes = [P, I]
+    lib.specverify_set_host_reads.restype = I
+    lib.specverify_wave_depth.argtypes = [P, I, ctypes.POINTER(I)]
+    lib.specverify_wave_depth.restype = I
+    lib.specverify_last_host_reads.argtypes = [P, ctypes.POINTER(I)]
+    lib.specverify_last_host_reads.restype = I
     lib.specverify_metrics.argtypes = [P, P, I, I, P, P, P, P, P]
     lib.specverify_metrics.restype = I
     lib.specverify_run_trimmed.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_uint64, I, I,

@@ -550,6 +550,8 @@ struct specverify_ctx {
   void* scratch;
   uint32_t epoch;
   // staging for specverify_run_host
+  int host_reads;       // SPECVERIFY_HOST_READS_*
+  int last_host_place;  // the last specverify_run_host: 1 read in place, 0 staged, -1 none
   void* stage;
   char* st_target;
   char* st_draft;
@@ -653,6 +655,8 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   h->last_stream = nullptr;
   h->last_run_empty = true;
   h->n_events = 0;
+  h->host_reads = SPECVERIFY_HOST_READS_AUTO;
+  h->last_host_place = -1;
   h->run_counter = 0;
   h->epoch = 0u;
   h->stage = nullptr;
@@ -767,6 +771,20 @@ int specverify_run_trimmed(specverify_t h, const void* target_logits, const void
   return run_impl(h, a, stream);
 }
 
+// The device address of host memory that is pinned and mapped into the
+// device's address space (cudaHostAlloc, or cudaHostRegister with mapping),
+// if `p` lies in such memory.
+static bool mapped_host(const void* p, const void** dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return false;
+  *dev = at.devicePointer;
+  return true;
+}
+
 int specverify_run_host(specverify_t h, const void* target_logits, const void* draft_logits,
                         const int32_t* draft_tokens, const int32_t* num_draft,
                         const float* temperature, uint64_t seed, int batch, int total_draft,
@@ -794,9 +812,22 @@ int specverify_run_host(specverify_t h, const void* target_logits, const void* d
   auto d2h = [&](void* dst, const void* src, size_t n) {
     if (n && ok) ok = cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, s) == cudaSuccess;
   };
-  h2d(h->st_target, target_logits, (size_t)(batch + total_draft) * row_bytes);
   const bool has_draft = draft_logits != nullptr && total_draft > 0;
-  if (has_draft) h2d(h->st_draft, draft_logits, (size_t)total_draft * row_bytes);
+  // Logits in pinned host memory that the device maps are read where they lie
+  // (over NVLink-C2C on Grace-Blackwell): only the rows the round needs cross
+  // to the GPU.  Anything else is copied into the staging buffers first.
+  const void* dev_target = nullptr;
+  const void* dev_draft = nullptr;
+  const bool in_place = h->host_reads == SPECVERIFY_HOST_READS_AUTO &&
+                        mapped_host(target_logits, &dev_target) &&
+                        (!has_draft || mapped_host(draft_logits, &dev_draft));
+  h->last_host_place = in_place ? 1 : 0;
+  if (!in_place) {
+    h2d(h->st_target, target_logits, (size_t)(batch + total_draft) * row_bytes);
+    if (has_draft) h2d(h->st_draft, draft_logits, (size_t)total_draft * row_bytes);
+    dev_target = h->st_target;
+    dev_draft = h->st_draft;
+  }
   h2d(h->st_tokens, draft_tokens, sizeof(int32_t) * (size_t)total_draft);
   h2d(h->st_num_draft, num_draft, sizeof(int32_t) * (size_t)batch);
   h2d(h->st_temperature, temperature, sizeof(float) * (size_t)batch);
@@ -804,7 +835,7 @@ int specverify_run_host(specverify_t h, const void* target_logits, const void* d
     cudaGetLastError();
     return SPECVERIFY_ERR_CUDA;
   }
-  const RunArgs a{h->st_target, has_draft ? h->st_draft : nullptr, h->st_tokens,
+  const RunArgs a{dev_target, has_draft ? dev_draft : nullptr, h->st_tokens,
                   h->st_num_draft, h->st_temperature, seed, batch, total_draft,
                   h->st_accepted, h->st_committed, h->st_flags,
                   nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -927,6 +958,32 @@ int specverify_set_depth(specverify_t h, int depth) {
   if (rc != SPECVERIFY_OK) return rc;
   if (depth < 0 || depth > h->cfg.max_k + 1) return SPECVERIFY_ERR_INVALID_ARG;
   h->cfg.depth_setting = depth;
+  return SPECVERIFY_OK;
+}
+
+int specverify_set_host_reads(specverify_t h, int mode) {
+  int rc = check_handle(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (mode != SPECVERIFY_HOST_READS_AUTO && mode != SPECVERIFY_HOST_READS_STAGE)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  h->host_reads = mode;
+  return SPECVERIFY_OK;
+}
+
+int specverify_wave_depth(specverify_t h, int batch, int* depth_out) {
+  int rc = check_handle(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (depth_out == nullptr || batch < 0 || batch > h->cfg.max_batch)
+    return SPECVERIFY_ERR_INVALID_ARG;
+  *depth_out = run_depth(h->cfg, batch);
+  return SPECVERIFY_OK;
+}
+
+int specverify_last_host_reads(specverify_t h, int* in_place_out) {
+  int rc = check_handle(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  if (in_place_out == nullptr) return SPECVERIFY_ERR_INVALID_ARG;
+  *in_place_out = h->last_host_place;
   return SPECVERIFY_OK;
 }
 

@@ -426,17 +426,25 @@ def _softmax(x, t):
 
 # --- host-buffer entry point ----------------------------------------------------------
 
-def test_run_host_matches_device_run():
+@pytest.mark.parametrize("mode,pinned,in_place", [("auto", True, 1), ("stage", True, 0),
+                                                   ("auto", False, 0)])
+def test_run_host_matches_device_run(mode, pinned, in_place):
+    """Pinned host logits read in place ('auto'), staged ('stage'), and pageable
+    ones (always staged): the same outputs as the device run."""
     b = W.make_batch("w3_v151936_bf16", device="cuda", batch=12)
     with Verifier(12, b.max_k, b.vocab, "bf16", host_staging=True) as v:
+        v.set_host_reads(mode)
+        assert v.last_host_reads() == -1
         dev = v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 9)
         torch.cuda.synchronize()
         h = b.to("cpu")
         acc = torch.empty(12, dtype=torch.int32).pin_memory()
         com = torch.empty(12, b.max_k + 1, dtype=torch.int32).pin_memory()
         flg = torch.empty(b.total_draft, dtype=torch.uint8).pin_memory()
-        v.run_host(h.target.pin_memory(), h.draft.pin_memory(), h.tokens, h.num_draft,
-                   h.temperature, 9, acc, com, flg)
+        tgt = h.target.pin_memory() if pinned else h.target.clone()
+        drf = h.draft.pin_memory() if pinned else h.draft.clone()
+        v.run_host(tgt, drf, h.tokens, h.num_draft, h.temperature, 9, acc, com, flg)
+        assert v.last_host_reads() == in_place
         assert torch.equal(acc, dev.accepted_len.cpu())
         assert torch.equal(com, dev.committed.cpu())
         assert torch.equal(flg, dev.flags.cpu())
