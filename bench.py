@@ -290,8 +290,10 @@ def measure_e2e(args, b, v, world, dev):
     small = 4 * (h_tokens.numel() + h_nd.numel() + h_temp.numel())
     in_place = v.last_host_reads() == 1
     if in_place:
-        # the kernels read the rows of every wave a request takes part in, where
-        # they lie, plus the two rows a correction draw reads again
+        # the kernels read the rows of every wave a request takes part in where
+        # they lie; the wave schedule copies each sampled row to the device as
+        # it streams, so a correction draw reads its two rows from there (the
+        # other schedules read them from the host again)
         depth = v.wave_depth(b.batch)
         A = h_acc.numpy().astype(np.int64)
         k = h_nd.numpy().astype(np.int64)
@@ -299,7 +301,8 @@ def measure_e2e(args, b, v, world, dev):
         last = np.minimum(k, (A // depth + 1) * depth - 1)
         rows = np.where(sampling, 2 * np.minimum(last + 1, k) + (last == k),
                         last + 1)
-        rows = rows + np.where(sampling & (A < k), 2, 0)
+        if args.schedule not in ("auto", "waves"):
+            rows = rows + np.where(sampling & (A < k), 2, 0)
         logits = int(rows.sum()) * b.vocab * h_target.element_size()
     else:
         logits = h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()

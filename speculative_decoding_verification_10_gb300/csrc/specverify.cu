@@ -422,6 +422,10 @@ struct RunArgs {
   const float* cost;
   int32_t* verified_k;
   bool trimmed = false;
+  // device copies for the rows a wave streams when the logits lie in host
+  // memory (specverify_run_host reading in place), or NULL
+  void* tee_target = nullptr;
+  void* tee_draft = nullptr;
 };
 
 // Checks that need no device (the batch must already be in range).
@@ -515,6 +519,11 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
     P.depth = 1;
     P.n_waves = 1;
     P.list_cap = c.max_batch;
+  } else if (aligned && a.tee_target != nullptr) {
+    // waves over host-resident logits: sampled rows are copied to the device
+    // as they stream, and the correction draws read those copies
+    P.tee_target = static_cast<char*>(a.tee_target);
+    P.tee_draft = static_cast<char*>(a.tee_draft);
   }
   return c.dtype == SPECVERIFY_BF16 ? launch_round<sv::BF16>(c, P, aligned, s, ev_start, ev_stop)
                                     : launch_round<sv::F32>(c, P, aligned, s, ev_start, ev_stop);
@@ -835,10 +844,14 @@ int specverify_run_host(specverify_t h, const void* target_logits, const void* d
     cudaGetLastError();
     return SPECVERIFY_ERR_CUDA;
   }
-  const RunArgs a{dev_target, has_draft ? dev_draft : nullptr, h->st_tokens,
-                  h->st_num_draft, h->st_temperature, seed, batch, total_draft,
-                  h->st_accepted, h->st_committed, h->st_flags,
-                  nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  RunArgs a{dev_target, has_draft ? dev_draft : nullptr, h->st_tokens,
+            h->st_num_draft, h->st_temperature, seed, batch, total_draft,
+            h->st_accepted, h->st_committed, h->st_flags,
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  if (in_place && has_draft) {
+    a.tee_target = h->st_target;
+    a.tee_draft = h->st_draft;
+  }
   rc = run_impl(h, a, stream);
   if (rc != SPECVERIFY_OK) return rc;
   d2h(accepted_len, h->st_accepted, sizeof(int32_t) * (size_t)batch);

@@ -174,6 +174,12 @@ struct Params {
   int cluster_mode;  // the plan lists one entry per request (the cluster launch)
   int unit_cap;      // cluster launch: more units than any round needs
   int stream_mode;   // the plan publishes its rows to the stream schedule's queue
+  // Device copies of the window, same layout as target / draft, or NULL.  When
+  // set (waves, 16-byte rows, logits read from host memory), every sampled
+  // row a wave streams is also written here, and the correction draws of the
+  // next wave read these copies instead of the host rows.
+  char* tee_target;
+  char* tee_draft;
   int band_rows;     // stream schedule: rows a full band takes
   int band_cap;      // stream schedule: bands a round may form
   int trimmed;              // num_draft is the window layout; verify trimmed windows
@@ -287,6 +293,7 @@ struct __align__(16) QItem {
   int sG, e0;
   int band;
   int snu;  // stream schedule: urgent entries of the segment's band
+  char* tee;  // where a softmax segment's row is copied (Params::tee_*), or NULL
 };
 
 // The logit x[y] held by vector x at element e (a select chain, no local memory).
@@ -632,10 +639,15 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
     LazySoftmax acc;
     acc.init();
     const int yv = itm.yv, ye = itm.y & (E::kVec - 1);
+    uint4* tee = reinterpret_cast<uint4*>(itm.tee);
     for (int st = 0; st < nst; ++st) {
       uint4 v0, v1;
       take(v0, v1);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
+      if (tee) {
+        if (vi < vend) tee[vi] = v0;
+        if (vi + kThreads < vend) tee[vi + kThreads] = v1;
+      }
       if (st >= nfull) {
         if (vi >= vend) v0 = E::pad();
         if (vi + kThreads >= vend) v1 = E::pad();
@@ -1366,6 +1378,7 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
   it.e0 = e0;
   it.mp = it.inv_sp = it.mq = it.inv_sq = 0.f;
   it.row2 = nullptr;
+  it.tee = nullptr;
   if (phase == 0) {
     const ResEntry re = ldcg_res(res + e);
     it.r = re.r;
@@ -1384,8 +1397,11 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
     it.inv_sq = re.inv_sq;
     it.req_lo = re.req_lo;
     it.req_hi = re.req_hi;
-    it.row = reinterpret_cast<const char*>(P.target) + (size_t)(re.d0 + re.r + re.j) * row_bytes;
-    it.row2 = reinterpret_cast<const char*>(P.draft) + (size_t)(re.d0 + re.j) * row_bytes;
+    // the rows were streamed (and, with a tee, copied) in an earlier wave
+    const char* tb = kAligned && P.tee_target ? P.tee_target : reinterpret_cast<const char*>(P.target);
+    const char* db = kAligned && P.tee_target ? P.tee_draft : reinterpret_cast<const char*>(P.draft);
+    it.row = tb + (size_t)(re.d0 + re.r + re.j) * row_bytes;
+    it.row2 = db + (size_t)(re.d0 + re.j) * row_bytes;
   } else {
     const Entry en = ldcg_entry(list + e);
     const int r = en.meta & 0x1fff;
@@ -1401,9 +1417,12 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
     it.req_lo = en.req_lo;
     it.req_hi = en.req_hi;
     it.kind = en.c == 0.f ? kArgmax : (it.is_draft || it.pos < it.k ? kSoftmax : kRace);
-    it.row = it.is_draft
-                 ? reinterpret_cast<const char*>(P.draft) + (size_t)(en.d0 + it.pos) * row_bytes
-                 : reinterpret_cast<const char*>(P.target) + (size_t)(en.d0 + r + it.pos) * row_bytes;
+    const size_t off = it.is_draft ? (size_t)(en.d0 + it.pos) * row_bytes
+                                   : (size_t)(en.d0 + r + it.pos) * row_bytes;
+    it.row = (it.is_draft ? reinterpret_cast<const char*>(P.draft)
+                          : reinterpret_cast<const char*>(P.target)) + off;
+    if (kAligned && P.tee_target && it.kind == kSoftmax)
+      it.tee = (it.is_draft ? P.tee_draft : P.tee_target) + off;
   }
   if (kAligned) {
     constexpr int kVPB = kRaceBlock / E::kVec;
