@@ -114,19 +114,23 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources a verify round on the default schedule is built from: the plan
+# and wave kernels, their device helpers, and the host code that launches them.
+ROUND_SOURCES = ("sv_device.cuh", "sv_kernels.cuh", "specverify.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_10_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in ROUND_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload):
-    """DRAM bytes per row-pass launch from the committed ncu summary, if it was
-    taken on the current kernel sources; else None."""
+    """DRAM bytes per round from the committed ncu summary, if it was taken on
+    the current sources of the round's kernels; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:

@@ -114,6 +114,152 @@ __device__ __forceinline__ void count_add(unsigned int* whist, bool valid, int d
 
 constexpr int kWin = 8;  // octave bins the first top-p level resolves below the maximum
 
+// ---------------------------------------------------------------------------
+// The window histogram of bf16 rows.  A bf16 logit is fixed by its 16-bit key,
+// so counts of exact keys give both rules at once: top-k from counts of the
+// keys at or above a key, top-p from masses count * 2^(c (x_key - max)).  The
+// window is the kWinBins high-byte bins at and below the maximum's (kWinKeys
+// keys); one pass counts the row's keys there (the other elements only add
+// their masses to a per-thread sum), and the thresholds come from block-wide
+// suffix scans over the window in a fixed order.  A row whose threshold lies
+// below the window goes on to the radix descent.
+// ---------------------------------------------------------------------------
+constexpr int kWinBins = 8;
+constexpr int kWinKeys = kWinBins * 256;
+static_assert(kWinKeys == 2 * kTruncThreads, "two window keys per thread");
+
+// The bf16 logit of a 16-bit order key (trunc_key<BF16> inverted).
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  const uint32_t h = (key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu);
+  return __uint_as_float(h << 16);
+}
+
+// Block-wide sum over the threads with larger index (exclusive suffix), in a
+// fixed order; *total gets the sum over all threads.  All threads call it.
+template <typename T>
+__device__ __forceinline__ T block_suffix_excl(T v, T* s_part, T* total) {
+  constexpr int kW = kTruncThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T x = v;  // inclusive suffix inside the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const T o = __shfl_down_sync(0xffffffffu, x, off);
+    if (lane + off < 32) x += o;
+  }
+  T ex = __shfl_down_sync(0xffffffffu, x, 1);
+  if (lane == 31) ex = T(0);
+  if (lane == 0) s_part[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const T w = lane < kW ? s_part[lane] : T(0);
+    T y = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const T o = __shfl_down_sync(0xffffffffu, y, off);
+      if (lane + off < 32) y += o;
+    }
+    T ye = __shfl_down_sync(0xffffffffu, y, 1);
+    if (lane == 31) ye = T(0);
+    if (lane < kW) s_part[lane] = ye;
+    if (lane == 0) s_part[kW] = y;
+  }
+  __syncthreads();
+  const T r = ex + s_part[warp];
+  *total = s_part[kW];
+  __syncthreads();
+  return r;
+}
+
+// Block-wide max (or min) of an int; all threads call it.
+__device__ __forceinline__ int block_extreme(int v, bool is_max, int* s_part) {
+  constexpr int kW = kTruncThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const int o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? max(v, o) : min(v, o);
+  }
+  if (lane == 0) s_part[warp] = v;
+  __syncthreads();
+  int r = s_part[0];
+  for (int w = 1; w < kW; ++w) r = is_max ? max(r, s_part[w]) : min(r, s_part[w]);
+  __syncthreads();
+  return r;
+}
+
+// The thresholds of one bf16 row from its window histogram: *tau gets the
+// 16-bit key to keep from (0 keeps everything).  Returns false, leaving *tau,
+// when the row needs the radix descent: a non-finite maximum, fewer than K
+// elements in the window, or a top-p boundary below the window.
+template <typename Each>
+__device__ bool window_thresholds(Each&& each, int V, float mx, float T, bool use_k, int K,
+                                  bool use_p, float Pp, unsigned int* s_hist, double* s_dpart,
+                                  unsigned int* s_upart, int* s_ipart, uint32_t* tau) {
+  if (!(mx > kNegInf && mx < 3.0e38f)) return false;
+  const int tid = threadIdx.x;
+  const int hb_top = (int)(trunc_key<BF16>(mx) >> 8);
+  const int lo = max(hb_top - (kWinBins - 1), 0);
+  const float c = kLog2e / T;
+  const float cm = c * mx;
+  s_hist[2 * tid] = 0u;
+  s_hist[2 * tid + 1] = 0u;
+  __syncthreads();
+  float below = 0.f;  // mass of this thread's elements below the window
+  each([&](bool ok, float x) {
+    const uint32_t k = trunc_key<BF16>(x);
+    const int hb = (int)(k >> 8);
+    if (ok && hb >= lo) {
+      atomicAdd(&s_hist[((hb - lo) << 8) | (int)(k & 0xffu)], 1u);
+    } else if (ok && use_p) {
+      below += fast_ex2(fmaf(x, c, -cm));
+    }
+  });
+  __syncthreads();
+  // thread t holds window keys i0 = 2t and i1 = 2t + 1 (key = (lo << 8) + i)
+  const int i0 = 2 * tid, i1 = i0 + 1;
+  const unsigned int n0 = s_hist[i0], n1 = s_hist[i1];
+  unsigned int n_win;
+  const unsigned int n_above = block_suffix_excl<unsigned int>(n0 + n1, s_upart, &n_win);
+  int first = 0;  // lowest window index a survivor of top-k may have
+  if (use_k) {
+    if (n_win < (unsigned int)K) return false;
+    // the highest key with at least K elements at or above it
+    const unsigned int s1 = n_above + n1, s0 = s1 + n0;
+    const int cand = s1 >= (unsigned int)K ? i1 : (s0 >= (unsigned int)K ? i0 : -1);
+    first = block_extreme(cand, true, s_ipart);
+  }
+  int pick = first;
+  if (use_p) {
+    const double w0 = (n0 && i0 >= first)
+                          ? (double)n0 * (double)fast_ex2(fmaf(key_logit((lo << 8) + i0), c, -cm))
+                          : 0.0;
+    const double w1 = (n1 && i1 >= first)
+                          ? (double)n1 * (double)fast_ex2(fmaf(key_logit((lo << 8) + i1), c, -cm))
+                          : 0.0;
+    double m_win;
+    const double m_above = block_suffix_excl<double>(w0 + w1, s_dpart, &m_win);
+    // survivors below the window exist only without a top-k cut inside it
+    const bool tail = !use_k && n_win < (unsigned int)V;
+    double m_tail = 0.0;
+    if (tail) {
+      const float wb = group_sum<32>(below);
+      if ((tid & 31) == 0) s_dpart[tid >> 5] = (double)wb;
+      __syncthreads();
+      for (int w = 0; w < kTruncThreads / 32; ++w) m_tail += s_dpart[w];
+      __syncthreads();
+    }
+    const double target = (double)Pp * (m_win + m_tail);
+    if (tail && m_win < target) return false;
+    // the lowest survivor key whose strictly larger survivors weigh below target
+    const bool k1 = n1 && i1 >= first && m_above < target;
+    const bool k0 = n0 && i0 >= first && m_above + w1 < target;
+    pick = block_extreme(k0 ? i0 : (k1 ? i1 : kWinKeys), false, s_ipart);
+    pick = max(pick, first);
+  }
+  *tau = (uint32_t)((lo << 8) + pick);
+  return true;
+}
+
 template <typename E, bool kAligned>
 __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
   constexpr int kWarps = kTruncThreads / 32;
@@ -126,7 +272,14 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
   __shared__ int s_digit;
   __shared__ unsigned long long s_above;
   __shared__ double s_dval[2];
+  // bf16 rows: exact keys of the 8 high-byte bins at and below the maximum's
+  __shared__ unsigned int s_hist[kWinKeys];
+  __shared__ double s_dpart[kWarps + 1];
+  __shared__ unsigned int s_upart[kWarps + 1];
+  __shared__ int s_ipart[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // bf16 rows with 16-byte vectors take the window histogram first
+  constexpr bool kFast = E::kBytes == 2 && kAligned;
   constexpr int kLevels = E::kBytes;  // 8-bit digits of the key
   const int V = P.vocab;
   const size_t row_bytes = (size_t)V * E::kBytes;
@@ -215,7 +368,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       each([&](bool ok, float x) {
         nan |= ok && x != x;
         mx = fmaxf(mx, x);
-        if (use_k) count_add(s_whist[warp], ok, (int)(trunc_key<E>(x) >> shift0));
+        if (!kFast && use_k) count_add(s_whist[warp], ok, (int)(trunc_key<E>(x) >> shift0));
       });
       if (__any_sync(0xffffffffu, nan) && lane == 0) s_nan = 1u;
       mx = warp_max(mx);
@@ -230,7 +383,22 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       mx = s_red[0];
       copy = s_nan != 0u;
       __syncthreads();
-      if (!copy && use_k) {
+      bool done = false;  // the thresholds were found by the window histogram
+      if constexpr (kFast) {
+        if (!copy) {
+          done = window_thresholds(each, P.vocab, mx, T, use_k, K, use_p, Pp, s_hist, s_dpart,
+                                   s_upart, s_ipart, &tau);
+          if (!done && use_k) {
+            // the radix descent below starts from the level-0 counts
+            clear_counts();
+            each([&](bool ok, float x) {
+              count_add(s_whist[warp], ok, (int)(trunc_key<E>(x) >> shift0));
+            });
+            sum_counts();
+          }
+        }
+      }
+      if (!copy && !done && use_k) {
         // ---- top-k: the key of the K-th largest logit, one level at a time -------
         unsigned long long need = (unsigned long long)K;
         uint32_t prefix = 0u;
@@ -260,7 +428,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
         }
         tau = prefix;
       }
-      if (!copy && use_p) {
+      if (!copy && !done && use_p) {
         // ---- top-p on the survivors, masses w = 2^(c (x - mx)) ---------------------
         const float c = kLog2e / T;
         const float cm = c * mx;
