@@ -26,6 +26,8 @@
 namespace sv {
 
 constexpr int kTruncThreads = 1024;
+constexpr int kTruncLoads = 4;  // 16-byte loads in flight per thread (window histogram passes)
+constexpr int kOutLoads = 1;    // ... and in the output pass
 constexpr uint32_t kStBadTrunc = 1024u;
 
 struct TruncParams {
@@ -318,17 +320,27 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
 
     // visit every element of the row: f(ok, x), warp-uniform (every lane of a
     // warp runs the same iterations; ok is false past the row's end); vector
-    // loads on aligned rows
-    auto each = [&](auto&& f) {
+    // loads on aligned rows, nl of them issued before any is used (a thread
+    // still visits its vectors i = tid + j * kTruncThreads in order of j)
+    auto each_n = [&](auto nl, auto&& f) {
+      constexpr int kN = decltype(nl)::value;
       if (kAligned) {
         const uint4* rv = reinterpret_cast<const uint4*>(in);
-        for (int i0 = warp * 32; i0 < nvec; i0 += kTruncThreads) {
-          const int i = i0 + lane;
-          const bool ok = i < nvec;
-          float x[E::kVec];
-          E::unpack(ok ? ld_stream(rv + i) : E::pad(), x);
+        for (int i0 = warp * 32; i0 < nvec; i0 += kN * kTruncThreads) {
+          uint4 q[kN];
 #pragma unroll
-          for (int e = 0; e < E::kVec; ++e) f(ok, x[e]);
+          for (int u = 0; u < kN; ++u) {
+            const int i = i0 + u * kTruncThreads + lane;
+            q[u] = i < nvec ? ld_stream(rv + i) : E::pad();
+          }
+#pragma unroll
+          for (int u = 0; u < kN; ++u) {
+            const bool ok = i0 + u * kTruncThreads + lane < nvec;
+            float x[E::kVec];
+            E::unpack(q[u], x);
+#pragma unroll
+            for (int e = 0; e < E::kVec; ++e) f(ok, x[e]);
+          }
         }
       } else {
         for (int v0 = warp * 32; v0 < V; v0 += kTruncThreads) {
@@ -337,6 +349,12 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
           f(ok, ok ? E::load1(in, v) : kNegInf);
         }
       }
+    };
+    // the radix descent's passes (register-heavy) keep one load in flight; the
+    // window histogram's passes, kTruncLoads
+    auto each = [&](auto&& f) { each_n(std::integral_constant<int, 1>{}, f); };
+    auto each_deep = [&](auto&& f) {
+      each_n(std::integral_constant<int, kFast ? kTruncLoads : 1>{}, f);
     };
     // the per-warp counts, zeroed before / summed into s_cnt after a pass
     auto clear_counts = [&]() {
@@ -365,7 +383,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       float mx = kNegInf;
       bool nan = false;
       const int shift0 = 8 * (kLevels - 1);
-      each([&](bool ok, float x) {
+      each_deep([&](bool ok, float x) {
         nan |= ok && x != x;
         mx = fmaxf(mx, x);
         if (!kFast && use_k) count_add(s_whist[warp], ok, (int)(trunc_key<E>(x) >> shift0));
@@ -386,7 +404,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       bool done = false;  // the thresholds were found by the window histogram
       if constexpr (kFast) {
         if (!copy) {
-          done = window_thresholds(each, P.vocab, mx, T, use_k, K, use_p, Pp, s_hist, s_dpart,
+          done = window_thresholds(each_deep, P.vocab, mx, T, use_k, K, use_p, Pp, s_hist, s_dpart,
                                    s_upart, s_ipart, &tau);
           if (!done && use_k) {
             // the radix descent below starts from the level-0 counts
@@ -558,24 +576,35 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
     if (kAligned) {
       const uint4* rv = reinterpret_cast<const uint4*>(in);
       uint4* ov = reinterpret_cast<uint4*>(out);
-      for (int i = tid; i < nvec; i += kTruncThreads) {
-        uint4 q = ld_stream(rv + i);
-        if (!copy) {
-          float x[E::kVec];
-          E::unpack(q, x);
-          uint32_t* w = reinterpret_cast<uint32_t*>(&q);
+      for (int i0 = tid; i0 < nvec; i0 += kOutLoads * kTruncThreads) {
+        uint4 qs[kOutLoads];
 #pragma unroll
-          for (int e = 0; e < E::kVec; ++e) {
-            if (trunc_key<E>(x[e]) >= tau) continue;
-            if (E::kBytes == 4) {
-              w[e] = 0xff800000u;
-            } else {
-              const int h = e >> 1;
-              w[h] = (e & 1) ? ((w[h] & 0x0000ffffu) | 0xff800000u) : ((w[h] & 0xffff0000u) | 0xff80u);
+        for (int u = 0; u < kOutLoads; ++u) {
+          const int i = i0 + u * kTruncThreads;
+          if (i < nvec) qs[u] = ld_stream(rv + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kOutLoads; ++u) {
+          const int i = i0 + u * kTruncThreads;
+          if (i >= nvec) break;
+          uint4 q = qs[u];
+          if (!copy) {
+            float x[E::kVec];
+            E::unpack(q, x);
+            uint32_t* w = reinterpret_cast<uint32_t*>(&q);
+#pragma unroll
+            for (int e = 0; e < E::kVec; ++e) {
+              if (trunc_key<E>(x[e]) >= tau) continue;
+              if (E::kBytes == 4) {
+                w[e] = 0xff800000u;
+              } else {
+                const int h = e >> 1;
+                w[h] = (e & 1) ? ((w[h] & 0x0000ffffu) | 0xff800000u) : ((w[h] & 0xffff0000u) | 0xff80u);
+              }
             }
           }
+          ov[i] = q;
         }
-        ov[i] = q;
       }
     } else {
       for (int v = tid; v < V; v += kTruncThreads) {
