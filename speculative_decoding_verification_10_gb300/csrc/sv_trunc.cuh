@@ -43,6 +43,22 @@ struct TruncParams {
   int32_t* status;  // nullable device word (atomicOr)
 };
 
+// The output pass is the last touch of a row: its loads and the stores of the
+// output row are marked evict-first (cache streaming), so they do not push out
+// of L2 the rows other CTAs are still taking their earlier passes over.
+__device__ __forceinline__ uint4 ld_last_use(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.cs.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_streaming(uint4* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 // Order-preserving key of a logit: larger logit, larger key (-inf lowest;
 // -0 and +0 compare equal, so they share a key).  bf16 logits carry their
 // information in the upper 16 bits.
@@ -581,7 +597,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
 #pragma unroll
         for (int u = 0; u < kOutLoads; ++u) {
           const int i = i0 + u * kTruncThreads;
-          if (i < nvec) qs[u] = ld_stream(rv + i);
+          if (i < nvec) qs[u] = ld_last_use(rv + i);
         }
 #pragma unroll
         for (int u = 0; u < kOutLoads; ++u) {
@@ -603,7 +619,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
               }
             }
           }
-          ov[i] = q;
+          st_streaming(ov + i, q);
         }
       }
     } else {
