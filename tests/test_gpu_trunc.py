@@ -163,3 +163,69 @@ def test_top_1_sampling_is_greedy_gpu():
         inp0 = dict(inp, temperature=np.zeros(B, np.float32))
         g = parity.run_gpu(v, inp0, 2)
     assert (s["committed"] == g["committed"]).all() and (s["accepted_len"] == g["accepted_len"]).all()
+
+
+def test_window_histogram_and_radix_descent_rows():
+    """bf16 rows built so that both ways to a threshold run: rows whose top-k or
+    top-p boundary lies among the exact keys of the eight high-byte bins below
+    the maximum (the window histogram), and rows it hands to the radix descent
+    (top-k larger than the window's count, a top-p boundary below the window, a
+    maximum that is not finite).  Every row against the oracle."""
+    rng = np.random.default_rng(21)
+    V = 4096
+
+    def normal(s, mu=0.0):
+        return rng.normal(size=V) * s + mu
+
+    def few_high():  # 50 logits in (1, 100), the rest far below zero
+        x = rng.normal(size=V) * 50.0 - 300.0
+        x[rng.choice(V, 50, replace=False)] = rng.uniform(1.0, 100.0, size=50)
+        return x
+
+    def flat():  # one logit 0.5, the rest in [-1, 0): the mass lies below the window
+        x = rng.uniform(-1.0, 0.0, size=V)
+        x[rng.integers(V)] = 0.5
+        return x
+
+    def ties():
+        return np.round(rng.normal(size=V) * 3.0)
+
+    def neg_inf():
+        return np.full(V, -np.inf)
+
+    designs = [  # (row maker, T, top_k, top_p)
+        (lambda: normal(2.5), 1.0, 20, 1.0),
+        (lambda: normal(2.5), 1.0, 0, 0.9),
+        (lambda: normal(2.5), 0.7, 50, 0.8),
+        (lambda: normal(0.5, -5.0), 1.0, 10, 0.9),
+        (few_high, 1.0, 1000, 1.0),
+        (few_high, 1.0, 1000, 0.5),
+        (flat, 10.0, 0, 0.5),
+        (flat, 10.0, 0, 0.999),
+        (ties, 1.0, 100, 1.0),
+        (ties, 1.3, 0, 0.7),
+        (neg_inf, 1.0, 5, 1.0),
+    ]
+    B = len(designs)
+    k = np.ones(B, np.int32)
+    temp = np.array([d[1] for d in designs], np.float32)
+    inp = cases.random_batch(k, temp, vocab=V, dtype="bf16", seed=22)
+    inp["max_k"] = 1
+    tgt, drf = [], []
+    for make, _, _, _ in designs:
+        rows = [make() for _ in range(2)]
+        tgt += rows
+        drf.append(rows[0] + rng.normal(size=V) * 0.3)
+    inp["target"] = cases.to_bf16_bits(np.array(tgt, np.float32))
+    inp["draft"] = cases.to_bf16_bits(np.array(drf, np.float32))
+    top_k = np.array([d[2] for d in designs], np.int32)
+    top_p = np.array([d[3] for d in designs], np.float32)
+    gt, gd, st = gpu_truncate(inp, top_k, top_p)
+    ot, od, mt, md, ost = oracle.truncate(inp["target"], inp["draft"], inp["num_draft"],
+                                          inp["temperature"], top_k, top_p)
+    assert st == ost == 0
+    ex = compare_rows(gt, ot, mt) + compare_rows(gd, od, md)
+    assert ex <= 2
+    # the constructed rows really do drop logits where a rule is on
+    kept = (gt != 0xFF80).sum(axis=1)
+    assert 20 <= kept[0] < V and kept[16] >= 100
