@@ -55,6 +55,7 @@ constexpr int kQueue = 16;                     // segment queue entries (power o
 constexpr int kMaxBatch = 4096;                // requests per round
 constexpr int kMaxK = 31;                      // draft positions per request
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanTokens = 4096;              // draft tokens the plan stages in shared memory
 constexpr int kRaceBlock = 128;                // vocab ids per race block
 constexpr int kMinSpanBytes = 16384;           // smallest share of a wave per CTA
 
@@ -832,7 +833,8 @@ __device__ __forceinline__ int wave_rows(const Params& P, bool sampling, int k, 
 
 // The j-th of those rows, as a list entry.
 __device__ __forceinline__ Entry wave_entry(const Params& P, bool sampling, int r, int d0, int k,
-                                            float c, RequestKey rk, int s, int j, int base) {
+                                            float c, RequestKey rk, int s, int j, int base,
+                                            const int32_t* tokens) {
   int pos, is_draft = 0, paired = 0;
   if (!sampling) {
     pos = s + j;
@@ -847,7 +849,7 @@ __device__ __forceinline__ Entry wave_entry(const Params& P, bool sampling, int 
   en.meta = entry_meta(r, is_draft, paired, k, pos);
   en.d0 = d0;
   en.c = c;
-  en.y = pos < k ? P.tokens[d0 + pos] : -1;
+  en.y = pos < k ? tokens[d0 + pos] : -1;
   en.req_lo = rk.lo;
   en.req_hi = rk.hi;
   en.base = base;
@@ -874,7 +876,7 @@ __device__ void append_next_wave(const Params& P, const ReqInfo& q, int next) {
   at = __shfl_sync(0xffffffffu, at, 0);
   Entry* list = P.lists + (size_t)w1 * P.list_cap;
   for (int j = lane; j < n; j += 32)
-    list[at + j] = wave_entry(P, sampling, q.r, q.d0, q.k, q.c, q.rk, next, j, at);
+    list[at + j] = wave_entry(P, sampling, q.r, q.d0, q.k, q.c, q.rk, next, j, at, P.tokens);
 }
 
 // ---------------------------------------------------------------------------
@@ -1546,10 +1548,27 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
   __shared__ int s_w[kPlanThreads / 32 + 1];
   __shared__ uint32_t s_layout;
   __shared__ int s_doff[kMaxBatch + 1];
+  __shared__ int32_t s_tok[kPlanTokens];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kW = kPlanThreads / 32;
+  constexpr int kPer = kMaxBatch / kPlanThreads;  // requests a thread takes
 
   pdl_launch_dependents();  // wave 0 may be scheduled; it waits for this grid
+  // The small inputs in one round trip: every thread's num_draft and
+  // temperature, and the draft tokens (total_draft of them, valid memory
+  // whatever num_draft holds) into shared memory when they fit; the checks
+  // and the list entries then read them there.
+  const bool tok_shared = P.total_draft <= kPlanTokens;
+  for (int i = tid; tok_shared && i < P.total_draft; i += kPlanThreads) s_tok[i] = P.tokens[i];
+  const int32_t* tokens = tok_shared ? s_tok : P.tokens;
+  int k_in[kPer];
+  float t_in[kPer];
+#pragma unroll
+  for (int b = 0; b < kPer; ++b) {
+    const int r = b * kPlanThreads + tid;
+    k_in[b] = r < P.batch ? P.num_draft[r] : 0;
+    t_in[b] = r < P.batch ? P.temperature[r] : 0.f;
+  }
   if (tid == 0) {
     s_layout = 0u;
     P.ctr[kCntStatus] = 0;
@@ -1595,9 +1614,12 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
 
   // draft-row offsets, and the checks that make the layout trustworthy
   int carry = 0;
-  for (int base = 0; base < P.batch; base += kPlanThreads) {
+#pragma unroll
+  for (int b = 0; b < kPer; ++b) {
+    const int base = b * kPlanThreads;
+    if (base >= P.batch) break;
     const int r = base + tid;
-    const int k = r < P.batch ? P.num_draft[r] : 0;
+    const int k = k_in[b];
     const bool badk = k < 0 || k > P.max_k;
     if (badk) atomicOr(&s_layout, kStBadK);
     const int kk = badk ? 0 : k;
@@ -1633,7 +1655,10 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
 
   // per request: the input checks, then its rows of wave 0
   int written = 0, live = 0;
-  for (int base = 0; base < P.batch; base += kPlanThreads) {
+#pragma unroll
+  for (int b = 0; b < kPer; ++b) {
+    const int base = b * kPlanThreads;
+    if (base >= P.batch) break;
     const int r = base + tid;
     int n = 0, d0 = 0, k = 0;
     float c = 0.f;
@@ -1659,12 +1684,12 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
           }
         }
       }
-      const float t = P.temperature[r];
+      const float t = t_in[b];
       const int mode = req_mode(t);
       if (!rs) {
         if (mode == kBadTemp) rs |= kStBadTemp;
         for (int i = 0; i < k; ++i) {
-          const int y = P.tokens[d0 + i];
+          const int y = tokens[d0 + i];
           if (y < 0 || y >= P.vocab) rs |= kStBadToken;
         }
         if (!rs && mode == kSampling && k > 0 && P.draft == nullptr) rs |= kStNoDraft;
@@ -1682,7 +1707,7 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
     if (n > 0) {
       const RequestKey rk = request_key(P, r);
       for (int j = 0; j < n; ++j) {
-        P.lists[at + j] = wave_entry(P, sampling, r, d0, k, c, rk, 0, j, at);
+        P.lists[at + j] = wave_entry(P, sampling, r, d0, k, c, rk, 0, j, at, tokens);
         if (P.stream_mode) P.ready_n[at + j] = P.epoch;
       }
     }

@@ -342,7 +342,7 @@ __device__ void publish_rows(const Params& P, const ReqInfo& q, int next) {
   if (lane == 0) at = atomicAdd(P.ctr + kCntNRes, n);
   at = __shfl_sync(0xffffffffu, at, 0);
   if (lane < n) {
-    P.lists[at + lane] = wave_entry(P, sampling, q.r, q.d0, q.k, q.c, q.rk, next, lane, at);
+    P.lists[at + lane] = wave_entry(P, sampling, q.r, q.d0, q.k, q.c, q.rk, next, lane, at, P.tokens);
     st_release_u32(P.ready_n + at + lane, P.epoch);
   }
 }
