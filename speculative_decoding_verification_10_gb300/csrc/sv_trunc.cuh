@@ -59,6 +59,35 @@ __device__ __forceinline__ void st_streaming(uint4* p, uint4 v) {
                : "memory");
 }
 
+// Two bf16 logits packed in a 32-bit word, worked on together.  Their order
+// keys: a positive logit gets its bits with the top bit set, a negative one its
+// bits inverted, so keys compare as the logits do (-inf lowest; a positive NaN
+// keys above +inf, a negative one below -inf).  Unlike trunc_key, -0 keeps
+// its own key 0x7fff, just below +0's 0x8000.
+__device__ __forceinline__ uint32_t bf16x2_keys(uint32_t w) {
+  const uint32_t neg = (w >> 15) & 0x00010001u;  // sign of each half, moved to its bit 0
+  return w ^ ((neg * 0x7fffu) | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// The word with each half whose key is below the threshold (t2: the 16-bit
+// key in both halves) replaced by -inf.
+__device__ __forceinline__ uint32_t keep_bf16x2(uint32_t w, uint32_t t2) {
+  const uint32_t k = bf16x2_keys(w);
+  const uint32_t d = max_u16x2(k, t2) ^ k;  // a half is zero where its key >= the threshold
+  const uint32_t nz = (((d & 0x7fff7fffu) + 0x7fff7fffu) | d) & 0x80008000u;
+  const uint32_t drop = (nz >> 15) * 0xffffu;  // 0xffff in each half to drop
+  return (w & ~drop) | (0xff80ff80u & drop);
+}
+
 // Order-preserving key of a logit: larger logit, larger key (-inf lowest;
 // -0 and +0 compare equal, so they share a key).  bf16 logits carry their
 // information in the upper 16 bits.
@@ -209,8 +238,8 @@ __device__ __forceinline__ int block_extreme(int v, bool is_max, int* s_part) {
 // 16-bit key to keep from (0 keeps everything).  Returns false, leaving *tau,
 // when the row needs the radix descent: a non-finite maximum, fewer than K
 // elements in the window, or a top-p boundary below the window.
-template <typename Each>
-__device__ bool window_thresholds(Each&& each, int V, float mx, float T, bool use_k, int K,
+template <typename EachVec>
+__device__ bool window_thresholds(EachVec&& each_vec, int V, float mx, float T, bool use_k, int K,
                                   bool use_p, float Pp, unsigned int* s_hist, double* s_dpart,
                                   unsigned int* s_upart, int* s_ipart, uint32_t* tau) {
   if (!(mx > kNegInf && mx < 3.0e38f)) return false;
@@ -223,15 +252,30 @@ __device__ bool window_thresholds(Each&& each, int V, float mx, float T, bool us
   s_hist[2 * tid + 1] = 0u;
   __syncthreads();
   float below = 0.f;  // mass of this thread's elements below the window
-  each([&](bool ok, float x) {
-    const uint32_t k = trunc_key<BF16>(x);
-    const int hb = (int)(k >> 8);
-    if (ok && hb >= lo) {
-      atomicAdd(&s_hist[((hb - lo) << 8) | (int)(k & 0xffu)], 1u);
-    } else if (ok && use_p) {
-      below += fast_ex2(fmaf(x, c, -cm));
+  const uint32_t kb = (uint32_t)lo << 8;  // the window's lowest key
+  each_vec([&](bool ok, uint4 q) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t k2 = bf16x2_keys(w[j]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // the lower-addressed logit is the low half
+        const uint32_t k = h ? (k2 >> 16) : (k2 & 0xffffu);
+        if (ok && k >= kb) {
+          atomicAdd(&s_hist[k - kb], 1u);  // below 2048: no key exceeds the maximum's
+        } else if (ok && use_p) {
+          const float x = __uint_as_float(h ? (w[j] & 0xffff0000u) : (w[j] << 16));
+          below += fast_ex2(fmaf(x, c, -cm));
+        }
+      }
     }
   });
+  __syncthreads();
+  // -0 was keyed apart, just below +0: its count joins +0's, as equal logits
+  if (tid == 0 && kb <= 0x7fffu && 0x8000u - kb < (uint32_t)kWinKeys) {
+    s_hist[0x8000u - kb] += s_hist[0x7fffu - kb];
+    s_hist[0x7fffu - kb] = 0u;
+  }
   __syncthreads();
   // thread t holds window keys i0 = 2t and i1 = 2t + 1 (key = (lo << 8) + i)
   const int i0 = 2 * tid, i1 = i0 + 1;
@@ -369,6 +413,21 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
     // the radix descent's passes (register-heavy) keep one load in flight; the
     // window histogram's passes, kTruncLoads
     auto each = [&](auto&& f) { each_n(std::integral_constant<int, 1>{}, f); };
+    // visit every 16-byte vector of an aligned row: g(ok, q), kTruncLoads loads in
+    // flight per thread (past the row's end: ok false and q the -inf padding)
+    auto each_vec = [&](auto&& g) {
+      const uint4* rv = reinterpret_cast<const uint4*>(in);
+      for (int i0 = warp * 32; i0 < nvec; i0 += kTruncLoads * kTruncThreads) {
+        uint4 q[kTruncLoads];
+#pragma unroll
+        for (int u = 0; u < kTruncLoads; ++u) {
+          const int i = i0 + u * kTruncThreads + lane;
+          q[u] = i < nvec ? ld_stream(rv + i) : E::pad();
+        }
+#pragma unroll
+        for (int u = 0; u < kTruncLoads; ++u) g(i0 + u * kTruncThreads + lane < nvec, q[u]);
+      }
+    };
     auto each_deep = [&](auto&& f) {
       each_n(std::integral_constant<int, kFast ? kTruncLoads : 1>{}, f);
     };
@@ -399,11 +458,30 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       float mx = kNegInf;
       bool nan = false;
       const int shift0 = 8 * (kLevels - 1);
-      each_deep([&](bool ok, float x) {
-        nan |= ok && x != x;
-        mx = fmaxf(mx, x);
-        if (!kFast && use_k) count_add(s_whist[warp], ok, (int)(trunc_key<E>(x) >> shift0));
-      });
+      if constexpr (kFast) {
+        // packed keys, two logits a word: their largest and smallest (the -inf
+        // padding moves neither test)
+        uint32_t kmax = 0u, kmin = 0xffffffffu;
+        each_vec([&](bool, uint4 q) {
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t k2 = bf16x2_keys(w[j]);
+            kmax = max_u16x2(kmax, k2);
+            kmin = min_u16x2(kmin, k2);
+          }
+        });
+        const uint32_t kx = max(kmax & 0xffffu, kmax >> 16);
+        const uint32_t kn = min(kmin & 0xffffu, kmin >> 16);
+        nan = kx > 0xff80u || kn < 0x007fu;  // above +inf's key or below -inf's
+        mx = nan ? kNegInf : key_logit(kx);
+      } else {
+        each_deep([&](bool ok, float x) {
+          nan |= ok && x != x;
+          mx = fmaxf(mx, x);
+          if (use_k) count_add(s_whist[warp], ok, (int)(trunc_key<E>(x) >> shift0));
+        });
+      }
       if (__any_sync(0xffffffffu, nan) && lane == 0) s_nan = 1u;
       mx = warp_max(mx);
       if (lane == 0) s_red[warp] = mx;
@@ -420,7 +498,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       bool done = false;  // the thresholds were found by the window histogram
       if constexpr (kFast) {
         if (!copy) {
-          done = window_thresholds(each_deep, P.vocab, mx, T, use_k, K, use_p, Pp, s_hist, s_dpart,
+          done = window_thresholds(each_vec, P.vocab, mx, T, use_k, K, use_p, Pp, s_hist, s_dpart,
                                    s_upart, s_ipart, &tau);
           if (!done && use_k) {
             // the radix descent below starts from the level-0 counts
@@ -589,7 +667,23 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       }
     }
     // ---- output: the kept logits, -inf elsewhere (or the row as it is) ----------
-    if (kAligned) {
+    if constexpr (kFast) {
+      // packed: -0 keys just below +0 here, so a threshold at +0 moves below it
+      const uint4* rv = reinterpret_cast<const uint4*>(in);
+      uint4* ov = reinterpret_cast<uint4*>(out);
+      const uint32_t tk = tau == 0x8000u ? 0x7fffu : tau;
+      const uint32_t t2 = tk | (tk << 16);
+      for (int i = tid; i < nvec; i += kTruncThreads) {
+        uint4 q = ld_last_use(rv + i);
+        if (!copy) {
+          q.x = keep_bf16x2(q.x, t2);
+          q.y = keep_bf16x2(q.y, t2);
+          q.z = keep_bf16x2(q.z, t2);
+          q.w = keep_bf16x2(q.w, t2);
+        }
+        st_streaming(ov + i, q);
+      }
+    } else if (kAligned) {
       const uint4* rv = reinterpret_cast<const uint4*>(in);
       uint4* ov = reinterpret_cast<uint4*>(out);
       for (int i0 = tid; i0 < nvec; i0 += kOutLoads * kTruncThreads) {
