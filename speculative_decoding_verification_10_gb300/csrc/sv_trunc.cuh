@@ -26,7 +26,8 @@
 namespace sv {
 
 constexpr int kTruncThreads = 1024;
-constexpr int kTruncLoads = 4;  // 16-byte loads in flight per thread (window histogram passes)
+constexpr int kTruncLoads = 8;  // 16-byte loads in flight per thread (packed passes)
+constexpr int kPackedOutLoads = 1;  // ... and in the packed output pass
 constexpr int kOutLoads = 1;    // ... and in the output pass
 constexpr uint32_t kStBadTrunc = 1024u;
 
@@ -673,15 +674,26 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       uint4* ov = reinterpret_cast<uint4*>(out);
       const uint32_t tk = tau == 0x8000u ? 0x7fffu : tau;
       const uint32_t t2 = tk | (tk << 16);
-      for (int i = tid; i < nvec; i += kTruncThreads) {
-        uint4 q = ld_last_use(rv + i);
-        if (!copy) {
-          q.x = keep_bf16x2(q.x, t2);
-          q.y = keep_bf16x2(q.y, t2);
-          q.z = keep_bf16x2(q.z, t2);
-          q.w = keep_bf16x2(q.w, t2);
+      for (int i0 = tid; i0 < nvec; i0 += kPackedOutLoads * kTruncThreads) {
+        uint4 qs[kPackedOutLoads];
+#pragma unroll
+        for (int u = 0; u < kPackedOutLoads; ++u) {
+          const int i = i0 + u * kTruncThreads;
+          if (i < nvec) qs[u] = ld_last_use(rv + i);
         }
-        st_streaming(ov + i, q);
+#pragma unroll
+        for (int u = 0; u < kPackedOutLoads; ++u) {
+          const int i = i0 + u * kTruncThreads;
+          if (i >= nvec) break;
+          uint4 q = qs[u];
+          if (!copy) {
+            q.x = keep_bf16x2(q.x, t2);
+            q.y = keep_bf16x2(q.y, t2);
+            q.z = keep_bf16x2(q.z, t2);
+            q.w = keep_bf16x2(q.w, t2);
+          }
+          st_streaming(ov + i, q);
+        }
       }
     } else if (kAligned) {
       const uint4* rv = reinterpret_cast<const uint4*>(in);
