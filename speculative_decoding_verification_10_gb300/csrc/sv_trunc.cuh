@@ -12,11 +12,18 @@
 //   the output row holds the kept logits and -inf elsewhere, so softmax of it
 //   is the truncated, renormalised distribution and the verify round runs on
 //   it unchanged.
-// Both rules keep the logits at or above a threshold, found exactly by a radix
-// descent over order-preserving keys of the logits, 8 bits a level (2 levels
-// for bf16, 4 for fp32): top-k from element counts, top-p from masses
-// 2^(c (x - max)) held as 2^-40 fixed-point integers.  Counts and masses are
-// integer sums, so the threshold does not depend on the order of the atomics.
+// Both rules keep the logits at or above a threshold on order-preserving keys
+// of the logits, found exactly in one of two ways:
+//   bf16 rows with 16-byte vectors first take the window histogram: a bf16
+//     logit is fixed by its 16-bit key, so counts of the exact keys in the 8
+//     high-byte bins at and below the maximum's give top-k from counts and
+//     top-p from masses count * 2^(c (x_key - max)), summed in fp64 in a fixed
+//     order; these passes work on packed words, two logits at a time;
+//   other rows, and bf16 rows whose threshold lies below the window, take a
+//     radix descent, 8 bits a level (2 levels for bf16, 4 for fp32): top-k from
+//     element counts, top-p from masses held as 2^-40 fixed-point integers.
+// Counts and fixed-point masses are integer sums and the fp64 sums run in a
+// fixed order, so the threshold does not depend on the order of the atomics.
 // Rows of greedy requests (T = 0), rows holding NaN, and rows whose top_p is
 // NaN or <= 0 (which also sets SPECVERIFY_STATUS_BAD_TRUNC) are copied.
 #pragma once
