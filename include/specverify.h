@@ -379,10 +379,11 @@ int specverify_metrics(const int32_t *accepted_len, const int32_t *num_draft, in
  * K <= 0 or K >= V turns top-k off, P >= 1 turns top-p off; rows of greedy
  * requests (T = 0) and rows holding NaN are copied; a P NaN or <= 0 copies the
  * rows and sets SPECVERIFY_STATUS_BAD_TRUNC in *status (nullable device int32,
- * OR-ed).  The top-k threshold is exact; the top-p masses are fp32 2^(c x)
- * summed as 2^-40 fixed-point integers (independent of summation order), so a
- * top-p decision within about 1e-6 of its threshold can differ from an exact
- * computation.
+ * OR-ed).  The top-k threshold is exact.  The top-p masses are fp32 weights
+ * 2^(c (x - max)): for bf16 rows, one per exact logit value times its count,
+ * summed in fp64 in a fixed order; otherwise summed as 2^-40 fixed-point
+ * integers.  Neither depends on the order of atomics, and a top-p decision
+ * within about 1e-6 of its threshold can differ from an exact computation.
  * Layout as specverify_run: target_in/_out [batch + total_draft, vocab],
  * draft_in/_out [total_draft, vocab] (both NULL, or both given), dtype F32 or
  * BF16, device pointers on the current device; asynchronous on stream, one
