@@ -225,9 +225,12 @@ int specverify_run_host(specverify_t h, const void *target_logits, const void *d
 /*
  * specverify_run_static -- the verify round of specverify_run without a handle
  * and without allocating anything: no cudaMalloc/cudaFree, no allocating
- * library routine.  The pages have no counterpart of this entry point; it
- * exists for callers that must not allocate device memory (graph capture of a
- * fixed pool, allocator-free serving loops).
+ * library routine.  The pages have no counterpart of this entry point.  It is
+ * for callers that may not allocate device memory: a serving process that
+ * reserves all of the GPU's memory for its own pool at start-up (KV cache and
+ * weights), where a cudaMalloc would fail or steal from the pool, and
+ * embedding runtimes whose rules forbid allocation once they are serving,
+ * because an allocation can block on device-wide synchronisation.
  *
  * Scratch is one file-scope static device array of about 0.62 MiB, sized for
  * batch <= SPECVERIFY_STATIC_MAX_BATCH (256) and max_k <=
@@ -235,7 +238,8 @@ int specverify_run_host(specverify_t h, const void *target_logits, const void *d
  * on a device the call takes the array's address (cudaGetSymbolAddress,
  * checked), sizes the kernel grids, and clears the array on `stream` (its
  * completion counters must start at zero); later calls on that device reuse
- * them.  Every other piece of scratch is reset by the round itself.
+ * them.  Because that first call does this set-up, make it before any stream
+ * capture begins.  Every other piece of scratch is reset by the round itself.
  *
  * Arguments as specverify_run, plus device, max_k (width of committed_tokens
  * is max_k + 1; every num_draft must lie in [0, max_k]), vocab and dtype.

@@ -247,10 +247,13 @@ class Verifier:
 def verify_static(target, draft, tokens, num_draft, temperature, seed: int, max_k: int,
                   accepted_len, committed, flags, stream=None) -> None:
     """One verify round through specverify_run_static: no handle and no device
-    allocation (scratch is the library's static arena; batch <= 256, max_k <= 7).
-    Outputs go to the caller's tensors: accepted_len [B] int32, committed
-    [B, max_k + 1] int32, flags [sum k] uint8.  Calls that overlap in time race
-    on the arena: keep them on one stream."""
+    allocation (scratch is the library's static arena; batch <= 256, max_k <= 7),
+    for callers that may not allocate device memory, such as a server that has
+    reserved the GPU's memory for its own pool.  Outputs go to the caller's
+    tensors: accepted_len [B] int32, committed [B, max_k + 1] int32, flags
+    [sum k] uint8.  The first call on a device sets the arena up (takes its
+    address, clears it): make it before any stream capture begins.  Calls that
+    overlap in time race on the arena: keep them on one stream."""
     lib = _lib.load()
     dtype = "bf16" if target.dtype == torch.bfloat16 else "f32"
     code_dtype = _DTYPES[dtype][0]

@@ -1,5 +1,11 @@
 """specverify_run_static (no handle, no allocation) against the handle entry point.
 
+The static entry point serves callers that may not allocate device memory: a
+server that reserves the GPU's memory for its own pool at start-up, where a
+cudaMalloc would fail or eat into the pool, or a runtime that forbids
+allocation while serving because it can block on device-wide synchronisation.
+Its scratch is one static device array shared by every call.
+
 Collected last on purpose: it must pass both alone in a fresh process and after
 every other GPU test has used the library in the same process.
 """
