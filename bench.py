@@ -119,12 +119,36 @@ def measured_peak():
 ROUND_SOURCES = ("sv_device.cuh", "sv_kernels.cuh", "specverify.cu")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank space, so that an edit to a comment
+    leaves the hash of the code unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":  # a literal, copied as it is
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_10_gb300", "csrc")
     for name in ROUND_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update((name + "\n" + _code_only(f.read())).encode())
     return h.hexdigest()[:16]
 
 

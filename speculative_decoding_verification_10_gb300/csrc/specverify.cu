@@ -531,7 +531,11 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
 
 // ---------------------------------------------------------------------------
 // The static arena of specverify_run_static: a fixed-size device array, set up
-// once per device (its address, the kernel grids, zeroed counters).
+// on the first call on each device (its address, the kernel grids, zeroed
+// counters).  It serves callers that may not allocate device memory, such as a
+// server that has reserved the GPU's memory for its own pool; every GPU that
+// loads the library holds it until the process exits, and every call shares it
+// (calls that overlap in time race on it).
 // ---------------------------------------------------------------------------
 constexpr int kStaticMaxDevices = 64;
 constexpr size_t kStaticGrid = 1024;  // CTAs a wave of the static path may use
