@@ -84,10 +84,10 @@ def _load():
         lib.orc_verify.restype = ctypes.c_uint32
         lib.orc_race_keys.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_float,
                                       ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int,
-                                      ctypes.c_int, P, P]
+                                      ctypes.c_int, P]
         lib.orc_race_keys.restype = ctypes.c_int
         lib.orc_race_weights.argtypes = [P, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
-                                         ctypes.c_int, P, P]
+                                         ctypes.c_int, P]
         lib.orc_race_weights.restype = ctypes.c_int
         lib.orc_metrics.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
         lib.orc_metrics.restype = None
@@ -201,14 +201,10 @@ def verify(target, draft, tokens, num_draft, temperature, seed, max_k,
     return out
 
 
-RACE_BLOCK = 128
-
-
 def race_keys(target_row, draft_row, temperature, seed, request, position, kind):
-    """Keys of one request's correction/bonus draw.
+    """Keys E_v / w_v of one request's correction/bonus draw.
 
-    Returns (winner, block_keys[ceil(V/128)], elem_keys[V]); keys are +inf where
-    the mass or weight is not positive.
+    Returns (winner, keys[V]); keys are +inf where the weight is not positive.
     """
     lib = _load()
     t, dt = _logits(np.asarray(target_row).reshape(1, -1))
@@ -216,25 +212,22 @@ def race_keys(target_row, draft_row, temperature, seed, request, position, kind)
     if draft_row is not None:
         d, _ = _logits(np.asarray(draft_row).reshape(1, -1))
     vocab = t.shape[1]
-    bkeys = np.zeros((vocab + RACE_BLOCK - 1) // RACE_BLOCK, dtype=np.float64)
-    ekeys = np.zeros(vocab, dtype=np.float64)
+    keys = np.zeros(vocab, dtype=np.float64)
     winner = lib.orc_race_keys(dt, vocab, _ptr(t), _ptr(d), float(temperature),
                                int(seed) & (2**64 - 1), int(request) & (2**64 - 1),
-                               int(position), int(kind), _ptr(bkeys), _ptr(ekeys))
-    return int(winner), bkeys, ekeys
+                               int(position), int(kind), _ptr(keys))
+    return int(winner), keys
 
 
 def race_weights(weights, seed, request, position):
-    """The two-level race over explicit float64 weights: (winner, block_keys, elem_keys)."""
+    """The exponential race over explicit float64 weights: (winner, keys[V])."""
     lib = _load()
     w = np.ascontiguousarray(weights, dtype=np.float64)
     vocab = len(w)
-    bkeys = np.zeros((vocab + RACE_BLOCK - 1) // RACE_BLOCK, dtype=np.float64)
-    ekeys = np.zeros(vocab, dtype=np.float64)
+    keys = np.zeros(vocab, dtype=np.float64)
     winner = lib.orc_race_weights(_ptr(w), vocab, int(seed) & (2**64 - 1),
-                                  int(request) & (2**64 - 1), int(position), _ptr(bkeys),
-                                  _ptr(ekeys))
-    return int(winner), bkeys, ekeys
+                                  int(request) & (2**64 - 1), int(position), _ptr(keys))
+    return int(winner), keys
 
 
 def metrics(accepted_len, num_draft, max_k, hist=None, proposed=None, accepted=None):

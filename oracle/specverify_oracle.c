@@ -32,15 +32,14 @@
  *   (key = seed low word, seed high word) with the counter
  *       (floor(v/4), position, request low word, stream | request high << 8)
  *   and output word v mod 4.  Stream 0 gives the acceptance uniform of a
- *   position (v = 0); streams 1 and 2 the exponentials of the correction or
- *   bonus draw (stream 2 indexed by vocab block, stream 1 by vocab id).
+ *   position (v = 0); stream 1 the exponentials of the correction or bonus
+ *   draw, one per vocab id v.
  *     u      = (w >> 8) * 2^-24                 in [0, 1)       (exact in fp32)
  *     E      = -ln((w + 1/2) * 2^-32)           in (1.2e-10, 22.9)
- *   A categorical draw from weights w_v >= 0 is a two-level exponential race
- *   over fixed blocks of 128 consecutive vocab ids, lowest index on ties:
- *     block  b* = argmin_{b: W_b > 0} E2_b / W_b,   W_b = sum_{v in block b} w_v,
- *     token  v* = argmin_{v in b*, w_v > 0} E1_v / w_v.
- *   P(v* = v) = (W_b / W) (w_v / W_b) = w_v / W, so it draws exactly from w.
+ *   A categorical draw from weights w_v >= 0 is the exponential race
+ *     token  v* = argmin_{v: w_v > 0} E_v / w_v,   lowest index on ties,
+ *   E_v from the stream-1 word of vocab id v at the draw's (request,
+ *   position).  E_v / w_v ~ Exp(w_v), so P(v* = v) = w_v / sum_u w_u.
  */
 #include <math.h>
 #include <stddef.h>
@@ -185,67 +184,38 @@ int orc_argmax(const void *base, int dtype, size_t row, int vocab)
     return best;
 }
 
-#define ORC_RACE_BLOCK 128
-
-/* Two-level exponential race over weights w (length V), blocks of
- * ORC_RACE_BLOCK ids: the block race picks b* = argmin E2_b / W_b over blocks
- * with positive mass W_b, then the element race picks argmin E1_v / w_v over
- * the positive weights of b* (lowest index on ties at both levels).
- * block_keys_out [ceil(V/128)] and elem_keys_out [V] (nullable) receive every
- * key (+inf where the mass or weight is not positive).  *margin (nullable)
- * gets min(second/best - 1) over the two decisive comparisons.  Returns the
- * winner, or -1 when no weight is positive. */
+/* Exponential race over weights w (length V): the token is
+ *     v* = argmin_{v: w_v > 0} E_v / w_v,
+ * E_v the race exponential of the stream-1 word at (request, position, v),
+ * lowest index on ties.  With E_v iid Exp(1), E_v / w_v is exponential with
+ * rate w_v, so P(v* = v) = w_v / sum_u w_u: a categorical draw from w that
+ * needs no normalisation and does not depend on the order the ids are
+ * visited in.  keys_out [V] (nullable) receives every key (+inf where the
+ * weight is not positive); *margin (nullable) gets second / best - 1.
+ * Returns the winner, or -1 when no weight is positive. */
 static int race(const double *w, int vocab, uint64_t seed, uint64_t request, uint32_t position,
-                double *block_keys_out, double *elem_keys_out, double *margin)
+                double *keys_out, double *margin)
 {
-    const int nblocks = (vocab + ORC_RACE_BLOCK - 1) / ORC_RACE_BLOCK;
-    int best_b = -1;
-    double b1 = INFINITY, b2 = INFINITY;
-    for (int b = 0; b < nblocks; ++b) {
-        double mass = 0.0;
-        for (int v = b * ORC_RACE_BLOCK; v < vocab && v < (b + 1) * ORC_RACE_BLOCK; ++v)
-            if (w[v] > 0.0)
-                mass += w[v];
-        double key = INFINITY;
-        if (mass > 0.0)
-            key = orc_exponential(orc_random_word(seed, 2u, request, position, (uint32_t)b)) / mass;
-        if (block_keys_out)
-            block_keys_out[b] = key;
-        if (key < b1) {
-            b2 = b1;
-            b1 = key;
-            best_b = b;
-        } else if (key < b2) {
-            b2 = key;
-        }
-    }
-    if (elem_keys_out)
-        for (int v = 0; v < vocab; ++v)
-            elem_keys_out[v] = w[v] > 0.0
-                ? orc_exponential(orc_random_word(seed, 1u, request, position, (uint32_t)v)) / w[v]
-                : INFINITY;
-    if (best_b < 0) {
-        if (margin) *margin = INFINITY;
-        return -1;
-    }
     int winner = -1;
-    double e1 = INFINITY, e2 = INFINITY;
-    for (int v = best_b * ORC_RACE_BLOCK; v < vocab && v < (best_b + 1) * ORC_RACE_BLOCK; ++v) {
+    double best = INFINITY, second = INFINITY;
+    for (int v = 0; v < vocab; ++v) {
+        double key = INFINITY;
+        if (w[v] > 0.0)
+            key = orc_exponential(orc_random_word(seed, 1u, request, position, (uint32_t)v)) / w[v];
+        if (keys_out)
+            keys_out[v] = key;
         if (!(w[v] > 0.0))
             continue;
-        double key = orc_exponential(orc_random_word(seed, 1u, request, position, (uint32_t)v)) / w[v];
-        if (key < e1) {
-            e2 = e1;
-            e1 = key;
+        if (key < best) {
+            second = best;
+            best = key;
             winner = v;
-        } else if (key < e2) {
-            e2 = key;
+        } else if (key < second) {
+            second = key;
         }
     }
-    if (margin) {
-        double m1 = b2 / b1 - 1.0, m2 = e2 / e1 - 1.0;
-        *margin = m1 < m2 ? m1 : m2;
-    }
+    if (margin)
+        *margin = winner < 0 ? INFINITY : second / best - 1.0;
     return winner;
 }
 
@@ -408,7 +378,7 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
                     bad_row = 1;
                 } else {
                     orc_softmax(target_logits, dtype, tgt_off + k, vocab, temp, p);
-                    token = race(p, vocab, seed, req, (uint32_t)k, NULL, NULL, &gap);
+                    token = race(p, vocab, seed, req, (uint32_t)k, NULL, &gap);
                     if (race_kind) race_kind[r] = ORC_RACE_BONUS;
                 }
             } else if (!bad_row) {
@@ -419,12 +389,12 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
                 orc_softmax(draft_logits, dtype, drf_off + j, vocab, temp, q);
                 for (int v = 0; v < vocab; ++v)
                     w[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
-                token = race(w, vocab, seed, req, (uint32_t)j, NULL, NULL, &gap);
+                token = race(w, vocab, seed, req, (uint32_t)j, NULL, &gap);
                 if (token >= 0) {
                     if (race_kind) race_kind[r] = ORC_RACE_RESIDUAL;
                 } else {
                     /* p <= q everywhere means p == q: draw from p instead. */
-                    token = race(p, vocab, seed, req, (uint32_t)j, NULL, NULL, &gap);
+                    token = race(p, vocab, seed, req, (uint32_t)j, NULL, &gap);
                     if (race_kind) race_kind[r] = ORC_RACE_FALLBACK;
                 }
             }
@@ -466,14 +436,13 @@ uint32_t orc_verify(int dtype, int vocab, int batch, int max_k, int total_draft,
 
 /*
  * Keys of one request's correction/bonus draw, so a test can check any token:
- * block_keys [ceil(V/128)] and elem_keys [V] as in race().  kind:
- * ORC_RACE_BONUS or ORC_RACE_FALLBACK (weights p from target_row),
- * ORC_RACE_RESIDUAL (weights [p - q]_+ from target_row and draft_row).  Rows
- * are single rows [V].  Returns the winner.
+ * keys [V] as in race().  kind: ORC_RACE_BONUS or ORC_RACE_FALLBACK (weights
+ * p from target_row), ORC_RACE_RESIDUAL (weights [p - q]_+ from target_row and
+ * draft_row).  Rows are single rows [V].  Returns the winner.
  */
 int orc_race_keys(int dtype, int vocab, const void *target_row, const void *draft_row,
                   float temperature, uint64_t seed, uint64_t request, int position, int kind,
-                  double *block_keys, double *elem_keys)
+                  double *keys)
 {
     double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
     double *q = (double *)malloc(sizeof(double) * (size_t)vocab);
@@ -484,9 +453,9 @@ int orc_race_keys(int dtype, int vocab, const void *target_row, const void *draf
         orc_softmax(draft_row, dtype, 0, vocab, (double)temperature, q);
         for (int v = 0; v < vocab; ++v)
             w[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
-        winner = race(w, vocab, seed, request, (uint32_t)position, block_keys, elem_keys, NULL);
+        winner = race(w, vocab, seed, request, (uint32_t)position, keys, NULL);
     } else {
-        winner = race(p, vocab, seed, request, (uint32_t)position, block_keys, elem_keys, NULL);
+        winner = race(p, vocab, seed, request, (uint32_t)position, keys, NULL);
     }
     free(p);
     free(q);
@@ -496,9 +465,9 @@ int orc_race_keys(int dtype, int vocab, const void *target_row, const void *draf
 
 /* The race over explicit weights (for tests): returns the winner. */
 int orc_race_weights(const double *w, int vocab, uint64_t seed, uint64_t request, int position,
-                     double *block_keys, double *elem_keys)
+                     double *keys)
 {
-    return race(w, vocab, seed, request, (uint32_t)position, block_keys, elem_keys, NULL);
+    return race(w, vocab, seed, request, (uint32_t)position, keys, NULL);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -161,34 +161,69 @@ def test_planted_mistakes_fail_the_pins():
     assert not (dec == (u * p0[y[:2000]] < q0[y[:2000]])).all()
 
 
-def test_two_level_race_draws_from_the_weights():
-    """The block race then the element race draw token v with probability w_v / W:
-    checked over blocks with zero mass, a partial last block and zero weights."""
+def test_race_draws_from_the_weights():
+    """The exponential race draws token v with probability w_v / sum w over the
+    positive weights: checked with zero weights scattered through the row."""
     rng = np.random.default_rng(31)
-    V = 700                                       # blocks of 128: 5 full + one of 60 ids
+    V = 700
     w = rng.gamma(0.7, size=V)
-    w[128:256] = 0.0                              # a block without mass
+    w[128:256] = 0.0                              # a run of zero weights
     w[rng.choice(V, 50, replace=False)] = 0.0     # scattered zero weights
     n = 40_000
     draws = np.array([oracle.race_weights(w, seed=3, request=r, position=2)[0] for r in range(n)])
     assert not np.isin(draws, np.flatnonzero(w == 0)).any()
     assert _chi2_pvalue(np.bincount(draws, minlength=V), w / w.sum()) > 1e-3
-    # the block of the draw follows the block masses
-    mass = np.add.reduceat(w, np.arange(0, V, 128))
-    assert _chi2_pvalue(np.bincount(draws // 128, minlength=len(mass)), mass / mass.sum()) > 1e-3
 
 
-def test_two_level_race_keys_are_consistent():
-    """The winner is the lowest key of the winning block, and that block has the
-    lowest block key; the keys use E / w."""
-    rng = np.random.default_rng(5)
-    w = rng.gamma(0.5, size=1000)
-    winner, bk, ek = oracle.race_weights(w, seed=9, request=77, position=0)
-    b = int(np.argmin(bk))
-    assert winner // 128 == b
-    assert winner == b * 128 + int(np.argmin(ek[b * 128:(b + 1) * 128]))
-    word = oracle.random_word(9, 2, 77, 0, b)
-    assert bk[b] == pytest.approx(oracle.exponential(word) / w[b * 128:(b + 1) * 128].sum(),
-                                  rel=1e-12)
-    word = oracle.random_word(9, 1, 77, 0, winner)
-    assert ek[winner] == pytest.approx(oracle.exponential(word) / w[winner], rel=1e-15)
+def test_race_equal_weights_follow_the_words():
+    """Two ids of equal weight: E = -ln((word + 1/2) 2^-32) falls as the word
+    grows, so the id whose stream-1 word is larger has the smaller key and wins.
+    The words come from the Philox known-answer-pinned generator, keyed by the
+    vocab id itself; both orders occur over the requests."""
+    V, a, b = 40, 9, 22
+    w = np.zeros(V)
+    w[a] = w[b] = 0.37
+    seen = set()
+    for r in range(64):
+        wa = oracle.random_word(11, 1, r, 3, a)
+        wb = oracle.random_word(11, 1, r, 3, b)
+        winner, _ = oracle.race_weights(w, seed=11, request=r, position=3)
+        assert winner == (a if wa > wb else b), (r, wa, wb, winner)
+        seen.add(winner)
+    assert seen == {a, b}
+
+
+def test_race_tie_goes_to_the_lowest_index():
+    """Weights equal to the ids' own exponentials make every key exactly 1
+    (x / x is exact in IEEE arithmetic): the lowest of the tied ids wins,
+    whatever the words."""
+    V = 30
+    ids = [4, 17, 25]
+    for r in range(8):
+        w = np.zeros(V)
+        for v in ids:
+            w[v] = oracle.exponential(oracle.random_word(5, 1, r, 0, v))
+        winner, keys = oracle.race_weights(w, seed=5, request=r, position=0)
+        assert winner == ids[0]
+        assert (keys[ids] == 1.0).all()
+        # without the lowest, the next one takes it
+        w[ids[0]] = 0.0
+        assert oracle.race_weights(w, seed=5, request=r, position=0)[0] == ids[1]
+
+
+def test_race_is_invariant_to_scale_and_keyed_by_vocab_id():
+    """Normalisation does not change the winner (power-of-two scales are exact),
+    and the key of id v depends only on v, not on the other weights: zeroing
+    every other id but the winner and one rival leaves the winner in place."""
+    rng = np.random.default_rng(8)
+    w = rng.gamma(0.5, size=500)
+    winner, keys = oracle.race_weights(w, seed=9, request=77, position=1)
+    assert oracle.race_weights(w * 2.0 ** -40, seed=9, request=77, position=1)[0] == winner
+    assert oracle.race_weights(w * 2.0 ** 30, seed=9, request=77, position=1)[0] == winner
+    rival = int(np.argsort(keys)[1])
+    w2 = np.zeros_like(w)
+    w2[[winner, rival]] = w[[winner, rival]]
+    win2, keys2 = oracle.race_weights(w2, seed=9, request=77, position=1)
+    assert win2 == winner
+    assert keys2[winner] == keys[winner] and keys2[rival] == keys[rival]
+    assert np.isinf(keys2[np.flatnonzero(w2 == 0)]).all()
