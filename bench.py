@@ -65,7 +65,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--host-reads", default="auto", choices=["auto", "stage"],
                     help="e2e: read pinned host logits in place (auto) or copy them in (stage)")
-    ap.add_argument("--schedule", default="auto", choices=["auto", "waves", "clusters", "stream"],
+    ap.add_argument("--schedule", default="auto", choices=["auto", "waves"],
                     help="launch layout of a round (results do not depend on it)")
     ap.add_argument("--depth", type=int, default=0,
                     help="positions per wave launch (0 = chosen per run)")
@@ -321,9 +321,8 @@ def measure_e2e(args, b, v, world, dev):
     in_place = v.last_host_reads() == 1
     if in_place:
         # the kernels read the rows of every wave a request takes part in where
-        # they lie; the wave schedule copies each sampled row to the device as
-        # it streams, so a correction draw reads its two rows from there (the
-        # other schedules read them from the host again)
+        # they lie; the waves copy each sampled row to the device as it
+        # streams, so a correction draw reads its two rows from there
         depth = v.wave_depth(b.batch)
         A = h_acc.numpy().astype(np.int64)
         k = h_nd.numpy().astype(np.int64)
@@ -331,8 +330,6 @@ def measure_e2e(args, b, v, world, dev):
         last = np.minimum(k, (A // depth + 1) * depth - 1)
         rows = np.where(sampling, 2 * np.minimum(last + 1, k) + (last == k),
                         last + 1)
-        if args.schedule not in ("auto", "waves"):
-            rows = rows + np.where(sampling & (A < k), 2, 0)
         logits = int(rows.sum()) * b.vocab * h_target.element_size()
     else:
         logits = h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()

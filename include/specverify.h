@@ -27,12 +27,14 @@
  *     taking output word v mod 4.  Stream 0, v = 0: acceptance uniform
  *     u = (word >> 8) * 2^-24.  Stream 1: race exponentials
  *     E_v = -ln((word + 1/2) * 2^-32).
- *   - Every categorical draw is the exponential race argmin_{w_v>0} E_v / w_v
- *     (lowest index on ties), so the result does not depend on how the
- *     vocabulary is split across threads.  Correction: w = [p_j - q_j]_+ at
- *     position j = A and Philox position j; if that residual has no mass the
- *     draw is made from p_j with the same exponentials.  Bonus: w = p_k at
- *     position k.
+ *   - Every categorical draw is one exponential race over the vocabulary:
+ *       token = argmin_{v: w_v > 0} E_v / w_v   (lowest index on ties),
+ *     E_v from the stream-1 word of vocab id v itself (counter floor(v/4),
+ *     word v mod 4) at the draw's position and request.  The result does not
+ *     depend on how the vocabulary is split across threads.  Correction:
+ *     w = [p_j - q_j]_+ at position j = A (Philox position j); if that
+ *     residual has no mass the draw is made from p_j with the same
+ *     exponentials.  Bonus: w = p_k at position k.
  *   - "request" is the batch index r unless request ids are given.
  *
  * Data layout (row-major, one row = V logits of one position):
@@ -94,12 +96,9 @@ typedef enum {
 #define SPECVERIFY_STATUS_BAD_TOTAL 16    /* sum of num_draft != total_draft: batch skipped */
 #define SPECVERIFY_STATUS_BAD_PARENT 32   /* tree: a parent outside [-1, node index): request skipped */
 #define SPECVERIFY_STATUS_NO_DRAFT 64     /* T > 0 and k > 0 but draft_logits is NULL: request skipped */
-#define SPECVERIFY_STATUS_OVERRUN 128     /* internal: a cluster launch hit its unit cap (a bug); outputs incomplete */
 #define SPECVERIFY_STATUS_BAD_CONF 512    /* trimmed run: a confidence NaN or outside [0, 1], or a NaN cost:
                                              request skipped */
 #define SPECVERIFY_STATUS_BAD_TRUNC 1024  /* truncation: a top_p NaN or <= 0 (its rows copied) */
-#define SPECVERIFY_STATUS_TIMEOUT 256     /* stream schedule: a bounded wait ran out (a bug, or the GPU
-                                             was held by other work for seconds); outputs incomplete */
 
 /* Flags for specverify_create_ex. */
 #define SPECVERIFY_CREATE_HOST_STAGING 1  /* allocate device staging for specverify_run_host */
@@ -264,6 +263,21 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
 int specverify_status(specverify_t h, int32_t *status_out);
 
 /*
+ * Round tags (test aid).  Each round tags its completion counters with a
+ * 32-bit round number; before the number would wrap past 2^32 - 1 the
+ * counters are cleared on the round's stream and numbering restarts at 1, so
+ * a handle (or the static arena) serves any number of rounds.  These calls let
+ * a test reach the wrap quickly: they wait for the device, clear the counters
+ * and set the number the last round had, so the next round is tagged
+ * epoch + 1 (epoch = 0xffffffff makes the next round clear and restart).
+ * specverify_static_debug_set_epoch needs a completed specverify_run_static
+ * on `device` (the arena's set-up) and returns SPECVERIFY_ERR_INVALID_ARG
+ * before it.  Not for use while rounds are in flight.
+ */
+int specverify_debug_set_epoch(specverify_t h, uint32_t epoch);
+int specverify_static_debug_set_epoch(int device, uint32_t epoch);
+
+/*
  * specverify_set_timing_events -- measurement aid.  After this call, run number
  * i (counting from 0) records start_events[i % n] on its stream just before its
  * first launch and stop_events[i % n] just after its last.  The arrays hold cudaEvent_t values created
@@ -292,20 +306,11 @@ int specverify_wave_depth(specverify_t h, int batch, int *depth_out);
  * not depend on it.
  *   SPECVERIFY_SCHEDULE_WAVES: a wave launch per group of `depth` positions
  *     (specverify_set_depth), every request in lockstep;
- *   SPECVERIFY_SCHEDULE_CLUSTERS: one launch of thread-block clusters, each
- *     taking requests one at a time and deciding each position as soon as its
- *     rows are read (16-byte aligned rows only; others use waves);
- *   SPECVERIFY_SCHEDULE_STREAM: one persistent launch whose CTAs take the
- *     rows from a queue that the decisions feed, in bands that every CTA
- *     splits alike; the correction draw re-reads its rows two or three bands
- *     later, from L2 (16-byte aligned rows only; others use waves);
- *   SPECVERIFY_SCHEDULE_AUTO (default): waves (the faster layout on every
- *     batch measured so far).
+ *   SPECVERIFY_SCHEDULE_AUTO (default): waves.
+ * Any other value returns SPECVERIFY_ERR_INVALID_ARG.
  */
 #define SPECVERIFY_SCHEDULE_AUTO 0
 #define SPECVERIFY_SCHEDULE_WAVES 1
-#define SPECVERIFY_SCHEDULE_CLUSTERS 2
-#define SPECVERIFY_SCHEDULE_STREAM 3
 int specverify_set_schedule(specverify_t h, int schedule);
 
 /*

@@ -58,6 +58,59 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _check_inputs(target, draft, tokens, num_draft, temperature, torch_dtype, device, vocab):
+    """Dtypes, devices, contiguity and shapes of a round's inputs (raises before
+    anything reaches the library)."""
+    if not isinstance(target, torch.Tensor) or target.dtype != torch_dtype:
+        raise TypeError(f"target logits must be a {torch_dtype} tensor")
+    if draft is not None and draft.numel() and draft.dtype != torch_dtype:
+        raise TypeError(f"draft logits must be {torch_dtype}")
+    for name, t, dt in (("draft_tokens", tokens, torch.int32),
+                        ("num_draft", num_draft, torch.int32),
+                        ("temperature", temperature, torch.float32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}")
+    for t in (target, draft, tokens, num_draft, temperature):
+        if t is not None and t.numel() and (t.device != device or not t.is_contiguous()):
+            raise ValueError("inputs must be contiguous tensors on the handle's device")
+    if target.dim() != 2 or target.shape[1] != vocab:
+        raise ValueError(f"target logits must be [rows, {vocab}]")
+    if tokens.dim() != 1 or num_draft.dim() != 1 or temperature.dim() != 1:
+        raise ValueError("draft_tokens, num_draft and temperature must be 1-D")
+    batch, total = int(num_draft.shape[0]), int(tokens.shape[0])
+    if temperature.shape[0] != batch:
+        raise ValueError("temperature must have one entry per request")
+    if batch and target.shape[0] < batch + total:
+        raise ValueError("target logits need sum(k_r + 1) rows")
+    if draft is not None and draft.numel() and (draft.dim() != 2 or draft.shape[1] != vocab
+                                                or draft.shape[0] < total):
+        raise ValueError(f"draft logits must be [sum(k_r), {vocab}]")
+
+
+def _check_outputs(accepted_len, committed, flags, batch, total_draft, max_k, device):
+    """Outputs must be contiguous int32 / int32 / uint8 tensors on the device,
+    at least [batch], [batch, max_k + 1] and [total_draft] long: the kernels
+    write that much."""
+    for name, t, dt, n in (("accepted_len", accepted_len, torch.int32, batch),
+                           ("committed", committed, torch.int32, batch * (max_k + 1)),
+                           ("flags", flags, torch.uint8, total_draft)):
+        if not isinstance(t, torch.Tensor) or t.dtype != dt:
+            raise TypeError(f"{name} must be a {dt} tensor")
+        if t.numel() and (t.device != device or not t.is_contiguous()):
+            raise ValueError(f"{name} must be contiguous on the inputs' device")
+        if t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements, the round writes {n}")
+    if committed.dim() != 2 or committed.shape[1] != max_k + 1:
+        raise ValueError(f"committed must be [batch, {max_k + 1}]")
+
+
+def _stream_of(stream, device):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    if s.device != device:
+        raise ValueError("the stream must belong to the inputs' device")
+    return ctypes.c_void_p(s.cuda_stream)
+
+
 class Verifier:
     """Owns one library handle (scratch memory sized at construction)."""
 
@@ -80,24 +133,11 @@ class Verifier:
 
     # -- helpers --------------------------------------------------------------
     def _stream(self, stream):
-        s = torch.cuda.current_stream(self.device) if stream is None else stream
-        return ctypes.c_void_p(s.cuda_stream)
+        return _stream_of(stream, self.device)
 
     def _check_inputs(self, target, draft, tokens, num_draft, temperature):
-        if target.dtype != self.torch_dtype:
-            raise TypeError(f"target logits must be {self.torch_dtype}")
-        if draft is not None and draft.numel() and draft.dtype != self.torch_dtype:
-            raise TypeError(f"draft logits must be {self.torch_dtype}")
-        for name, t, dt in (("draft_tokens", tokens, torch.int32),
-                            ("num_draft", num_draft, torch.int32),
-                            ("temperature", temperature, torch.float32)):
-            if t.dtype != dt:
-                raise TypeError(f"{name} must be {dt}")
-        for t in (target, draft, tokens, num_draft, temperature):
-            if t is not None and t.numel() and (t.device != self.device or not t.is_contiguous()):
-                raise ValueError("inputs must be contiguous tensors on the handle's device")
-        if target.dim() != 2 or target.shape[1] != self.vocab:
-            raise ValueError(f"target logits must be [rows, {self.vocab}]")
+        _check_inputs(target, draft, tokens, num_draft, temperature, self.torch_dtype,
+                      self.device, self.vocab)
 
     def outputs(self, batch: int, total_draft: int, debug: bool = False) -> VerifyResult:
         """Allocate output tensors for a batch (run() does this when none are given)."""
@@ -123,6 +163,8 @@ class Verifier:
             total_draft = int(tokens.shape[0])
         if out is None:
             out = self.outputs(batch, total_draft, debug=debug)
+        _check_outputs(out.accepted_len, out.committed, out.flags, batch, total_draft,
+                       self.max_k, self.device)
         if request_ids is not None and (request_ids.dtype != torch.int64
                                         or request_ids.device != self.device):
             raise TypeError("request_ids must be int64 on the handle's device")
@@ -190,9 +232,8 @@ class Verifier:
         return int(n.value)
 
     def set_schedule(self, schedule: str):
-        """'auto', 'waves', 'clusters' or 'stream' (see specverify_set_schedule)."""
-        code = {"auto": _lib.SCHEDULE_AUTO, "waves": _lib.SCHEDULE_WAVES,
-                "clusters": _lib.SCHEDULE_CLUSTERS, "stream": _lib.SCHEDULE_STREAM}[schedule]
+        """'auto' or 'waves' (see specverify_set_schedule)."""
+        code = {"auto": _lib.SCHEDULE_AUTO, "waves": _lib.SCHEDULE_WAVES}[schedule]
         _check(self.lib.specverify_set_schedule(self._h, code), "specverify_set_schedule")
 
     def set_host_reads(self, mode: str):
@@ -215,6 +256,12 @@ class Verifier:
         _check(self.lib.specverify_last_host_reads(self._h, ctypes.byref(out)),
                "specverify_last_host_reads")
         return out.value
+
+    def debug_set_epoch(self, epoch: int) -> None:
+        """Test aid: the round tag of the last round (see specverify_debug_set_epoch);
+        the next round is tagged epoch + 1, wrapping to a cleared restart."""
+        _check(self.lib.specverify_debug_set_epoch(self._h, int(epoch) & 0xffffffff),
+               "specverify_debug_set_epoch")
 
     def set_depth(self, depth: int):
         """Positions per wave launch: 1 .. max_k + 1, or 0 to choose per run."""
@@ -255,17 +302,35 @@ def verify_static(target, draft, tokens, num_draft, temperature, seed: int, max_
     address, clears it): make it before any stream capture begins.  Calls that
     overlap in time race on the arena: keep them on one stream."""
     lib = _lib.load()
+    if not isinstance(target, torch.Tensor) or target.dtype not in (torch.bfloat16,
+                                                                      torch.float32):
+        raise TypeError("target logits must be a bfloat16 or float32 tensor")
     dtype = "bf16" if target.dtype == torch.bfloat16 else "f32"
-    code_dtype = _DTYPES[dtype][0]
+    code_dtype, torch_dtype = _DTYPES[dtype]
     dev = target.device
-    s = torch.cuda.current_stream(dev) if stream is None else stream
+    if dev.type != "cuda":
+        raise ValueError("verify_static takes CUDA tensors")
+    if target.dim() != 2:
+        raise ValueError("target logits must be [rows, vocab]")
+    _check_inputs(target, draft, tokens, num_draft, temperature, torch_dtype, dev,
+                  int(target.shape[1]))
+    _check_outputs(accepted_len, committed, flags, int(num_draft.shape[0]),
+                   int(tokens.shape[0]), int(max_k), dev)
+    s = _stream_of(stream, dev)
     d = draft if (draft is not None and draft.numel()) else None
     code = lib.specverify_run_static(
         dev.index, int(max_k), int(target.shape[1]), code_dtype, _ptr(target), _ptr(d),
         _ptr(tokens), _ptr(num_draft), _ptr(temperature), int(seed) & (2**64 - 1),
         int(num_draft.shape[0]), int(tokens.shape[0]), _ptr(accepted_len), _ptr(committed),
-        _ptr(flags), ctypes.c_void_p(s.cuda_stream))
+        _ptr(flags), s)
     _check(code, "specverify_run_static")
+
+
+def static_debug_set_epoch(device: int, epoch: int) -> None:
+    """Test aid: the round tag of the static arena on `device` (see
+    specverify_static_debug_set_epoch); needs one verify_static call first."""
+    _check(_lib.load().specverify_static_debug_set_epoch(int(device), int(epoch) & 0xffffffff),
+           "specverify_static_debug_set_epoch")
 
 
 def verify(target, draft, tokens, num_draft, temperature, seed: int, max_k: int | None = None,

@@ -23,8 +23,6 @@ ERR_TOO_LARGE = -6
 
 SCHEDULE_AUTO = 0
 SCHEDULE_WAVES = 1
-SCHEDULE_CLUSTERS = 2
-SCHEDULE_STREAM = 3
 
 HOST_READS_AUTO = 0
 HOST_READS_STAGE = 1
@@ -91,6 +89,10 @@ def load(path: str | None = None):
     lib.specverify_run_static.argtypes = [I, I, I, I, P, P, P, P, P, ctypes.c_uint64, I, I,
                                           P, P, P, P]
     lib.specverify_run_static.restype = I
+    lib.specverify_debug_set_epoch.argtypes = [P, ctypes.c_uint32]
+    lib.specverify_debug_set_epoch.restype = I
+    lib.specverify_static_debug_set_epoch.argtypes = [I, ctypes.c_uint32]
+    lib.specverify_static_debug_set_epoch.restype = I
     lib.specverify_set_schedule.argtypes = [P, I]
     lib.specverify_set_schedule.restype = I
     lib.specverify_set_depth.argtypes = [P, I]

@@ -15,9 +15,8 @@
 #include <new>
 
 #include "specverify.h"
-#include "sv_cluster.cuh"
+#include "sv_kernels.cuh"
 #include "sv_metrics.cuh"
-#include "sv_stream.cuh"
 #include "sv_tree.cuh"
 #include "sv_trunc.cuh"
 
@@ -43,40 +42,25 @@ struct DeviceGuard {
 
 // ---------------------------------------------------------------------------
 // Scratch: byte offsets of every piece, sized for `mb` requests, positions
-// 0..max_k, every wave depth 1..max_k+1 and a grid of at most `grid` CTAs;
-// with `stream`, also the bands and ready tags of the stream schedule.
+// 0..max_k, every wave depth 1..max_k+1 and a grid of at most `grid` CTAs.
 // ---------------------------------------------------------------------------
+// The epoch-tagged completion counters come first, so that one memset of
+// `tagged` bytes clears them all.
 struct ScratchLayout {
   size_t lists, lcnt, res, rcnt, pos, rescnt, part, rpart, ctr, recs, rdy;
-  size_t bands, ready_n, ready_u, spart, srpart;
-  size_t list_entries, band_cap, bytes;
+  size_t list_entries, tagged, bytes;
 };
 
-// Fewest race blocks in one CTA's share of a wave or band: rows and residual
+// Fewest vocab blocks in one CTA's share of a wave: rows and residual
 // row pairs (each CTA streams at least 16 KB of a split).
 int min_span_blocks(int elem_bytes) {
-  return std::max(1, sv::kMinSpanBytes / (sv::kRaceBlock * elem_bytes));
+  return std::max(1, sv::kMinSpanBytes / (sv::kVocabBlock * elem_bytes));
 }
 int min_span_res_blocks(int elem_bytes) {
-  return std::max(1, sv::kMinSpanBytes / (2 * sv::kRaceBlock * elem_bytes));
+  return std::max(1, sv::kMinSpanBytes / (2 * sv::kVocabBlock * elem_bytes));
 }
 
-// Most segments a flat split cuts one entry of nb race blocks into: shares
-// are at least `span` blocks long, so at most (nb - 1) / span share
-// boundaries fall inside the entry.
-constexpr size_t max_segments(size_t nb, size_t span) { return (nb - 1) / span + 2; }
-
-// Segment counts of the stream schedule's per-entry partial slots.
-struct StreamSegs {
-  size_t rows, res;
-};
-
-// Bands a stream round can form: each holds at least one queue entry, and a
-// round queues at most (2 max_k + 1) rows and one residual per request.
-constexpr size_t stream_band_cap(size_t mb, int max_k) { return (2 * (size_t)max_k + 2) * mb + 2; }
-
-constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid, bool stream,
-                                       StreamSegs segs = StreamSegs{0, 0}) {
+constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid) {
   size_t list_entries = 0, max_waves = 0, max_cap = 0;
   for (int d = 1; d <= max_k + 1; ++d) {
     const size_t w = (size_t)sv::wave_count(max_k, d), cap = 2 * (size_t)d * mb;
@@ -86,6 +70,13 @@ constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid, bool s
   }
   ScratchLayout L{};
   size_t off = 0;
+  L.pos = off;
+  off = align_up(off + sizeof(unsigned long long) * ((size_t)max_k + 1) * mb, 256);
+  L.rescnt = off;
+  off = align_up(off + sizeof(unsigned long long) * mb, 256);
+  L.rdy = off;
+  off = align_up(off + sizeof(unsigned long long) * max_waves * mb, 256);
+  L.tagged = off;
   L.lists = off;
   off = align_up(off + sizeof(sv::Entry) * list_entries, 256);
   L.lcnt = off;
@@ -94,10 +85,6 @@ constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid, bool s
   off = align_up(off + sizeof(sv::ResEntry) * max_waves * mb, 256);
   L.rcnt = off;
   off = align_up(off + sizeof(int) * max_waves, 256);
-  L.pos = off;
-  off = align_up(off + sizeof(unsigned long long) * ((size_t)max_k + 1) * mb, 256);
-  L.rescnt = off;
-  off = align_up(off + sizeof(unsigned long long) * mb, 256);
   L.part = off;
   off = align_up(off + sizeof(sv::Partial) * (grid + max_cap), 256);
   L.rpart = off;
@@ -106,22 +93,7 @@ constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid, bool s
   off = align_up(off + sizeof(int) * sv::kCntCount, 256);
   L.recs = off;
   off = align_up(off + sizeof(sv::PosRec) * ((size_t)max_k + 1) * mb, 256);
-  L.rdy = off;
-  off = align_up(off + sizeof(unsigned long long) * max_waves * mb, 256);
   L.list_entries = list_entries;
-  L.band_cap = stream ? stream_band_cap(mb, max_k) : 0;
-  L.bands = off;
-  off = align_up(off + sizeof(sv::Band) * L.band_cap, 256);
-  // a stream round queues at most 2 max_k + 1 rows per request
-  const size_t stream_entries = (2 * (size_t)max_k + 1) * mb;
-  L.ready_n = off;
-  off = align_up(off + (stream ? sizeof(uint32_t) * stream_entries : 0), 256);
-  L.ready_u = off;
-  off = align_up(off + (stream ? sizeof(uint32_t) * mb : 0), 256);
-  L.spart = off;
-  off = align_up(off + (stream ? sizeof(sv::Partial) * stream_entries * segs.rows : 0), 256);
-  L.srpart = off;
-  off = align_up(off + (stream ? sizeof(sv::Partial) * mb * segs.res : 0), 256);
   L.bytes = off;
   return L;
 }
@@ -138,12 +110,8 @@ struct Scratch {
   int* ctr;
   sv::PosRec* recs;
   unsigned long long* rdy;  // epoch-tagged: must start at zero
-  sv::Band* bands;     // epoch-tagged: must start at zero (stream schedule only)
-  uint32_t* ready_n;   // epoch tags: must start at zero (stream schedule only)
-  uint32_t* ready_u;
-  sv::Partial* spart;
-  sv::Partial* srpart;
-  int band_cap;
+  char* tagged;             // the epoch-tagged counters above, one block
+  size_t tagged_bytes;
 };
 
 Scratch scratch_at(char* b, const ScratchLayout& L) {
@@ -159,12 +127,8 @@ Scratch scratch_at(char* b, const ScratchLayout& L) {
   s.ctr = reinterpret_cast<int*>(b + L.ctr);
   s.recs = reinterpret_cast<sv::PosRec*>(b + L.recs);
   s.rdy = reinterpret_cast<unsigned long long*>(b + L.rdy);
-  s.band_cap = (int)L.band_cap;
-  s.bands = L.band_cap ? reinterpret_cast<sv::Band*>(b + L.bands) : nullptr;
-  s.ready_n = L.band_cap ? reinterpret_cast<uint32_t*>(b + L.ready_n) : nullptr;
-  s.ready_u = L.band_cap ? reinterpret_cast<uint32_t*>(b + L.ready_u) : nullptr;
-  s.spart = L.band_cap ? reinterpret_cast<sv::Partial*>(b + L.spart) : nullptr;
-  s.srpart = L.band_cap ? reinterpret_cast<sv::Partial*>(b + L.srpart) : nullptr;
+  s.tagged = b;
+  s.tagged_bytes = L.tagged;
   return s;
 }
 
@@ -180,15 +144,11 @@ const void* wave_kernel(bool aligned, bool three) {
 }
 
 // Grids on the current device, every CTA resident at once: the wave kernels
-// (aligned and scalar rows) and the cluster kernel (clusters of cluster_n).
+// (aligned and scalar rows).
 struct KernelShape {
   int grid_aligned, grid_scalar;    // the wave kernel built for two CTAs per SM
   int grid3_aligned, grid3_scalar;  // ... and for three
-  int grid_cluster, cluster_n;
-  int grid_stream;
 };
-
-constexpr int kClusterN = 8;  // CTAs per cluster (portable size)
 
 bool kernel_shape(int device, int dtype, KernelShape* out) {
   int sms = 0;
@@ -212,57 +172,16 @@ bool kernel_shape(int device, int dtype, KernelShape* out) {
   out->grid_aligned = occ[1] * sms;
   out->grid3_scalar = occ[2] * sms;
   out->grid3_aligned = occ[3] * sms;
-  // the cluster kernel: as many clusters as fit at once
-  const void* fc = dtype == SPECVERIFY_BF16 ? reinterpret_cast<const void*>(sv::sv_cluster<sv::BF16>)
-                                            : reinterpret_cast<const void*>(sv::sv_cluster<sv::F32>);
-  if (cudaFuncSetAttribute(fc, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-      cudaFuncSetAttribute(fc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_bytes()) !=
-          cudaSuccess)
-    return false;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(kClusterN * sms));
-  cfg.blockDim = dim3(sv::kBlock);
-  cfg.dynamicSmemBytes = ring_bytes();
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kClusterN;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, fc, &cfg) != cudaSuccess || clusters < 1)
-    return false;
-  out->cluster_n = kClusterN;
-  out->grid_cluster = clusters * kClusterN;
-  // the stream kernel: every CTA resident at once (its CTAs wait on one another)
-  const void* fs = dtype == SPECVERIFY_BF16 ? reinterpret_cast<const void*>(sv::sv_stream<sv::BF16>)
-                                            : reinterpret_cast<const void*>(sv::sv_stream<sv::F32>);
-  int occ_s = 0;
-  if (cudaFuncSetAttribute(fs, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-      cudaFuncSetAttribute(fs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_bytes()) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_s, fs, sv::kBlock, ring_bytes()) !=
-          cudaSuccess ||
-      occ_s < 1)
-    return false;
-  out->grid_stream = occ_s * sms;
   return true;
 }
 
 // What a round needs besides its arguments.
 struct RunConfig {
   int device, max_batch, max_k, vocab, dtype, elem_bytes;
-  int depth_setting;     // 0: chosen per run from the batch size
-  int schedule_setting;  // SPECVERIFY_SCHEDULE_*
+  int depth_setting;  // 0: chosen per run from the batch size
   KernelShape shape;
   Scratch sc;
 };
-
-// Largest handle scratch that still carries the stream schedule's arrays.
-constexpr size_t kStreamScratchCap = (size_t)512 << 20;
 
 // Batches whose whole verify window (every row of every position) is at most
 // kShallowBytes are verified in one wave of all positions: reading rows past a
@@ -290,21 +209,6 @@ bool wave_three(const RunConfig& c, int batch) {
   return window <= kShallowBytes;
 }
 
-// Cluster launch or waves: waves unless clusters are asked for (and the rows
-// are 16-byte aligned).  Measured on GB300 the wave launches are faster on
-// every workload so far, so they are the default.
-bool run_clusters(const RunConfig& c, int batch, bool aligned) {
-  (void)batch;
-  return aligned && c.schedule_setting == SPECVERIFY_SCHEDULE_CLUSTERS;
-}
-
-// The stream launch: asked for, with 16-byte aligned rows and scratch that
-// has the bands.
-bool run_stream(const RunConfig& c, int batch, bool aligned) {
-  (void)batch;
-  return aligned && c.sc.bands != nullptr && c.schedule_setting == SPECVERIFY_SCHEDULE_STREAM;
-}
-
 bool rows_aligned(const RunConfig& c, const void* target, const void* draft) {
   return ((size_t)c.vocab * c.elem_bytes) % 16 == 0 && ((uintptr_t)target & 15u) == 0 &&
          ((uintptr_t)draft & 15u) == 0;
@@ -327,57 +231,13 @@ cudaError_t launch_wave(K kernel, int grid, size_t smem, cudaStream_t s, const s
   return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 
-// The cluster launch after the plan: clusters of kClusterN CTAs, programmatic
-// dependent launch on the plan.
-template <typename E>
-cudaError_t launch_cluster(const RunConfig& c, cudaStream_t s, const sv::Params& P) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)c.shape.grid_cluster);
-  cfg.blockDim = dim3(sv::kBlock);
-  cfg.dynamicSmemBytes = ring_bytes();
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)c.shape.cluster_n;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, sv::sv_cluster<E>, P);
-}
-
-// The stream launch after the plan (programmatic dependent launch on it).
-template <typename E>
-cudaError_t launch_stream(const RunConfig& c, cudaStream_t s, const sv::Params& P) {
-  return launch_wave(sv::sv_stream<E>, c.shape.grid_stream, ring_bytes(), s, P);
-}
-
-// One round: the plan launch, then the stream launch, the cluster launch or
-// the waves (a wave with nothing to do returns at once), optionally bracketed
-// by two events.
+// One round: the plan launch, then the waves (a wave with nothing to do
+// returns at once), optionally bracketed by two events.
 template <typename E>
 int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
                  cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (ev_start && cudaEventRecord(ev_start, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
   sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
-  if (P.stream_mode) {
-    if (launch_stream<E>(c, s, P) != cudaSuccess) {
-      cudaGetLastError();
-      return SPECVERIFY_ERR_CUDA;
-    }
-    if (ev_stop && cudaEventRecord(ev_stop, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
-  }
-  if (P.cluster_mode) {
-    if (launch_cluster<E>(c, s, P) != cudaSuccess) {
-      cudaGetLastError();
-      return SPECVERIFY_ERR_CUDA;
-    }
-    if (ev_stop && cudaEventRecord(ev_stop, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;
-  }
   const size_t smem = aligned ? ring_bytes() : 0;
   const bool three = wave_three(c, P.batch);
   const int grid = three ? (aligned ? c.shape.grid3_aligned : c.shape.grid3_scalar)
@@ -443,6 +303,23 @@ int check_args(const RunConfig& c, const RunArgs& a) {
   return SPECVERIFY_OK;
 }
 
+// The tag of the next round.  Tags run 1, 2, ..., 2^32 - 1; a counter last
+// raised in an earlier round holds a smaller tag, which the next round's
+// atomicMax replaces.  Before the tag would wrap to 0, every tagged counter is
+// cleared on the round's stream (ordered after the rounds before it) and the
+// tags restart at 1, so no stale count can outlive the wrap.
+int next_epoch(uint32_t* epoch, const Scratch& sc, cudaStream_t s) {
+  if (*epoch == 0xffffffffu) {
+    if (cudaMemsetAsync(sc.tagged, 0, sc.tagged_bytes, s) != cudaSuccess) {
+      cudaGetLastError();
+      return SPECVERIFY_ERR_CUDA;
+    }
+    *epoch = 0u;
+  }
+  ++*epoch;
+  return SPECVERIFY_OK;
+}
+
 // Enqueues one round (a.batch > 0, arguments checked) on the current device.
 int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStream_t s,
                   cudaEvent_t ev_start, cudaEvent_t ev_stop) {
@@ -463,9 +340,9 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
   P.depth = run_depth(c, a.batch);
   P.n_waves = sv::wave_count(c.max_k, P.depth);
   P.list_cap = 2 * P.depth * c.max_batch;
-  P.nb = (c.vocab + sv::kRaceBlock - 1) / sv::kRaceBlock;
+  P.nb = (c.vocab + sv::kVocabBlock - 1) / sv::kVocabBlock;
   P.nvec = (int)((size_t)c.vocab * c.elem_bytes / 16);
-  const int block_bytes = sv::kRaceBlock * c.elem_bytes;
+  const int block_bytes = sv::kVocabBlock * c.elem_bytes;
   (void)block_bytes;
   P.min_span = min_span_blocks(c.elem_bytes);
   P.min_span_res = min_span_res_blocks(c.elem_bytes);
@@ -492,34 +369,9 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
   P.ctr = c.sc.ctr;
   P.recs = c.sc.recs;
   P.rdy = c.sc.rdy;
-  P.bands = c.sc.bands;
-  P.ready_n = c.sc.ready_n;
-  P.ready_u = c.sc.ready_u;
-  P.band_cap = c.sc.band_cap;
-  P.spart = c.sc.spart;
-  P.srpart = c.sc.srpart;
-  P.seg_max = (int)max_segments((size_t)P.nb, (size_t)P.min_span);
-  // a residual entry streams two rows: 2 nb units of the stream split
-  P.seg_max_res = (int)max_segments(2 * (size_t)P.nb, (size_t)P.min_span);
   // the vector path needs every row on a 16-byte boundary
   const bool aligned = rows_aligned(c, a.target_logits, P.draft);
-  if (run_stream(c, a.batch, aligned)) {
-    P.stream_mode = 1;
-    P.depth = 1;
-    P.n_waves = 1;
-    P.list_cap = 0;
-    const size_t row_bytes = (size_t)c.vocab * c.elem_bytes;
-    // a full band: about kBandSpanBytes per CTA, at most kBandMaxRows entries
-    P.band_rows = (int)std::max<size_t>(
-        1, std::min<size_t>((size_t)c.shape.grid_stream * sv::kBandSpanBytes / row_bytes,
-                            (size_t)sv::kBandMaxRows));
-  } else if (run_clusters(c, a.batch, aligned)) {
-    P.cluster_mode = 1;
-    P.unit_cap = 2 * a.batch * (c.max_k + 2) + 16;
-    P.depth = 1;
-    P.n_waves = 1;
-    P.list_cap = c.max_batch;
-  } else if (aligned && a.tee_target != nullptr) {
+  if (aligned && a.tee_target != nullptr) {
     // waves over host-resident logits: sampled rows are copied to the device
     // as they stream, and the correction draws read those copies
     P.tee_target = static_cast<char*>(a.tee_target);
@@ -540,7 +392,7 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
 constexpr int kStaticMaxDevices = 64;
 constexpr size_t kStaticGrid = 1024;  // CTAs a wave of the static path may use
 constexpr ScratchLayout kStaticLayout =
-    scratch_layout(SPECVERIFY_STATIC_MAX_BATCH, SPECVERIFY_STATIC_MAX_K, kStaticGrid, false);
+    scratch_layout(SPECVERIFY_STATIC_MAX_BATCH, SPECVERIFY_STATIC_MAX_K, kStaticGrid);
 
 struct StaticDevice {
   bool ready;
@@ -627,8 +479,9 @@ static int run_impl(specverify_t h, const RunArgs& a, void* stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int slot = h->n_events > 0 ? (int)(h->run_counter % (unsigned long long)h->n_events) : -1;
   h->run_counter++;
-  rc = enqueue_round(h->cfg, a, ++h->epoch,  // never 0: 0 is the initial value of every tag
-                     s, slot >= 0 ? h->ev_start[slot] : nullptr,
+  rc = next_epoch(&h->epoch, h->cfg.sc, s);
+  if (rc != SPECVERIFY_OK) return rc;
+  rc = enqueue_round(h->cfg, a, h->epoch, s, slot >= 0 ? h->ev_start[slot] : nullptr,
                      slot >= 0 ? h->ev_stop[slot] : nullptr);
   h->last_stream = s;
   h->last_run_empty = false;
@@ -664,7 +517,6 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
   c.dtype = dtype;
   c.elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
   c.depth_setting = 0;
-  c.schedule_setting = SPECVERIFY_SCHEDULE_AUTO;
   h->last_stream = nullptr;
   h->last_run_empty = true;
   h->n_events = 0;
@@ -678,16 +530,9 @@ int specverify_create_ex(specverify_t* out, int device, int max_batch, int max_k
     delete h;
     return SPECVERIFY_ERR_CUDA;
   }
-  // the stream schedule's scratch grows with the number of segments a row can
-  // be cut into; above kStreamScratchCap it is left out (waves only)
-  const size_t nb = ((size_t)vocab + sv::kRaceBlock - 1) / sv::kRaceBlock;
-  const StreamSegs segs{max_segments(nb, (size_t)min_span_blocks(c.elem_bytes)),
-                        max_segments(2 * nb, (size_t)min_span_blocks(c.elem_bytes))};
-  const size_t grid_all =
-      (size_t)std::max({c.shape.grid_aligned, c.shape.grid_scalar, c.shape.grid3_aligned,
-                        c.shape.grid3_scalar, c.shape.grid_stream});
-  ScratchLayout L = scratch_layout((size_t)max_batch, max_k, grid_all, true, segs);
-  if (L.bytes > kStreamScratchCap) L = scratch_layout((size_t)max_batch, max_k, grid_all, false);
+  const size_t grid_all = (size_t)std::max({c.shape.grid_aligned, c.shape.grid_scalar,
+                                             c.shape.grid3_aligned, c.shape.grid3_scalar});
+  const ScratchLayout L = scratch_layout((size_t)max_batch, max_k, grid_all);
   if (cudaMalloc(&h->scratch, L.bytes) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -889,7 +734,6 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
   c.dtype = dtype;
   c.elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
   c.depth_setting = 0;
-  c.schedule_setting = SPECVERIFY_SCHEDULE_WAVES;  // the arena has no bands
   const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
                   batch, total_draft, accepted_len, committed_tokens, accept_flags,
                   nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -921,8 +765,6 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
       sd.shape[t].grid_scalar = std::min<int>(sd.shape[t].grid_scalar, (int)kStaticGrid);
       sd.shape[t].grid3_aligned = std::min<int>(sd.shape[t].grid3_aligned, (int)kStaticGrid);
       sd.shape[t].grid3_scalar = std::min<int>(sd.shape[t].grid3_scalar, (int)kStaticGrid);
-      sd.shape[t].grid_cluster = std::min<int>(sd.shape[t].grid_cluster,
-                                               (int)kStaticGrid / kClusterN * kClusterN);
     }
     sd.base = static_cast<char*>(base);
     sd.epoch = 0u;
@@ -930,8 +772,40 @@ int specverify_run_static(int device, int max_k, int vocab, int dtype,
   }
   c.shape = sd.shape[dtype];
   c.sc = scratch_at(sd.base, kStaticLayout);
-  if (++sd.epoch == 0u) ++sd.epoch;  // 0 is the tag of a counter never used
+  rc = next_epoch(&sd.epoch, c.sc, s);
+  if (rc != SPECVERIFY_OK) return rc;
   return enqueue_round(c, a, sd.epoch, s, nullptr, nullptr);
+}
+
+int specverify_debug_set_epoch(specverify_t h, uint32_t epoch) {
+  int rc = check_handle(h);
+  if (rc != SPECVERIFY_OK) return rc;
+  DeviceGuard guard(h->cfg.device);
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemset(h->cfg.sc.tagged, 0, h->cfg.sc.tagged_bytes) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return SPECVERIFY_ERR_CUDA;
+  }
+  h->epoch = epoch;
+  return SPECVERIFY_OK;
+}
+
+int specverify_static_debug_set_epoch(int device, uint32_t epoch) {
+  if (device < 0 || device >= kStaticMaxDevices) return SPECVERIFY_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  StaticDevice& sd = g_static_dev[device];
+  if (!sd.ready) return SPECVERIFY_ERR_INVALID_ARG;
+  DeviceGuard guard(device);
+  const Scratch sc = scratch_at(sd.base, kStaticLayout);
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemset(sc.tagged, 0, sc.tagged_bytes) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return SPECVERIFY_ERR_CUDA;
+  }
+  sd.epoch = epoch;
+  return SPECVERIFY_OK;
 }
 
 int specverify_status(specverify_t h, int32_t* status_out) {
@@ -1007,10 +881,8 @@ int specverify_last_host_reads(specverify_t h, int* in_place_out) {
 int specverify_set_schedule(specverify_t h, int schedule) {
   int rc = check_handle(h);
   if (rc != SPECVERIFY_OK) return rc;
-  if (schedule != SPECVERIFY_SCHEDULE_AUTO && schedule != SPECVERIFY_SCHEDULE_WAVES &&
-      schedule != SPECVERIFY_SCHEDULE_CLUSTERS && schedule != SPECVERIFY_SCHEDULE_STREAM)
+  if (schedule != SPECVERIFY_SCHEDULE_AUTO && schedule != SPECVERIFY_SCHEDULE_WAVES)
     return SPECVERIFY_ERR_INVALID_ARG;
-  h->cfg.schedule_setting = schedule;
   return SPECVERIFY_OK;
 }
 
@@ -1019,14 +891,7 @@ int specverify_launches_per_run(specverify_t h, int batch, int* launches_out) {
   if (rc != SPECVERIFY_OK) return rc;
   if (launches_out == nullptr || batch < 0 || batch > h->cfg.max_batch)
     return SPECVERIFY_ERR_INVALID_ARG;
-  // rows are taken as 16-byte aligned (the caller's tensors decide in the end)
-  const bool aligned = rows_aligned(h->cfg, nullptr, nullptr);
-  if (batch == 0)
-    *launches_out = 0;
-  else if (run_stream(h->cfg, batch, aligned) || run_clusters(h->cfg, batch, aligned))
-    *launches_out = 2;
-  else
-    *launches_out = 1 + sv::wave_count(h->cfg.max_k, run_depth(h->cfg, batch));
+  *launches_out = batch == 0 ? 0 : 1 + sv::wave_count(h->cfg.max_k, run_depth(h->cfg, batch));
   return SPECVERIFY_OK;
 }
 

@@ -4,10 +4,10 @@
 // the three row reductions the verify step needs:
 //   * online max / sum-exp of x/T (the softmax normaliser of p_i and q_i),
 //   * argmax with lowest index (greedy rows),
-//   * the exponential race argmax_v (c*x_v - log2 E_v)  ==  argmin_v E_v / p_v
-//     (bonus draw; "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree,
-//     and DSpark", section 1: one more token from the target when every
-//     draft survives).
+//   * the best (score, index) of the exponential race
+//     argmax_v (log2 w_v - log2 E_v)  ==  argmin_v E_v / w_v
+//     (correction and bonus draws; "Speculative Decoding: Medusa, MTP, EAGLE,
+//     DFlash, DDTree, and DSpark", section 1).
 // Every quantity is kept in the base-2 log domain: c = log2(e)/T, so
 // exp(x/T - m) = 2^(c*x - m2) and the MUFU ex2/lg2 units do the work.
 #pragma once
@@ -94,6 +94,14 @@ __device__ __forceinline__ float race_exponential(uint32_t w) {
 //   looser than 0.529 but still valid, so one branch-free formula serves.)
 __device__ __forceinline__ float race_gain_bound(uint32_t w) {
   return (float)__clz(~w) + 1.001f;
+}
+
+// Sum over aligned groups of kLanes lanes (every lane gets its group's sum).
+template <int kLanes>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -377,27 +385,6 @@ struct BestAcc {
     o.v = __shfl_xor_sync(0xffffffffu, v, lane_mask);
     o.idx = __shfl_xor_sync(0xffffffffu, idx, lane_mask);
     o.nan = __shfl_xor_sync(0xffffffffu, nan, lane_mask);
-    return o;
-  }
-};
-
-// Two races at once (residual draw and its fallback on p).
-struct Best2Acc {
-  BestAcc a, b;
-  __device__ __forceinline__ void init() {
-    a.init();
-    b.init();
-  }
-  __device__ static __forceinline__ Best2Acc merge(Best2Acc x, Best2Acc y) {
-    Best2Acc r;
-    r.a = BestAcc::merge(x.a, y.a);
-    r.b = BestAcc::merge(x.b, y.b);
-    return r;
-  }
-  __device__ __forceinline__ Best2Acc shfl_xor(int lane_mask) const {
-    Best2Acc o;
-    o.a = a.shfl_xor(lane_mask);
-    o.b = b.shfl_xor(lane_mask);
     return o;
   }
 };

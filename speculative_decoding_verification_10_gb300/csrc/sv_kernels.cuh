@@ -17,7 +17,7 @@
 // fewer launches, which pays for small batches.
 //
 // Inside a wave the work is split flat: the wave's rows form one sequence of
-// race blocks (128 vocab ids), and CTA c takes the contiguous range
+// vocab blocks (128 vocab ids), and CTA c takes the contiguous range
 // [c*T/G, (c+1)*T/G) of it, so every CTA streams the same number of bytes
 // whatever the row lengths.  A CTA's range cuts into a few row segments; each
 // segment reduces to one 16-byte partial.  A position is decided by the CTA
@@ -56,7 +56,7 @@ constexpr int kMaxBatch = 4096;                // requests per round
 constexpr int kMaxK = 31;                      // draft positions per request
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanTokens = 4096;              // draft tokens the plan stages in shared memory
-constexpr int kRaceBlock = 128;                // vocab ids per race block
+constexpr int kVocabBlock = 128;               // vocab ids per block of the flat split
 constexpr int kMinSpanBytes = 16384;           // smallest share of a wave per CTA
 
 enum RowKind : int { kSoftmax = 0, kArgmax = 1, kRace = 2, kResidual = 3 };
@@ -70,7 +70,7 @@ constexpr int kCtaThreads = kThreads + 32;
 
 // Status bits (equal to the SPECVERIFY_STATUS_* values of the header).
 constexpr uint32_t kStBadToken = 1u, kStBadK = 2u, kStBadTemp = 4u, kStNonfinite = 8u,
-                   kStBadTotal = 16u, kStNoDraft = 64u, kStOverrun = 128u, kStTimeout = 256u,
+                   kStBadTotal = 16u, kStNoDraft = 64u,
                    kStBadConf = 512u;
 
 // Number of waves of a round with positions 0..max_k taken D at a time: one
@@ -123,34 +123,12 @@ struct __align__(16) ResEntry {
   uint32_t req_lo, req_hi, pad2;
 };
 
-// Global counters.  The stream schedule uses the reservation counts of its two
-// queues, the number of finished requests and the number it must finish.
+// Global counters.
 enum Counter : int {
   kCntStatus = 0,
-  kCntClaim = 1,
-  kCntNRes = 2,   // row entries reserved in the normal queue
-  kCntURes = 3,   // residual entries reserved in the urgent queue
-  kCntDone = 4,   // requests whose outputs are final
-  kCntLive = 5,   // requests the plan left to verify
+  kCntLive = 1,   // requests the plan left to verify
   kCntCount = 8
 };
-
-// A band of the stream schedule: the urgent entries [u0, u1) and the row
-// entries [n0, n1) that every CTA splits the same way, where u0 and n0 are
-// where the band before it ended.  One 64-bit word, written once per round:
-// epoch << 32 | payload, payload = u1 << 18 | n1 for a formed band, or one of
-// the markers below; a word of an earlier round reads as open.
-struct Band {
-  unsigned long long word;
-};
-constexpr uint32_t kBandFormingMark = 0xffffffffu;  // being formed by one CTA
-constexpr uint32_t kBandEndMark = 0xfffffffeu;      // the round is over
-constexpr int kBandRowBits = 18;                    // n1 < 2^18, u1 < 2^13
-__host__ __device__ constexpr uint32_t band_payload(int u1, int n1) {
-  return ((uint32_t)u1 << kBandRowBits) | (uint32_t)n1;
-}
-__host__ __device__ constexpr int band_u1(uint32_t p) { return (int)((p >> kBandRowBits) & 0x1fffu); }
-__host__ __device__ constexpr int band_n1(uint32_t p) { return (int)(p & ((1u << kBandRowBits) - 1u)); }
 
 struct Params {
   const void* target;
@@ -166,23 +144,18 @@ struct Params {
   int pos0, pos1;
   int n_waves;
   uint32_t epoch;    // this round's tag of the completion counters
-  int nb;            // race blocks per row
+  int nb;            // vocab blocks per row
   int nvec;          // 16-byte vectors per row (aligned rows)
-  int min_span;      // fewest race blocks per CTA share of the row phase
+  int min_span;      // fewest vocab blocks per CTA share of the row phase
   int min_span_res;  // ... and of the residual phase
   int stride;        // capacity of a request-indexed array (max_batch)
   int list_cap;      // entries per wave list: 2 * D * stride
-  int cluster_mode;  // the plan lists one entry per request (the cluster launch)
-  int unit_cap;      // cluster launch: more units than any round needs
-  int stream_mode;   // the plan publishes its rows to the stream schedule's queue
   // Device copies of the window, same layout as target / draft, or NULL.  When
   // set (waves, 16-byte rows, logits read from host memory), every sampled
   // row a wave streams is also written here, and the correction draws of the
   // next wave read these copies instead of the host rows.
   char* tee_target;
   char* tee_draft;
-  int band_rows;     // stream schedule: rows a full band takes
-  int band_cap;      // stream schedule: bands a round may form
   int trimmed;              // num_draft is the window layout; verify trimmed windows
   const float* confidence;  // trimmed runs: c_i per draft position of the window layout
   const float* cost;        // trimmed runs: cost of one verified position, per request
@@ -205,12 +178,6 @@ struct Params {
   int* ctr;                     // [kCntCount]
   PosRec* recs;                 // [(max_k + 1) * stride] merged rows of multi-position waves
   unsigned long long* rdy;      // [n_waves * stride] epoch | positions of a request merged
-  Band* bands;                  // [band_cap] stream schedule
-  Partial* spart;               // stream: [list entries * seg_max] row segment partials
-  Partial* srpart;              // stream: [stride * seg_max_res] residual segment partials
-  int seg_max, seg_max_res;     // stream: most segments one row entry is cut into
-  uint32_t* ready_n;            // [list entries] epoch once a row entry is written
-  uint32_t* ready_u;            // [stride] epoch once a residual entry is written
 };
 
 __device__ __forceinline__ Partial ld_cg(const Partial* p) {
@@ -241,7 +208,7 @@ __device__ __forceinline__ RequestKey request_key(const Params& P, int r) {
 }
 
 // ---------------------------------------------------------------------------
-// The flat split of one phase of a wave: n rows of nb race blocks, T = n * nb
+// The flat split of one phase of a wave: n rows of nb vocab blocks, T = n * nb
 // blocks over G CTAs; CTA c takes blocks [c*T/G, (c+1)*T/G).
 // ---------------------------------------------------------------------------
 struct Split {
@@ -281,19 +248,14 @@ struct __align__(16) QItem {
   int pos;           // the position the row belongs to (Philox position)
   int base;          // list index of the request's first row in this wave
   int paired, is_draft;
-  int vbeg, vend;    // vectors (aligned rows) or race blocks (scalar path)
+  int vbeg, vend;    // vectors (aligned rows) or vocab blocks (scalar path)
   int nst;           // ring stages (aligned rows)
   int g;             // partial index: CTA + entry
-  int yv;            // vector (aligned) or race block (scalar) holding y, -1 if none
+  int yv;            // vector (aligned) or vocab block (scalar) holding y, -1 if none
   float c;           // log2(e) / T
   float mp, inv_sp, mq, inv_sq;  // residual segments: normalisers of p_j and q_j
   uint32_t req_lo, req_hi;
-  // stream schedule: the split of the segment's band phase and that phase's
-  // first queue index (entry e of the phase is queue entry e0 + e)
-  unsigned long long sT;
-  int sG, e0;
-  int band;
-  int snu;  // stream schedule: urgent entries of the segment's band
+  int e0;    // entry e of the phase is partial slot CTA + e0 + e
   char* tee;  // where a softmax segment's row is copied (Params::tee_*), or NULL
 };
 
@@ -308,251 +270,246 @@ __device__ __forceinline__ float pick(const float (&x)[N], int e) {
 }
 
 // ---------------------------------------------------------------------------
-// Two-level exponential race: blocks of kRaceBlock vocab ids.  The block race
-// picks argmax_b log2 W_b - log2 E2_b over blocks with mass W_b > 0 (Philox
-// stream 2, indexed by block); the element race inside the winning block picks
-// argmax_v log2 w_v - log2 E1_v (stream 1, indexed by vocab id).  Lowest index
-// on ties at both levels.
+// Exponential race over vocab ids.  A categorical draw from weights w_v >= 0
+// is argmin_{v: w_v > 0} E_v / w_v, E_v the race exponential of the Philox
+// stream-1 word of vocab id v at the draw's (request, position), lowest index
+// on ties; in the base-2 log domain it is the argmax of the score
+//   s_v = log2 w_v + gain_v,   gain_v = -log2 E_v.
+// E_v / w_v is exponential with rate w_v, so the winner is an exact sample of
+// w / sum w, and the order in which ids are visited does not change it.
+//
+// Every id needs its word (one Philox call gives the words of four
+// consecutive ids), but not its exponential: race_gain_bound(word) bounds the
+// gain from integer operations, so an id whose bounded score cannot beat the
+// thread's best so far is passed over without a logarithm, and a group of
+// four whose largest logit plus the largest possible gain (kMaxGain) cannot
+// beat it is passed over without the Philox call.  Both skips are exact: a
+// skipped id's computed score is never above the best it is compared with.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t race_word(uint32_t stream, int idx, uint32_t pos,
-                                              RequestKey rk, PhiloxKey key) {
-  const uint4 r = philox4x32_10(make_uint4((uint32_t)idx >> 2, pos, rk.lo, stream | (rk.hi << 8)), key);
-  return word_of(r, idx & 3);
+constexpr float kMaxGain = 33.001f;   // >= race_gain_bound(w) for every word w
+constexpr float kBoundSlack = 1e-3f;  // margin of the fast log2 p_v bound below
+
+// Words of ids 4 g .. 4 g + 3 (stream 1).
+__device__ __forceinline__ uint4 race_words(uint32_t g, uint32_t pos, RequestKey rk,
+                                            PhiloxKey key) {
+  return philox4x32_10(make_uint4(g, pos, rk.lo, 1u | (rk.hi << 8)), key);
 }
 
-// -log2 E for a race word (the additive "gain" of an element or block).
+// -log2 E for a race word.
 __device__ __forceinline__ float race_gain(uint32_t w) { return -fast_lg2(race_exponential(w)); }
 
-template <int kLanes>
-__device__ __forceinline__ float group_max(float v) {
-#pragma unroll
-  for (int off = kLanes / 2; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
-}
-template <int kLanes>
-__device__ __forceinline__ float group_sum(float v) {
-#pragma unroll
-  for (int off = kLanes / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
+// IEEE max that propagates NaN (a NaN logit is then seen by the group test).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
-// Block gains of a warp's vector groups, made 32 groups at a time: lane L
-// holds the gains of the kBlocksPerGroup blocks of group g0 + L.  A vector
-// group is the warp's 32 consecutive vectors (32 * kVec ids, block aligned).
 template <typename E>
-struct GroupGains {
-  static constexpr int kBlocksPerGroup = 32 * E::kVec / kRaceBlock;   // 2 (bf16) or 1 (fp32)
-  static constexpr int kLanesPerBlock = kRaceBlock / E::kVec;          // 16 or 32
-  float lo, hi;
-  // first element of group g of warp w, for a segment starting at vector vbeg
-  __device__ static __forceinline__ int group_elem(int vbeg, int g, int w) {
-    return (vbeg + g * kThreads + w * 32) * E::kVec;
-  }
-  __device__ __forceinline__ void make(int vbeg, int g0, int w, uint32_t pos, RequestKey rk,
-                                       PhiloxKey key) {
-    const int lane = threadIdx.x & 31;
-    const int b = group_elem(vbeg, g0 + lane, w) / kRaceBlock;
-    const uint4 r = philox4x32_10(make_uint4((uint32_t)b >> 2, pos, rk.lo, 2u | (rk.hi << 8)), key);
-    lo = race_gain(word_of(r, b & 3));
-    hi = lo;
-    if (kBlocksPerGroup > 1) {
-      // a segment may start on an odd block: block b + 1 can open the next
-      // Philox counter
-      const int b1 = b + 1;
-      const uint4 r1 = (b1 & 3) ? r
-                                : philox4x32_10(make_uint4((uint32_t)b1 >> 2, pos, rk.lo,
-                                                           2u | (rk.hi << 8)), key);
-      hi = race_gain(word_of(r1, b1 & 3));
-    }
-  }
-  // the gain of this lane's block in group g (all lanes call it)
-  __device__ __forceinline__ float get(int g) const {
-    const int src = g & 31;
-    const float a = __shfl_sync(0xffffffffu, lo, src);
-    const float c = __shfl_sync(0xffffffffu, hi, src);
-    return ((threadIdx.x & 31) / kLanesPerBlock) ? c : a;
-  }
-};
-
-// Bonus race over one vector group: block weight W_b = sum 2^(c x_v) (kept as
-// log2: block max + log2 of the rescaled sum), score log2 W_b + gain.
-template <typename E>
-__device__ __forceinline__ void group_bonus(BestAcc& acc, const float (&x)[E::kVec], int e_lane,
-                                            float c, float gain) {
-  constexpr int kL = GroupGains<E>::kLanesPerBlock;
-  float mx = x[0];
-#pragma unroll
-  for (int e = 1; e < E::kVec; ++e) mx = fmaxf(mx, x[e]);
-  const float m = group_max<kL>(mx) * c;
-  float s = 0.f;
-  if (m > kNegInf) {
-    const float2 cc = make_float2(c, c), nm = make_float2(-m, -m);
-    float2 a2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int e = 0; e < E::kVec; e += 2) {
-      const float2 t = __ffma2_rn(make_float2(x[e], x[e + 1]), cc, nm);
-      a2 = __fadd2_rn(a2, make_float2(fast_ex2(t.x), fast_ex2(t.y)));
-    }
-    s = a2.x + a2.y;
-  } else if (m != m) {
-    s = m;  // a block of NaNs
-  }
-  s = group_sum<kL>(s);
-  acc.nan |= (s != s);
-  if (s > 0.f) acc.take_cmp(m + fast_lg2(s) + gain, e_lane / kRaceBlock);
+__device__ __forceinline__ void group_max(const float (&x)[E::kVec], int h, float& mx) {
+  mx = fmax_nan(fmax_nan(x[h], x[h + 1]), fmax_nan(x[h + 2], x[h + 3]));
 }
 
-// Bonus-race gains of a warp's blocks for one window of kGroups vector groups
-// (8 stages in bf16, 16 in fp32): lane L holds the gain of block slot L, which
-// is block L % kBlocksPerGroup of group g0 + L / kBlocksPerGroup.
+// Bonus race (weights 2^(c x_v), unnormalised) over one vector of kVec
+// consecutive ids starting at id e0 (a multiple of 4); ids must come in
+// increasing order per thread.  A NaN or +inf logit marks the row bad.
 template <typename E>
-struct WindowGains {
-  static constexpr int kBPG = GroupGains<E>::kBlocksPerGroup;
-  static constexpr int kGroups = 32 / kBPG;
-  float g;
-  __device__ __forceinline__ void make(int vbeg, int g0, int w, uint32_t pos, RequestKey rk,
-                                       PhiloxKey key) {
-    const int lane = threadIdx.x & 31;
-    const int b = GroupGains<E>::group_elem(vbeg, g0 + lane / kBPG, w) / kRaceBlock + lane % kBPG;
-    g = race_gain(race_word(2u, b, pos, rk, key));
-  }
-  __device__ __forceinline__ float get(int slot) const {
-    return __shfl_sync(0xffffffffu, g, slot);
-  }
-};
-
-// Bonus race over one stage: the warp's two vector groups x0 (group g) and x1
-// (group g + 1), kBPG blocks each.  Block weights are summed against a
-// warp-uniform reference R, the largest c*x the warp has seen (log2 domain):
-//   log2 W_b = R + log2 sum_v 2^(c x_v - R),
-// which needs no per-block maximum.  R is raised (and the sums redone) when it
-// is still -inf or a lane's sum passes 2^64, i.e. an element stands more than
-// about 60 above R.  Terms that underflow (c x_v < R - 126) are dropped; a
-// block made only of such terms scores below R - 95 even with the largest
-// gain, while the block holding R's element scores at least R - 4.1, so it
-// cannot win.  The reduction is transposed: one exchange leaves slot-0 sums in
-// the lanes whose bit kL/2 is clear and slot-1 sums in the others, so both
-// groups' blocks are reduced by the same log2(kL) shuffles.
-template <typename E>
-__device__ __forceinline__ void stage_bonus(BestAcc& acc, float& R, const float (&x0)[E::kVec],
-                                            const float (&x1)[E::kVec], int vbeg, int g, int w,
-                                            int g0, float c, const WindowGains<E>& wg) {
-  constexpr int kL = GroupGains<E>::kLanesPerBlock;
-  const int lane = threadIdx.x & 31;
-  float s0 = 0.f, s1 = 0.f;
-  auto sums = [&]() {
-    const float2 cc = make_float2(c, c), nr = make_float2(-R, -R);
-    float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+__device__ __forceinline__ void race_vec(BestAcc& acc, const float (&x)[E::kVec], int e0, float c,
+                                         uint32_t pos, RequestKey rk, PhiloxKey key) {
 #pragma unroll
-    for (int e = 0; e < E::kVec; e += 2) {
-      const float2 t = __ffma2_rn(make_float2(x0[e], x0[e + 1]), cc, nr);
-      a = __fadd2_rn(a, make_float2(fast_ex2(t.x), fast_ex2(t.y)));
-      const float2 u = __ffma2_rn(make_float2(x1[e], x1[e + 1]), cc, nr);
-      b = __fadd2_rn(b, make_float2(fast_ex2(u.x), fast_ex2(u.y)));
-    }
-    s0 = a.x + a.y;
-    s1 = b.x + b.y;
-  };
-  if (R > kNegInf) sums();
-  if (__any_sync(0xffffffffu, !(R > kNegInf) || s0 > 0x1p64f || s1 > 0x1p64f)) {
-    float mx = x0[0];
+  for (int h = 0; h < E::kVec; h += 4) {
+    float mx;
+    group_max<E>(x, h, mx);
+    acc.nan |= !(mx < -kNegInf);
+    if (fmaf(mx, c, kMaxGain) > acc.v) {
+      const uint4 r = race_words((uint32_t)(e0 + h) >> 2, pos, rk, key);
 #pragma unroll
-    for (int e = 1; e < E::kVec; ++e) mx = fmaxf(mx, x0[e]);
-#pragma unroll
-    for (int e = 0; e < E::kVec; ++e) mx = fmaxf(mx, x1[e]);
-    R = fmaxf(R, warp_max(mx) * c);
-    if (R > kNegInf) {
-      sums();
-    } else {
-      s0 = s1 = 0.f;
-    }
-  }
-  const bool hi = (lane & (kL / 2)) != 0;
-  float v = (hi ? s1 : s0) + __shfl_xor_sync(0xffffffffu, hi ? s0 : s1, kL / 2);
-#pragma unroll
-  for (int off = kL / 4; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  const int grp = g + (hi ? 1 : 0);
-  const int sub = lane / kL;
-  const float gain = wg.get((grp - g0) * WindowGains<E>::kBPG + sub);
-  acc.nan |= (v != v);
-  if (v > 0.f)
-    acc.take_cmp(R + fast_lg2(v) + gain,
-                 GroupGains<E>::group_elem(vbeg, grp, w) / kRaceBlock + sub);
-}
-
-// Residual race over one vector group: W_b = sum max(p_v - q_v, 0).
-struct ResidualRow {
-  float c, mp, inv_sp, mq, inv_sq;
-};
-
-template <typename E>
-__device__ __forceinline__ void group_residual(BestAcc& acc, const float (&x)[E::kVec],
-                                               const float (&z)[E::kVec], int e_lane,
-                                               const ResidualRow& rr, float gain) {
-  constexpr int kL = GroupGains<E>::kLanesPerBlock;
-  const float2 cc = make_float2(rr.c, rr.c), nm = make_float2(-rr.mp, -rr.mq);
-  const float2 inv = make_float2(rr.inv_sp, rr.inv_sq);
-  float s = 0.f;
-#pragma unroll
-  for (int e = 0; e < E::kVec; ++e) {
-    const float2 t = __ffma2_rn(make_float2(x[e], z[e]), cc, nm);
-    const float2 pq = __fmul2_rn(make_float2(fast_ex2(t.x), fast_ex2(t.y)), inv);
-    s += fmaxf(pq.x - pq.y, 0.f);
-  }
-  s = group_sum<kL>(s);
-  if (s > 0.f) acc.take_cmp(fast_lg2(s) + gain, e_lane / kRaceBlock);
-}
-
-// Element race inside block b (one warp, lane l takes ids 128 b + 4 l .. +3):
-// bonus/fallback weights 2^(c x_v) (kResid false) or residual [p - q]_+.
-template <typename E, bool kResid>
-__device__ __forceinline__ int inner_race(const Params& P, const char* trow, const char* drow,
-                                          int b, const ResidualRow& rr, uint32_t pos,
-                                          RequestKey rk) {
-  const int lane = threadIdx.x & 31;
-  const int v0 = b * kRaceBlock + 4 * lane;
-  const uint4 r = philox4x32_10(make_uint4((uint32_t)v0 >> 2, pos, rk.lo, 1u | (rk.hi << 8)), P.key);
-  BestAcc acc;
-  acc.init();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int v = v0 + i;
-    if (v < P.vocab) {
-      const float x = E::load1(trow, v);
-      const float g = race_gain(word_of(r, i));
-      if (kResid) {
-        const float p = fast_ex2(fmaf(x, rr.c, -rr.mp)) * rr.inv_sp;
-        const float q = fast_ex2(fmaf(E::load1(drow, v), rr.c, -rr.mq)) * rr.inv_sq;
-        const float w = p - q;
-        if (w > 0.f) acc.take(fast_lg2(w) + g, v);
-      } else {
-        acc.take(fmaf(x, rr.c, g), v);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w = word_of(r, i);
+        if (fmaf(x[h + i], c, race_gain_bound(w)) > acc.v)
+          acc.take(fmaf(x[h + i], c, race_gain(w)), e0 + h + i);
       }
     }
   }
-  acc = warp_reduce(acc);
-  return acc.idx;
 }
 
-// The block race over a whole row by one warp with plain loads: the draw from
-// p_j when a residual turns out to have no mass (p == q in fp32).
+// Residual race over [p - q]_+ (the normalisers of p_j and q_j known) for one
+// vector of each row.  log2 p_v + kBoundSlack = fmaf(x, c, rr.lp) bounds
+// log2 (p_v - q_v) from above.
+struct ResidualRow {
+  float c, mp, inv_sp, mq, inv_sq;
+  float lp;  // -mp + log2(inv_sp) + kBoundSlack
+};
+
 template <typename E>
-__device__ BestAcc warp_block_race(const Params& P, const char* trow, float c, uint32_t pos,
-                                   RequestKey rk) {
+__device__ __forceinline__ void residual_vec(BestAcc& acc, const float (&x)[E::kVec],
+                                             const float (&z)[E::kVec], int e0,
+                                             const ResidualRow& rr, uint32_t pos, RequestKey rk,
+                                             PhiloxKey key) {
+#pragma unroll
+  for (int h = 0; h < E::kVec; h += 4) {
+    const float mx = fmaxf(fmaxf(x[h], x[h + 1]), fmaxf(x[h + 2], x[h + 3]));
+    if (fmaf(mx, rr.c, rr.lp) + kMaxGain > acc.v) {
+      const uint4 r = race_words((uint32_t)(e0 + h) >> 2, pos, rk, key);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w = word_of(r, i);
+        if (fmaf(x[h + i], rr.c, rr.lp) + race_gain_bound(w) > acc.v) {
+          const float p = fast_ex2(fmaf(x[h + i], rr.c, -rr.mp)) * rr.inv_sp;
+          const float q = fast_ex2(fmaf(z[h + i], rr.c, -rr.mq)) * rr.inv_sq;
+          const float d = p - q;
+          if (d > 0.f) acc.take(fast_lg2(d) + race_gain(w), e0 + h + i);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ ResidualRow residual_row(float c, float mp, float inv_sp, float mq,
+                                                    float inv_sq) {
+  return ResidualRow{c, mp, inv_sp, mq, inv_sq, -mp + fast_lg2(inv_sp) + kBoundSlack};
+}
+
+// N Philox blocks of stream 1 (ids 4 g[i] .. 4 g[i] + 3) with their rounds
+// interleaved: independent dependency chains the scheduler overlaps.
+template <int N>
+__device__ __forceinline__ void race_words_n(uint4 (&r)[N], const uint32_t (&g)[N], uint32_t pos,
+                                             RequestKey rk, PhiloxKey key) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) r[i] = make_uint4(g[i], pos, rk.lo, 1u | (rk.hi << 8));
+  uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const uint4 c = r[i];
+      const uint64_t p0 = (uint64_t)c.x * 0xD2511F53u;
+      const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57u;
+      r[i] = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1,
+                        (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
+    }
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
+
+// The exact gain of a word that passed its bound: kept out of line, since it
+// is rare and its code (two logarithms) would otherwise be copied into every
+// element's slot.
+__device__ __noinline__ float race_gain_slow(uint32_t w) { return race_gain(w); }
+
+// A race score enters the best only when finite: an id of zero weight (a
+// logit of -inf, or a residual that underflows) never wins, even against an
+// empty best of -inf.
+__device__ __forceinline__ void take_finite(BestAcc& acc, float score, int i) {
+  if (score > kNegInf) acc.take_cmp(score, i);
+}
+
+// Bonus race over one stage of the copy ring: vectors x0 (ids e0 ..) and x1
+// (ids e1 ..), kVec ids each.  `wbest` is the best score of the warp so far
+// (warp-uniform, raised after a stage where some lane took an element): an id
+// whose bounded score is below it cannot be the row's winner, so every lane
+// tests against the warp's best, not only its own.  The test keeps ties
+// (>=), which take_cmp then orders by index.  Call with the whole warp.
+template <typename E>
+__device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const float (&x0)[E::kVec],
+                                           const float (&x1)[E::kVec], int e0, int e1, float c,
+                                           uint32_t pos, RequestKey rk, PhiloxKey key) {
+  constexpr int G = E::kVec / 4;  // Philox blocks per vector
+  float mx = x0[0];
+#pragma unroll
+  for (int i = 1; i < E::kVec; ++i) mx = fmax_nan(mx, x0[i]);
+#pragma unroll
+  for (int i = 0; i < E::kVec; ++i) mx = fmax_nan(mx, x1[i]);
+  acc.nan |= !(mx < -kNegInf);  // NaN or +inf
+  if (!__any_sync(0xffffffffu, fmaf(mx, c, kMaxGain) >= wbest)) return;
+  uint32_t g[2 * G];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    g[j] = (uint32_t)(e0 >> 2) + j;
+    g[G + j] = (uint32_t)(e1 >> 2) + j;
+  }
+  uint4 r[2 * G];
+  race_words_n<2 * G>(r, g, pos, rk, key);
+  bool pass = false;
+#pragma unroll
+  for (int i = 0; i < E::kVec; ++i) {
+    pass |= fmaf(x0[i], c, race_gain_bound(word_of(r[i >> 2], i & 3))) >= wbest;
+    pass |= fmaf(x1[i], c, race_gain_bound(word_of(r[G + (i >> 2)], i & 3))) >= wbest;
+  }
+  if (pass) {
+#pragma unroll
+    for (int i = 0; i < E::kVec; ++i) {
+      const uint32_t w = word_of(r[i >> 2], i & 3);
+      if (fmaf(x0[i], c, race_gain_bound(w)) >= wbest)
+        take_finite(acc, fmaf(x0[i], c, race_gain_slow(w)), e0 + i);
+    }
+#pragma unroll
+    for (int i = 0; i < E::kVec; ++i) {
+      const uint32_t w = word_of(r[G + (i >> 2)], i & 3);
+      if (fmaf(x1[i], c, race_gain_bound(w)) >= wbest)
+        take_finite(acc, fmaf(x1[i], c, race_gain_slow(w)), e1 + i);
+    }
+  }
+  if (__any_sync(0xffffffffu, pass)) wbest = warp_max(acc.v);
+}
+
+// Residual race over one stage: vector x of t_j and z of d_j, the same kVec
+// ids from e0.  fmaf(x, c, rr.lp) bounds log2 (p_v - q_v) from above, so the
+// two exponentials are only taken for ids that pass.  Call with the whole warp.
+template <typename E>
+__device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
+                                               const float (&x)[E::kVec],
+                                               const float (&z)[E::kVec], int e0,
+                                               const ResidualRow& rr, uint32_t pos,
+                                               RequestKey rk, PhiloxKey key) {
+  constexpr int G = E::kVec / 4;
+  float mx = x[0];
+#pragma unroll
+  for (int i = 1; i < E::kVec; ++i) mx = fmaxf(mx, x[i]);
+  if (!__any_sync(0xffffffffu, fmaf(mx, rr.c, rr.lp) + kMaxGain >= wbest)) return;
+  uint32_t g[G];
+#pragma unroll
+  for (int j = 0; j < G; ++j) g[j] = (uint32_t)(e0 >> 2) + j;
+  uint4 r[G];
+  race_words_n<G>(r, g, pos, rk, key);
+  bool pass = false;
+#pragma unroll
+  for (int i = 0; i < E::kVec; ++i)
+    pass |= fmaf(x[i], rr.c, rr.lp) + race_gain_bound(word_of(r[i >> 2], i & 3)) >= wbest;
+  if (pass) {
+#pragma unroll
+    for (int i = 0; i < E::kVec; ++i) {
+      const uint32_t w = word_of(r[i >> 2], i & 3);
+      if (fmaf(x[i], rr.c, rr.lp) + race_gain_bound(w) >= wbest) {
+        const float p = fast_ex2(fmaf(x[i], rr.c, -rr.mp)) * rr.inv_sp;
+        const float q = fast_ex2(fmaf(z[i], rr.c, -rr.mq)) * rr.inv_sq;
+        const float d = p - q;
+        if (d > 0.f) take_finite(acc, fast_lg2(d) + race_gain_slow(w), e0 + i);
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, pass)) wbest = warp_max(acc.v);
+}
+
+// The race over a whole row by one warp with plain loads (lane l takes ids
+// 128 b + 4 l .. + 3): the draw from p_j when a residual turns out to have no
+// mass in fp32 (p <= q everywhere), an edge case.
+template <typename E>
+__device__ int warp_row_race(const Params& P, const char* trow, float c, uint32_t pos,
+                             RequestKey rk) {
   const int lane = threadIdx.x & 31;
-  const int nblocks = (P.vocab + kRaceBlock - 1) / kRaceBlock;
   BestAcc acc;
   acc.init();
-  for (int b = lane; b < nblocks; b += 32) {
-    const int v_end = min(P.vocab, (b + 1) * kRaceBlock);
-    float m = kNegInf, s = 0.f;
-    for (int v = b * kRaceBlock; v < v_end; ++v) m = fmaxf(m, E::load1(trow, v));
-    m *= c;
-    if (m > kNegInf)
-      for (int v = b * kRaceBlock; v < v_end; ++v) s += fast_ex2(fmaf(E::load1(trow, v), c, -m));
-    if (s > 0.f) acc.take(m + fast_lg2(s) + race_gain(race_word(2u, b, pos, rk, P.key)), b);
+  for (int v0 = 4 * lane; v0 < P.vocab; v0 += 128) {
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = v0 + i < P.vocab ? E::load1(trow, v0 + i) : kNegInf;
+    const uint4 r = race_words((uint32_t)v0 >> 2, pos, rk, P.key);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc.take(fmaf(x[i], c, race_gain(word_of(r, i))), v0 + i);
   }
-  return warp_reduce(acc);
+  return warp_reduce(acc).idx;
 }
 
 // ---------------------------------------------------------------------------
@@ -699,10 +656,7 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       vec(x, (vi + kThreads) * E::kVec);
     }
   } else if (kind == kRace) {
-    static_assert(kStageVecs == 2, "a stage holds two vector groups");
-    WindowGains<E> wg;
-    float R = kNegInf;
-    int g0 = 0;
+    float wbest = kNegInf;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
       take(v[0], v[1]);
@@ -711,19 +665,15 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
         if (vi >= vend) v[0] = E::pad();
         if (vi + kThreads >= vend) v[1] = E::pad();
       }
-      const int g = st * kStageVecs;
-      if (g % WindowGains<E>::kGroups == 0) {
-        g0 = g;
-        wg.make(vbeg, g0, w, (uint32_t)pos, rk, P.key);
-      }
       float x0[E::kVec], x1[E::kVec];
       E::unpack(v[0], x0);
       E::unpack(v[1], x1);
-      stage_bonus<E>(acc, R, x0, x1, vbeg, g, w, g0, c, wg);
+      race_stage<E>(acc, wbest, x0, x1, vi * E::kVec, (vi + kThreads) * E::kVec, c,
+                    (uint32_t)pos, rk, P.key);
     }
   } else {
-    const ResidualRow rr{c, itm.mp, itm.inv_sp, itm.mq, itm.inv_sq};
-    GroupGains<E> gg;
+    const ResidualRow rr = residual_row(c, itm.mp, itm.inv_sp, itm.mq, itm.inv_sq);
+    float wbest = kNegInf;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
       take(v[0], v[1]);
@@ -732,11 +682,10 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
         v[0] = E::pad();
         v[1] = E::pad();
       }
-      if ((st & 31) == 0) gg.make(vbeg, st, w, (uint32_t)pos, rk, P.key);
       float x[E::kVec], z[E::kVec];
       E::unpack(v[0], x);
       E::unpack(v[1], z);
-      group_residual<E>(acc, x, z, vi * E::kVec, rr, gg.get(st));
+      residual_stage<E>(acc, wbest, x, z, vi * E::kVec, rr, (uint32_t)pos, rk, P.key);
     }
   }
   acc = warp_reduce(acc);
@@ -751,7 +700,7 @@ __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* que
   return seg_reduce<E>(P, itm, s_xy, take);
 }
 
-// Scalar path (rows not 16-byte aligned): warp w takes race blocks
+// Scalar path (rows not 16-byte aligned): warp w takes vocab blocks
 // vbeg + w, vbeg + w + 7, ...; lane l the ids 128 b + l + 32 j.
 template <typename E>
 __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, float* s_xy) {
@@ -762,7 +711,7 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
     acc.init();
     for (int b = it.vbeg + w; b < it.vend; b += kComputeWarps)
       for (int j = 0; j < 4; ++j) {
-        const int v = b * kRaceBlock + lane + 32 * j;
+        const int v = b * kVocabBlock + lane + 32 * j;
         if (v < P.vocab) {
           const float x = E::load1(it.row, v);
           if (v == it.y) *s_xy = x;
@@ -778,7 +727,7 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
   for (int b = it.vbeg + w; b < it.vend; b += kComputeWarps) {
     if (it.kind == kArgmax) {
       for (int j = 0; j < 4; ++j) {
-        const int v = b * kRaceBlock + lane + 32 * j;
+        const int v = b * kVocabBlock + lane + 32 * j;
         if (v < P.vocab) {
           const float x = E::load1(it.row, v);
           acc.nan |= (x != x);
@@ -787,33 +736,20 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
       }
       continue;
     }
-    float s = 0.f;
-    float m = 0.f;
-    if (it.kind == kRace) {
-      float x[4];
-      float mx = kNegInf;
-      for (int j = 0; j < 4; ++j) {
-        const int v = b * kRaceBlock + lane + 32 * j;
-        x[j] = v < P.vocab ? E::load1(it.row, v) : kNegInf;
-        mx = fmaxf(mx, x[j]);
-        acc.nan |= (x[j] != x[j]) || (x[j] == -kNegInf);
-      }
-      m = warp_max(mx) * it.c;
-      if (m > kNegInf)
-        for (int j = 0; j < 4; ++j) s += fast_ex2(fmaf(x[j], it.c, -m));
-    } else {
-      for (int j = 0; j < 4; ++j) {
-        const int v = b * kRaceBlock + lane + 32 * j;
-        if (v < P.vocab) {
-          const float p = fast_ex2(fmaf(E::load1(it.row, v), it.c, -it.mp)) * it.inv_sp;
-          const float q = fast_ex2(fmaf(E::load1(it.row2, v), it.c, -it.mq)) * it.inv_sq;
-          s += fmaxf(p - q, 0.f);
-        }
-      }
+    // race rows: lane l takes ids 128 b + 4 l .. + 3 (one Philox call)
+    const int v0 = b * kVocabBlock + 4 * lane;
+    float x[4], z[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[i] = v0 + i < P.vocab ? E::load1(it.row, v0 + i) : kNegInf;
+      z[i] = (it.kind == kResidual && v0 + i < P.vocab) ? E::load1(it.row2, v0 + i) : kNegInf;
     }
-    s = group_sum<32>(s);
-    acc.nan = __reduce_or_sync(0xffffffffu, acc.nan);
-    if (s > 0.f) acc.take_cmp(m + fast_lg2(s) + race_gain(race_word(2u, b, pos, rk, P.key)), b);
+    if (it.kind == kRace) {
+      race_vec<F32>(acc, x, v0, it.c, pos, rk, P.key);
+    } else {
+      const ResidualRow rr = residual_row(it.c, it.mp, it.inv_sp, it.mq, it.inv_sq);
+      residual_vec<F32>(acc, x, z, v0, rr, pos, rk, P.key);
+    }
   }
   acc = warp_reduce(acc);
   return Partial{acc.v, 0.f, acc.idx, acc.nan};
@@ -1135,7 +1071,6 @@ __device__ void decide_chain(const Params& P, const Split& sp, const ReqInfo& q,
                              RowRes d, int y, const WaveRecs* recs = nullptr) {
   (void)sp;
   const int lane = threadIdx.x & 31;
-  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
   const bool sampling = q.c > 0.f;
   for (;;) {
     if (!sampling) {
@@ -1148,16 +1083,12 @@ __device__ void decide_chain(const Params& P, const Split& sp, const ReqInfo& q,
         return;
       }
     } else if (i == q.k) {
-      // every draft accepted: the element race inside the winning block
+      // every draft accepted: the bonus race's winner over the whole row
       if (t.bad || t.idx < 0) {
         skip_request_warp(P, q.r, q.d0, q.k, kStNonfinite);
         return;
       }
-      const char* trow =
-          reinterpret_cast<const char*>(P.target) + (size_t)(q.d0 + q.r + i) * row_bytes;
-      const ResidualRow rr{q.c, 0.f, 0.f, 0.f, 0.f};
-      const int token = inner_race<E, false>(P, trow, nullptr, t.idx, rr, (uint32_t)i, q.rk);
-      finish_request(P, q.r, q.d0, q.k, i, token, false);
+      finish_request(P, q.r, q.d0, q.k, i, t.idx, false);
       return;
     } else {
       if (t.bad || d.bad) {
@@ -1283,9 +1214,8 @@ __device__ void complete_row(const Params& P, const Split& sp, const QItem& it, 
 }
 
 // Completion of a residual segment: the CTA completing the count merges the
-// block race, runs the element race in the winning block and commits the
-// correction token (a residual without mass in fp32, i.e. p == q, draws from
-// p_j instead).
+// race over the row's segments and commits the correction token (a residual
+// without mass in fp32, i.e. p <= q everywhere, draws from p_j instead).
 template <typename E>
 __device__ void complete_residual(const Params& P, const Split& sp, const QItem& it,
                                   const Partial* mb) {
@@ -1310,16 +1240,9 @@ __device__ void complete_residual(const Params& P, const Split& sp, const QItem&
     merge_position(P, P.rpart, sp, it.e, false, kResidual, best, unused);
   }
   const int j = it.pos;
-  const RequestKey rk{it.req_lo, it.req_hi};
-  int token;
-  if (best.idx >= 0) {
-    const ResidualRow rr{it.c, it.mp, it.inv_sp, it.mq, it.inv_sq};
-    token = inner_race<E, true>(P, it.row, it.row2, best.idx, rr, (uint32_t)j, rk);
-  } else {
-    const ResidualRow rr{it.c, 0.f, 0.f, 0.f, 0.f};
-    const BestAcc br = warp_block_race<E>(P, it.row, it.c, (uint32_t)j, rk);
-    token = inner_race<E, false>(P, it.row, nullptr, br.idx, rr, (uint32_t)j, rk);
-  }
+  int token = best.idx;
+  if (token < 0)
+    token = warp_row_race<E>(P, it.row, it.c, (uint32_t)j, RequestKey{it.req_lo, it.req_hi});
   if (lane == 0) P.committed[(size_t)it.r * (P.max_k + 1) + j] = token;
 }
 
@@ -1328,9 +1251,21 @@ __device__ void complete_residual(const Params& P, const Split& sp, const QItem&
 // then of the row phase, cut at row boundaries and decoded lane-parallel.
 // ---------------------------------------------------------------------------
 struct SegGen {
-  int phase;                  // 0 residual, 1 rows, 2 done
+  int step;                   // 0, 1: the CTA's first and second phase; 2 done
+  int order;                  // 0: residual phase first; 1: row phase first
   unsigned long long x, x1;   // next block, end of the share
   int q_head, q_used;
+  __device__ __forceinline__ int phase() const { return step < 2 ? step ^ order : 2; }
+  // the CTA's share of its current phase (empty when it has none)
+  __device__ __forceinline__ void open(const Split* sp) {
+    const int ph = phase();
+    if (ph < 2 && (int)blockIdx.x < sp[ph].G) {
+      x = sp[ph].begin(blockIdx.x);
+      x1 = sp[ph].begin(blockIdx.x + 1);
+    } else {
+      x = x1 = 0ull;
+    }
+  }
 };
 
 // Queue entries are read from L2 (another CTA may have written them during
@@ -1427,7 +1362,7 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
       it.tee = (it.is_draft ? P.tee_draft : P.tee_target) + off;
   }
   if (kAligned) {
-    constexpr int kVPB = kRaceBlock / E::kVec;
+    constexpr int kVPB = kVocabBlock / E::kVec;
     it.vbeg = b0 * kVPB;
     it.vend = min(b1 * kVPB, P.nvec);
     const int per = it.kind == kResidual ? kThreads : kThreads * kStageVecs;
@@ -1438,7 +1373,7 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
     it.vbeg = b0;
     it.vend = b1;
     it.nst = 0;
-    const int by = it.y >= 0 ? it.y / kRaceBlock : -1;
+    const int by = it.y >= 0 ? it.y / kVocabBlock : -1;
     it.yv = (it.kind == kSoftmax && by >= b0 && by < b1) ? by : -1;
   }
 }
@@ -1457,19 +1392,16 @@ template <typename E, bool kAligned>
 __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* s_qend,
                            SegGen& sg) {
   const int lane = threadIdx.x & 31;
-  if (sg.phase < 2 && sg.q_head >= sg.q_used + kRefillAt) return;
-  while (sg.phase < 2 && sg.q_head < sg.q_used + kQueue - 2) {
+  if (sg.step < 2 && sg.q_head >= sg.q_used + kRefillAt) return;
+  while (sg.step < 2 && sg.q_head < sg.q_used + kQueue - 2) {
     const int room = min(8, kQueue - 2 - (sg.q_head - sg.q_used));
     // cut the next `room` segments (all lanes alike); lane j keeps the j-th
     int n = 0, my_phase = 0, my_e = 0, my_b0 = 0, my_b1 = 0;
-    while (n < room && sg.phase < 2) {
+    while (n < room && sg.step < 2) {
       if (sg.x >= sg.x1) {
         // next phase: the share of this CTA in it
-        ++sg.phase;
-        if (sg.phase == 1 && (int)blockIdx.x < sp[1].G) {
-          sg.x = sp[1].begin(blockIdx.x);
-          sg.x1 = sp[1].begin(blockIdx.x + 1);
-        }
+        ++sg.step;
+        sg.open(sp);
         continue;
       }
       const int e = (int)(sg.x / (unsigned long long)P.nb);
@@ -1478,7 +1410,7 @@ __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* 
       const unsigned long long end = sg.x1 < row0 + P.nb ? sg.x1 : row0 + P.nb;
       const int b1 = (int)(end - row0);
       if (lane == n) {
-        my_phase = sg.phase;
+        my_phase = sg.phase();
         my_e = e;
         my_b0 = b0;
         my_b1 = b1;
@@ -1497,7 +1429,7 @@ __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* 
   __syncwarp();
   if (lane == 0) {
     // queue entries before the count that publishes them
-    st_release_shared(s_qend, sg.phase >= 2 ? -1 - sg.q_head : sg.q_head);
+    st_release_shared(s_qend, sg.step >= 2 ? -1 - sg.q_head : sg.q_head);
   }
   __syncwarp();
 }
@@ -1572,10 +1504,6 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
   if (tid == 0) {
     s_layout = 0u;
     P.ctr[kCntStatus] = 0;
-    P.ctr[kCntClaim] = 0;
-    P.ctr[kCntNRes] = 0;
-    P.ctr[kCntURes] = 0;
-    P.ctr[kCntDone] = 0;
     P.ctr[kCntLive] = 0;
   }
   for (int i = tid; i < P.n_waves; i += kPlanThreads) {
@@ -1699,30 +1627,21 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
       } else {
         sampling = mode == kSampling;
         c = sampling ? kLog2e / t : 0.f;
-        n = P.cluster_mode ? 1 : wave_rows(P, sampling, k, 0);
+        n = wave_rows(P, sampling, k, 0);
       }
     }
     int tot;
     const int at = written + scan(n, &tot);
     if (n > 0) {
       const RequestKey rk = request_key(P, r);
-      for (int j = 0; j < n; ++j) {
+      for (int j = 0; j < n; ++j)
         P.lists[at + j] = wave_entry(P, sampling, r, d0, k, c, rk, 0, j, at, tokens);
-        if (P.stream_mode) P.ready_n[at + j] = P.epoch;
-      }
     }
     written += tot;
     live += __syncthreads_count(n > 0);
   }
-  if (P.stream_mode) {
-    // the stream schedule counts segments with plain atomics from zero
-    for (int i = tid; i < (P.max_k + 1) * P.batch; i += kPlanThreads)
-      P.pos_cnt[(size_t)(i / P.batch) * P.stride + i % P.batch] = 0ull;
-    for (int r = tid; r < P.batch; r += kPlanThreads) P.rcnt[r] = 0ull;
-  }
   if (tid == 0) {
     P.list_cnt[0] = written;
-    P.ctr[kCntNRes] = written;
     P.ctr[kCntLive] = live;
   }
 }
@@ -1756,15 +1675,15 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   const int c = blockIdx.x;
   if (c >= sp[0].G && c >= sp[1].G) return;  // no share in this wave
 
+  // Half of the CTAs (every other block of one CTA per SM, the way the
+  // block scheduler fills the SMs) take their row share first: an SM then
+  // runs the ALU-heavy correction draws of one CTA beside the streaming of
+  // another instead of both at once.
   SegGen sg;
-  sg.phase = 0;
+  sg.step = 0;
+  sg.order = (c / max(1, (int)gridDim.x / kMinBlocks)) & 1;
   sg.q_head = sg.q_used = 0;
-  if (c < sp[0].G) {
-    sg.x = sp[0].begin(c);
-    sg.x1 = sp[0].begin(c + 1);
-  } else {
-    sg.x = sg.x1 = 0ull;
-  }
+  sg.open(sp);
   if (control) fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
   __syncthreads();
 

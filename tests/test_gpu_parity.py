@@ -23,12 +23,11 @@ def _built():
     build.build()
 
 
-def _verifier(inp, dtype, max_batch=None, max_k=None, depth=0, schedule="auto"):
+def _verifier(inp, dtype, max_batch=None, max_k=None, depth=0):
     B = len(inp["num_draft"])
     V = inp["target"].shape[1]
     v = Verifier(max(1, max_batch or B), inp["max_k"] if max_k is None else max_k, V, dtype)
     v.set_depth(depth)
-    v.set_schedule(schedule)
     return v
 
 
@@ -36,10 +35,10 @@ def _dtype_of(inp):
     return "bf16" if inp["target"].dtype == np.uint16 else "f32"
 
 
-def _check(inp, seeds=(1,), max_batch=None, max_k=None, depth=0, schedule="auto"):
+def _check(inp, seeds=(1,), max_batch=None, max_k=None, depth=0):
     dtype = _dtype_of(inp)
     reps = []
-    with _verifier(inp, dtype, max_batch, max_k, depth, schedule) as v:
+    with _verifier(inp, dtype, max_batch, max_k, depth) as v:
         for seed in seeds:
             g = parity.run_gpu(v, inp, seed)
             o = parity.run_oracle(inp, seed)
@@ -55,9 +54,12 @@ def test_small_workloads_full_parity(name):
     inp = b.numpy_inputs()
     reps = _check(inp, seeds=(1, 2, 3, 4))
     total = sum(r["sampling"] + r["greedy"] for r in reps)
-    exempt = sum(r["exempt_accept"] + r["exempt_race"] + r["exempt_residual_mass"] for r in reps)
     print(name, reps)
-    assert exempt <= max(1, total // 100)
+    assert _exempt(reps) <= max(1, total // 100)
+
+
+def _exempt(reps):
+    return sum(r["exempt_accept"] + r["exempt_race"] + r["exempt_residual_mass"] for r in reps)
 
 
 @pytest.mark.parametrize("name", ["w2_v128256_bf16", "w3_v151936_bf16", "w4_v262144_bf16"])
@@ -66,33 +68,20 @@ def test_large_vocab_reduced_batch_parity(name):
     b = W.make_batch(name, device="cuda", batch=20)
     inp = b.numpy_inputs()
     reps = _check(inp, seeds=(1, 7))
+    reps += _check(inp, seeds=(3,), depth=1)
+    reps += _check(inp, seeds=(8,), depth=2)
     print(name, reps)
-    _check(inp, seeds=(3,), schedule="clusters")
-    _check(inp, seeds=(3,), schedule="waves")
-    _check(inp, seeds=(3, 8), schedule="stream")
+    assert _exempt(reps) <= max(1, sum(r["sampling"] + r["greedy"] for r in reps) // 100)
 
 
-def _slice_outputs(gpu, num_draft, idx):
-    d_off = np.concatenate([[0], np.cumsum(num_draft)])
-    sel = np.concatenate([np.arange(d_off[r], d_off[r + 1]) for r in idx]) if len(idx) else []
-    out = {"accepted_len": gpu["accepted_len"][idx], "committed": gpu["committed"][idx],
-           "flags": gpu["flags"][sel], "status": gpu["status"]}
-    for key in ("p_y", "q_y", "u"):
-        out[key] = gpu[key][sel]
-    out["req_status"] = gpu["req_status"][idx]
-    return out
-
-
-@pytest.mark.parametrize("schedule", ["auto", "stream"])
 @pytest.mark.parametrize("name", ["w2_v128256_bf16", "w3_v151936_bf16", "w4_v262144_bf16"])
-def test_full_size_workload_sampled_parity(name, schedule):
-    """Full batch in the benchmark's launch configuration; the oracle re-verifies
-    a sample of requests one by one (keyed by their batch index)."""
+def test_full_size_workload_parity(name):
+    """The full batch in the benchmark's launch configuration, every request
+    compared with the oracle; near-threshold exemptions stay under 1 %."""
     b = W.make_batch(name, device="cuda")
     seed = 1
     nd = b.num_draft.cpu().numpy()
     with Verifier(b.batch, b.max_k, b.vocab, b.dtype) as v:
-        v.set_schedule(schedule)
         res = v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, seed, debug=True)
         torch.cuda.synchronize()
         gpu = {"accepted_len": res.accepted_len.cpu().numpy(),
@@ -101,14 +90,12 @@ def test_full_size_workload_sampled_parity(name, schedule):
                "u": res.u.cpu().numpy(), "req_status": res.req_status.cpu().numpy(),
                "status": v.status()}
     assert gpu["status"] == 0
-    rng = np.random.default_rng(0)
-    idx = np.sort(rng.choice(b.batch, size=min(16, b.batch), replace=False))
-    idx = np.unique(np.concatenate([idx, [0, b.batch - 1]]))
-    sub = W.subset(b, idx)
-    inp = sub.numpy_inputs()
+    inp = b.numpy_inputs()
     o = parity.run_oracle(inp, seed)
-    rep = parity.compare(_slice_outputs(gpu, nd, idx), o, inp, seed)
+    rep = parity.compare(gpu, o, inp, seed)
     print(name, rep)
+    assert rep["sampling"] + rep["greedy"] == b.batch
+    assert _exempt([rep]) <= max(1, b.batch // 100)
     # invariants over the whole batch
     A = gpu["accepted_len"]
     assert (A >= 0).all() and (A <= nd).all()
@@ -170,76 +157,28 @@ def test_wave_depths(depth, dtype, vocab):
     _check(inp, seeds=(2, 5), depth=depth)
 
 
-@pytest.mark.parametrize("B", [5, 41, 300])
-@pytest.mark.parametrize("dtype,vocab", [("bf16", 4096), ("bf16", 16), ("f32", 3000),
-                                         ("bf16", 32000)])
-def test_cluster_schedule(B, dtype, vocab):
-    """The cluster launch (requests claimed by clusters, positions decided as
-    soon as their rows are read, correction drawn right after) against the
-    oracle: fewer requests than slots, a few per cluster, and many; a row
-    narrower than the cluster (16 ids: empty slices)."""
-    rng = np.random.default_rng(B + vocab)
-    k = rng.integers(0, 7, size=B)
-    temp = rng.choice([0.0, 0.6, 1.0, 1.3], size=B)
-    inp = cases.random_batch(k, temp, vocab=vocab, sigma_t=2.0, sigma_d=0.8, dtype=dtype,
-                             seed=B * 3 + vocab)
-    inp["max_k"] = 6
-    _check(inp, seeds=(2, 9), schedule="clusters")
-
-
-@pytest.mark.parametrize("B", [1, 5, 41, 300, 1500])
-@pytest.mark.parametrize("dtype,vocab", [("bf16", 4096), ("bf16", 16), ("f32", 3000),
-                                         ("bf16", 32000), ("f32", 1024)])
-def test_stream_schedule(B, dtype, vocab):
-    """The stream launch (rows queued by the decisions, consumed in bands that
-    every CTA splits alike, corrections through the urgent queue) against the
-    oracle: one request, a few, many, more bands than requests; rows narrower
-    than a CTA's share; ragged k with k = 0, greedy and sampling mixed."""
-    rng = np.random.default_rng(B * 11 + vocab)
-    k = rng.integers(0, 7, size=B)
-    temp = rng.choice([0.0, 0.6, 1.0, 1.3], size=B)
-    inp = cases.random_batch(k, temp, vocab=vocab, sigma_t=2.0, sigma_d=0.8, dtype=dtype,
-                             seed=B * 5 + vocab)
-    inp["max_k"] = 6
-    _check(inp, seeds=(2, 9), schedule="stream")
-
-
-@pytest.mark.parametrize("name", ["w0_v1024_f32", "w1_v32000_bf16"])
-def test_small_workloads_stream_schedule(name):
-    b = W.make_batch(name, device="cpu")
-    _check(b.numpy_inputs(), seeds=(1, 2, 3), schedule="stream")
-
-
-@pytest.mark.parametrize("name", ["w0_v1024_f32", "w1_v32000_bf16"])
-def test_small_workloads_cluster_schedule(name):
-    b = W.make_batch(name, device="cpu")
-    _check(b.numpy_inputs(), seeds=(1, 2), schedule="clusters")
-
-
 @pytest.mark.parametrize("depth", [1, 4])
 def test_small_workload_depths(depth):
     b = W.make_batch("w1_v32000_bf16", device="cpu")
     _check(b.numpy_inputs(), seeds=(1, 2), depth=depth)
 
 
-@pytest.mark.parametrize("schedule", ["auto", "stream"])
 @pytest.mark.parametrize("max_k", [15, 31])
-def test_long_windows(max_k, schedule):
+def test_long_windows(max_k):
     B = 9
     k = np.array([max_k] * 4 + [0, 1, max_k // 2, max_k, 3])
     temp = np.array([1.0, 0.8, 0.0, 1.0, 1.0, 0.0, 0.9, 1.0, 0.7])
     inp = cases.random_batch(k, temp, vocab=2048, sigma_t=2.0, sigma_d=0.3, dtype="bf16", seed=5)
     inp["max_k"] = max_k
-    _check(inp, seeds=(1, 2), schedule=schedule)
+    _check(inp, seeds=(1, 2))
 
 
-@pytest.mark.parametrize("schedule", ["auto", "stream"])
-def test_identical_and_disjoint_rows(schedule):
+def test_identical_and_disjoint_rows():
     inp = cases.random_batch([4] * 16, [0.9] * 16, vocab=3000, dtype="bf16", seed=8)
     t_off = np.concatenate([[0], np.cumsum(inp["num_draft"] + 1)])
     src = np.concatenate([np.arange(t_off[r], t_off[r] + 4) for r in range(16)])
     inp["draft"] = inp["target"][src].copy()
-    with _verifier(inp, "bf16", schedule=schedule) as v:
+    with _verifier(inp, "bf16") as v:
         g = parity.run_gpu(v, inp, 4)
     assert (g["accepted_len"] == 4).all()
     V, B = 64, 100
@@ -249,20 +188,19 @@ def test_identical_and_disjoint_rows(schedule):
     drf[:, 32:] = 0.0
     inp = dict(target=tgt, draft=drf, tokens=(32 + np.arange(B) % 32).astype(np.int32),
                num_draft=np.ones(B, np.int32), temperature=np.ones(B, np.float32), max_k=1)
-    reps = _check(inp, seeds=(1,), schedule=schedule)
-    with _verifier(inp, "f32", schedule=schedule) as v:
+    reps = _check(inp, seeds=(1,))
+    with _verifier(inp, "f32") as v:
         g = parity.run_gpu(v, inp, 1)
     assert (g["accepted_len"] == 0).all() and (g["committed"][:, 0] < 32).all()
 
 
-@pytest.mark.parametrize("schedule", ["auto", "stream"])
-def test_greedy_only_without_draft_logits(schedule):
+def test_greedy_only_without_draft_logits():
     inp = cases.random_batch([3, 0, 5, 2], [0.0] * 4, vocab=5000, dtype="bf16", seed=2)
     inp["max_k"] = 5
     o = parity.run_oracle(inp, 1)
     inp2 = dict(inp)
     inp2["draft"] = None
-    with _verifier(inp2, "bf16", schedule=schedule) as v:
+    with _verifier(inp2, "bf16") as v:
         g = parity.run_gpu(v, inp2, 1)
     assert g["status"] == 0
     assert (g["committed"] == o["committed"]).all() and (g["accepted_len"] == o["accepted_len"]).all()
@@ -274,7 +212,7 @@ def test_all_zero_drafts_and_empty_batch():
     _check(inp, seeds=(1, 2))
     inp = cases.random_batch([0] * 10, [1.0] * 5 + [0.0] * 5, vocab=776, dtype="bf16", seed=3)
     inp["max_k"] = 2
-    _check(inp, seeds=(1, 2), schedule="stream")
+    _check(inp, seeds=(1, 2))
     with Verifier(4, 2, 777, "bf16") as v:
         e = torch.empty(0, dtype=torch.int32, device="cuda")
         res = v.run(torch.empty(0, 777, dtype=torch.bfloat16, device="cuda"), None, e, e,
@@ -282,15 +220,14 @@ def test_all_zero_drafts_and_empty_batch():
         assert res.accepted_len.numel() == 0
 
 
-@pytest.mark.parametrize("depth,schedule", [(1, "waves"), (2, "waves"), (6, "waves"),
-                                            (0, "clusters"), (0, "stream")])
-def test_rows_after_the_first_rejection_do_not_matter(depth, schedule):
+@pytest.mark.parametrize("depth", [1, 2, 6])
+def test_rows_after_the_first_rejection_do_not_matter(depth):
     """Garbage (NaN / +inf) in rows beyond the first rejection changes nothing:
     at depth 1 those rows are never read; at larger depths they may be read but
     their positions are never decided."""
     inp = cases.random_batch([5] * 48, [1.0] * 24 + [0.0] * 24, vocab=4096, sigma_d=2.5,
                              dtype="bf16", seed=13)
-    with _verifier(inp, "bf16", depth=depth, schedule=schedule) as v:
+    with _verifier(inp, "bf16", depth=depth) as v:
         base = parity.run_gpu(v, inp, 5)
         A = base["accepted_len"]
         k = inp["num_draft"]
@@ -323,18 +260,16 @@ def test_invalid_inputs_status_and_skip():
     # and the bonus row is read), and a bonus row without a finite logit
     bad["draft"][6 * 2:6 * 2 + 2] = bad["target"][6 * 3:6 * 3 + 2]
     bad["target"][6 * 3 + 2, :] = -np.inf
-    _check(bad, seeds=(1,))
-    for schedule in ("waves", "clusters", "stream"):
-        _check(bad, seeds=(1,), schedule=schedule)
-        with _verifier(bad, "f32", schedule=schedule) as v:
+    for depth in (0, 1):
+        _check(bad, seeds=(1,), depth=depth)
+        with _verifier(bad, "f32", depth=depth) as v:
             g = parity.run_gpu(v, bad, 1)
         assert g["status"] == (oracle.BAD_TOKEN | oracle.BAD_TEMP | oracle.NONFINITE)
         assert g["accepted_len"][0] >= 0 and (g["accepted_len"][1:] == -1).all()
     # layout errors skip the whole batch
     wrong = dict(inp)
     wrong["num_draft"] = np.array([2, 2, 2, 2, 2, 2, 3], np.int32)   # k > max_k
-    for schedule in ("auto", "stream"):
-        _layout_errors(inp, wrong, schedule)
+    _layout_errors(inp, wrong)
     nod = dict(inp)
     nod["draft"] = None
     with _verifier(inp, "f32") as v:
@@ -343,8 +278,8 @@ def test_invalid_inputs_status_and_skip():
     assert (g["accepted_len"][[0, 1, 3, 4, 5, 6]] == -1).all() and g["accepted_len"][2] >= 0
 
 
-def _layout_errors(inp, wrong, schedule):
-    with _verifier(inp, "f32", schedule=schedule) as v:
+def _layout_errors(inp, wrong):
+    with _verifier(inp, "f32") as v:
         t = parity.to_torch(wrong, "cuda")
         res = v.run(t["target"], t["draft"], t["tokens"], t["num_draft"], t["temperature"], 1,
                     total_draft=14)
@@ -448,3 +383,22 @@ def test_run_host_matches_device_run(mode, pinned, in_place):
         assert torch.equal(acc, dev.accepted_len.cpu())
         assert torch.equal(com, dev.committed.cpu())
         assert torch.equal(flg, dev.flags.cpu())
+
+
+# --- round tags ---------------------------------------------------------------------------
+
+def test_rounds_across_the_round_tag_wrap():
+    """Completion counters carry a 32-bit round tag; five rounds from 0xfffffffd
+    cross the wrap (counters cleared, numbering restarted at 1), alternating
+    one-wave-per-position and all-positions-in-one-wave rounds, and each
+    matches the oracle."""
+    b = W.make_batch("w1_v32000_bf16", device="cpu", batch=64)
+    inp = b.numpy_inputs()
+    with _verifier(inp, "bf16") as v:
+        parity.run_gpu(v, inp, 1)
+        v.debug_set_epoch(0xfffffffd)
+        for i, seed in enumerate(range(1, 6)):
+            v.set_depth(1 if i % 2 else 0)
+            g = parity.run_gpu(v, inp, seed)
+            rep = parity.compare(g, parity.run_oracle(inp, seed), inp, seed)
+            assert _exempt([rep]) <= 1, (seed, rep)

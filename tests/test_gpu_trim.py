@@ -1,5 +1,5 @@
 """Trimmed verify rounds (specverify_run_trimmed) against the oracle's trimmed
-verify, element by element, on every schedule."""
+verify, element by element, at the chosen and the one-position wave depths."""
 import numpy as np
 import pytest
 import torch
@@ -31,12 +31,12 @@ def run_trimmed_gpu(v, inp, conf, cost, seed):
             "verified_k": res.verified_k.cpu().numpy()}
 
 
-def check(inp, conf, cost, seeds, schedule="auto", dtype=None):
+def check(inp, conf, cost, seeds, depth=0, dtype=None):
     dtype = dtype or ("bf16" if inp["target"].dtype == np.uint16 else "f32")
     B = len(inp["num_draft"])
     reps = []
     with Verifier(max(B, 1), inp["max_k"], inp["target"].shape[1], dtype) as v:
-        v.set_schedule(schedule)
+        v.set_depth(depth)
         for seed in seeds:
             g = run_trimmed_gpu(v, inp, conf, cost, seed)
             o = oracle.verify_trimmed(inp["target"], inp.get("draft"), inp["tokens"],
@@ -61,12 +61,12 @@ def batch(B, vocab, dtype, seed, max_k=6):
     return inp, conf, cost
 
 
-@pytest.mark.parametrize("schedule", ["auto", "stream", "clusters"])
+@pytest.mark.parametrize("depth", [0, 1])
 @pytest.mark.parametrize("dtype,vocab", [("bf16", 4096), ("f32", 3000), ("bf16", 1001),
                                          ("bf16", 32000)])
-def test_trimmed_rounds(schedule, dtype, vocab):
+def test_trimmed_rounds(depth, dtype, vocab):
     inp, conf, cost = batch(45, vocab, dtype, vocab + 3)
-    reps = check(inp, conf, cost, (1, 4), schedule=schedule)
+    reps = check(inp, conf, cost, (1, 4), depth=depth)
     assert sum(r["exempt_accept"] + r["exempt_race"] for r in reps) <= 2
 
 
