@@ -393,10 +393,31 @@ __device__ __forceinline__ void race_words_n(uint4 (&r)[N], const uint32_t (&g)[
   }
 }
 
-// The exact gain of a word that passed its bound: kept out of line, since it
-// is rare and its code (two logarithms) would otherwise be copied into every
-// element's slot.
-__device__ __noinline__ float race_gain_slow(uint32_t w) { return race_gain(w); }
+// The race's best score so far, shared by the warps that reduce one segment
+// (a shared-memory word per mailbox slot, raised with atomicMax): every warp
+// then prunes with the best any of them has found.  Floats map to unsigned
+// words in the same order.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float from_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+constexpr uint32_t kOrderKeyNegInf = 0x007fffffu;  // order_key(-inf)
+
+struct SharedBest {
+  uint32_t* word;  // the segment's mailbox-slot word
+  __device__ __forceinline__ float load() const {
+    return from_order_key(*reinterpret_cast<volatile uint32_t*>(word));
+  }
+  __device__ __forceinline__ void raise(float v) const {
+    if ((threadIdx.x & 31) == 0) atomicMax(word, order_key(v));
+  }
+};
+
+// Smallest gain any word can have: E < 22.9, so -log2 E > -4.52.
+constexpr float kMinGain = -4.52f;
 
 // A race score enters the best only when finite: an id of zero weight (a
 // logit of -inf, or a residual that underflows) never wins, even against an
@@ -412,7 +433,8 @@ __device__ __forceinline__ void take_finite(BestAcc& acc, float score, int i) {
 // tests against the warp's best, not only its own.  The test keeps ties
 // (>=), which take_cmp then orders by index.  Call with the whole warp.
 template <typename E>
-__device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const float (&x0)[E::kVec],
+__device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const SharedBest& sb,
+                                           const float (&x0)[E::kVec],
                                            const float (&x1)[E::kVec], int e0, int e1, float c,
                                            uint32_t pos, RequestKey rk, PhiloxKey key) {
   constexpr int G = E::kVec / 4;  // Philox blocks per vector
@@ -422,6 +444,13 @@ __device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const flo
 #pragma unroll
   for (int i = 0; i < E::kVec; ++i) mx = fmax_nan(mx, x1[i]);
   acc.nan |= !(mx < -kNegInf);  // NaN or +inf
+  wbest = fmaxf(wbest, sb.load());
+  if (wbest == kNegInf) {
+    // first stage: the largest logit seen, with the smallest gain any word can
+    // have, is a score some id reaches, so the winner's score is at least that
+    const float lo = warp_max(mx < -kNegInf ? mx : kNegInf) * c + kMinGain;
+    if (lo > kNegInf) wbest = lo - kBoundSlack;
+  }
   if (!__any_sync(0xffffffffu, fmaf(mx, c, kMaxGain) >= wbest)) return;
   uint32_t g[2 * G];
 #pragma unroll
@@ -442,23 +471,26 @@ __device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const flo
     for (int i = 0; i < E::kVec; ++i) {
       const uint32_t w = word_of(r[i >> 2], i & 3);
       if (fmaf(x0[i], c, race_gain_bound(w)) >= wbest)
-        take_finite(acc, fmaf(x0[i], c, race_gain_slow(w)), e0 + i);
+        take_finite(acc, fmaf(x0[i], c, race_gain(w)), e0 + i);
     }
 #pragma unroll
     for (int i = 0; i < E::kVec; ++i) {
       const uint32_t w = word_of(r[G + (i >> 2)], i & 3);
       if (fmaf(x1[i], c, race_gain_bound(w)) >= wbest)
-        take_finite(acc, fmaf(x1[i], c, race_gain_slow(w)), e1 + i);
+        take_finite(acc, fmaf(x1[i], c, race_gain(w)), e1 + i);
     }
   }
-  if (__any_sync(0xffffffffu, pass)) wbest = warp_max(acc.v);
+  if (__any_sync(0xffffffffu, pass)) {
+    wbest = fmaxf(wbest, warp_max(acc.v));
+    sb.raise(wbest);
+  }
 }
 
 // Residual race over one stage: vector x of t_j and z of d_j, the same kVec
 // ids from e0.  fmaf(x, c, rr.lp) bounds log2 (p_v - q_v) from above, so the
 // two exponentials are only taken for ids that pass.  Call with the whole warp.
 template <typename E>
-__device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
+__device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest, const SharedBest& sb,
                                                const float (&x)[E::kVec],
                                                const float (&z)[E::kVec], int e0,
                                                const ResidualRow& rr, uint32_t pos,
@@ -467,6 +499,7 @@ __device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
   float mx = x[0];
 #pragma unroll
   for (int i = 1; i < E::kVec; ++i) mx = fmaxf(mx, x[i]);
+  wbest = fmaxf(wbest, sb.load());
   if (!__any_sync(0xffffffffu, fmaf(mx, rr.c, rr.lp) + kMaxGain >= wbest)) return;
   uint32_t g[G];
 #pragma unroll
@@ -485,11 +518,14 @@ __device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
         const float p = fast_ex2(fmaf(x[i], rr.c, -rr.mp)) * rr.inv_sp;
         const float q = fast_ex2(fmaf(z[i], rr.c, -rr.mq)) * rr.inv_sq;
         const float d = p - q;
-        if (d > 0.f) take_finite(acc, fast_lg2(d) + race_gain_slow(w), e0 + i);
+        if (d > 0.f) take_finite(acc, fast_lg2(d) + race_gain(w), e0 + i);
       }
     }
   }
-  if (__any_sync(0xffffffffu, pass)) wbest = warp_max(acc.v);
+  if (__any_sync(0xffffffffu, pass)) {
+    wbest = fmaxf(wbest, warp_max(acc.v));
+    sb.raise(wbest);
+  }
 }
 
 // The race over a whole row by one warp with plain loads (lane l takes ids
@@ -583,7 +619,7 @@ __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend,
 // `take(v0, v1)` hands over the next stage of the segment from the copy ring.
 template <typename E, typename Take>
 __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm, float* s_xy,
-                                              Take& take) {
+                                              uint32_t* s_best, Take& take) {
   const int w = threadIdx.x >> 5;
   const int tid = threadIdx.x;
   // the segment's fields in registers (the queue is shared memory, which the
@@ -668,7 +704,7 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       float x0[E::kVec], x1[E::kVec];
       E::unpack(v[0], x0);
       E::unpack(v[1], x1);
-      race_stage<E>(acc, wbest, x0, x1, vi * E::kVec, (vi + kThreads) * E::kVec, c,
+      race_stage<E>(acc, wbest, SharedBest{s_best}, x0, x1, vi * E::kVec, (vi + kThreads) * E::kVec, c,
                     (uint32_t)pos, rk, P.key);
     }
   } else {
@@ -685,7 +721,8 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       float x[E::kVec], z[E::kVec];
       E::unpack(v[0], x);
       E::unpack(v[1], z);
-      residual_stage<E>(acc, wbest, x, z, vi * E::kVec, rr, (uint32_t)pos, rk, P.key);
+      residual_stage<E>(acc, wbest, SharedBest{s_best}, x, z, vi * E::kVec, rr, (uint32_t)pos, rk,
+                        P.key);
     }
   }
   acc = warp_reduce(acc);
@@ -695,9 +732,10 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
 template <typename E>
 __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
                                                const int* s_qend, uint4* ring, LoadCursor& lc,
-                                               int& gs, const QItem& itm, float* s_xy) {
+                                               int& gs, const QItem& itm, float* s_xy,
+                                               uint32_t* s_best) {
   auto take = [&](uint4& v0, uint4& v1) { ring_take(queue, s_qend, ring, lc, gs, v0, v1); };
-  return seg_reduce<E>(P, itm, s_xy, take);
+  return seg_reduce<E>(P, itm, s_xy, s_best, take);
 }
 
 // Scalar path (rows not 16-byte aligned): warp w takes vocab blocks
@@ -1659,6 +1697,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   __shared__ QItem queue[kQueue];
   __shared__ Partial mailbox[kMailSlots][kComputeWarps];
   __shared__ float s_xy[kMailSlots];
+  __shared__ uint32_t s_best[kMailSlots];  // race best of the slot's segment (order key)
   __shared__ int s_qend;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -1685,6 +1724,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   sg.q_head = sg.q_used = 0;
   sg.open(sp);
   if (control) fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
+  if (tid < kMailSlots) s_best[tid] = kOrderKeyNegInf;
   __syncthreads();
 
   // Segment u travels through mailbox slot u % kMailSlots.  The compute warps
@@ -1718,7 +1758,8 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
       if (u >= (qe >= 0 ? qe : -1 - qe)) break;  // only once the count is final
       const QItem& it = queue[u & (kQueue - 1)];
       const Partial out = kAligned
-                              ? seg_aligned<E>(P, queue, &s_qend, ring, lc, gs, it, &s_xy[slot])
+                              ? seg_aligned<E>(P, queue, &s_qend, ring, lc, gs, it, &s_xy[slot],
+                                               &s_best[slot])
                               : seg_scalar<E>(P, it, &s_xy[slot]);
       if ((tid & 31) == 0) mailbox[slot][warp] = out;
       named_bar_arrive(kBarReady + slot, kCtaThreads);
@@ -1737,6 +1778,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
       }
       sg.q_used = u + 1;  // its queue entry may now be reused
       fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
+      if ((tid & 31) == 0) s_best[slot] = kOrderKeyNegInf;  // for segment u + kMailSlots
       if (u + kMailSlots <= sg.q_head) named_bar_arrive(kBarFree + slot, kCtaThreads);
     }
   }
