@@ -47,7 +47,7 @@ struct DeviceGuard {
 // The epoch-tagged completion counters come first, so that one memset of
 // `tagged` bytes clears them all.
 struct ScratchLayout {
-  size_t lists, lcnt, res, rcnt, pos, rescnt, part, rpart, ctr, recs, rdy;
+  size_t lists, lcnt, blists, blcnt, res, rcnt, pos, rescnt, part, bpart, rpart, ctr, recs, rdy;
   size_t list_entries, tagged, bytes;
 };
 
@@ -81,12 +81,18 @@ constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid) {
   off = align_up(off + sizeof(sv::Entry) * list_entries, 256);
   L.lcnt = off;
   off = align_up(off + sizeof(int) * max_waves, 256);
+  L.blists = off;
+  off = align_up(off + sizeof(sv::Entry) * max_waves * mb, 256);
+  L.blcnt = off;
+  off = align_up(off + sizeof(int) * max_waves, 256);
   L.res = off;
   off = align_up(off + sizeof(sv::ResEntry) * max_waves * mb, 256);
   L.rcnt = off;
   off = align_up(off + sizeof(int) * max_waves, 256);
   L.part = off;
   off = align_up(off + sizeof(sv::Partial) * (grid + max_cap), 256);
+  L.bpart = off;
+  off = align_up(off + sizeof(sv::Partial) * (grid + mb), 256);
   L.rpart = off;
   off = align_up(off + sizeof(sv::Partial) * (grid + mb), 256);
   L.ctr = off;
@@ -101,6 +107,9 @@ constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid) {
 struct Scratch {
   sv::Entry* lists;
   int* list_cnt;
+  sv::Entry* blists;
+  int* blist_cnt;
+  sv::Partial* bpart;
   sv::ResEntry* res;
   int* res_cnt;
   unsigned long long* pos_cnt;  // epoch-tagged: must start at zero
@@ -118,6 +127,9 @@ Scratch scratch_at(char* b, const ScratchLayout& L) {
   Scratch s;
   s.lists = reinterpret_cast<sv::Entry*>(b + L.lists);
   s.list_cnt = reinterpret_cast<int*>(b + L.lcnt);
+  s.blists = reinterpret_cast<sv::Entry*>(b + L.blists);
+  s.blist_cnt = reinterpret_cast<int*>(b + L.blcnt);
+  s.bpart = reinterpret_cast<sv::Partial*>(b + L.bpart);
   s.res = reinterpret_cast<sv::ResEntry*>(b + L.res);
   s.res_cnt = reinterpret_cast<int*>(b + L.rcnt);
   s.pos_cnt = reinterpret_cast<unsigned long long*>(b + L.pos);
@@ -360,6 +372,9 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
   P.verified_k = a.verified_k;
   P.lists = c.sc.lists;
   P.list_cnt = c.sc.list_cnt;
+  P.blists = c.sc.blists;
+  P.blist_cnt = c.sc.blist_cnt;
+  P.bpart = c.sc.bpart;
   P.res = c.sc.res;
   P.res_cnt = c.sc.res_cnt;
   P.pos_cnt = c.sc.pos_cnt;

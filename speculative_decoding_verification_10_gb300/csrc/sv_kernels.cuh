@@ -167,13 +167,16 @@ struct Params {
   float* q_y;
   float* u_dbg;
   int32_t* req_status;
-  Entry* lists;                 // [n_waves * list_cap] rows of each wave
+  Entry* lists;                 // [n_waves * list_cap] rows of each wave (bonus rows apart)
   int* list_cnt;                // [n_waves]
+  Entry* blists;                // [n_waves * stride] bonus rows of each wave
+  int* blist_cnt;               // [n_waves]
   ResEntry* res;                // [n_waves * stride] rejections of each wave
   int* res_cnt;                 // [n_waves]
   unsigned long long* pos_cnt;  // [(max_k + 1) * stride] epoch | count of a position
   unsigned long long* rcnt;     // [stride] epoch | residual segments merged
   Partial* part;                // [grid + list_cap] row segment partials
+  Partial* bpart;               // [grid + stride] bonus-row segment partials
   Partial* rpart;               // [grid + stride] residual segment partials
   int* ctr;                     // [kCntCount]
   PosRec* recs;                 // [(max_k + 1) * stride] merged rows of multi-position waves
@@ -256,6 +259,7 @@ struct __align__(16) QItem {
   float mp, inv_sp, mq, inv_sq;  // residual segments: normalisers of p_j and q_j
   uint32_t req_lo, req_hi;
   int e0;    // entry e of the phase is partial slot CTA + e0 + e
+  int phase;  // 0 correction draws, 1 rows, 2 bonus rows
   char* tee;  // where a softmax segment's row is copied (Params::tee_*), or NULL
 };
 
@@ -804,6 +808,11 @@ __device__ __forceinline__ int wave_rows(const Params& P, bool sampling, int k, 
   if (!sampling) return last - s + 1;
   return 2 * (min(s + P.depth, k) - s) + (last == k ? 1 : 0);
 }
+// Whether the last of those rows is a bonus row (sampling, position k in the
+// wave); bonus rows go to the wave's bonus list, the others to its row list.
+__device__ __forceinline__ bool wave_has_bonus(const Params& P, bool sampling, int k, int s) {
+  return sampling && min(s + P.depth - 1, k) == k;
+}
 
 // The j-th of those rows, as a list entry.
 __device__ __forceinline__ Entry wave_entry(const Params& P, bool sampling, int r, int d0, int k,
@@ -844,13 +853,20 @@ __device__ void append_next_wave(const Params& P, const ReqInfo& q, int next) {
   const int lane = threadIdx.x & 31;
   const bool sampling = q.c > 0.f;
   const int n = wave_rows(P, sampling, q.k, next);
+  const bool bonus = wave_has_bonus(P, sampling, q.k, next);
+  const int nm = n - (bonus ? 1 : 0);
   const int w1 = P.wave + 1;
-  int at = 0;
-  if (lane == 0) at = atomicAdd(P.list_cnt + w1, n);
+  int at = 0, bat = 0;
+  if (lane == 0 && nm > 0) at = atomicAdd(P.list_cnt + w1, nm);
+  if (lane == 0 && bonus) bat = atomicAdd(P.blist_cnt + w1, 1);
   at = __shfl_sync(0xffffffffu, at, 0);
+  bat = __shfl_sync(0xffffffffu, bat, 0);
   Entry* list = P.lists + (size_t)w1 * P.list_cap;
-  for (int j = lane; j < n; j += 32)
+  for (int j = lane; j < nm; j += 32)
     list[at + j] = wave_entry(P, sampling, q.r, q.d0, q.k, q.c, q.rk, next, j, at, P.tokens);
+  if (lane == 0 && bonus)
+    P.blists[(size_t)w1 * P.stride + bat] =
+        wave_entry(P, sampling, q.r, q.d0, q.k, q.c, q.rk, next, nm, bat, P.tokens);
 }
 
 // ---------------------------------------------------------------------------
@@ -1189,8 +1205,8 @@ __device__ void decide_chain(const Params& P, const Split& sp, const ReqInfo& q,
 // Completion of a row segment: partial out; the CTA that completes the count
 // of the segment's position merges the position's rows and decides it.
 template <typename E>
-__device__ void complete_row(const Params& P, const Split& sp, const QItem& it, const Partial* mb,
-                             float xy) {
+__device__ void complete_row(const Params& P, const Split& sp, Partial* parts, const QItem& it,
+                             const Partial* mb, float xy) {
   const int lane = threadIdx.x & 31;
   Partial p;
   if (it.kind == kSoftmax) {
@@ -1210,7 +1226,7 @@ __device__ void complete_row(const Params& P, const Split& sp, const QItem& it, 
   } else {
     int last = 0;
     if (lane == 0) {
-      P.part[it.g] = p;
+      parts[it.g] = p;
       fence_acq_rel_gpu();
       last = epoch_add(P.pos_cnt + (size_t)i * P.stride + it.r, P.epoch) == (uint32_t)target;
       if (last) fence_acq_rel_gpu();  // acquire: every writer's data is visible here
@@ -1218,7 +1234,7 @@ __device__ void complete_row(const Params& P, const Split& sp, const QItem& it, 
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
     __syncwarp();  // ... and, past the warp barrier, to every lane
-    merge_position(P, P.part, sp, et, it.paired != 0, tkind, t, d);
+    merge_position(P, parts, sp, et, it.paired != 0, tkind, t, d);
   }
   const ReqInfo q{it.r, it.d0, it.k, it.base, it.c, RequestKey{it.req_lo, it.req_hi}};
   // positions of this request in this wave: each is merged where its last
@@ -1288,16 +1304,20 @@ __device__ void complete_residual(const Params& P, const Split& sp, const QItem&
 // Segment generation (control warp): the CTA's share of the residual phase,
 // then of the row phase, cut at row boundaries and decoded lane-parallel.
 // ---------------------------------------------------------------------------
+// A CTA takes its share of three phases, each split flat over the grid on its
+// own so that every CTA gets the same part of each kind of work: the
+// correction draws (ALU-bound), the bonus rows (ALU-bound races) and the
+// other rows (bound by memory).
+constexpr int kPhases = 3;
 struct SegGen {
-  int step;                   // 0, 1: the CTA's first and second phase; 2 done
-  int order;                  // 0: residual phase first; 1: row phase first
+  int step;                   // 0, 1, 2: phases 0, 2, 1 in turn; kPhases once done
   unsigned long long x, x1;   // next block, end of the share
   int q_head, q_used;
-  __device__ __forceinline__ int phase() const { return step < 2 ? step ^ order : 2; }
+  __device__ __forceinline__ int phase() const { return step == 0 ? 0 : (step == 1 ? 2 : 1); }
   // the CTA's share of its current phase (empty when it has none)
   __device__ __forceinline__ void open(const Split* sp) {
-    const int ph = phase();
-    if (ph < 2 && (int)blockIdx.x < sp[ph].G) {
+    const int ph = step < kPhases ? phase() : 0;
+    if (step < kPhases && (int)blockIdx.x < sp[ph].G) {
       x = sp[ph].begin(blockIdx.x);
       x1 = sp[ph].begin(blockIdx.x + 1);
     } else {
@@ -1342,8 +1362,8 @@ __device__ __forceinline__ ResEntry ldcg_res(const ResEntry* p) {
   return r;
 }
 
-// Entry e of a phase is res[e] (phase 0) or list[e] (phase 1); its segment
-// partials go to slot CTA + e0 + e.
+// Entry e of a phase is res[e] (phase 0) or list[e] (phase 1: the row list,
+// phase 2: the bonus list); its segment partials go to slot CTA + e0 + e.
 template <typename E, bool kAligned>
 __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1, QItem& it,
                                const ResEntry* res, const Entry* list, int e0) {
@@ -1351,6 +1371,7 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
   it.e = e;
   it.g = (int)blockIdx.x + e0 + e;
   it.e0 = e0;
+  it.phase = phase;
   it.mp = it.inv_sp = it.mq = it.inv_sq = 0.f;
   it.row2 = nullptr;
   it.tee = nullptr;
@@ -1430,12 +1451,12 @@ template <typename E, bool kAligned>
 __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* s_qend,
                            SegGen& sg) {
   const int lane = threadIdx.x & 31;
-  if (sg.step < 2 && sg.q_head >= sg.q_used + kRefillAt) return;
-  while (sg.step < 2 && sg.q_head < sg.q_used + kQueue - 2) {
+  if (sg.step < kPhases && sg.q_head >= sg.q_used + kRefillAt) return;
+  while (sg.step < kPhases && sg.q_head < sg.q_used + kQueue - 2) {
     const int room = min(8, kQueue - 2 - (sg.q_head - sg.q_used));
     // cut the next `room` segments (all lanes alike); lane j keeps the j-th
     int n = 0, my_phase = 0, my_e = 0, my_b0 = 0, my_b1 = 0;
-    while (n < room && sg.step < 2) {
+    while (n < room && sg.step < kPhases) {
       if (sg.x >= sg.x1) {
         // next phase: the share of this CTA in it
         ++sg.step;
@@ -1460,14 +1481,16 @@ __device__ void fill_queue(const Params& P, const Split* sp, QItem* queue, int* 
     if (lane < n)
       decode_segment<E, kAligned>(P, my_phase, my_e, my_b0, my_b1, it,
                                   P.res + (P.wave > 0 ? (size_t)(P.wave - 1) * P.stride : 0),
-                                  P.lists + (size_t)P.wave * P.list_cap, 0);
+                                  my_phase == 2 ? P.blists + (size_t)P.wave * P.stride
+                                                : P.lists + (size_t)P.wave * P.list_cap,
+                                  0);
     if (lane < n) queue[(sg.q_head + lane) & (kQueue - 1)] = it;
     sg.q_head += n;
   }
   __syncwarp();
   if (lane == 0) {
     // queue entries before the count that publishes them
-    st_release_shared(s_qend, sg.step >= 2 ? -1 - sg.q_head : sg.q_head);
+    st_release_shared(s_qend, sg.step >= kPhases ? -1 - sg.q_head : sg.q_head);
   }
   __syncwarp();
 }
@@ -1546,6 +1569,7 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
   }
   for (int i = tid; i < P.n_waves; i += kPlanThreads) {
     P.list_cnt[i] = 0;
+    P.blist_cnt[i] = 0;
     P.res_cnt[i] = 0;
   }
   __syncthreads();
@@ -1619,8 +1643,9 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
     return;
   }
 
-  // per request: the input checks, then its rows of wave 0
-  int written = 0, live = 0;
+  // per request: the input checks, then its rows of wave 0 (the bonus row, if
+  // the wave reaches position k, in the bonus list)
+  int written = 0, bwritten = 0, live = 0;
 #pragma unroll
   for (int b = 0; b < kPer; ++b) {
     const int base = b * kPlanThreads;
@@ -1628,7 +1653,7 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
     const int r = base + tid;
     int n = 0, d0 = 0, k = 0;
     float c = 0.f;
-    bool sampling = false;
+    bool sampling = false, bonus = false;
     if (r < P.batch) {
       d0 = s_doff[r];
       const int K = s_doff[r + 1] - d0;  // the window's layout
@@ -1666,20 +1691,26 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
         sampling = mode == kSampling;
         c = sampling ? kLog2e / t : 0.f;
         n = wave_rows(P, sampling, k, 0);
+        bonus = wave_has_bonus(P, sampling, k, 0);
       }
     }
-    int tot;
-    const int at = written + scan(n, &tot);
+    const int nm = n - (bonus ? 1 : 0);
+    int tot, btot;
+    const int at = written + scan(nm, &tot);
+    const int bat = bwritten + scan(bonus ? 1 : 0, &btot);
     if (n > 0) {
       const RequestKey rk = request_key(P, r);
-      for (int j = 0; j < n; ++j)
+      for (int j = 0; j < nm; ++j)
         P.lists[at + j] = wave_entry(P, sampling, r, d0, k, c, rk, 0, j, at, tokens);
+      if (bonus) P.blists[bat] = wave_entry(P, sampling, r, d0, k, c, rk, 0, nm, bat, tokens);
     }
     written += tot;
+    bwritten += btot;
     live += __syncthreads_count(n > 0);
   }
   if (tid == 0) {
     P.list_cnt[0] = written;
+    P.blist_cnt[0] = bwritten;
     P.ctr[kCntLive] = live;
   }
 }
@@ -1707,20 +1738,18 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   pdl_wait();               // the previous launch's lists are complete
 
   const int n_rows = P.list_cnt[P.wave];
+  const int n_bonus = P.blist_cnt[P.wave];
   const int n_res = P.wave > 0 ? P.res_cnt[P.wave - 1] : 0;
-  Split sp[2];
+  Split sp[kPhases];
   sp[0].init(n_res, P.nb, P.min_span_res, gridDim.x);
   sp[1].init(n_rows, P.nb, P.min_span, gridDim.x);
+  // a race costs about four times a softmax per byte: shares of a quarter
+  sp[2].init(n_bonus, P.nb, max(1, P.min_span / 4), gridDim.x);
   const int c = blockIdx.x;
-  if (c >= sp[0].G && c >= sp[1].G) return;  // no share in this wave
+  if (c >= sp[0].G && c >= sp[1].G && c >= sp[2].G) return;  // no share in this wave
 
-  // Half of the CTAs (every other block of one CTA per SM, the way the
-  // block scheduler fills the SMs) take their row share first: an SM then
-  // runs the ALU-heavy correction draws of one CTA beside the streaming of
-  // another instead of both at once.
   SegGen sg;
   sg.step = 0;
-  sg.order = (c / max(1, (int)gridDim.x / kMinBlocks)) & 1;
   sg.q_head = sg.q_used = 0;
   sg.open(sp);
   if (control) fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
@@ -1771,10 +1800,11 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
       const int slot = u % kMailSlots;
       named_bar_sync(kBarReady + slot, kCtaThreads);
       const QItem& pv = queue[u & (kQueue - 1)];
-      if (pv.kind == kResidual) {
+      if (pv.phase == 0) {
         complete_residual<E>(P, sp[0], pv, mailbox[slot]);
       } else {
-        complete_row<E>(P, sp[1], pv, mailbox[slot], s_xy[slot]);
+        complete_row<E>(P, sp[pv.phase], pv.phase == 2 ? P.bpart : P.part, pv, mailbox[slot],
+                        s_xy[slot]);
       }
       sg.q_used = u + 1;  // its queue entry may now be reused
       fill_queue<E, kAligned>(P, sp, queue, &s_qend, sg);
