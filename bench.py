@@ -31,6 +31,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -233,21 +234,57 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
-def oracle_rows_per_sec(batch, requests):
-    """Time the CPU oracle on the given requests of `batch` (single thread)."""
+def oracle_rows_per_sec(batch, requests, full=False):
+    """Time the CPU oracle on the given requests of `batch` (single thread).
+    With full=True (requests = the whole batch) also return the oracle's
+    outputs and the inputs it was given."""
     import oracle
     from speculative_decoding_verification_10_gb300 import workloads as W
-    sub = W.subset(batch, requests)
-    inp = sub.numpy_inputs()
+    inp = (batch if full else W.subset(batch, requests)).numpy_inputs()
     t0 = time.perf_counter()
-    oracle.verify(inp["target"], inp["draft"], inp["tokens"], inp["num_draft"],
-                  inp["temperature"], 1, inp["max_k"], request_ids=inp["request_ids"])
+    out = oracle.verify(inp["target"], inp["draft"], inp["tokens"], inp["num_draft"],
+                        inp["temperature"], 1, inp["max_k"], request_ids=inp["request_ids"])
     dt = time.perf_counter() - t0
     rows = int(inp["num_draft"].astype(np.int64).sum()) + len(requests)
+    if full:
+        return rows / dt, dt, rows, out, inp
     return rows / dt, dt, rows
 
 
-def estimate_sample(batch, target_seconds=10.0):
+def cpu_model():
+    """The host CPU's model name (lscpu), for the baseline's record."""
+    try:
+        outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in outp.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def bench_parity(v, b, oracle_out, inp):
+    """The benchmark batch verified once more (seed 1, debug outputs) and compared
+    with the oracle request by request, outside the timed region.  Counts the
+    requests checked, the exact ones and the near-threshold exemptions."""
+    import torch
+    from tests import parity
+    res = v.run(b.target, b.draft, b.tokens, b.num_draft, b.temperature, 1, debug=True)
+    torch.cuda.synchronize()
+    gpu = {"accepted_len": res.accepted_len.cpu().numpy(), "committed": res.committed.cpu().numpy(),
+           "flags": res.flags.cpu().numpy(), "p_y": res.p_y.cpu().numpy(),
+           "q_y": res.q_y.cpu().numpy(), "u": res.u.cpu().numpy(),
+           "req_status": res.req_status.cpu().numpy(), "status": v.status()}
+    rep = parity.compare(gpu, oracle_out, inp, 1)
+    exempt = rep["exempt_accept"] + rep["exempt_race"] + rep["exempt_residual_mass"]
+    return {"requests_checked": rep["requests"], "exact": rep["requests"] - exempt,
+            "exempt_accept": rep["exempt_accept"], "exempt_race": rep["exempt_race"],
+            "exempt_residual_mass": rep["exempt_residual_mass"],
+            "seed": 1, "rule": "tokens, lengths and flags bit-exact; decisions within 1e-5 "
+                               "relative of their threshold exempt and counted"}
+
+
+def estimate_sample(batch, target_seconds=15.0):
     """Requests whose oracle run takes about target_seconds (from a 1-request probe)."""
     _, dt, _ = oracle_rows_per_sec(batch, [0])
     n = int(max(1, min(batch.batch, target_seconds / max(dt, 1e-4))))
@@ -262,7 +299,9 @@ def run_reference(args):
     from speculative_decoding_verification_10_gb300 import workloads as W
     dev = f"cuda:{local}" if torch.cuda.is_available() else "cpu"
     b = W.make_batch(args.workload, device=dev)
-    per_step = args.cpu_sample or max(1, min(b.batch, int(120.0 / max(1, args.steps + args.warmup)
+    # the whole batch per step when the run fits in about five minutes (it does
+    # for twenty steps and five warm-up steps), else a bounded sample of it
+    per_step = args.cpu_sample or max(1, min(b.batch, int(300.0 / max(1, args.steps + args.warmup)
                                                         / max(_probe_seconds(b), 1e-4))))
     times, rows_total = [], 0
     order = np.arange(b.batch)
@@ -278,10 +317,15 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "batch": b.batch, "vocab": b.vocab,
-                       "logits": b.dtype, "requests_per_step": per_step},
+            "config": {"workload": args.workload, "batch": b.batch, "k": W.SPECS[args.workload].k,
+                       "vocab": b.vocab, "logits": b.dtype,
+                       "rows_per_step": rows_total // max(1, args.steps)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{per_step} requests of {args.workload} per step"},
+                             "cpu_model": cpu_model(),
+                             "sample": (f"the whole batch ({b.batch} requests) per step"
+                                        if per_step == b.batch else
+                                        f"{per_step} of {b.batch} requests of {args.workload} "
+                                        "per step")},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -289,8 +333,10 @@ def run_reference(args):
 
 
 def _probe_seconds(b):
-    _, dt, _ = oracle_rows_per_sec(b, [0])
-    return dt
+    """Oracle seconds per request, from the first few requests."""
+    n = min(4, b.batch)
+    _, dt, _ = oracle_rows_per_sec(b, np.arange(n))
+    return dt / n
 
 
 def measure_e2e(args, b, v, world, dev):
@@ -496,14 +542,22 @@ def run_ours(args):
     if not args.no_e2e:
         e2e = measure_e2e(args, b, v, world, dev)
 
-    # CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
+    # CPU oracle baseline on a bounded sample (rank 0, N = 1 only); when the
+    # sample is the whole batch, the oracle's outputs also check the GPU's
+    # outputs for the same batch request by request (the parity record)
     cpu = None
+    par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample or estimate_sample(b)
-        req = np.sort(np.random.default_rng(0).choice(b.batch, size=n, replace=False))
-        rps, dt, rows = oracle_rows_per_sec(b, req)
-        cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} of {b.batch} requests ({rows} verified rows), {dt:.1f} s"}
+        if n >= b.batch and conf is None and trunc is None:
+            rps, dt, rows, orc, inp = oracle_rows_per_sec(b, np.arange(b.batch), full=True)
+            par = bench_parity(v, b, orc, inp)
+        else:
+            req = np.sort(np.random.default_rng(0).choice(b.batch, size=n, replace=False))
+            rps, dt, rows = oracle_rows_per_sec(b, req)
+        cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle", "cpu_model": cpu_model(),
+               "sample": f"{n if n < b.batch else b.batch} of {b.batch} requests "
+                         f"({rows} verified rows), {dt:.1f} s"}
 
     if rank != 0:
         v.close()
@@ -554,6 +608,7 @@ def run_ours(args):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback"},
         "cpu_baseline": cpu,
+        "parity": par,
         "e2e": e2e,
         "clocks": clock_info,
         "gpu_launches": v.launches_per_run(b.batch) * args.steps,

@@ -180,6 +180,19 @@ bool kernel_shape(int device, int dtype, KernelShape* out) {
             cudaSuccess || occ[v] < 1)
       return false;
   }
+  // the builds for logits in host memory (aligned rows only): the same shared
+  // memory, launched on the same grids
+  const void* host_fn[2] = {
+      dtype == SPECVERIFY_BF16 ? reinterpret_cast<const void*>(sv::sv_wave<sv::BF16, true, 2, false>)
+                               : reinterpret_cast<const void*>(sv::sv_wave<sv::F32, true, 2, false>),
+      dtype == SPECVERIFY_BF16 ? reinterpret_cast<const void*>(sv::sv_wave<sv::BF16, true, 3, false>)
+                               : reinterpret_cast<const void*>(sv::sv_wave<sv::F32, true, 3, false>)};
+  for (const void* fn : host_fn)
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ring_bytes()) != cudaSuccess)
+      return false;
   out->grid_scalar = occ[0] * sms;
   out->grid_aligned = occ[1] * sms;
   out->grid3_scalar = occ[2] * sms;
@@ -258,12 +271,18 @@ int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
     P.wave = w;
     P.pos0 = std::min(w * P.depth, c.max_k + 1);
     P.pos1 = std::min((w + 1) * P.depth, c.max_k + 1);
+    // logits read in place from host memory stream faster in the build
+    // without the shared race best (measured on GB300: 8.3 against 14.5 ms
+    // per w4 round end to end)
+    const bool host = P.tee_target != nullptr;
     cudaError_t e;
     if (three)
-      e = aligned ? launch_wave(sv::sv_wave<E, true, 3>, grid, smem, s, P)
+      e = aligned ? (host ? launch_wave(sv::sv_wave<E, true, 3, false>, grid, smem, s, P)
+                          : launch_wave(sv::sv_wave<E, true, 3>, grid, smem, s, P))
                   : launch_wave(sv::sv_wave<E, false, 3>, grid, smem, s, P);
     else
-      e = aligned ? launch_wave(sv::sv_wave<E, true, 2>, grid, smem, s, P)
+      e = aligned ? (host ? launch_wave(sv::sv_wave<E, true, 2, false>, grid, smem, s, P)
+                          : launch_wave(sv::sv_wave<E, true, 2>, grid, smem, s, P))
                   : launch_wave(sv::sv_wave<E, false, 2>, grid, smem, s, P);
     if (e != cudaSuccess) {
       cudaGetLastError();

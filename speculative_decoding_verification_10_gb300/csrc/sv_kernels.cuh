@@ -410,13 +410,17 @@ __device__ __forceinline__ float from_order_key(uint32_t k) {
 }
 constexpr uint32_t kOrderKeyNegInf = 0x007fffffu;  // order_key(-inf)
 
+// kOn = false (the build for logits read from host memory, whose streaming
+// measured slower with the shared word in the kernel) keeps each warp's best
+// to itself.
+template <bool kOn>
 struct SharedBest {
   uint32_t* word;  // the segment's mailbox-slot word
   __device__ __forceinline__ float load() const {
-    return from_order_key(*reinterpret_cast<volatile uint32_t*>(word));
+    return kOn ? from_order_key(*reinterpret_cast<volatile uint32_t*>(word)) : kNegInf;
   }
   __device__ __forceinline__ void raise(float v) const {
-    if ((threadIdx.x & 31) == 0) atomicMax(word, order_key(v));
+    if (kOn && (threadIdx.x & 31) == 0) atomicMax(word, order_key(v));
   }
 };
 
@@ -436,8 +440,8 @@ __device__ __forceinline__ void take_finite(BestAcc& acc, float score, int i) {
 // whose bounded score is below it cannot be the row's winner, so every lane
 // tests against the warp's best, not only its own.  The test keeps ties
 // (>=), which take_cmp then orders by index.  Call with the whole warp.
-template <typename E>
-__device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const SharedBest& sb,
+template <typename E, bool kShare>
+__device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const SharedBest<kShare>& sb,
                                            const float (&x0)[E::kVec],
                                            const float (&x1)[E::kVec], int e0, int e1, float c,
                                            uint32_t pos, RequestKey rk, PhiloxKey key) {
@@ -493,8 +497,9 @@ __device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const Sha
 // Residual race over one stage: vector x of t_j and z of d_j, the same kVec
 // ids from e0.  fmaf(x, c, rr.lp) bounds log2 (p_v - q_v) from above, so the
 // two exponentials are only taken for ids that pass.  Call with the whole warp.
-template <typename E>
-__device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest, const SharedBest& sb,
+template <typename E, bool kShare>
+__device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
+                                               const SharedBest<kShare>& sb,
                                                const float (&x)[E::kVec],
                                                const float (&z)[E::kVec], int e0,
                                                const ResidualRow& rr, uint32_t pos,
@@ -621,7 +626,7 @@ __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend,
 // softmax segment that holds the draft token y also leaves x[y] in *s_xy.
 // ---------------------------------------------------------------------------
 // `take(v0, v1)` hands over the next stage of the segment from the copy ring.
-template <typename E, typename Take>
+template <typename E, bool kShare, typename Take>
 __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm, float* s_xy,
                                               uint32_t* s_best, Take& take) {
   const int w = threadIdx.x >> 5;
@@ -708,7 +713,7 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       float x0[E::kVec], x1[E::kVec];
       E::unpack(v[0], x0);
       E::unpack(v[1], x1);
-      race_stage<E>(acc, wbest, SharedBest{s_best}, x0, x1, vi * E::kVec, (vi + kThreads) * E::kVec, c,
+      race_stage<E>(acc, wbest, SharedBest<kShare>{s_best}, x0, x1, vi * E::kVec, (vi + kThreads) * E::kVec, c,
                     (uint32_t)pos, rk, P.key);
     }
   } else {
@@ -725,7 +730,7 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       float x[E::kVec], z[E::kVec];
       E::unpack(v[0], x);
       E::unpack(v[1], z);
-      residual_stage<E>(acc, wbest, SharedBest{s_best}, x, z, vi * E::kVec, rr, (uint32_t)pos, rk,
+      residual_stage<E>(acc, wbest, SharedBest<kShare>{s_best}, x, z, vi * E::kVec, rr, (uint32_t)pos, rk,
                         P.key);
     }
   }
@@ -733,13 +738,13 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
   return Partial{acc.v, 0.f, acc.idx, acc.nan};
 }
 
-template <typename E>
+template <typename E, bool kShare>
 __device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
                                                const int* s_qend, uint4* ring, LoadCursor& lc,
                                                int& gs, const QItem& itm, float* s_xy,
                                                uint32_t* s_best) {
   auto take = [&](uint4& v0, uint4& v1) { ring_take(queue, s_qend, ring, lc, gs, v0, v1); };
-  return seg_reduce<E>(P, itm, s_xy, s_best, take);
+  return seg_reduce<E, kShare>(P, itm, s_xy, s_best, take);
 }
 
 // Scalar path (rows not 16-byte aligned): warp w takes vocab blocks
@@ -1721,7 +1726,8 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
 // ---------------------------------------------------------------------------
 // kMinBlocks CTAs per SM bound the registers: 2 (up to 128 a thread) for
 // windows that stream long shares, 3 (up to 80) for small, latency-bound ones.
-template <typename E, bool kAligned, int kMinBlocks>
+// kShare: the race's best shared by the warps of a segment (see SharedBest).
+template <typename E, bool kAligned, int kMinBlocks, bool kShare = true>
 __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* ring = reinterpret_cast<uint4*>(smem_raw);
@@ -1787,7 +1793,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
       if (u >= (qe >= 0 ? qe : -1 - qe)) break;  // only once the count is final
       const QItem& it = queue[u & (kQueue - 1)];
       const Partial out = kAligned
-                              ? seg_aligned<E>(P, queue, &s_qend, ring, lc, gs, it, &s_xy[slot],
+                              ? seg_aligned<E, kShare>(P, queue, &s_qend, ring, lc, gs, it, &s_xy[slot],
                                                &s_best[slot])
                               : seg_scalar<E>(P, it, &s_xy[slot]);
       if ((tid & 31) == 0) mailbox[slot][warp] = out;
