@@ -645,6 +645,16 @@ def run_tree(args):
     if tv.status() != 0:
         raise RuntimeError(f"tree status {tv.status()}")
     A = res.accepted_len.cpu().numpy()
+    # the walk reads A_r + 1 rows per tree; when those fit twice in the L2,
+    # every round runs after an L2 eviction and is timed alone
+    walked = int((A.astype(np.int64) + 1).sum()) * tb.row_bytes()
+    flush = walked < 2 * L2_BYTES
+    if flush:
+        fl_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        fl_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        fl_sink = torch.empty((), dtype=torch.float32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps if flush else 1)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)
@@ -654,12 +664,18 @@ def run_tree(args):
     torch.cuda.synchronize()
     clocks.mark("start")
     t0.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
+        if flush:
+            fl_w.fill_(0.0)
+            torch.sum(fl_r, dim=0, out=fl_sink)
+            ev[i][0].record(stream)
         tv.run(tb.target, tb.num_nodes, tb.parent, tb.tokens)
+        if flush:
+            ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     clocks.mark("stop")
-    ms = t0.elapsed_time(t1) / args.steps
+    ms = (sum(a.elapsed_time(b) for a, b in ev) if flush else t0.elapsed_time(t1)) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
     clock_info = clocks.stop()
     # end to end through the public API: pinned host inputs copied in, outputs back
@@ -676,7 +692,7 @@ def run_tree(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
-        n = min(tb.batch, 8)
+        n = tb.batch
         sub = slice(0, n * (tb.max_nodes + 1))
         tgt = tb.target[sub].cpu()
         tgt = tgt.view(torch.int16).numpy().view(np.uint16) if tb.dtype == "bf16" else tgt.numpy()
@@ -703,18 +719,25 @@ def run_tree(args):
         "config": {"workload": args.workload, "batch": tb.batch, "nodes": tb.max_nodes,
                    "vocab": tb.vocab, "logits": tb.dtype, "rows_per_step": rows,
                    "mean_accepted": float(A.mean()),
-                   "l2": "no flush: each step reads %.2f GB of logits, larger than the 129 MB L2"
-                         % (alg / 1e9), "parallelism": f"replicas x{world}"},
+                   "l2": (("L2 evicted before every round (%d MB written, then %d MB read; "
+                           "rounds timed alone): a round walks %.1f MB of a %.2f GB tree window"
+                           % (FLUSH_BYTES >> 20, FLUSH_BYTES >> 20, walked / 1e6, alg / 1e9))
+                          if flush else
+                          "no flush: each round walks %.2f GB, more than twice the 129 MB L2"
+                          % (walked / 1e9)),
+                   "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "sv_tree_rows", "alg_bytes_per_launch": alg,
-                     "window": "one round: sv_tree_plan + sv_tree_rows + sv_tree_walk",
+                     "kernel": "sv_tree_path", "alg_bytes_per_launch": alg,
+                     "walked_bytes_per_launch": walked,
+                     "walked_gbs": walked / (ms_max * 1e-3) / 1e9,
+                     "window": "one round: sv_tree_plan + sv_tree_path",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
         "cpu_baseline": cpu,
         "e2e": {"value": world * rows / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "clocks": clock_info,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

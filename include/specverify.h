@@ -434,11 +434,12 @@ int specverify_truncate(int dtype, int vocab, const void *target_in, const void 
  * request: a parent out of range (BAD_PARENT), a token outside [0, V)
  * (BAD_TOKEN), NaN/+inf or no finite logit in a row the walk reads
  * (NONFINITE); a num_nodes outside [0, max_nodes] (BAD_K) or a sum other
- * than total_nodes (BAD_TOTAL) skips the batch.  Every row is read once, in
- * one HBM pass, then the walk runs (three launches, asynchronous on stream).
+ * than total_nodes (BAD_TOTAL) skips the batch.  Only the rows of the
+ * accepted path are read (A_r + 1 rows of request r), by one block of threads
+ * per tree walking from the root (two launches, asynchronous on stream).
  */
 /* max_batch in [1, 4096], max_nodes in [0, 1024], vocab in [1, 2^30]; allocates
- * the scratch (chunk maxima of max_batch * (max_nodes + 1) rows) now. */
+ * the scratch (offsets and status words) now. */
 int specverify_tree_create(specverify_tree_t *out, int device, int max_batch, int max_nodes,
                            int vocab, int dtype);
 /* batch in [0, max_batch], total_nodes = host copy of sum num_nodes. */

@@ -469,15 +469,12 @@ struct specverify_ctx {
   cudaEvent_t ev_stop[64];
 };
 
-// A greedy tree verifier: scratch for the chunk partials of every row of the
-// largest batch, the prefix offsets and the status words.
+// A greedy tree verifier: scratch for the prefix offsets and the status words.
 struct specverify_tree_ctx {
   uint32_t magic;
   int device, max_batch, max_nodes, vocab, dtype, elem_bytes;
-  int grid_aligned, grid_scalar;
-  int nchunk;
+  int sms;  // one walking CTA per SM at most
   void* scratch;
-  sv::Partial* part;
   int* t_off;
   int* n_off;
   int* ctr;
@@ -989,33 +986,13 @@ int specverify_tree_create(specverify_tree_t* out, int device, int max_batch, in
   h->elem_bytes = dtype == SPECVERIFY_BF16 ? 2 : 4;
   h->last_stream = nullptr;
   h->last_run_empty = true;
-  const int per_vec = 16 / h->elem_bytes;
-  const long long chunk = (long long)sv::kTreeChunkVecs * per_vec;
-  h->nchunk = (int)((vocab + chunk - 1) / chunk);
-  int sms = 0, occ[2] = {0, 0};
-  const void* fn[2];
-  if (dtype == SPECVERIFY_BF16) {
-    fn[0] = reinterpret_cast<const void*>(sv::sv_tree_rows<sv::BF16, false>);
-    fn[1] = reinterpret_cast<const void*>(sv::sv_tree_rows<sv::BF16, true>);
-  } else {
-    fn[0] = reinterpret_cast<const void*>(sv::sv_tree_rows<sv::F32, false>);
-    fn[1] = reinterpret_cast<const void*>(sv::sv_tree_rows<sv::F32, true>);
-  }
-  bool ok = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess;
-  for (int a = 0; a < 2 && ok; ++a)
-    ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[a], fn[a], sv::kTreeThreads, 0) ==
-             cudaSuccess && occ[a] > 0;
-  if (!ok) {
+  if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      h->sms < 1) {
     cudaGetLastError();
     delete h;
     return SPECVERIFY_ERR_CUDA;
   }
-  h->grid_scalar = occ[0] * sms;
-  h->grid_aligned = occ[1] * sms;
-  const size_t rows = (size_t)max_batch * ((size_t)max_nodes + 1);
   size_t off = 0;
-  const size_t o_part = off;
-  off = align_up(off + sizeof(sv::Partial) * rows * (size_t)h->nchunk, 256);
   const size_t o_t = off;
   off = align_up(off + sizeof(int) * ((size_t)max_batch + 1), 256);
   const size_t o_n = off;
@@ -1030,7 +1007,6 @@ int specverify_tree_create(specverify_tree_t* out, int device, int max_batch, in
     return SPECVERIFY_ERR_CUDA;
   }
   char* b = static_cast<char*>(h->scratch);
-  h->part = reinterpret_cast<sv::Partial*>(b + o_part);
   h->t_off = reinterpret_cast<int*>(b + o_t);
   h->n_off = reinterpret_cast<int*>(b + o_n);
   h->ctr = reinterpret_cast<int*>(b + o_c);
@@ -1069,35 +1045,45 @@ int specverify_tree_run(specverify_tree_t h, const void* target_logits, const in
   P.max_nodes = h->max_nodes;
   P.vocab = h->vocab;
   P.nvec = (int)((size_t)h->vocab * h->elem_bytes / 16);
-  P.nchunk = h->nchunk;
-  P.chunk = sv::kTreeChunkVecs * (16 / h->elem_bytes);
   P.rows = batch + total_nodes;
   P.accepted_len = accepted_len;
   P.path = path;
   P.committed = committed;
   P.req_status = req_status;
-  P.part = h->part;
   P.t_off = h->t_off;
   P.n_off = h->n_off;
   P.ctr = h->ctr;
   const bool aligned = ((size_t)h->vocab * h->elem_bytes) % 16 == 0 &&
                        ((uintptr_t)target_logits & 15u) == 0;
-  const long long items = (long long)P.rows * P.nchunk;
-  const int grid = (int)std::min<long long>(items, aligned ? h->grid_aligned : h->grid_scalar);
+  // a cluster of cs CTAs per tree: the largest power of two up to 8 that still
+  // lets every tree's cluster be resident at once (two CTAs per SM)
+  const int resident = 2 * h->sms;
+  int cs = 1;
+  while (cs < sv::kPathMaxCluster && (long long)batch * cs * 2 <= resident) cs *= 2;
+  const int clusters = std::max(1, std::min(batch, resident / cs));
   sv::sv_tree_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
-  if (h->dtype == SPECVERIFY_BF16) {
-    if (aligned)
-      sv::sv_tree_rows<sv::BF16, true><<<grid, sv::kTreeThreads, 0, s>>>(P);
-    else
-      sv::sv_tree_rows<sv::BF16, false><<<grid, sv::kTreeThreads, 0, s>>>(P);
-  } else {
-    if (aligned)
-      sv::sv_tree_rows<sv::F32, true><<<grid, sv::kTreeThreads, 0, s>>>(P);
-    else
-      sv::sv_tree_rows<sv::F32, false><<<grid, sv::kTreeThreads, 0, s>>>(P);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(clusters * cs));
+  cfg.blockDim = dim3(sv::kPathThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (h->dtype == SPECVERIFY_BF16)
+    e = aligned ? cudaLaunchKernelEx(&cfg, sv::sv_tree_path<sv::BF16, true>, P)
+                : cudaLaunchKernelEx(&cfg, sv::sv_tree_path<sv::BF16, false>, P);
+  else
+    e = aligned ? cudaLaunchKernelEx(&cfg, sv::sv_tree_path<sv::F32, true>, P)
+                : cudaLaunchKernelEx(&cfg, sv::sv_tree_path<sv::F32, false>, P);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return SPECVERIFY_ERR_CUDA;
   }
-  const int walk_grid = (batch + sv::kTreeWalkWarps - 1) / sv::kTreeWalkWarps;
-  sv::sv_tree_walk<<<walk_grid, sv::kTreeWalkWarps * 32, 0, s>>>(P);
   h->last_stream = s;
   h->last_run_empty = false;
   return cudaGetLastError() == cudaSuccess ? SPECVERIFY_OK : SPECVERIFY_ERR_CUDA;

@@ -629,7 +629,6 @@ __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend,
 template <typename E, bool kShare, typename Take>
 __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm, float* s_xy,
                                               uint32_t* s_best, Take& take) {
-  const int w = threadIdx.x >> 5;
   const int tid = threadIdx.x;
   // the segment's fields in registers (the queue is shared memory, which the
   // copy ring's memory clobbers would otherwise make the loop reload)

@@ -13,29 +13,25 @@
 // target rows are consecutive: row 0 is the target's output at the root, row
 // 1 + i its output after node i.
 //
-// A round is three launches:
+// A round is two launches:
 //   sv_tree_plan   one CTA: prefix offsets of rows and nodes, the layout checks;
-//   sv_tree_rows   the HBM pass: every target row is cut into chunks of
-//                  kTreeChunkVecs 16-byte vectors and each chunk reduced to its
-//                  first maximum (value, index, NaN seen) by one CTA;
-//   sv_tree_walk   one warp per request: validates its nodes, then from the
-//                  root merges the chunk partials of the current row, takes
-//                  its argmax tau and moves to the lowest-index child carrying
-//                  tau, until no child does (tau is then the bonus token).
-// Every row is read once, also rows off the accepted path: the walk needs the
-// argmax of whichever row it reaches, and reading all rows in one pass keeps
-// HBM streaming instead of one dependent launch per depth.
+//   sv_tree_path   one thread-block cluster per tree: validates the tree's nodes,
+//                  then from the root reads the row of the node it stands on
+//                  (each CTA a slice of it), takes its argmax tau (first
+//                  maximum) and moves to the lowest-index child carrying tau,
+//                  until no child does (tau is then the bonus token).
+// Only the rows of the accepted path are read: A + 1 rows of a tree whose
+// walk accepts A nodes, one after another, each by the CS CTAs of its
+// cluster (64 KB of loads in flight per CTA) while other clusters walk
+// other trees.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include "sv_kernels.cuh"
 
 namespace sv {
 
-constexpr int kTreeThreads = 256;
-constexpr int kTreeVecsPerThread = 8;                                  // loads in flight
-constexpr int kTreeChunkVecs = kTreeThreads * kTreeVecsPerThread * 2;  // 64 KB chunks
-constexpr int kTreeWalkWarps = 8;
-constexpr int kTreeRegNodes = 4;  // nodes per lane the walk keeps in registers (128 per tree)
 constexpr int kTreeMaxNodes = 1024;
 constexpr uint32_t kStBadParent = 32u;
 
@@ -46,14 +42,11 @@ struct TreeParams {
   const int32_t* tokens;
   int batch, total_nodes, max_nodes, vocab;
   int nvec;     // 16-byte vectors per row (aligned rows)
-  int nchunk;   // chunks per row
-  int chunk;    // elements per chunk
   int rows;     // batch + total_nodes
   int32_t* accepted_len;
   int32_t* path;       // [batch, max_nodes]
   int32_t* committed;  // [batch, max_nodes + 1]
   int32_t* req_status;
-  Partial* part;       // [rows * nchunk]
   int* t_off;          // [batch + 1]
   int* n_off;          // [batch + 1]
   int* ctr;            // [0] status, [1] layout bits
@@ -115,149 +108,160 @@ __global__ void __launch_bounds__(kPlanThreads) sv_tree_plan(TreeParams P) {
 }
 
 // ---------------------------------------------------------------------------
-// The row pass: first maximum of every chunk of every target row.
+// The walk: one thread-block cluster of CS CTAs per tree (trees cluster c,
+// c + clusters, ...).  CTA q of the cluster reduces its slice q/CS of the
+// current row to a first maximum; the slices' maxima are exchanged through
+// distributed shared memory, so every CTA of the cluster takes the same tau,
+// the same child and the same number of steps (cluster barriers are always
+// matched).  CTA 0 writes the outputs.
 // ---------------------------------------------------------------------------
-template <typename E, bool kAligned>
-__global__ void __launch_bounds__(kTreeThreads, 4) sv_tree_rows(TreeParams P) {
-  __shared__ BestAcc s_red[kTreeThreads / 32];
-  const int tid = threadIdx.x;
-  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
-  const long long items = (long long)P.rows * P.nchunk;
-  for (long long item = blockIdx.x; item < items; item += gridDim.x) {
-    const int row = (int)(item / P.nchunk), ch = (int)(item % P.nchunk);
-    const char* rp = reinterpret_cast<const char*>(P.target) + (size_t)row * row_bytes;
-    BestAcc acc;
-    acc.init();
-    if (kAligned) {
-      const uint4* rv = reinterpret_cast<const uint4*>(rp);
-      const int v0 = ch * kTreeChunkVecs, v1 = min(v0 + kTreeChunkVecs, P.nvec);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint4 buf[kTreeVecsPerThread];
-#pragma unroll
-        for (int j = 0; j < kTreeVecsPerThread; ++j) {
-          const int vi = v0 + (half * kTreeVecsPerThread + j) * kTreeThreads + tid;
-          buf[j] = vi < v1 ? ld_stream(rv + vi) : E::pad();
-        }
-#pragma unroll
-        for (int j = 0; j < kTreeVecsPerThread; ++j) {
-          const int vi = v0 + (half * kTreeVecsPerThread + j) * kTreeThreads + tid;
-          float x[E::kVec];
-          E::unpack(buf[j], x);
-#pragma unroll
-          for (int e = 0; e < E::kVec; ++e) {
-            acc.nan |= (x[e] != x[e]);
-            acc.take(x[e], vi * E::kVec + e);  // increasing index: strict > keeps the first
-          }
-        }
-      }
-    } else {
-      const int e0 = ch * P.chunk, e1 = min(e0 + P.chunk, P.vocab);
-      for (int v = e0 + tid; v < e1; v += kTreeThreads) {
-        const float x = E::load1(rp, v);
-        acc.nan |= (x != x);
-        acc.take(x, v);
-      }
-    }
-    acc = warp_reduce(acc);
-    if ((tid & 31) == 0) s_red[tid >> 5] = acc;
-    __syncthreads();
-    if (tid < 32) {
-      BestAcc b;
-      b.init();
-      if (tid < kTreeThreads / 32) b = s_red[tid];
-      b = warp_reduce(b);
-      if (tid == 0) P.part[item] = Partial{b.v, 0.f, b.idx, b.nan};
-    }
-    __syncthreads();
-  }
-}
+constexpr int kPathThreads = 512;
+constexpr int kPathVecs = 8;       // 16-byte loads in flight per thread
+constexpr int kPathMaxCluster = 8; // portable cluster size
 
-// ---------------------------------------------------------------------------
-// The walk: one warp per request.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTreeWalkWarps * 32) sv_tree_walk(TreeParams P) {
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * kTreeWalkWarps + (threadIdx.x >> 5);
-  if (r >= P.batch) return;
-  const int pw = P.max_nodes, cw = P.max_nodes + 1;
-  int32_t* pth = P.path + (size_t)r * pw;
-  int32_t* com = P.committed + (size_t)r * cw;
-  const uint32_t layout = (uint32_t)P.ctr[1];
-  uint32_t rs = layout;
-  int a = 0;
-  if (!layout) {
-    const int n = P.num_nodes[r];
-    const int n0 = P.n_off[r], t0 = P.t_off[r];
-    const int32_t* par = P.parent + n0;
-    const int32_t* tok = P.tokens + n0;
-    // the first 32 * kTreeRegNodes nodes stay in registers for the whole walk
-    int rp[kTreeRegNodes], rt[kTreeRegNodes];
+// The first maximum of elements [e0, e1) of one row (all threads call it; the
+// result is valid in every thread).
+template <typename E, bool kAligned>
+__device__ BestAcc path_slice_argmax(const TreeParams& P, const char* rp, int v0, int v1,
+                                     BestAcc* s_red) {
+  const int tid = threadIdx.x;
+  BestAcc acc;
+  acc.init();
+  if (kAligned) {
+    const uint4* rv = reinterpret_cast<const uint4*>(rp);
+    for (int b = v0; b < v1; b += kPathVecs * kPathThreads) {
+      uint4 buf[kPathVecs];
 #pragma unroll
-    for (int j = 0; j < kTreeRegNodes; ++j) {
-      const int i = j * 32 + lane;
-      rp[j] = i < n ? par[i] : -2;
-      rt[j] = i < n ? tok[i] : -1;
-    }
-    for (int i = lane; i < n; i += 32) {
-      const int pi = i < 32 * kTreeRegNodes ? rp[i / 32] : par[i];
-      const int ti = i < 32 * kTreeRegNodes ? rt[i / 32] : tok[i];
-      if (pi < -1 || pi >= i) rs |= kStBadParent;
-      if (ti < 0 || ti >= P.vocab) rs |= kStBadToken;
-    }
-    rs = __reduce_or_sync(0xffffffffu, rs);
-    int cur = -1;
-    while (!rs) {
-      // the argmax of the current node's row, from its chunk partials
-      const Partial* pp = P.part + (size_t)(t0 + cur + 1) * P.nchunk;
-      BestAcc best;
-      best.init();
-      for (int c = lane; c < P.nchunk; c += 32) {
-        const Partial q = pp[c];
-        BestAcc x;
-        x.v = q.a;
-        x.idx = q.idx;
-        x.nan = q.bad;
-        best = BestAcc::merge(best, x);
+      for (int j = 0; j < kPathVecs; ++j) {
+        const int vi = b + j * kPathThreads + tid;
+        buf[j] = vi < v1 ? ld_stream(rv + vi) : E::pad();
       }
-      best = warp_reduce(best);
-      if (best.nan != 0u || best.idx < 0 || !(best.v < 3.0e38f)) {
-        rs = kStNonfinite;
-        break;
-      }
-      const int tau = best.idx;
-      if (lane == 0) com[a] = tau;
-      // the lowest-index child of `cur` whose token is tau
-      int child = -1;
 #pragma unroll
-      for (int j = 0; j < kTreeRegNodes; ++j) {
-        const unsigned m = __ballot_sync(0xffffffffu, rp[j] == cur && rt[j] == tau);
-        if (child < 0 && m) child = j * 32 + __ffs(m) - 1;
+      for (int j = 0; j < kPathVecs; ++j) {
+        const int vi = b + j * kPathThreads + tid;
+        float x[E::kVec];
+        E::unpack(buf[j], x);
+#pragma unroll
+        for (int e = 0; e < E::kVec; ++e) {
+          acc.nan |= (x[e] != x[e]);
+          acc.take(x[e], vi * E::kVec + e);  // increasing index: strict > keeps the first
+        }
       }
-      for (int i0 = 32 * kTreeRegNodes; i0 < n && child < 0; i0 += 32) {
-        const int i = i0 + lane;
-        const unsigned m = __ballot_sync(0xffffffffu, i < n && par[i] == cur && tok[i] == tau);
-        if (m) child = i0 + __ffs(m) - 1;
-      }
-      if (child < 0) break;
-      if (lane == 0) pth[a] = child;
-      ++a;
-      cur = child;
-    }
-  }
-  if (rs) {
-    for (int d = lane; d < cw; d += 32) com[d] = -1;
-    for (int d = lane; d < pw; d += 32) pth[d] = -1;
-    if (lane == 0) {
-      P.accepted_len[r] = -1;
-      atomicOr(reinterpret_cast<unsigned int*>(P.ctr), rs);
     }
   } else {
-    for (int d = a + 1 + lane; d < cw; d += 32) com[d] = -1;
-    for (int d = a + lane; d < pw; d += 32) pth[d] = -1;
-    if (lane == 0) P.accepted_len[r] = a;
+    for (int v = v0 + tid; v < v1; v += kPathThreads) {
+      const float x = E::load1(rp, v);
+      acc.nan |= (x != x);
+      acc.take(x, v);
+    }
   }
-  if (P.req_status && lane == 0) P.req_status[r] = (int32_t)rs;
+  acc = warp_reduce(acc);
+  if ((tid & 31) == 0) s_red[tid >> 5] = acc;
+  __syncthreads();
+  BestAcc b;
+  b.init();
+  if ((tid & 31) < kPathThreads / 32) b = s_red[tid & 31];
+  b = warp_reduce(b);  // every warp reduces the partials alike
+  __syncthreads();     // s_red is reused by the next row
+  return b;
+}
+
+template <typename E, bool kAligned>
+__global__ void __launch_bounds__(kPathThreads, 2) sv_tree_path(TreeParams P) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int cs = (int)cl.num_blocks(), crank = (int)cl.block_rank();
+  const int cluster = (int)blockIdx.x / cs, clusters = (int)gridDim.x / cs;
+  __shared__ BestAcc s_red[kPathThreads / 32];
+  __shared__ BestAcc s_slice[2];  // this CTA's slice maximum, double-buffered by step
+  __shared__ int s_par[kTreeMaxNodes];
+  __shared__ int s_tok[kTreeMaxNodes];
+  __shared__ int s_flag[kPathThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t row_bytes = (size_t)P.vocab * E::kBytes;
+  const int units = kAligned ? P.nvec : P.vocab;  // vectors or elements of a row
+  const int u0 = (int)((long long)units * crank / cs), u1 = (int)((long long)units * (crank + 1) / cs);
+  const uint32_t layout = (uint32_t)P.ctr[1];
+  const int pw = P.max_nodes, cw = P.max_nodes + 1;
+  int step = 0;
+  for (int r = cluster; r < P.batch; r += clusters) {
+    int32_t* pth = P.path + (size_t)r * pw;
+    int32_t* com = P.committed + (size_t)r * cw;
+    uint32_t rs = layout;
+    int a = 0;
+    if (!layout) {
+      const int n = P.num_nodes[r];
+      const int n0 = P.n_off[r], t0 = P.t_off[r];
+      uint32_t bad = 0u;
+      for (int i = tid; i < n; i += kPathThreads) {
+        const int pi = P.parent[n0 + i], ti = P.tokens[n0 + i];
+        s_par[i] = pi;
+        s_tok[i] = ti;
+        if (pi < -1 || pi >= i) bad |= kStBadParent;
+        if (ti < 0 || ti >= P.vocab) bad |= kStBadToken;
+      }
+      bad = __reduce_or_sync(0xffffffffu, bad);
+      if (lane == 0) s_flag[warp] = (int)bad;
+      __syncthreads();
+      rs = 0u;
+#pragma unroll 1
+      for (int w = 0; w < kPathThreads / 32; ++w) rs |= (uint32_t)s_flag[w];
+      __syncthreads();
+      int cur = -1;
+      while (!rs) {
+        const char* rp =
+            reinterpret_cast<const char*>(P.target) + (size_t)(t0 + cur + 1) * row_bytes;
+        const BestAcc mine = path_slice_argmax<E, kAligned>(P, rp, u0, u1, s_red);
+        const int buf = step & 1;
+        if (tid == 0) s_slice[buf] = mine;
+        cl.sync();  // every slice maximum of this step is in place
+        BestAcc best;
+        best.init();
+#pragma unroll 1
+        for (int q = 0; q < cs; ++q) best = BestAcc::merge(best, *cl.map_shared_rank(&s_slice[buf], q));
+        ++step;
+        if (best.nan != 0u || best.idx < 0 || !(best.v < 3.0e38f)) {
+          rs = kStNonfinite;
+          break;
+        }
+        const int tau = best.idx;
+        if (crank == 0 && tid == 0) com[a] = tau;
+        // the lowest-index child of `cur` whose token is tau
+        int child = -1;
+        for (int i0 = 0; i0 < n && child < 0; i0 += kPathThreads) {
+          const int i = i0 + tid;
+          const bool match = i < n && s_par[i] == cur && s_tok[i] == tau;
+          const unsigned m = __ballot_sync(0xffffffffu, match);
+          if (lane == 0) s_flag[warp] = m ? i0 + warp * 32 + __ffs(m) - 1 : -1;
+          __syncthreads();
+#pragma unroll 1
+          for (int w = 0; w < kPathThreads / 32 && child < 0; ++w) child = s_flag[w];
+          __syncthreads();
+        }
+        if (child < 0) break;
+        if (crank == 0 && tid == 0) pth[a] = child;
+        ++a;
+        cur = child;
+      }
+    }
+    if (crank == 0) {
+      if (rs) {
+        for (int d = tid; d < cw; d += kPathThreads) com[d] = -1;
+        for (int d = tid; d < pw; d += kPathThreads) pth[d] = -1;
+        if (tid == 0) {
+          P.accepted_len[r] = -1;
+          atomicOr(reinterpret_cast<unsigned int*>(P.ctr), rs);
+        }
+      } else {
+        for (int d = a + 1 + tid; d < cw; d += kPathThreads) com[d] = -1;
+        for (int d = a + tid; d < pw; d += kPathThreads) pth[d] = -1;
+        if (tid == 0) P.accepted_len[r] = a;
+      }
+      if (P.req_status && tid == 0) P.req_status[r] = (int32_t)rs;
+    }
+    __syncthreads();  // s_par / s_tok are reused by the next tree
+  }
+  cl.sync();  // no CTA leaves while another may still read its slice maximum
 }
 
 }  // namespace sv

@@ -145,3 +145,32 @@ def test_empty_batch():
                      torch.empty(0, dtype=torch.int32, device="cuda"),
                      torch.empty(0, dtype=torch.int32, device="cuda"))
         assert res.accepted_len.numel() == 0 and tv.status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_rows_off_the_accepted_path_are_never_read(dtype):
+    """The walk reads only the rows of its accepted path: filling every other
+    row with NaN changes nothing and raises no status bit, while NaN in a row on
+    the path does."""
+    target, num, par, tok = random_trees(24, 16, 4096, dtype, seed=77)
+    g = check(target, num, par, tok, 16, dtype)
+    t_off = np.concatenate([[0], np.cumsum(num.astype(np.int64) + 1)])
+    on_path = np.zeros(len(target), bool)
+    for r in range(len(num)):
+        if g["accepted_len"][r] < 0:
+            continue
+        on_path[t_off[r]] = True                                   # the root row
+        for d in range(g["accepted_len"][r]):
+            on_path[t_off[r] + 1 + g["path"][r][d]] = True         # the accepted nodes' rows
+    poisoned = target.copy()
+    nan = np.uint16(0x7fc0) if dtype == "bf16" else np.float32(np.nan)
+    poisoned[~on_path] = nan
+    with TreeVerifier(len(num), 16, 4096, dtype) as tv:
+        h = run_gpu(tv, poisoned, num, par, tok)
+        assert h["status"] == 0
+        assert (h["accepted_len"] == g["accepted_len"]).all()
+        assert (h["committed"] == g["committed"]).all() and (h["path"] == g["path"]).all()
+        # NaN in the root row of the first request, which every walk reads
+        poisoned[t_off[0]] = nan
+        h = run_gpu(tv, poisoned, num, par, tok)
+        assert h["status"] == oracle.NONFINITE and h["accepted_len"][0] == -1
