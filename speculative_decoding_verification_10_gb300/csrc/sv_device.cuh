@@ -124,6 +124,15 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
+// The copy only where `on` holds, as a predicated instruction (no branch).
+__device__ __forceinline__ void cp_async16_if(void* smem, const void* gmem, bool on) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(s),
+      "l"(gmem), "r"((int)on)
+      : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

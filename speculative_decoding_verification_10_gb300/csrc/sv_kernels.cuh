@@ -263,15 +263,6 @@ struct __align__(16) QItem {
   char* tee;  // where a softmax segment's row is copied (Params::tee_*), or NULL
 };
 
-// The logit x[y] held by vector x at element e (a select chain, no local memory).
-template <int N>
-__device__ __forceinline__ float pick(const float (&x)[N], int e) {
-  float v = x[0];
-#pragma unroll
-  for (int i = 1; i < N; ++i)
-    if (i == e) v = x[i];
-  return v;
-}
 
 // ---------------------------------------------------------------------------
 // Exponential race over vocab ids.  A categorical draw from weights w_v >= 0
@@ -397,6 +388,15 @@ __device__ __forceinline__ void race_words_n(uint4 (&r)[N], const uint32_t (&g)[
   }
 }
 
+// Largest of the 4 N words of N Philox blocks.
+template <int N>
+__device__ __forceinline__ uint32_t max_word(const uint4 (&r)[N]) {
+  uint32_t m = max(max(r[0].x, r[0].y), max(r[0].z, r[0].w));
+#pragma unroll
+  for (int i = 1; i < N; ++i) m = max(m, max(max(r[i].x, r[i].y), max(r[i].z, r[i].w)));
+  return m;
+}
+
 // The race's best score so far, shared by the warps that reduce one segment
 // (a shared-memory word per mailbox slot, raised with atomicMax): every warp
 // then prunes with the best any of them has found.  Floats map to unsigned
@@ -468,12 +468,9 @@ __device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const Sha
   }
   uint4 r[2 * G];
   race_words_n<2 * G>(r, g, pos, rk, key);
-  bool pass = false;
-#pragma unroll
-  for (int i = 0; i < E::kVec; ++i) {
-    pass |= fmaf(x0[i], c, race_gain_bound(word_of(r[i >> 2], i & 3))) >= wbest;
-    pass |= fmaf(x1[i], c, race_gain_bound(word_of(r[G + (i >> 2)], i & 3))) >= wbest;
-  }
+  // the stage's largest logit with its largest word bounds every id's score
+  // from above (both terms are monotone), so one test stands for all of them
+  const bool pass = fmaf(mx, c, race_gain_bound(max_word<2 * G>(r))) >= wbest;
   if (pass) {
 #pragma unroll
     for (int i = 0; i < E::kVec; ++i) {
@@ -515,10 +512,8 @@ __device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
   for (int j = 0; j < G; ++j) g[j] = (uint32_t)(e0 >> 2) + j;
   uint4 r[G];
   race_words_n<G>(r, g, pos, rk, key);
-  bool pass = false;
-#pragma unroll
-  for (int i = 0; i < E::kVec; ++i)
-    pass |= fmaf(x[i], rr.c, rr.lp) + race_gain_bound(word_of(r[i >> 2], i & 3)) >= wbest;
+  // one bound for the whole vector: its largest logit with its largest word
+  const bool pass = fmaf(mx, rr.c, rr.lp) + race_gain_bound(max_word<G>(r)) >= wbest;
   if (pass) {
 #pragma unroll
     for (int i = 0; i < E::kVec; ++i) {
@@ -595,8 +590,8 @@ struct LoadCursor {
     if (!active) open(queue, s_qend);
     if (active) {
       uint4* dst = ring + slot * kStageVecs * kThreads + threadIdx.x;
-      if (i0 < vend) cp_async16(dst, b0 + i0);
-      if (i1 < vend) cp_async16(dst + kThreads, b1 + i1);
+      cp_async16_if(dst, b0 + i0, i0 < vend);
+      cp_async16_if(dst + kThreads, b1 + i1, i1 < vend);
       i0 += step;
       i1 += step;
       if (--left == 0) {
@@ -640,27 +635,39 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
   if (kind == kSoftmax) {
     LazySoftmax acc;
     acc.init();
-    const int yv = itm.yv, ye = itm.y & (E::kVec - 1);
-    uint4* tee = reinterpret_cast<uint4*>(itm.tee);
-    for (int st = 0; st < nst; ++st) {
-      uint4 v0, v1;
-      take(v0, v1);
-      const int vi = vbeg + st * kStageVecs * kThreads + tid;
-      if (tee) {
-        if (vi < vend) tee[vi] = v0;
-        if (vi + kThreads < vend) tee[vi + kThreads] = v1;
+    // x[y] comes from the thread whose vectors hold it, loaded before the
+    // stages so that its latency hides under them (no test inside the loop)
+    const int yv = itm.yv;
+    const bool own_y = yv >= vbeg && yv < vend && (yv - vbeg) % kThreads == tid;
+    float xy = 0.f;
+    if (own_y) xy = E::load1(itm.row, itm.y);
+    // the stages, with or without the copy to the device staging (a loop of
+    // its own for each, so the common one carries no test of it)
+    auto stages = [&](auto tee_on) {
+      uint4* tee = reinterpret_cast<uint4*>(itm.tee);
+      for (int st = 0; st < nst; ++st) {
+        uint4 v0, v1;
+        take(v0, v1);
+        const int vi = vbeg + st * kStageVecs * kThreads + tid;
+        if (decltype(tee_on)::value) {
+          if (vi < vend) tee[vi] = v0;
+          if (vi + kThreads < vend) tee[vi + kThreads] = v1;
+        }
+        if (st >= nfull) {
+          if (vi >= vend) v0 = E::pad();
+          if (vi + kThreads >= vend) v1 = E::pad();
+        }
+        float x0[E::kVec], x1[E::kVec];
+        E::unpack(v0, x0);
+        E::unpack(v1, x1);
+        acc.add2(x0, x1, c);
       }
-      if (st >= nfull) {
-        if (vi >= vend) v0 = E::pad();
-        if (vi + kThreads >= vend) v1 = E::pad();
-      }
-      float x0[E::kVec], x1[E::kVec];
-      E::unpack(v0, x0);
-      E::unpack(v1, x1);
-      if (vi == yv) *s_xy = pick(x0, ye);
-      if (vi + kThreads == yv) *s_xy = pick(x1, ye);
-      acc.add2(x0, x1, c);
-    }
+    };
+    if (itm.tee)
+      stages(std::true_type{});
+    else
+      stages(std::false_type{});
+    if (own_y) *s_xy = xy;
     SoftmaxAcc a = warp_reduce(acc.result());
     return Partial{a.m, a.s, -1, 0u};
   }
@@ -735,15 +742,6 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
   }
   acc = warp_reduce(acc);
   return Partial{acc.v, 0.f, acc.idx, acc.nan};
-}
-
-template <typename E, bool kShare>
-__device__ __forceinline__ Partial seg_aligned(const Params& P, const QItem* queue,
-                                               const int* s_qend, uint4* ring, LoadCursor& lc,
-                                               int& gs, const QItem& itm, float* s_xy,
-                                               uint32_t* s_best) {
-  auto take = [&](uint4& v0, uint4& v1) { ring_take(queue, s_qend, ring, lc, gs, v0, v1); };
-  return seg_reduce<E, kShare>(P, itm, s_xy, s_best, take);
 }
 
 // Scalar path (rows not 16-byte aligned): warp w takes vocab blocks
@@ -1777,28 +1775,33 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   // streaming.
   if (!control) {
     // ---- compute warps: stream segment after segment ---------------------------
-    LoadCursor lc;
-    int gs = 0;
-    if (kAligned) {
+    auto segments = [&](auto&& seg) {
+      for (int u = 0;; ++u) {
+        const int slot = u % kMailSlots;
+        if (u >= kMailSlots) named_bar_sync(kBarFree + slot, kCtaThreads);
+        const int qe = ld_acquire_shared(&s_qend);
+        if (u >= (qe >= 0 ? qe : -1 - qe)) break;  // only once the count is final
+        const QItem& it = queue[u & (kQueue - 1)];
+        const Partial out = seg(it, slot);
+        if ((tid & 31) == 0) mailbox[slot][warp] = out;
+        named_bar_arrive(kBarReady + slot, kCtaThreads);
+      }
+    };
+    if (!kAligned) {
+      segments([&](const QItem& it, int slot) { return seg_scalar<E>(P, it, &s_xy[slot]); });
+    } else {
+      int gs = 0;
+      LoadCursor lc;
       lc.q = 0;
       lc.active = false;
       lc.open(queue, &s_qend);
       for (int s = 0; s < kStages - 1; ++s) lc.issue(queue, &s_qend, ring, s);
+      auto take = [&](uint4& v0, uint4& v1) { ring_take(queue, &s_qend, ring, lc, gs, v0, v1); };
+      segments([&](const QItem& it, int slot) {
+        return seg_reduce<E, kShare>(P, it, &s_xy[slot], &s_best[slot], take);
+      });
+      cp_async_wait_all();
     }
-    for (int u = 0;; ++u) {
-      const int slot = u % kMailSlots;
-      if (u >= kMailSlots) named_bar_sync(kBarFree + slot, kCtaThreads);
-      const int qe = ld_acquire_shared(&s_qend);
-      if (u >= (qe >= 0 ? qe : -1 - qe)) break;  // only once the count is final
-      const QItem& it = queue[u & (kQueue - 1)];
-      const Partial out = kAligned
-                              ? seg_aligned<E, kShare>(P, queue, &s_qend, ring, lc, gs, it, &s_xy[slot],
-                                               &s_best[slot])
-                              : seg_scalar<E>(P, it, &s_xy[slot]);
-      if ((tid & 31) == 0) mailbox[slot][warp] = out;
-      named_bar_arrive(kBarReady + slot, kCtaThreads);
-    }
-    if (kAligned) cp_async_wait_all();
   } else {
     // ---- control warp: complete segment after segment, keep the queue full ----
     for (int u = 0; u < sg.q_head; ++u) {
