@@ -52,6 +52,34 @@ L2_BYTES = 129 * 1000 * 1000
 FLUSH_BYTES = 512 << 20
 
 
+def truncated_draft_tokens(b, top_k: int, top_p: float, seed: int, chunk: int = 64):
+    """Input preparation for truncated rounds: the draft tokens of sampling
+    requests are redrawn from their truncated draft distributions (plain torch
+    ops: temperature, then top-k, then top-p on the survivors), as a drafter
+    sampling from its truncated distribution would emit them."""
+    import torch
+    dev = b.draft.device
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    nd = b.num_draft.cpu().numpy()
+    temps = b.temperature.cpu().numpy()
+    row_t = torch.as_tensor(np.repeat(temps, nd), dtype=torch.float32, device=dev)
+    V = b.draft.shape[1]
+    for s0 in range(0, b.total_draft, chunk):
+        T = row_t[s0:s0 + chunk]
+        x = b.draft[s0:s0 + chunk].float() / torch.where(T > 0, T, 1.0)[:, None]
+        if 0 < top_k < V:
+            kth = torch.topk(x, top_k, dim=1).values[:, -1:]
+            x = torch.where(x >= kth, x, float("-inf"))
+        if top_p < 1.0:
+            srt, _ = torch.sort(x, dim=1, descending=True)
+            p = torch.softmax(srt, dim=1)
+            above = torch.cumsum(p, dim=1) - p          # mass of the larger survivors
+            keep = above < top_p
+            thr = torch.where(keep, srt, float("inf")).min(dim=1, keepdim=True).values
+            x = torch.where(x >= thr, x, float("-inf"))
+        tok = torch.multinomial(torch.softmax(x, dim=1), 1, generator=gen).squeeze(1)
+        b.tokens[s0:s0 + chunk] = torch.where(T > 0, tok.to(torch.int32), b.tokens[s0:s0 + chunk])
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -73,9 +101,12 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per batch (0 = the workload's own); for profiling captures")
     ap.add_argument("--top-k", type=int, default=None,
-                    help="truncate every row to its top-k logits before the round (specverify_truncate)")
+                    help="truncate every target and draft row to its top-k logits")
     ap.add_argument("--top-p", type=float, default=None,
-                    help="truncate every row to its top-p nucleus before the round (specverify_truncate)")
+                    help="truncate every target and draft row to its top-p nucleus")
+    ap.add_argument("--trunc-path", choices=["masked", "copy"], default="masked",
+                    help="truncation: thresholds and a mask on load inside the round "
+                         "(specverify_run_truncated), or a truncated copy then the round")
     ap.add_argument("--trim", type=float, default=None,
                     help="verify windows trimmed from draft confidences, at this cost per "
                          "verified position (specverify_run_trimmed)")
@@ -435,12 +466,21 @@ def run_ours(args):
         tk = torch.full((b.batch,), int(args.top_k or 0), dtype=torch.int32, device=dev)
         tp = torch.full((b.batch,), float(args.top_p if args.top_p is not None else 1.0),
                         dtype=torch.float32, device=dev)
-        tgt_out, drf_out = torch.empty_like(b.target), torch.empty_like(b.draft)
-        trunc = (truncate, tk, tp, tgt_out, drf_out)
+        truncated_draft_tokens(b, int(args.top_k or 0),
+                               float(args.top_p if args.top_p is not None else 1.0), 4343 + rank)
+        if args.trunc_path == "copy":
+            tgt_out, drf_out = torch.empty_like(b.target), torch.empty_like(b.draft)
+            trunc = (truncate, tk, tp, tgt_out, drf_out)
+        else:
+            trunc = (None, tk, tp, None, None)
 
     def step():
         if trunc is not None:
             fn, tk, tp, to, do = trunc
+            if fn is None:
+                # thresholds, then the round masking the rows as it loads them
+                return v.run_truncated(b.target, b.draft, b.tokens, b.num_draft, b.temperature,
+                                       tk, tp, 1, out=out)
             fn(b.target, b.draft, b.num_draft, b.temperature, tk, tp, out_target=to,
                out_draft=do)
             v.run(to, do, b.tokens, b.num_draft, b.temperature, 1, out=out)
@@ -471,7 +511,7 @@ def run_ours(args):
     alg_bytes = window_bytes + b.io_bytes()
 
     trunc_ms = None
-    if trunc is not None:
+    if trunc is not None and trunc[0] is not None:
         # the truncation pass alone (it reads every window row and writes it once)
         fn, tk, tp, to, do = trunc
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -591,8 +631,14 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}",
                    "schedule": args.schedule, "depth": args.depth,
                    "trim_cost": args.trim, "top_k": args.top_k, "top_p": args.top_p,
-                   "truncation_bytes_per_step": (2 * full_window_bytes
-                                                 if trunc is not None else 0),
+                   "truncation": (None if trunc is None else
+                                  ("copy: the truncated rows written, then the round"
+                                   if trunc[0] is not None else
+                                   "masked: a threshold pass, then the round masking rows "
+                                   "on load (both inside the timed round)")),
+                   "truncation_bytes_per_step": (0 if trunc is None else
+                                                 (2 if trunc[0] is not None else 1)
+                                                 * full_window_bytes),
                    "truncation_ms": trunc_ms,
                    "truncation_gbs": (2 * full_window_bytes / (trunc_ms * 1e-3) / 1e9
                                       if trunc_ms else None)},

@@ -164,6 +164,30 @@ int specverify_run_ex(specverify_t h, const void *target_logits, const void *dra
                       int32_t *req_status, void *stream);
 
 /*
+ * specverify_run_truncated -- specverify_run on top-k / top-p truncated
+ * distributions, applied alike to each request's target and draft rows.
+ *
+ * "Speculative Decoding: Medusa, MTP, EAGLE, DFlash, DDTree, and DSpark",
+ * section 1: truncation must enter the acceptance test and the residual
+ * consistently.  The rules and their thresholds are those of
+ * specverify_truncate (top_k [batch] int32, top_p [batch] float32, same
+ * meaning), but no truncated copy is written: a threshold pass stores one
+ * order-key threshold per window row in the handle's scratch, and the verify
+ * waves read every logit below its row's threshold as -inf as they load it.
+ * The outputs are those of specverify_run on the rows specverify_truncate
+ * writes (draft tokens must come from the truncated draft distributions).  A
+ * top_p NaN or <= 0 keeps its rows whole and sets SPECVERIFY_STATUS_BAD_TRUNC.
+ * The other arguments are those of specverify_run; the round has one more
+ * launch (the threshold pass, one CTA per SM over every window row).
+ */
+int specverify_run_truncated(specverify_t h, const void *target_logits,
+                             const void *draft_logits, const int32_t *draft_tokens,
+                             const int32_t *num_draft, const float *temperature,
+                             const int32_t *top_k, const float *top_p, uint64_t seed, int batch,
+                             int total_draft, int32_t *accepted_len, int32_t *committed_tokens,
+                             uint8_t *accept_flags, void *stream);
+
+/*
  * specverify_run_trimmed -- verify per-request windows chosen from draft
  * confidences, in place in a full-window layout.
  *

@@ -177,6 +177,32 @@ class Verifier:
         _check(code, "specverify_run")
         return out
 
+    def run_truncated(self, target, draft, tokens, num_draft, temperature, top_k, top_p,
+                      seed: int, *, total_draft: int | None = None,
+                      out: VerifyResult | None = None, stream=None) -> VerifyResult:
+        """One verify round on top-k / top-p truncated distributions
+        (specverify_run_truncated): top_k [B] int32, top_p [B] float32 on the
+        handle's device.  No truncated copy is made: the waves mask the rows
+        as they load them."""
+        self._check_inputs(target, draft, tokens, num_draft, temperature)
+        batch = int(num_draft.shape[0])
+        for t, dt, name in ((top_k, torch.int32, "top_k"), (top_p, torch.float32, "top_p")):
+            if t.dtype != dt or t.device != self.device or t.numel() < batch:
+                raise TypeError(f"{name} must be [batch] {dt} on the handle's device")
+        if total_draft is None:
+            total_draft = int(tokens.shape[0])
+        if out is None:
+            out = self.outputs(batch, total_draft)
+        _check_outputs(out.accepted_len, out.committed, out.flags, batch, total_draft,
+                       self.max_k, self.device)
+        d = draft if (draft is not None and draft.numel()) else None
+        code = self.lib.specverify_run_truncated(
+            self._h, _ptr(target), _ptr(d), _ptr(tokens), _ptr(num_draft), _ptr(temperature),
+            _ptr(top_k), _ptr(top_p), int(seed) & (2**64 - 1), batch, int(total_draft),
+            _ptr(out.accepted_len), _ptr(out.committed), _ptr(out.flags), self._stream(stream))
+        _check(code, "specverify_run_truncated")
+        return out
+
     def run_trimmed(self, target, draft, tokens, window, confidence, cost, temperature,
                     seed: int, *, total_draft: int | None = None, debug: bool = False,
                     stream=None) -> VerifyResult:

@@ -105,6 +105,9 @@ def load(path: str | None = None):
     lib.specverify_last_host_reads.restype = I
     lib.specverify_metrics.argtypes = [P, P, I, I, P, P, P, P, P]
     lib.specverify_metrics.restype = I
+    lib.specverify_run_truncated.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_uint64, I, I,
+                                             P, P, P, P]
+    lib.specverify_run_truncated.restype = I
     lib.specverify_run_trimmed.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_uint64, I, I,
                                            P, P, P, P, P, P, P, P, P]
     lib.specverify_run_trimmed.restype = I

@@ -48,6 +48,7 @@ struct DeviceGuard {
 // `tagged` bytes clears them all.
 struct ScratchLayout {
   size_t lists, lcnt, blists, blcnt, res, rcnt, pos, rescnt, part, bpart, rpart, ctr, recs, rdy;
+  size_t thr_t, thr_d;
   size_t list_entries, tagged, bytes;
 };
 
@@ -99,6 +100,10 @@ constexpr ScratchLayout scratch_layout(size_t mb, int max_k, size_t grid) {
   off = align_up(off + sizeof(int) * sv::kCntCount, 256);
   L.recs = off;
   off = align_up(off + sizeof(sv::PosRec) * ((size_t)max_k + 1) * mb, 256);
+  L.thr_t = off;
+  off = align_up(off + sizeof(uint32_t) * ((size_t)max_k + 1) * mb, 256);
+  L.thr_d = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)max_k * mb, 256);
   L.list_entries = list_entries;
   L.bytes = off;
   return L;
@@ -119,6 +124,8 @@ struct Scratch {
   int* ctr;
   sv::PosRec* recs;
   unsigned long long* rdy;  // epoch-tagged: must start at zero
+  uint32_t* thr_t;          // truncated rounds: per-row thresholds of the window
+  uint32_t* thr_d;
   char* tagged;             // the epoch-tagged counters above, one block
   size_t tagged_bytes;
 };
@@ -139,6 +146,8 @@ Scratch scratch_at(char* b, const ScratchLayout& L) {
   s.ctr = reinterpret_cast<int*>(b + L.ctr);
   s.recs = reinterpret_cast<sv::PosRec*>(b + L.recs);
   s.rdy = reinterpret_cast<unsigned long long*>(b + L.rdy);
+  s.thr_t = reinterpret_cast<uint32_t*>(b + L.thr_t);
+  s.thr_d = reinterpret_cast<uint32_t*>(b + L.thr_d);
   s.tagged = b;
   s.tagged_bytes = L.tagged;
   return s;
@@ -160,6 +169,7 @@ const void* wave_kernel(bool aligned, bool three) {
 struct KernelShape {
   int grid_aligned, grid_scalar;    // the wave kernel built for two CTAs per SM
   int grid3_aligned, grid3_scalar;  // ... and for three
+  int sms;
 };
 
 bool kernel_shape(int device, int dtype, KernelShape* out) {
@@ -197,6 +207,7 @@ bool kernel_shape(int device, int dtype, KernelShape* out) {
   out->grid_aligned = occ[1] * sms;
   out->grid3_scalar = occ[2] * sms;
   out->grid3_aligned = occ[3] * sms;
+  out->sms = sms;
   return true;
 }
 
@@ -260,9 +271,20 @@ cudaError_t launch_wave(K kernel, int grid, size_t smem, cudaStream_t s, const s
 // returns at once), optionally bracketed by two events.
 template <typename E>
 int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
-                 cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+                 cudaEvent_t ev_start, cudaEvent_t ev_stop, const sv::TruncParams* tp) {
   if (ev_start && cudaEventRecord(ev_start, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
   sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
+  if (tp) {
+    // truncated round: every window row's threshold, after the plan (which
+    // resets the status word its bad top_p values are OR-ed into) and before
+    // the first wave (which waits for it)
+    const long long rows = (long long)tp->batch + (tp->draft_in ? 2ll : 1ll) * tp->total_draft;
+    const int tgrid = (int)std::min<long long>(rows, c.shape.sms);
+    if (aligned)
+      sv::sv_truncate<E, true><<<tgrid, sv::kTruncThreads, 0, s>>>(*tp);
+    else
+      sv::sv_truncate<E, false><<<tgrid, sv::kTruncThreads, 0, s>>>(*tp);
+  }
   const size_t smem = aligned ? ring_bytes() : 0;
   const bool three = wave_three(c, P.batch);
   const int grid = three ? (aligned ? c.shape.grid3_aligned : c.shape.grid3_scalar)
@@ -317,6 +339,9 @@ struct RunArgs {
   // memory (specverify_run_host reading in place), or NULL
   void* tee_target = nullptr;
   void* tee_draft = nullptr;
+  // truncated rounds (specverify_run_truncated): per-request top-k / top-p
+  const int32_t* top_k = nullptr;
+  const float* top_p = nullptr;
 };
 
 // Checks that need no device (the batch must already be in range).
@@ -411,8 +436,28 @@ int enqueue_round(const RunConfig& c, const RunArgs& a, uint32_t epoch, cudaStre
     P.tee_target = static_cast<char*>(a.tee_target);
     P.tee_draft = static_cast<char*>(a.tee_draft);
   }
-  return c.dtype == SPECVERIFY_BF16 ? launch_round<sv::BF16>(c, P, aligned, s, ev_start, ev_stop)
-                                    : launch_round<sv::F32>(c, P, aligned, s, ev_start, ev_stop);
+  sv::TruncParams tp;
+  std::memset(&tp, 0, sizeof tp);
+  if (a.top_k != nullptr) {
+    P.thr_t = c.sc.thr_t;
+    P.thr_d = c.sc.thr_d;
+    tp.target_in = a.target_logits;
+    tp.draft_in = P.draft;
+    tp.num_draft = a.num_draft;
+    tp.temperature = a.temperature;
+    tp.top_k = a.top_k;
+    tp.top_p = a.top_p;
+    tp.batch = a.batch;
+    tp.total_draft = a.total_draft;
+    tp.vocab = c.vocab;
+    tp.status = c.sc.ctr + sv::kCntStatus;
+    tp.thr_target = c.sc.thr_t;
+    tp.thr_draft = c.sc.thr_d;
+  }
+  const sv::TruncParams* tpp = a.top_k != nullptr ? &tp : nullptr;
+  return c.dtype == SPECVERIFY_BF16
+             ? launch_round<sv::BF16>(c, P, aligned, s, ev_start, ev_stop, tpp)
+             : launch_round<sv::F32>(c, P, aligned, s, ev_start, ev_stop, tpp);
 }
 
 // ---------------------------------------------------------------------------
@@ -640,6 +685,21 @@ int specverify_run_ex(specverify_t h, const void* target_logits, const void* dra
   const RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
                   batch, total_draft, accepted_len, committed_tokens, accept_flags,
                   request_ids, p_y, q_y, u, req_status, nullptr, nullptr, nullptr};
+  return run_impl(h, a, stream);
+}
+
+int specverify_run_truncated(specverify_t h, const void* target_logits,
+                             const void* draft_logits, const int32_t* draft_tokens,
+                             const int32_t* num_draft, const float* temperature,
+                             const int32_t* top_k, const float* top_p, uint64_t seed, int batch,
+                             int total_draft, int32_t* accepted_len, int32_t* committed_tokens,
+                             uint8_t* accept_flags, void* stream) {
+  if (batch > 0 && (top_k == nullptr || top_p == nullptr)) return SPECVERIFY_ERR_INVALID_ARG;
+  RunArgs a{target_logits, draft_logits, draft_tokens, num_draft, temperature, seed,
+            batch, total_draft, accepted_len, committed_tokens, accept_flags,
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  a.top_k = top_k;
+  a.top_p = top_p;
   return run_impl(h, a, stream);
 }
 
@@ -1148,7 +1208,7 @@ int specverify_truncate(int dtype, int vocab, const void* target_in, const void*
     cudaGetLastError();
     return SPECVERIFY_ERR_CUDA;
   }
-  sv::TruncParams P;
+  sv::TruncParams P{};  // every field set, the threshold outputs NULL (copy mode)
   P.target_in = target_in;
   P.draft_in = total_draft > 0 ? draft_in : nullptr;
   P.target_out = target_out;
@@ -1161,6 +1221,8 @@ int specverify_truncate(int dtype, int vocab, const void* target_in, const void*
   P.total_draft = total_draft;
   P.vocab = vocab;
   P.status = status;
+  P.thr_target = nullptr;
+  P.thr_draft = nullptr;
   // one CTA per SM: the rows in flight (one per CTA) stay in L2 across the passes
   const long long rows = (long long)batch + 2ll * total_draft;
   const int grid = (int)std::min<long long>(rows, sms);

@@ -13,6 +13,8 @@
 #pragma once
 
 #include <cstdint>
+
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace sv {
@@ -231,6 +233,87 @@ struct BF16 {
     return __uint_as_float((uint32_t)h << 16);
   }
 };
+
+// Two bf16 logits packed in a 32-bit word, worked on together.  Their order
+// keys: a positive logit gets its bits with the top bit set, a negative one its
+// bits inverted, so keys compare as the logits do (-inf lowest; a positive NaN
+// keys above +inf, a negative one below -inf).  Unlike trunc_key, -0 keeps
+// its own key 0x7fff, just below +0's 0x8000.
+__device__ __forceinline__ uint32_t bf16x2_keys(uint32_t w) {
+  const uint32_t neg = (w >> 15) & 0x00010001u;  // sign of each half, moved to its bit 0
+  return w ^ ((neg * 0x7fffu) | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// The word with each half whose key is below the threshold (t2: the 16-bit
+// key in both halves) replaced by -inf.
+__device__ __forceinline__ uint32_t keep_bf16x2(uint32_t w, uint32_t t2) {
+  const uint32_t k = bf16x2_keys(w);
+  const uint32_t d = max_u16x2(k, t2) ^ k;  // a half is zero where its key >= the threshold
+  const uint32_t nz = (((d & 0x7fff7fffu) + 0x7fff7fffu) | d) & 0x80008000u;
+  const uint32_t drop = (nz >> 15) * 0xffffu;  // 0xffff in each half to drop
+  return (w & ~drop) | (0xff80ff80u & drop);
+}
+
+// Order-preserving key of a logit: larger logit, larger key (-inf lowest;
+// -0 and +0 compare equal, so they share a key).  bf16 logits carry their
+// information in the upper 16 bits.
+template <typename E>
+__device__ __forceinline__ uint32_t trunc_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return E::kBytes == 2 ? (k >> 16) : k;
+}
+
+// Truncation on load: a truncated row keeps the logits whose order key is at
+// or above the row's threshold key and reads -inf for the others, so every
+// pass over the row sees the truncated distribution.  A threshold key of 0
+// keeps the row as it is (its callers test for it, so a NaN stays visible).
+// The test is the logit comparison x >= x_thr, x_thr the logit of the key: on
+// the rows that get a threshold (no NaN) it keeps exactly the keys >= thr, -0
+// and +0 comparing equal as they share a key.
+// The threshold logit of a key, as the masks take it: bf16 in both halves of
+// a word, fp32 as its bits.
+template <typename E>
+__device__ __forceinline__ uint32_t mask_bits(uint32_t key) {
+  if (E::kBytes == 2) {
+    const uint32_t h = (key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu);
+    return h | (h << 16);
+  }
+  return (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+}
+template <typename E>
+__device__ __forceinline__ float mask1(float x, uint32_t key) {
+  if (key == 0u) return x;
+  const uint32_t b = mask_bits<E>(key);
+  const float t = __uint_as_float(E::kBytes == 2 ? (b << 16) : b);
+  return x >= t ? x : kNegInf;
+}
+// A vector with `bits` = mask_bits(key) of a key that is not 0: bf16 pairs
+// compared and selected two at a time (a compare mask and one bit select).
+template <typename E>
+__device__ __forceinline__ void mask_vec(uint4& v, uint32_t bits) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (E::kBytes == 2) {
+      const unsigned m = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[e]),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&bits));
+      w[e] = (w[e] & m) | (0xff80ff80u & ~m);
+    } else {
+      w[e] = __uint_as_float(w[e]) >= __uint_as_float(bits) ? w[e] : 0xff800000u;
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Accumulators.  Each is a per-thread state with an element update and a

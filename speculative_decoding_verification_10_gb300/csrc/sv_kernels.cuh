@@ -167,6 +167,10 @@ struct Params {
   float* q_y;
   float* u_dbg;
   int32_t* req_status;
+  // Truncated rounds: the order-key threshold of every target / draft row of
+  // the window (the logits below it read as -inf), or NULL.
+  const uint32_t* thr_t;
+  const uint32_t* thr_d;
   Entry* lists;                 // [n_waves * list_cap] rows of each wave (bonus rows apart)
   int* list_cnt;                // [n_waves]
   Entry* blists;                // [n_waves * stride] bonus rows of each wave
@@ -260,6 +264,7 @@ struct __align__(16) QItem {
   uint32_t req_lo, req_hi;
   int e0;    // entry e of the phase is partial slot CTA + e0 + e
   int phase;  // 0 correction draws, 1 rows, 2 bonus rows
+  uint32_t thr, thr2;  // truncation thresholds of row and row2 (0: none)
   char* tee;  // where a softmax segment's row is copied (Params::tee_*), or NULL
 };
 
@@ -459,7 +464,8 @@ __device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const Sha
     const float lo = warp_max(mx < -kNegInf ? mx : kNegInf) * c + kMinGain;
     if (lo > kNegInf) wbest = lo - kBoundSlack;
   }
-  if (!__any_sync(0xffffffffu, fmaf(mx, c, kMaxGain) >= wbest)) return;
+  // a stage of -inf logits (a truncated row) has no id to race
+  if (!__any_sync(0xffffffffu, mx > kNegInf && fmaf(mx, c, kMaxGain) >= wbest)) return;
   uint32_t g[2 * G];
 #pragma unroll
   for (int j = 0; j < G; ++j) {
@@ -506,7 +512,8 @@ __device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
 #pragma unroll
   for (int i = 1; i < E::kVec; ++i) mx = fmaxf(mx, x[i]);
   wbest = fmaxf(wbest, sb.load());
-  if (!__any_sync(0xffffffffu, fmaf(mx, rr.c, rr.lp) + kMaxGain >= wbest)) return;
+  if (!__any_sync(0xffffffffu, mx > kNegInf && fmaf(mx, rr.c, rr.lp) + kMaxGain >= wbest))
+    return;
   uint32_t g[G];
 #pragma unroll
   for (int j = 0; j < G; ++j) g[j] = (uint32_t)(e0 >> 2) + j;
@@ -537,14 +544,19 @@ __device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
 // mass in fp32 (p <= q everywhere), an edge case.
 template <typename E>
 __device__ int warp_row_race(const Params& P, const char* trow, float c, uint32_t pos,
-                             RequestKey rk) {
+                             RequestKey rk, uint32_t thr) {
   const int lane = threadIdx.x & 31;
   BestAcc acc;
   acc.init();
   for (int v0 = 4 * lane; v0 < P.vocab; v0 += 128) {
     float x[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = v0 + i < P.vocab ? E::load1(trow, v0 + i) : kNegInf;
+    for (int i = 0; i < 4; ++i)
+      x[i] = v0 + i < P.vocab ? mask1<E>(E::load1(trow, v0 + i), thr) : kNegInf;
+    // a group that cannot beat this lane's best (all -inf, in a truncated
+    // row) needs no Philox call
+    const float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    if (!(mx > kNegInf && fmaf(mx, c, kMaxGain) >= acc.v)) continue;
     const uint4 r = race_words((uint32_t)v0 >> 2, pos, rk, P.key);
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc.take(fmaf(x[i], c, race_gain(word_of(r, i))), v0 + i);
@@ -639,19 +651,25 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
     // stages so that its latency hides under them (no test inside the loop)
     const int yv = itm.yv;
     const bool own_y = yv >= vbeg && yv < vend && (yv - vbeg) % kThreads == tid;
+    const uint32_t thr = itm.thr, tb = mask_bits<E>(thr);
     float xy = 0.f;
-    if (own_y) xy = E::load1(itm.row, itm.y);
-    // the stages, with or without the copy to the device staging (a loop of
-    // its own for each, so the common one carries no test of it)
-    auto stages = [&](auto tee_on) {
+    if (own_y) xy = mask1<E>(E::load1(itm.row, itm.y), thr);
+    // the stages: plain, with the copy to the device staging, or truncated
+    // (a loop of its own for each, so the common one carries no test)
+    auto stages = [&](auto mode) {
+      constexpr int kMode = decltype(mode)::value;
       uint4* tee = reinterpret_cast<uint4*>(itm.tee);
       for (int st = 0; st < nst; ++st) {
         uint4 v0, v1;
         take(v0, v1);
         const int vi = vbeg + st * kStageVecs * kThreads + tid;
-        if (decltype(tee_on)::value) {
+        if (kMode == 1) {
           if (vi < vend) tee[vi] = v0;
           if (vi + kThreads < vend) tee[vi + kThreads] = v1;
+        }
+        if (kMode == 2) {
+          mask_vec<E>(v0, tb);
+          mask_vec<E>(v1, tb);
         }
         if (st >= nfull) {
           if (vi >= vend) v0 = E::pad();
@@ -664,9 +682,11 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       }
     };
     if (itm.tee)
-      stages(std::true_type{});
+      stages(std::integral_constant<int, 1>{});
+    else if (thr)
+      stages(std::integral_constant<int, 2>{});
     else
-      stages(std::false_type{});
+      stages(std::integral_constant<int, 0>{});
     if (own_y) *s_xy = xy;
     SoftmaxAcc a = warp_reduce(acc.result());
     return Partial{a.m, a.s, -1, 0u};
@@ -696,6 +716,10 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       uint4 v[kStageVecs];
       take(v[0], v[1]);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
+      if (itm.thr) {
+        mask_vec<E>(v[0], mask_bits<E>(itm.thr));
+        mask_vec<E>(v[1], mask_bits<E>(itm.thr));
+      }
       if (st >= nfull) {
         if (vi >= vend) v[0] = E::pad();
         if (vi + kThreads >= vend) v[1] = E::pad();
@@ -712,6 +736,10 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       uint4 v[kStageVecs];
       take(v[0], v[1]);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
+      if (itm.thr) {
+        mask_vec<E>(v[0], mask_bits<E>(itm.thr));
+        mask_vec<E>(v[1], mask_bits<E>(itm.thr));
+      }
       if (st >= nfull) {
         if (vi >= vend) v[0] = E::pad();
         if (vi + kThreads >= vend) v[1] = E::pad();
@@ -729,6 +757,8 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       uint4 v[kStageVecs];
       take(v[0], v[1]);
       const int vi = vbeg + st * kThreads + tid;
+      if (itm.thr) mask_vec<E>(v[0], mask_bits<E>(itm.thr));
+      if (itm.thr2) mask_vec<E>(v[1], mask_bits<E>(itm.thr2));
       if (st >= nfull && vi >= vend) {
         v[0] = E::pad();
         v[1] = E::pad();
@@ -757,7 +787,7 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
       for (int j = 0; j < 4; ++j) {
         const int v = b * kVocabBlock + lane + 32 * j;
         if (v < P.vocab) {
-          const float x = E::load1(it.row, v);
+          const float x = mask1<E>(E::load1(it.row, v), it.thr);
           if (v == it.y) *s_xy = x;
           acc.add1(x, it.c);
         }
@@ -773,7 +803,7 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
       for (int j = 0; j < 4; ++j) {
         const int v = b * kVocabBlock + lane + 32 * j;
         if (v < P.vocab) {
-          const float x = E::load1(it.row, v);
+          const float x = mask1<E>(E::load1(it.row, v), it.thr);
           acc.nan |= (x != x);
           acc.take(x, v);
         }
@@ -785,8 +815,10 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
     float x[4], z[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      x[i] = v0 + i < P.vocab ? E::load1(it.row, v0 + i) : kNegInf;
-      z[i] = (it.kind == kResidual && v0 + i < P.vocab) ? E::load1(it.row2, v0 + i) : kNegInf;
+      x[i] = v0 + i < P.vocab ? mask1<E>(E::load1(it.row, v0 + i), it.thr) : kNegInf;
+      z[i] = (it.kind == kResidual && v0 + i < P.vocab)
+                 ? mask1<E>(E::load1(it.row2, v0 + i), it.thr2)
+                 : kNegInf;
     }
     if (it.kind == kRace) {
       race_vec<F32>(acc, x, v0, it.c, pos, rk, P.key);
@@ -1298,7 +1330,8 @@ __device__ void complete_residual(const Params& P, const Split& sp, const QItem&
   const int j = it.pos;
   int token = best.idx;
   if (token < 0)
-    token = warp_row_race<E>(P, it.row, it.c, (uint32_t)j, RequestKey{it.req_lo, it.req_hi});
+    token = warp_row_race<E>(P, it.row, it.c, (uint32_t)j, RequestKey{it.req_lo, it.req_hi},
+                             it.thr);
   if (lane == 0) P.committed[(size_t)it.r * (P.max_k + 1) + j] = token;
 }
 
@@ -1377,6 +1410,7 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
   it.mp = it.inv_sp = it.mq = it.inv_sq = 0.f;
   it.row2 = nullptr;
   it.tee = nullptr;
+  it.thr = it.thr2 = 0u;
   if (phase == 0) {
     const ResEntry re = ldcg_res(res + e);
     it.r = re.r;
@@ -1400,6 +1434,10 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
     const char* db = kAligned && P.tee_target ? P.tee_draft : reinterpret_cast<const char*>(P.draft);
     it.row = tb + (size_t)(re.d0 + re.r + re.j) * row_bytes;
     it.row2 = db + (size_t)(re.d0 + re.j) * row_bytes;
+    if (P.thr_t) {
+      it.thr = __ldcg(P.thr_t + re.d0 + re.r + re.j);
+      it.thr2 = __ldcg(P.thr_d + re.d0 + re.j);
+    }
   } else {
     const Entry en = ldcg_entry(list + e);
     const int r = en.meta & 0x1fff;
@@ -1419,6 +1457,8 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
                                    : (size_t)(en.d0 + r + it.pos) * row_bytes;
     it.row = (it.is_draft ? reinterpret_cast<const char*>(P.draft)
                           : reinterpret_cast<const char*>(P.target)) + off;
+    if (P.thr_t)
+      it.thr = __ldcg(it.is_draft ? P.thr_d + en.d0 + it.pos : P.thr_t + en.d0 + r + it.pos);
     if (kAligned && P.tee_target && it.kind == kSoftmax)
       it.tee = (it.is_draft ? P.tee_draft : P.tee_target) + off;
   }

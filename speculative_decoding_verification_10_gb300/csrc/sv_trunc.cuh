@@ -49,6 +49,10 @@ struct TruncParams {
   const float* top_p;
   int batch, total_draft, vocab;
   int32_t* status;  // nullable device word (atomicOr)
+  // Threshold mode (both set, outputs unused): each row's order-key threshold
+  // is written here instead of a truncated copy (0 for a row kept whole).
+  uint32_t* thr_target;
+  uint32_t* thr_draft;
 };
 
 // The output pass is the last touch of a row: its loads and the stores of the
@@ -65,46 +69,6 @@ __device__ __forceinline__ void st_streaming(uint4* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
-}
-
-// Two bf16 logits packed in a 32-bit word, worked on together.  Their order
-// keys: a positive logit gets its bits with the top bit set, a negative one its
-// bits inverted, so keys compare as the logits do (-inf lowest; a positive NaN
-// keys above +inf, a negative one below -inf).  Unlike trunc_key, -0 keeps
-// its own key 0x7fff, just below +0's 0x8000.
-__device__ __forceinline__ uint32_t bf16x2_keys(uint32_t w) {
-  const uint32_t neg = (w >> 15) & 0x00010001u;  // sign of each half, moved to its bit 0
-  return w ^ ((neg * 0x7fffu) | 0x80008000u);
-}
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-// The word with each half whose key is below the threshold (t2: the 16-bit
-// key in both halves) replaced by -inf.
-__device__ __forceinline__ uint32_t keep_bf16x2(uint32_t w, uint32_t t2) {
-  const uint32_t k = bf16x2_keys(w);
-  const uint32_t d = max_u16x2(k, t2) ^ k;  // a half is zero where its key >= the threshold
-  const uint32_t nz = (((d & 0x7fff7fffu) + 0x7fff7fffu) | d) & 0x80008000u;
-  const uint32_t drop = (nz >> 15) * 0xffffu;  // 0xffff in each half to drop
-  return (w & ~drop) | (0xff80ff80u & drop);
-}
-
-// Order-preserving key of a logit: larger logit, larger key (-inf lowest;
-// -0 and +0 compare equal, so they share a key).  bf16 logits carry their
-// information in the upper 16 bits.
-template <typename E>
-__device__ __forceinline__ uint32_t trunc_key(float x) {
-  uint32_t u = __float_as_uint(x);
-  if (u == 0x80000000u) u = 0u;
-  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return E::kBytes == 2 ? (k >> 16) : k;
 }
 
 // The digit a warp-0 scan picks from 256 bins, lanes holding 8 bins each.
@@ -375,8 +339,6 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
     }
     const char* in = reinterpret_cast<const char*>(is_draft ? P.draft_in : P.target_in) +
                      (size_t)local * row_bytes;
-    char* out = reinterpret_cast<char*>(is_draft ? P.draft_out : P.target_out) +
-                (size_t)local * row_bytes;
     const float T = P.temperature[r_cur];
     const int K = P.top_k[r_cur];
     const float Pp = P.top_p[r_cur];
@@ -674,7 +636,15 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
         tau = max(tau, prefix);
       }
     }
+    if (P.thr_target) {
+      // threshold mode: the verify round masks the row as it loads it
+      if (tid == 0) (is_draft ? P.thr_draft : P.thr_target)[local] = copy ? 0u : tau;
+      __syncthreads();
+      continue;
+    }
     // ---- output: the kept logits, -inf elsewhere (or the row as it is) ----------
+    char* out = reinterpret_cast<char*>(is_draft ? P.draft_out : P.target_out) +
+                (size_t)local * row_bytes;
     if constexpr (kFast) {
       // packed: -0 keys just below +0 here, so a threshold at +0 moves below it
       const uint4* rv = reinterpret_cast<const uint4*>(in);
