@@ -49,8 +49,9 @@ namespace sv {
 constexpr int kComputeWarps = 7;
 constexpr int kThreads = kComputeWarps * 32;   // compute threads
 constexpr int kBlock = kThreads + 32;          // + the control warp
-constexpr int kStages = 8;
-constexpr int kStageVecs = 2;
+constexpr int kStages = 8;                     // ring stages (power of 2)
+constexpr int kStageVecs = 2;                  // 16-byte vectors per thread and stage (even)
+constexpr int kStagePairs = kStageVecs / 2;    // ... t_j / d_j pairs of a residual stage
 constexpr int kQueue = 16;                     // segment queue entries (power of 2)
 constexpr int kMaxBatch = 4096;                // requests per round
 constexpr int kMaxK = 31;                      // draft positions per request
@@ -566,17 +567,18 @@ __device__ int warp_row_race(const Params& P, const char* trow, float c, uint32_
 
 // ---------------------------------------------------------------------------
 // The per-thread copy ring (compute threads, aligned rows).  Stage s of a
-// segment holds two vectors per thread: vectors vbeg + 2 s kThreads + tid and
-// + kThreads of a single row, or vector vbeg + s kThreads + tid of t_j and of
-// d_j for a residual segment.
+// segment holds kStageVecs vectors per thread: vectors vbeg + (kStageVecs s +
+// j) kThreads + tid, j = 0 .. kStageVecs - 1, of a single row; or, for a
+// residual segment, vector vbeg + (kStagePairs s + p) kThreads + tid of t_j
+// (slot vector 2 p) and of d_j (slot vector 2 p + 1).
 // ---------------------------------------------------------------------------
 struct LoadCursor {
   int q;      // queue index of the segment being loaded
   int left;   // its stages still to copy
   const uint4* b0;
   const uint4* b1;
-  int i0, i1, step, vend;
-  bool active;
+  int i, step, vend;  // this thread's first vector of the next stage
+  bool active, pair;
 
   // s_qend: segments the control warp has queued, or -1 - n once all n are.
   __device__ __forceinline__ void open(const QItem* queue, const int* s_qend) {
@@ -585,12 +587,11 @@ struct LoadCursor {
     active = q < avail;
     if (active) {
       const QItem& it = queue[q & (kQueue - 1)];
-      const bool pair = it.kind == kResidual;
+      pair = it.kind == kResidual;
       b0 = reinterpret_cast<const uint4*>(it.row);
       b1 = reinterpret_cast<const uint4*>(pair ? it.row2 : it.row);
-      i0 = it.vbeg + (int)threadIdx.x;
-      i1 = pair ? i0 : i0 + kThreads;
-      step = pair ? kThreads : kStageVecs * kThreads;
+      i = it.vbeg + (int)threadIdx.x;
+      step = (pair ? kStagePairs : kStageVecs) * kThreads;
       vend = it.vend;
       left = it.nst;
     }
@@ -602,10 +603,12 @@ struct LoadCursor {
     if (!active) open(queue, s_qend);
     if (active) {
       uint4* dst = ring + slot * kStageVecs * kThreads + threadIdx.x;
-      cp_async16_if(dst, b0 + i0, i0 < vend);
-      cp_async16_if(dst + kThreads, b1 + i1, i1 < vend);
-      i0 += step;
-      i1 += step;
+#pragma unroll
+      for (int j = 0; j < kStageVecs; ++j) {
+        const int v = i + (pair ? (j >> 1) : j) * kThreads;
+        cp_async16_if(dst + j * kThreads, ((pair && (j & 1)) ? b1 : b0) + v, v < vend);
+      }
+      i += step;
       if (--left == 0) {
         ++q;
         open(queue, s_qend);
@@ -618,12 +621,13 @@ struct LoadCursor {
 // Reads one stage of the ring (after its copies landed) and refills the ring
 // one stage ahead.
 __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend, uint4* ring,
-                                          LoadCursor& lc, int& g_stage, uint4& v0, uint4& v1) {
+                                          LoadCursor& lc, int& g_stage,
+                                          uint4 (&v)[kStageVecs]) {
   cp_async_wait<kStages - 2>();
   const int slot = g_stage & (kStages - 1);
   const uint4* src = ring + slot * kStageVecs * kThreads + threadIdx.x;
-  v0 = src[0];
-  v1 = src[kThreads];
+#pragma unroll
+  for (int j = 0; j < kStageVecs; ++j) v[j] = src[j * kThreads];
   lc.issue(queue, s_qend, ring, (g_stage + kStages - 1) & (kStages - 1));
   ++g_stage;
 }
@@ -632,7 +636,7 @@ __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend,
 // Segment reductions (compute threads).  Each returns this warp's partial; a
 // softmax segment that holds the draft token y also leaves x[y] in *s_xy.
 // ---------------------------------------------------------------------------
-// `take(v0, v1)` hands over the next stage of the segment from the copy ring.
+// `take(v)` hands over the next stage of the segment from the copy ring.
 template <typename E, bool kShare, typename Take>
 __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm, float* s_xy,
                                               uint32_t* s_best, Take& take) {
@@ -642,7 +646,7 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
   const int kind = itm.kind, vbeg = itm.vbeg, vend = itm.vend, nst = itm.nst, pos = itm.pos;
   const float c = itm.c;
   const RequestKey rk{itm.req_lo, itm.req_hi};
-  const int per = kind == kResidual ? kThreads : kStageVecs * kThreads;
+  const int per = (kind == kResidual ? kStagePairs : kStageVecs) * kThreads;
   const int nfull = (vend - vbeg) / per;
   if (kind == kSoftmax) {
     LazySoftmax acc;
@@ -660,25 +664,26 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
       constexpr int kMode = decltype(mode)::value;
       uint4* tee = reinterpret_cast<uint4*>(itm.tee);
       for (int st = 0; st < nst; ++st) {
-        uint4 v0, v1;
-        take(v0, v1);
+        uint4 v[kStageVecs];
+        take(v);
         const int vi = vbeg + st * kStageVecs * kThreads + tid;
-        if (kMode == 1) {
-          if (vi < vend) tee[vi] = v0;
-          if (vi + kThreads < vend) tee[vi + kThreads] = v1;
-        }
-        if (kMode == 2) {
-          mask_vec<E>(v0, tb);
-          mask_vec<E>(v1, tb);
+#pragma unroll
+        for (int j = 0; j < kStageVecs; ++j) {
+          if (kMode == 1 && vi + j * kThreads < vend) tee[vi + j * kThreads] = v[j];
+          if (kMode == 2) mask_vec<E>(v[j], tb);
         }
         if (st >= nfull) {
-          if (vi >= vend) v0 = E::pad();
-          if (vi + kThreads >= vend) v1 = E::pad();
+#pragma unroll
+          for (int j = 0; j < kStageVecs; ++j)
+            if (vi + j * kThreads >= vend) v[j] = E::pad();
         }
-        float x0[E::kVec], x1[E::kVec];
-        E::unpack(v0, x0);
-        E::unpack(v1, x1);
-        acc.add2(x0, x1, c);
+#pragma unroll
+        for (int j = 0; j < kStageVecs; j += 2) {
+          float x0[E::kVec], x1[E::kVec];
+          E::unpack(v[j], x0);
+          E::unpack(v[j + 1], x1);
+          acc.add2(x0, x1, c);
+        }
       }
     };
     if (itm.tee)
@@ -714,60 +719,60 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
     };
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      take(v[0], v[1]);
+      take(v);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
-      if (itm.thr) {
-        mask_vec<E>(v[0], mask_bits<E>(itm.thr));
-        mask_vec<E>(v[1], mask_bits<E>(itm.thr));
+#pragma unroll
+      for (int j = 0; j < kStageVecs; ++j) {
+        if (itm.thr) mask_vec<E>(v[j], mask_bits<E>(itm.thr));
+        if (st >= nfull && vi + j * kThreads >= vend) v[j] = E::pad();
+        float x[E::kVec];
+        E::unpack(v[j], x);
+        vec(x, (vi + j * kThreads) * E::kVec);
       }
-      if (st >= nfull) {
-        if (vi >= vend) v[0] = E::pad();
-        if (vi + kThreads >= vend) v[1] = E::pad();
-      }
-      float x[E::kVec];
-      E::unpack(v[0], x);
-      vec(x, vi * E::kVec);
-      E::unpack(v[1], x);
-      vec(x, (vi + kThreads) * E::kVec);
     }
   } else if (kind == kRace) {
     float wbest = kNegInf;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      take(v[0], v[1]);
+      take(v);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
-      if (itm.thr) {
-        mask_vec<E>(v[0], mask_bits<E>(itm.thr));
-        mask_vec<E>(v[1], mask_bits<E>(itm.thr));
+#pragma unroll
+      for (int j = 0; j < kStageVecs; ++j) {
+        if (itm.thr) mask_vec<E>(v[j], mask_bits<E>(itm.thr));
+        if (st >= nfull && vi + j * kThreads >= vend) v[j] = E::pad();
       }
-      if (st >= nfull) {
-        if (vi >= vend) v[0] = E::pad();
-        if (vi + kThreads >= vend) v[1] = E::pad();
+#pragma unroll
+      for (int j = 0; j < kStageVecs; j += 2) {
+        float x0[E::kVec], x1[E::kVec];
+        E::unpack(v[j], x0);
+        E::unpack(v[j + 1], x1);
+        race_stage<E>(acc, wbest, SharedBest<kShare>{s_best}, x0, x1,
+                      (vi + j * kThreads) * E::kVec, (vi + (j + 1) * kThreads) * E::kVec, c,
+                      (uint32_t)pos, rk, P.key);
       }
-      float x0[E::kVec], x1[E::kVec];
-      E::unpack(v[0], x0);
-      E::unpack(v[1], x1);
-      race_stage<E>(acc, wbest, SharedBest<kShare>{s_best}, x0, x1, vi * E::kVec, (vi + kThreads) * E::kVec, c,
-                    (uint32_t)pos, rk, P.key);
     }
   } else {
     const ResidualRow rr = residual_row(c, itm.mp, itm.inv_sp, itm.mq, itm.inv_sq);
     float wbest = kNegInf;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      take(v[0], v[1]);
-      const int vi = vbeg + st * kThreads + tid;
-      if (itm.thr) mask_vec<E>(v[0], mask_bits<E>(itm.thr));
-      if (itm.thr2) mask_vec<E>(v[1], mask_bits<E>(itm.thr2));
-      if (st >= nfull && vi >= vend) {
-        v[0] = E::pad();
-        v[1] = E::pad();
+      take(v);
+#pragma unroll
+      for (int p = 0; p < kStagePairs; ++p) {
+        const int vi = vbeg + (st * kStagePairs + p) * kThreads + tid;
+        uint4 vt = v[2 * p], vd = v[2 * p + 1];
+        if (itm.thr) mask_vec<E>(vt, mask_bits<E>(itm.thr));
+        if (itm.thr2) mask_vec<E>(vd, mask_bits<E>(itm.thr2));
+        if (st >= nfull && vi >= vend) {
+          vt = E::pad();
+          vd = E::pad();
+        }
+        float x[E::kVec], z[E::kVec];
+        E::unpack(vt, x);
+        E::unpack(vd, z);
+        residual_stage<E>(acc, wbest, SharedBest<kShare>{s_best}, x, z, vi * E::kVec, rr,
+                          (uint32_t)pos, rk, P.key);
       }
-      float x[E::kVec], z[E::kVec];
-      E::unpack(v[0], x);
-      E::unpack(v[1], z);
-      residual_stage<E>(acc, wbest, SharedBest<kShare>{s_best}, x, z, vi * E::kVec, rr, (uint32_t)pos, rk,
-                        P.key);
     }
   }
   acc = warp_reduce(acc);
@@ -1466,7 +1471,7 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
     constexpr int kVPB = kVocabBlock / E::kVec;
     it.vbeg = b0 * kVPB;
     it.vend = min(b1 * kVPB, P.nvec);
-    const int per = it.kind == kResidual ? kThreads : kThreads * kStageVecs;
+    const int per = (it.kind == kResidual ? kStagePairs : kStageVecs) * kThreads;
     it.nst = (it.vend - it.vbeg + per - 1) / per;
     const int vy = it.y >= 0 ? it.y / E::kVec : -1;
     it.yv = (it.kind == kSoftmax && vy >= it.vbeg && vy < it.vend) ? vy : -1;
@@ -1836,7 +1841,7 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
       lc.active = false;
       lc.open(queue, &s_qend);
       for (int s = 0; s < kStages - 1; ++s) lc.issue(queue, &s_qend, ring, s);
-      auto take = [&](uint4& v0, uint4& v1) { ring_take(queue, &s_qend, ring, lc, gs, v0, v1); };
+      auto take = [&](uint4 (&v)[kStageVecs]) { ring_take(queue, &s_qend, ring, lc, gs, v); };
       segments([&](const QItem& it, int slot) {
         return seg_reduce<E, kShare>(P, it, &s_xy[slot], &s_best[slot], take);
       });

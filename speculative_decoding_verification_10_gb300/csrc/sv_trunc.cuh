@@ -210,10 +210,13 @@ __device__ __forceinline__ int block_extreme(int v, bool is_max, int* s_part) {
 // 16-bit key to keep from (0 keeps everything).  Returns false, leaving *tau,
 // when the row needs the radix descent: a non-finite maximum, fewer than K
 // elements in the window, or a top-p boundary below the window.
+//   kfloor: a key at or below the K-th largest (0 when unknown): with top-k
+//   on, keys below it cannot survive and are not counted.
 template <typename EachVec>
 __device__ bool window_thresholds(EachVec&& each_vec, int V, float mx, float T, bool use_k, int K,
-                                  bool use_p, float Pp, unsigned int* s_hist, double* s_dpart,
-                                  unsigned int* s_upart, int* s_ipart, uint32_t* tau) {
+                                  bool use_p, float Pp, uint32_t kfloor, unsigned int* s_hist,
+                                  double* s_dpart, unsigned int* s_upart, int* s_ipart,
+                                  uint32_t* tau) {
   if (!(mx > kNegInf && mx < 3.0e38f)) return false;
   const int tid = threadIdx.x;
   const int hb_top = (int)(trunc_key<BF16>(mx) >> 8);
@@ -225,6 +228,8 @@ __device__ bool window_thresholds(EachVec&& each_vec, int V, float mx, float T, 
   __syncthreads();
   float below = 0.f;  // mass of this thread's elements below the window
   const uint32_t kb = (uint32_t)lo << 8;  // the window's lowest key
+  const uint32_t kc = use_k ? max(kb, kfloor) : kb;  // the lowest key counted
+  const bool tail_mass = use_p && !use_k;  // survivors below the window exist
   each_vec([&](bool ok, uint4 q) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -233,9 +238,9 @@ __device__ bool window_thresholds(EachVec&& each_vec, int V, float mx, float T, 
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // the lower-addressed logit is the low half
         const uint32_t k = h ? (k2 >> 16) : (k2 & 0xffffu);
-        if (ok && k >= kb) {
+        if (ok && k >= kc) {
           atomicAdd(&s_hist[k - kb], 1u);  // below 2048: no key exceeds the maximum's
-        } else if (ok && use_p) {
+        } else if (ok && tail_mass && k < kb) {
           const float x = __uint_as_float(h ? (w[j] & 0xffff0000u) : (w[j] << 16));
           below += fast_ex2(fmaf(x, c, -cm));
         }
@@ -427,6 +432,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       clear_counts();
       float mx = kNegInf;
       bool nan = false;
+      uint32_t kx_t = 0u;  // this thread's largest key (packed bf16 pass)
       const int shift0 = 8 * (kLevels - 1);
       if constexpr (kFast) {
         // packed keys, two logits a word: their largest and smallest (the -inf
@@ -445,6 +451,7 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
         const uint32_t kn = min(kmin & 0xffffu, kmin >> 16);
         nan = kx > 0xff80u || kn < 0x007fu;  // above +inf's key or below -inf's
         mx = nan ? kNegInf : key_logit(kx);
+        kx_t = kx;
       } else {
         each_deep([&](bool ok, float x) {
           nan |= ok && x != x;
@@ -467,9 +474,27 @@ __global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
       __syncthreads();
       bool done = false;  // the thresholds were found by the window histogram
       if constexpr (kFast) {
+        // top-k floor: the threads' maxima are distinct elements, so the high
+        // byte h with at least K of them in bins >= h bounds the K-th largest
+        // key from below (a thread that saw only padding counts as -inf,
+        // which can only lower the floor)
+        uint32_t kfloor = 0u;
+        if (!copy && use_k && K <= kTruncThreads) {
+          atomicAdd(&s_cnt[kx_t >> 8], 1u);
+          __syncthreads();
+          if (warp == 0) {
+            unsigned long long above;
+            const int d = pick_digit(s_cnt, nullptr, 0, (unsigned long long)K, 0.0, 1.0, &above);
+            if (lane == 0) s_digit = d;
+          }
+          __syncthreads();
+          kfloor = (uint32_t)s_digit << 8;
+          if (tid < 256) s_cnt[tid] = 0u;
+          __syncthreads();
+        }
         if (!copy) {
-          done = window_thresholds(each_vec, P.vocab, mx, T, use_k, K, use_p, Pp, s_hist, s_dpart,
-                                   s_upart, s_ipart, &tau);
+          done = window_thresholds(each_vec, P.vocab, mx, T, use_k, K, use_p, Pp, kfloor, s_hist,
+                                   s_dpart, s_upart, s_ipart, &tau);
           if (!done && use_k) {
             // the radix descent below starts from the level-0 counts
             clear_counts();
