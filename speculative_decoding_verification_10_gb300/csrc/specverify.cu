@@ -203,6 +203,15 @@ bool kernel_shape(int device, int dtype, KernelShape* out) {
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ring_bytes()) != cudaSuccess)
       return false;
+  // the builds for truncated rounds (two CTAs per SM, the same grids)
+  const void* trunc_fn = dtype == SPECVERIFY_BF16
+                             ? reinterpret_cast<const void*>(sv::sv_wave<sv::BF16, true, 2, true, true>)
+                             : reinterpret_cast<const void*>(sv::sv_wave<sv::F32, true, 2, true, true>);
+  if (cudaFuncSetAttribute(trunc_fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+      cudaFuncSetAttribute(trunc_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)ring_bytes()) != cudaSuccess)
+    return false;
   out->grid_scalar = occ[0] * sms;
   out->grid_aligned = occ[1] * sms;
   out->grid3_scalar = occ[2] * sms;
@@ -286,7 +295,8 @@ int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
       sv::sv_truncate<E, false><<<tgrid, sv::kTruncThreads, 0, s>>>(*tp);
   }
   const size_t smem = aligned ? ring_bytes() : 0;
-  const bool three = wave_three(c, P.batch);
+  const bool trunc = P.thr_t != nullptr;  // truncated rounds: the masking build, two CTAs per SM
+  const bool three = !trunc && wave_three(c, P.batch);
   const int grid = three ? (aligned ? c.shape.grid3_aligned : c.shape.grid3_scalar)
                          : (aligned ? c.shape.grid_aligned : c.shape.grid_scalar);
   for (int w = 0; w < P.n_waves; ++w) {
@@ -298,7 +308,10 @@ int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
     // per w4 round end to end)
     const bool host = P.tee_target != nullptr;
     cudaError_t e;
-    if (three)
+    if (trunc)
+      e = aligned ? launch_wave(sv::sv_wave<E, true, 2, true, true>, grid, smem, s, P)
+                  : launch_wave(sv::sv_wave<E, false, 2, true, true>, grid, smem, s, P);
+    else if (three)
       e = aligned ? (host ? launch_wave(sv::sv_wave<E, true, 3, false>, grid, smem, s, P)
                           : launch_wave(sv::sv_wave<E, true, 3>, grid, smem, s, P))
                   : launch_wave(sv::sv_wave<E, false, 3>, grid, smem, s, P);

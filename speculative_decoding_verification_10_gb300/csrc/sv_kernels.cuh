@@ -49,9 +49,8 @@ namespace sv {
 constexpr int kComputeWarps = 7;
 constexpr int kThreads = kComputeWarps * 32;   // compute threads
 constexpr int kBlock = kThreads + 32;          // + the control warp
-constexpr int kStages = 8;                     // ring stages (power of 2)
-constexpr int kStageVecs = 2;                  // 16-byte vectors per thread and stage (even)
-constexpr int kStagePairs = kStageVecs / 2;    // ... t_j / d_j pairs of a residual stage
+constexpr int kStages = 8;
+constexpr int kStageVecs = 2;
 constexpr int kQueue = 16;                     // segment queue entries (power of 2)
 constexpr int kMaxBatch = 4096;                // requests per round
 constexpr int kMaxK = 31;                      // draft positions per request
@@ -446,7 +445,8 @@ __device__ __forceinline__ void take_finite(BestAcc& acc, float score, int i) {
 // whose bounded score is below it cannot be the row's winner, so every lane
 // tests against the warp's best, not only its own.  The test keeps ties
 // (>=), which take_cmp then orders by index.  Call with the whole warp.
-template <typename E, bool kShare>
+// kSkipEmpty (truncated rounds): a stage of -inf logits has no id to race.
+template <typename E, bool kShare, bool kSkipEmpty>
 __device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const SharedBest<kShare>& sb,
                                            const float (&x0)[E::kVec],
                                            const float (&x1)[E::kVec], int e0, int e1, float c,
@@ -465,8 +465,8 @@ __device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const Sha
     const float lo = warp_max(mx < -kNegInf ? mx : kNegInf) * c + kMinGain;
     if (lo > kNegInf) wbest = lo - kBoundSlack;
   }
-  // a stage of -inf logits (a truncated row) has no id to race
-  if (!__any_sync(0xffffffffu, mx > kNegInf && fmaf(mx, c, kMaxGain) >= wbest)) return;
+  if (!__any_sync(0xffffffffu, (!kSkipEmpty || mx > kNegInf) && fmaf(mx, c, kMaxGain) >= wbest))
+    return;
   uint32_t g[2 * G];
 #pragma unroll
   for (int j = 0; j < G; ++j) {
@@ -501,7 +501,7 @@ __device__ __forceinline__ void race_stage(BestAcc& acc, float& wbest, const Sha
 // Residual race over one stage: vector x of t_j and z of d_j, the same kVec
 // ids from e0.  fmaf(x, c, rr.lp) bounds log2 (p_v - q_v) from above, so the
 // two exponentials are only taken for ids that pass.  Call with the whole warp.
-template <typename E, bool kShare>
+template <typename E, bool kShare, bool kSkipEmpty>
 __device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
                                                const SharedBest<kShare>& sb,
                                                const float (&x)[E::kVec],
@@ -513,7 +513,8 @@ __device__ __forceinline__ void residual_stage(BestAcc& acc, float& wbest,
 #pragma unroll
   for (int i = 1; i < E::kVec; ++i) mx = fmaxf(mx, x[i]);
   wbest = fmaxf(wbest, sb.load());
-  if (!__any_sync(0xffffffffu, mx > kNegInf && fmaf(mx, rr.c, rr.lp) + kMaxGain >= wbest))
+  if (!__any_sync(0xffffffffu,
+                  (!kSkipEmpty || mx > kNegInf) && fmaf(mx, rr.c, rr.lp) + kMaxGain >= wbest))
     return;
   uint32_t g[G];
 #pragma unroll
@@ -567,18 +568,17 @@ __device__ int warp_row_race(const Params& P, const char* trow, float c, uint32_
 
 // ---------------------------------------------------------------------------
 // The per-thread copy ring (compute threads, aligned rows).  Stage s of a
-// segment holds kStageVecs vectors per thread: vectors vbeg + (kStageVecs s +
-// j) kThreads + tid, j = 0 .. kStageVecs - 1, of a single row; or, for a
-// residual segment, vector vbeg + (kStagePairs s + p) kThreads + tid of t_j
-// (slot vector 2 p) and of d_j (slot vector 2 p + 1).
+// segment holds two vectors per thread: vectors vbeg + 2 s kThreads + tid and
+// + kThreads of a single row, or vector vbeg + s kThreads + tid of t_j and of
+// d_j for a residual segment.
 // ---------------------------------------------------------------------------
 struct LoadCursor {
   int q;      // queue index of the segment being loaded
   int left;   // its stages still to copy
   const uint4* b0;
   const uint4* b1;
-  int i, step, vend;  // this thread's first vector of the next stage
-  bool active, pair;
+  int i0, i1, step, vend;
+  bool active;
 
   // s_qend: segments the control warp has queued, or -1 - n once all n are.
   __device__ __forceinline__ void open(const QItem* queue, const int* s_qend) {
@@ -587,11 +587,12 @@ struct LoadCursor {
     active = q < avail;
     if (active) {
       const QItem& it = queue[q & (kQueue - 1)];
-      pair = it.kind == kResidual;
+      const bool pair = it.kind == kResidual;
       b0 = reinterpret_cast<const uint4*>(it.row);
       b1 = reinterpret_cast<const uint4*>(pair ? it.row2 : it.row);
-      i = it.vbeg + (int)threadIdx.x;
-      step = (pair ? kStagePairs : kStageVecs) * kThreads;
+      i0 = it.vbeg + (int)threadIdx.x;
+      i1 = pair ? i0 : i0 + kThreads;
+      step = pair ? kThreads : kStageVecs * kThreads;
       vend = it.vend;
       left = it.nst;
     }
@@ -603,12 +604,10 @@ struct LoadCursor {
     if (!active) open(queue, s_qend);
     if (active) {
       uint4* dst = ring + slot * kStageVecs * kThreads + threadIdx.x;
-#pragma unroll
-      for (int j = 0; j < kStageVecs; ++j) {
-        const int v = i + (pair ? (j >> 1) : j) * kThreads;
-        cp_async16_if(dst + j * kThreads, ((pair && (j & 1)) ? b1 : b0) + v, v < vend);
-      }
-      i += step;
+      cp_async16_if(dst, b0 + i0, i0 < vend);
+      cp_async16_if(dst + kThreads, b1 + i1, i1 < vend);
+      i0 += step;
+      i1 += step;
       if (--left == 0) {
         ++q;
         open(queue, s_qend);
@@ -621,13 +620,12 @@ struct LoadCursor {
 // Reads one stage of the ring (after its copies landed) and refills the ring
 // one stage ahead.
 __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend, uint4* ring,
-                                          LoadCursor& lc, int& g_stage,
-                                          uint4 (&v)[kStageVecs]) {
+                                          LoadCursor& lc, int& g_stage, uint4& v0, uint4& v1) {
   cp_async_wait<kStages - 2>();
   const int slot = g_stage & (kStages - 1);
   const uint4* src = ring + slot * kStageVecs * kThreads + threadIdx.x;
-#pragma unroll
-  for (int j = 0; j < kStageVecs; ++j) v[j] = src[j * kThreads];
+  v0 = src[0];
+  v1 = src[kThreads];
   lc.issue(queue, s_qend, ring, (g_stage + kStages - 1) & (kStages - 1));
   ++g_stage;
 }
@@ -636,8 +634,9 @@ __device__ __forceinline__ void ring_take(const QItem* queue, const int* s_qend,
 // Segment reductions (compute threads).  Each returns this warp's partial; a
 // softmax segment that holds the draft token y also leaves x[y] in *s_xy.
 // ---------------------------------------------------------------------------
-// `take(v)` hands over the next stage of the segment from the copy ring.
-template <typename E, bool kShare, typename Take>
+// `take(v0, v1)` hands over the next stage of the segment from the copy ring.
+// kTrunc: the build for truncated rounds, which masks the rows on load.
+template <typename E, bool kShare, bool kTrunc, typename Take>
 __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm, float* s_xy,
                                               uint32_t* s_best, Take& take) {
   const int tid = threadIdx.x;
@@ -645,8 +644,10 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
   // copy ring's memory clobbers would otherwise make the loop reload)
   const int kind = itm.kind, vbeg = itm.vbeg, vend = itm.vend, nst = itm.nst, pos = itm.pos;
   const float c = itm.c;
+  const uint32_t thr = itm.thr, thr2 = itm.thr2;  // truncation (0: none)
+  const uint32_t tb = mask_bits<E>(thr), tb2 = mask_bits<E>(thr2);
   const RequestKey rk{itm.req_lo, itm.req_hi};
-  const int per = (kind == kResidual ? kStagePairs : kStageVecs) * kThreads;
+  const int per = kind == kResidual ? kThreads : kStageVecs * kThreads;
   const int nfull = (vend - vbeg) / per;
   if (kind == kSoftmax) {
     LazySoftmax acc;
@@ -655,43 +656,46 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
     // stages so that its latency hides under them (no test inside the loop)
     const int yv = itm.yv;
     const bool own_y = yv >= vbeg && yv < vend && (yv - vbeg) % kThreads == tid;
-    const uint32_t thr = itm.thr, tb = mask_bits<E>(thr);
     float xy = 0.f;
-    if (own_y) xy = mask1<E>(E::load1(itm.row, itm.y), thr);
+    if (own_y) xy = kTrunc ? mask1<E>(E::load1(itm.row, itm.y), thr) : E::load1(itm.row, itm.y);
     // the stages: plain, with the copy to the device staging, or truncated
     // (a loop of its own for each, so the common one carries no test)
     auto stages = [&](auto mode) {
       constexpr int kMode = decltype(mode)::value;
       uint4* tee = reinterpret_cast<uint4*>(itm.tee);
       for (int st = 0; st < nst; ++st) {
-        uint4 v[kStageVecs];
-        take(v);
+        uint4 v0, v1;
+        take(v0, v1);
         const int vi = vbeg + st * kStageVecs * kThreads + tid;
-#pragma unroll
-        for (int j = 0; j < kStageVecs; ++j) {
-          if (kMode == 1 && vi + j * kThreads < vend) tee[vi + j * kThreads] = v[j];
-          if (kMode == 2) mask_vec<E>(v[j], tb);
+        if (kMode == 1) {
+          if (vi < vend) tee[vi] = v0;
+          if (vi + kThreads < vend) tee[vi + kThreads] = v1;
+        }
+        if (kMode == 2) {
+          mask_vec<E>(v0, tb);
+          mask_vec<E>(v1, tb);
         }
         if (st >= nfull) {
-#pragma unroll
-          for (int j = 0; j < kStageVecs; ++j)
-            if (vi + j * kThreads >= vend) v[j] = E::pad();
+          if (vi >= vend) v0 = E::pad();
+          if (vi + kThreads >= vend) v1 = E::pad();
         }
-#pragma unroll
-        for (int j = 0; j < kStageVecs; j += 2) {
-          float x0[E::kVec], x1[E::kVec];
-          E::unpack(v[j], x0);
-          E::unpack(v[j + 1], x1);
-          acc.add2(x0, x1, c);
-        }
+        float x0[E::kVec], x1[E::kVec];
+        E::unpack(v0, x0);
+        E::unpack(v1, x1);
+        acc.add2(x0, x1, c);
       }
     };
-    if (itm.tee)
-      stages(std::integral_constant<int, 1>{});
-    else if (thr)
-      stages(std::integral_constant<int, 2>{});
-    else
-      stages(std::integral_constant<int, 0>{});
+    if constexpr (kTrunc) {
+      if (thr)
+        stages(std::integral_constant<int, 2>{});
+      else
+        stages(std::integral_constant<int, 0>{});
+    } else {
+      if (itm.tee)
+        stages(std::integral_constant<int, 1>{});
+      else
+        stages(std::integral_constant<int, 0>{});
+    }
     if (own_y) *s_xy = xy;
     SoftmaxAcc a = warp_reduce(acc.result());
     return Partial{a.m, a.s, -1, 0u};
@@ -719,60 +723,62 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
     };
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      take(v);
+      take(v[0], v[1]);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
-#pragma unroll
-      for (int j = 0; j < kStageVecs; ++j) {
-        if (itm.thr) mask_vec<E>(v[j], mask_bits<E>(itm.thr));
-        if (st >= nfull && vi + j * kThreads >= vend) v[j] = E::pad();
-        float x[E::kVec];
-        E::unpack(v[j], x);
-        vec(x, (vi + j * kThreads) * E::kVec);
+      if (kTrunc && thr) {
+        mask_vec<E>(v[0], tb);
+        mask_vec<E>(v[1], tb);
       }
+      if (st >= nfull) {
+        if (vi >= vend) v[0] = E::pad();
+        if (vi + kThreads >= vend) v[1] = E::pad();
+      }
+      float x[E::kVec];
+      E::unpack(v[0], x);
+      vec(x, vi * E::kVec);
+      E::unpack(v[1], x);
+      vec(x, (vi + kThreads) * E::kVec);
     }
   } else if (kind == kRace) {
     float wbest = kNegInf;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      take(v);
+      take(v[0], v[1]);
       const int vi = vbeg + st * kStageVecs * kThreads + tid;
-#pragma unroll
-      for (int j = 0; j < kStageVecs; ++j) {
-        if (itm.thr) mask_vec<E>(v[j], mask_bits<E>(itm.thr));
-        if (st >= nfull && vi + j * kThreads >= vend) v[j] = E::pad();
+      if (kTrunc && thr) {
+        mask_vec<E>(v[0], tb);
+        mask_vec<E>(v[1], tb);
       }
-#pragma unroll
-      for (int j = 0; j < kStageVecs; j += 2) {
-        float x0[E::kVec], x1[E::kVec];
-        E::unpack(v[j], x0);
-        E::unpack(v[j + 1], x1);
-        race_stage<E>(acc, wbest, SharedBest<kShare>{s_best}, x0, x1,
-                      (vi + j * kThreads) * E::kVec, (vi + (j + 1) * kThreads) * E::kVec, c,
-                      (uint32_t)pos, rk, P.key);
+      if (st >= nfull) {
+        if (vi >= vend) v[0] = E::pad();
+        if (vi + kThreads >= vend) v[1] = E::pad();
       }
+      float x0[E::kVec], x1[E::kVec];
+      E::unpack(v[0], x0);
+      E::unpack(v[1], x1);
+      race_stage<E, kShare, kTrunc>(acc, wbest, SharedBest<kShare>{s_best}, x0, x1, vi * E::kVec,
+                                    (vi + kThreads) * E::kVec, c, (uint32_t)pos, rk, P.key);
     }
   } else {
     const ResidualRow rr = residual_row(c, itm.mp, itm.inv_sp, itm.mq, itm.inv_sq);
     float wbest = kNegInf;
     for (int st = 0; st < nst; ++st) {
       uint4 v[kStageVecs];
-      take(v);
-#pragma unroll
-      for (int p = 0; p < kStagePairs; ++p) {
-        const int vi = vbeg + (st * kStagePairs + p) * kThreads + tid;
-        uint4 vt = v[2 * p], vd = v[2 * p + 1];
-        if (itm.thr) mask_vec<E>(vt, mask_bits<E>(itm.thr));
-        if (itm.thr2) mask_vec<E>(vd, mask_bits<E>(itm.thr2));
-        if (st >= nfull && vi >= vend) {
-          vt = E::pad();
-          vd = E::pad();
-        }
-        float x[E::kVec], z[E::kVec];
-        E::unpack(vt, x);
-        E::unpack(vd, z);
-        residual_stage<E>(acc, wbest, SharedBest<kShare>{s_best}, x, z, vi * E::kVec, rr,
-                          (uint32_t)pos, rk, P.key);
+      take(v[0], v[1]);
+      const int vi = vbeg + st * kThreads + tid;
+      if (kTrunc) {
+        if (thr) mask_vec<E>(v[0], tb);
+        if (thr2) mask_vec<E>(v[1], tb2);
       }
+      if (st >= nfull && vi >= vend) {
+        v[0] = E::pad();
+        v[1] = E::pad();
+      }
+      float x[E::kVec], z[E::kVec];
+      E::unpack(v[0], x);
+      E::unpack(v[1], z);
+      residual_stage<E, kShare, kTrunc>(acc, wbest, SharedBest<kShare>{s_best}, x, z,
+                                        vi * E::kVec, rr, (uint32_t)pos, rk, P.key);
     }
   }
   acc = warp_reduce(acc);
@@ -781,8 +787,13 @@ __device__ __forceinline__ Partial seg_reduce(const Params& P, const QItem& itm,
 
 // Scalar path (rows not 16-byte aligned): warp w takes vocab blocks
 // vbeg + w, vbeg + w + 7, ...; lane l the ids 128 b + l + 32 j.
-template <typename E>
+template <typename E, bool kTrunc>
 __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, float* s_xy) {
+  // one logit, masked in truncated rounds
+  auto ld = [&](const char* row, int v, uint32_t thr) {
+    const float x = E::load1(row, v);
+    return kTrunc ? mask1<E>(x, thr) : x;
+  };
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const RequestKey rk{it.req_lo, it.req_hi};
   if (it.kind == kSoftmax) {
@@ -792,7 +803,7 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
       for (int j = 0; j < 4; ++j) {
         const int v = b * kVocabBlock + lane + 32 * j;
         if (v < P.vocab) {
-          const float x = mask1<E>(E::load1(it.row, v), it.thr);
+          const float x = ld(it.row, v, it.thr);
           if (v == it.y) *s_xy = x;
           acc.add1(x, it.c);
         }
@@ -808,7 +819,7 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
       for (int j = 0; j < 4; ++j) {
         const int v = b * kVocabBlock + lane + 32 * j;
         if (v < P.vocab) {
-          const float x = mask1<E>(E::load1(it.row, v), it.thr);
+          const float x = ld(it.row, v, it.thr);
           acc.nan |= (x != x);
           acc.take(x, v);
         }
@@ -820,10 +831,8 @@ __device__ __forceinline__ Partial seg_scalar(const Params& P, const QItem& it, 
     float x[4], z[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      x[i] = v0 + i < P.vocab ? mask1<E>(E::load1(it.row, v0 + i), it.thr) : kNegInf;
-      z[i] = (it.kind == kResidual && v0 + i < P.vocab)
-                 ? mask1<E>(E::load1(it.row2, v0 + i), it.thr2)
-                 : kNegInf;
+      x[i] = v0 + i < P.vocab ? ld(it.row, v0 + i, it.thr) : kNegInf;
+      z[i] = (it.kind == kResidual && v0 + i < P.vocab) ? ld(it.row2, v0 + i, it.thr2) : kNegInf;
     }
     if (it.kind == kRace) {
       race_vec<F32>(acc, x, v0, it.c, pos, rk, P.key);
@@ -1471,7 +1480,7 @@ __device__ void decode_segment(const Params& P, int phase, int e, int b0, int b1
     constexpr int kVPB = kVocabBlock / E::kVec;
     it.vbeg = b0 * kVPB;
     it.vend = min(b1 * kVPB, P.nvec);
-    const int per = (it.kind == kResidual ? kStagePairs : kStageVecs) * kThreads;
+    const int per = it.kind == kResidual ? kThreads : kThreads * kStageVecs;
     it.nst = (it.vend - it.vbeg + per - 1) / per;
     const int vy = it.y >= 0 ? it.y / E::kVec : -1;
     it.yv = (it.kind == kSoftmax && vy >= it.vbeg && vy < it.vend) ? vy : -1;
@@ -1769,7 +1778,9 @@ __global__ void __launch_bounds__(kPlanThreads) sv_plan(Params P) {
 // kMinBlocks CTAs per SM bound the registers: 2 (up to 128 a thread) for
 // windows that stream long shares, 3 (up to 80) for small, latency-bound ones.
 // kShare: the race's best shared by the warps of a segment (see SharedBest).
-template <typename E, bool kAligned, int kMinBlocks, bool kShare = true>
+// kTrunc: the build for truncated rounds (Params::thr_t set), which masks
+// every row it loads with the row's threshold.
+template <typename E, bool kAligned, int kMinBlocks, bool kShare = true, bool kTrunc = false>
 __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* ring = reinterpret_cast<uint4*>(smem_raw);
@@ -1833,7 +1844,8 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
       }
     };
     if (!kAligned) {
-      segments([&](const QItem& it, int slot) { return seg_scalar<E>(P, it, &s_xy[slot]); });
+      segments(
+          [&](const QItem& it, int slot) { return seg_scalar<E, kTrunc>(P, it, &s_xy[slot]); });
     } else {
       int gs = 0;
       LoadCursor lc;
@@ -1841,9 +1853,9 @@ __global__ void __launch_bounds__(kBlock, kMinBlocks) sv_wave(Params P) {
       lc.active = false;
       lc.open(queue, &s_qend);
       for (int s = 0; s < kStages - 1; ++s) lc.issue(queue, &s_qend, ring, s);
-      auto take = [&](uint4 (&v)[kStageVecs]) { ring_take(queue, &s_qend, ring, lc, gs, v); };
+      auto take = [&](uint4& v0, uint4& v1) { ring_take(queue, &s_qend, ring, lc, gs, v0, v1); };
       segments([&](const QItem& it, int slot) {
-        return seg_reduce<E, kShare>(P, it, &s_xy[slot], &s_best[slot], take);
+        return seg_reduce<E, kShare, kTrunc>(P, it, &s_xy[slot], &s_best[slot], take);
       });
       cp_async_wait_all();
     }
