@@ -22,7 +22,8 @@ The line also carries:
                outputs copied back, every step; the kernels read the pinned
                logits in place (only the rows a round reads cross the link);
   cpu_baseline the CPU oracle on a bounded sample of the same batch (1 core);
-  clocks       nvidia-smi samples taken during the timed region.
+  clocks       SM clock samples taken during the timed region (NVML every
+               millisecond, else nvidia-smi every 200 ms).
 --impl reference times the CPU oracle instead (the only other arm there is).
 """
 from __future__ import annotations
@@ -199,8 +200,67 @@ def recorded_traffic(workload):
     return ent.get("dram_bytes_per_launch")
 
 
+class NvmlClocks:
+    """Read-only NVML queries through ctypes (libnvidia-ml): the SM clock, its
+    maximum and the clock event reasons of one GPU, polled every millisecond
+    from a host thread between mark("start") and mark("stop").  None of the
+    calls changes a setting."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index),
+                                                  ctypes.byref(self.dev)) != 0:
+            raise RuntimeError("no NVML handle")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.running = False
+
+    def _one(self):
+        ct = self.ct
+        mhz, mx, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(mhz)) != 0:  # NVML_CLOCK_SM
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ct.byref(mx))
+        self.reasons_fn(self.dev, ct.byref(rs))
+        return mhz.value, mx.value, rs.value
+
+    def _loop(self):
+        while self.running:
+            one = self._one()
+            if one is not None:
+                self.samples.append(one)
+            time.sleep(0.001)
+
+    def start(self):
+        self.samples = []
+        self.running = True
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.running = False
+        self.thread.join(timeout=1.0)
+        if not self.samples:
+            return None
+        reasons = sorted({name for _, _, r in self.samples
+                          for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(s for s, _, _ in self.samples),
+                "sm_max_mhz": max(m for _, m, _ in self.samples), "reasons": reasons,
+                "samples": len(self.samples), "window": "timed region (NVML, 1 ms period)"}
+
+
 class ClockSampler:
-    """nvidia-smi samples every 200 ms; keeps those inside [start, stop]."""
+    """Clock samples of the timed region: NVML polled every millisecond when the
+    library loads, else nvidia-smi every 200 ms (samples inside [start, stop])."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -211,6 +271,10 @@ class ClockSampler:
         self.samples = []
         self.proc = None
         self.t_start = self.t_stop = None
+        try:
+            self.nvml = NvmlClocks(gpu_index)
+        except Exception:
+            self.nvml = None
 
     def start(self):
         try:
@@ -230,8 +294,22 @@ class ClockSampler:
 
     def mark(self, which):
         setattr(self, "t_" + which, time.time())
+        if self.nvml is not None:
+            if which == "start":
+                self.nvml.start()
+            elif which == "stop":
+                self.nvml_info = self.nvml.stop()
 
     def stop(self):
+        fast = getattr(self, "nvml_info", None)
+        if fast is not None:
+            if self.proc is not None:
+                self.proc.terminate()
+                try:
+                    self.proc.wait(timeout=5)
+                except Exception:
+                    self.proc.kill()
+            return fast
         if self.proc is None:
             return None
         time.sleep(0.25)

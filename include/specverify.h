@@ -178,7 +178,7 @@ int specverify_run_ex(specverify_t h, const void *target_logits, const void *dra
  * writes (draft tokens must come from the truncated draft distributions).  A
  * top_p NaN or <= 0 keeps its rows whole and sets SPECVERIFY_STATUS_BAD_TRUNC.
  * The other arguments are those of specverify_run; the round has one more
- * launch (the threshold pass, one CTA per SM over every window row).
+ * launch (the threshold pass, two CTAs per SM over every window row).
  */
 int specverify_run_truncated(specverify_t h, const void *target_logits,
                              const void *draft_logits, const int32_t *draft_tokens,
@@ -420,7 +420,7 @@ int specverify_metrics(const int32_t *accepted_len, const int32_t *num_draft, in
  * Layout as specverify_run: target_in/_out [batch + total_draft, vocab],
  * draft_in/_out [total_draft, vocab] (both NULL, or both given), dtype F32 or
  * BF16, device pointers on the current device; asynchronous on stream, one
- * launch (one CTA per SM, a few passes over each row through L2).
+ * launch (two CTAs per SM, a few passes over each row through L2).
  */
 int specverify_truncate(int dtype, int vocab, const void *target_in, const void *draft_in,
                         const int32_t *num_draft, const float *temperature, const int32_t *top_k,

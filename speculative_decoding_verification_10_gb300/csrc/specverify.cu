@@ -288,7 +288,7 @@ int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
     // resets the status word its bad top_p values are OR-ed into) and before
     // the first wave (which waits for it)
     const long long rows = (long long)tp->batch + (tp->draft_in ? 2ll : 1ll) * tp->total_draft;
-    const int tgrid = (int)std::min<long long>(rows, c.shape.sms);
+    const int tgrid = (int)std::min<long long>(rows, 2ll * c.shape.sms);
     if (aligned)
       sv::sv_truncate<E, true><<<tgrid, sv::kTruncThreads, 0, s>>>(*tp);
     else
@@ -1236,9 +1236,10 @@ int specverify_truncate(int dtype, int vocab, const void* target_in, const void*
   P.status = status;
   P.thr_target = nullptr;
   P.thr_draft = nullptr;
-  // one CTA per SM: the rows in flight (one per CTA) stay in L2 across the passes
+  // two CTAs per SM, a row each at a time: the rows in flight stay in L2 across
+  // the passes, and one CTA's scans overlap the other's loads
   const long long rows = (long long)batch + 2ll * total_draft;
-  const int grid = (int)std::min<long long>(rows, sms);
+  const int grid = (int)std::min<long long>(rows, 2ll * sms);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == SPECVERIFY_BF16) {
     if (aligned)

@@ -32,7 +32,7 @@
 
 namespace sv {
 
-constexpr int kTruncThreads = 1024;
+constexpr int kTruncThreads = 512;  // two CTAs per SM: one's scans overlap the other's loads
 constexpr int kTruncLoads = 8;  // 16-byte loads in flight per thread (packed passes)
 constexpr int kPackedOutLoads = 1;  // ... and in the packed output pass
 constexpr int kOutLoads = 1;    // ... and in the output pass
@@ -145,7 +145,8 @@ constexpr int kWin = 8;  // octave bins the first top-p level resolves below the
 // ---------------------------------------------------------------------------
 constexpr int kWinBins = 8;
 constexpr int kWinKeys = kWinBins * 256;
-static_assert(kWinKeys == 2 * kTruncThreads, "two window keys per thread");
+constexpr int kWinPerThread = kWinKeys / kTruncThreads;  // window keys a thread holds
+static_assert(kWinPerThread * kTruncThreads == kWinKeys, "whole window keys per thread");
 
 // The bf16 logit of a 16-bit order key (trunc_key<BF16> inverted).
 __device__ __forceinline__ float key_logit(uint32_t key) {
@@ -223,8 +224,8 @@ __device__ bool window_thresholds(EachVec&& each_vec, int V, float mx, float T, 
   const int lo = max(hb_top - (kWinBins - 1), 0);
   const float c = kLog2e / T;
   const float cm = c * mx;
-  s_hist[2 * tid] = 0u;
-  s_hist[2 * tid + 1] = 0u;
+#pragma unroll
+  for (int j = 0; j < kWinPerThread; ++j) s_hist[kWinPerThread * tid + j] = 0u;
   __syncthreads();
   float below = 0.f;  // mass of this thread's elements below the window
   const uint32_t kb = (uint32_t)lo << 8;  // the window's lowest key
@@ -254,29 +255,43 @@ __device__ bool window_thresholds(EachVec&& each_vec, int V, float mx, float T, 
     s_hist[0x7fffu - kb] = 0u;
   }
   __syncthreads();
-  // thread t holds window keys i0 = 2t and i1 = 2t + 1 (key = (lo << 8) + i)
-  const int i0 = 2 * tid, i1 = i0 + 1;
-  const unsigned int n0 = s_hist[i0], n1 = s_hist[i1];
+  // thread t holds window keys i = kWinPerThread t + j (key = (lo << 8) + i); the
+  // scans run from the highest key down
+  constexpr int kP = kWinPerThread;
+  const int ib = kP * tid;
+  unsigned int n[kP], n_own = 0u;
+#pragma unroll
+  for (int j = 0; j < kP; ++j) {
+    n[j] = s_hist[ib + j];
+    n_own += n[j];
+  }
   unsigned int n_win;
-  const unsigned int n_above = block_suffix_excl<unsigned int>(n0 + n1, s_upart, &n_win);
+  const unsigned int n_above = block_suffix_excl<unsigned int>(n_own, s_upart, &n_win);
   int first = 0;  // lowest window index a survivor of top-k may have
   if (use_k) {
     if (n_win < (unsigned int)K) return false;
     // the highest key with at least K elements at or above it
-    const unsigned int s1 = n_above + n1, s0 = s1 + n0;
-    const int cand = s1 >= (unsigned int)K ? i1 : (s0 >= (unsigned int)K ? i0 : -1);
+    unsigned int run = n_above;
+    int cand = -1;
+#pragma unroll
+    for (int j = kP - 1; j >= 0; --j) {
+      run += n[j];
+      if (cand < 0 && run >= (unsigned int)K) cand = ib + j;
+    }
     first = block_extreme(cand, true, s_ipart);
   }
   int pick = first;
   if (use_p) {
-    const double w0 = (n0 && i0 >= first)
-                          ? (double)n0 * (double)fast_ex2(fmaf(key_logit((lo << 8) + i0), c, -cm))
-                          : 0.0;
-    const double w1 = (n1 && i1 >= first)
-                          ? (double)n1 * (double)fast_ex2(fmaf(key_logit((lo << 8) + i1), c, -cm))
-                          : 0.0;
+    double w[kP], w_own = 0.0;
+#pragma unroll
+    for (int j = 0; j < kP; ++j) {
+      w[j] = (n[j] && ib + j >= first)
+                 ? (double)n[j] * (double)fast_ex2(fmaf(key_logit((lo << 8) + ib + j), c, -cm))
+                 : 0.0;
+      w_own += w[j];
+    }
     double m_win;
-    const double m_above = block_suffix_excl<double>(w0 + w1, s_dpart, &m_win);
+    const double m_above = block_suffix_excl<double>(w_own, s_dpart, &m_win);
     // survivors below the window exist only without a top-k cut inside it
     const bool tail = !use_k && n_win < (unsigned int)V;
     double m_tail = 0.0;
@@ -284,15 +299,20 @@ __device__ bool window_thresholds(EachVec&& each_vec, int V, float mx, float T, 
       const float wb = group_sum<32>(below);
       if ((tid & 31) == 0) s_dpart[tid >> 5] = (double)wb;
       __syncthreads();
-      for (int w = 0; w < kTruncThreads / 32; ++w) m_tail += s_dpart[w];
+      for (int wi = 0; wi < kTruncThreads / 32; ++wi) m_tail += s_dpart[wi];
       __syncthreads();
     }
     const double target = (double)Pp * (m_win + m_tail);
     if (tail && m_win < target) return false;
     // the lowest survivor key whose strictly larger survivors weigh below target
-    const bool k1 = n1 && i1 >= first && m_above < target;
-    const bool k0 = n0 && i0 >= first && m_above + w1 < target;
-    pick = block_extreme(k0 ? i0 : (k1 ? i1 : kWinKeys), false, s_ipart);
+    double run = m_above;
+    int lowest = kWinKeys;
+#pragma unroll
+    for (int j = kP - 1; j >= 0; --j) {
+      if (n[j] && ib + j >= first && run < target) lowest = ib + j;
+      run += w[j];
+    }
+    pick = block_extreme(lowest, false, s_ipart);
     pick = max(pick, first);
   }
   *tau = (uint32_t)((lo << 8) + pick);
@@ -300,7 +320,7 @@ __device__ bool window_thresholds(EachVec&& each_vec, int V, float mx, float T, 
 }
 
 template <typename E, bool kAligned>
-__global__ void __launch_bounds__(kTruncThreads, 1) sv_truncate(TruncParams P) {
+__global__ void __launch_bounds__(kTruncThreads, 2) sv_truncate(TruncParams P) {
   constexpr int kWarps = kTruncThreads / 32;
   __shared__ unsigned int s_whist[kWarps][256];  // per-warp counts
   __shared__ unsigned int s_cnt[256];
