@@ -171,14 +171,16 @@ int specverify_run_ex(specverify_t h, const void *target_logits, const void *dra
  * section 1: truncation must enter the acceptance test and the residual
  * consistently.  The rules and their thresholds are those of
  * specverify_truncate (top_k [batch] int32, top_p [batch] float32, same
- * meaning), but no truncated copy is written: a threshold pass stores one
- * order-key threshold per window row in the handle's scratch, and the verify
- * waves read every logit below its row's threshold as -inf as they load it.
+ * meaning), but no truncated copy is written: before each wave of the round a
+ * threshold pass stores one order-key threshold for every row that wave reads
+ * (in the handle's scratch), and the wave reads every logit below its row's
+ * threshold as -inf as it loads it; rows the round never reads get none.
  * The outputs are those of specverify_run on the rows specverify_truncate
  * writes (draft tokens must come from the truncated draft distributions).  A
- * top_p NaN or <= 0 keeps its rows whole and sets SPECVERIFY_STATUS_BAD_TRUNC.
- * The other arguments are those of specverify_run; the round has one more
- * launch (the threshold pass, two CTAs per SM over every window row).
+ * top_p NaN or <= 0 keeps its request's rows whole and sets
+ * SPECVERIFY_STATUS_BAD_TRUNC.  The other arguments are those of
+ * specverify_run; the round has one more launch per wave (its threshold pass,
+ * two CTAs per SM).
  */
 int specverify_run_truncated(specverify_t h, const void *target_logits,
                              const void *draft_logits, const int32_t *draft_tokens,

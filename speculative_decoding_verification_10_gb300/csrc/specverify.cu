@@ -283,17 +283,6 @@ int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
                  cudaEvent_t ev_start, cudaEvent_t ev_stop, const sv::TruncParams* tp) {
   if (ev_start && cudaEventRecord(ev_start, s) != cudaSuccess) return SPECVERIFY_ERR_CUDA;
   sv::sv_plan<<<1, sv::kPlanThreads, 0, s>>>(P);
-  if (tp) {
-    // truncated round: every window row's threshold, after the plan (which
-    // resets the status word its bad top_p values are OR-ed into) and before
-    // the first wave (which waits for it)
-    const long long rows = (long long)tp->batch + (tp->draft_in ? 2ll : 1ll) * tp->total_draft;
-    const int tgrid = (int)std::min<long long>(rows, 2ll * c.shape.sms);
-    if (aligned)
-      sv::sv_truncate<E, true><<<tgrid, sv::kTruncThreads, 0, s>>>(*tp);
-    else
-      sv::sv_truncate<E, false><<<tgrid, sv::kTruncThreads, 0, s>>>(*tp);
-  }
   const size_t smem = aligned ? ring_bytes() : 0;
   const bool trunc = P.thr_t != nullptr;  // truncated rounds: the masking build, two CTAs per SM
   const bool three = !trunc && wave_three(c, P.batch);
@@ -307,6 +296,24 @@ int launch_round(const RunConfig& c, sv::Params P, bool aligned, cudaStream_t s,
     // without the shared race best (measured on GB300: 8.3 against 14.5 ms
     // per w4 round end to end)
     const bool host = P.tee_target != nullptr;
+    if (trunc) {
+      // truncated round: before each wave, the thresholds of the rows that wave
+      // streams (its row and bonus lists; a correction draw re-reads rows whose
+      // thresholds an earlier wave's pass wrote).  A plain launch: it waits for
+      // the previous wave (or the plan, which also resets the status word its
+      // bad top_p values are OR-ed into), and the wave's dependent launch waits
+      // for it.
+      sv::TruncParams lt = *tp;
+      lt.lists = P.lists + (size_t)w * P.list_cap;
+      lt.list_cnt = P.list_cnt + w;
+      lt.blists = P.blists + (size_t)w * P.stride;
+      lt.blist_cnt = P.blist_cnt + w;
+      const int tgrid = 2 * c.shape.sms;
+      if (aligned)
+        sv::sv_truncate<E, true><<<tgrid, sv::kTruncThreads, 0, s>>>(lt);
+      else
+        sv::sv_truncate<E, false><<<tgrid, sv::kTruncThreads, 0, s>>>(lt);
+    }
     cudaError_t e;
     if (trunc)
       e = aligned ? launch_wave(sv::sv_wave<E, true, 2, true, true>, grid, smem, s, P)

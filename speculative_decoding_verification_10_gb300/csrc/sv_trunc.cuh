@@ -53,6 +53,12 @@ struct TruncParams {
   // is written here instead of a truncated copy (0 for a row kept whole).
   uint32_t* thr_target;
   uint32_t* thr_draft;
+  // List mode (threshold mode within a verify round, lists set): the rows are
+  // those of one wave, its row list and its bonus list, not the whole window.
+  const Entry* lists;   // the wave's row list
+  const int* list_cnt;  // its length
+  const Entry* blists;  // the wave's bonus list
+  const int* blist_cnt;
 };
 
 // The output pass is the last touch of a row: its loads and the stores of the
@@ -344,23 +350,37 @@ __global__ void __launch_bounds__(kTruncThreads, 2) sv_truncate(TruncParams P) {
   const size_t row_bytes = (size_t)V * E::kBytes;
   const int nvec = (int)(row_bytes / 16);
   const long long n_t = (long long)P.batch + P.total_draft;
-  const long long rows = n_t + (P.draft_in ? P.total_draft : 0);
+  const bool list_mode = P.lists != nullptr;
+  const int n_list = list_mode ? *P.list_cnt : 0;
+  const long long rows =
+      list_mode ? (long long)n_list + *P.blist_cnt : n_t + (P.draft_in ? P.total_draft : 0);
   // request of the current row: a cursor over the target layout (k_r + 1 rows
   // per request), then over the draft layout (k_r rows); rows only increase
   int r_cur = -1;
   long long r_end = 0;  // rows before r_end belong to requests <= r_cur
   bool draft_phase = false;
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
-    const bool is_draft = row >= n_t;
-    const long long local = is_draft ? row - n_t : row;
-    if (is_draft != draft_phase) {
-      draft_phase = is_draft;
-      r_cur = -1;
-      r_end = 0;
-    }
-    while (local >= r_end && r_cur < P.batch - 1) {
-      ++r_cur;
-      r_end += max(P.num_draft[r_cur], 0) + (is_draft ? 0 : 1);
+    bool is_draft;
+    long long local;  // row index in the target or the draft layout
+    if (list_mode) {
+      // a wave entry: request r, position pos, the request's first draft row d0
+      const Entry en = row < n_list ? P.lists[row] : P.blists[row - n_list];
+      r_cur = en.meta & 0x1fff;
+      is_draft = ((en.meta >> 13) & 1) != 0;
+      const int pos = (en.meta >> 20) & 31;
+      local = is_draft ? (long long)en.d0 + pos : (long long)en.d0 + r_cur + pos;
+    } else {
+      is_draft = row >= n_t;
+      local = is_draft ? row - n_t : row;
+      if (is_draft != draft_phase) {
+        draft_phase = is_draft;
+        r_cur = -1;
+        r_end = 0;
+      }
+      while (local >= r_end && r_cur < P.batch - 1) {
+        ++r_cur;
+        r_end += max(P.num_draft[r_cur], 0) + (is_draft ? 0 : 1);
+      }
     }
     const char* in = reinterpret_cast<const char*>(is_draft ? P.draft_in : P.target_in) +
                      (size_t)local * row_bytes;
