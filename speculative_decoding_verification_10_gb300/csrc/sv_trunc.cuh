@@ -26,6 +26,11 @@
 // fixed order, so the threshold does not depend on the order of the atomics.
 // Rows of greedy requests (T = 0), rows holding NaN, and rows whose top_p is
 // NaN or <= 0 (which also sets SPECVERIFY_STATUS_BAD_TRUNC) are copied.
+//
+// One kernel, three uses: copy mode writes the truncated rows; threshold mode
+// writes one threshold key per row instead (0 for a row kept whole); list mode
+// is threshold mode over the rows of one verify wave (its row and bonus
+// lists), launched before that wave of a truncated round.
 #pragma once
 
 #include "sv_kernels.cuh"
