@@ -58,9 +58,10 @@ def batch(B, vocab, dtype, seed, max_k=5):
 
 
 @pytest.mark.parametrize("dtype,vocab", [("bf16", 4096), ("f32", 3000), ("bf16", 1001),
-                                         ("f32", 777), ("bf16", 32000), ("bf16", 151936)])
+                                         ("f32", 777), ("bf16", 32000), ("bf16", 151936),
+                                         ("bf16", 262144)])
 def test_truncation_matches_oracle(dtype, vocab):
-    B = 40 if vocab < 100000 else 8
+    B = 40 if vocab < 100000 else (8 if vocab < 200000 else 6)
     inp, top_k, top_p = batch(B, vocab, dtype, vocab + 1)
     gt, gd, st = gpu_truncate(inp, top_k, top_p)
     ot, od, mt, md, ost = oracle.truncate(inp["target"], inp["draft"], inp["num_draft"],

@@ -152,3 +152,22 @@ def test_truncated_round_all_greedy_and_no_truncation():
         g = parity.run_gpu(v, greedy, 4, debug=False)
         for key in ("accepted_len", "committed", "flags", "status"):
             assert np.array_equal(np.asarray(f[key]), np.asarray(g[key])), key
+
+
+def test_truncated_round_without_draft_logits():
+    """An all-greedy batch may pass no draft logits: the threshold passes then
+    see target rows only, and the round is specverify_run's."""
+    B, V = 20, 4096
+    inp, _, _ = batch(B, V, "bf16", 41)
+    inp = dict(inp, temperature=np.zeros(B, np.float32))
+    t = parity.to_torch(inp, "cuda")
+    tk, tp = _dev(np.full(B, 7, np.int32), np.int32), _dev(np.full(B, 0.5, np.float32), np.float32)
+    with Verifier(B, inp["max_k"], V, "bf16") as v:
+        f = v.run_truncated(t["target"], None, t["tokens"], t["num_draft"], t["temperature"],
+                            tk, tp, 3)
+        g = v.run(t["target"], None, t["tokens"], t["num_draft"], t["temperature"], 3)
+        torch.cuda.synchronize()
+        assert v.status() == 0
+        for a, b in ((f.accepted_len, g.accepted_len), (f.committed, g.committed),
+                     (f.flags, g.flags)):
+            assert torch.equal(a, b)
