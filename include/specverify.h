@@ -257,7 +257,7 @@ int specverify_run_host(specverify_t h, const void *target_logits, const void *d
  * embedding runtimes whose rules forbid allocation once they are serving,
  * because an allocation can block on device-wide synchronisation.
  *
- * Scratch is one file-scope static device array of about 0.70 MiB, sized for
+ * Scratch is one file-scope static device array of about 0.71 MiB, sized for
  * batch <= SPECVERIFY_STATIC_MAX_BATCH (256) and max_k <=
  * SPECVERIFY_STATIC_MAX_K (7) on a grid of at most 1024 CTAs.  On its first use
  * on a device the call takes the array's address (cudaGetSymbolAddress,
